@@ -1,0 +1,131 @@
+"""NVFP4 block quantization (E2M1 values, one E4M3 scale per 1x16 block, one
+FP32 outer scale per tensor).  Test infrastructure only.
+
+End-to-End 4-Bit Training, "Low-precision formats on Blackwell": each block of
+16 consecutive values is scaled by its largest magnitude -- a block whose
+largest value is -54 stores -6 with scale 9 -- and a second FP32 scale over a
+very large group (a whole tensor) shifts the representable range, so that a
+value decodes as x_i^FP4 * x_{i//16}^FP8 * x^FP32.  "Recipe details": weights
+use one outer scale per expert, i.e. each expert's matrix is "the tensor".
+
+Conventions (the pages do not state them):
+  sg       = fp32(amax / 2688) with 2688 = 6 * 448, or 1 when amax == 0
+  den6     = fp32(6 * sg)
+  s        = RN_E4M3(fp32(bamax / den6))          (saturates at 448)
+  s == 0  -> every code is a signed zero, scale byte 0x00
+  inv      = fp32(1 / fp32(s * sg))
+  q_i      = RN_E2M1(fp32(x_i * inv))
+  packing  : element 2j in the low nibble of byte j, 2j+1 in the high nibble
+The element step multiplies by a per-block reciprocal rather than dividing.
+Results are defined while s * sg is a normal fp32 number (any tensor whose
+largest magnitude is at least 2^-100).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import formats as F
+
+F32 = np.float32
+NVFP4_BLOCK = 16
+OUTER_DEN = F32(6.0 * 448.0)  # 2688
+
+
+def outer_scale(x) -> np.float32:
+    """Per-tensor FP32 outer scale sg = amax / (6 * 448), or 1 for an
+    all-zero tensor."""
+    x = np.asarray(x, dtype=F32)
+    amax = F32(np.max(np.abs(x))) if x.size else F32(0.0)
+    if amax == 0:
+        return F32(1.0)
+    return F32(amax / OUTER_DEN)
+
+
+def _quantize_blocks(xb: np.ndarray, sg: np.float32):
+    """Quantize rows of a [nblocks, blocksize] float32 array, one scale each.
+    Returns (nibble codes [nblocks, blocksize], E4M3 scale codes [nblocks])."""
+    sg = F32(sg)
+    den6 = F32(F32(6.0) * sg)
+    bamax = np.max(np.abs(xb), axis=1).astype(F32)
+    s_code = F.rn_code((bamax / den6).astype(F32), F.E4M3_TABLE)
+    s = F.decode_e4m3_array(s_code).astype(F32)
+    nonzero = s != 0
+    prod = (s * sg).astype(F32)
+    with np.errstate(divide="ignore"):
+        inv = np.where(nonzero, (F32(1.0) / np.where(nonzero, prod, F32(1.0))).astype(F32), F32(0.0))
+    scaled = (xb * inv[:, None]).astype(F32)
+    codes = F.rn_code(scaled, F.E2M1_TABLE)
+    # an all-zero (or underflowed) block: signed zeros whatever the values
+    zero_codes = np.where(np.signbit(xb), F.E2M1_SIGN, np.uint8(0)).astype(np.uint8)
+    codes = np.where(nonzero[:, None], codes, zero_codes)
+    return codes.astype(np.uint8), s_code.astype(np.uint8)
+
+
+def quantize(x, sg=None):
+    """NVFP4 1x16 round-to-nearest quantization of a float32 matrix [R, C]
+    (C a multiple of 16) with blocks along the row.
+
+    Returns (codes uint8 [R, C] of 4-bit E2M1 codes, scales uint8 [R, C/16]
+    of E4M3 codes, sg float32).  ``sg`` defaults to ``outer_scale(x)``."""
+    x = np.asarray(x, dtype=F32)
+    R, C = x.shape
+    if C % NVFP4_BLOCK:
+        raise ValueError("C must be a multiple of 16")
+    sg = outer_scale(x) if sg is None else F32(sg)
+    codes, scales = _quantize_blocks(x.reshape(R * C // 16, 16), sg)
+    return codes.reshape(R, C), scales.reshape(R, C // 16), sg
+
+
+def quantize_col16(x, sg=None):
+    """16x1 blocks (along columns): the backward-pass grouping that the page's
+    Figure 2 compares with 1x16 ("Block-scaled backward passes")."""
+    codes, scales, sg = quantize(np.asarray(x, dtype=F32).T, sg)
+    return codes.T, scales.T, sg
+
+
+def quantize_tile16x16(x, sg=None):
+    """One E4M3 scale per 16x16 tile (NVIDIA's transpose-invariant weight
+    scheme, Figure 3 of "Block-scaled backward passes").  Returns codes [R, C]
+    and scales [R/16, C/16]."""
+    x = np.asarray(x, dtype=F32)
+    R, C = x.shape
+    sg = outer_scale(x) if sg is None else F32(sg)
+    tiles = x.reshape(R // 16, 16, C // 16, 16).transpose(0, 2, 1, 3).reshape(-1, 256)
+    codes, scales = _quantize_blocks(tiles, sg)
+    codes = codes.reshape(R // 16, C // 16, 16, 16).transpose(0, 2, 1, 3).reshape(R, C)
+    return codes, scales.reshape(R // 16, C // 16), sg
+
+
+def pack(codes) -> np.ndarray:
+    """Pack 4-bit codes [R, C] into bytes [R, C/2]: low nibble = even element."""
+    c = np.asarray(codes, dtype=np.uint8)
+    return (c[:, 0::2] & 0xF) | ((c[:, 1::2] & 0xF) << 4)
+
+
+def unpack(packed) -> np.ndarray:
+    """Inverse of ``pack``."""
+    p = np.asarray(packed, dtype=np.uint8)
+    out = np.empty((p.shape[0], p.shape[1] * 2), dtype=np.uint8)
+    out[:, 0::2] = p & 0xF
+    out[:, 1::2] = p >> 4
+    return out
+
+
+def dequantize_f32(codes, scales, sg) -> np.ndarray:
+    """Dequantized values in fp32: fp32(fp32(e2m1 * e4m3) * sg).  The inner
+    product is exact (at most 6 significant bits).  Used by the re-quantizer."""
+    v = F.decode_e2m1_array(codes)
+    s = F.decode_e4m3_array(np.repeat(np.asarray(scales, dtype=np.uint8), NVFP4_BLOCK, axis=-1))
+    return ((v * s).astype(F32) * F32(sg)).astype(F32)
+
+
+def dequantize_f64(codes, scales, sg) -> np.ndarray:
+    """Exact dequantized values e2m1 * e4m3 * sg in float64 (GEMM references)."""
+    v = F.decode_e2m1_array(codes)
+    s = F.decode_e4m3_array(np.repeat(np.asarray(scales, dtype=np.uint8), NVFP4_BLOCK, axis=-1))
+    return v * s * np.float64(F32(sg))
+
+
+def dequantize_tile16x16_f64(codes, tile_scales, sg) -> np.ndarray:
+    s = F.decode_e4m3_array(np.repeat(np.repeat(tile_scales, 16, axis=0), 16, axis=1))
+    return F.decode_e2m1_array(codes) * s * np.float64(F32(sg))
