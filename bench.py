@@ -1,0 +1,465 @@
+"""Benchmark of the NVFP4-forward / MXFP8-backward expert hot path on GB300.
+
+One step = one pass of the whole path over one batch: the routed experts of a
+MoE layer with 16384 tokens, d_model 4096, 64 experts, top-8 routing and
+SwiGLU experts (gate/up 4096 -> 1536 x 2, down 1536 -> 4096), forward and
+backward:
+  forward   NVFP4 quantization of x, w13, w2 (amax -> FP32 outer scale ->
+            1x16 E4M3 block scales -> E2M1), grouped NVFP4 GEMM w13, SwiGLU,
+            NVFP4 quantization of h, grouped NVFP4 GEMM w2
+  backward  dequant -> transpose -> SR requant to MXFP8 of w13, w2, x_q, h_q;
+            SR MXFP8 quantization (row-wise + transposed per expert) of the
+            down-output gradient g2 and of dy13; grouped MXFP8 dgrad and wgrad
+            GEMMs for the down and gate/up projections; SwiGLU backward.
+Inputs are seeded synthetic tensors of that shape (the pages measure on no
+public dataset): x ~ N(0,1), weights ~ N(0,0.02), router logits and bias
+~ N(0,1), g2 ~ N(0,1e-3).
+
+value  = GEMM FLOPs of the step (forward + backward, unpadded groups) / step
+         time, with inputs resident in HBM, in TFLOP/s.
+e2e    = the same, with the step's activations and upstream gradient copied
+         from pinned host memory and dx read back inside the timed region.
+roofline: the kernel with the largest share of the step, achieved against
+         MEASURED_PEAKS.json (HBM GB/s, bf16 TFLOP/s x the nominal fp8/fp4
+         ratio) or the documented fallback.
+
+--impl reference times the CPU oracle (oracle/, numpy) on a bounded sample of
+the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "NVFP4/MXFP8 expert GEMM TFLOPS + quant/requant GB/s, % of GB300 roofline"
+WORKLOAD = "moe_expert_layer_fwd_bwd: 16384 tokens x top-8 (131072 rows), d_model 4096, d_ff 1536, 64 experts"
+SHAPE = dict(tokens=16384, topk=8, d_model=4096, d_ff=1536, experts=64)
+
+# fallbacks when MEASURED_PEAKS.json is absent (one earlier GB300 measurement)
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+NOMINAL_RATIO = {"bf16": 1.0, "fp8": 4.5 / 2.25, "fp4": 13.5 / 2.25}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            return {
+                "hbm_gbs": float(d.get("hbm_gbs", FALLBACK["hbm_gbs"])),
+                "bf16_tflops": float(d.get("bf16_tflops", FALLBACK["bf16_tflops"])),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d.get("bf16_tflops", 1700.0))),
+                "source": "measured",
+            }
+        except Exception:
+            pass
+    return dict(FALLBACK, source="fallback")
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas: one process per GPU, no data-path collective)
+# ---------------------------------------------------------------------------
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def init_dist(backend):
+    import torch.distributed as dist
+    rank, world, _ = dist_env()
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return rank, world
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """Largest value of x over all ranks (the slowest replica sets the time)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(units_per_rank: float, seconds_max: float, world: int) -> float:
+    """Whole-job throughput: units all ranks processed / the slowest rank's time."""
+    return units_per_rank * world / seconds_max
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index=0, out_path=None):
+        self.gpu, self.out_path, self.proc, self.lines = gpu_index, out_path, None, []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        if self.out_path:
+            with open(self.out_path, "w") as f:
+                f.write(self.FIELDS + "\n" + "\n".join(self.lines) + "\n")
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+class EventLog:
+    """CUDA events around each library call on the launching stream."""
+
+    def __init__(self):
+        self.rec = []
+
+    def call(self, name, fn, *a, **k):
+        import torch
+        s = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        fn(*a, **k)
+        e1.record(s)
+        self.rec.append((name, e0, e1))
+
+    def per_name_ms(self):
+        out = {}
+        for name, e0, e1 in self.rec:
+            out.setdefault(name, []).append(e0.elapsed_time(e1))
+        return out
+
+
+def build_step(layer, m, log: EventLog | None):
+    """Returns step() running the whole path; with `log`, each call is bracketed by events."""
+    from precision_moe_numerics_nvfp4_gb300 import nvfp4moe as N
+    from precision_moe_numerics_nvfp4_gb300 import pipeline as PL
+
+    def wrap(name, fn):
+        if log is None:
+            return fn
+        return lambda *a, **k: log.call(name, fn, *a, **k)
+
+    class Proxy:  # the layer's calls go through the event log
+        def __getattr__(self, n):
+            f = getattr(N, n)
+            return wrap(n, f) if callable(f) and not n.startswith("_") else f
+
+    def step(x, g2):
+        saved = PL.N
+        PL.N = Proxy()
+        try:
+            layer.step(x, m.w13, m.w2, g2, m.group_offsets, seed=3)
+        finally:
+            PL.N = saved
+
+    return step
+
+
+def kernel_units(layer, m):
+    """Algorithmic bytes (quantizers) and FLOPs (GEMMs) per call, by call name
+    and argument pattern, in the order MoELayer.step issues them."""
+    M, d, I, E = layer.M, layer.d, layer.I, layer.E
+    fl13 = 2.0 * M * 2 * I * d
+    fl2 = 2.0 * M * d * I
+    return {
+        "nvfp4_quantize": [(E * 2 * I * d, 2.5625), (E * d * I, 2.5625), (M * d, 2.5625), (M * I, 2.5625)],
+        "grouped_gemm_nvfp4_fwd": [fl13, fl2],
+        "dequant_transpose_requant_sr": [(E * 2 * I * d, 1.59375), (E * d * I, 1.59375), (M * d, 1.59375),
+                                         (M * I, 1.59375)],
+        "mxfp8_quantize": [(M * d, 4.0625), (M * 2 * I, 4.0625)],
+        "grouped_gemm_mxfp8_dx": [fl2, fl13],
+        "grouped_gemm_mxfp8_dw": [fl2, fl13],
+        "nvfp4moe_swiglu_fwd": [(M * I, 3 * 2.0)],
+        "nvfp4moe_swiglu_bwd": [(M * I, 5 * 2.0)],
+    }
+
+
+def run_ours(args):
+    import torch
+    from precision_moe_numerics_nvfp4_gb300 import nvfp4moe as N
+    from precision_moe_numerics_nvfp4_gb300 import workloads as W
+    from precision_moe_numerics_nvfp4_gb300.pipeline import MoELayer
+
+    rank, world = init_dist("nccl")
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    N.lib()
+    peaks = load_peaks()
+    m = W.moe("cuda", seed=2, with_grad=True, grad_seed=3)
+    M = m.x_perm.shape[0]
+    layer = MoELayer(M, SHAPE["d_model"], SHAPE["d_ff"], SHAPE["experts"])
+    fwd_fl, bwd_fl = layer.flops()
+    step_flops = fwd_fl + bwd_fl
+
+    # warm-up
+    plain = build_step(layer, m, None)
+    for _ in range(args.warmup):
+        plain(m.x_perm, m.g2)
+    torch.cuda.synchronize()
+    st = N.nvfp4moe_get_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} after warm-up")
+
+    # timed region: device-resident inputs
+    log = EventLog()
+    step = build_step(layer, m, log)
+    sampler = ClockSampler(local, os.path.join(ROOT, "gpurun_out", "clocks.csv") if os.path.isdir(
+        os.path.join(ROOT, "gpurun_out")) else None)
+    sampler.start()
+    barrier()
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(s)
+    for _ in range(args.steps):
+        step(m.x_perm, m.g2)
+    t1.record(s)
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    ms = t0.elapsed_time(t1) / args.steps
+    ms_max = max_over_ranks(ms, torch.device("cuda"))
+    value = aggregate(step_flops / 1e12, ms_max / 1e3, world)
+    st = N.nvfp4moe_get_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} after the timed region")
+
+    # per-kernel breakdown (same timed region)
+    per = log.per_name_ms()
+    units = kernel_units(layer, m)
+    kernels = {}
+    for name, times in per.items():
+        n_per_step = len(units.get(name, [])) or 1
+        tot = sum(times) / args.steps
+        u = units.get(name, [])
+        entry = {"ms_per_step": tot, "share": tot / ms, "calls_per_step": n_per_step}
+        if u and isinstance(u[0], tuple):
+            by = [sum(times[i::n_per_step]) / args.steps for i in range(n_per_step)]
+            gbs = [uu[0] * uu[1] / (b / 1e3) / 1e9 for uu, b in zip(u, by)]
+            entry.update({"GB_s": gbs, "frac_hbm": [g / peaks["hbm_gbs"] for g in gbs]})
+        elif u:
+            by = [sum(times[i::n_per_step]) / args.steps for i in range(n_per_step)]
+            entry.update({"TFLOP_s": [f / (b / 1e3) / 1e12 for f, b in zip(u, by)]})
+        kernels[name] = entry
+    dom = max(kernels, key=lambda k: kernels[k]["ms_per_step"])
+    roof = roofline_of(dom, per[dom], units[dom], args.steps, peaks)
+
+    # e2e through host buffers: x and g2 in, dx out
+    x_h = m.x_perm.cpu().pin_memory()
+    g_h = m.g2.cpu().pin_memory()
+    dx_h = torch.empty(layer.dx.shape, dtype=layer.dx.dtype).pin_memory()
+    x_d, g_d = torch.empty_like(m.x_perm), torch.empty_like(m.g2)
+    e2e_steps = max(2, min(args.steps, 5))
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(e2e_steps):
+        x_d.copy_(x_h, non_blocking=True)
+        g_d.copy_(g_h, non_blocking=True)
+        plain(x_d, g_d)
+        dx_h.copy_(layer.dx, non_blocking=True)
+    e1.record(s)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, torch.device("cuda"))
+    h2d = x_h.numel() * x_h.element_size() + g_h.numel() * g_h.element_size()
+    d2h = dx_h.numel() * dx_h.element_size()
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.cpu_tokens)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "nvfp4 fwd / mxfp8 bwd (fp32 accumulate)", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "global_batch": SHAPE["tokens"] * world, "rows": M,
+                   "group_sizes": "top-8 of logits~N(0,1)+bias~N(0,1), uneven", "seed": 2,
+                   "parallelism": f"replicas x{world}", "l2": "inputs > L2 (GB-sized tensors), no flush"},
+        "gemm_flops_per_step": step_flops,
+        "roofline": roof, "kernels": kernels, "clocks": clocks,
+        "e2e": {"value": aggregate(step_flops / 1e12, e2e_ms / 1e3, world), "unit": "TFLOP/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": MoELayer.LAUNCHES_PER_STEP * args.steps,
+        "peaks": peaks,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line))
+
+
+def roofline_of(name, times, units, steps, peaks):
+    n = len(units)
+    per_launch = [sum(times[i::n]) / steps for i in range(n)]
+    if isinstance(units[0], tuple):
+        byts = sum(u[0] * u[1] for u in units)
+        dur = sum(per_launch)
+        ach = byts / (dur / 1e3) / 1e9
+        return {"kernel": name, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / peaks["hbm_gbs"], "traffic": None,
+                "peak_source": peaks["source"] + " (HBM copy)", "algorithmic_bytes_per_step": byts}
+    fl = sum(units)
+    dur = sum(per_launch)
+    ach = fl / (dur / 1e3) / 1e12
+    ratio = NOMINAL_RATIO["fp4"] if "nvfp4" in name else NOMINAL_RATIO["fp8"]
+    peak = peaks["bf16_tflops_sustained"] * ratio
+    return {"kernel": name, "bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+            "frac": ach / peak, "traffic": None,
+            "peak_source": f"{peaks['source']} sustained bf16 x {ratio:g} (nominal {'fp4' if ratio > 3 else 'fp8'}/bf16)",
+            "algorithmic_flops_per_step": fl}
+
+
+# ---------------------------------------------------------------------------
+# the oracle: cpu_baseline and the reference arm
+# ---------------------------------------------------------------------------
+def oracle_sample_step(tokens: int, seed: int = 2):
+    """One expert (of the workload's 64) with `tokens` routed rows, full
+    d_model / d_ff, through every step of the path in the oracle.  Returns
+    the sample's GEMM FLOPs."""
+    import torch
+    from oracle import gemm as G
+    from oracle import layout as L
+    from oracle import mxfp8 as MX
+    from oracle import nvfp4 as NV
+    from oracle import requant as RQ
+    from oracle import swiglu as SW
+    d, I = SHAPE["d_model"], SHAPE["d_ff"]
+    gen = torch.Generator().manual_seed(seed)
+    x = (torch.randn((tokens, d), generator=gen)).to(torch.bfloat16).float().numpy()
+    w13 = (torch.randn((2 * I, d), generator=gen) * 0.02).to(torch.bfloat16).float().numpy()
+    w2 = (torch.randn((d, I), generator=gen) * 0.02).to(torch.bfloat16).float().numpy()
+    g2 = (torch.randn((tokens, d), generator=gen) * 1e-3).to(torch.bfloat16).float().numpy()
+    o = np.array([0, tokens])
+    P = L.padded_cap(tokens, 1)
+    xc, xs, xsg = NV.quantize(x)
+    w13c, w13s, w13sg = NV.quantize(w13)
+    w2c, w2s, w2sg = NV.quantize(w2)
+    y13, _ = G.grouped_rows(NV.dequantize_f64(xc, xs, xsg), NV.dequantize_f64(w13c, w13s, w13sg)[None], o)
+    h = SW.forward(y13.astype(np.float32))
+    hc, hs, hsg = NV.quantize(h.astype(np.float32))
+    G.grouped_rows(NV.dequantize_f64(hc, hs, hsg), NV.dequantize_f64(w2c, w2s, w2sg)[None], o)
+    w13t = RQ.requant_weights(w13c[None], w13s[None], np.array([w13sg]), 3, 0)
+    w2t = RQ.requant_weights(w2c[None], w2s[None], np.array([w2sg]), 3, 1)
+    xt = RQ.requant_grouped(xc, xs, xsg, o, 3, 2, P)
+    ht = RQ.requant_grouped(hc, hs, hsg, o, 3, 3, P)
+    gr = RQ.quantize_grad_rowwise(g2, 3, 4)
+    gt = RQ.transposed_grouped_sr(g2, o, 3, 5, P)
+    dh, _ = G.grouped_rows(MX.dequantize_f64(*gr), MX.dequantize_f64(w2t[0][0], w2t[1][0])[None], o)
+    G.grouped_contraction(MX.dequantize_f64(*gt), MX.dequantize_f64(*ht), np.array([0, P]))
+    dy13 = SW.backward(dh, y13).astype(np.float32)
+    dr = RQ.quantize_grad_rowwise(dy13, 3, 6)
+    dt = RQ.transposed_grouped_sr(dy13, o, 3, 7, P)
+    G.grouped_rows(MX.dequantize_f64(*dr), MX.dequantize_f64(w13t[0][0], w13t[1][0])[None], o)
+    G.grouped_contraction(MX.dequantize_f64(*dt), MX.dequantize_f64(*xt), np.array([0, P]))
+    return 3 * (2.0 * tokens * 2 * I * d + 2.0 * tokens * d * I)
+
+
+def cpu_baseline(tokens: int):
+    t0 = time.perf_counter()
+    flops = oracle_sample_step(tokens)
+    dt = time.perf_counter() - t0
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"one expert of the workload with {tokens} routed rows, full d_model/d_ff, every step "
+                      f"(quantize, GEMM references in float64, requant, SR) in numpy; {dt:.1f} s"}
+
+
+def run_reference(args):
+    rank, world = init_dist("gloo")
+    if rank != 0:
+        return
+    for _ in range(args.warmup):
+        oracle_sample_step(args.ref_tokens)
+    t0 = time.perf_counter()
+    flops = 0.0
+    for _ in range(args.steps):
+        flops += oracle_sample_step(args.ref_tokens)
+    dt = time.perf_counter() - t0
+    v = flops / dt / 1e12
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 oracle",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "sample_rows_per_step": args.ref_tokens},
+        "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": f"one expert, {args.ref_tokens} rows per step, full d_model/d_ff"},
+        "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-tokens", type=int, default=256)
+    ap.add_argument("--ref-tokens", type=int, default=64)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

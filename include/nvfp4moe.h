@@ -1,0 +1,270 @@
+/*
+ * nvfp4moe.h -- C ABI of libnvfp4moe.so: the data-parallel hot path of
+ * NVFP4-forward / MXFP8-backward MoE expert training on one GB300 (sm_103a).
+ *
+ * The method is the one described in "End-to-End 4-Bit Training" (Thinking
+ * Machines Lab): NVFP4 block quantization of activations and weights, grouped
+ * NVFP4 expert GEMMs in the forward pass, dequantize -> transpose -> stochastic
+ * re-quantization of the saved forward tensors to MXFP8, SR quantization of
+ * the BF16 output gradient, and grouped MXFP8 dgrad / wgrad GEMMs.
+ *
+ * General rules (every entry point):
+ *  - Pointers are DEVICE pointers unless a parameter says otherwise.  The
+ *    caller owns and allocates every buffer, including workspaces; the library
+ *    never allocates, frees or retains device memory.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy default
+ *    stream) and is asynchronous.  The return value reports argument checks
+ *    and launch errors only (NV_OK or a negative NV_ERR_*).  Errors the GPU
+ *    detects (inconsistent group offsets, a bounded wait that ran out) are
+ *    recorded in a per-device status word read by nvfp4moe_get_device_status.
+ *    No kernel traps or prints.
+ *  - Every pointer must be 16-byte aligned.  Results are bitwise
+ *    deterministic: the same inputs give the same bytes on every run.
+ *  - Matrices are row-major.  bf16 is IEEE bfloat16 bits (uint16).
+ *
+ * Number formats ("Low-precision formats on Blackwell" on the pages):
+ *  - E2M1 (FP4): +-{0, 0.5, 1, 1.5, 2, 3, 4, 6}; two per byte, element 2j in
+ *    the low nibble of byte j.
+ *  - E4M3: 1 sign, 4 exponent (bias 7), 3 mantissa bits; largest 448; used for
+ *    NVFP4 block scales and for MXFP8 elements.
+ *  - E8M0: 2^(code - 127); MXFP8 block scales.
+ *  - NVFP4: E2M1 codes, one E4M3 scale per 16 consecutive values of a row and
+ *    one FP32 outer scale per tensor: x = e2m1 * e4m3 * sg.
+ *  - MXFP8: E4M3 codes, one E8M0 scale per 32 consecutive values of a row.
+ *
+ * Conventions the pages leave open (identical in the CPU oracle):
+ *  - sg = amax / (6 * 448) per tensor (per expert matrix for weights), 1 for
+ *    an all-zero tensor; NVFP4 scale s = RN_E4M3(blockamax / (6 * sg))
+ *    saturating at 448; codes = RN_E2M1(x * (1 / (s * sg))); an all-zero (or
+ *    underflowed) block gets scale 0 and signed-zero codes.  All steps are
+ *    IEEE fp32, round to nearest even.
+ *  - MXFP8 scale = floor(log2 blockamax) - 8 clamped to [-127, 127] (OCP MX),
+ *    code = scale + 127; scale code 0 and signed zeros for an all-zero block;
+ *    elements RN or SR to E4M3 saturating at 448.
+ *  - Stochastic rounding ("Re-quantization with stochastic rounding"): with
+ *    a <= |w| < b the neighbouring E4M3 values, round up iff
+ *    R < floor(2^16 (|w| - a) / (b - a)), R = 16 random bits.
+ *  - Random bits: Philox4x32-10 (Salmon et al., SC'11), key = (seed lo, seed
+ *    hi), counter = (q lo, q hi, offset lo, offset hi) with q = e >> 3; element
+ *    e uses the 16-bit half (e & 1) of output word (e & 7) >> 1, where e is
+ *    the element's row-major index in the SOURCE tensor of the call.
+ *
+ * Scale-factor layout (all block scales, NVFP4 and MXFP8): the 128x4 tile
+ * that block-scaled tcgen05 MMA reads.  The scale of padded row r', block
+ * column c, in a matrix with KB block columns is at byte
+ *     ((r' / 128) * ceil(KB / 4) + c / 4) * 512 + (r' % 32) * 16
+ *       + ((r' / 32) % 4) * 4 + c % 4,
+ * every padding byte zero.  Padded rows: a stack of `batch` matrices with R
+ * rows uses r' = b * roundup(R, 128) + r; a matrix whose rows are grouped by
+ * expert (group_offsets o, sizes M_e = o[e+1] - o[e]) uses
+ * r' = P_e + (r - o[e]) with P_e = sum_{e' < e} roundup(M_e', 128), so that
+ * every 128-row tile of an expert owns its scale atoms.  Grouped buffers are
+ * sized for P_cap = nvfp4moe_padded_cap(M_total, E) rows.
+ *
+ * group_offsets: int32 [E + 1] on the device, o[0] = 0, non-decreasing,
+ * o[E] = M_total.  Empty groups are allowed.  Kernels that read them record
+ * NV_ERR_OFFSETS in the status word (and write nothing) when they are
+ * inconsistent.
+ */
+#ifndef NVFP4MOE_H
+#define NVFP4MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *nv_stream_t; /* a cudaStream_t */
+
+enum nv_status {
+  NV_OK = 0,
+  NV_ERR_ARG = -1,          /* null pointer, negative size, bad enum */
+  NV_ERR_ALIGN = -2,        /* a pointer is not 16-byte aligned */
+  NV_ERR_SHAPE = -3,        /* a size violates the divisibility rules */
+  NV_ERR_OFFSETS = -4,      /* (device) group offsets inconsistent */
+  NV_ERR_TIMEOUT = -5,      /* (device) a bounded wait ran out */
+  NV_ERR_CUDA = -6,         /* a CUDA runtime call failed */
+  NV_ERR_UNSUPPORTED = -7,  /* a feature or GPU this build does not support */
+  NV_ERR_WORKSPACE = -8     /* workspace missing or too small */
+};
+enum nv_round { NV_RN = 0, NV_SR = 1 };
+enum nv_out_dtype { NV_OUT_BF16 = 0, NV_OUT_FP32 = 1 };
+
+/* ---- sizes and layout helpers (host only, no GPU work) --------------------- */
+
+/* Padded rows reserved for a grouped layout: roundup(M_total + 127 E, 128). */
+int64_t nvfp4moe_padded_cap(int64_t M_total, int64_t E);
+
+/* Bytes of a scale buffer for `padded_rows` rows and `kblocks` block columns:
+ * roundup(padded_rows, 128) / 128 * ceil(kblocks / 4) * 512. */
+int64_t nvfp4moe_scale_bytes(int64_t padded_rows, int64_t kblocks);
+
+/* Byte offset of the scale of padded row rp, block column c (see above). */
+int64_t nvfp4moe_scale_offset(int64_t rp, int64_t c, int64_t kblocks);
+
+/* Workspace bytes nvfp4_quantize needs when it computes the outer scales. */
+size_t nvfp4moe_quantize_workspace_bytes(int64_t batch, int64_t rows, int64_t cols);
+
+/* ---- a1 + a2: NVFP4 quantization ----------------------------------------------
+ * "Low-precision formats on Blackwell": block scaling by the largest value of
+ * each 16 consecutive values, E4M3 block scale, FP32 outer scale per tensor;
+ * "Recipe details": one outer scale per expert for weights.
+ *
+ * x:        bf16 [batch][rows][cols], cols % 16 == 0.
+ * group_offsets / num_groups: NULL / 0 for plain or batched matrices; else
+ *           (batch == 1 only) the expert groups of the rows, which selects the
+ *           grouped scale layout.
+ * outer_scale_in: NULL -> compute sg = amax / 2688 of every batch entry
+ *           (step a1, one extra read of x) and write it to outer_scale_out
+ *           [batch]; non-NULL -> fp32 [batch] scales to use (copied to
+ *           outer_scale_out when that is non-NULL).
+ * codes:    u8 [batch][rows][cols / 2].
+ * scales:   u8, batched layout (batch * roundup(rows,128) padded rows) or
+ *           grouped layout (P_cap padded rows), cols / 16 block columns.
+ *           Every byte of the buffer is written (padding zero).
+ * workspace: nvfp4moe_quantize_workspace_bytes(...) bytes when
+ *           outer_scale_in is NULL, else may be NULL.
+ */
+int nvfp4_quantize(const void *x, int64_t batch, int64_t rows, int64_t cols,
+                   const int32_t *group_offsets, int32_t num_groups,
+                   const float *outer_scale_in, float *outer_scale_out,
+                   uint8_t *codes, uint8_t *scales,
+                   void *workspace, size_t workspace_bytes, nv_stream_t stream);
+
+/* ---- a6 (and the MXFP8 RN sweep): MXFP8 quantization of a bf16 matrix --------
+ * Chinese translation of the pages, Figure 4: the BF16 gradient is quantized
+ * to MXFP8 with SR once row-wise (DGRAD operand) and once after a transpose
+ * (WGRAD operand).
+ *
+ * x:        bf16 [rows][cols], cols % 32 == 0.
+ * group_offsets / num_groups: expert groups of the rows (NULL / 0: one group
+ *           of all rows).
+ * mode:     NV_RN or NV_SR; SR draws bits with (seed, counter_offset_row) for
+ *           the row-wise output and (seed, counter_offset_t) for the
+ *           transposed one, element index = row * cols + col.
+ * codes_row [rows][cols] E4M3, scales_row grouped layout (cols / 32 block
+ *           columns; P_cap padded rows, or roundup(rows,128) for one group):
+ *           the row-wise output, or both NULL to skip it.
+ * codes_t   [cols][P_cap] E4M3: the transpose of each group, zero-padded to
+ *           a multiple of 128 tokens and placed at column P_e; blocks of 32
+ *           along the new rows.  scales_t: batched layout of one matrix with
+ *           `cols` rows and P_cap / 32 block columns.  Columns >= P_total are
+ *           left untouched.  Both NULL to skip.  rows with num_groups == 0 are
+ *           one group (P_cap = roundup(rows, 128)).
+ */
+int mxfp8_quantize(const void *x, int64_t rows, int64_t cols,
+                   const int32_t *group_offsets, int32_t num_groups,
+                   int mode, uint64_t seed, uint64_t counter_offset_row,
+                   uint64_t counter_offset_t,
+                   uint8_t *codes_row, uint8_t *scales_row,
+                   uint8_t *codes_t, uint8_t *scales_t, nv_stream_t stream);
+
+/* ---- a5: dequantize -> transpose -> SR re-quantize NVFP4 -> MXFP8 -------------
+ * "Re-quantization with stochastic rounding": the forward NVFP4 tensor is
+ * dequantized (fp32: fp32(e2m1 * e4m3) * sg), transposed at that precision,
+ * and re-quantized to MXFP8 with stochastic rounding, so that the backward
+ * operand equals the forward one in expectation.
+ *
+ * codes / scales / outer_scale: an nvfp4_quantize output (same batch, rows,
+ *           cols, group_offsets); outer_scale fp32 [batch] on the device.
+ * Batched (group_offsets NULL): rows % 128 == 0; out_codes [batch][cols][rows]
+ *           E4M3, out_scales batched layout (batch matrices of `cols` rows,
+ *           rows / 32 block columns).
+ * Grouped (batch == 1): out_codes [cols][P_cap] and out_scales as codes_t /
+ *           scales_t of mxfp8_quantize.
+ * Element index for the random bits: the source row-major index
+ *           (b * rows + r) * cols + c.
+ */
+int dequant_transpose_requant_sr(const uint8_t *codes, const uint8_t *scales,
+                                 const float *outer_scale,
+                                 int64_t batch, int64_t rows, int64_t cols,
+                                 const int32_t *group_offsets, int32_t num_groups,
+                                 uint64_t seed, uint64_t counter_offset,
+                                 uint8_t *out_codes, uint8_t *out_scales,
+                                 nv_stream_t stream);
+
+/* ---- a3: grouped NVFP4 forward GEMM  y_e = x_q,e w_q,e^T ----------------------
+ * "Block-scaled backward passes": y = x_q w_q^T, 16-value blocks of a row of
+ * x_q and of w_q multiplied pairwise and scaled by both block scales; the
+ * outer scales multiply the result (y = acc * sg_x * sg_w[e]).
+ *
+ * x_codes [M_total][K/2], x_scales grouped layout (K/16 block columns),
+ * x_outer_scale fp32 [1]; w_codes [E][N][K/2], w_scales batched layout,
+ * w_outer_scale fp32 [E]; y [M_total][N] bf16 or fp32.
+ * N % 128 == 0, K % 256 == 0.  x_bf16 must be NULL (reserved for a fused
+ * producer-side activation quantization; non-NULL returns NV_ERR_UNSUPPORTED).
+ * workspace: may be NULL (no scratch needed).
+ */
+int grouped_gemm_nvfp4_fwd(const void *x_bf16, const float *x_outer_scale,
+                           const uint8_t *x_codes, const uint8_t *x_scales,
+                           const uint8_t *w_codes, const uint8_t *w_scales,
+                           const float *w_outer_scale,
+                           const int32_t *group_offsets, int32_t E,
+                           int64_t M_total, int64_t N, int64_t K,
+                           void *y, int y_dtype,
+                           void *workspace, size_t workspace_bytes, nv_stream_t stream);
+
+/* ---- a7: grouped MXFP8 dgrad  dx_e = g_e w_e -----------------------------------
+ * "Block-scaled backward passes": dx = g w_q, here with both operands MXFP8.
+ * g_codes [M_total][N] + g_scales (mxfp8_quantize row-wise output, grouped
+ * layout); wt_codes [E][K][N] + wt_scales (dequant_transpose_requant_sr of the
+ * weights [E][N][K]); dx [M_total][K] bf16 or fp32.  N % 128 == 0,
+ * K % 128 == 0.
+ */
+int grouped_gemm_mxfp8_dx(const uint8_t *g_codes, const uint8_t *g_scales,
+                          const uint8_t *wt_codes, const uint8_t *wt_scales,
+                          const int32_t *group_offsets, int32_t E,
+                          int64_t M_total, int64_t N, int64_t K,
+                          void *dx, int dx_dtype,
+                          void *workspace, size_t workspace_bytes, nv_stream_t stream);
+
+/* ---- a8: grouped MXFP8 wgrad  dw_e = g_e^T x_q,e ---------------------------------
+ * "Block-scaled backward passes": dw = g^T x_q, computed from the quantized
+ * forward activations ("Quantized communications": the WGRAD input is the
+ * quantized, not the high-precision, activation).  The contraction runs over
+ * the tokens of expert e, zero-padded to a multiple of 128.
+ * gt_codes [N][P_cap] + gt_scales (mxfp8_quantize transposed output of g),
+ * xt_codes [K][P_cap] + xt_scales (dequant_transpose_requant_sr of x_q);
+ * dw [E][N][K] fp32 (experts without tokens get zeros).  N % 128 == 0,
+ * K % 128 == 0.
+ */
+int grouped_gemm_mxfp8_dw(const uint8_t *gt_codes, const uint8_t *gt_scales,
+                          const uint8_t *xt_codes, const uint8_t *xt_scales,
+                          const int32_t *group_offsets, int32_t E,
+                          int64_t M_total, int64_t N, int64_t K,
+                          float *dw,
+                          void *workspace, size_t workspace_bytes, nv_stream_t stream);
+
+/* ---- a4: SwiGLU between the expert GEMMs (Figure 5: w13 GEMM, Q, w2 GEMM) -----
+ * y13 bf16 [M][2I] (gate columns 0..I-1, up columns I..2I-1);
+ * h = bf16(silu(gate) * up) computed in fp32, silu(x) = x / (1 + exp(-x)).
+ * Backward: dy13 = [dh * up * silu'(gate), dh * silu(gate)] as bf16.
+ * I % 8 == 0. */
+int nvfp4moe_swiglu_fwd(const void *y13, int64_t M, int64_t I, void *h, nv_stream_t stream);
+int nvfp4moe_swiglu_bwd(const void *dh, const void *y13, int64_t M, int64_t I,
+                        void *dy13, nv_stream_t stream);
+
+/* ---- status ------------------------------------------------------------------ */
+
+/* Synchronizes `stream`, returns the first error code any kernel recorded on
+ * the current device since the last call (NV_OK if none) and clears it. */
+int nvfp4moe_get_device_status(nv_stream_t stream);
+
+/* Self-test of the bounded-wait path: launches one CTA that waits on an
+ * mbarrier nothing arrives at, with an iteration limit of `spins`; the wait
+ * runs out, the kernel records NV_ERR_TIMEOUT and returns.  No fault, no
+ * hang.  Returns the launch status. */
+int nvfp4moe_selftest_wait_timeout(int64_t spins, nv_stream_t stream);
+
+/* Static description of a status code (never NULL). */
+const char *nvfp4moe_status_string(int status);
+
+/* Library version string. */
+const char *nvfp4moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NVFP4MOE_H */

@@ -1,0 +1,251 @@
+// The C ABI of libnvfp4moe.so: argument checks, the per-device status word,
+// and the launches of every step of the hot path.  See include/nvfp4moe.h for
+// the contract of each entry point.
+#include <cstdio>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace nvm {
+
+// First error any kernel recorded on this device (0 = none).
+static __device__ int g_status;
+
+int *status_ptr() {
+  static int *cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!cache[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
+    cache[dev] = static_cast<int *>(p);
+  }
+  return cache[dev];
+}
+
+static bool al16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+static int64_t rup(int64_t a, int64_t b) { return (a + b - 1) / b * b; }
+
+static int amax_blocks(int64_t per_batch) {
+  const int64_t n16 = per_batch / 8;
+  int64_t nb = (n16 + 2047) / 2048;
+  if (nb < 1) nb = 1;
+  if (nb > 1216) nb = 1216;
+  return (int)nb;
+}
+
+}  // namespace nvm
+
+using namespace nvm;
+
+extern "C" {
+
+int64_t nvfp4moe_padded_cap(int64_t M_total, int64_t E) { return rup(M_total + 127 * E, 128); }
+
+int64_t nvfp4moe_scale_bytes(int64_t padded_rows, int64_t kblocks) {
+  return rup(padded_rows, 128) / 128 * ((kblocks + 3) / 4) * 512;
+}
+
+int64_t nvfp4moe_scale_offset(int64_t rp, int64_t c, int64_t kblocks) {
+  return scale_offset(rp, c, (kblocks + 3) / 4);
+}
+
+size_t nvfp4moe_quantize_workspace_bytes(int64_t batch, int64_t rows, int64_t cols) {
+  if (batch < 1 || rows < 0 || cols < 0) return 0;
+  const int nb = amax_blocks(rows * cols);
+  return (size_t)rup((batch * nb + batch) * 4, 256);
+}
+
+const char *nvfp4moe_version(void) { return "nvfp4moe 0.1 (sm_103a)"; }
+
+const char *nvfp4moe_status_string(int s) {
+  switch (s) {
+    case NV_OK: return "ok";
+    case NV_ERR_ARG: return "invalid argument";
+    case NV_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case NV_ERR_SHAPE: return "shape violates divisibility rules";
+    case NV_ERR_OFFSETS: return "group offsets inconsistent";
+    case NV_ERR_TIMEOUT: return "bounded wait ran out";
+    case NV_ERR_CUDA: return "CUDA runtime error";
+    case NV_ERR_UNSUPPORTED: return "unsupported";
+    case NV_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+  }
+}
+
+int nvfp4moe_get_device_status(nv_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return NV_ERR_CUDA;
+  int *p = status_ptr();
+  if (!p) return NV_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return NV_ERR_CUDA;
+  if (v != 0 && cudaMemset(p, 0, sizeof(int)) != cudaSuccess) return NV_ERR_CUDA;
+  return v;
+}
+
+int nvfp4moe_selftest_wait_timeout(int64_t spins, nv_stream_t stream) {
+  if (spins < 1) return NV_ERR_ARG;
+  int *st = status_ptr();
+  if (!st) return NV_ERR_CUDA;
+  return launch_wait_selftest(spins, st, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int nvfp4_quantize(const void *x, int64_t batch, int64_t rows, int64_t cols, const int32_t *group_offsets,
+                   int32_t num_groups, const float *outer_scale_in, float *outer_scale_out, uint8_t *codes,
+                   uint8_t *scales, void *workspace, size_t workspace_bytes, nv_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!x || !codes || !scales || batch < 1 || rows < 0 || cols < 0) return NV_ERR_ARG;
+  if (cols % 16) return NV_ERR_SHAPE;
+  if (group_offsets && (batch != 1 || num_groups < 1 || num_groups > kMaxGroups)) return NV_ERR_ARG;
+  if (!al16(x) || !al16(codes) || !al16(scales) || !al16(group_offsets)) return NV_ERR_ALIGN;
+  if (rows == 0 || cols == 0) return NV_OK;
+  if (rows * cols / 16 >= (int64_t)1 << 31 || (group_offsets && rows >= (int64_t)1 << 30)) return NV_ERR_SHAPE;
+  int *st = status_ptr();
+  if (!st) return NV_ERR_CUDA;
+  const float *sg = outer_scale_in;
+  if (!outer_scale_in) {
+    const size_t need = nvfp4moe_quantize_workspace_bytes(batch, rows, cols);
+    if (!workspace || workspace_bytes < need || !al16(workspace)) return NV_ERR_WORKSPACE;
+    const int nb = amax_blocks(rows * cols);
+    float *partial = static_cast<float *>(workspace);
+    float *dst = outer_scale_out ? outer_scale_out : partial + batch * nb;
+    int r = launch_amax(static_cast<const uint16_t *>(x), batch, rows * cols, partial, nb, dst, s);
+    if (r != NV_OK) return r;
+    sg = dst;
+  } else if (outer_scale_out && outer_scale_out != outer_scale_in) {
+    if (cudaMemcpyAsync(outer_scale_out, outer_scale_in, batch * sizeof(float), cudaMemcpyDeviceToDevice, s) !=
+        cudaSuccess)
+      return NV_ERR_CUDA;
+  }
+  return launch_nvfp4_quant(static_cast<const uint16_t *>(x), batch, rows, cols, group_offsets, num_groups, sg, codes,
+                            scales, st, s);
+}
+
+int mxfp8_quantize(const void *x, int64_t rows, int64_t cols, const int32_t *group_offsets, int32_t num_groups,
+                   int mode, uint64_t seed, uint64_t counter_offset_row, uint64_t counter_offset_t,
+                   uint8_t *codes_row, uint8_t *scales_row, uint8_t *codes_t, uint8_t *scales_t,
+                   nv_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!x || rows < 0 || cols < 0 || (mode != NV_RN && mode != NV_SR)) return NV_ERR_ARG;
+  if ((codes_row == nullptr) != (scales_row == nullptr) || (codes_t == nullptr) != (scales_t == nullptr))
+    return NV_ERR_ARG;
+  if (group_offsets && (num_groups < 1 || num_groups > kMaxGroups)) return NV_ERR_ARG;
+  if (cols % 32) return NV_ERR_SHAPE;
+  if (codes_t && cols % 128) return NV_ERR_SHAPE;
+  if (!al16(x) || !al16(codes_row) || !al16(scales_row) || !al16(codes_t) || !al16(scales_t) || !al16(group_offsets))
+    return NV_ERR_ALIGN;
+  if (rows == 0 || cols == 0 || (!codes_row && !codes_t)) return NV_OK;
+  if (rows >= (int64_t)1 << 30 || rows * cols >= (int64_t)1 << 40) return NV_ERR_SHAPE;
+  int *st = status_ptr();
+  if (!st) return NV_ERR_CUDA;
+  const int E = group_offsets ? num_groups : 0;
+  const int sr = mode == NV_SR;
+  if (codes_t)
+    return launch_mx_transpose_bf16(static_cast<const uint16_t *>(x), rows, cols, group_offsets, E, sr, seed,
+                                    counter_offset_t, counter_offset_row, codes_t, scales_t, codes_row, scales_row, st,
+                                    s);
+  return launch_mxfp8_rowwise(static_cast<const uint16_t *>(x), rows, cols, group_offsets, E, sr, seed,
+                              counter_offset_row, codes_row, scales_row, st, s);
+}
+
+int dequant_transpose_requant_sr(const uint8_t *codes, const uint8_t *scales, const float *outer_scale, int64_t batch,
+                                 int64_t rows, int64_t cols, const int32_t *group_offsets, int32_t num_groups,
+                                 uint64_t seed, uint64_t counter_offset, uint8_t *out_codes, uint8_t *out_scales,
+                                 nv_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!codes || !scales || !outer_scale || !out_codes || !out_scales || batch < 1 || rows < 0 || cols < 0)
+    return NV_ERR_ARG;
+  if (group_offsets && (batch != 1 || num_groups < 1 || num_groups > kMaxGroups)) return NV_ERR_ARG;
+  if (cols % 128) return NV_ERR_SHAPE;
+  if (!group_offsets && rows % 128) return NV_ERR_SHAPE;
+  if (!al16(codes) || !al16(scales) || !al16(out_codes) || !al16(out_scales) || !al16(group_offsets))
+    return NV_ERR_ALIGN;
+  if (rows == 0 || cols == 0) return NV_OK;
+  if (rows >= (int64_t)1 << 30) return NV_ERR_SHAPE;
+  int *st = status_ptr();
+  if (!st) return NV_ERR_CUDA;
+  return launch_requant(codes, scales, outer_scale, batch, rows, cols, group_offsets, group_offsets ? num_groups : 0,
+                        seed, counter_offset, out_codes, out_scales, st, s);
+}
+
+static int gemm_common_checks(const int32_t *go, int32_t E, int64_t M_total, int64_t N, int64_t K) {
+  if (!go || E < 1 || E > kMaxGroups || M_total < 0 || N <= 0 || K <= 0) return NV_ERR_ARG;
+  if (!al16(go)) return NV_ERR_ALIGN;
+  if (M_total >= (int64_t)1 << 30) return NV_ERR_SHAPE;
+  return NV_OK;
+}
+
+int grouped_gemm_nvfp4_fwd(const void *x_bf16, const float *x_outer_scale, const uint8_t *x_codes,
+                           const uint8_t *x_scales, const uint8_t *w_codes, const uint8_t *w_scales,
+                           const float *w_outer_scale, const int32_t *group_offsets, int32_t E, int64_t M_total,
+                           int64_t N, int64_t K, void *y, int y_dtype, void *workspace, size_t workspace_bytes,
+                           nv_stream_t stream) {
+  (void)workspace; (void)workspace_bytes;
+  if (x_bf16) return NV_ERR_UNSUPPORTED;
+  int r = gemm_common_checks(group_offsets, E, M_total, N, K);
+  if (r != NV_OK) return r;
+  if (!x_outer_scale || !x_codes || !x_scales || !w_codes || !w_scales || !w_outer_scale || !y) return NV_ERR_ARG;
+  if (y_dtype != NV_OUT_BF16 && y_dtype != NV_OUT_FP32) return NV_ERR_ARG;
+  if (N % 128 || K % 256) return NV_ERR_SHAPE;
+  if (!al16(x_codes) || !al16(x_scales) || !al16(w_codes) || !al16(w_scales) || !al16(y)) return NV_ERR_ALIGN;
+  int *st = status_ptr();
+  if (!st) return NV_ERR_CUDA;
+  GemmProblem p = {kGemmNvfp4Fwd, x_codes, x_scales, w_codes, w_scales, x_outer_scale, w_outer_scale,
+                   group_offsets, E, M_total, N, K, y, y_dtype == NV_OUT_FP32};
+  return launch_grouped_gemm(p, st, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int grouped_gemm_mxfp8_dx(const uint8_t *g_codes, const uint8_t *g_scales, const uint8_t *wt_codes,
+                          const uint8_t *wt_scales, const int32_t *group_offsets, int32_t E, int64_t M_total,
+                          int64_t N, int64_t K, void *dx, int dx_dtype, void *workspace, size_t workspace_bytes,
+                          nv_stream_t stream) {
+  (void)workspace; (void)workspace_bytes;
+  int r = gemm_common_checks(group_offsets, E, M_total, N, K);
+  if (r != NV_OK) return r;
+  if (!g_codes || !g_scales || !wt_codes || !wt_scales || !dx) return NV_ERR_ARG;
+  if (dx_dtype != NV_OUT_BF16 && dx_dtype != NV_OUT_FP32) return NV_ERR_ARG;
+  if (N % 128 || K % 128) return NV_ERR_SHAPE;
+  if (!al16(g_codes) || !al16(g_scales) || !al16(wt_codes) || !al16(wt_scales) || !al16(dx)) return NV_ERR_ALIGN;
+  int *st = status_ptr();
+  if (!st) return NV_ERR_CUDA;
+  GemmProblem p = {kGemmMxfp8Dx, g_codes, g_scales, wt_codes, wt_scales, nullptr, nullptr,
+                   group_offsets, E, M_total, N, K, dx, dx_dtype == NV_OUT_FP32};
+  return launch_grouped_gemm(p, st, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int grouped_gemm_mxfp8_dw(const uint8_t *gt_codes, const uint8_t *gt_scales, const uint8_t *xt_codes,
+                          const uint8_t *xt_scales, const int32_t *group_offsets, int32_t E, int64_t M_total,
+                          int64_t N, int64_t K, float *dw, void *workspace, size_t workspace_bytes,
+                          nv_stream_t stream) {
+  (void)workspace; (void)workspace_bytes;
+  int r = gemm_common_checks(group_offsets, E, M_total, N, K);
+  if (r != NV_OK) return r;
+  if (!gt_codes || !gt_scales || !xt_codes || !xt_scales || !dw) return NV_ERR_ARG;
+  if (N % 128 || K % 128) return NV_ERR_SHAPE;
+  if (!al16(gt_codes) || !al16(gt_scales) || !al16(xt_codes) || !al16(xt_scales) || !al16(dw)) return NV_ERR_ALIGN;
+  int *st = status_ptr();
+  if (!st) return NV_ERR_CUDA;
+  GemmProblem p = {kGemmMxfp8Dw, gt_codes, gt_scales, xt_codes, xt_scales, nullptr, nullptr,
+                   group_offsets, E, M_total, N, K, dw, 1};
+  return launch_grouped_gemm(p, st, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int nvfp4moe_swiglu_fwd(const void *y13, int64_t M, int64_t I, void *h, nv_stream_t stream) {
+  if (!y13 || !h || M < 0 || I <= 0) return NV_ERR_ARG;
+  if (I % 8) return NV_ERR_SHAPE;
+  if (!al16(y13) || !al16(h)) return NV_ERR_ALIGN;
+  if (M == 0) return NV_OK;
+  return launch_swiglu_fwd(static_cast<const uint16_t *>(y13), M, I, static_cast<uint16_t *>(h),
+                           reinterpret_cast<cudaStream_t>(stream));
+}
+
+int nvfp4moe_swiglu_bwd(const void *dh, const void *y13, int64_t M, int64_t I, void *dy13, nv_stream_t stream) {
+  if (!dh || !y13 || !dy13 || M < 0 || I <= 0) return NV_ERR_ARG;
+  if (I % 8) return NV_ERR_SHAPE;
+  if (!al16(dh) || !al16(y13) || !al16(dy13)) return NV_ERR_ALIGN;
+  if (M == 0) return NV_OK;
+  return launch_swiglu_bwd(static_cast<const uint16_t *>(dh), static_cast<const uint16_t *>(y13), M, I,
+                           static_cast<uint16_t *>(dy13), reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,305 @@
+// Device-side building blocks shared by the kernels of libnvfp4moe.so:
+// number-format conversions, Philox4x32-10, 16-bit stochastic rounding to
+// E4M3, the block-scale layout, and expert-group bookkeeping.
+//
+// Formats follow "End-to-End 4-Bit Training", "Low-precision formats on
+// Blackwell" (E2M1 values, E4M3 NVFP4 scales, E8M0 MX scales); rounding and
+// random-bit conventions are the ones stated in include/nvfp4moe.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "nvfp4moe.h"
+
+namespace nvm {
+
+constexpr int kMaxGroups = 1024;  // experts per grouped call (smem tables)
+
+// ---------------------------------------------------------------------------
+// status word
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void record_error(int *status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+// ---------------------------------------------------------------------------
+// memory helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+__device__ __forceinline__ uint2 ld_stream_v2(const void *p) {
+  uint2 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
+               : "=r"(r.x), "=r"(r.y)
+               : "l"(p));
+  return r;
+}
+__device__ __forceinline__ uint32_t ld_stream_u32(const void *p) {
+  uint32_t r;
+  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(r) : "l"(p));
+  return r;
+}
+
+// ---------------------------------------------------------------------------
+// bf16
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// max of |bf16| over the two halves of four words, as a packed bf16x2
+__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a & 0x7FFF7FFFu), "r"(b & 0x7FFF7FFFu));
+  return d;
+}
+__device__ __forceinline__ float bf16x2_max_to_f32(uint32_t m) {
+  return fmaxf(bf16_lo(m), bf16_hi(m));
+}
+
+// round fp32 -> bf16 (nearest even), returns the 16-bit pattern
+__device__ __forceinline__ uint32_t f32_to_bf16_bits(float x) {
+  uint16_t r;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(x));
+  return r;
+}
+
+// ---------------------------------------------------------------------------
+// E2M1 / E4M3 conversions (hardware cvt: round to nearest even, saturating)
+// ---------------------------------------------------------------------------
+// Eight fp32 values -> eight E2M1 codes packed little-endian in 32 bits:
+// element k in nibble k (element 2j in the low nibble of byte j).
+__device__ __forceinline__ uint32_t cvt_e2m1x8(float v0, float v1, float v2, float v3,
+                                               float v4, float v5, float v6, float v7) {
+  uint32_t out;
+  asm("{\n\t"
+      ".reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t"
+      "}"
+      : "=r"(out)
+      : "f"(v0), "f"(v1), "f"(v2), "f"(v3), "f"(v4), "f"(v5), "f"(v6), "f"(v7));
+  return out;
+}
+
+// One fp32 -> E4M3 code (round to nearest even, saturating at 448).
+__device__ __forceinline__ uint32_t cvt_e4m3_rn(float x) {
+  uint16_t d;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(0.0f), "f"(x));
+  return d & 0xFFu;
+}
+// Two fp32 -> two E4M3 codes in the low 16 bits (a in byte 0, b in byte 1).
+__device__ __forceinline__ uint32_t cvt_e4m3x2_rn(float a, float b) {
+  uint16_t d;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(b), "f"(a));
+  return d;
+}
+
+// E4M3 code -> fp32 (exact; via f16, which holds every E4M3 value).
+__device__ __forceinline__ float e4m3_to_f32(uint32_t code) {
+  uint32_t h2;
+  uint16_t c16 = (uint16_t)(code & 0xFFu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c16));
+  float f;
+  asm("{ .reg .f16 lo, hi;\n\t mov.b32 {lo, hi}, %1;\n\t cvt.f32.f16 %0, lo; }" : "=f"(f) : "r"(h2));
+  return f;
+}
+
+// E2M1 code (4 bits) -> fp32 value, from the bit fields (sign, 2-bit exponent
+// with bias 1, 1-bit mantissa).
+__device__ __forceinline__ float e2m1_to_f32(uint32_t c) {
+  const uint32_t e = (c >> 1) & 3u, m = c & 1u;
+  // subnormal: m * 0.5 ; normal: (1 + m/2) * 2^(e-1)
+  float mag = (e == 0) ? 0.5f * (float)m : __uint_as_float(((e - 1u + 127u) << 23) | (m << 22));
+  return (c & 8u) ? -mag : mag;
+}
+
+// ---------------------------------------------------------------------------
+// E8M0 (OCP MX): scale = floor(log2 amax) - 8, clamped to [-127, 127]
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int floor_log2_nonzero(float a) {
+  const uint32_t u = __float_as_uint(a) & 0x7FFFFFFFu;
+  const int e = (int)(u >> 23);
+  if (e == 0) return (31 - __clz(u)) - 149;  // fp32 subnormal
+  return e - 127;
+}
+// returns the E8M0 code; *mult = 2^-sexp (exact fp32)
+__device__ __forceinline__ uint32_t e8m0_scale(float bamax, float *mult) {
+  int sexp = -127;
+  if (bamax > 0.0f) {
+    sexp = floor_log2_nonzero(bamax) - 8;
+    sexp = sexp < -127 ? -127 : (sexp > 127 ? 127 : sexp);
+  }
+  *mult = __uint_as_float((uint32_t)(127 - sexp) << 23);
+  return (uint32_t)(sexp + 127);
+}
+
+// ---------------------------------------------------------------------------
+// Stochastic rounding fp32 -> E4M3 with a 16-bit random integer r:
+// with a <= |w| < b the E4M3 neighbours, round up iff r < floor(2^16 f),
+// f = (|w| - a) / (b - a); |w| >= 448 saturates; the sign is kept.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t sr_e4m3(float w, uint32_t r) {
+  const uint32_t u = __float_as_uint(w);
+  const uint32_t sign = (u >> 24) & 0x80u;
+  const uint32_t a = u & 0x7FFFFFFFu;
+  uint32_t code;
+  if (a >= 0x43E00000u) {  // >= 448
+    code = 0x7Eu;
+  } else if (a >= 0x3C800000u) {  // [2^-6, 448): 3 kept mantissa bits, 20 dropped
+    const uint32_t thr = (a & 0xFFFFFu) >> 4;
+    code = (a >> 20) + (r < thr ? 1u : 0u) - (120u << 3);
+  } else {  // E4M3 subnormal range, step 2^-9
+    const float k = __uint_as_float(a) * 512.0f;  // exact
+    const float ak = floorf(k);
+    const uint32_t thr = (uint32_t)((k - ak) * 65536.0f);
+    code = (uint32_t)ak + (r < thr ? 1u : 0u);
+  }
+  return code | sign;
+}
+
+// ---------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of two 32x32
+// multiplies into 64-bit products, the high halves XORed with the other two
+// words and the round key, with the key bumped by the Weyl constants.
+// ---------------------------------------------------------------------------
+struct PhiloxKey {
+  uint32_t k0, k1;
+};
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, PhiloxKey key) {
+  uint32_t k0 = key.k0, k1 = key.k1;
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint64_t p0 = (uint64_t)0xD2511F53u * c.x;
+    const uint64_t p1 = (uint64_t)0xCD9E8D57u * c.z;
+    const uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+    const uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return c;
+}
+// The 8 x 16-bit draws of elements 8q .. 8q+7 under (seed, offset).
+__device__ __forceinline__ uint4 philox_bits8(uint64_t q, uint64_t seed, uint64_t offset) {
+  return philox4x32_10(make_uint4((uint32_t)q, (uint32_t)(q >> 32), (uint32_t)offset,
+                                  (uint32_t)(offset >> 32)),
+                       PhiloxKey{(uint32_t)seed, (uint32_t)(seed >> 32)});
+}
+// element k (0..7) of a philox_bits8 result
+__device__ __forceinline__ uint32_t draw16(const uint4 &w, int k) {
+  const uint32_t word = (k >> 1) == 0 ? w.x : (k >> 1) == 1 ? w.y : (k >> 1) == 2 ? w.z : w.w;
+  return (k & 1) ? (word >> 16) : (word & 0xFFFFu);
+}
+
+// ---------------------------------------------------------------------------
+// Block-scale layout: 128x4 tiles of 512 bytes (see nvfp4moe.h)
+// ---------------------------------------------------------------------------
+__host__ __device__ __forceinline__ int64_t scale_offset(int64_t rp, int64_t c, int64_t ka) {
+  return ((rp >> 7) * ka + (c >> 2)) * 512 + (rp & 31) * 16 + ((rp >> 5) & 3) * 4 + (c & 3);
+}
+// byte position inside one 512-byte tile for row r (mod 128), column c (mod 4)
+__host__ __device__ __forceinline__ int atom_pos(int r, int c) {
+  return (r & 31) * 16 + ((r >> 5) & 3) * 4 + (c & 3);
+}
+
+// ---------------------------------------------------------------------------
+// Expert groups: load group_offsets into shared memory, check them, and build
+// the group-padded starts P_e = sum_{e'<e} roundup(M_e', 128).
+// Every thread of the CTA must call it.  Returns false (and records
+// NV_ERR_OFFSETS) when the offsets are inconsistent.
+// ---------------------------------------------------------------------------
+__device__ inline bool load_groups(const int32_t *__restrict__ go, int E, int64_t M_total,
+                                   int *s_off, int *s_pad, int *s_flag, int *status) {
+  if (threadIdx.x == 0) *s_flag = 0;
+  __syncthreads();
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+    const int v = go[e];
+    s_off[e] = v;
+    bool bad = (e == 0 && v != 0) || (e == E && (int64_t)v != M_total) || v < 0 || (int64_t)v > M_total;
+    if (e > 0) bad |= go[e - 1] > v;
+    if (bad) atomicOr(s_flag, 1);
+  }
+  __syncthreads();
+  const bool ok = *s_flag == 0;
+  if (!ok) {
+    if (threadIdx.x == 0) record_error(status, NV_ERR_OFFSETS);
+    return false;
+  }
+  if (threadIdx.x < 32) {  // warp 0: exclusive scan of the padded sizes
+    int carry = 0;
+    for (int base = 0; base <= E; base += 32) {
+      const int e = base + (int)threadIdx.x;
+      int v = 0;
+      if (e < E) v = ((s_off[e + 1] - s_off[e]) + 127) & ~127;
+      int incl = v;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int n = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+        if ((int)threadIdx.x >= d) incl += n;
+      }
+      if (e <= E) s_pad[e] = carry + incl - v;
+      carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    }
+  }
+  __syncthreads();
+  return true;
+}
+
+// largest e in [0, E) with s_pad[e] <= p (the group owning padded row p)
+__device__ __forceinline__ int find_group(const int *s_pad, int E, int p) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_pad[mid] <= p) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+}  // namespace nvm
+
+// ---------------------------------------------------------------------------
+// mbarrier helpers with bounded waits (a wait that runs out returns false;
+// callers record NV_ERR_TIMEOUT and leave without touching the data)
+// ---------------------------------------------------------------------------
+namespace nvm {
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t a, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t a, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(a), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, uint64_t limit) {
+  for (uint64_t i = 0; i < limit; ++i)
+    if (mbar_try_wait(a, parity)) return true;
+  return false;
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t a) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(a) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t a, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(a), "r"(bytes) : "memory");
+}
+}  // namespace nvm

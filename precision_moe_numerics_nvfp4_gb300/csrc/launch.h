@@ -1,0 +1,42 @@
+// Host-side launchers shared between the translation units of libnvfp4moe.so.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "nvfp4moe.h"
+
+namespace nvm {
+
+int *status_ptr();  // device address of this device's status word (api.cu)
+
+int launch_amax(const uint16_t *x, int64_t batch, int64_t per_batch, float *partial, int nblk, float *sg_out,
+                cudaStream_t s);
+int launch_nvfp4_quant(const uint16_t *x, int64_t batch, int64_t rows, int64_t cols, const int32_t *groups, int E,
+                       const float *sg, uint8_t *codes, uint8_t *scales, int *status, cudaStream_t s);
+int launch_mxfp8_rowwise(const uint16_t *x, int64_t rows, int64_t cols, const int32_t *groups, int E, int sr,
+                         uint64_t seed, uint64_t off, uint8_t *codes, uint8_t *scales, int *status, cudaStream_t s);
+int launch_mx_transpose_bf16(const uint16_t *x, int64_t rows, int64_t cols, const int32_t *groups, int E, int sr,
+                             uint64_t seed, uint64_t off_t, uint64_t off_row, uint8_t *codes_t, uint8_t *scales_t,
+                             uint8_t *codes_row, uint8_t *scales_row, int *status, cudaStream_t s);
+int launch_requant(const uint8_t *codes, const uint8_t *scales, const float *sg, int64_t batch, int64_t rows,
+                   int64_t cols, const int32_t *groups, int E, uint64_t seed, uint64_t off, uint8_t *out_codes,
+                   uint8_t *out_scales, int *status, cudaStream_t s);
+int launch_swiglu_fwd(const uint16_t *y13, int64_t M, int64_t I, uint16_t *h, cudaStream_t s);
+int launch_swiglu_bwd(const uint16_t *dh, const uint16_t *y13, int64_t M, int64_t I, uint16_t *dy13, cudaStream_t s);
+int launch_wait_selftest(int64_t spins, int *status, cudaStream_t s);
+
+// grouped GEMMs (gemm.cu)
+enum GemmKind { kGemmNvfp4Fwd = 0, kGemmMxfp8Dx = 1, kGemmMxfp8Dw = 2 };
+struct GemmProblem {
+  int kind;
+  const uint8_t *a_codes, *a_scales, *b_codes, *b_scales;
+  const float *a_sg, *b_sg;  // NVFP4 outer scales (fwd only)
+  const int32_t *groups;
+  int E;
+  int64_t M_total, N, K;
+  void *out;
+  int out_fp32;
+};
+int launch_grouped_gemm(const GemmProblem &p, int *status, cudaStream_t s);
+
+}  // namespace nvm

@@ -1,0 +1,593 @@
+// Quantization kernels of libnvfp4moe.so (HBM-bound):
+//   amax_partial / outer_scale_finalize   step a1: per-tensor amax -> sg
+//   nvfp4_quant                           step a2: bf16 -> NVFP4 1x16 (RN)
+//   mxfp8_rowwise                         MXFP8 1x32 along rows (RN or SR)
+//   mx_transpose<...>                     steps a5 / a6: transpose through
+//                                         shared memory + MXFP8 (SR or RN)
+//                                         of bf16 or dequantized NVFP4 input
+//
+// "End-to-End 4-Bit Training": "Low-precision formats on Blackwell" (NVFP4
+// block scaling, FP32 outer scale), "Re-quantization with stochastic
+// rounding" (dequantize, transpose at higher precision, SR to MXFP8), and the
+// Figure 4 dataflow of the Chinese translation (row-wise and transposed SR
+// quantization of the BF16 gradient).
+//
+// Work decomposition: every CTA owns one "window" of 128 padded rows of one
+// expert group (or of one matrix of a batch) and a chunk of columns, so it
+// produces whole 512-byte scale tiles, which it stages in shared memory and
+// writes out with 16-byte stores.
+#include "common.cuh"
+#include "launch.h"
+
+namespace nvm {
+
+// ---------------------------------------------------------------------------
+// a1: amax
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) amax_partial_kernel(const uint16_t *__restrict__ x,
+                                                           int64_t per_batch, float *__restrict__ partial,
+                                                           int nblk) {
+  const int b = blockIdx.y;
+  const uint4 *p = reinterpret_cast<const uint4 *>(x + (int64_t)b * per_batch);
+  const int64_t n16 = per_batch >> 3;
+  const int64_t st = (int64_t)nblk * 256;
+  int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x;
+  uint32_t acc0 = 0, acc1 = 0;
+  for (; i + 3 * st < n16; i += 4 * st) {
+    const uint4 v0 = ld_stream_v4(p + i), v1 = ld_stream_v4(p + i + st);
+    const uint4 v2 = ld_stream_v4(p + i + 2 * st), v3 = ld_stream_v4(p + i + 3 * st);
+    acc0 = bf16x2_absmax(acc0, bf16x2_absmax(bf16x2_absmax(v0.x, v0.y), bf16x2_absmax(v0.z, v0.w)));
+    acc1 = bf16x2_absmax(acc1, bf16x2_absmax(bf16x2_absmax(v1.x, v1.y), bf16x2_absmax(v1.z, v1.w)));
+    acc0 = bf16x2_absmax(acc0, bf16x2_absmax(bf16x2_absmax(v2.x, v2.y), bf16x2_absmax(v2.z, v2.w)));
+    acc1 = bf16x2_absmax(acc1, bf16x2_absmax(bf16x2_absmax(v3.x, v3.y), bf16x2_absmax(v3.z, v3.w)));
+  }
+  for (; i < n16; i += st) {
+    const uint4 v = ld_stream_v4(p + i);
+    acc0 = bf16x2_absmax(acc0, bf16x2_absmax(bf16x2_absmax(v.x, v.y), bf16x2_absmax(v.z, v.w)));
+  }
+  float m = bf16x2_max_to_f32(bf16x2_absmax(acc0, acc1));
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, d));
+  __shared__ float s_m[8];
+  if ((threadIdx.x & 31) == 0) s_m[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float r = s_m[0];
+    for (int w = 1; w < 8; ++w) r = fmaxf(r, s_m[w]);
+    partial[(int64_t)b * nblk + blockIdx.x] = r;
+  }
+}
+
+// sg = amax / (6 * 448), or 1 for an all-zero tensor
+__global__ void __launch_bounds__(32) outer_scale_finalize_kernel(const float *__restrict__ partial, int nblk,
+                                                                  float *__restrict__ sg_out) {
+  const int b = blockIdx.x;
+  float m = 0.0f;
+  for (int i = threadIdx.x; i < nblk; i += 32) m = fmaxf(m, partial[(int64_t)b * nblk + i]);
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, d));
+  if (threadIdx.x == 0) sg_out[b] = (m == 0.0f) ? 1.0f : __fdiv_rn(m, 2688.0f);
+}
+
+// ---------------------------------------------------------------------------
+// window -> rows mapping shared by the quantizers
+// ---------------------------------------------------------------------------
+struct Window {
+  int64_t src_row0;  // first source row of the window
+  int64_t rp0;       // padded row of the window's first row
+  int nvalid;        // rows of the window that exist (0..128)
+  int seg;           // group (grouped) or matrix (batched)
+};
+
+// grouped: windows tile the group-padded rows; batched: `wpb` windows per
+// matrix of `rows` rows.  s_off/s_pad are valid when grouped.
+__device__ __forceinline__ Window map_window(bool grouped, int win, int E, const int *s_off, const int *s_pad,
+                                             int64_t rows, int wpb) {
+  Window w;
+  if (grouped) {
+    const int p0 = win * 128;
+    w.rp0 = p0;
+    if (p0 >= s_pad[E]) {
+      w.src_row0 = 0; w.nvalid = 0; w.seg = E;
+    } else {
+      const int e = find_group(s_pad, E, p0);
+      w.seg = e;
+      w.src_row0 = (int64_t)s_off[e] + (p0 - s_pad[e]);
+      const int64_t left = (int64_t)s_off[e + 1] - w.src_row0;
+      w.nvalid = left < 128 ? (int)left : 128;
+    }
+  } else {
+    const int b = win / wpb, wb = win - b * wpb;
+    w.seg = b;
+    w.src_row0 = (int64_t)b * rows + (int64_t)wb * 128;
+    w.rp0 = ((int64_t)b * wpb + wb) * 128;
+    const int64_t left = rows - (int64_t)wb * 128;
+    w.nvalid = left < 128 ? (int)left : 128;
+  }
+  return w;
+}
+
+// Shared-memory group tables.  E == 0 with `single` means one group of all
+// rows (offsets {0, rows}) built without reading global memory.
+struct GroupSmem {
+  int flag;
+  int off[kMaxGroups + 1];
+  int pad[kMaxGroups + 1];
+};
+
+__device__ __forceinline__ bool setup_groups(GroupSmem &g, const int32_t *go, int &E, int64_t rows, int *status) {
+  if (go == nullptr) {  // one group of all rows
+    if (threadIdx.x == 0) {
+      g.off[0] = 0; g.off[1] = (int)rows;
+      g.pad[0] = 0; g.pad[1] = (int)((rows + 127) & ~127LL);
+    }
+    E = 1;
+    __syncthreads();
+    return true;
+  }
+  return load_groups(go, E, rows, g.off, g.pad, &g.flag, status);
+}
+
+// ---------------------------------------------------------------------------
+// a2: NVFP4 quantization, one CTA = 128 padded rows x 256 columns
+// ---------------------------------------------------------------------------
+struct NvQuantArgs {
+  const uint16_t *x;
+  int64_t rows, cols;
+  const int32_t *groups;  // non-null: grouped scale layout (batch == 1)
+  int E;
+  int wpb;                // windows per matrix (batched)
+  const float *sg;        // [batch]
+  uint8_t *codes, *scales;
+  int64_t ka;             // scale tiles per padded row tile = ceil(cols / 64)
+  int *status;
+};
+
+__device__ __forceinline__ void nvfp4_block(const uint4 &a, const uint4 &b, float sg, float den6, uint2 &codes,
+                                            uint32_t &scode) {
+  uint32_t m = bf16x2_absmax(bf16x2_absmax(a.x, a.y), bf16x2_absmax(a.z, a.w));
+  m = bf16x2_absmax(m, bf16x2_absmax(bf16x2_absmax(b.x, b.y), bf16x2_absmax(b.z, b.w)));
+  const float bamax = bf16x2_max_to_f32(m);
+  scode = cvt_e4m3_rn(__fdiv_rn(bamax, den6));
+  const float s = e4m3_to_f32(scode);
+  const float inv = (s == 0.0f) ? 0.0f : __frcp_rn(__fmul_rn(s, sg));
+  codes.x = cvt_e2m1x8(__fmul_rn(bf16_lo(a.x), inv), __fmul_rn(bf16_hi(a.x), inv), __fmul_rn(bf16_lo(a.y), inv),
+                       __fmul_rn(bf16_hi(a.y), inv), __fmul_rn(bf16_lo(a.z), inv), __fmul_rn(bf16_hi(a.z), inv),
+                       __fmul_rn(bf16_lo(a.w), inv), __fmul_rn(bf16_hi(a.w), inv));
+  codes.y = cvt_e2m1x8(__fmul_rn(bf16_lo(b.x), inv), __fmul_rn(bf16_hi(b.x), inv), __fmul_rn(bf16_lo(b.y), inv),
+                       __fmul_rn(bf16_hi(b.y), inv), __fmul_rn(bf16_lo(b.z), inv), __fmul_rn(bf16_hi(b.z), inv),
+                       __fmul_rn(bf16_lo(b.w), inv), __fmul_rn(bf16_hi(b.w), inv));
+}
+
+__global__ void __launch_bounds__(256) nvfp4_quant_kernel(NvQuantArgs A) {
+  __shared__ __align__(16) uint8_t s_sc[4 * 512];
+  __shared__ GroupSmem s_g;
+  const bool grouped = A.groups != nullptr;
+  int E = A.E;
+  if (grouped && !load_groups(A.groups, E, A.rows, s_g.off, s_g.pad, &s_g.flag, A.status)) return;
+  const Window w = map_window(grouped, blockIdx.y, E, s_g.off, s_g.pad, A.rows, A.wpb);
+  const float sg = A.sg[grouped ? 0 : w.seg];
+  const float den6 = __fmul_rn(6.0f, sg);
+
+  reinterpret_cast<uint2 *>(s_sc)[threadIdx.x] = make_uint2(0u, 0u);
+  __syncthreads();
+
+  const int KB = (int)(A.cols >> 4);
+  const int kb0 = blockIdx.x * 16;
+  const int nkb = min(16, KB - kb0);
+  // four blocks of 16 per thread per phase, two phases
+#pragma unroll
+  for (int ph = 0; ph < 2; ++ph) {
+    uint4 va[4], vb[4];
+    bool ok[4];
+    int64_t off[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int q = (ph * 4 + u) * 256 + threadIdx.x;
+      const int i = q >> 4, kbl = q & 15;
+      ok[u] = (i < w.nvalid) && (kbl < nkb);
+      off[u] = (w.src_row0 + i) * A.cols + (int64_t)(kb0 + kbl) * 16;
+      if (ok[u]) {
+        va[u] = ld_stream_v4(A.x + off[u]);
+        vb[u] = ld_stream_v4(A.x + off[u] + 8);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (!ok[u]) continue;
+      const int q = (ph * 4 + u) * 256 + threadIdx.x;
+      const int i = q >> 4, kbl = q & 15;
+      uint2 c;
+      uint32_t sc;
+      nvfp4_block(va[u], vb[u], sg, den6, c, sc);
+      *reinterpret_cast<uint2 *>(A.codes + (off[u] >> 1)) = c;
+      s_sc[(kbl >> 2) * 512 + atom_pos(i, kbl)] = (uint8_t)sc;
+    }
+  }
+  __syncthreads();
+  // write the (up to) four 512-byte scale tiles of this window / chunk
+  if (threadIdx.x < 128) {
+    const int a = threadIdx.x >> 5, part = threadIdx.x & 31;
+    const int64_t tile_col = kb0 / 4 + a;
+    if (tile_col < A.ka) {
+      const int64_t dst = ((w.rp0 >> 7) * A.ka + tile_col) * 512 + part * 16;
+      *reinterpret_cast<uint4 *>(A.scales + dst) = reinterpret_cast<const uint4 *>(s_sc + a * 512)[part];
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// MXFP8 along rows: one CTA = 128 padded rows x 256 columns (8 blocks of 32)
+// ---------------------------------------------------------------------------
+struct MxRowArgs {
+  const uint16_t *x;
+  int64_t rows, cols;
+  const int32_t *groups;
+  int E;
+  int sr;
+  uint64_t seed, offset;
+  uint8_t *codes, *scales;
+  int64_t ka;  // ceil(cols / 128)
+  int *status;
+};
+
+// quantize 8 consecutive elements starting at source index e0 (a multiple of
+// 8) with multiplier `mult`; RN or SR with the draws of `bits`
+__device__ __forceinline__ uint2 mx_quant8(const float (&v)[8], float mult, bool sr, const uint4 &bits) {
+  uint32_t b[8];
+  if (sr) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) b[k] = sr_e4m3(__fmul_rn(v[k], mult), draw16(bits, k));
+    return make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24), b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
+  }
+  const uint32_t p0 = cvt_e4m3x2_rn(__fmul_rn(v[0], mult), __fmul_rn(v[1], mult));
+  const uint32_t p1 = cvt_e4m3x2_rn(__fmul_rn(v[2], mult), __fmul_rn(v[3], mult));
+  const uint32_t p2 = cvt_e4m3x2_rn(__fmul_rn(v[4], mult), __fmul_rn(v[5], mult));
+  const uint32_t p3 = cvt_e4m3x2_rn(__fmul_rn(v[6], mult), __fmul_rn(v[7], mult));
+  return make_uint2(p0 | (p1 << 16), p2 | (p3 << 16));
+}
+
+__device__ __forceinline__ void unpack8(const uint4 &q, float (&v)[8]) {
+  v[0] = bf16_lo(q.x); v[1] = bf16_hi(q.x); v[2] = bf16_lo(q.y); v[3] = bf16_hi(q.y);
+  v[4] = bf16_lo(q.z); v[5] = bf16_hi(q.z); v[6] = bf16_lo(q.w); v[7] = bf16_hi(q.w);
+}
+
+__global__ void __launch_bounds__(256) mxfp8_rowwise_kernel(MxRowArgs A) {
+  __shared__ __align__(16) uint8_t s_sc[2 * 512];
+  __shared__ GroupSmem s_g;
+  int E = A.E;
+  if (!setup_groups(s_g, A.groups, E, A.rows, A.status)) return;
+  const Window w = map_window(true, blockIdx.y, E, s_g.off, s_g.pad, A.rows, 0);
+  reinterpret_cast<uint32_t *>(s_sc)[threadIdx.x] = 0u;
+  __syncthreads();
+  const int KB = (int)(A.cols >> 5);
+  const int kb0 = blockIdx.x * 8;
+  const int nkb = min(8, KB - kb0);
+#pragma unroll 1
+  for (int it = 0; it < 4; ++it) {
+    const int q = it * 256 + threadIdx.x;
+    const int i = q >> 3, kbl = q & 7;
+    if (i >= w.nvalid || kbl >= nkb) continue;
+    const int64_t e0 = (w.src_row0 + i) * A.cols + (int64_t)(kb0 + kbl) * 32;
+    uint4 raw[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) raw[k] = ld_stream_v4(A.x + e0 + 8 * k);
+    uint32_t m = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) m = bf16x2_absmax(m, bf16x2_absmax(bf16x2_absmax(raw[k].x, raw[k].y), bf16x2_absmax(raw[k].z, raw[k].w)));
+    float mult;
+    const uint32_t sc = e8m0_scale(bf16x2_max_to_f32(m), &mult);
+    uint2 out[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float v[8];
+      unpack8(raw[k], v);
+      uint4 bits = make_uint4(0, 0, 0, 0);
+      if (A.sr) bits = philox_bits8((uint64_t)(e0 >> 3) + k, A.seed, A.offset);
+      out[k] = mx_quant8(v, mult, A.sr != 0, bits);
+    }
+    uint4 *dst = reinterpret_cast<uint4 *>(A.codes + e0);
+    dst[0] = make_uint4(out[0].x, out[0].y, out[1].x, out[1].y);
+    dst[1] = make_uint4(out[2].x, out[2].y, out[3].x, out[3].y);
+    s_sc[(kbl >> 2) * 512 + atom_pos(i, kbl)] = (uint8_t)sc;
+  }
+  __syncthreads();
+  if (threadIdx.x < 64) {
+    const int a = threadIdx.x >> 5, part = threadIdx.x & 31;
+    const int64_t tile_col = kb0 / 4 + a;
+    if (tile_col < A.ka) {
+      const int64_t dst = ((w.rp0 >> 7) * A.ka + tile_col) * 512 + part * 16;
+      *reinterpret_cast<uint4 *>(A.scales + dst) = reinterpret_cast<const uint4 *>(s_sc + a * 512)[part];
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Transposed MXFP8 (a5 and the WGRAD operand of a6): one CTA = 128 padded
+// source rows (one window) x 128 source columns.
+//   phase 1  load the tile into shared memory (bf16 values, or NVFP4 codes +
+//            decoded block scales); optionally emit the row-wise MXFP8 output
+//   phase 2  per output row (= source column) and 32-token block: amax, E8M0
+//            scale, SR (bits drawn at the source index) or RN -> bytes
+//   phase 3  write 128-byte output rows and one 512-byte scale tile
+// ---------------------------------------------------------------------------
+struct MxTArgs {
+  // input
+  const uint16_t *x;                 // bf16 source (kNvfp4 == false)
+  const uint8_t *nv_codes;           // NVFP4 source (kNvfp4 == true)
+  const uint8_t *nv_scales;
+  const float *nv_sg;                // [batch] (batched) or [1]
+  int64_t rows, cols;                // rows per matrix (batched) or total rows
+  const int32_t *groups;             // grouped mode when non-null or `single`
+  int E;
+  int grouped;                       // 1: grouped/single-group layouts, 0: batched
+  int wpb;                           // windows per matrix (batched)
+  int sr;
+  uint64_t seed, off_t, off_row;
+  // transposed output
+  uint8_t *out_codes, *out_scales;
+  int64_t out_stride;                // P_cap (grouped)
+  int64_t out_ka;                    // scale tiles per 128 output rows
+  // row-wise output (bf16 source only; may be null)
+  uint8_t *row_codes, *row_scales;
+  int64_t row_ka;
+  int *status;
+};
+
+constexpr int kTileSmemBf16 = 128 * 256;             // 128 rows x 128 bf16, 16B-chunk swizzled
+constexpr int kTileOutStride = 144;                  // output tile row stride (bytes)
+constexpr int kCodeStrideW = 17;                     // NVFP4 code row stride (32-bit words)
+
+template <bool kNvfp4>
+__global__ void __launch_bounds__(256) mx_transpose_kernel(MxTArgs A) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ GroupSmem s_g;
+  __shared__ __align__(16) uint8_t s_tsc[512];   // transposed scale tile
+  __shared__ __align__(16) uint8_t s_rsc[512];   // row-wise scale tile
+  uint8_t *s_out = smem;                                  // [128][144]
+  uint8_t *s_in = smem + 128 * kTileOutStride;            // bf16 tile or NVFP4 codes
+  float *s_bsc = reinterpret_cast<float *>(s_in + 128 * kCodeStrideW * 4);  // NVFP4 block scales [128][9]
+
+  int E = A.E;
+  if (A.grouped) {
+    if (!setup_groups(s_g, A.groups, E, A.rows, A.status)) return;
+  }
+  const Window w = map_window(A.grouped != 0, blockIdx.y, E, s_g.off, s_g.pad, A.rows, A.wpb);
+  const int64_t col0 = (int64_t)blockIdx.x * 128;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const float sg = kNvfp4 ? A.nv_sg[A.grouped ? 0 : w.seg] : 1.0f;
+  if (tid < 128) {
+    reinterpret_cast<uint32_t *>(s_tsc)[tid] = 0u;
+    reinterpret_cast<uint32_t *>(s_rsc)[tid] = 0u;
+  }
+
+  // ---- phase 1 --------------------------------------------------------------
+  if (!kNvfp4) {
+    const bool do_row = A.row_codes != nullptr;
+#pragma unroll 1
+    for (int it = 0; it < 8; ++it) {
+      const int q = it * 256 + tid;
+      const int i = q >> 4, c8 = q & 15;
+      uint4 raw = make_uint4(0, 0, 0, 0);
+      const bool valid = i < w.nvalid;
+      const int64_t e0 = (w.src_row0 + i) * A.cols + col0 + c8 * 8;
+      if (valid) raw = ld_stream_v4(A.x + e0);
+      // 16-byte chunk c8 of row i lives at chunk c8 ^ ((i >> 2) & 7)
+      reinterpret_cast<uint4 *>(s_in + i * 256)[c8 ^ ((i >> 2) & 7)] = raw;
+      if (do_row) {  // row-wise MXFP8: a block of 32 = four neighbouring lanes
+        uint32_t m = bf16x2_absmax(bf16x2_absmax(raw.x, raw.y), bf16x2_absmax(raw.z, raw.w));
+        float fm = bf16x2_max_to_f32(m);
+        fm = fmaxf(fm, __shfl_xor_sync(0xFFFFFFFFu, fm, 1));
+        fm = fmaxf(fm, __shfl_xor_sync(0xFFFFFFFFu, fm, 2));
+        if (valid) {
+          float mult;
+          const uint32_t sc = e8m0_scale(fm, &mult);
+          float v[8];
+          unpack8(raw, v);
+          uint4 bits = make_uint4(0, 0, 0, 0);
+          if (A.sr) bits = philox_bits8((uint64_t)(e0 >> 3), A.seed, A.off_row);
+          *reinterpret_cast<uint2 *>(A.row_codes + e0) = mx_quant8(v, mult, A.sr != 0, bits);
+          if ((c8 & 3) == 0) s_rsc[atom_pos(i, c8 >> 2)] = (uint8_t)sc;
+        }
+      }
+    }
+  } else {
+    // NVFP4 codes: 128 rows x 64 bytes, 8 bytes per thread-step
+    const int64_t half_cols = A.cols >> 1;
+#pragma unroll 1
+    for (int it = 0; it < 4; ++it) {
+      const int q = it * 256 + tid;
+      const int i = q >> 3, part = q & 7;
+      uint2 raw = make_uint2(0, 0);
+      if (i < w.nvalid) raw = ld_stream_v2(A.nv_codes + (w.src_row0 + i) * half_cols + (col0 >> 1) + part * 8);
+      uint32_t *row = reinterpret_cast<uint32_t *>(s_in) + i * kCodeStrideW;
+      row[2 * part] = raw.x;
+      row[2 * part + 1] = raw.y;
+    }
+    // block scales of rows [rp0, rp0+128) x kblocks [col0/16, col0/16 + 8):
+    // two consecutive 512-byte tiles of the source scale layout
+    const int64_t ka_src = (A.cols + 63) >> 6;
+    const int64_t tile0 = (w.rp0 >> 7) * ka_src + (col0 >> 6);
+#pragma unroll 1
+    for (int t = tid; t < 128 * 8; t += 256) {
+      const int i = t >> 3, kb = t & 7;
+      float s = 0.0f;
+      if (i < w.nvalid) s = e4m3_to_f32(A.nv_scales[(tile0 + (kb >> 2)) * 512 + atom_pos(i, kb)]);
+      s_bsc[i * 9 + kb] = s;
+    }
+  }
+  __syncthreads();
+
+  // ---- phase 2 --------------------------------------------------------------
+  // warp handles groups of 8 output rows (source columns c8*8 .. c8*8+7);
+  // lane handles tokens 4*lane .. 4*lane+3; tokens 32b .. 32b+31 sit on lanes
+  // 8b .. 8b+7.
+#pragma unroll 1
+  for (int c8 = warp; c8 < 16; c8 += 8) {
+    float v[4][8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = 4 * lane + j;
+      if (!kNvfp4) {
+        const uint4 raw = reinterpret_cast<const uint4 *>(s_in + i * 256)[c8 ^ ((i >> 2) & 7)];
+        unpack8(raw, v[j]);
+      } else {
+        const uint32_t cw = reinterpret_cast<const uint32_t *>(s_in)[i * kCodeStrideW + c8];
+        const float s = s_bsc[i * 9 + (c8 >> 1)];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[j][k] = __fmul_rn(__fmul_rn(e2m1_to_f32((cw >> (4 * k)) & 0xFu), s), sg);
+      }
+    }
+    uint4 bits[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      bits[j] = make_uint4(0, 0, 0, 0);
+      const int i = 4 * lane + j;
+      if (A.sr && i < w.nvalid) {
+        const int64_t e0 = (w.src_row0 + i) * A.cols + col0 + c8 * 8;
+        bits[j] = philox_bits8((uint64_t)(e0 >> 3), A.seed, A.off_t);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int c = c8 * 8 + k;
+      float m = fmaxf(fmaxf(fabsf(v[0][k]), fabsf(v[1][k])), fmaxf(fabsf(v[2][k]), fabsf(v[3][k])));
+      m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+      m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+      m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+      float mult;
+      const uint32_t sc = e8m0_scale(m, &mult);
+      uint32_t packed = 0;
+      if (A.sr) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) packed |= sr_e4m3(__fmul_rn(v[j][k], mult), draw16(bits[j], k)) << (8 * j);
+      } else {
+        packed = cvt_e4m3x2_rn(__fmul_rn(v[0][k], mult), __fmul_rn(v[1][k], mult)) |
+                 (cvt_e4m3x2_rn(__fmul_rn(v[2][k], mult), __fmul_rn(v[3][k], mult)) << 16);
+      }
+      reinterpret_cast<uint32_t *>(s_out + c * kTileOutStride)[lane] = packed;
+      if ((lane & 7) == 0) s_tsc[atom_pos(c, lane >> 3)] = (uint8_t)sc;
+    }
+  }
+  __syncthreads();
+
+  // ---- phase 3 --------------------------------------------------------------
+  int64_t out_base, out_stride, tile_idx;
+  if (A.grouped) {
+    out_base = col0 * A.out_stride + w.rp0;
+    out_stride = A.out_stride;
+    tile_idx = (col0 >> 7) * A.out_ka + (w.rp0 >> 7);
+  } else {
+    const int b = w.seg;
+    const int64_t wb = w.rp0 / 128 - (int64_t)b * A.wpb;
+    out_base = ((int64_t)b * A.cols + col0) * A.rows + wb * 128;
+    out_stride = A.rows;
+    const int64_t cpad = (A.cols + 127) & ~127LL;
+    tile_idx = (((int64_t)b * cpad + col0) >> 7) * A.out_ka + wb;
+  }
+  if (w.nvalid > 0) {
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+      const int t = it * 256 + tid;
+      const int c = t >> 3, part = t & 7;
+      *reinterpret_cast<uint4 *>(A.out_codes + out_base + (int64_t)c * out_stride + part * 16) =
+          *reinterpret_cast<const uint4 *>(s_out + c * kTileOutStride + part * 16);
+    }
+  }
+  if (tid < 32) {
+    if (w.nvalid > 0 || A.grouped)
+      reinterpret_cast<uint4 *>(A.out_scales + tile_idx * 512)[tid] = reinterpret_cast<const uint4 *>(s_tsc)[tid];
+  } else if (tid < 64 && A.row_codes != nullptr) {  // zero tiles for padding windows too
+    reinterpret_cast<uint4 *>(A.row_scales + ((w.rp0 >> 7) * A.row_ka + (col0 >> 7)) * 512)[tid - 32] =
+        reinterpret_cast<const uint4 *>(s_rsc)[tid - 32];
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host launchers
+// ---------------------------------------------------------------------------
+static int launch_status(cudaError_t e) { return e == cudaSuccess ? NV_OK : NV_ERR_CUDA; }
+
+int launch_amax(const uint16_t *x, int64_t batch, int64_t per_batch, float *partial, int nblk, float *sg_out,
+                cudaStream_t s) {
+  amax_partial_kernel<<<dim3(nblk, (unsigned)batch), 256, 0, s>>>(x, per_batch, partial, nblk);
+  outer_scale_finalize_kernel<<<(unsigned)batch, 32, 0, s>>>(partial, nblk, sg_out);
+  return launch_status(cudaGetLastError());
+}
+
+int launch_nvfp4_quant(const uint16_t *x, int64_t batch, int64_t rows, int64_t cols, const int32_t *groups, int E,
+                       const float *sg, uint8_t *codes, uint8_t *scales, int *status, cudaStream_t s) {
+  NvQuantArgs A;
+  A.x = x; A.rows = rows; A.cols = cols; A.groups = groups; A.E = E;
+  A.wpb = (int)((rows + 127) / 128);
+  A.sg = sg; A.codes = codes; A.scales = scales; A.ka = (cols / 16 + 3) / 4; A.status = status;
+  const int64_t nwin = groups ? nvfp4moe_padded_cap(rows, E) / 128 : batch * A.wpb;
+  const int64_t nchunk = (cols / 16 + 15) / 16;
+  if (nwin == 0) return NV_OK;
+  nvfp4_quant_kernel<<<dim3((unsigned)nchunk, (unsigned)nwin), 256, 0, s>>>(A);
+  return launch_status(cudaGetLastError());
+}
+
+int launch_mxfp8_rowwise(const uint16_t *x, int64_t rows, int64_t cols, const int32_t *groups, int E, int sr,
+                         uint64_t seed, uint64_t off, uint8_t *codes, uint8_t *scales, int *status, cudaStream_t s) {
+  MxRowArgs A;
+  A.x = x; A.rows = rows; A.cols = cols; A.groups = groups; A.E = E; A.sr = sr; A.seed = seed; A.offset = off;
+  A.codes = codes; A.scales = scales; A.ka = (cols / 32 + 3) / 4; A.status = status;
+  const int64_t P = groups ? nvfp4moe_padded_cap(rows, E) : ((rows + 127) / 128) * 128;
+  const int64_t nwin = P / 128, nchunk = (cols / 32 + 7) / 8;
+  if (nwin == 0) return NV_OK;
+  mxfp8_rowwise_kernel<<<dim3((unsigned)nchunk, (unsigned)nwin), 256, 0, s>>>(A);
+  return launch_status(cudaGetLastError());
+}
+
+static size_t mx_t_smem(bool nv) {
+  return 128 * kTileOutStride + (nv ? (size_t)128 * kCodeStrideW * 4 + 128 * 9 * 4 : (size_t)kTileSmemBf16);
+}
+
+int launch_mx_transpose_bf16(const uint16_t *x, int64_t rows, int64_t cols, const int32_t *groups, int E, int sr,
+                             uint64_t seed, uint64_t off_t, uint64_t off_row, uint8_t *codes_t, uint8_t *scales_t,
+                             uint8_t *codes_row, uint8_t *scales_row, int *status, cudaStream_t s) {
+  MxTArgs A = {};
+  A.x = x; A.rows = rows; A.cols = cols; A.groups = groups; A.E = E; A.grouped = 1; A.sr = sr;
+  A.seed = seed; A.off_t = off_t; A.off_row = off_row;
+  const int64_t P = groups ? nvfp4moe_padded_cap(rows, E) : ((rows + 127) / 128) * 128;
+  A.out_codes = codes_t; A.out_scales = scales_t; A.out_stride = P; A.out_ka = P / 128;
+  A.row_codes = codes_row; A.row_scales = scales_row; A.row_ka = cols / 128;
+  A.status = status;
+  const size_t sm = mx_t_smem(false);
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaFuncSetAttribute(mx_transpose_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    attr_set = true;
+  }
+  if (P == 0) return NV_OK;
+  mx_transpose_kernel<false><<<dim3((unsigned)(cols / 128), (unsigned)(P / 128)), 256, sm, s>>>(A);
+  return launch_status(cudaGetLastError());
+}
+
+int launch_requant(const uint8_t *codes, const uint8_t *scales, const float *sg, int64_t batch, int64_t rows,
+                   int64_t cols, const int32_t *groups, int E, uint64_t seed, uint64_t off, uint8_t *out_codes,
+                   uint8_t *out_scales, int *status, cudaStream_t s) {
+  MxTArgs A = {};
+  A.nv_codes = codes; A.nv_scales = scales; A.nv_sg = sg; A.rows = rows; A.cols = cols; A.groups = groups; A.E = E;
+  A.sr = 1; A.seed = seed; A.off_t = off; A.status = status;
+  A.out_codes = out_codes; A.out_scales = out_scales;
+  int64_t nwin;
+  if (groups) {
+    const int64_t P = nvfp4moe_padded_cap(rows, E);
+    A.grouped = 1; A.out_stride = P; A.out_ka = P / 128; nwin = P / 128;
+  } else {
+    A.grouped = 0; A.wpb = (int)(rows / 128); A.out_ka = rows / 128; nwin = batch * A.wpb;
+  }
+  const size_t sm = mx_t_smem(true);
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaFuncSetAttribute(mx_transpose_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    attr_set = true;
+  }
+  if (nwin == 0) return NV_OK;
+  mx_transpose_kernel<true><<<dim3((unsigned)(cols / 128), (unsigned)nwin), 256, sm, s>>>(A);
+  return launch_status(cudaGetLastError());
+}
+
+}  // namespace nvm

@@ -1,0 +1,209 @@
+"""Device buffers and the order of library calls for the hot path.
+
+Every step runs in libnvfp4moe.so; this module only allocates device memory
+(through PyTorch) and enqueues the C-ABI calls on the current stream.
+
+SingleLinear   one quantized expert linear layer, forward and backward
+               ("End-to-End 4-Bit Training", Figure 4 of the Chinese
+               translation): NVFP4 x and w, FPROP NVFP4 GEMM, dequantize ->
+               transpose -> SR re-quantize both to MXFP8, SR-quantize the BF16
+               gradient row-wise and transposed, DGRAD and WGRAD MXFP8 GEMMs.
+MoELayer       the routed experts of one MoE layer (Figure 5: w13 GEMM, Q,
+               w2 GEMM) forward and backward on grouped rows: every step of
+               the single layer, for the gate/up (w13) and down (w2)
+               projections, with SwiGLU between them.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import nvfp4moe as N
+
+U8 = torch.uint8
+BF16 = torch.bfloat16
+F32 = torch.float32
+
+# Philox counter offsets of the stochastic roundings of one backward pass
+OFF_W13, OFF_W2, OFF_XQ, OFF_HQ, OFF_G2_ROW, OFF_G2_T, OFF_DY13_ROW, OFF_DY13_T = range(8)
+
+
+def _u8(n, dev):
+    return torch.empty(max(int(n), 16), dtype=U8, device=dev)
+
+
+class NvTensor:
+    """NVFP4 codes + block scales + outer scale(s) of a [batch][rows][cols]
+    matrix (grouped layout when E is given)."""
+
+    def __init__(self, batch, rows, cols, dev, E=None):
+        cb, sb = N.nvfp4_sizes(batch, rows, cols, E)
+        self.batch, self.rows, self.cols, self.E = batch, rows, cols, E
+        self.codes, self.scales = _u8(cb, dev), _u8(sb, dev)
+        self.sg = torch.empty(batch, dtype=F32, device=dev)
+        self.ws = _u8(N.nvfp4moe_quantize_workspace_bytes(batch, rows, cols), dev)
+
+    def quantize(self, x, groups=None, stream=None):
+        N.nvfp4_quantize(x, self.batch, self.rows, self.cols, groups, None, self.sg, self.codes, self.scales,
+                         self.ws, stream)
+
+
+class MxTransposed:
+    """MXFP8 transposed operand: [cols][P] grouped (E given) or
+    [batch][cols][rows] for weights."""
+
+    def __init__(self, rows, cols, dev, E=None, batch=1):
+        if E is not None:
+            self.P, cb, sb = N.mxfp8_t_sizes(rows, cols, E)
+        else:
+            cb, sb = N.requant_weight_sizes(batch, rows, cols)
+            self.P = None
+        self.codes, self.scales = _u8(cb, dev), _u8(sb, dev)
+
+
+class MxRows:
+    """MXFP8 row-wise operand [rows][cols], grouped scale layout."""
+
+    def __init__(self, rows, cols, dev, E=None):
+        cb, sb = N.mxfp8_row_sizes(rows, cols, E)
+        self.codes, self.scales = _u8(cb, dev), _u8(sb, dev)
+
+
+class SingleLinear:
+    """y = x_q w_q^T; dx = g w_q; dw = g^T x_q for x [T, d_in], w [d_out, d_in]."""
+
+    def __init__(self, tokens, d_in, d_out, device="cuda"):
+        dev = torch.device(device)
+        self.T, self.din, self.dout = tokens, d_in, d_out
+        self.groups = torch.tensor([0, tokens], dtype=torch.int32, device=dev)
+        self.xq = NvTensor(1, tokens, d_in, dev, E=1)
+        self.wq = NvTensor(1, d_out, d_in, dev)
+        self.y = torch.empty((tokens, d_out), dtype=F32, device=dev)
+        self.xt = MxTransposed(tokens, d_in, dev, E=1)
+        self.wt = MxTransposed(d_out, d_in, dev)
+        self.g_row = MxRows(tokens, d_out, dev, E=1)
+        self.gt = MxTransposed(tokens, d_out, dev, E=1)
+        self.dx = torch.empty((tokens, d_in), dtype=F32, device=dev)
+        self.dw = torch.empty((d_out, d_in), dtype=F32, device=dev)
+
+    def enqueue(self, x, w, g, seed=0, stream=None):
+        T, din, dout, go = self.T, self.din, self.dout, self.groups
+        self.xq.quantize(x, go, stream)
+        self.wq.quantize(w, None, stream)
+        N.grouped_gemm_nvfp4_fwd(None, self.xq.sg, self.xq.codes, self.xq.scales, self.wq.codes, self.wq.scales,
+                                 self.wq.sg, go, 1, T, dout, din, self.y, N.NV_OUT_FP32, None, stream)
+        N.dequant_transpose_requant_sr(self.wq.codes, self.wq.scales, self.wq.sg, 1, dout, din, None, seed, 0,
+                                       self.wt.codes, self.wt.scales, stream)
+        N.dequant_transpose_requant_sr(self.xq.codes, self.xq.scales, self.xq.sg, 1, T, din, go, seed, 1,
+                                       self.xt.codes, self.xt.scales, stream)
+        N.mxfp8_quantize(g, T, dout, go, N.NV_SR, seed, 2, 3, self.g_row.codes, self.g_row.scales,
+                         self.gt.codes, self.gt.scales, stream)
+        N.grouped_gemm_mxfp8_dx(self.g_row.codes, self.g_row.scales, self.wt.codes, self.wt.scales, go, 1, T, dout,
+                                din, self.dx, N.NV_OUT_FP32, None, stream)
+        N.grouped_gemm_mxfp8_dw(self.gt.codes, self.gt.scales, self.xt.codes, self.xt.scales, go, 1, T, dout, din,
+                                self.dw, None, stream)
+
+    def run(self, x, w, g, seed=0):
+        """Enqueue the layer and return its outputs on the host (numpy)."""
+        self.enqueue(x, w, g, seed)
+        torch.cuda.synchronize()
+        T, din, dout = self.T, self.din, self.dout
+        P = self.xt.P
+        return {
+            "x_sg": self.xq.sg.cpu().numpy()[0], "w_sg": self.wq.sg.cpu().numpy()[0],
+            "x_codes": self.xq.codes[: T * din // 2].cpu().numpy().reshape(T, din // 2),
+            "w_codes": self.wq.codes[: dout * din // 2].cpu().numpy().reshape(dout, din // 2),
+            "y": self.y.cpu().numpy(),
+            "wt_codes": self.wt.codes[: din * dout].cpu().numpy(),
+            "g_codes": self.g_row.codes[: T * dout].cpu().numpy(),
+            "P": P,
+            "gt_codes": self.gt.codes[: dout * P].cpu().numpy(), "gt_scales": self.gt.scales.cpu().numpy(),
+            "xt_codes": self.xt.codes[: din * P].cpu().numpy(), "xt_scales": self.xt.scales.cpu().numpy(),
+            "dx": self.dx.cpu().numpy(), "dw": self.dw.cpu().numpy(),
+        }
+
+
+class MoELayer:
+    """Routed experts of one MoE layer: rows grouped by expert (group_offsets),
+    w13 [E][2I][d] (gate rows then up rows), w2 [E][d][I]."""
+
+    def __init__(self, M, d_model, d_ff, E, device="cuda"):
+        dev = torch.device(device)
+        self.M, self.d, self.I, self.E = M, d_model, d_ff, E
+        I2 = 2 * d_ff
+        # forward
+        self.xq = NvTensor(1, M, d_model, dev, E=E)
+        self.w13q = NvTensor(E, I2, d_model, dev)
+        self.w2q = NvTensor(E, d_model, d_ff, dev)
+        self.y13 = torch.empty((M, I2), dtype=BF16, device=dev)
+        self.h = torch.empty((M, d_ff), dtype=BF16, device=dev)
+        self.hq = NvTensor(1, M, d_ff, dev, E=E)
+        self.y2 = torch.empty((M, d_model), dtype=BF16, device=dev)
+        # backward
+        self.xt = MxTransposed(M, d_model, dev, E=E)
+        self.ht = MxTransposed(M, d_ff, dev, E=E)
+        self.w13t = MxTransposed(I2, d_model, dev, batch=E)
+        self.w2t = MxTransposed(d_model, d_ff, dev, batch=E)
+        self.g2_row = MxRows(M, d_model, dev, E=E)
+        self.g2t = MxTransposed(M, d_model, dev, E=E)
+        self.dh = torch.empty((M, d_ff), dtype=BF16, device=dev)
+        self.dy13 = torch.empty((M, I2), dtype=BF16, device=dev)
+        self.dy13_row = MxRows(M, I2, dev, E=E)
+        self.dy13t = MxTransposed(M, I2, dev, E=E)
+        self.dx = torch.empty((M, d_model), dtype=BF16, device=dev)
+        self.dw2 = torch.empty((E, d_model, d_ff), dtype=F32, device=dev)
+        self.dw13 = torch.empty((E, I2, d_model), dtype=F32, device=dev)
+
+    # GEMM FLOPs of one forward (2 GEMMs) and one backward (4 GEMMs)
+    def flops(self):
+        fwd = 2 * self.M * (2 * self.I) * self.d + 2 * self.M * self.d * self.I
+        return fwd, 2 * fwd
+
+    def forward(self, x, w13, w2, groups, stream=None):
+        M, d, I, E = self.M, self.d, self.I, self.E
+        self.w13q.quantize(w13, None, stream)
+        self.w2q.quantize(w2, None, stream)
+        self.xq.quantize(x, groups, stream)
+        N.grouped_gemm_nvfp4_fwd(None, self.xq.sg, self.xq.codes, self.xq.scales, self.w13q.codes,
+                                 self.w13q.scales, self.w13q.sg, groups, E, M, 2 * I, d, self.y13, N.NV_OUT_BF16,
+                                 None, stream)
+        N.nvfp4moe_swiglu_fwd(self.y13, M, I, self.h, stream)
+        self.hq.quantize(self.h, groups, stream)
+        N.grouped_gemm_nvfp4_fwd(None, self.hq.sg, self.hq.codes, self.hq.scales, self.w2q.codes, self.w2q.scales,
+                                 self.w2q.sg, groups, E, M, d, I, self.y2, N.NV_OUT_BF16, None, stream)
+
+    def backward(self, g2, groups, seed=3, stream=None):
+        M, d, I, E = self.M, self.d, self.I, self.E
+        I2 = 2 * I
+        # re-quantize the saved forward tensors (dequantize -> transpose -> SR to MXFP8)
+        N.dequant_transpose_requant_sr(self.w13q.codes, self.w13q.scales, self.w13q.sg, E, I2, d, None, seed,
+                                       OFF_W13, self.w13t.codes, self.w13t.scales, stream)
+        N.dequant_transpose_requant_sr(self.w2q.codes, self.w2q.scales, self.w2q.sg, E, d, I, None, seed, OFF_W2,
+                                       self.w2t.codes, self.w2t.scales, stream)
+        N.dequant_transpose_requant_sr(self.xq.codes, self.xq.scales, self.xq.sg, 1, M, d, groups, seed, OFF_XQ,
+                                       self.xt.codes, self.xt.scales, stream)
+        N.dequant_transpose_requant_sr(self.hq.codes, self.hq.scales, self.hq.sg, 1, M, I, groups, seed, OFF_HQ,
+                                       self.ht.codes, self.ht.scales, stream)
+        # down projection: dh = g2 w2, dW2 = g2^T h_q
+        N.mxfp8_quantize(g2, M, d, groups, N.NV_SR, seed, OFF_G2_ROW, OFF_G2_T, self.g2_row.codes,
+                         self.g2_row.scales, self.g2t.codes, self.g2t.scales, stream)
+        N.grouped_gemm_mxfp8_dx(self.g2_row.codes, self.g2_row.scales, self.w2t.codes, self.w2t.scales, groups, E,
+                                M, d, I, self.dh, N.NV_OUT_BF16, None, stream)
+        N.grouped_gemm_mxfp8_dw(self.g2t.codes, self.g2t.scales, self.ht.codes, self.ht.scales, groups, E, M, d, I,
+                                self.dw2, None, stream)
+        # SwiGLU backward, then gate/up: dx = dy13 w13, dW13 = dy13^T x_q
+        N.nvfp4moe_swiglu_bwd(self.dh, self.y13, M, I, self.dy13, stream)
+        N.mxfp8_quantize(self.dy13, M, I2, groups, N.NV_SR, seed, OFF_DY13_ROW, OFF_DY13_T, self.dy13_row.codes,
+                         self.dy13_row.scales, self.dy13t.codes, self.dy13t.scales, stream)
+        N.grouped_gemm_mxfp8_dx(self.dy13_row.codes, self.dy13_row.scales, self.w13t.codes, self.w13t.scales,
+                                groups, E, M, I2, d, self.dx, N.NV_OUT_BF16, None, stream)
+        N.grouped_gemm_mxfp8_dw(self.dy13t.codes, self.dy13t.scales, self.xt.codes, self.xt.scales, groups, E, M,
+                                I2, d, self.dw13, None, stream)
+
+    def step(self, x, w13, w2, g2, groups, seed=3, stream=None):
+        self.forward(x, w13, w2, groups, stream)
+        self.backward(g2, groups, seed, stream)
+
+    # kernels one step launches: forward = 4 NVFP4 quantizations x 3 kernels
+    # (amax, finalize, quantize) + 2 GEMMs + SwiGLU; backward = 4 requants +
+    # 2 MXFP8 quantizations + 4 GEMMs + SwiGLU backward
+    LAUNCHES_PER_STEP = (4 * 3 + 2 + 1) + (4 + 2 + 4 + 1)
