@@ -219,7 +219,8 @@ def kernel_units(layer, m):
     fl13 = 2.0 * M * 2 * I * d
     fl2 = 2.0 * M * d * I
     return {
-        "nvfp4_quantize": [(E * 2 * I * d, 2.5625), (E * d * I, 2.5625), (M * d, 2.5625), (M * I, 2.5625)],
+        # a call = the amax pass (2 B/elem) + the quantize pass (2 + 0.5 + 1/16 B/elem)
+        "nvfp4_quantize": [(E * 2 * I * d, 4.5625), (E * d * I, 4.5625), (M * d, 4.5625), (M * I, 4.5625)],
         "grouped_gemm_nvfp4_fwd": [fl13, fl2],
         "dequant_transpose_requant_sr": [(E * 2 * I * d, 1.59375), (E * d * I, 1.59375), (M * d, 1.59375),
                                          (M * I, 1.59375)],
@@ -369,10 +370,11 @@ def roofline_of(name, times, units, steps, peaks):
 # ---------------------------------------------------------------------------
 # the oracle: cpu_baseline and the reference arm
 # ---------------------------------------------------------------------------
-def oracle_sample_step(tokens: int, seed: int = 2):
+def oracle_sample_step(tokens: int, seed: int = 2, d_ff: int | None = None):
     """One expert (of the workload's 64) with `tokens` routed rows, full
-    d_model / d_ff, through every step of the path in the oracle.  Returns
-    the sample's GEMM FLOPs."""
+    d_model and the first `d_ff` hidden features (all of them by default),
+    through every step of the path in the oracle.  Returns the sample's GEMM
+    FLOPs."""
     import torch
     from oracle import gemm as G
     from oracle import layout as L
@@ -380,7 +382,7 @@ def oracle_sample_step(tokens: int, seed: int = 2):
     from oracle import nvfp4 as NV
     from oracle import requant as RQ
     from oracle import swiglu as SW
-    d, I = SHAPE["d_model"], SHAPE["d_ff"]
+    d, I = SHAPE["d_model"], d_ff or SHAPE["d_ff"]
     gen = torch.Generator().manual_seed(seed)
     x = (torch.randn((tokens, d), generator=gen)).to(torch.bfloat16).float().numpy()
     w13 = (torch.randn((2 * I, d), generator=gen) * 0.02).to(torch.bfloat16).float().numpy()
@@ -425,20 +427,22 @@ def run_reference(args):
     if rank != 0:
         return
     for _ in range(args.warmup):
-        oracle_sample_step(args.ref_tokens)
+        oracle_sample_step(args.ref_tokens, d_ff=args.ref_dff)
     t0 = time.perf_counter()
     flops = 0.0
     for _ in range(args.steps):
-        flops += oracle_sample_step(args.ref_tokens)
+        flops += oracle_sample_step(args.ref_tokens, d_ff=args.ref_dff)
     dt = time.perf_counter() - t0
     v = flops / dt / 1e12
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 oracle",
-        "data": "synthetic", "config": {"workload": WORKLOAD, "sample_rows_per_step": args.ref_tokens},
+        "data": "synthetic", "config": {"workload": WORKLOAD, "sample_rows_per_step": args.ref_tokens,
+                                        "sample_d_ff": args.ref_dff},
         "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
-                         "sample": f"one expert, {args.ref_tokens} rows per step, full d_model/d_ff"},
+                         "sample": f"one expert, {args.ref_tokens} rows and a {args.ref_dff}-wide slice of "
+                                   f"d_ff per step, full d_model, every step of the path"},
         "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
 
@@ -451,6 +455,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-tokens", type=int, default=256)
     ap.add_argument("--ref-tokens", type=int, default=64)
+    ap.add_argument("--ref-dff", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
