@@ -11,7 +11,8 @@
  * General rules (every entry point):
  *  - Pointers are DEVICE pointers unless a parameter says otherwise.  The
  *    caller owns and allocates every buffer, including workspaces; the library
- *    never allocates, frees or retains device memory.
+ *    never allocates or frees device memory.  Its only device memory of its
+ *    own is the status word and the fixed scratch of nvfp4_quantize_noalloc.
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy default
  *    stream) and is asynchronous.  The return value reports argument checks
  *    and launch errors only (NV_OK or a negative NV_ERR_*).  Errors the GPU
@@ -132,6 +133,32 @@ int nvfp4_quantize(const void *x, int64_t batch, int64_t rows, int64_t cols,
                    const float *outer_scale_in, float *outer_scale_out,
                    uint8_t *codes, uint8_t *scales,
                    void *workspace, size_t workspace_bytes, nv_stream_t stream);
+
+/* ---- nvfp4_quantize for callers that cannot allocate device memory -------------
+ * The pages have no counterpart to this entry point; it is a convenience of
+ * this library.  nvfp4_quantize needs a caller-provided workspace when it
+ * computes the outer scales.  Callers that cannot allocate device memory (code
+ * running inside a host runtime that owns every allocation, or that must not
+ * allocate once it is running) use this variant, which takes the same
+ * arguments minus the workspace and uses a fixed 512 KiB scratch array in the
+ * library's own device memory instead.  Every GPU that loads the library
+ * holds that array until the process exits.
+ *  - Limit: with outer_scale_in == NULL the call needs
+ *    nvfp4moe_quantize_workspace_bytes(batch, rows, cols) <= 524288, else it
+ *    returns NV_ERR_WORKSPACE and enqueues nothing.  With outer_scale_in set
+ *    no scratch is used and there is no limit.
+ *  - The first call on a device looks up the scratch's device address (with
+ *    that device current); make that first call before any stream capture.
+ *  - Every call shares the one array and it keeps the last call's contents;
+ *    nothing in it needs clearing (each call writes every slot it reads), but
+ *    calls that overlap on the GPU (different streams, or another thread)
+ *    race on it: serialize them.
+ *  - It calls no cudaMalloc, cudaFree or allocating library routine.
+ */
+int nvfp4_quantize_noalloc(const void *x, int64_t batch, int64_t rows, int64_t cols,
+                           const int32_t *group_offsets, int32_t num_groups,
+                           const float *outer_scale_in, float *outer_scale_out,
+                           uint8_t *codes, uint8_t *scales, nv_stream_t stream);
 
 /* ---- a6 (and the MXFP8 RN sweep): MXFP8 quantization of a bf16 matrix --------
  * Chinese translation of the pages, Figure 4: the BF16 gradient is quantized

@@ -37,6 +37,7 @@ _SIGS = {
     "nvfp4moe_scale_offset": (_I64, [_I64, _I64, _I64]),
     "nvfp4moe_quantize_workspace_bytes": (_SZ, [_I64, _I64, _I64]),
     "nvfp4_quantize": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _I32, _P, _P, _P, _P, _P, _SZ, _P]),
+    "nvfp4_quantize_noalloc": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _I32, _P, _P, _P, _P, _P]),
     "mxfp8_quantize": (ctypes.c_int, [_P, _I64, _I64, _P, _I32, ctypes.c_int, _U64, _U64, _U64,
                                       _P, _P, _P, _P, _P]),
     "dequant_transpose_requant_sr": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _I64, _P, _I32, _U64, _U64,
@@ -147,6 +148,15 @@ def nvfp4_quantize(x, batch, rows, cols, group_offsets, outer_scale_in, outer_sc
     return _check("nvfp4_quantize", lib().nvfp4_quantize(
         _ptr(x), batch, rows, cols, _ptr(group_offsets), _ng(group_offsets), _ptr(outer_scale_in),
         _ptr(outer_scale_out), _ptr(codes), _ptr(scales), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def nvfp4_quantize_noalloc(x, batch, rows, cols, group_offsets, outer_scale_in, outer_scale_out, codes, scales,
+                           stream=None):
+    """nvfp4_quantize without a workspace argument, for callers that cannot
+    allocate device memory: the library uses its own fixed scratch."""
+    return _check("nvfp4_quantize_noalloc", lib().nvfp4_quantize_noalloc(
+        _ptr(x), batch, rows, cols, _ptr(group_offsets), _ng(group_offsets), _ptr(outer_scale_in),
+        _ptr(outer_scale_out), _ptr(codes), _ptr(scales), _stream(stream)))
 
 
 def mxfp8_quantize(x, rows, cols, group_offsets, mode, seed, counter_offset_row, counter_offset_t,
