@@ -120,7 +120,7 @@ class ClockSampler:
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -447,21 +447,141 @@ def run_reference(args):
     }))
 
 
+def run_quant_sweep(args):
+    """The quantization-only workload: bf16 [8192 x 8192] and [16384 x 7168],
+    Student-t(3) x 0.05 with 0.01% of elements x1000.  Ops: NVFP4 1x16 RN
+    quantize (with its amax pass), MXFP8 1x32 RN quantize along rows, and
+    dequant -> transpose -> SR requant of the NVFP4 result.  One JSON line per
+    (shape, op) with achieved GB/s of algorithmic bytes."""
+    import torch
+    from precision_moe_numerics_nvfp4_gb300 import nvfp4moe as N
+    from precision_moe_numerics_nvfp4_gb300 import workloads as W
+    from precision_moe_numerics_nvfp4_gb300.pipeline import MxRows, MxTransposed, NvTensor
+
+    N.lib()
+    peaks = load_peaks()
+    shapes = W.QUANT_SWEEP_SHAPES if args.sweep_shape is None else [tuple(int(v) for v in args.sweep_shape.split("x"))]
+    for shape in shapes:
+        R, C = shape
+        x = W.quant_sweep(shape, "cuda")
+        nv = NvTensor(1, R, C, torch.device("cuda"))
+        mr = MxRows(R, C, torch.device("cuda"))
+        mt = MxTransposed(R, C, torch.device("cuda"), batch=1)
+        mt2 = MxTransposed(R, C, torch.device("cuda"), E=1)
+        ops = {
+            "nvfp4_quantize": (lambda: nv.quantize(x), 4.5625),
+            "mxfp8_quantize_rn": (lambda: N.mxfp8_quantize(x, R, C, None, N.NV_RN, 0, 0, 0, mr.codes, mr.scales,
+                                                           None, None), 3.03125),
+            "dequant_transpose_requant_sr": (lambda: N.dequant_transpose_requant_sr(
+                nv.codes, nv.scales, nv.sg, 1, R, C, None, 1, 0, mt.codes, mt.scales), 1.59375),
+            # not an op of the sweep: the gradient's SR quantization (row-wise + transposed) on the same tensor
+            "mxfp8_quantize_sr_dual": (lambda: N.mxfp8_quantize(x, R, C, None, N.NV_SR, 0, 0, 1, mr.codes, mr.scales,
+                                                                mt2.codes, mt2.scales), 4.0625),
+        }
+        nv.quantize(x)
+        torch.cuda.synchronize()
+        for name, (fn, bpe) in ops.items():
+            if args.sweep_op and args.sweep_op != name:
+                continue
+            for _ in range(args.warmup):
+                fn()
+            torch.cuda.synchronize()
+            s = torch.cuda.current_stream()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            for _ in range(args.steps):
+                fn()
+            e1.record(s)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / args.steps
+            gbs = R * C * bpe / (ms / 1e3) / 1e9
+            print(json.dumps({"workload": "quant_sweep", "shape": [R, C], "op": name, "ms": ms, "GB_s": gbs,
+                              "frac_hbm": gbs / peaks["hbm_gbs"], "bytes_per_elem": bpe,
+                              "peak_source": peaks["source"]}))
+        assert N.nvfp4moe_get_device_status() == 0
+        del x, nv, mr, mt, mt2
+        torch.cuda.empty_cache()
+
+
+def run_gemm(args):
+    """One grouped GEMM of the MoE layer at a reduced token count (for
+    profiling): fwd = x_q w13^T (N 3072, K 4096), dx = dy13 w13 (N 3072,
+    K 4096), dw = dy13^T x_q.  Prints achieved TFLOP/s."""
+    import torch
+    from precision_moe_numerics_nvfp4_gb300 import nvfp4moe as N
+    from precision_moe_numerics_nvfp4_gb300 import workloads as W
+    from precision_moe_numerics_nvfp4_gb300.pipeline import MxRows, MxTransposed, NvTensor
+
+    N.lib()
+    dev = torch.device("cuda")
+    m = W.moe("cuda", seed=2, tokens=args.gemm_tokens)
+    M, d, I2, E = m.x_perm.shape[0], SHAPE["d_model"], 2 * SHAPE["d_ff"], SHAPE["experts"]
+    go = m.group_offsets
+    sizes = torch.diff(go.to(torch.int64))
+    flops = float(2 * M * I2 * d)
+    xq, wq = NvTensor(1, M, d, dev, E=E), NvTensor(E, I2, d, dev)
+    xq.quantize(m.x_perm, go)
+    wq.quantize(m.w13)
+    if args.gemm_kind == "fwd":
+        y = torch.empty((M, I2), dtype=torch.bfloat16, device=dev)
+        fn = lambda: N.grouped_gemm_nvfp4_fwd(None, xq.sg, xq.codes, xq.scales, wq.codes, wq.scales, wq.sg, go, E, M,
+                                              I2, d, y, N.NV_OUT_BF16)
+    else:
+        g = (torch.randn((M, I2), device=dev) * 1e-3).to(torch.bfloat16)
+        gr, gt = MxRows(M, I2, dev, E=E), MxTransposed(M, I2, dev, E=E)
+        N.mxfp8_quantize(g, M, I2, go, N.NV_SR, 3, 6, 7, gr.codes, gr.scales, gt.codes, gt.scales)
+        if args.gemm_kind == "dx":
+            wt = MxTransposed(I2, d, dev, batch=E)
+            N.dequant_transpose_requant_sr(wq.codes, wq.scales, wq.sg, E, I2, d, None, 3, 0, wt.codes, wt.scales)
+            dx = torch.empty((M, d), dtype=torch.bfloat16, device=dev)
+            fn = lambda: N.grouped_gemm_mxfp8_dx(gr.codes, gr.scales, wt.codes, wt.scales, go, E, M, I2, d, dx,
+                                                 N.NV_OUT_BF16)
+        else:
+            xt = MxTransposed(M, d, dev, E=E)
+            N.dequant_transpose_requant_sr(xq.codes, xq.scales, xq.sg, 1, M, d, go, 3, 2, xt.codes, xt.scales)
+            dw = torch.empty((E, I2, d), dtype=torch.float32, device=dev)
+            fn = lambda: N.grouped_gemm_mxfp8_dw(gt.codes, gt.scales, xt.codes, xt.scales, go, E, M, I2, d, dw)
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(args.steps):
+        fn()
+    e1.record(s)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    assert N.nvfp4moe_get_device_status() == 0
+    print(json.dumps({"workload": "gemm", "kind": args.gemm_kind, "rows": M, "experts": E,
+                      "min_group": int(sizes.min()), "max_group": int(sizes.max()), "ms": ms,
+                      "TFLOP_s": flops / (ms / 1e3) / 1e12}))
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-tokens", type=int, default=256)
     ap.add_argument("--ref-tokens", type=int, default=64)
     ap.add_argument("--ref-dff", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=["moe", "quant_sweep", "gemm"], default="moe")
+    ap.add_argument("--gemm-kind", choices=["fwd", "dx", "dw"], default="fwd")
+    ap.add_argument("--gemm-tokens", type=int, default=16384)
+    ap.add_argument("--sweep-op", default=None)
+    ap.add_argument("--sweep-shape", default=None, help="RxC, e.g. 8192x8192")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "quant_sweep":
+        run_quant_sweep(args)
+    elif args.workload == "gemm":
+        run_gemm(args)
     else:
         run_ours(args)
 

@@ -62,8 +62,8 @@
  * every 128-row tile of an expert owns its scale atoms.  Grouped buffers are
  * sized for P_cap = nvfp4moe_padded_cap(M_total, E) rows.
  *
- * group_offsets: int32 [E + 1] on the device, o[0] = 0, non-decreasing,
- * o[E] = M_total.  Empty groups are allowed.  Kernels that read them record
+ * group_offsets: int32 [E + 1] on the device, 1 <= E <= 512, o[0] = 0,
+ * non-decreasing, o[E] = M_total.  Empty groups are allowed.  Kernels that read them record
  * NV_ERR_OFFSETS in the status word (and write nothing) when they are
  * inconsistent.
  */

@@ -14,7 +14,7 @@
 
 namespace nvm {
 
-constexpr int kMaxGroups = 1024;  // experts per grouped call (smem tables)
+constexpr int kMaxGroups = 512;  // experts per grouped call (smem tables)
 
 // ---------------------------------------------------------------------------
 // status word

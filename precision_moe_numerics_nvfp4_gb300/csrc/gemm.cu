@@ -9,20 +9,29 @@
 // sums them and scales the sum by both block scales; "Kernels for
 // low-precision training": the MoE layer is dominated by these GEMMs.
 //
-// One CTA computes one 128 x BN output tile with all of K:
-//   warp 0      TMA producer: A/B tiles (128-byte swizzle) and the scale tiles
-//               (1-D bulk copies of whole 512-byte 128x4 scale tiles) into a
-//               STAGES-deep shared-memory ring, one mbarrier per stage
-//   warp 1      allocates tensor memory; one thread copies the stage's scales
-//               to tensor memory (tcgen05.cp) and issues 4 block-scaled MMAs
-//               per stage into a 128 x BN fp32 accumulator in tensor memory;
-//               tcgen05.commit frees the stage
-//   warps 2-5   epilogue: tcgen05.ld of the accumulator, outer-scale multiply,
-//               bf16/fp32 stores of the rows that belong to the expert
-// Every wait is bounded: a wait that runs out records NV_ERR_TIMEOUT, stops
-// issuing, waits (bounded) for its own copies, frees tensor memory and returns.
+// Persistent kernel looping over 128 x 128 output tiles in a static
+// round-robin order.  Default: two CTAs per SM, each with a 3-stage ring and
+// one accumulator, so one CTA's epilogue and barrier waits are covered by the
+// other CTA's MMAs (measured faster than one CTA per SM with a 6-stage ring
+// and two accumulators, which NVFP4MOE_GEMM_VARIANT=1 selects).  Roles:
+//   warp 0      TMA producer: A/B tiles (128-byte swizzle) and whole 512-byte
+//               128x4 scale tiles (1-D bulk copies) into a STAGES-deep ring,
+//               continuously across tiles
+//   warp 1      allocates tensor memory; one thread copies each stage's scales
+//               to tensor memory (tcgen05.cp, one buffer per ring stage) and
+//               issues 4 block-scaled MMAs per stage into the fp32
+//               accumulator (or alternates two, variant 1)
+//   warps 2-5   epilogue: tcgen05.ld of the finished accumulator, outer-scale
+//               multiply, bf16/fp32 stores of the rows that belong to the
+//               expert, then release of the accumulator
+// Every wait is bounded: a wait that runs out records NV_ERR_TIMEOUT and
+// raises a CTA-wide abort flag so that the other roles stop too; the producer
+// waits (bounded) for its own copies and tensor memory is always freed.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+
+#include <cstdlib>
+#include <cstring>
 
 #include "common.cuh"
 #include "launch.h"
@@ -110,24 +119,29 @@ constexpr int cpow2(int x) {
   return p;
 }
 
-template <int KIND, int BN, int STAGES>
+constexpr int kBN = 128;  // output tile columns (and rows: 128)
+
+template <int KIND, int STAGES, int NACC>
 struct Cfg {
   static constexpr bool kFp4 = KIND == kGemmNvfp4Fwd;
   static constexpr int kAtomsPerStage = kFp4 ? 4 : 1;  // 128x4 scale tiles per 128 rows per stage
   static constexpr int A_BYTES = 128 * 128;
-  static constexpr int B_BYTES = BN * 128;
+  static constexpr int B_BYTES = kBN * 128;
   static constexpr int SFA_BYTES = kAtomsPerStage * 512;
-  static constexpr int SFB_BYTES = (BN / 128) * SFA_BYTES;
+  static constexpr int SFB_BYTES = (kBN / 128) * SFA_BYTES;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
-  static constexpr int SFA_COLS = kAtomsPerStage * 4;         // tensor-memory columns per stage
-  static constexpr int SFB_COLS = kAtomsPerStage * (BN / 32);
+  static constexpr int SFA_COLS = kAtomsPerStage * 4;  // tensor-memory columns per stage
+  static constexpr int SFB_COLS = kAtomsPerStage * (kBN / 32);
   static constexpr int SF_COLS = SFA_COLS + SFB_COLS;
-  static constexpr int TMEM_COLS = cpow2(BN + 2 * SF_COLS);
-  static constexpr int BAR_BYTES = (2 * STAGES + 1) * 8 + 16;
+  static constexpr int ACC_COLS = NACC * kBN;           // one or two accumulators
+  // one scale buffer per ring stage: a stage's buffer is rewritten only after
+  // the producer has refilled that stage, i.e. after its previous MMAs retired
+  static constexpr int TMEM_COLS = cpow2(ACC_COLS + STAGES * SF_COLS);
+  static constexpr int NBARS = 2 * STAGES + 2 * NACC;   // full, empty, acc_full[], acc_empty[]
   static constexpr uint32_t IDESC =
-      (kFp4 ? ((1u << 7) | (1u << 10)) : (1u << 23)) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+      (kFp4 ? ((1u << 7) | (1u << 10)) : (1u << 23)) | ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
   static size_t smem_bytes(int E) {
-    return 1024 + (size_t)STAGES * STAGE_BYTES + BAR_BYTES + (size_t)(E + 1) * 8 + 64;
+    return 1024 + (size_t)STAGES * STAGE_BYTES + NBARS * 8 + 32 + (size_t)(E + 1) * 8 + 64;
   }
   static_assert(TMEM_COLS <= 512, "tensor memory");
 };
@@ -154,13 +168,70 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return d;
 }
 
+// A bounded mbarrier wait that also gives up when another role of the CTA
+// has raised the abort flag.  A wait that runs out raises the flag and records
+// NV_ERR_TIMEOUT.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uint64_t limit, volatile int *abort,
+                                              int *status) {
+  for (uint64_t i = 0; i < limit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255) == 255 && *abort) return false;
+  }
+  *abort = 1;
+  record_error(status, NV_ERR_TIMEOUT);
+  return false;
+}
+
+// One output tile of the schedule.
+struct Tile {
+  int e, nk, a_row, b_row, mrows, k_off;
+  int64_t a_tile, b_tile, k_atom0, out_row0, out_col0;
+};
+
+template <int KIND>
+__device__ __forceinline__ Tile decode_tile(int t, const GemmArgs &A, const int *s_off, const int *s_pad) {
+  Tile T;
+  if (KIND != kGemmMxfp8Dw) {
+    const int pm = t / A.ntn, nt = t - (t / A.ntn) * A.ntn;
+    const int p0 = pm * 128;
+    const int e = find_group(s_pad, A.E, p0);
+    T.e = e;
+    T.a_row = s_off[e] + (p0 - s_pad[e]);
+    T.mrows = min(128, s_off[e + 1] - T.a_row);
+    T.b_row = e * (int)(KIND == kGemmNvfp4Fwd ? A.N : A.K) + nt * kBN;
+    T.a_tile = pm;
+    T.b_tile = T.b_row / 128;
+    T.nk = (int)(KIND == kGemmNvfp4Fwd ? A.K / 256 : A.N / 128);
+    T.k_off = 0;
+    T.k_atom0 = 0;
+    T.out_row0 = T.a_row;
+    T.out_col0 = (int64_t)nt * kBN;
+  } else {
+    const int per_e = A.ntm * A.ntn;
+    const int e = t / per_e;
+    const int r = t - e * per_e, mt = r / A.ntn, nt = r - (r / A.ntn) * A.ntn;
+    T.e = e;
+    T.a_row = mt * 128;
+    T.b_row = nt * kBN;
+    T.mrows = 128;
+    T.nk = (s_pad[e + 1] - s_pad[e]) / 128;
+    T.k_off = s_pad[e];
+    T.a_tile = mt;
+    T.b_tile = T.b_row / 128;
+    T.k_atom0 = s_pad[e] / 128;
+    T.out_row0 = (int64_t)e * A.N + (int64_t)mt * 128;
+    T.out_col0 = (int64_t)nt * kBN;
+  }
+  return T;
+}
+
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <int KIND, int BN, int STAGES>
+template <int KIND, int STAGES, int NACC>
 __global__ void __launch_bounds__(192, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmArgs A) {
-  using C = Cfg<KIND, BN, STAGES>;
+  using C = Cfg<KIND, STAGES, NACC>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint8_t *sA = smem;
@@ -168,55 +239,29 @@ __global__ void __launch_bounds__(192, 1)
   uint8_t *sSFA = sB + STAGES * C::B_BYTES;
   uint8_t *sSFB = sSFA + STAGES * C::SFA_BYTES;
   uint64_t *bars = reinterpret_cast<uint64_t *>(sSFB + STAGES * C::SFB_BYTES);
-  uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 1);
+  uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + C::NBARS);
+  volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
   int *s_flag = reinterpret_cast<int *>(s_tmem + 2);
   int *s_off = s_flag + 2;
   int *s_pad = s_off + (A.E + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (!load_groups(A.groups, A.E, A.M_total, s_off, s_pad, s_flag, A.status)) return;
+  const int num_tiles =
+      KIND == kGemmMxfp8Dw ? A.E * A.ntm * A.ntn : (s_pad[A.E] / 128) * A.ntn;
+  if ((int)blockIdx.x >= num_tiles) return;  // uniform over the CTA
 
-  // ---- which tile -----------------------------------------------------------
-  int e, nk, a_row, b_row, mrows, k_off;
-  int64_t a_tile, b_tile, k_atom0, out_row0, out_col0;
-  if (KIND != kGemmMxfp8Dw) {
-    const int pm = blockIdx.x / A.ntn, nt = blockIdx.x - (blockIdx.x / A.ntn) * A.ntn;
-    const int p0 = pm * 128;
-    if (p0 >= s_pad[A.E]) return;  // past the last group (uniform over the CTA)
-    e = find_group(s_pad, A.E, p0);
-    a_row = s_off[e] + (p0 - s_pad[e]);
-    mrows = min(128, s_off[e + 1] - a_row);
-    b_row = e * (int)(KIND == kGemmNvfp4Fwd ? A.N : A.K) + nt * BN;
-    a_tile = pm;
-    b_tile = b_row / 128;
-    nk = (int)(KIND == kGemmNvfp4Fwd ? A.K / 256 : A.N / 128);
-    k_off = 0;
-    k_atom0 = 0;
-    out_row0 = a_row;
-    out_col0 = (int64_t)nt * BN;
-  } else {
-    const int per_e = A.ntm * A.ntn;
-    e = blockIdx.x / per_e;
-    const int r = blockIdx.x - e * per_e, mt = r / A.ntn, nt = r - (r / A.ntn) * A.ntn;
-    a_row = mt * 128;
-    b_row = nt * BN;
-    mrows = 128;
-    nk = (s_pad[e + 1] - s_pad[e]) / 128;
-    k_off = s_pad[e];
-    a_tile = mt;
-    b_tile = b_row / 128;
-    k_atom0 = s_pad[e] / 128;
-    out_row0 = (int64_t)e * A.N + (int64_t)mt * 128;
-    out_col0 = (int64_t)nt * BN;
-  }
-
-  uint64_t *full = bars, *empty = bars + STAGES, *accb = bars + 2 * STAGES;
+  uint64_t *full = bars, *empty = bars + STAGES, *acc_full = bars + 2 * STAGES, *acc_empty = acc_full + NACC;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
       mbar_init(smem_u32(&empty[s]), 1);
     }
-    mbar_init(smem_u32(accb), 1);
+    for (int b = 0; b < NACC; ++b) {
+      mbar_init(smem_u32(&acc_full[b]), 1);
+      mbar_init(smem_u32(&acc_empty[b]), 4);  // one arrival per epilogue warp
+    }
+    *s_abort = 0;
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(smem_u32(s_tmem), C::TMEM_COLS);
@@ -229,105 +274,117 @@ __global__ void __launch_bounds__(192, 1)
     // ---- producer -----------------------------------------------------------
     asm volatile("prefetch.tensormap [%0];" ::"l"(&tmA) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(&tmB) : "memory");
-    int issued = 0;
-    for (int ks = 0; ks < nk; ++ks) {
-      const int s = ks % STAGES;
-      if (ks >= STAGES && !mbar_wait(smem_u32(&empty[s]), ((ks / STAGES) - 1) & 1, A.wait_limit)) {
-        record_error(A.status, NV_ERR_TIMEOUT);
-        break;
-      }
-      const uint32_t fb = smem_u32(&full[s]);
-      mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
-      tma_load_2d(smem_u32(sA + s * C::A_BYTES), &tmA, k_off + ks * 128, a_row, fb);
-      tma_load_2d(smem_u32(sB + s * C::B_BYTES), &tmB, k_off + ks * 128, b_row, fb);
-      const int64_t katom = k_atom0 + (int64_t)ks * C::kAtomsPerStage;
-      bulk_load(smem_u32(sSFA + s * C::SFA_BYTES), A.a_scales + (a_tile * A.ka + katom) * 512, C::SFA_BYTES, fb);
+    uint32_t it = 0;  // global stage counter of this CTA
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+      const Tile T = decode_tile<KIND>(t, A, s_off, s_pad);
+      for (int ks = 0; ks < T.nk; ++ks, ++it) {
+        const uint32_t s = it % STAGES;
+        if (it >= STAGES &&
+            !wait_or_abort(smem_u32(&empty[s]), ((it / STAGES) - 1) & 1, A.wait_limit, s_abort, A.status)) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = smem_u32(&full[s]);
+        mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+        tma_load_2d(smem_u32(sA + s * C::A_BYTES), &tmA, T.k_off + ks * 128, T.a_row, fb);
+        tma_load_2d(smem_u32(sB + s * C::B_BYTES), &tmB, T.k_off + ks * 128, T.b_row, fb);
+        const int64_t katom = T.k_atom0 + (int64_t)ks * C::kAtomsPerStage;
+        bulk_load(smem_u32(sSFA + s * C::SFA_BYTES), A.a_scales + (T.a_tile * A.ka + katom) * 512, C::SFA_BYTES,
+                  fb);
 #pragma unroll
-      for (int j = 0; j < BN / 128; ++j)
-        bulk_load(smem_u32(sSFB + s * C::SFB_BYTES + j * C::SFA_BYTES),
-                  A.b_scales + ((b_tile + j) * A.ka + katom) * 512, C::SFA_BYTES, fb);
-      issued = ks + 1;
+        for (int j = 0; j < kBN / 128; ++j)
+          bulk_load(smem_u32(sSFB + s * C::SFB_BYTES + j * C::SFA_BYTES),
+                    A.b_scales + ((T.b_tile + j) * A.ka + katom) * 512, C::SFA_BYTES, fb);
+      }
     }
     // drain: every copy this thread issued has landed before the CTA leaves
-    for (int ks = issued > STAGES ? issued - STAGES : 0; ks < issued; ++ks)
-      if (!mbar_wait(smem_u32(&full[ks % STAGES]), (ks / STAGES) & 1, A.wait_limit)) {
+    const uint32_t first = it > STAGES ? it - STAGES : 0;
+    for (uint32_t k = first; k < it; ++k)
+      if (!mbar_wait(smem_u32(&full[k % STAGES]), (k / STAGES) & 1, A.wait_limit)) {
         record_error(A.status, NV_ERR_TIMEOUT);
         break;
       }
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer ------------------------------------------------------------
-    for (int ks = 0; ks < nk; ++ks) {
-      const int s = ks % STAGES;
-      if (!mbar_wait(smem_u32(&full[s]), (ks / STAGES) & 1, A.wait_limit)) {
-        record_error(A.status, NV_ERR_TIMEOUT);
+    uint32_t it = 0, tc = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x, ++tc) {
+      const Tile T = decode_tile<KIND>(t, A, s_off, s_pad);
+      const uint32_t acc = tc % NACC, use = tc / NACC;
+      // the accumulator's previous tile has been drained by the epilogue
+      if (use >= 1 &&
+          !wait_or_abort(smem_u32(&acc_empty[acc]), (use - 1) & 1, A.wait_limit, s_abort, A.status))
         break;
-      }
       tc_fence_after();
-      // the scale buffer about to be overwritten was last read by stage ks-2
-      if (ks >= 2 && !mbar_wait(smem_u32(&empty[(ks - 2) % STAGES]), ((ks - 2) / STAGES) & 1, A.wait_limit)) {
-        record_error(A.status, NV_ERR_TIMEOUT);
-        break;
-      }
-      const uint32_t sfa = tmem + BN + (ks & 1) * C::SF_COLS;
-      const uint32_t sfb = sfa + C::SFA_COLS;
-      const uint32_t a_sf_smem = smem_u32(sSFA + s * C::SFA_BYTES);
-      const uint32_t b_sf_smem = smem_u32(sSFB + s * C::SFB_BYTES);
-#pragma unroll
-      for (int j = 0; j < C::kAtomsPerStage; ++j) {
-        tc_cp_sf(sfa + 4 * j, desc_sf(a_sf_smem + j * 512));
-#pragma unroll
-        for (int r = 0; r < BN / 128; ++r)
-          tc_cp_sf(sfb + j * (BN / 32) + 4 * r, desc_sf(b_sf_smem + r * C::SFA_BYTES + j * 512));
-      }
-      const uint64_t da = desc_sw128(smem_u32(sA + s * C::A_BYTES));
-      const uint64_t db = desc_sw128(smem_u32(sB + s * C::B_BYTES));
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t acc = (ks | j) != 0;
-        if (C::kFp4) {
-          mma_nvf4(tmem, da + 2 * j, db + 2 * j, C::IDESC, sfa + 4 * j, sfb + j * (BN / 32), acc);
-        } else {
-          const uint32_t idesc = C::IDESC | ((uint32_t)j << 4) | ((uint32_t)j << 29);
-          mma_mxf8(tmem, da + 2 * j, db + 2 * j, idesc, sfa, sfb, acc);
+      const uint32_t d = tmem + acc * kBN;
+      for (int ks = 0; ks < T.nk; ++ks, ++it) {
+        const uint32_t s = it % STAGES;
+        if (!wait_or_abort(smem_u32(&full[s]), (it / STAGES) & 1, A.wait_limit, s_abort, A.status)) {
+          ok = false;
+          break;
         }
+        tc_fence_after();
+        const uint32_t sfa = tmem + C::ACC_COLS + s * C::SF_COLS;
+        const uint32_t sfb = sfa + C::SFA_COLS;
+        const uint32_t a_sf_smem = smem_u32(sSFA + s * C::SFA_BYTES);
+        const uint32_t b_sf_smem = smem_u32(sSFB + s * C::SFB_BYTES);
+#pragma unroll
+        for (int j = 0; j < C::kAtomsPerStage; ++j) {
+          tc_cp_sf(sfa + 4 * j, desc_sf(a_sf_smem + j * 512));
+#pragma unroll
+          for (int r = 0; r < kBN / 128; ++r)
+            tc_cp_sf(sfb + j * (kBN / 32) + 4 * r, desc_sf(b_sf_smem + r * C::SFA_BYTES + j * 512));
+        }
+        const uint64_t da = desc_sw128(smem_u32(sA + s * C::A_BYTES));
+        const uint64_t db = desc_sw128(smem_u32(sB + s * C::B_BYTES));
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t accum = (ks | j) != 0;
+          if (C::kFp4) {
+            mma_nvf4(d, da + 2 * j, db + 2 * j, C::IDESC, sfa + 4 * j, sfb + j * (kBN / 32), accum);
+          } else {
+            const uint32_t idesc = C::IDESC | ((uint32_t)j << 4) | ((uint32_t)j << 29);
+            mma_mxf8(d, da + 2 * j, db + 2 * j, idesc, sfa, sfb, accum);
+          }
+        }
+        tc_commit(smem_u32(&empty[s]));
       }
-      tc_commit(smem_u32(&empty[s]));
+      tc_commit(smem_u32(&acc_full[acc]));  // arrives once this tile's MMAs are done (at once if none)
     }
-    tc_commit(smem_u32(accb));
   } else if (warp >= 2) {
     // ---- epilogue ----------------------------------------------------------------
     const int q = warp & 3;
     const int row = q * 32 + lane;
-    bool ok = true;
-    if (nk > 0) {
-      ok = mbar_wait(smem_u32(accb), 0, A.wait_limit);
-      if (!ok) record_error(A.status, NV_ERR_TIMEOUT);
+    uint32_t tc = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++tc) {
+      const Tile T = decode_tile<KIND>(t, A, s_off, s_pad);
+      const uint32_t acc = tc % NACC;
+      if (!wait_or_abort(smem_u32(&acc_full[acc]), (tc / NACC) & 1, A.wait_limit, s_abort, A.status)) break;
       tc_fence_after();
-    }
-    if (ok) {
       float alpha = 1.0f;
-      if (KIND == kGemmNvfp4Fwd) alpha = __fmul_rn(A.a_sg[0], A.b_sg[e]);
-      const bool store = row < mrows;
-      const int64_t orow = out_row0 + row;
+      if (KIND == kGemmNvfp4Fwd) alpha = __fmul_rn(A.a_sg[0], A.b_sg[T.e]);
+      const bool store = row < T.mrows;
+      const int64_t orow = T.out_row0 + row;
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 32) {
+      for (int c0 = 0; c0 < kBN; c0 += 32) {
         uint32_t v[32];
-        if (nk > 0) {
-          tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, v);
+        if (T.nk > 0) {
+          tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + acc * kBN + (uint32_t)c0, v);
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = 0u;
         }
         if (!store) continue;
         if (A.out_fp32) {
-          float *dst = static_cast<float *>(A.out) + orow * A.out_ld + out_col0 + c0;
+          float *dst = static_cast<float *>(A.out) + orow * A.out_ld + T.out_col0 + c0;
 #pragma unroll
           for (int i = 0; i < 32; i += 4)
             *reinterpret_cast<float4 *>(dst + i) =
                 make_float4(__fmul_rn(__uint_as_float(v[i]), alpha), __fmul_rn(__uint_as_float(v[i + 1]), alpha),
                             __fmul_rn(__uint_as_float(v[i + 2]), alpha), __fmul_rn(__uint_as_float(v[i + 3]), alpha));
         } else {
-          uint16_t *dst = static_cast<uint16_t *>(A.out) + orow * A.out_ld + out_col0 + c0;
+          uint16_t *dst = static_cast<uint16_t *>(A.out) + orow * A.out_ld + T.out_col0 + c0;
 #pragma unroll
           for (int i = 0; i < 32; i += 8) {
             uint4 w;
@@ -339,6 +396,9 @@ __global__ void __launch_bounds__(192, 1)
           }
         }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&acc_empty[acc]));
     }
   }
   tc_fence_before();
@@ -378,12 +438,30 @@ static bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int KIND, int BN, int STAGES>
-static int run(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &args, int64_t grid, cudaStream_t s) {
-  using C = Cfg<KIND, BN, STAGES>;
+static int num_sms() {
+  static int n[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (!n[dev] && cudaDeviceGetAttribute(&n[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) n[dev] = 0;
+  return n[dev];
+}
+
+template <int KIND, int STAGES, int NACC>
+static int run(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &args, int64_t max_tiles,
+               cudaStream_t s) {
+  using C = Cfg<KIND, STAGES, NACC>;
   const size_t sm = C::smem_bytes(args.E);
-  auto k = grouped_gemm_kernel<KIND, BN, STAGES>;
-  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) != cudaSuccess) return NV_ERR_CUDA;
+  auto k = grouped_gemm_kernel<KIND, STAGES, NACC>;
+  static size_t attr_bytes = 0;  // largest dynamic shared memory requested so far
+  if (sm > attr_bytes) {
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) != cudaSuccess)
+      return NV_ERR_CUDA;
+    attr_bytes = sm;
+  }
+  const int sms = num_sms();
+  if (sms <= 0) return NV_ERR_CUDA;
+  const int64_t ctas = (int64_t)sms * (NACC == 1 ? 2 : 1);  // one accumulator: two CTAs share an SM
+  const int64_t grid = max_tiles < ctas ? max_tiles : ctas;
   if (grid <= 0) return NV_OK;
   k<<<(unsigned)grid, 192, sm, s>>>(ta, tb, args);
   return cudaGetLastError() == cudaSuccess ? NV_OK : NV_ERR_CUDA;
@@ -397,46 +475,53 @@ int launch_grouped_gemm(const GemmProblem &p, int *status, cudaStream_t s) {
   a.groups = p.groups; a.E = p.E; a.M_total = p.M_total; a.N = p.N; a.K = p.K;
   a.out = p.out; a.out_fp32 = p.out_fp32; a.status = status;
   a.wait_limit = (uint64_t)1 << 26;
+  const int64_t out_cols = p.kind == kGemmNvfp4Fwd ? p.N : p.K;
   CUtensorMap ta, tb;
-  const int bn = 256;
-  int64_t out_cols, grid;
   bool ok;
   switch (p.kind) {
     case kGemmNvfp4Fwd:
-      out_cols = p.N;
       ok = make_map(&ta, p.a_codes, p.K / 2, p.M_total, p.K / 2, 128) &&
-           make_map(&tb, p.b_codes, p.K / 2, (uint64_t)p.E * p.N, p.K / 2, (out_cols % bn) ? 128 : bn);
+           make_map(&tb, p.b_codes, p.K / 2, (uint64_t)p.E * p.N, p.K / 2, kBN);
       a.ka = p.K / 64;
       break;
     case kGemmMxfp8Dx:
-      out_cols = p.K;
       ok = make_map(&ta, p.a_codes, p.N, p.M_total, p.N, 128) &&
-           make_map(&tb, p.b_codes, p.N, (uint64_t)p.E * p.K, p.N, (out_cols % bn) ? 128 : bn);
+           make_map(&tb, p.b_codes, p.N, (uint64_t)p.E * p.K, p.N, kBN);
       a.ka = p.N / 128;
       break;
     default:
-      out_cols = p.K;
-      ok = make_map(&ta, p.a_codes, P, p.N, P, 128) && make_map(&tb, p.b_codes, P, p.K, P, (out_cols % bn) ? 128 : bn);
+      ok = make_map(&ta, p.a_codes, P, p.N, P, 128) && make_map(&tb, p.b_codes, P, p.K, P, kBN);
       a.ka = P / 128;
       break;
   }
   if (!ok) return NV_ERR_CUDA;
-  const bool wide = out_cols % bn == 0;
-  a.ntn = (int)(out_cols / (wide ? 256 : 128));
+  a.ntn = (int)(out_cols / kBN);
   a.out_ld = out_cols;
+  int64_t max_tiles;
   if (p.kind == kGemmMxfp8Dw) {
     a.ntm = (int)(p.N / 128);
-    grid = (int64_t)p.E * a.ntm * a.ntn;
+    max_tiles = (int64_t)p.E * a.ntm * a.ntn;
   } else {
-    grid = (P / 128) * a.ntn;
+    max_tiles = (P / 128) * a.ntn;
   }
+  // variant 2 (default): two CTAs per SM with one accumulator each (3 stages);
+  // variant 1: one CTA per SM with two accumulators (6 stages)
+  static int forced = -2;
+  if (forced == -2) {
+    const char *e = getenv("NVFP4MOE_GEMM_VARIANT");
+    forced = e ? atoi(e) : -1;
+  }
+  const bool two_per_sm = forced != 1;
   switch (p.kind) {
     case kGemmNvfp4Fwd:
-      return wide ? run<kGemmNvfp4Fwd, 256, 4>(ta, tb, a, grid, s) : run<kGemmNvfp4Fwd, 128, 5>(ta, tb, a, grid, s);
+      return two_per_sm ? run<kGemmNvfp4Fwd, 3, 1>(ta, tb, a, max_tiles, s)
+                        : run<kGemmNvfp4Fwd, 6, 2>(ta, tb, a, max_tiles, s);
     case kGemmMxfp8Dx:
-      return wide ? run<kGemmMxfp8Dx, 256, 4>(ta, tb, a, grid, s) : run<kGemmMxfp8Dx, 128, 6>(ta, tb, a, grid, s);
+      return two_per_sm ? run<kGemmMxfp8Dx, 3, 1>(ta, tb, a, max_tiles, s)
+                        : run<kGemmMxfp8Dx, 6, 2>(ta, tb, a, max_tiles, s);
     default:
-      return wide ? run<kGemmMxfp8Dw, 256, 4>(ta, tb, a, grid, s) : run<kGemmMxfp8Dw, 128, 6>(ta, tb, a, grid, s);
+      return two_per_sm ? run<kGemmMxfp8Dw, 3, 1>(ta, tb, a, max_tiles, s)
+                        : run<kGemmMxfp8Dw, 6, 2>(ta, tb, a, max_tiles, s);
   }
 }
 

@@ -305,11 +305,17 @@ __global__ void __launch_bounds__(256) mxfp8_rowwise_kernel(MxRowArgs A) {
 // ---------------------------------------------------------------------------
 // Transposed MXFP8 (a5 and the WGRAD operand of a6): one CTA = 128 padded
 // source rows (one window) x 128 source columns.
-//   phase 1  load the tile into shared memory (bf16 values, or NVFP4 codes +
-//            decoded block scales); optionally emit the row-wise MXFP8 output
-//   phase 2  per output row (= source column) and 32-token block: amax, E8M0
-//            scale, SR (bits drawn at the source index) or RN -> bytes
+//   phase 1  stream the tile into shared memory as 16-bit values: bf16 input
+//            as is, NVFP4 input as the exact f16 products e2m1 * e4m3 (at most
+//            6 significant bits, inside the f16 range); optionally emit the
+//            row-wise MXFP8 output (bf16 input)
+//   phase 2  per output row (= source column) and 32-token block: amax on
+//            packed halves, E8M0 scale, SR (bits drawn at the source index) or
+//            RN -> bytes
 //   phase 3  write 128-byte output rows and one 512-byte scale tile
+// The value tile keeps 16-byte chunk c8 of row i at chunk c8 ^ ((i >> 2) & 7),
+// which makes both the row-wise fill and the 4-tokens-per-lane column reads
+// bank-conflict free.
 // ---------------------------------------------------------------------------
 struct MxTArgs {
   // input
@@ -334,9 +340,49 @@ struct MxTArgs {
   int *status;
 };
 
-constexpr int kTileSmemBf16 = 128 * 256;             // 128 rows x 128 bf16, 16B-chunk swizzled
-constexpr int kTileOutStride = 144;                  // output tile row stride (bytes)
-constexpr int kCodeStrideW = 17;                     // NVFP4 code row stride (32-bit words)
+constexpr int kTileSmem = 128 * 256;                 // 128 rows x 128 16-bit values, swizzled
+constexpr int kTileOutStride = 128;                  // output tile row stride (bytes)
+
+__device__ __forceinline__ int chunk_of(int i, int c8) { return c8 ^ ((i >> 2) & 7); }
+
+// eight E2M1 codes (one 32-bit word, element k in nibble k) -> four f16x2
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&h)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(w));
+}
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t habsmax2(uint32_t a, uint32_t b) {  // max(|a|, |b|) per f16 half
+  uint32_t d;
+  asm("max.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a & 0x7FFF7FFFu), "r"(b & 0x7FFF7FFFu));
+  return d;
+}
+__device__ __forceinline__ float f16_lo(uint32_t w) {
+  float f;
+  asm("{ .reg .f16 lo, hi;\n\t mov.b32 {lo, hi}, %1;\n\t cvt.f32.f16 %0, lo; }" : "=f"(f) : "r"(w));
+  return f;
+}
+__device__ __forceinline__ float f16_hi(uint32_t w) {
+  float f;
+  asm("{ .reg .f16 lo, hi;\n\t mov.b32 {lo, hi}, %1;\n\t cvt.f32.f16 %0, hi; }" : "=f"(f) : "r"(w));
+  return f;
+}
+// E4M3 code -> f16x2 (s, s), exact
+__device__ __forceinline__ uint32_t e4m3_to_f16x2_dup(uint32_t code) {
+  uint32_t h2;
+  const uint16_t c16 = (uint16_t)((code & 0xFFu) * 0x0101u);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c16));
+  return h2;
+}
 
 template <bool kNvfp4>
 __global__ void __launch_bounds__(256) mx_transpose_kernel(MxTArgs A) {
@@ -344,9 +390,8 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(MxTArgs A) {
   __shared__ GroupSmem s_g;
   __shared__ __align__(16) uint8_t s_tsc[512];   // transposed scale tile
   __shared__ __align__(16) uint8_t s_rsc[512];   // row-wise scale tile
-  uint8_t *s_out = smem;                                  // [128][144]
-  uint8_t *s_in = smem + 128 * kTileOutStride;            // bf16 tile or NVFP4 codes
-  float *s_bsc = reinterpret_cast<float *>(s_in + 128 * kCodeStrideW * 4);  // NVFP4 block scales [128][9]
+  uint8_t *s_out = smem;                                  // [128][128] output bytes
+  uint8_t *s_in = smem + 128 * kTileOutStride;            // [128][256 B] 16-bit values
 
   int E = A.E;
   if (A.grouped) {
@@ -364,79 +409,87 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(MxTArgs A) {
   // ---- phase 1 --------------------------------------------------------------
   if (!kNvfp4) {
     const bool do_row = A.row_codes != nullptr;
-#pragma unroll 1
-    for (int it = 0; it < 8; ++it) {
-      const int q = it * 256 + tid;
-      const int i = q >> 4, c8 = q & 15;
-      uint4 raw = make_uint4(0, 0, 0, 0);
-      const bool valid = i < w.nvalid;
-      const int64_t e0 = (w.src_row0 + i) * A.cols + col0 + c8 * 8;
-      if (valid) raw = ld_stream_v4(A.x + e0);
-      // 16-byte chunk c8 of row i lives at chunk c8 ^ ((i >> 2) & 7)
-      reinterpret_cast<uint4 *>(s_in + i * 256)[c8 ^ ((i >> 2) & 7)] = raw;
-      if (do_row) {  // row-wise MXFP8: a block of 32 = four neighbouring lanes
-        uint32_t m = bf16x2_absmax(bf16x2_absmax(raw.x, raw.y), bf16x2_absmax(raw.z, raw.w));
-        float fm = bf16x2_max_to_f32(m);
-        fm = fmaxf(fm, __shfl_xor_sync(0xFFFFFFFFu, fm, 1));
-        fm = fmaxf(fm, __shfl_xor_sync(0xFFFFFFFFu, fm, 2));
-        if (valid) {
-          float mult;
-          const uint32_t sc = e8m0_scale(fm, &mult);
-          float v[8];
-          unpack8(raw, v);
-          uint4 bits = make_uint4(0, 0, 0, 0);
-          if (A.sr) bits = philox_bits8((uint64_t)(e0 >> 3), A.seed, A.off_row);
-          *reinterpret_cast<uint2 *>(A.row_codes + e0) = mx_quant8(v, mult, A.sr != 0, bits);
-          if ((c8 & 3) == 0) s_rsc[atom_pos(i, c8 >> 2)] = (uint8_t)sc;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      uint4 raw[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {  // all loads of this half in flight together
+        const int q = (half * 4 + u) * 256 + tid;
+        const int i = q >> 4, c8 = q & 15;
+        raw[u] = make_uint4(0, 0, 0, 0);
+        if (i < w.nvalid) raw[u] = ld_stream_v4(A.x + (w.src_row0 + i) * A.cols + col0 + c8 * 8);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int q = (half * 4 + u) * 256 + tid;
+        const int i = q >> 4, c8 = q & 15;
+        reinterpret_cast<uint4 *>(s_in + i * 256)[chunk_of(i, c8)] = raw[u];
+        if (do_row) {  // row-wise MXFP8: a block of 32 = four neighbouring lanes
+          const bool valid = i < w.nvalid;
+          const int64_t e0 = (w.src_row0 + i) * A.cols + col0 + c8 * 8;
+          uint32_t m = bf16x2_absmax(bf16x2_absmax(raw[u].x, raw[u].y), bf16x2_absmax(raw[u].z, raw[u].w));
+          m = bf16x2_absmax(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+          m = bf16x2_absmax(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+          if (valid) {
+            float mult;
+            const uint32_t sc = e8m0_scale(bf16x2_max_to_f32(m), &mult);
+            float v[8];
+            unpack8(raw[u], v);
+            uint4 bits = make_uint4(0, 0, 0, 0);
+            if (A.sr) bits = philox_bits8((uint64_t)(e0 >> 3), A.seed, A.off_row);
+            *reinterpret_cast<uint2 *>(A.row_codes + e0) = mx_quant8(v, mult, A.sr != 0, bits);
+            if ((c8 & 3) == 0) s_rsc[atom_pos(i, c8 >> 2)] = (uint8_t)sc;
+          }
         }
       }
     }
   } else {
-    // NVFP4 codes: 128 rows x 64 bytes, 8 bytes per thread-step
+    // NVFP4: (row, 16-column block) pairs; 8 code bytes + 1 scale byte each
     const int64_t half_cols = A.cols >> 1;
-#pragma unroll 1
-    for (int it = 0; it < 4; ++it) {
-      const int q = it * 256 + tid;
-      const int i = q >> 3, part = q & 7;
-      uint2 raw = make_uint2(0, 0);
-      if (i < w.nvalid) raw = ld_stream_v2(A.nv_codes + (w.src_row0 + i) * half_cols + (col0 >> 1) + part * 8);
-      uint32_t *row = reinterpret_cast<uint32_t *>(s_in) + i * kCodeStrideW;
-      row[2 * part] = raw.x;
-      row[2 * part + 1] = raw.y;
-    }
-    // block scales of rows [rp0, rp0+128) x kblocks [col0/16, col0/16 + 8):
-    // two consecutive 512-byte tiles of the source scale layout
     const int64_t ka_src = (A.cols + 63) >> 6;
     const int64_t tile0 = (w.rp0 >> 7) * ka_src + (col0 >> 6);
-#pragma unroll 1
-    for (int t = tid; t < 128 * 8; t += 256) {
-      const int i = t >> 3, kb = t & 7;
-      float s = 0.0f;
-      if (i < w.nvalid) s = e4m3_to_f32(A.nv_scales[(tile0 + (kb >> 2)) * 512 + atom_pos(i, kb)]);
-      s_bsc[i * 9 + kb] = s;
+    uint2 raw[4];
+    uint32_t sc[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int q = u * 256 + tid;
+      const int i = q >> 3, kb = q & 7;
+      raw[u] = make_uint2(0, 0);
+      sc[u] = 0;
+      if (i < w.nvalid) {
+        raw[u] = ld_stream_v2(A.nv_codes + (w.src_row0 + i) * half_cols + (col0 >> 1) + kb * 8);
+        sc[u] = A.nv_scales[(tile0 + (kb >> 2)) * 512 + atom_pos(i, kb)];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int q = u * 256 + tid;
+      const int i = q >> 3, kb = q & 7;
+      const uint32_t s2 = e4m3_to_f16x2_dup(sc[u]);
+      uint32_t h0[4], h1[4];
+      e2m1x8_to_f16x2(raw[u].x, h0);
+      e2m1x8_to_f16x2(raw[u].y, h1);
+      uint4 *row = reinterpret_cast<uint4 *>(s_in + i * 256);
+      row[chunk_of(i, 2 * kb)] =
+          make_uint4(hmul2_u32(h0[0], s2), hmul2_u32(h0[1], s2), hmul2_u32(h0[2], s2), hmul2_u32(h0[3], s2));
+      row[chunk_of(i, 2 * kb + 1)] =
+          make_uint4(hmul2_u32(h1[0], s2), hmul2_u32(h1[1], s2), hmul2_u32(h1[2], s2), hmul2_u32(h1[3], s2));
     }
   }
   __syncthreads();
 
   // ---- phase 2 --------------------------------------------------------------
   // warp handles groups of 8 output rows (source columns c8*8 .. c8*8+7);
-  // lane handles tokens 4*lane .. 4*lane+3; tokens 32b .. 32b+31 sit on lanes
-  // 8b .. 8b+7.
+  // lane handles tokens 4*lane .. 4*lane+3, so tokens 32b .. 32b+31 sit on
+  // lanes 8b .. 8b+7.
 #pragma unroll 1
   for (int c8 = warp; c8 < 16; c8 += 8) {
-    float v[4][8];
+    uint32_t v[4][4];  // [token j][column pair] packed 16-bit values
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int i = 4 * lane + j;
-      if (!kNvfp4) {
-        const uint4 raw = reinterpret_cast<const uint4 *>(s_in + i * 256)[c8 ^ ((i >> 2) & 7)];
-        unpack8(raw, v[j]);
-      } else {
-        const uint32_t cw = reinterpret_cast<const uint32_t *>(s_in)[i * kCodeStrideW + c8];
-        const float s = s_bsc[i * 9 + (c8 >> 1)];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) v[j][k] = __fmul_rn(__fmul_rn(e2m1_to_f32((cw >> (4 * k)) & 0xFu), s), sg);
-      }
+      const uint4 raw = reinterpret_cast<const uint4 *>(s_in + i * 256)[chunk_of(i, c8)];
+      v[j][0] = raw.x; v[j][1] = raw.y; v[j][2] = raw.z; v[j][3] = raw.w;
     }
     uint4 bits[4];
 #pragma unroll
@@ -449,24 +502,51 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(MxTArgs A) {
       }
     }
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int c = c8 * 8 + k;
-      float m = fmaxf(fmaxf(fabsf(v[0][k]), fabsf(v[1][k])), fmaxf(fabsf(v[2][k]), fabsf(v[3][k])));
-      m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-      m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-      m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
-      float mult;
-      const uint32_t sc = e8m0_scale(m, &mult);
-      uint32_t packed = 0;
-      if (A.sr) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) packed |= sr_e4m3(__fmul_rn(v[j][k], mult), draw16(bits[j], k)) << (8 * j);
+    for (int p = 0; p < 4; ++p) {  // column pair (2p, 2p+1)
+      uint32_t m;
+      if (kNvfp4) {
+        m = habsmax2(habsmax2(v[0][p], v[1][p]), habsmax2(v[2][p], v[3][p]));
+        m = habsmax2(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+        m = habsmax2(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+        m = habsmax2(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
       } else {
-        packed = cvt_e4m3x2_rn(__fmul_rn(v[0][k], mult), __fmul_rn(v[1][k], mult)) |
-                 (cvt_e4m3x2_rn(__fmul_rn(v[2][k], mult), __fmul_rn(v[3][k], mult)) << 16);
+        m = bf16x2_absmax(bf16x2_absmax(v[0][p], v[1][p]), bf16x2_absmax(v[2][p], v[3][p]));
+        m = bf16x2_absmax(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+        m = bf16x2_absmax(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+        m = bf16x2_absmax(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
       }
-      reinterpret_cast<uint32_t *>(s_out + c * kTileOutStride)[lane] = packed;
-      if ((lane & 7) == 0) s_tsc[atom_pos(c, lane >> 3)] = (uint8_t)sc;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int k = 2 * p + h, c = c8 * 8 + k;
+        float amax, mult;
+        if (kNvfp4) {
+          // max_i fp32(p_i * sg) = fp32(max_i p_i * sg): rounding is monotonic
+          amax = __fmul_rn(h ? f16_hi(m) : f16_lo(m), sg);
+        } else {
+          amax = h ? bf16_hi(m) : bf16_lo(m);
+        }
+        const uint32_t sc = e8m0_scale(amax, &mult);
+        // NVFP4: fp32(fp32(p * sg) * 2^-s) == fp32(p * (sg * 2^-s)) for the
+        // normal-range values the contract covers (the power of two is exact)
+        // (an all-zero block keeps its signed zeros: use multiplier 0, not sg * 2^127)
+        const float m2 = kNvfp4 ? (amax == 0.0f ? 0.0f : __fmul_rn(sg, mult)) : mult;
+        float x[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float val = kNvfp4 ? (h ? f16_hi(v[j][p]) : f16_lo(v[j][p]))
+                                   : (h ? bf16_hi(v[j][p]) : bf16_lo(v[j][p]));
+          x[j] = __fmul_rn(val, m2);
+        }
+        uint32_t packed;
+        if (A.sr) {
+          packed = sr_e4m3(x[0], draw16(bits[0], k)) | (sr_e4m3(x[1], draw16(bits[1], k)) << 8) |
+                   (sr_e4m3(x[2], draw16(bits[2], k)) << 16) | (sr_e4m3(x[3], draw16(bits[3], k)) << 24);
+        } else {
+          packed = cvt_e4m3x2_rn(x[0], x[1]) | (cvt_e4m3x2_rn(x[2], x[3]) << 16);
+        }
+        reinterpret_cast<uint32_t *>(s_out + c * kTileOutStride)[lane] = packed;
+        if ((lane & 7) == 0) s_tsc[atom_pos(c, lane >> 3)] = (uint8_t)sc;
+      }
     }
   }
   __syncthreads();
@@ -540,9 +620,7 @@ int launch_mxfp8_rowwise(const uint16_t *x, int64_t rows, int64_t cols, const in
   return launch_status(cudaGetLastError());
 }
 
-static size_t mx_t_smem(bool nv) {
-  return 128 * kTileOutStride + (nv ? (size_t)128 * kCodeStrideW * 4 + 128 * 9 * 4 : (size_t)kTileSmemBf16);
-}
+static size_t mx_t_smem(bool) { return 128 * kTileOutStride + (size_t)kTileSmem; }
 
 int launch_mx_transpose_bf16(const uint16_t *x, int64_t rows, int64_t cols, const int32_t *groups, int E, int sr,
                              uint64_t seed, uint64_t off_t, uint64_t off_row, uint8_t *codes_t, uint8_t *scales_t,

@@ -350,3 +350,21 @@ def test_quant_sweep_full_size_sampled(shape):
         ec, es = MX.quantize(deq, "sr", bits)
         assert np.array_equal(oc[c], ec[0])
         assert np.array_equal(L.unswizzle(os_, np.array([c]), rows // 32), es)
+
+
+def test_requant_zero_blocks_with_large_outer_scale():
+    """Whole 32-row column blocks of zeros (signed) next to values whose outer
+    scale exceeds 2: the zeros must stay signed zeros with scale code 0."""
+    rows, cols = 256, 128
+    x = _tensor((rows, cols), seed=77, kind="n", scale=3000.0)
+    x[32:64, :] = 0.0
+    x[40, 5] = -0.0
+    codes, scales, sg = _nvfp4_on_gpu(x, 1, rows, cols)
+    assert sg.cpu().numpy()[0] > 2.0
+    oc, os_ = _gpu_requant(codes, scales, sg, 1, rows, cols, None, 5, 1)
+    c, s = unpack_gpu_nvfp4(codes.cpu().numpy(), scales.cpu().numpy(), 1, rows, cols)
+    ec, es = RQ.requant_weights(c[None], s[None], sg.cpu().numpy(), 5, 1)
+    assert np.array_equal(oc.reshape(1, cols, rows), ec)
+    got = L.unswizzle(os_, L.batched_row_map(1, cols), rows // 32).reshape(1, cols, rows // 32)
+    assert np.array_equal(got, es)
+    assert np.all(es[0, :, 1] == 0)
