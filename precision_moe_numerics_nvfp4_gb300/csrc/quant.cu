@@ -231,20 +231,22 @@ struct MxRowArgs {
   int *status;
 };
 
-// quantize 8 consecutive elements starting at source index e0 (a multiple of
-// 8) with multiplier `mult`; RN or SR with the draws of `bits`
-__device__ __forceinline__ uint2 mx_quant8(const float (&v)[8], float mult, bool sr, const uint4 &bits) {
-  uint32_t b[8];
-  if (sr) {
-#pragma unroll
-    for (int k = 0; k < 8; ++k) b[k] = sr_e4m3(__fmul_rn(v[k], mult), draw16(bits, k));
-    return make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24), b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
-  }
+// RN of 8 consecutive elements with multiplier `mult`
+__device__ __forceinline__ uint2 mx_rn8(const float (&v)[8], float mult) {
   const uint32_t p0 = cvt_e4m3x2_rn(__fmul_rn(v[0], mult), __fmul_rn(v[1], mult));
   const uint32_t p1 = cvt_e4m3x2_rn(__fmul_rn(v[2], mult), __fmul_rn(v[3], mult));
   const uint32_t p2 = cvt_e4m3x2_rn(__fmul_rn(v[4], mult), __fmul_rn(v[5], mult));
   const uint32_t p3 = cvt_e4m3x2_rn(__fmul_rn(v[6], mult), __fmul_rn(v[7], mult));
   return make_uint2(p0 | (p1 << 16), p2 | (p3 << 16));
+}
+
+// SR of 8 consecutive elements of a row with multiplier `mult`; w0 and w1 are
+// the Philox words of their four pairs (pairs 0,1 in w0, pairs 2,3 in w1)
+__device__ __forceinline__ uint2 mx_sr8(const float (&v)[8], float mult, uint32_t w0, uint32_t w1) {
+  return make_uint2(cvt_e4m3x4_sr(__fmul_rn(v[0], mult), __fmul_rn(v[1], mult), __fmul_rn(v[2], mult),
+                                  __fmul_rn(v[3], mult), ~w0),
+                    cvt_e4m3x4_sr(__fmul_rn(v[4], mult), __fmul_rn(v[5], mult), __fmul_rn(v[6], mult),
+                                  __fmul_rn(v[7], mult), ~w1));
 }
 
 __device__ __forceinline__ void unpack8(const uint4 &q, float (&v)[8]) {
@@ -278,13 +280,22 @@ __global__ void __launch_bounds__(256) mxfp8_rowwise_kernel(MxRowArgs A) {
     float mult;
     const uint32_t sc = e8m0_scale(bf16x2_max_to_f32(m), &mult);
     uint2 out[4];
+    // pair keys (e0 / 2) .. (e0 / 2) + 15: two Philox calls, one word per 4 elements
+    uint4 bits0 = make_uint4(0, 0, 0, 0), bits1 = make_uint4(0, 0, 0, 0);
+    if (A.sr) {
+      bits0 = philox_bits8((uint64_t)(e0 >> 4), A.seed, A.offset);
+      bits1 = philox_bits8((uint64_t)(e0 >> 4) + 1, A.seed, A.offset);
+    }
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       float v[8];
       unpack8(raw[k], v);
-      uint4 bits = make_uint4(0, 0, 0, 0);
-      if (A.sr) bits = philox_bits8((uint64_t)(e0 >> 3) + k, A.seed, A.offset);
-      out[k] = mx_quant8(v, mult, A.sr != 0, bits);
+      if (A.sr) {
+        const uint4 &b = k < 2 ? bits0 : bits1;
+        out[k] = (k & 1) ? mx_sr8(v, mult, b.z, b.w) : mx_sr8(v, mult, b.x, b.y);
+      } else {
+        out[k] = mx_rn8(v, mult);
+      }
     }
     uint4 *dst = reinterpret_cast<uint4 *>(A.codes + e0);
     dst[0] = make_uint4(out[0].x, out[0].y, out[1].x, out[1].y);
@@ -408,37 +419,54 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(MxTArgs A) {
 
   // ---- phase 1 --------------------------------------------------------------
   if (!kNvfp4) {
+    // items of 16 columns (32 bytes) of one row; a row-wise MXFP8 block of 32
+    // is two neighbouring lanes, and one Philox call covers an item's 8 pairs
     const bool do_row = A.row_codes != nullptr;
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
-      uint4 raw[4];
+      uint4 raw[2][2];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {  // all loads of this half in flight together
-        const int q = (half * 4 + u) * 256 + tid;
-        const int i = q >> 4, c8 = q & 15;
-        raw[u] = make_uint4(0, 0, 0, 0);
-        if (i < w.nvalid) raw[u] = ld_stream_v4(A.x + (w.src_row0 + i) * A.cols + col0 + c8 * 8);
+      for (int u = 0; u < 2; ++u) {  // all loads of this half in flight together
+        const int q = (half * 2 + u) * 256 + tid;
+        const int i = q >> 3, c16 = q & 7;
+        raw[u][0] = raw[u][1] = make_uint4(0, 0, 0, 0);
+        if (i < w.nvalid) {
+          const uint16_t *src = A.x + (w.src_row0 + i) * A.cols + col0 + c16 * 16;
+          raw[u][0] = ld_stream_v4(src);
+          raw[u][1] = ld_stream_v4(src + 8);
+        }
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int q = (half * 4 + u) * 256 + tid;
-        const int i = q >> 4, c8 = q & 15;
-        reinterpret_cast<uint4 *>(s_in + i * 256)[chunk_of(i, c8)] = raw[u];
-        if (do_row) {  // row-wise MXFP8: a block of 32 = four neighbouring lanes
+      for (int u = 0; u < 2; ++u) {
+        const int q = (half * 2 + u) * 256 + tid;
+        const int i = q >> 3, c16 = q & 7;
+        uint4 *row = reinterpret_cast<uint4 *>(s_in + i * 256);
+        row[chunk_of(i, 2 * c16)] = raw[u][0];
+        row[chunk_of(i, 2 * c16 + 1)] = raw[u][1];
+        if (do_row) {
           const bool valid = i < w.nvalid;
-          const int64_t e0 = (w.src_row0 + i) * A.cols + col0 + c8 * 8;
-          uint32_t m = bf16x2_absmax(bf16x2_absmax(raw[u].x, raw[u].y), bf16x2_absmax(raw[u].z, raw[u].w));
+          const int64_t e0 = (w.src_row0 + i) * A.cols + col0 + c16 * 16;
+          uint32_t m = bf16x2_absmax(bf16x2_absmax(raw[u][0].x, raw[u][0].y), bf16x2_absmax(raw[u][0].z, raw[u][0].w));
+          m = bf16x2_absmax(m, bf16x2_absmax(bf16x2_absmax(raw[u][1].x, raw[u][1].y),
+                                             bf16x2_absmax(raw[u][1].z, raw[u][1].w)));
           m = bf16x2_absmax(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-          m = bf16x2_absmax(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
           if (valid) {
             float mult;
             const uint32_t sc = e8m0_scale(bf16x2_max_to_f32(m), &mult);
-            float v[8];
-            unpack8(raw[u], v);
-            uint4 bits = make_uint4(0, 0, 0, 0);
-            if (A.sr) bits = philox_bits8((uint64_t)(e0 >> 3), A.seed, A.off_row);
-            *reinterpret_cast<uint2 *>(A.row_codes + e0) = mx_quant8(v, mult, A.sr != 0, bits);
-            if ((c8 & 3) == 0) s_rsc[atom_pos(i, c8 >> 2)] = (uint8_t)sc;
+            float v0[8], v1[8];
+            unpack8(raw[u][0], v0);
+            unpack8(raw[u][1], v1);
+            uint2 o0, o1;
+            if (A.sr) {
+              const uint4 b = philox_bits8((uint64_t)(e0 >> 4), A.seed, A.off_row);  // pair keys e0/2 .. e0/2+7
+              o0 = mx_sr8(v0, mult, b.x, b.y);
+              o1 = mx_sr8(v1, mult, b.z, b.w);
+            } else {
+              o0 = mx_rn8(v0, mult);
+              o1 = mx_rn8(v1, mult);
+            }
+            *reinterpret_cast<uint4 *>(A.row_codes + e0) = make_uint4(o0.x, o0.y, o1.x, o1.y);
+            if ((c16 & 1) == 0) s_rsc[atom_pos(i, c16 >> 1)] = (uint8_t)sc;
           }
         }
       }
@@ -481,7 +509,10 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(MxTArgs A) {
   // ---- phase 2 --------------------------------------------------------------
   // warp handles groups of 8 output rows (source columns c8*8 .. c8*8+7);
   // lane handles tokens 4*lane .. 4*lane+3, so tokens 32b .. 32b+31 sit on
-  // lanes 8b .. 8b+7.
+  // lanes 8b .. 8b+7.  The lane's two token pairs (4l, 4l+1) and (4l+2, 4l+3)
+  // draw from one Philox call each: pair keys (row * cols + column) for the
+  // 8 consecutive columns.  Each lane computes the E8M0 scale of one column
+  // (lane & 7) of its block and broadcasts its multiplier.
 #pragma unroll 1
   for (int c8 = warp; c8 < 16; c8 += 8) {
     uint32_t v[4][4];  // [token j][column pair] packed 16-bit values
@@ -491,62 +522,69 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(MxTArgs A) {
       const uint4 raw = reinterpret_cast<const uint4 *>(s_in + i * 256)[chunk_of(i, c8)];
       v[j][0] = raw.x; v[j][1] = raw.y; v[j][2] = raw.z; v[j][3] = raw.w;
     }
-    uint4 bits[4];
+    uint4 ba = make_uint4(0, 0, 0, 0), bb = make_uint4(0, 0, 0, 0);
+    if (A.sr && 4 * lane < w.nvalid) {
+      const int64_t ka = (w.src_row0 + 4 * lane) * A.cols + col0 + c8 * 8;
+      ba = philox_bits8((uint64_t)(ka >> 3), A.seed, A.off_t);
+      bb = philox_bits8((uint64_t)((ka + 2 * A.cols) >> 3), A.seed, A.off_t);
+    }
+    uint32_t m[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      bits[j] = make_uint4(0, 0, 0, 0);
-      const int i = 4 * lane + j;
-      if (A.sr && i < w.nvalid) {
-        const int64_t e0 = (w.src_row0 + i) * A.cols + col0 + c8 * 8;
-        bits[j] = philox_bits8((uint64_t)(e0 >> 3), A.seed, A.off_t);
+    for (int p = 0; p < 4; ++p) {  // column pair (2p, 2p+1): max over the 32 tokens of the block
+      if (kNvfp4) {
+        m[p] = habsmax2(habsmax2(v[0][p], v[1][p]), habsmax2(v[2][p], v[3][p]));
+        m[p] = habsmax2(m[p], __shfl_xor_sync(0xFFFFFFFFu, m[p], 1));
+        m[p] = habsmax2(m[p], __shfl_xor_sync(0xFFFFFFFFu, m[p], 2));
+        m[p] = habsmax2(m[p], __shfl_xor_sync(0xFFFFFFFFu, m[p], 4));
+      } else {
+        m[p] = bf16x2_absmax(bf16x2_absmax(v[0][p], v[1][p]), bf16x2_absmax(v[2][p], v[3][p]));
+        m[p] = bf16x2_absmax(m[p], __shfl_xor_sync(0xFFFFFFFFu, m[p], 1));
+        m[p] = bf16x2_absmax(m[p], __shfl_xor_sync(0xFFFFFFFFu, m[p], 2));
+        m[p] = bf16x2_absmax(m[p], __shfl_xor_sync(0xFFFFFFFFu, m[p], 4));
       }
     }
-#pragma unroll
-    for (int p = 0; p < 4; ++p) {  // column pair (2p, 2p+1)
-      uint32_t m;
+    // this lane's column: k_own = lane & 7
+    float m2_own;
+    {
+      const int k_own = lane & 7;
+      const uint32_t mp = k_own < 2 ? m[0] : k_own < 4 ? m[1] : k_own < 6 ? m[2] : m[3];
+      float amax, mult;
       if (kNvfp4) {
-        m = habsmax2(habsmax2(v[0][p], v[1][p]), habsmax2(v[2][p], v[3][p]));
-        m = habsmax2(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-        m = habsmax2(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-        m = habsmax2(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+        // max_i fp32(p_i * sg) = fp32(max_i p_i * sg): rounding is monotonic
+        amax = __fmul_rn((k_own & 1) ? f16_hi(mp) : f16_lo(mp), sg);
       } else {
-        m = bf16x2_absmax(bf16x2_absmax(v[0][p], v[1][p]), bf16x2_absmax(v[2][p], v[3][p]));
-        m = bf16x2_absmax(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-        m = bf16x2_absmax(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-        m = bf16x2_absmax(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+        amax = (k_own & 1) ? bf16_hi(mp) : bf16_lo(mp);
       }
+      const uint32_t sc = e8m0_scale(amax, &mult);
+      // NVFP4: fp32(fp32(p * sg) * 2^-s) == fp32(p * (sg * 2^-s)) for the
+      // normal-range values the contract covers (the power of two is exact);
+      // an all-zero block keeps its signed zeros: multiplier 0, not sg * 2^127
+      m2_own = kNvfp4 ? (amax == 0.0f ? 0.0f : __fmul_rn(sg, mult)) : mult;
+      s_tsc[atom_pos(c8 * 8 + k_own, lane >> 3)] = (uint8_t)sc;
+    }
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int k = 2 * p + h, c = c8 * 8 + k;
-        float amax, mult;
-        if (kNvfp4) {
-          // max_i fp32(p_i * sg) = fp32(max_i p_i * sg): rounding is monotonic
-          amax = __fmul_rn(h ? f16_hi(m) : f16_lo(m), sg);
-        } else {
-          amax = h ? bf16_hi(m) : bf16_lo(m);
-        }
-        const uint32_t sc = e8m0_scale(amax, &mult);
-        // NVFP4: fp32(fp32(p * sg) * 2^-s) == fp32(p * (sg * 2^-s)) for the
-        // normal-range values the contract covers (the power of two is exact)
-        // (an all-zero block keeps its signed zeros: use multiplier 0, not sg * 2^127)
-        const float m2 = kNvfp4 ? (amax == 0.0f ? 0.0f : __fmul_rn(sg, mult)) : mult;
-        float x[4];
+    for (int k = 0; k < 8; ++k) {
+      const int c = c8 * 8 + k;
+      const float m2 = __shfl_sync(0xFFFFFFFFu, m2_own, (lane & ~7) | k);
+      const int p = k >> 1, h = k & 1;
+      float x[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float val = kNvfp4 ? (h ? f16_hi(v[j][p]) : f16_lo(v[j][p]))
-                                   : (h ? bf16_hi(v[j][p]) : bf16_lo(v[j][p]));
-          x[j] = __fmul_rn(val, m2);
-        }
-        uint32_t packed;
-        if (A.sr) {
-          packed = sr_e4m3(x[0], draw16(bits[0], k)) | (sr_e4m3(x[1], draw16(bits[1], k)) << 8) |
-                   (sr_e4m3(x[2], draw16(bits[2], k)) << 16) | (sr_e4m3(x[3], draw16(bits[3], k)) << 24);
-        } else {
-          packed = cvt_e4m3x2_rn(x[0], x[1]) | (cvt_e4m3x2_rn(x[2], x[3]) << 16);
-        }
-        reinterpret_cast<uint32_t *>(s_out + c * kTileOutStride)[lane] = packed;
-        if ((lane & 7) == 0) s_tsc[atom_pos(c, lane >> 3)] = (uint8_t)sc;
+      for (int j = 0; j < 4; ++j) {
+        const float val = kNvfp4 ? (h ? f16_hi(v[j][p]) : f16_lo(v[j][p]))
+                                 : (h ? bf16_hi(v[j][p]) : bf16_lo(v[j][p]));
+        x[j] = __fmul_rn(val, m2);
       }
+      uint32_t packed;
+      if (A.sr) {
+        const uint32_t wa = p == 0 ? ba.x : p == 1 ? ba.y : p == 2 ? ba.z : ba.w;
+        const uint32_t wb = p == 0 ? bb.x : p == 1 ? bb.y : p == 2 ? bb.z : bb.w;
+        // Ua = half h of wa (tokens 4l, 4l+1), Ub = half h of wb (tokens 4l+2, 4l+3)
+        const uint32_t u = __byte_perm(wa, wb, h ? 0x7632 : 0x5410);
+        packed = cvt_e4m3x4_sr(x[0], x[1], x[2], x[3], ~u);
+      } else {
+        packed = cvt_e4m3x2_rn(x[0], x[1]) | (cvt_e4m3x2_rn(x[2], x[3]) << 16);
+      }
+      reinterpret_cast<uint32_t *>(s_out + c * kTileOutStride)[lane] = packed;
     }
   }
   __syncthreads();

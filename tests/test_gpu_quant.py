@@ -11,7 +11,6 @@ from oracle import mxfp8 as MX
 from oracle import nvfp4 as NV
 from oracle import requant as RQ
 from oracle import swiglu as SW
-from oracle.philox import element_bits16
 from precision_moe_numerics_nvfp4_gb300 import nvfp4moe as N
 from precision_moe_numerics_nvfp4_gb300 import workloads as W
 from tests.gpu_helpers import (bf16_f32, check_status, dev, filled, gpu_nvfp4, oracle_nvfp4,
@@ -346,7 +345,9 @@ def test_quant_sweep_full_size_sampled(shape):
         col_scale = s_all[:, kb]
         deq = (F.decode_e2m1_array(col_codes) * F.decode_e4m3_array(col_scale)).astype(np.float32) * np.float32(esg)
         deq = deq.astype(np.float32)[None, :]
-        bits = element_bits16(1, 0, np.arange(rows, dtype=np.int64) * cols + c)[None, :]
+        r = np.arange(rows, dtype=np.int64)
+        u = RQ.pair_draws16(1, 0, (r - (r & 1)) * cols + c)
+        bits = np.where(r & 1, RQ.bitrev16(u), u)[None, :]
         ec, es = MX.quantize(deq, "sr", bits)
         assert np.array_equal(oc[c], ec[0])
         assert np.array_equal(L.unswizzle(os_, np.array([c]), rows // 32), es)
@@ -368,3 +369,27 @@ def test_requant_zero_blocks_with_large_outer_scale():
     got = L.unswizzle(os_, L.batched_row_map(1, cols), rows // 32).reshape(1, cols, rows // 32)
     assert np.array_equal(got, es)
     assert np.all(es[0, :, 1] == 0)
+
+
+@pytest.mark.parametrize("mode", [N.NV_RN, N.NV_SR])
+def test_mxfp8_wide_range_blocks_match_oracle(mode):
+    """Blocks whose elements span the E4M3 subnormal range, the normal range
+    and the saturation region (|w| in [416, 512)), with signed zeros: the
+    hardware conversions agree with the oracle's rules everywhere."""
+    rows, cols = 256, 256
+    rng = np.random.default_rng(31)
+    mag = np.exp2(rng.uniform(-16, 9, size=(rows, cols)))
+    v = mag * rng.choice([-1.0, 1.0], size=(rows, cols))
+    v[rng.random((rows, cols)) < 0.03] = 0.0
+    v[rng.random((rows, cols)) < 0.01] = -0.0
+    v[:, ::32] = np.where(rng.random((rows, cols // 32)) < 0.5, 256.0, -300.0)   # block maxima
+    v[::7, 5] = 470.0                                                              # saturating elements
+    x = torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16).to(dev()).contiguous()
+    r = _gpu_mx(x, rows, cols, None, mode, 12, 3, 4, want_row=True, want_t=(mode == N.NV_SR))
+    xf = bf16_f32(x)
+    ec, es = _oracle_mx_row(xf, None, mode, 12, 3)
+    assert np.array_equal(r["cr"], ec) and np.array_equal(r["sr"], es)
+    if mode == N.NV_SR:
+        tc, ts = _oracle_mx_t(xf, None, mode, 12, 4, r["P"])
+        assert np.array_equal(r["ct"].reshape(cols, r["P"]), tc)
+        assert np.array_equal(L.unswizzle(r["st"], np.arange(cols), r["P"] // 32), ts)

@@ -11,7 +11,7 @@ from oracle import layout as L
 from oracle import mxfp8 as MX
 from oracle import nvfp4 as NV
 from oracle import requant as RQ
-from oracle.philox import element_bits16
+from oracle.philox import bitrev16, pair_draws16
 
 
 # --- E8M0 scale rule ---------------------------------------------------------
@@ -129,13 +129,16 @@ def test_requant_exact_when_dequant_is_representable():
         assert np.array_equal(MX.dequantize_f64(oc[0], osc[0]), deq.T)
 
 
-def test_requant_uses_source_row_major_index():
-    """A lone non-representable element rounds up iff its 16 bits, drawn at
-    its source row-major index r*C + c, fall below floor(f 2^16).  With every
-    other code 6, scale 1 and sg = 1.0625 the transposed block holding
-    element (r0, 3) has amax 6.375, so sexp = -6 and the element's value
-    0.5 * 1.0625 * 64 = 34 sits halfway between the E4M3 points 32 and 36."""
-    R, C, r0 = 32, 32, 9
+@pytest.mark.parametrize("r0", [9, 8])
+def test_requant_uses_the_pair_draw(r0):
+    """A lone non-representable element rounds up iff its draw falls below
+    floor(f 2^16).  Output element (c=3, r=r0) of weights [R, C] belongs to
+    the pair of source rows (r0 - r0 % 2, +1) with key (r0 - r0 % 2) * C + 3;
+    it uses the draw itself when r0 is even and its bit-reversal when odd.
+    With every other code 6, scale 1 and sg = 1.0625 the transposed block
+    holding it has amax 6.375, so sexp = -6 and its value 0.5 * 1.0625 * 64 =
+    34 sits halfway between the E4M3 points 32 and 36."""
+    R, C = 32, 32
     codes = np.full((R, C), 0x7, dtype=np.uint8)
     scales = np.full((R, C // 16), 0x38, dtype=np.uint8)
     codes[r0, 3] = 0x1
@@ -145,11 +148,30 @@ def test_requant_uses_source_row_major_index():
         oc, osc = RQ.requant_weights(codes[None], scales[None], np.array([sg]), seed, 0)
         assert int(osc[0][3, 0]) - 127 == -6
         val = MX.dequantize_f64(oc[0], osc[0])[3, r0]
-        bits = int(element_bits16(seed, 0, np.array([r0 * C + 3]))[0])
-        want_up = bits < 32768
+        u = int(pair_draws16(seed, 0, np.array([(r0 - r0 % 2) * C + 3]))[0])
+        r = int(bitrev16(np.array([u]))[0]) if r0 % 2 else u
+        want_up = r < 32768
         assert val == (36.0 if want_up else 32.0) * 2.0 ** -6
         ups += want_up
     assert 10 < ups < 54
+
+
+def test_gradient_rowwise_pairs_share_a_draw():
+    """Columns (2j, 2j+1) of a row use U and bitrev16(U) of key (m N + 2j) / 2:
+    with both at f = 1/2 the two decisions are the top and the bottom bit of U."""
+    M, N = 2, 32
+    g = np.zeros((M, N), dtype=np.float32)
+    g[:, 0] = 256.0                       # block max -> scale 2^0
+    g[1, 4] = g[1, 5] = 34.0              # halfway between 32 and 36
+    for seed in range(16):
+        codes, sc = RQ.quantize_grad_rowwise(g, seed, 9)
+        assert int(sc[1, 0]) == 127
+        u = int(pair_draws16(seed, 9, np.array([(1 * N + 4) // 2]))[0])
+        up4 = u < 32768
+        up5 = int(bitrev16(np.array([u]))[0]) < 32768
+        vals = MX.dequantize_f64(codes, sc)
+        assert vals[1, 4] == (36.0 if up4 else 32.0) and vals[1, 5] == (36.0 if up5 else 32.0)
+        assert up4 == (not (u >> 15) & 1) and up5 == (not (u & 1))
 
 
 @pytest.mark.slow
