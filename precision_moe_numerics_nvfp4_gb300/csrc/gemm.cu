@@ -21,9 +21,10 @@
 //               to tensor memory (tcgen05.cp, one buffer per ring stage) and
 //               issues 4 block-scaled MMAs per stage into the fp32
 //               accumulator (or alternates two, variant 1)
-//   warps 2-5   epilogue: tcgen05.ld of the finished accumulator, outer-scale
-//               multiply, bf16/fp32 stores of the rows that belong to the
-//               expert, then release of the accumulator
+//   warps 2-5   epilogue: tcgen05.ld of the finished accumulator into
+//               registers, release of the accumulator, then outer-scale
+//               multiply and 32-byte streaming stores of the rows that belong
+//               to the expert
 // Every wait is bounded: a wait that runs out records NV_ERR_TIMEOUT and
 // raises a CTA-wide abort flag so that the other roles stop too; the producer
 // waits (bounded) for its own copies and tensor memory is always freed.
@@ -87,7 +88,8 @@ __device__ __forceinline__ void mma_mxf8(uint32_t d, uint64_t a, uint64_t b, uin
       "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb)
       : "memory");
 }
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+// 32 consecutive accumulator columns of this warp's 32 lanes, no wait
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t *v) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
       "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
@@ -96,7 +98,15 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
         "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
         "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
       : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// 32-byte streaming store (evict-first): the GEMM outputs are written once
+__device__ __forceinline__ void st_cs_v8(void *p, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t a4,
+                                         uint32_t a5, uint32_t a6, uint32_t a7) {
+  asm volatile("st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a0), "r"(a1), "r"(a2),
+               "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
+               : "memory");
 }
 
 // Shared-memory matrix descriptor, K-major operand tile with rows of 128 bytes
@@ -229,7 +239,7 @@ __device__ __forceinline__ Tile decode_tile(int t, const GemmArgs &A, const int 
 // the kernel
 // ---------------------------------------------------------------------------
 template <int KIND, int STAGES, int NACC>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(192, 2)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmArgs A) {
   using C = Cfg<KIND, STAGES, NACC>;
   extern __shared__ uint8_t smem_raw[];
@@ -366,39 +376,44 @@ __global__ void __launch_bounds__(192, 1)
       if (KIND == kGemmNvfp4Fwd) alpha = __fmul_rn(A.a_sg[0], A.b_sg[T.e]);
       const bool store = row < T.mrows;
       const int64_t orow = T.out_row0 + row;
-#pragma unroll 1
-      for (int c0 = 0; c0 < kBN; c0 += 32) {
-        uint32_t v[32];
-        if (T.nk > 0) {
-          tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + acc * kBN + (uint32_t)c0, v);
-        } else {
+      // read the whole accumulator row into registers, release the
+      // accumulator to the MMA thread, then convert and store
+      uint32_t r[kBN];
+      if (T.nk > 0) {
+        const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + acc * kBN;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = 0u;
-        }
-        if (!store) continue;
-        if (A.out_fp32) {
-          float *dst = static_cast<float *>(A.out) + orow * A.out_ld + T.out_col0 + c0;
+        for (int c0 = 0; c0 < kBN; c0 += 32) tmem_ld32_nowait(tb + (uint32_t)c0, &r[c0]);
+        tmem_wait_ld();
+      } else {
 #pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            *reinterpret_cast<float4 *>(dst + i) =
-                make_float4(__fmul_rn(__uint_as_float(v[i]), alpha), __fmul_rn(__uint_as_float(v[i + 1]), alpha),
-                            __fmul_rn(__uint_as_float(v[i + 2]), alpha), __fmul_rn(__uint_as_float(v[i + 3]), alpha));
-        } else {
-          uint16_t *dst = static_cast<uint16_t *>(A.out) + orow * A.out_ld + T.out_col0 + c0;
-#pragma unroll
-          for (int i = 0; i < 32; i += 8) {
-            uint4 w;
-            w.x = pack_bf16x2(__fmul_rn(__uint_as_float(v[i]), alpha), __fmul_rn(__uint_as_float(v[i + 1]), alpha));
-            w.y = pack_bf16x2(__fmul_rn(__uint_as_float(v[i + 2]), alpha), __fmul_rn(__uint_as_float(v[i + 3]), alpha));
-            w.z = pack_bf16x2(__fmul_rn(__uint_as_float(v[i + 4]), alpha), __fmul_rn(__uint_as_float(v[i + 5]), alpha));
-            w.w = pack_bf16x2(__fmul_rn(__uint_as_float(v[i + 6]), alpha), __fmul_rn(__uint_as_float(v[i + 7]), alpha));
-            *reinterpret_cast<uint4 *>(dst + i) = w;
-          }
-        }
+        for (int i = 0; i < kBN; ++i) r[i] = 0u;
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&acc_empty[acc]));
+      if (store) {
+        if (A.out_fp32) {
+          float *dst = static_cast<float *>(A.out) + orow * A.out_ld + T.out_col0;
+#pragma unroll
+          for (int i = 0; i < kBN; i += 8) {
+            uint32_t w[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) w[k] = __float_as_uint(__fmul_rn(__uint_as_float(r[i + k]), alpha));
+            st_cs_v8(dst + i, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+          }
+        } else {
+          uint16_t *dst = static_cast<uint16_t *>(A.out) + orow * A.out_ld + T.out_col0;
+#pragma unroll
+          for (int i = 0; i < kBN; i += 16) {
+            uint32_t w[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              w[k] = pack_bf16x2(__fmul_rn(__uint_as_float(r[i + 2 * k]), alpha),
+                                 __fmul_rn(__uint_as_float(r[i + 2 * k + 1]), alpha));
+            st_cs_v8(dst + i, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+          }
+        }
+      }
     }
   }
   tc_fence_before();
