@@ -558,6 +558,44 @@ def run_gemm(args):
                       "TFLOP_s": flops / (ms / 1e3) / 1e12}))
 
 
+def run_decode(args):
+    """Sampler-style decode forward: 128 experts, SwiGLU gate/up [7168 -> 2048
+    x2] and down [2048 -> 7168] quantized to NVFP4 beforehand (untimed), 256
+    tokens routed top-8 (~16 rows per expert).  Timed: NVFP4 quantization of
+    the activations, both grouped NVFP4 GEMMs and SwiGLU.  Reported as HBM
+    GB/s of the NVFP4 weight + scale bytes (0.5625 B per parameter)."""
+    import torch
+    from precision_moe_numerics_nvfp4_gb300 import nvfp4moe as N
+    from precision_moe_numerics_nvfp4_gb300 import workloads as W
+    from precision_moe_numerics_nvfp4_gb300.pipeline import MoELayer
+
+    N.lib()
+    peaks = load_peaks()
+    m = W.decode("cuda")
+    M, D, I, E = m.x_perm.shape[0], 7168, 2048, 128
+    layer = MoELayer(M, D, I, E, backward=False)
+    layer.quantize_weights(m.w13, m.w2)
+    params = E * (2 * I * D + D * I)
+    wbytes = params * 0.5625
+    for _ in range(args.warmup):
+        layer.forward_activations(m.x_perm, m.group_offsets)
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(args.steps):
+        layer.forward_activations(m.x_perm, m.group_offsets)
+    e1.record(s)
+    torch.cuda.synchronize()
+    assert N.nvfp4moe_get_device_status() == 0
+    ms = e0.elapsed_time(e1) / args.steps
+    gbs = wbytes / (ms / 1e3) / 1e9
+    sizes = torch.diff(m.group_offsets.to(torch.int64))
+    print(json.dumps({"workload": "decode", "experts": E, "rows": M, "min_group": int(sizes.min()),
+                      "max_group": int(sizes.max()), "weight_bytes": wbytes, "ms": ms, "GB_s": gbs,
+                      "frac_hbm": gbs / peaks["hbm_gbs"], "peak_source": peaks["source"]}))
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -568,7 +606,7 @@ def main(argv=None):
     ap.add_argument("--ref-tokens", type=int, default=64)
     ap.add_argument("--ref-dff", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["moe", "quant_sweep", "gemm"], default="moe")
+    ap.add_argument("--workload", choices=["moe", "quant_sweep", "gemm", "decode"], default="moe")
     ap.add_argument("--gemm-kind", choices=["fwd", "dx", "dw"], default="fwd")
     ap.add_argument("--gemm-tokens", type=int, default=16384)
     ap.add_argument("--sweep-op", default=None)
@@ -582,6 +620,8 @@ def main(argv=None):
         run_quant_sweep(args)
     elif args.workload == "gemm":
         run_gemm(args)
+    elif args.workload == "decode":
+        run_decode(args)
     else:
         run_ours(args)
 

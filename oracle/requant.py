@@ -46,12 +46,13 @@ def _pair_bits(seed, offset, key, second):
     return np.where(second, bitrev16(u), u)
 
 
-def requant_weights(codes, scales, sg, seed: int, offset: int):
+def requant_weights(codes, scales, sg, seed: int, offset: int, b0: int = 0):
     """Per-expert weights: NVFP4 codes [B, R, C] (4-bit codes), E4M3 scales
     [B, R, C/16], outer scales sg [B]  ->  MXFP8 (SR) of the transposes:
     E4M3 codes [B, C, R] and E8M0 scales [B, C, R/32].  R % 32 == 0.
     Output element (b, c, r) belongs to the pair of source rows (r0, r0+1),
-    r0 = r - r % 2, with key (b*R + r0) * C + c."""
+    r0 = r - r % 2, with key ((b0 + b)*R + r0) * C + c; b0 > 0 treats the
+    arrays as experts b0, b0+1, ... of a larger stack."""
     codes = np.asarray(codes)
     B, R, C = codes.shape
     oc = np.empty((B, C, R), dtype=np.uint8)
@@ -59,7 +60,7 @@ def requant_weights(codes, scales, sg, seed: int, offset: int):
     rr, cc = np.meshgrid(np.arange(R, dtype=np.int64), np.arange(C, dtype=np.int64), indexing="xy")  # [C, R]
     for b in range(B):
         deq = NV.dequantize_f32(codes[b], scales[b], np.asarray(sg, dtype=F32).reshape(-1)[b])
-        key = (b * R + (rr - (rr & 1))) * C + cc
+        key = ((b0 + b) * R + (rr - (rr & 1))) * C + cc
         bits = _pair_bits(seed, offset, key, (rr & 1) == 1)
         oc[b], osc[b] = MX.quantize(deq.T, "sr", bits)
     return oc, osc

@@ -126,7 +126,7 @@ class MoELayer:
     """Routed experts of one MoE layer: rows grouped by expert (group_offsets),
     w13 [E][2I][d] (gate rows then up rows), w2 [E][d][I]."""
 
-    def __init__(self, M, d_model, d_ff, E, device="cuda"):
+    def __init__(self, M, d_model, d_ff, E, device="cuda", backward=True):
         dev = torch.device(device)
         self.M, self.d, self.I, self.E = M, d_model, d_ff, E
         I2 = 2 * d_ff
@@ -138,6 +138,8 @@ class MoELayer:
         self.h = torch.empty((M, d_ff), dtype=BF16, device=dev)
         self.hq = NvTensor(1, M, d_ff, dev, E=E)
         self.y2 = torch.empty((M, d_model), dtype=BF16, device=dev)
+        if not backward:  # forward-only use (sampling): no backward buffers
+            return
         # backward
         self.xt = MxTransposed(M, d_model, dev, E=E)
         self.ht = MxTransposed(M, d_ff, dev, E=E)
@@ -158,10 +160,18 @@ class MoELayer:
         fwd = 2 * self.M * (2 * self.I) * self.d + 2 * self.M * self.d * self.I
         return fwd, 2 * fwd
 
-    def forward(self, x, w13, w2, groups, stream=None):
-        M, d, I, E = self.M, self.d, self.I, self.E
+    def quantize_weights(self, w13, w2, stream=None):
+        """NVFP4 of both expert weight stacks, one outer scale per expert."""
         self.w13q.quantize(w13, None, stream)
         self.w2q.quantize(w2, None, stream)
+
+    def forward(self, x, w13, w2, groups, stream=None):
+        self.quantize_weights(w13, w2, stream)
+        self.forward_activations(x, groups, stream)
+
+    def forward_activations(self, x, groups, stream=None):
+        """The forward with the weights already quantized (e.g. sampling)."""
+        M, d, I, E = self.M, self.d, self.I, self.E
         self.xq.quantize(x, groups, stream)
         N.grouped_gemm_nvfp4_fwd(None, self.xq.sg, self.xq.codes, self.xq.scales, self.w13q.codes,
                                  self.w13q.scales, self.w13q.sg, groups, E, M, 2 * I, d, self.y13, N.NV_OUT_BF16,

@@ -15,7 +15,8 @@ layer with 1x16 NVFP4 forward and MXFP8 backward -- made synthetic):
                      from logits ~N(0,1) + bias ~N(0,1); SwiGLU experts
                      gate/up [4096->1536 x2], down [1536->4096], ~N(0,0.02)
   moe_backward       same shapes, down-output gradient ~N(0,1e-3)
-  decode             128 experts [7168 x 2048 gate/up/down], 256 tokens top-8
+  decode             128 experts [7168 x 2048 gate/up/down], 256 tokens plain
+                     top-8 (no bias)
 The second parameter of N(mean, s) is the standard deviation.
 """
 from __future__ import annotations
@@ -120,10 +121,12 @@ class MoE:
 
 def moe(device="cpu", seed: int = 2, tokens: int = 16384, d_model: int = 4096, experts: int = 64,
         topk: int = 8, d_ff: int = 1536, with_grad: bool = False, grad_seed: int = 3,
-        weights: bool = True):
+        weights: bool = True, bias_std: float = 1.0):
+    """Routed expert inputs: top-k of logits ~ N(0,1) plus a per-expert bias
+    ~ N(0, bias_std) (uneven groups; bias_std 0 gives plain top-k)."""
     gen = _gen(seed, device)
     logits = torch.randn((tokens, experts), generator=gen, device=device)
-    bias = torch.randn((experts,), generator=gen, device=device)
+    bias = torch.randn((experts,), generator=gen, device=device) * bias_std
     token, offsets = route_topk(logits, bias, topk)
     x = normal((tokens, d_model), 1.0, gen, device)
     x_perm = x[token].contiguous()
@@ -143,8 +146,9 @@ def moe(device="cpu", seed: int = 2, tokens: int = 16384, d_model: int = 4096, e
 
 def decode(device="cpu", seed: int = 4, tokens: int = 256, d_model: int = 7168, d_ff: int = 2048,
            experts: int = 128, topk: int = 8):
-    """Sampler-style decode: ~16 rows per expert (asserted 1..64)."""
-    m = moe(device, seed, tokens, d_model, experts, topk, d_ff)
+    """Sampler-style decode: plain top-8 routing of logits ~ N(0,1), ~16 rows
+    per expert (asserted 1..64)."""
+    m = moe(device, seed, tokens, d_model, experts, topk, d_ff, bias_std=0.0)
     sizes = torch.diff(m.group_offsets.to(torch.int64))
     if int(sizes.min()) < 1 or int(sizes.max()) > 64:
         raise RuntimeError("decode routing left an expert outside 1..64 rows")
