@@ -58,6 +58,8 @@ size_t nvfp4moe_quantize_workspace_bytes(int64_t batch, int64_t rows, int64_t co
 
 const char *nvfp4moe_version(void) { return "nvfp4moe 0.1 (sm_103a)"; }
 
+int nvfp4moe_set_gemm_kernel(int variant) { return nvm::set_gemm_variant(variant); }
+
 const char *nvfp4moe_status_string(int s) {
   switch (s) {
     case NV_OK: return "ok";

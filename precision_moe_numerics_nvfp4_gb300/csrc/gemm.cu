@@ -425,6 +425,393 @@ __global__ void __launch_bounds__(192, 2)
 }
 
 // ---------------------------------------------------------------------------
+// CTA-pair variant (cta_group::2): one 256 x 256 output tile per pair of SMs.
+// Each CTA of the pair stages 128 rows of A and its 128-row half of B; one
+// thread of the even CTA issues M=256, N=256 MMAs that read both CTAs' shared
+// memory and accumulate 128 rows x 256 columns in each CTA's tensor memory.
+// Per FLOP this moves half the L2 -> SM operand bytes of the 128 x 128 tile.
+// The odd CTA's TMA loads signal the even CTA's "full" barrier; the MMA
+// commits arrive on both CTAs' barriers (multicast); the odd CTA's epilogue
+// warps release the accumulator on the even CTA's barrier.  The block-scale
+// tiles are loaded with TMA too (2-D view of the scale buffer, 128-byte rows)
+// so that they can signal the peer's barrier; each CTA holds the scales of
+// its own A rows and of all 256 B rows.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"((uint16_t)3)
+      : "memory");
+}
+__device__ __forceinline__ void tc_cp_sf_pair(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+__device__ __forceinline__ void mma_nvf4_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                              uint32_t sfb, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+          d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb)
+      : "memory");
+}
+__device__ __forceinline__ void mma_mxf8_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                              uint32_t sfb, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+          d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb)
+      : "memory");
+}
+// Relaxed: the only ordering needed is that this warp's tensor-memory loads
+// have completed (tcgen05.wait::ld), not that its earlier global stores are
+// visible, so no release fence is paid here.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
+constexpr int kPairN = 256;  // output tile of a CTA pair: 256 x 256
+
+template <int KIND, int STAGES>
+struct CfgPair {
+  static constexpr bool kFp4 = KIND == kGemmNvfp4Fwd;
+  static constexpr int kAtomsPerStage = kFp4 ? 4 : 1;
+  static constexpr int A_BYTES = 128 * 128;
+  static constexpr int B_BYTES = 128 * 128;             // this CTA's half of B
+  static constexpr int SFA_BYTES = kAtomsPerStage * 512;
+  static constexpr int SFB_BYTES = 2 * SFA_BYTES;       // scales of all 256 B rows
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+  static constexpr int SFA_COLS = kAtomsPerStage * 4;
+  static constexpr int SFB_COLS = kAtomsPerStage * 8;
+  static constexpr int SF_COLS = SFA_COLS + SFB_COLS;
+  static constexpr int ACC_COLS = kPairN;
+  static constexpr int TMEM_COLS = cpow2(ACC_COLS + STAGES * SF_COLS);
+  static constexpr int NBARS = 2 * STAGES + 2;          // full, empty, acc_full, acc_empty
+  static constexpr int kEpiWarps = 8;                   // two per lane quadrant, 128 columns each
+  static constexpr int kThreads = 32 * (2 + kEpiWarps);
+  static constexpr uint32_t IDESC = (kFp4 ? ((1u << 7) | (1u << 10)) : (1u << 23)) |
+                                    ((uint32_t)(kPairN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+  static size_t smem_bytes(int E) {
+    return 1024 + (size_t)STAGES * STAGE_BYTES + NBARS * 8 + 32 + (size_t)(E + 1) * 12 + 64;
+  }
+  static_assert(TMEM_COLS <= 512, "tensor memory");
+};
+
+// One pair tile, seen from CTA `cta` (0 or 1) of the pair.
+struct PairTile {
+  int e, nk, k_off, mrows;
+  int a_row, b_row;
+  int64_t a_tile, b_tile0, k_atom0, out_row0, out_col0;
+};
+
+// s_pb[e]: number of 256-row pair blocks before expert e (fwd, dgrad)
+template <int KIND>
+__device__ __forceinline__ PairTile decode_pair(int t, const GemmArgs &A, const int *s_off, const int *s_pad,
+                                                const int *s_pb, int cta) {
+  PairTile T;
+  if (KIND != kGemmMxfp8Dw) {
+    const int pm = t / A.ntn, nt = t - (t / A.ntn) * A.ntn;
+    const int e = find_group(s_pb, A.E, pm);
+    const int p0 = s_pad[e] + (pm - s_pb[e]) * 256;
+    int ph = p0 + 128 * cta;
+    const bool live = ph < s_pad[e + 1];
+    if (!live) ph = p0;  // an empty half re-reads the first half; nothing of it is stored
+    T.e = e;
+    T.a_row = s_off[e] + (ph - s_pad[e]);
+    T.mrows = live ? min(128, s_off[e + 1] - T.a_row) : 0;
+    T.a_tile = ph / 128;
+    const int nb = (int)(KIND == kGemmNvfp4Fwd ? A.N : A.K);
+    T.b_row = e * nb + nt * kPairN + 128 * cta;
+    T.b_tile0 = ((int64_t)e * nb + (int64_t)nt * kPairN) / 128;
+    T.nk = (int)(KIND == kGemmNvfp4Fwd ? A.K / 256 : A.N / 128);
+    T.k_off = 0;
+    T.k_atom0 = 0;
+    T.out_row0 = T.a_row;
+    T.out_col0 = (int64_t)nt * kPairN;
+  } else {
+    const int per_e = A.ntm * A.ntn;
+    const int e = t / per_e;
+    const int r = t - e * per_e, mt = r / A.ntn, nt = r - (r / A.ntn) * A.ntn;
+    T.e = e;
+    T.a_row = mt * 256 + 128 * cta;
+    T.b_row = nt * kPairN + 128 * cta;
+    T.mrows = 128;
+    T.nk = (s_pad[e + 1] - s_pad[e]) / 128;
+    T.k_off = s_pad[e];
+    T.a_tile = T.a_row / 128;
+    T.b_tile0 = (int64_t)nt * 2;
+    T.k_atom0 = s_pad[e] / 128;
+    T.out_row0 = (int64_t)e * A.N + T.a_row;
+    T.out_col0 = (int64_t)nt * kPairN;
+  }
+  return T;
+}
+
+// warp 0: exclusive scan of ceil(padded group size / 256) into s_pb[0..E]
+__device__ inline void scan_pair_blocks(const int *s_pad, int E, int *s_pb) {
+  if (threadIdx.x < 32) {
+    int carry = 0;
+    for (int base = 0; base <= E; base += 32) {
+      const int e = base + (int)threadIdx.x;
+      int v = 0;
+      if (e < E) v = (s_pad[e + 1] - s_pad[e] + 255) / 256;
+      int incl = v;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int n = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+        if ((int)threadIdx.x >= d) incl += n;
+      }
+      if (e <= E) s_pb[e] = carry + incl - v;
+      carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    }
+  }
+  __syncthreads();
+}
+
+// A bounded wait that raises the abort flag of both CTAs of the pair when it
+// runs out (or gives up when one of them is raised).
+__device__ __forceinline__ bool wait_pair(uint32_t bar, uint32_t parity, uint64_t limit, volatile int *abort,
+                                          uint32_t peer_abort, int *status) {
+  for (uint64_t i = 0; i < limit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255) == 255 && *abort) return false;
+  }
+  *abort = 1;
+  st_cluster_u32(peer_abort, 1u);
+  record_error(status, NV_ERR_TIMEOUT);
+  return false;
+}
+
+template <int KIND, int STAGES>
+__global__ void __launch_bounds__(CfgPair<KIND, STAGES>::kThreads, 1)
+    grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                             const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
+                             GemmArgs A) {
+  using C = CfgPair<KIND, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint8_t *sA = smem;
+  uint8_t *sB = sA + STAGES * C::A_BYTES;
+  uint8_t *sSFA = sB + STAGES * C::B_BYTES;
+  uint8_t *sSFB = sSFA + STAGES * C::SFA_BYTES;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sSFB + STAGES * C::SFB_BYTES);
+  uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + C::NBARS);
+  volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
+  int *s_flag = reinterpret_cast<int *>(s_tmem + 2);
+  int *s_off = s_flag + 2;
+  int *s_pad = s_off + (A.E + 1);
+  int *s_pb = s_pad + (A.E + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cta = (int)cluster_ctarank();
+  const int pair = (int)(blockIdx.x >> 1), npairs = (int)(gridDim.x >> 1);
+  // identical in both CTAs of the pair, so an early return is taken by both
+  if (!load_groups(A.groups, A.E, A.M_total, s_off, s_pad, s_flag, A.status)) return;
+  scan_pair_blocks(s_pad, A.E, s_pb);
+  const int num_tiles = KIND == kGemmMxfp8Dw ? A.E * A.ntm * A.ntn : s_pb[A.E] * A.ntn;
+  if (pair >= num_tiles) return;
+
+  uint64_t *full = bars, *empty = bars + STAGES, *acc_full = bars + 2 * STAGES, *acc_empty = acc_full + 1;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    mbar_init(smem_u32(acc_full), 1);
+    mbar_init(smem_u32(acc_empty), 2 * C::kEpiWarps);  // every epilogue warp of both CTAs
+    *s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc_pair(smem_u32(s_tmem), C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // barriers of both CTAs initialised before any remote use
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  const uint32_t peer_abort = mapa_shared(smem_u32((const void *)s_abort), (uint32_t)(cta ^ 1));
+
+  if (warp == 0 && lane == 0) {
+    // ---- producer (both CTAs) ----------------------------------------------------
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmA) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmB) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmSA) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmSB) : "memory");
+    uint32_t it = 0;
+    bool ok = true;
+    for (int t = pair; ok && t < num_tiles; t += npairs) {
+      const PairTile T = decode_pair<KIND>(t, A, s_off, s_pad, s_pb, cta);
+      for (int ks = 0; ks < T.nk; ++ks, ++it) {
+        const uint32_t s = it % STAGES;
+        if (it >= STAGES &&
+            !wait_pair(smem_u32(&empty[s]), ((it / STAGES) - 1) & 1, A.wait_limit, s_abort, peer_abort, A.status)) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb_local = smem_u32(&full[s]);
+        const uint32_t fb = cta == 0 ? fb_local : mapa_shared(fb_local, 0);
+        if (cta == 0) mbar_arrive_expect_tx(fb_local, 2 * C::STAGE_BYTES);
+        tma_load_2d_pair(smem_u32(sA + s * C::A_BYTES), &tmA, T.k_off + ks * 128, T.a_row, fb);
+        tma_load_2d_pair(smem_u32(sB + s * C::B_BYTES), &tmB, T.k_off + ks * 128, T.b_row, fb);
+        const int64_t katom = T.k_atom0 + (int64_t)ks * C::kAtomsPerStage;
+        tma_load_2d_pair(smem_u32(sSFA + s * C::SFA_BYTES), &tmSA, 0, (int)((T.a_tile * A.ka + katom) * 4), fb);
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+          tma_load_2d_pair(smem_u32(sSFB + s * C::SFB_BYTES + j * C::SFA_BYTES), &tmSB, 0,
+                           (int)(((T.b_tile0 + j) * A.ka + katom) * 4), fb);
+      }
+    }
+    if (cta == 0) {  // the even CTA's barriers count both CTAs' bytes: wait for the last copies
+      const uint32_t first = it > STAGES ? it - STAGES : 0;
+      for (uint32_t k = first; k < it; ++k)
+        if (!mbar_wait(smem_u32(&full[k % STAGES]), (k / STAGES) & 1, A.wait_limit)) {
+          record_error(A.status, NV_ERR_TIMEOUT);
+          break;
+        }
+    }
+  } else if (warp == 1 && lane == 0 && cta == 0) {
+    // ---- MMA issuer (even CTA only) ---------------------------------------------
+    uint32_t it = 0, tc = 0;
+    bool ok = true;
+    for (int t = pair; ok && t < num_tiles; t += npairs, ++tc) {
+      const PairTile T = decode_pair<KIND>(t, A, s_off, s_pad, s_pb, 0);
+      if (tc >= 1 && !wait_pair(smem_u32(acc_empty), (tc - 1) & 1, A.wait_limit, s_abort, peer_abort, A.status))
+        break;
+      tc_fence_after();
+      for (int ks = 0; ks < T.nk; ++ks, ++it) {
+        const uint32_t s = it % STAGES;
+        if (!wait_pair(smem_u32(&full[s]), (it / STAGES) & 1, A.wait_limit, s_abort, peer_abort, A.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sfa = tmem + C::ACC_COLS + s * C::SF_COLS;
+        const uint32_t sfb = sfa + C::SFA_COLS;
+        const uint32_t a_sf_smem = smem_u32(sSFA + s * C::SFA_BYTES);
+        const uint32_t b_sf_smem = smem_u32(sSFB + s * C::SFB_BYTES);
+#pragma unroll
+        for (int j = 0; j < C::kAtomsPerStage; ++j) {
+          tc_cp_sf_pair(sfa + 4 * j, desc_sf(a_sf_smem + j * 512));
+#pragma unroll
+          for (int r = 0; r < 2; ++r)
+            tc_cp_sf_pair(sfb + j * 8 + 4 * r, desc_sf(b_sf_smem + r * C::SFA_BYTES + j * 512));
+        }
+        const uint64_t da = desc_sw128(smem_u32(sA + s * C::A_BYTES));
+        const uint64_t db = desc_sw128(smem_u32(sB + s * C::B_BYTES));
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t accum = (ks | j) != 0;
+          if (C::kFp4) {
+            mma_nvf4_pair(tmem, da + 2 * j, db + 2 * j, C::IDESC, sfa + 4 * j, sfb + j * 8, accum);
+          } else {
+            const uint32_t idesc = C::IDESC | ((uint32_t)j << 4) | ((uint32_t)j << 29);
+            mma_mxf8_pair(tmem, da + 2 * j, db + 2 * j, idesc, sfa, sfb, accum);
+          }
+        }
+        tc_commit_pair(smem_u32(&empty[s]));
+      }
+      tc_commit_pair(smem_u32(acc_full));  // both CTAs: this tile's accumulator is complete
+    }
+  } else if (warp >= 2) {
+    // ---- epilogue (both CTAs): 8 warps, 128 columns each ----------------------------
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int row = q * 32 + lane;
+    const uint32_t acc_empty_addr = cta == 0 ? smem_u32(acc_empty) : mapa_shared(smem_u32(acc_empty), 0);
+    uint32_t tc = 0;
+    for (int t = pair; t < num_tiles; t += npairs, ++tc) {
+      const PairTile T = decode_pair<KIND>(t, A, s_off, s_pad, s_pb, cta);
+      if (!wait_pair(smem_u32(acc_full), tc & 1, A.wait_limit, s_abort, peer_abort, A.status)) break;
+      tc_fence_after();
+      float alpha = 1.0f;
+      if (KIND == kGemmNvfp4Fwd) alpha = __fmul_rn(A.a_sg[0], A.b_sg[T.e]);
+      const bool store = row < T.mrows;
+      const int64_t orow = T.out_row0 + row;
+      const int64_t ocol = T.out_col0 + half * 128;
+      uint32_t r[128];
+      if (T.nk > 0) {
+        const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(half * 128);
+#pragma unroll
+        for (int c0 = 0; c0 < 128; c0 += 32) tmem_ld32_nowait(tb + (uint32_t)c0, &r[c0]);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 128; ++i) r[i] = 0u;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (cta == 0)
+          mbar_arrive(acc_empty_addr);
+        else
+          mbar_arrive_cluster(acc_empty_addr);
+      }
+      if (store) {
+        if (A.out_fp32) {
+          float *dst = static_cast<float *>(A.out) + orow * A.out_ld + ocol;
+#pragma unroll
+          for (int i = 0; i < 128; i += 8) {
+            uint32_t w[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) w[k] = __float_as_uint(__fmul_rn(__uint_as_float(r[i + k]), alpha));
+            st_cs_v8(dst + i, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+          }
+        } else {
+          uint16_t *dst = static_cast<uint16_t *>(A.out) + orow * A.out_ld + ocol;
+#pragma unroll
+          for (int i = 0; i < 128; i += 16) {
+            uint32_t w[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              w[k] = pack_bf16x2(__fmul_rn(__uint_as_float(r[i + 2 * k]), alpha),
+                                 __fmul_rn(__uint_as_float(r[i + 2 * k + 1]), alpha));
+            st_cs_v8(dst + i, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // no CTA leaves while its peer may still signal it or read its shared memory
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, C::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -450,6 +837,20 @@ static bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t 
   cuuint32_t es[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// A scale buffer of `bytes` bytes (a multiple of 512) viewed as rows of 128
+// bytes; one box is `box_rows` rows (4 rows = one 512-byte 128x4 tile).
+static bool make_sf_map(CUtensorMap *m, const void *base, uint64_t bytes, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {128, bytes / 128};
+  cuuint64_t strides[1] = {128};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -480,6 +881,63 @@ static int run(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &arg
   if (grid <= 0) return NV_OK;
   k<<<(unsigned)grid, 192, sm, s>>>(ta, tb, args);
   return cudaGetLastError() == cudaSuccess ? NV_OK : NV_ERR_CUDA;
+}
+
+template <int KIND, int STAGES>
+static int run_pair(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tsa, const CUtensorMap &tsb,
+                    const GemmArgs &args, int64_t max_tiles, cudaStream_t s) {
+  using C = CfgPair<KIND, STAGES>;
+  const size_t sm = C::smem_bytes(args.E);
+  auto k = grouped_gemm_pair_kernel<KIND, STAGES>;
+  static size_t attr_bytes = 0;
+  static int max_pairs = 0;  // co-resident CTA pairs at the largest shared-memory size requested so far
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(C::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = sm;
+  cfg.stream = s;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  if (sm > attr_bytes) {
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) != cudaSuccess)
+      return NV_ERR_CUDA;
+    const int sms = num_sms();
+    if (sms <= 0) return NV_ERR_CUDA;
+    cfg.gridDim = dim3((unsigned)(sms & ~1), 1, 1);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess || n <= 0) return NV_ERR_CUDA;
+    max_pairs = n;
+    attr_bytes = sm;
+  }
+  const int64_t pairs = max_tiles < max_pairs ? max_tiles : max_pairs;
+  if (pairs <= 0) return NV_OK;
+  cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
+  if (cudaLaunchKernelEx(&cfg, k, ta, tb, tsa, tsb, args) != cudaSuccess) return NV_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? NV_OK : NV_ERR_CUDA;
+}
+
+// Which kernel runs a problem: the CTA-pair kernel needs 256-wide output
+// tiles; for fwd and dgrad it pays off only when the experts hold several
+// 128-row blocks each (a half-empty pair tile wastes half of its MMAs).
+static volatile int g_variant = -1;  // -1: not yet read from the environment
+
+static int gemm_variant() {
+  if (g_variant < 0) {
+    const char *e = getenv("NVFP4MOE_GEMM_VARIANT");
+    const int v = e ? atoi(e) : 0;
+    g_variant = (v >= 0 && v <= 3) ? v : 0;
+  }
+  return g_variant;
+}
+
+int set_gemm_variant(int v) {
+  if (v < 0 || v > 3) return NV_ERR_ARG;
+  g_variant = v;
+  return NV_OK;
 }
 
 int launch_grouped_gemm(const GemmProblem &p, int *status, cudaStream_t s) {
@@ -519,12 +977,50 @@ int launch_grouped_gemm(const GemmProblem &p, int *status, cudaStream_t s) {
   } else {
     max_tiles = (P / 128) * a.ntn;
   }
-  // variant 2 (default): two CTAs per SM with one accumulator each (3 stages);
-  // variant 1: one CTA per SM with two accumulators (6 stages)
-  static int forced = -2;
-  if (forced == -2) {
-    const char *e = getenv("NVFP4MOE_GEMM_VARIANT");
-    forced = e ? atoi(e) : -1;
+  // variant 3: CTA pairs with 256 x 256 tiles; variant 2: two CTAs per SM
+  // with one accumulator each (3 stages); variant 1: one CTA per SM with two
+  // accumulators (6 stages).  Default: 3 where it applies (see below), else 2.
+  const int forced = gemm_variant();
+  const int64_t out_rows_per_expert = p.kind == kGemmMxfp8Dw ? p.N : 0;
+  const bool pair_shape = (out_cols % kPairN == 0) && (p.kind != kGemmMxfp8Dw || out_rows_per_expert % 256 == 0);
+  // measured: the pair kernel is faster for the MXFP8 GEMMs; for NVFP4 its
+  // three tensor-memory scale copies per MMA cost more than the tile saves
+  const bool pair_pays = p.kind == kGemmMxfp8Dw || (p.kind == kGemmMxfp8Dx && p.M_total >= (int64_t)512 * p.E);
+  const bool use_pair = pair_shape && (forced == 3 || (forced == 0 && pair_pays));
+  if (use_pair) {
+    const int atoms = p.kind == kGemmNvfp4Fwd ? 4 : 1;
+    uint64_t a_sf_bytes, b_sf_bytes;
+    switch (p.kind) {
+      case kGemmNvfp4Fwd:
+        a_sf_bytes = (uint64_t)(P / 128) * a.ka * 512;
+        b_sf_bytes = (uint64_t)(p.E * p.N / 128) * a.ka * 512;
+        break;
+      case kGemmMxfp8Dx:
+        a_sf_bytes = (uint64_t)(P / 128) * a.ka * 512;
+        b_sf_bytes = (uint64_t)(p.E * p.K / 128) * a.ka * 512;
+        break;
+      default:
+        a_sf_bytes = (uint64_t)(p.N / 128) * a.ka * 512;
+        b_sf_bytes = (uint64_t)(p.K / 128) * a.ka * 512;
+        break;
+    }
+    CUtensorMap tsa, tsb;
+    if (!make_sf_map(&tsa, p.a_scales, a_sf_bytes, 4 * atoms) || !make_sf_map(&tsb, p.b_scales, b_sf_bytes, 4 * atoms))
+      return NV_ERR_CUDA;
+    GemmArgs b = a;
+    b.ntn = (int)(out_cols / kPairN);
+    int64_t pair_tiles;
+    if (p.kind == kGemmMxfp8Dw) {
+      b.ntm = (int)(p.N / 256);
+      pair_tiles = (int64_t)p.E * b.ntm * b.ntn;
+    } else {
+      pair_tiles = ((P / 128 + p.E) / 2) * b.ntn;  // upper bound of sum_e ceil(P_e / 256) tiles
+    }
+    switch (p.kind) {
+      case kGemmNvfp4Fwd: return run_pair<kGemmNvfp4Fwd, 5>(ta, tb, tsa, tsb, b, pair_tiles, s);
+      case kGemmMxfp8Dx: return run_pair<kGemmMxfp8Dx, 6>(ta, tb, tsa, tsb, b, pair_tiles, s);
+      default: return run_pair<kGemmMxfp8Dw, 6>(ta, tb, tsa, tsb, b, pair_tiles, s);
+    }
   }
   const bool two_per_sm = forced != 1;
   switch (p.kind) {

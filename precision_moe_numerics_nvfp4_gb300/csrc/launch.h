@@ -38,5 +38,6 @@ struct GemmProblem {
   int out_fp32;
 };
 int launch_grouped_gemm(const GemmProblem &p, int *status, cudaStream_t s);
+int set_gemm_variant(int v);  // 0 automatic, 1-3 forced (see nvfp4moe_set_gemm_kernel)
 
 }  // namespace nvm

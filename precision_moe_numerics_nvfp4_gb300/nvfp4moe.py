@@ -53,6 +53,7 @@ _SIGS = {
     "nvfp4moe_selftest_wait_timeout": (ctypes.c_int, [_I64, _P]),
     "nvfp4moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "nvfp4moe_version": (ctypes.c_char_p, []),
+    "nvfp4moe_set_gemm_kernel": (ctypes.c_int, [ctypes.c_int]),
 }
 
 
@@ -139,6 +140,15 @@ def status_string(status: int) -> str:
 
 def nvfp4moe_version() -> str:
     return lib().nvfp4moe_version().decode()
+
+
+GEMM_AUTO, GEMM_ONE_PER_SM, GEMM_TWO_PER_SM, GEMM_CTA_PAIR = 0, 1, 2, 3
+
+
+def nvfp4moe_set_gemm_kernel(variant: int) -> None:
+    """Kernel choice of the grouped GEMMs: GEMM_AUTO, GEMM_ONE_PER_SM,
+    GEMM_TWO_PER_SM or GEMM_CTA_PAIR (the pair kernel where the shape allows)."""
+    _check("nvfp4moe_set_gemm_kernel", lib().nvfp4moe_set_gemm_kernel(int(variant)))
 
 
 # ---- the hot path -------------------------------------------------------------

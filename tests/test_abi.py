@@ -45,3 +45,11 @@ def test_status_strings(lib):
     assert N.status_string(0) == "ok"
     assert N.status_string(N.NV_ERR_TIMEOUT) == "bounded wait ran out"
     assert "sm_103a" in N.nvfp4moe_version()
+
+
+def test_gemm_kernel_choice_is_validated(lib):
+    for v in (N.GEMM_ONE_PER_SM, N.GEMM_TWO_PER_SM, N.GEMM_CTA_PAIR, N.GEMM_AUTO):
+        N.nvfp4moe_set_gemm_kernel(v)
+    for bad in (-1, 4, 99):
+        with pytest.raises(N.NvError):
+            N.nvfp4moe_set_gemm_kernel(bad)

@@ -54,9 +54,22 @@ def _fwd(sizes, N_, K, out_fp32=True, seed=0):
     return y, xq, wq, o
 
 
+@pytest.fixture(params=[N.GEMM_TWO_PER_SM, N.GEMM_CTA_PAIR, N.GEMM_ONE_PER_SM],
+                ids=["two_per_sm", "cta_pair", "one_per_sm"])
+def gemm_kernel(request):
+    """Each kernel choice must meet the same bound; shapes whose output width
+    is not a multiple of 256 run the 128 x 128 kernel under every choice."""
+    N.nvfp4moe_set_gemm_kernel(request.param)
+    yield request.param
+    N.nvfp4moe_set_gemm_kernel(N.GEMM_AUTO)
+
+
+# expert sizes cover: one full pair block, half-empty pair blocks (P_e / 128
+# odd), empty experts, a single row, and widths that are not multiples of 256
 @pytest.mark.parametrize("sizes,N_,K", [([256], 1024, 512), ([5, 0, 295, 130], 256, 512), ([1], 256, 256),
-                                        ([200, 77], 384, 2048), ([128, 128, 0], 512, 1536)])
-def test_nvfp4_fwd_within_bound(sizes, N_, K):
+                                        ([200, 77], 384, 2048), ([128, 128, 0], 512, 1536),
+                                        ([0, 700, 1, 0, 129], 768, 768)])
+def test_nvfp4_fwd_within_bound(sizes, N_, K, gemm_kernel):
     y, xq, wq, o = _fwd(sizes, N_, K)
     A = _deq_nvfp4(xq, o)
     B = _deq_nvfp4(wq)
@@ -67,7 +80,7 @@ def test_nvfp4_fwd_within_bound(sizes, N_, K):
     assert ok.all(), f"{(~ok).sum()} of {ok.size} outside the bound; max err {np.abs(y.cpu().numpy() - y_ref).max()}"
 
 
-def test_nvfp4_fwd_bf16_output_and_determinism():
+def test_nvfp4_fwd_bf16_output_and_determinism(gemm_kernel):
     y1, xq, wq, o = _fwd([5, 0, 295, 130], 256, 1024, out_fp32=False, seed=4)
     y2, _, _, _ = _fwd([5, 0, 295, 130], 256, 1024, out_fp32=False, seed=4)
     assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
@@ -96,8 +109,9 @@ def _mx_operands(sizes, Nd, K, seed):
     return go, o, M, E, gr, gt, wt, xt
 
 
-@pytest.mark.parametrize("sizes,Nd,K", [([256], 1024, 512), ([5, 0, 295, 130], 256, 384), ([1, 300], 128, 256)])
-def test_mxfp8_dgrad_and_wgrad_within_bound(sizes, Nd, K):
+@pytest.mark.parametrize("sizes,Nd,K", [([256], 1024, 512), ([5, 0, 295, 130], 256, 384), ([1, 300], 128, 256),
+                                       ([5, 0, 295, 130], 256, 512), ([0, 700, 1, 0, 129], 512, 768)])
+def test_mxfp8_dgrad_and_wgrad_within_bound(sizes, Nd, K, gemm_kernel):
     go, o, M, E, gr, gt, wt, xt = _mx_operands(sizes, Nd, K, seed=len(sizes) + Nd)
     dx = torch.full((M, K), float("nan"), dtype=torch.float32, device=dev())
     dw = torch.full((E, Nd, K), float("nan"), dtype=torch.float32, device=dev())
