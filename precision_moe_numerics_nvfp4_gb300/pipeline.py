@@ -12,6 +12,9 @@ MoELayer       the routed experts of one MoE layer (Figure 5: w13 GEMM, Q,
                w2 GEMM) forward and backward on grouped rows: every step of
                the single layer, for the gate/up (w13) and down (w2)
                projections, with SwiGLU between them.
+HostStaged     MoELayer steps fed from pinned host memory: the copies in of
+               step i+1 and out of step i-1 run on their own streams while
+               step i computes (two device slots per staged tensor).
 """
 from __future__ import annotations
 
@@ -181,8 +184,10 @@ class MoELayer:
         N.grouped_gemm_nvfp4_fwd(None, self.hq.sg, self.hq.codes, self.hq.scales, self.w2q.codes, self.w2q.scales,
                                  self.w2q.sg, groups, E, M, d, I, self.y2, N.NV_OUT_BF16, None, stream)
 
-    def backward(self, g2, groups, seed=3, stream=None):
+    def backward(self, g2, groups, seed=3, stream=None, dx_out=None):
+        """dx goes to `dx_out` when given (bf16 [M][d_model]), else self.dx."""
         M, d, I, E = self.M, self.d, self.I, self.E
+        dx = self.dx if dx_out is None else dx_out
         I2 = 2 * I
         # re-quantize the saved forward tensors (dequantize -> transpose -> SR to MXFP8)
         N.dequant_transpose_requant_sr(self.w13q.codes, self.w13q.scales, self.w13q.sg, E, I2, d, None, seed,
@@ -205,15 +210,78 @@ class MoELayer:
         N.mxfp8_quantize(self.dy13, M, I2, groups, N.NV_SR, seed, OFF_DY13_ROW, OFF_DY13_T, self.dy13_row.codes,
                          self.dy13_row.scales, self.dy13t.codes, self.dy13t.scales, stream)
         N.grouped_gemm_mxfp8_dx(self.dy13_row.codes, self.dy13_row.scales, self.w13t.codes, self.w13t.scales,
-                                groups, E, M, I2, d, self.dx, N.NV_OUT_BF16, None, stream)
+                                groups, E, M, I2, d, dx, N.NV_OUT_BF16, None, stream)
         N.grouped_gemm_mxfp8_dw(self.dy13t.codes, self.dy13t.scales, self.xt.codes, self.xt.scales, groups, E, M,
                                 I2, d, self.dw13, None, stream)
 
-    def step(self, x, w13, w2, g2, groups, seed=3, stream=None):
+    def step(self, x, w13, w2, g2, groups, seed=3, stream=None, dx_out=None):
         self.forward(x, w13, w2, groups, stream)
-        self.backward(g2, groups, seed, stream)
+        self.backward(g2, groups, seed, stream, dx_out)
 
     # kernels one step launches: forward = 4 NVFP4 quantizations x 3 kernels
     # (amax, finalize, quantize) + 2 GEMMs + SwiGLU; backward = 4 requants +
     # 2 MXFP8 quantizations + 4 GEMMs + SwiGLU backward
     LAUNCHES_PER_STEP = (4 * 3 + 2 + 1) + (4 + 2 + 4 + 1)
+
+
+class HostStaged:
+    """MoELayer steps whose activations x and upstream gradient g2 come from
+    pinned host memory and whose dx goes back to pinned host memory.
+
+    Step i copies its inputs into device slot i % 2 on the copy-in stream,
+    computes on the caller's current stream and copies dx out of slot i % 2 on
+    the copy-out stream, so the transfers of neighbouring steps overlap the
+    compute of step i.  Events order every reuse of a slot: the copy into a
+    slot waits until the step that last read it has finished, and a step waits
+    until the copy out of its dx slot (from two steps earlier) has finished.
+    The host buffers must stay untouched until `synchronize()` (or until the
+    copy-out of that step has completed)."""
+
+    def __init__(self, layer: MoELayer, device="cuda"):
+        dev = torch.device(device)
+        M, d = layer.M, layer.d
+        self.layer = layer
+        self.x = [torch.empty((M, d), dtype=BF16, device=dev) for _ in range(2)]
+        self.g2 = [torch.empty((M, d), dtype=BF16, device=dev) for _ in range(2)]
+        self.dx = [torch.empty((M, d), dtype=BF16, device=dev) for _ in range(2)]
+        self.s_in = torch.cuda.Stream(dev)
+        self.s_out = torch.cuda.Stream(dev)
+        self.read_done = [None, None]   # compute of the slot's last step finished
+        self.out_done = [None, None]    # copy-out of the slot's last dx finished
+        self.n = 0
+
+    def bytes_per_step(self):
+        """(host -> device, device -> host) bytes of one step."""
+        b = lambda t: t.numel() * t.element_size()
+        return b(self.x[0]) + b(self.g2[0]), b(self.dx[0])
+
+    def step(self, x_h, g2_h, dx_h, w13, w2, groups, seed=3):
+        k = self.n % 2
+        comp = torch.cuda.current_stream()
+        if self.read_done[k] is not None:
+            self.s_in.wait_event(self.read_done[k])
+        with torch.cuda.stream(self.s_in):
+            self.x[k].copy_(x_h, non_blocking=True)
+            self.g2[k].copy_(g2_h, non_blocking=True)
+        landed = torch.cuda.Event()
+        landed.record(self.s_in)
+        comp.wait_event(landed)
+        if self.out_done[k] is not None:
+            comp.wait_event(self.out_done[k])
+        self.layer.step(self.x[k], w13, w2, self.g2[k], groups, seed, stream=comp, dx_out=self.dx[k])
+        done = torch.cuda.Event()
+        done.record(comp)
+        self.read_done[k] = done
+        self.s_out.wait_event(done)
+        with torch.cuda.stream(self.s_out):
+            dx_h.copy_(self.dx[k], non_blocking=True)
+        out = torch.cuda.Event()
+        out.record(self.s_out)
+        self.out_done[k] = out
+        self.n += 1
+        return out
+
+    def synchronize(self):
+        for e in self.out_done:
+            if e is not None:
+                e.synchronize()
