@@ -52,15 +52,35 @@ __device__ __forceinline__ uint32_t ld_stream_u32(const void *p) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// max of |bf16| over the two halves of four words, as a packed bf16x2
+// max(|a|, |b|) per bf16 half, as a packed bf16x2 whose sign bits are
+// meaningless (max.xorsign.abs: one instruction); read it through |.|.
+// Inputs are finite.
 __device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t a, uint32_t b) {
   uint32_t d;
-  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a & 0x7FFF7FFFu), "r"(b & 0x7FFF7FFFu));
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
 }
 __device__ __forceinline__ float bf16x2_max_to_f32(uint32_t m) {
-  return fmaxf(bf16_lo(m), bf16_hi(m));
+  return fmaxf(fabsf(bf16_lo(m)), fabsf(bf16_hi(m)));
 }
+// fp32(bf16 half * m) for a power-of-two multiplier m given by its bf16 bits:
+// one mixed-precision FMA with addend -0, exact like the fp32 product (the
+// product of an 8-bit and a 1-bit significand is exact; subnormal results are
+// rounded the same way; -0 keeps the product's sign of zero).
+__device__ __forceinline__ float bf16_lo_times(uint32_t w, uint16_t m) {
+  float d;
+  asm("{ .reg .b16 lo, hi;\n\t mov.b32 {lo, hi}, %1;\n\t fma.rn.f32.bf16 %0, lo, %2, %3; }"
+      : "=f"(d) : "r"(w), "h"(m), "f"(-0.0f));
+  return d;
+}
+__device__ __forceinline__ float bf16_hi_times(uint32_t w, uint16_t m) {
+  float d;
+  asm("{ .reg .b16 lo, hi;\n\t mov.b32 {lo, hi}, %1;\n\t fma.rn.f32.bf16 %0, hi, %2, %3; }"
+      : "=f"(d) : "r"(w), "h"(m), "f"(-0.0f));
+  return d;
+}
+// bf16 bits of a power of two held as fp32 (exact)
+__device__ __forceinline__ uint16_t pow2_bf16_bits(float p) { return (uint16_t)(__float_as_uint(p) >> 16); }
 
 // round fp32 -> bf16 (nearest even), returns the 16-bit pattern
 __device__ __forceinline__ uint32_t f32_to_bf16_bits(float x) {
@@ -184,6 +204,34 @@ __device__ __forceinline__ uint4 philox_bits8(uint64_t q, uint64_t seed, uint64_
   return philox4x32_10(make_uint4((uint32_t)q, (uint32_t)(q >> 32), (uint32_t)offset,
                                   (uint32_t)(offset >> 32)),
                        PhiloxKey{(uint32_t)seed, (uint32_t)(seed >> 32)});
+}
+// The same generator with its ten round keys (k0 + r W0, k1 + r W1) computed
+// once on the host and passed in the kernel parameters, so the rounds read
+// them from the parameter bank instead of bumping the key per call.
+struct PhiloxRoundKeys {
+  uint32_t k[10][2];
+};
+inline PhiloxRoundKeys philox_round_keys(uint64_t seed) {
+  PhiloxRoundKeys rk;
+  uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
+  for (int r = 0; r < 10; ++r) {
+    rk.k[r][0] = k0;
+    rk.k[r][1] = k1;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return rk;
+}
+__device__ __forceinline__ uint4 philox_bits8_rk(uint64_t q, uint64_t offset, const PhiloxRoundKeys &rk) {
+  uint4 c = make_uint4((uint32_t)q, (uint32_t)(q >> 32), (uint32_t)offset, (uint32_t)(offset >> 32));
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint64_t p0 = (uint64_t)0xD2511F53u * c.x;
+    const uint64_t p1 = (uint64_t)0xCD9E8D57u * c.z;
+    c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ rk.k[r][0], (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c.w ^ rk.k[r][1],
+                   (uint32_t)p0);
+  }
+  return c;
 }
 // ---------------------------------------------------------------------------
 // Block-scale layout: 128x4 tiles of 512 bytes (see nvfp4moe.h)

@@ -226,6 +226,7 @@ struct MxRowArgs {
   int E;
   int sr;
   uint64_t seed, offset;
+  PhiloxRoundKeys rk;  // round keys of `seed`
   uint8_t *codes, *scales;
   int64_t ka;  // ceil(cols / 128)
   int *status;
@@ -240,13 +241,14 @@ __device__ __forceinline__ uint2 mx_rn8(const float (&v)[8], float mult) {
   return make_uint2(p0 | (p1 << 16), p2 | (p3 << 16));
 }
 
-// SR of 8 consecutive elements of a row with multiplier `mult`; w0 and w1 are
-// the Philox words of their four pairs (pairs 0,1 in w0, pairs 2,3 in w1)
-__device__ __forceinline__ uint2 mx_sr8(const float (&v)[8], float mult, uint32_t w0, uint32_t w1) {
-  return make_uint2(cvt_e4m3x4_sr(__fmul_rn(v[0], mult), __fmul_rn(v[1], mult), __fmul_rn(v[2], mult),
-                                  __fmul_rn(v[3], mult), ~w0),
-                    cvt_e4m3x4_sr(__fmul_rn(v[4], mult), __fmul_rn(v[5], mult), __fmul_rn(v[6], mult),
-                                  __fmul_rn(v[7], mult), ~w1));
+// SR of 8 consecutive bf16 elements of a row (one uint4) with the power-of-two
+// multiplier whose bf16 bits are `m`; w0 and w1 are the Philox words of their
+// four pairs (pairs 0,1 in w0, pairs 2,3 in w1)
+__device__ __forceinline__ uint2 mx_sr8(const uint4 &q, uint16_t m, uint32_t w0, uint32_t w1) {
+  return make_uint2(cvt_e4m3x4_sr(bf16_lo_times(q.x, m), bf16_hi_times(q.x, m), bf16_lo_times(q.y, m),
+                                  bf16_hi_times(q.y, m), ~w0),
+                    cvt_e4m3x4_sr(bf16_lo_times(q.z, m), bf16_hi_times(q.z, m), bf16_lo_times(q.w, m),
+                                  bf16_hi_times(q.w, m), ~w1));
 }
 
 __device__ __forceinline__ void unpack8(const uint4 &q, float (&v)[8]) {
@@ -254,7 +256,7 @@ __device__ __forceinline__ void unpack8(const uint4 &q, float (&v)[8]) {
   v[4] = bf16_lo(q.z); v[5] = bf16_hi(q.z); v[6] = bf16_lo(q.w); v[7] = bf16_hi(q.w);
 }
 
-__global__ void __launch_bounds__(256) mxfp8_rowwise_kernel(MxRowArgs A) {
+__global__ void __launch_bounds__(256) mxfp8_rowwise_kernel(const __grid_constant__ MxRowArgs A) {
   __shared__ __align__(16) uint8_t s_sc[2 * 512];
   __shared__ GroupSmem s_g;
   int E = A.E;
@@ -283,17 +285,18 @@ __global__ void __launch_bounds__(256) mxfp8_rowwise_kernel(MxRowArgs A) {
     // pair keys (e0 / 2) .. (e0 / 2) + 15: two Philox calls, one word per 4 elements
     uint4 bits0 = make_uint4(0, 0, 0, 0), bits1 = make_uint4(0, 0, 0, 0);
     if (A.sr) {
-      bits0 = philox_bits8((uint64_t)(e0 >> 4), A.seed, A.offset);
-      bits1 = philox_bits8((uint64_t)(e0 >> 4) + 1, A.seed, A.offset);
+      bits0 = philox_bits8_rk((uint64_t)(e0 >> 4), A.offset, A.rk);
+      bits1 = philox_bits8_rk((uint64_t)(e0 >> 4) + 1, A.offset, A.rk);
     }
+    const uint16_t mb = pow2_bf16_bits(mult);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      float v[8];
-      unpack8(raw[k], v);
       if (A.sr) {
         const uint4 &b = k < 2 ? bits0 : bits1;
-        out[k] = (k & 1) ? mx_sr8(v, mult, b.z, b.w) : mx_sr8(v, mult, b.x, b.y);
+        out[k] = (k & 1) ? mx_sr8(raw[k], mb, b.z, b.w) : mx_sr8(raw[k], mb, b.x, b.y);
       } else {
+        float v[8];
+        unpack8(raw[k], v);
         out[k] = mx_rn8(v, mult);
       }
     }
@@ -341,6 +344,7 @@ struct MxTArgs {
   int wpb;                           // windows per matrix (batched)
   int sr;
   uint64_t seed, off_t, off_row;
+  PhiloxRoundKeys rk;                // round keys of `seed`
   // transposed output
   uint8_t *out_codes, *out_scales;
   int64_t out_stride;                // P_cap (grouped)
@@ -372,9 +376,10 @@ __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
 }
-__device__ __forceinline__ uint32_t habsmax2(uint32_t a, uint32_t b) {  // max(|a|, |b|) per f16 half
+// max(|a|, |b|) per f16 half; the sign bits of the result are meaningless
+__device__ __forceinline__ uint32_t habsmax2(uint32_t a, uint32_t b) {
   uint32_t d;
-  asm("max.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a & 0x7FFF7FFFu), "r"(b & 0x7FFF7FFFu));
+  asm("max.xorsign.abs.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
 }
 __device__ __forceinline__ float f16_lo(uint32_t w) {
@@ -396,7 +401,7 @@ __device__ __forceinline__ uint32_t e4m3_to_f16x2_dup(uint32_t code) {
 }
 
 template <bool kNvfp4>
-__global__ void __launch_bounds__(256) mx_transpose_kernel(MxTArgs A) {
+__global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant__ MxTArgs A) {
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ GroupSmem s_g;
   __shared__ __align__(16) uint8_t s_tsc[512];   // transposed scale tile
@@ -453,15 +458,16 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(MxTArgs A) {
           if (valid) {
             float mult;
             const uint32_t sc = e8m0_scale(bf16x2_max_to_f32(m), &mult);
-            float v0[8], v1[8];
-            unpack8(raw[u][0], v0);
-            unpack8(raw[u][1], v1);
             uint2 o0, o1;
             if (A.sr) {
-              const uint4 b = philox_bits8((uint64_t)(e0 >> 4), A.seed, A.off_row);  // pair keys e0/2 .. e0/2+7
-              o0 = mx_sr8(v0, mult, b.x, b.y);
-              o1 = mx_sr8(v1, mult, b.z, b.w);
+              const uint4 b = philox_bits8_rk((uint64_t)(e0 >> 4), A.off_row, A.rk);  // pair keys e0/2 .. e0/2+7
+              const uint16_t mb = pow2_bf16_bits(mult);
+              o0 = mx_sr8(raw[u][0], mb, b.x, b.y);
+              o1 = mx_sr8(raw[u][1], mb, b.z, b.w);
             } else {
+              float v0[8], v1[8];
+              unpack8(raw[u][0], v0);
+              unpack8(raw[u][1], v1);
               o0 = mx_rn8(v0, mult);
               o1 = mx_rn8(v1, mult);
             }
@@ -525,8 +531,8 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(MxTArgs A) {
     uint4 ba = make_uint4(0, 0, 0, 0), bb = make_uint4(0, 0, 0, 0);
     if (A.sr && 4 * lane < w.nvalid) {
       const int64_t ka = (w.src_row0 + 4 * lane) * A.cols + col0 + c8 * 8;
-      ba = philox_bits8((uint64_t)(ka >> 3), A.seed, A.off_t);
-      bb = philox_bits8((uint64_t)((ka + 2 * A.cols) >> 3), A.seed, A.off_t);
+      ba = philox_bits8_rk((uint64_t)(ka >> 3), A.off_t, A.rk);
+      bb = philox_bits8_rk((uint64_t)((ka + 2 * A.cols) >> 3), A.off_t, A.rk);
     }
     uint32_t m[4];
 #pragma unroll
@@ -551,9 +557,9 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(MxTArgs A) {
       float amax, mult;
       if (kNvfp4) {
         // max_i fp32(p_i * sg) = fp32(max_i p_i * sg): rounding is monotonic
-        amax = __fmul_rn((k_own & 1) ? f16_hi(mp) : f16_lo(mp), sg);
+        amax = __fmul_rn(fabsf((k_own & 1) ? f16_hi(mp) : f16_lo(mp)), sg);
       } else {
-        amax = (k_own & 1) ? bf16_hi(mp) : bf16_lo(mp);
+        amax = fabsf((k_own & 1) ? bf16_hi(mp) : bf16_lo(mp));
       }
       const uint32_t sc = e8m0_scale(amax, &mult);
       // NVFP4: fp32(fp32(p * sg) * 2^-s) == fp32(p * (sg * 2^-s)) for the
@@ -568,11 +574,13 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(MxTArgs A) {
       const float m2 = __shfl_sync(0xFFFFFFFFu, m2_own, (lane & ~7) | k);
       const int p = k >> 1, h = k & 1;
       float x[4];
+      if (kNvfp4) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float val = kNvfp4 ? (h ? f16_hi(v[j][p]) : f16_lo(v[j][p]))
-                                 : (h ? bf16_hi(v[j][p]) : bf16_lo(v[j][p]));
-        x[j] = __fmul_rn(val, m2);
+        for (int j = 0; j < 4; ++j) x[j] = __fmul_rn(h ? f16_hi(v[j][p]) : f16_lo(v[j][p]), m2);
+      } else {  // m2 is a power of two: one mixed-precision FMA per value
+        const uint16_t mb = pow2_bf16_bits(m2);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) x[j] = h ? bf16_hi_times(v[j][p], mb) : bf16_lo_times(v[j][p], mb);
       }
       uint32_t packed;
       if (A.sr) {
@@ -650,6 +658,7 @@ int launch_mxfp8_rowwise(const uint16_t *x, int64_t rows, int64_t cols, const in
                          uint64_t seed, uint64_t off, uint8_t *codes, uint8_t *scales, int *status, cudaStream_t s) {
   MxRowArgs A;
   A.x = x; A.rows = rows; A.cols = cols; A.groups = groups; A.E = E; A.sr = sr; A.seed = seed; A.offset = off;
+  A.rk = philox_round_keys(seed);
   A.codes = codes; A.scales = scales; A.ka = (cols / 32 + 3) / 4; A.status = status;
   const int64_t P = groups ? nvfp4moe_padded_cap(rows, E) : ((rows + 127) / 128) * 128;
   const int64_t nwin = P / 128, nchunk = (cols / 32 + 7) / 8;
@@ -666,6 +675,7 @@ int launch_mx_transpose_bf16(const uint16_t *x, int64_t rows, int64_t cols, cons
   MxTArgs A = {};
   A.x = x; A.rows = rows; A.cols = cols; A.groups = groups; A.E = E; A.grouped = 1; A.sr = sr;
   A.seed = seed; A.off_t = off_t; A.off_row = off_row;
+  A.rk = philox_round_keys(seed);
   const int64_t P = groups ? nvfp4moe_padded_cap(rows, E) : ((rows + 127) / 128) * 128;
   A.out_codes = codes_t; A.out_scales = scales_t; A.out_stride = P; A.out_ka = P / 128;
   A.row_codes = codes_row; A.row_scales = scales_row; A.row_ka = cols / 128;
@@ -687,6 +697,7 @@ int launch_requant(const uint8_t *codes, const uint8_t *scales, const float *sg,
   MxTArgs A = {};
   A.nv_codes = codes; A.nv_scales = scales; A.nv_sg = sg; A.rows = rows; A.cols = cols; A.groups = groups; A.E = E;
   A.sr = 1; A.seed = seed; A.off_t = off; A.status = status;
+  A.rk = philox_round_keys(seed);
   A.out_codes = out_codes; A.out_scales = out_scales;
   int64_t nwin;
   if (groups) {
