@@ -54,6 +54,43 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 NOMINAL_RATIO = {"bf16": 1.0, "fp8": 4.5 / 2.25, "fp4": 13.5 / 2.25}
 
 
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic_moe_layer_fwd_bwd.txt")
+
+
+def source_digest():
+    """sha256 over the library's CUDA sources and its header: DRAM counters
+    taken from an older build no longer describe the kernels."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "precision_moe_numerics_nvfp4_gb300", "csrc")
+    files = sorted(os.path.join(csrc, f) for f in os.listdir(csrc) if f.endswith((".cu", ".cuh", ".h")))
+    for f in files + [os.path.join(ROOT, "include", "nvfp4moe.h")]:
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def measured_traffic(entry_point):
+    """DRAM bytes (read + write) per launch of `entry_point` in the MoE step,
+    averaged over its calls, from the committed one-pass ncu capture; None
+    when the capture is missing or was taken from different sources."""
+    try:
+        with open(TRAFFIC_FILE) as fh:
+            lines = fh.read().splitlines()
+    except OSError:
+        return None
+    digest = next((l.split(":", 1)[1].strip() for l in lines if l.startswith("# source-sha256:")), None)
+    if digest != source_digest():
+        return None
+    vals = []
+    for l in lines:
+        f = l.split()
+        if len(f) == 4 and not l.startswith("#") and f[0] == entry_point:
+            vals.append(int(f[2]) + int(f[3]))
+    return sum(vals) / len(vals) if vals else None
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -303,6 +340,8 @@ def run_ours(args):
         kernels[name] = entry
     dom = max(kernels, key=lambda k: kernels[k]["ms_per_step"])
     roof = roofline_of(dom, per[dom], units[dom], args.steps, peaks)
+    roof["traffic"] = measured_traffic(dom)
+    roof["traffic_unit"] = "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum), null if stale"
 
     # e2e through host buffers: x and g2 in, dx out, every step; the copies of
     # neighbouring steps overlap the compute (pipeline.HostStaged)
