@@ -409,18 +409,18 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant
   uint8_t *s_out = smem;                                  // [128][128] output bytes
   uint8_t *s_in = smem + 128 * kTileOutStride;            // [128][256 B] 16-bit values
 
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // the row-wise scale tile keeps zeros for rows without data; cleared before
+  // the barrier below so that no phase-1 write can precede the clearing
+  if (tid < 128) reinterpret_cast<uint32_t *>(s_rsc)[tid] = 0u;
+  __syncthreads();
   int E = A.E;
   if (A.grouped) {
     if (!setup_groups(s_g, A.groups, E, A.rows, A.status)) return;
   }
   const Window w = map_window(A.grouped != 0, blockIdx.y, E, s_g.off, s_g.pad, A.rows, A.wpb);
   const int64_t col0 = (int64_t)blockIdx.x * 128;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const float sg = kNvfp4 ? A.nv_sg[A.grouped ? 0 : w.seg] : 1.0f;
-  if (tid < 128) {
-    reinterpret_cast<uint32_t *>(s_tsc)[tid] = 0u;
-    reinterpret_cast<uint32_t *>(s_rsc)[tid] = 0u;
-  }
 
   // ---- phase 1 --------------------------------------------------------------
   if (!kNvfp4) {
