@@ -260,6 +260,9 @@ def kernel_units(layer, m):
     return {
         # a call = the amax pass (2 B/elem) + the quantize pass (2 + 0.5 + 1/16 B/elem)
         "nvfp4_quantize": [(E * 2 * I * d, 4.5625), (E * d * I, 4.5625), (M * d, 4.5625), (M * I, 4.5625)],
+        # amax pass (2) + one pass reading bf16 (2) and writing NVFP4 (0.5 + 1/16) and MXFP8 (1 + 1/32)
+        "nvfp4_quantize_requant": [(E * 2 * I * d, 5.59375), (E * d * I, 5.59375), (M * d, 5.59375),
+                                   (M * I, 5.59375)],
         "grouped_gemm_nvfp4_fwd": [fl13, fl2],
         "dequant_transpose_requant_sr": [(E * 2 * I * d, 1.59375), (E * d * I, 1.59375), (M * d, 1.59375),
                                          (M * I, 1.59375)],
@@ -385,7 +388,7 @@ def run_ours(args):
         "e2e": {"value": aggregate(step_flops / 1e12, e2e_ms / 1e3, world), "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "overlap": "copies in (step i+1) and out (step i-1) on their own streams during step i"},
-        "gpu_launches": MoELayer.LAUNCHES_PER_STEP * args.steps,
+        "gpu_launches": layer.launches_per_step() * args.steps,
         "peaks": peaks,
         "cpu_baseline": cpu,
     }
@@ -521,7 +524,10 @@ def run_quant_sweep(args):
                                                            None, None), 3.03125),
             "dequant_transpose_requant_sr": (lambda: N.dequant_transpose_requant_sr(
                 nv.codes, nv.scales, nv.sg, 1, R, C, None, 1, 0, mt.codes, mt.scales), 1.59375),
-            # not an op of the sweep: the gradient's SR quantization (row-wise + transposed) on the same tensor
+            # not ops of the sweep: NVFP4 quantize + requant in one pass, and the gradient's SR
+            # quantization (row-wise + transposed), on the same tensor
+            "nvfp4_quantize_requant": (lambda: N.nvfp4_quantize_requant(
+                x, 1, R, C, None, None, nv.sg, nv.codes, nv.scales, nv.ws, 1, 0, mt.codes, mt.scales), 5.59375),
             "mxfp8_quantize_sr_dual": (lambda: N.mxfp8_quantize(x, R, C, None, N.NV_SR, 0, 0, 1, mr.codes, mr.scales,
                                                                 mt2.codes, mt2.scales), 4.0625),
         }

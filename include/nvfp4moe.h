@@ -218,6 +218,29 @@ int dequant_transpose_requant_sr(const uint8_t *codes, const uint8_t *scales,
                                  uint8_t *out_codes, uint8_t *out_scales,
                                  nv_stream_t stream);
 
+/* ---- a2 + a5 in one pass: NVFP4 quantize and the SR re-quantization ----------
+ * Both outputs of nvfp4_quantize (codes, scales, outer scale) and of
+ * dequant_transpose_requant_sr applied to them (same seed and counter
+ * offset), bit-identical to the two calls in sequence, from one read of the
+ * bf16 source: each 128 x 128 tile is quantized to NVFP4 with the block rule
+ * of nvfp4_quantize, and the exact products e2m1 * e4m3 of the codes just
+ * made feed the transposed stochastic rounding.  For a training step this
+ * produces the backward's MXFP8 operand already in the forward pass.
+ * No counterpart on the pages as a single operation (a fusion of the two).
+ *
+ * Arguments: those of nvfp4_quantize, then seed, counter_offset, out_codes,
+ * out_scales of dequant_transpose_requant_sr (its layouts).  cols % 128 == 0;
+ * batched (group_offsets NULL): rows % 128 == 0.  With outer_scale_in NULL
+ * the amax pass runs first (workspace as nvfp4_quantize).
+ */
+int nvfp4_quantize_requant(const void *x, int64_t batch, int64_t rows, int64_t cols,
+                           const int32_t *group_offsets, int32_t num_groups,
+                           const float *outer_scale_in, float *outer_scale_out,
+                           uint8_t *codes, uint8_t *scales,
+                           void *workspace, size_t workspace_bytes,
+                           uint64_t seed, uint64_t counter_offset,
+                           uint8_t *out_codes, uint8_t *out_scales, nv_stream_t stream);
+
 /* ---- a3: grouped NVFP4 forward GEMM  y_e = x_q,e w_q,e^T ----------------------
  * "Block-scaled backward passes": y = x_q w_q^T, 16-value blocks of a row of
  * x_q and of w_q multiplied pairwise and scaled by both block scales; the

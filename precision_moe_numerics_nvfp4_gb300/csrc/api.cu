@@ -123,6 +123,41 @@ int nvfp4_quantize(const void *x, int64_t batch, int64_t rows, int64_t cols, con
                             scales, st, s);
 }
 
+int nvfp4_quantize_requant(const void *x, int64_t batch, int64_t rows, int64_t cols, const int32_t *group_offsets,
+                           int32_t num_groups, const float *outer_scale_in, float *outer_scale_out, uint8_t *codes,
+                           uint8_t *scales, void *workspace, size_t workspace_bytes, uint64_t seed,
+                           uint64_t counter_offset, uint8_t *out_codes, uint8_t *out_scales, nv_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!x || !codes || !scales || !out_codes || !out_scales || batch < 1 || rows < 0 || cols < 0) return NV_ERR_ARG;
+  if (group_offsets && (batch != 1 || num_groups < 1 || num_groups > kMaxGroups)) return NV_ERR_ARG;
+  if (cols % 128) return NV_ERR_SHAPE;
+  if (!group_offsets && rows % 128) return NV_ERR_SHAPE;
+  if (!al16(x) || !al16(codes) || !al16(scales) || !al16(out_codes) || !al16(out_scales) || !al16(group_offsets))
+    return NV_ERR_ALIGN;
+  if (rows == 0 || cols == 0) return NV_OK;
+  if (rows >= (int64_t)1 << 30 || rows * cols / 16 >= (int64_t)1 << 31) return NV_ERR_SHAPE;
+  int *st = status_ptr();
+  if (!st) return NV_ERR_CUDA;
+  const float *sg = outer_scale_in;
+  if (!outer_scale_in) {
+    const size_t need = nvfp4moe_quantize_workspace_bytes(batch, rows, cols);
+    if (!workspace || workspace_bytes < need || !al16(workspace)) return NV_ERR_WORKSPACE;
+    const int nb = amax_blocks(rows * cols);
+    float *partial = static_cast<float *>(workspace);
+    float *dst = outer_scale_out ? outer_scale_out : partial + batch * nb;
+    int r = launch_amax(static_cast<const uint16_t *>(x), batch, rows * cols, partial, nb, dst, s);
+    if (r != NV_OK) return r;
+    sg = dst;
+  } else if (outer_scale_out && outer_scale_out != outer_scale_in) {
+    if (cudaMemcpyAsync(outer_scale_out, outer_scale_in, batch * sizeof(float), cudaMemcpyDeviceToDevice, s) !=
+        cudaSuccess)
+      return NV_ERR_CUDA;
+  }
+  return launch_nvfp4_requant(static_cast<const uint16_t *>(x), sg, batch, rows, cols, group_offsets,
+                              group_offsets ? num_groups : 0, codes, scales, seed, counter_offset, out_codes,
+                              out_scales, st, s);
+}
+
 int mxfp8_quantize(const void *x, int64_t rows, int64_t cols, const int32_t *group_offsets, int32_t num_groups,
                    int mode, uint64_t seed, uint64_t counter_offset_row, uint64_t counter_offset_t,
                    uint8_t *codes_row, uint8_t *scales_row, uint8_t *codes_t, uint8_t *scales_t,

@@ -524,10 +524,41 @@ struct CfgPair {
   static constexpr uint32_t IDESC = (kFp4 ? ((1u << 7) | (1u << 10)) : (1u << 23)) |
                                     ((uint32_t)(kPairN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
   static size_t smem_bytes(int E) {
-    return 1024 + (size_t)STAGES * STAGE_BYTES + NBARS * 8 + 32 + (size_t)(E + 1) * 12 + 64;
+    return 1024 + (size_t)STAGES * STAGE_BYTES + NBARS * 8 + 32 + (size_t)(E + 1) * 16 + 64;
   }
   static_assert(TMEM_COLS <= 512, "tensor memory");
 };
+
+// Wgrad tile order.  Every expert writes its whole fp32 dW (the same bytes
+// whatever its token count) while its MMA time grows with its tokens, so a
+// small expert's tiles are store-bound and a large one's MMA-bound.  The
+// schedule interleaves the two: D lists the tiles expert by expert in
+// decreasing padded token count; position i of the processing order takes
+// D[i / 2] for even i and D[T - 1 - i / 2] for odd i (largest and smallest
+// experts alternate), and with an even number of pairs every other round is
+// walked in reverse so that each pair alternates between the two kinds.
+// Only two experts' operands are live at a time, as before.
+__device__ __forceinline__ int dw_sorted_index(int t, int pair, int npairs, int T) {
+  const int r = t / npairs;
+  int x = t;
+  if ((npairs & 1) == 0 && (r & 1) && (r + 1) * npairs <= T) x = r * npairs + (npairs - 1 - pair);
+  return (x & 1) ? T - 1 - (x >> 1) : (x >> 1);
+}
+
+// s_ord[k]: the expert with the k-th largest padded token count (ties: lower
+// index first).  Every thread of the CTA must call it.
+__device__ inline void sort_experts_by_size(const int *s_pad, int E, int *s_ord) {
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int pe = s_pad[e + 1] - s_pad[e];
+    int rank = 0;
+    for (int f = 0; f < E; ++f) {
+      const int pf = s_pad[f + 1] - s_pad[f];
+      rank += (pf > pe) || (pf == pe && f < e);
+    }
+    s_ord[rank] = e;
+  }
+  __syncthreads();
+}
 
 // One pair tile, seen from CTA `cta` (0 or 1) of the pair.
 struct PairTile {
@@ -536,10 +567,12 @@ struct PairTile {
   int64_t a_tile, b_tile0, k_atom0, out_row0, out_col0;
 };
 
-// s_pb[e]: number of 256-row pair blocks before expert e (fwd, dgrad)
+// s_pb[e]: number of 256-row pair blocks before expert e (fwd, dgrad);
+// s_ord: experts by decreasing size (wgrad)
 template <int KIND>
 __device__ __forceinline__ PairTile decode_pair(int t, const GemmArgs &A, const int *s_off, const int *s_pad,
-                                                const int *s_pb, int cta) {
+                                                const int *s_pb, const int *s_ord, int pair, int npairs,
+                                                int num_tiles, int cta) {
   PairTile T;
   if (KIND != kGemmMxfp8Dw) {
     const int pm = t / A.ntn, nt = t - (t / A.ntn) * A.ntn;
@@ -562,8 +595,10 @@ __device__ __forceinline__ PairTile decode_pair(int t, const GemmArgs &A, const 
     T.out_col0 = (int64_t)nt * kPairN;
   } else {
     const int per_e = A.ntm * A.ntn;
-    const int e = t / per_e;
-    const int r = t - e * per_e, mt = r / A.ntn, nt = r - (r / A.ntn) * A.ntn;
+    const int d = dw_sorted_index(t, pair, npairs, num_tiles);
+    const int k = d / per_e;
+    const int e = s_ord[k];
+    const int r = d - k * per_e, mt = r / A.ntn, nt = r - (r / A.ntn) * A.ntn;
     T.e = e;
     T.a_row = mt * 256 + 128 * cta;
     T.b_row = nt * kPairN + 128 * cta;
@@ -633,6 +668,7 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES>::kThreads, 1)
   int *s_off = s_flag + 2;
   int *s_pad = s_off + (A.E + 1);
   int *s_pb = s_pad + (A.E + 1);
+  int *s_ord = s_pb + (A.E + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cta = (int)cluster_ctarank();
@@ -640,6 +676,7 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES>::kThreads, 1)
   // identical in both CTAs of the pair, so an early return is taken by both
   if (!load_groups(A.groups, A.E, A.M_total, s_off, s_pad, s_flag, A.status)) return;
   scan_pair_blocks(s_pad, A.E, s_pb);
+  if (KIND == kGemmMxfp8Dw) sort_experts_by_size(s_pad, A.E, s_ord);
   const int num_tiles = KIND == kGemmMxfp8Dw ? A.E * A.ntm * A.ntn : s_pb[A.E] * A.ntn;
   if (pair >= num_tiles) return;
 
@@ -671,7 +708,7 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES>::kThreads, 1)
     uint32_t it = 0;
     bool ok = true;
     for (int t = pair; ok && t < num_tiles; t += npairs) {
-      const PairTile T = decode_pair<KIND>(t, A, s_off, s_pad, s_pb, cta);
+      const PairTile T = decode_pair<KIND>(t, A, s_off, s_pad, s_pb, s_ord, pair, npairs, num_tiles, cta);
       for (int ks = 0; ks < T.nk; ++ks, ++it) {
         const uint32_t s = it % STAGES;
         if (it >= STAGES &&
@@ -705,7 +742,7 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES>::kThreads, 1)
     uint32_t it = 0, tc = 0;
     bool ok = true;
     for (int t = pair; ok && t < num_tiles; t += npairs, ++tc) {
-      const PairTile T = decode_pair<KIND>(t, A, s_off, s_pad, s_pb, 0);
+      const PairTile T = decode_pair<KIND>(t, A, s_off, s_pad, s_pb, s_ord, pair, npairs, num_tiles, 0);
       if (tc >= 1 && !wait_pair(smem_u32(acc_empty), (tc - 1) & 1, A.wait_limit, s_abort, peer_abort, A.status))
         break;
       tc_fence_after();
@@ -751,7 +788,7 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES>::kThreads, 1)
     const uint32_t acc_empty_addr = cta == 0 ? smem_u32(acc_empty) : mapa_shared(smem_u32(acc_empty), 0);
     uint32_t tc = 0;
     for (int t = pair; t < num_tiles; t += npairs, ++tc) {
-      const PairTile T = decode_pair<KIND>(t, A, s_off, s_pad, s_pb, cta);
+      const PairTile T = decode_pair<KIND>(t, A, s_off, s_pad, s_pb, s_ord, pair, npairs, num_tiles, cta);
       if (!wait_pair(smem_u32(acc_full), tc & 1, A.wait_limit, s_abort, peer_abort, A.status)) break;
       tc_fence_after();
       float alpha = 1.0f;

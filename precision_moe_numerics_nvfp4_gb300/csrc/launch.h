@@ -21,6 +21,9 @@ int launch_mx_transpose_bf16(const uint16_t *x, int64_t rows, int64_t cols, cons
 int launch_requant(const uint8_t *codes, const uint8_t *scales, const float *sg, int64_t batch, int64_t rows,
                    int64_t cols, const int32_t *groups, int E, uint64_t seed, uint64_t off, uint8_t *out_codes,
                    uint8_t *out_scales, int *status, cudaStream_t s);
+int launch_nvfp4_requant(const uint16_t *x, const float *sg, int64_t batch, int64_t rows, int64_t cols,
+                         const int32_t *groups, int E, uint8_t *codes, uint8_t *scales, uint64_t seed, uint64_t off,
+                         uint8_t *out_codes, uint8_t *out_scales, int *status, cudaStream_t s);
 int launch_swiglu_fwd(const uint16_t *y13, int64_t M, int64_t I, uint16_t *h, cudaStream_t s);
 int launch_swiglu_bwd(const uint16_t *dh, const uint16_t *y13, int64_t M, int64_t I, uint16_t *dy13, cudaStream_t s);
 int launch_wait_selftest(int64_t spins, int *status, cudaStream_t s);

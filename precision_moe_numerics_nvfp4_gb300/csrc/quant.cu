@@ -318,7 +318,14 @@ __global__ void __launch_bounds__(256) mxfp8_rowwise_kernel(const __grid_constan
 
 // ---------------------------------------------------------------------------
 // Transposed MXFP8 (a5 and the WGRAD operand of a6): one CTA = 128 padded
-// source rows (one window) x 128 source columns.
+// source rows (one window) x 128 source columns.  Three sources (kMode):
+//   kSrcBf16        bf16 -> MXFP8 SR/RN, transposed (+ optional row-wise)
+//   kSrcNvfp4       NVFP4 codes + scales + outer scale -> dequantize ->
+//                   transposed SR to MXFP8 (the re-quantization)
+//   kSrcBf16ToNvfp4 bf16 -> NVFP4 (codes, scales; the quantizer's block rule)
+//                   and, from the codes just made, the same re-quantization:
+//                   both outputs of nvfp4_quantize + dequant_transpose_
+//                   requant_sr in one pass over the source
 //   phase 1  stream the tile into shared memory as 16-bit values: bf16 input
 //            as is, NVFP4 input as the exact f16 products e2m1 * e4m3 (at most
 //            6 significant bits, inside the f16 range); optionally emit the
@@ -331,12 +338,17 @@ __global__ void __launch_bounds__(256) mxfp8_rowwise_kernel(const __grid_constan
 // which makes both the row-wise fill and the 4-tokens-per-lane column reads
 // bank-conflict free.
 // ---------------------------------------------------------------------------
+enum { kSrcBf16 = 0, kSrcNvfp4 = 1, kSrcBf16ToNvfp4 = 2 };
+
 struct MxTArgs {
   // input
-  const uint16_t *x;                 // bf16 source (kNvfp4 == false)
-  const uint8_t *nv_codes;           // NVFP4 source (kNvfp4 == true)
+  const uint16_t *x;                 // bf16 source (kSrcBf16, kSrcBf16ToNvfp4)
+  const uint8_t *nv_codes;           // NVFP4 source (kSrcNvfp4)
   const uint8_t *nv_scales;
-  const float *nv_sg;                // [batch] (batched) or [1]
+  const float *nv_sg;                // outer scale: [batch] (batched) or [1]
+  // NVFP4 output (kSrcBf16ToNvfp4)
+  uint8_t *nv_codes_out, *nv_scales_out;
+  int64_t nv_ka;                     // NVFP4 scale tiles per 128 rows = cols / 64
   int64_t rows, cols;                // rows per matrix (batched) or total rows
   const int32_t *groups;             // grouped mode when non-null or `single`
   int E;
@@ -400,20 +412,36 @@ __device__ __forceinline__ uint32_t e4m3_to_f16x2_dup(uint32_t code) {
   return h2;
 }
 
-template <bool kNvfp4>
+// the 16 exact f16 products e2m1 * e4m3 of one (row i, 16-column block kb)
+// unit into the swizzled 16-bit tile
+__device__ __forceinline__ void store_f16_products(uint8_t *s_in, int i, int kb, uint2 codes, uint32_t scale) {
+  const uint32_t s2 = e4m3_to_f16x2_dup(scale);
+  uint32_t h0[4], h1[4];
+  e2m1x8_to_f16x2(codes.x, h0);
+  e2m1x8_to_f16x2(codes.y, h1);
+  uint4 *row = reinterpret_cast<uint4 *>(s_in + i * 256);
+  row[chunk_of(i, 2 * kb)] =
+      make_uint4(hmul2_u32(h0[0], s2), hmul2_u32(h0[1], s2), hmul2_u32(h0[2], s2), hmul2_u32(h0[3], s2));
+  row[chunk_of(i, 2 * kb + 1)] =
+      make_uint4(hmul2_u32(h1[0], s2), hmul2_u32(h1[1], s2), hmul2_u32(h1[2], s2), hmul2_u32(h1[3], s2));
+}
+
+template <int kMode>
 __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant__ MxTArgs A) {
+  constexpr bool kNvfp4 = kMode != kSrcBf16;  // phase 2 on exact f16 products of NVFP4 values
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ GroupSmem s_g;
   __shared__ __align__(16) uint8_t s_tsc[512];   // transposed scale tile
   __shared__ __align__(16) uint8_t s_rsc[512];   // row-wise scale tile
+  __shared__ __align__(16) uint8_t s_nvsc[kMode == kSrcBf16ToNvfp4 ? 1024 : 16];  // NVFP4 scale tiles
   uint8_t *s_out = smem;                                  // [128][128] output bytes
   uint8_t *s_in = smem + 128 * kTileOutStride;            // [128][256 B] 16-bit values
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // the row-wise scale tile keeps zeros for rows without data; cleared before
-  // the barrier below so that no phase-1 write can precede the clearing
-  if (tid < 128) reinterpret_cast<uint32_t *>(s_rsc)[tid] = 0u;
-  __syncthreads();
+  // the row-wise scale tile (bf16 source, always grouped) keeps zeros for rows
+  // without data; the barriers of the group setup order this clearing before
+  // any phase-1 write
+  if (kMode == kSrcBf16 && tid < 128) reinterpret_cast<uint32_t *>(s_rsc)[tid] = 0u;
   int E = A.E;
   if (A.grouped) {
     if (!setup_groups(s_g, A.groups, E, A.rows, A.status)) return;
@@ -477,7 +505,7 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant
         }
       }
     }
-  } else {
+  } else if (kMode == kSrcNvfp4) {
     // NVFP4: (row, 16-column block) pairs; 8 code bytes + 1 scale byte each
     const int64_t half_cols = A.cols >> 1;
     const int64_t ka_src = (A.cols + 63) >> 6;
@@ -499,15 +527,39 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant
     for (int u = 0; u < 4; ++u) {
       const int q = u * 256 + tid;
       const int i = q >> 3, kb = q & 7;
-      const uint32_t s2 = e4m3_to_f16x2_dup(sc[u]);
-      uint32_t h0[4], h1[4];
-      e2m1x8_to_f16x2(raw[u].x, h0);
-      e2m1x8_to_f16x2(raw[u].y, h1);
-      uint4 *row = reinterpret_cast<uint4 *>(s_in + i * 256);
-      row[chunk_of(i, 2 * kb)] =
-          make_uint4(hmul2_u32(h0[0], s2), hmul2_u32(h0[1], s2), hmul2_u32(h0[2], s2), hmul2_u32(h0[3], s2));
-      row[chunk_of(i, 2 * kb + 1)] =
-          make_uint4(hmul2_u32(h1[0], s2), hmul2_u32(h1[1], s2), hmul2_u32(h1[2], s2), hmul2_u32(h1[3], s2));
+      store_f16_products(s_in, i, kb, raw[u], sc[u]);
+    }
+  } else {
+    // bf16 -> NVFP4 with the quantizer's block rule (nvfp4_block), codes to
+    // global memory, scales to the shared tile; then the exact f16 products
+    // of the new codes for phase 2
+    const float den6 = __fmul_rn(6.0f, sg);
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      uint4 va[2], vb[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {  // the half's loads in flight together
+        const int q = (half * 2 + u) * 256 + tid;
+        const int i = q >> 3, kb = q & 7;
+        va[u] = vb[u] = make_uint4(0, 0, 0, 0);
+        if (i < w.nvalid) {
+          const uint16_t *src = A.x + (w.src_row0 + i) * A.cols + col0 + kb * 16;
+          va[u] = ld_stream_v4(src);
+          vb[u] = ld_stream_v4(src + 8);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int q = (half * 2 + u) * 256 + tid;
+        const int i = q >> 3, kb = q & 7;
+        uint2 c;
+        uint32_t sc;
+        nvfp4_block(va[u], vb[u], sg, den6, c, sc);  // an all-zero (padding) block gives scale 0 and zero codes
+        if (i < w.nvalid)
+          *reinterpret_cast<uint2 *>(A.nv_codes_out + ((w.src_row0 + i) * A.cols + col0 + kb * 16) / 2) = c;
+        s_nvsc[(kb >> 2) * 512 + atom_pos(i, kb)] = (uint8_t)sc;
+        store_f16_products(s_in, i, kb, c, sc);
+      }
     }
   }
   __syncthreads();
@@ -626,6 +678,9 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant
   } else if (tid < 64 && A.row_codes != nullptr) {  // zero tiles for padding windows too
     reinterpret_cast<uint4 *>(A.row_scales + ((w.rp0 >> 7) * A.row_ka + (col0 >> 7)) * 512)[tid - 32] =
         reinterpret_cast<const uint4 *>(s_rsc)[tid - 32];
+  } else if (kMode == kSrcBf16ToNvfp4 && tid >= 64 && tid < 128) {  // the two NVFP4 tiles (zeros for padding)
+    reinterpret_cast<uint4 *>(A.nv_scales_out + ((w.rp0 >> 7) * A.nv_ka + (col0 >> 6)) * 512)[tid - 64] =
+        reinterpret_cast<const uint4 *>(s_nvsc)[tid - 64];
   }
 }
 
@@ -683,11 +738,11 @@ int launch_mx_transpose_bf16(const uint16_t *x, int64_t rows, int64_t cols, cons
   const size_t sm = mx_t_smem(false);
   static bool attr_set = false;
   if (!attr_set) {
-    cudaFuncSetAttribute(mx_transpose_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    cudaFuncSetAttribute(mx_transpose_kernel<kSrcBf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     attr_set = true;
   }
   if (P == 0) return NV_OK;
-  mx_transpose_kernel<false><<<dim3((unsigned)(cols / 128), (unsigned)(P / 128)), 256, sm, s>>>(A);
+  mx_transpose_kernel<kSrcBf16><<<dim3((unsigned)(cols / 128), (unsigned)(P / 128)), 256, sm, s>>>(A);
   return launch_status(cudaGetLastError());
 }
 
@@ -709,11 +764,39 @@ int launch_requant(const uint8_t *codes, const uint8_t *scales, const float *sg,
   const size_t sm = mx_t_smem(true);
   static bool attr_set = false;
   if (!attr_set) {
-    cudaFuncSetAttribute(mx_transpose_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    cudaFuncSetAttribute(mx_transpose_kernel<kSrcNvfp4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     attr_set = true;
   }
   if (nwin == 0) return NV_OK;
-  mx_transpose_kernel<true><<<dim3((unsigned)(cols / 128), (unsigned)nwin), 256, sm, s>>>(A);
+  mx_transpose_kernel<kSrcNvfp4><<<dim3((unsigned)(cols / 128), (unsigned)nwin), 256, sm, s>>>(A);
+  return launch_status(cudaGetLastError());
+}
+
+
+int launch_nvfp4_requant(const uint16_t *x, const float *sg, int64_t batch, int64_t rows, int64_t cols,
+                         const int32_t *groups, int E, uint8_t *codes, uint8_t *scales, uint64_t seed, uint64_t off,
+                         uint8_t *out_codes, uint8_t *out_scales, int *status, cudaStream_t s) {
+  MxTArgs A = {};
+  A.x = x; A.nv_sg = sg; A.rows = rows; A.cols = cols; A.groups = groups; A.E = E;
+  A.nv_codes_out = codes; A.nv_scales_out = scales; A.nv_ka = cols / 64;
+  A.sr = 1; A.seed = seed; A.off_t = off; A.status = status;
+  A.rk = philox_round_keys(seed);
+  A.out_codes = out_codes; A.out_scales = out_scales;
+  int64_t nwin;
+  if (groups) {
+    const int64_t P = nvfp4moe_padded_cap(rows, E);
+    A.grouped = 1; A.out_stride = P; A.out_ka = P / 128; nwin = P / 128;
+  } else {
+    A.grouped = 0; A.wpb = (int)(rows / 128); A.out_ka = rows / 128; nwin = batch * A.wpb;
+  }
+  const size_t sm = mx_t_smem(true);
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaFuncSetAttribute(mx_transpose_kernel<kSrcBf16ToNvfp4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    attr_set = true;
+  }
+  if (nwin == 0) return NV_OK;
+  mx_transpose_kernel<kSrcBf16ToNvfp4><<<dim3((unsigned)(cols / 128), (unsigned)nwin), 256, sm, s>>>(A);
   return launch_status(cudaGetLastError());
 }
 

@@ -38,6 +38,8 @@ _SIGS = {
     "nvfp4moe_quantize_workspace_bytes": (_SZ, [_I64, _I64, _I64]),
     "nvfp4_quantize": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _I32, _P, _P, _P, _P, _P, _SZ, _P]),
     "nvfp4_quantize_noalloc": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _I32, _P, _P, _P, _P, _P]),
+    "nvfp4_quantize_requant": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _I32, _P, _P, _P, _P, _P, _SZ, _U64, _U64,
+                                              _P, _P, _P]),
     "mxfp8_quantize": (ctypes.c_int, [_P, _I64, _I64, _P, _I32, ctypes.c_int, _U64, _U64, _U64,
                                       _P, _P, _P, _P, _P]),
     "dequant_transpose_requant_sr": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _I64, _P, _I32, _U64, _U64,
@@ -167,6 +169,15 @@ def nvfp4_quantize_noalloc(x, batch, rows, cols, group_offsets, outer_scale_in, 
     return _check("nvfp4_quantize_noalloc", lib().nvfp4_quantize_noalloc(
         _ptr(x), batch, rows, cols, _ptr(group_offsets), _ng(group_offsets), _ptr(outer_scale_in),
         _ptr(outer_scale_out), _ptr(codes), _ptr(scales), _stream(stream)))
+
+
+def nvfp4_quantize_requant(x, batch, rows, cols, group_offsets, outer_scale_in, outer_scale_out, codes, scales,
+                           workspace, seed, counter_offset, out_codes, out_scales, stream=None):
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return _check("nvfp4_quantize_requant", lib().nvfp4_quantize_requant(
+        _ptr(x), batch, rows, cols, _ptr(group_offsets), _ng(group_offsets), _ptr(outer_scale_in),
+        _ptr(outer_scale_out), _ptr(codes), _ptr(scales), _ptr(workspace), ws_bytes, seed, counter_offset,
+        _ptr(out_codes), _ptr(out_scales), _stream(stream)))
 
 
 def mxfp8_quantize(x, rows, cols, group_offsets, mode, seed, counter_offset_row, counter_offset_t,

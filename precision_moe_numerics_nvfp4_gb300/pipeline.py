@@ -49,6 +49,12 @@ class NvTensor:
         N.nvfp4_quantize(x, self.batch, self.rows, self.cols, groups, None, self.sg, self.codes, self.scales,
                          self.ws, stream)
 
+    def quantize_requant(self, x, mx, seed, offset, groups=None, stream=None):
+        """quantize() plus the SR re-quantization of the result into `mx`
+        (an MxTransposed), in one pass over x."""
+        N.nvfp4_quantize_requant(x, self.batch, self.rows, self.cols, groups, None, self.sg, self.codes,
+                                 self.scales, self.ws, seed, offset, mx.codes, mx.scales, stream)
+
 
 class MxTransposed:
     """MXFP8 transposed operand: [cols][P] grouped (E given) or
@@ -127,9 +133,16 @@ class SingleLinear:
 
 class MoELayer:
     """Routed experts of one MoE layer: rows grouped by expert (group_offsets),
-    w13 [E][2I][d] (gate rows then up rows), w2 [E][d][I]."""
+    w13 [E][2I][d] (gate rows then up rows), w2 [E][d][I].
 
-    def __init__(self, M, d_model, d_ff, E, device="cuda", backward=True):
+    A training step (`step`) quantizes each forward tensor with
+    nvfp4_quantize_requant, so the MXFP8 re-quantized operands of the
+    backward come out of the forward's quantization pass; `fuse_requant=False`
+    runs nvfp4_quantize in the forward and the four
+    dequant_transpose_requant_sr calls in the backward instead (same results,
+    bit for bit)."""
+
+    def __init__(self, M, d_model, d_ff, E, device="cuda", backward=True, fuse_requant=True):
         dev = torch.device(device)
         self.M, self.d, self.I, self.E = M, d_model, d_ff, E
         I2 = 2 * d_ff
@@ -141,6 +154,8 @@ class MoELayer:
         self.h = torch.empty((M, d_ff), dtype=BF16, device=dev)
         self.hq = NvTensor(1, M, d_ff, dev, E=E)
         self.y2 = torch.empty((M, d_model), dtype=BF16, device=dev)
+        self.fuse_requant = fuse_requant and backward
+        self._requant_seed = None  # seed of the operands the last forward re-quantized
         if not backward:  # forward-only use (sampling): no backward buffers
             return
         # backward
@@ -163,24 +178,39 @@ class MoELayer:
         fwd = 2 * self.M * (2 * self.I) * self.d + 2 * self.M * self.d * self.I
         return fwd, 2 * fwd
 
-    def quantize_weights(self, w13, w2, stream=None):
-        """NVFP4 of both expert weight stacks, one outer scale per expert."""
-        self.w13q.quantize(w13, None, stream)
-        self.w2q.quantize(w2, None, stream)
+    def quantize_weights(self, w13, w2, stream=None, seed=None):
+        """NVFP4 of both expert weight stacks, one outer scale per expert
+        (plus their MXFP8 re-quantization when `seed` is given)."""
+        if seed is None:
+            self.w13q.quantize(w13, None, stream)
+            self.w2q.quantize(w2, None, stream)
+        else:
+            self.w13q.quantize_requant(w13, self.w13t, seed, OFF_W13, None, stream)
+            self.w2q.quantize_requant(w2, self.w2t, seed, OFF_W2, None, stream)
 
-    def forward(self, x, w13, w2, groups, stream=None):
-        self.quantize_weights(w13, w2, stream)
-        self.forward_activations(x, groups, stream)
+    def forward(self, x, w13, w2, groups, stream=None, seed=None):
+        """`seed` (training): also re-quantize the forward tensors for the
+        backward in the same passes."""
+        seed = seed if self.fuse_requant else None
+        self.quantize_weights(w13, w2, stream, seed)
+        self.forward_activations(x, groups, stream, seed)
+        self._requant_seed = seed
 
-    def forward_activations(self, x, groups, stream=None):
+    def forward_activations(self, x, groups, stream=None, seed=None):
         """The forward with the weights already quantized (e.g. sampling)."""
         M, d, I, E = self.M, self.d, self.I, self.E
-        self.xq.quantize(x, groups, stream)
+        if seed is None:
+            self.xq.quantize(x, groups, stream)
+        else:
+            self.xq.quantize_requant(x, self.xt, seed, OFF_XQ, groups, stream)
         N.grouped_gemm_nvfp4_fwd(None, self.xq.sg, self.xq.codes, self.xq.scales, self.w13q.codes,
                                  self.w13q.scales, self.w13q.sg, groups, E, M, 2 * I, d, self.y13, N.NV_OUT_BF16,
                                  None, stream)
         N.nvfp4moe_swiglu_fwd(self.y13, M, I, self.h, stream)
-        self.hq.quantize(self.h, groups, stream)
+        if seed is None:
+            self.hq.quantize(self.h, groups, stream)
+        else:
+            self.hq.quantize_requant(self.h, self.ht, seed, OFF_HQ, groups, stream)
         N.grouped_gemm_nvfp4_fwd(None, self.hq.sg, self.hq.codes, self.hq.scales, self.w2q.codes, self.w2q.scales,
                                  self.w2q.sg, groups, E, M, d, I, self.y2, N.NV_OUT_BF16, None, stream)
 
@@ -188,8 +218,15 @@ class MoELayer:
         """dx goes to `dx_out` when given (bf16 [M][d_model]), else self.dx."""
         M, d, I, E = self.M, self.d, self.I, self.E
         dx = self.dx if dx_out is None else dx_out
+        # re-quantize the saved forward tensors (dequantize -> transpose -> SR to
+        # MXFP8), unless the forward already did with this seed
+        if self._requant_seed != seed:
+            self.requant_saved(groups, seed, stream)
+        self._backward_gemms(g2, groups, seed, stream, dx)
+
+    def requant_saved(self, groups, seed, stream=None):
+        M, d, I, E = self.M, self.d, self.I, self.E
         I2 = 2 * I
-        # re-quantize the saved forward tensors (dequantize -> transpose -> SR to MXFP8)
         N.dequant_transpose_requant_sr(self.w13q.codes, self.w13q.scales, self.w13q.sg, E, I2, d, None, seed,
                                        OFF_W13, self.w13t.codes, self.w13t.scales, stream)
         N.dequant_transpose_requant_sr(self.w2q.codes, self.w2q.scales, self.w2q.sg, E, d, I, None, seed, OFF_W2,
@@ -198,6 +235,10 @@ class MoELayer:
                                        self.xt.codes, self.xt.scales, stream)
         N.dequant_transpose_requant_sr(self.hq.codes, self.hq.scales, self.hq.sg, 1, M, I, groups, seed, OFF_HQ,
                                        self.ht.codes, self.ht.scales, stream)
+
+    def _backward_gemms(self, g2, groups, seed, stream, dx):
+        M, d, I, E = self.M, self.d, self.I, self.E
+        I2 = 2 * I
         # down projection: dh = g2 w2, dW2 = g2^T h_q
         N.mxfp8_quantize(g2, M, d, groups, N.NV_SR, seed, OFF_G2_ROW, OFF_G2_T, self.g2_row.codes,
                          self.g2_row.scales, self.g2t.codes, self.g2t.scales, stream)
@@ -215,13 +256,15 @@ class MoELayer:
                                 I2, d, self.dw13, None, stream)
 
     def step(self, x, w13, w2, g2, groups, seed=3, stream=None, dx_out=None):
-        self.forward(x, w13, w2, groups, stream)
+        self.forward(x, w13, w2, groups, stream, seed)
         self.backward(g2, groups, seed, stream, dx_out)
 
-    # kernels one step launches: forward = 4 NVFP4 quantizations x 3 kernels
-    # (amax, finalize, quantize) + 2 GEMMs + SwiGLU; backward = 4 requants +
-    # 2 MXFP8 quantizations + 4 GEMMs + SwiGLU backward
-    LAUNCHES_PER_STEP = (4 * 3 + 2 + 1) + (4 + 2 + 4 + 1)
+    def launches_per_step(self):
+        """Kernels one step launches: forward = 4 NVFP4 quantizations x 3
+        kernels (amax, finalize, quantize or quantize + requant) + 2 GEMMs +
+        SwiGLU; backward = (4 requants unless fused) + 2 MXFP8 quantizations +
+        4 GEMMs + SwiGLU backward."""
+        return (4 * 3 + 2 + 1) + (0 if self.fuse_requant else 4) + (2 + 4 + 1)
 
 
 class HostStaged:
