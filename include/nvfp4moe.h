@@ -295,13 +295,15 @@ int grouped_gemm_mxfp8_dw(const uint8_t *gt_codes, const uint8_t *gt_scales,
 
 /* ---- kernel choice for the three grouped GEMMs (no counterpart in the paper) --
  * 0: automatic (the default): for the MXFP8 GEMMs, CTA pairs with 256 x 256
- *    output tiles where the shape allows it (output columns, and for wgrad N,
+ *    tiles where the shape allows it (output columns, and for wgrad N,
  *    multiples of 256) and, for dgrad, the experts average at least 512 rows;
  *    otherwise (and for the NVFP4 forward GEMM) two CTAs per SM with
  *    128 x 128 tiles.
  * 1: one CTA per SM, 128 x 128 tiles, two accumulators.
  * 2: two CTAs per SM, 128 x 128 tiles.
- * 3: CTA pairs wherever the shape allows it, else 2.
+ * 3: CTA pairs with 256 x 256 tiles wherever the shape allows it, else 2.
+ * 4: CTA pairs with 256 x 128 tiles (two pairs per SM pair) wherever the
+ *    shape allows it, else 2.
  * The environment variable NVFP4MOE_GEMM_VARIANT (read at the first GEMM
  * call) gives the initial setting.  Applies to later launches from every host
  * thread; set it while no other thread launches a GEMM.  Returns NV_OK, or

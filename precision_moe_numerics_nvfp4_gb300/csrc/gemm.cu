@@ -502,31 +502,37 @@ __device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 
-constexpr int kPairN = 256;  // output tile of a CTA pair: 256 x 256
-
-template <int KIND, int STAGES>
+// Output tile of a CTA pair: 256 x BN.  BN = 256: one pair per SM pair (the
+// 256-column accumulator fills half of each SM's tensor memory); BN = 128: two
+// pairs per SM pair, so one pair's epilogue runs under the other's MMAs, with
+// half the scale copies per FLOP of the 128 x 128 kernel.
+template <int KIND, int STAGES, int BN>
 struct CfgPair {
+  static_assert(BN == 128 || BN == 256, "pair tile width");
   static constexpr bool kFp4 = KIND == kGemmNvfp4Fwd;
   static constexpr int kAtomsPerStage = kFp4 ? 4 : 1;
+  static constexpr int kBHalf = BN / 2;                 // B rows staged by each CTA
+  static constexpr int kSfbTiles = BN / 128;            // 128-row scale tiles of B per k-atom
   static constexpr int A_BYTES = 128 * 128;
-  static constexpr int B_BYTES = 128 * 128;             // this CTA's half of B
+  static constexpr int B_BYTES = kBHalf * 128;          // this CTA's half of B
   static constexpr int SFA_BYTES = kAtomsPerStage * 512;
-  static constexpr int SFB_BYTES = 2 * SFA_BYTES;       // scales of all 256 B rows
+  static constexpr int SFB_BYTES = kSfbTiles * SFA_BYTES;  // scales of all BN rows of B
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
   static constexpr int SFA_COLS = kAtomsPerStage * 4;
-  static constexpr int SFB_COLS = kAtomsPerStage * 8;
+  static constexpr int SFB_COLS = kAtomsPerStage * (BN / 32);
   static constexpr int SF_COLS = SFA_COLS + SFB_COLS;
-  static constexpr int ACC_COLS = kPairN;
+  static constexpr int ACC_COLS = BN;
   static constexpr int TMEM_COLS = cpow2(ACC_COLS + STAGES * SF_COLS);
   static constexpr int NBARS = 2 * STAGES + 2;          // full, empty, acc_full, acc_empty
-  static constexpr int kEpiWarps = 8;                   // two per lane quadrant, 128 columns each
+  static constexpr int kEpiWarps = BN / 32;             // per lane quadrant: BN / 128 warps of 128 columns
   static constexpr int kThreads = 32 * (2 + kEpiWarps);
+  static constexpr int kCtasPerSm = BN == 128 ? 2 : 1;
   static constexpr uint32_t IDESC = (kFp4 ? ((1u << 7) | (1u << 10)) : (1u << 23)) |
-                                    ((uint32_t)(kPairN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+                                    ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
   static size_t smem_bytes(int E) {
     return 1024 + (size_t)STAGES * STAGE_BYTES + NBARS * 8 + 32 + (size_t)(E + 1) * 16 + 64;
   }
-  static_assert(TMEM_COLS <= 512, "tensor memory");
+  static_assert(TMEM_COLS * kCtasPerSm <= 512, "tensor memory");
 };
 
 // Wgrad tile order.  Every expert writes its whole fp32 dW (the same bytes
@@ -569,7 +575,7 @@ struct PairTile {
 
 // s_pb[e]: number of 256-row pair blocks before expert e (fwd, dgrad);
 // s_ord: experts by decreasing size (wgrad)
-template <int KIND>
+template <int KIND, int BN>
 __device__ __forceinline__ PairTile decode_pair(int t, const GemmArgs &A, const int *s_off, const int *s_pad,
                                                 const int *s_pb, const int *s_ord, int pair, int npairs,
                                                 int num_tiles, int cta) {
@@ -586,13 +592,13 @@ __device__ __forceinline__ PairTile decode_pair(int t, const GemmArgs &A, const 
     T.mrows = live ? min(128, s_off[e + 1] - T.a_row) : 0;
     T.a_tile = ph / 128;
     const int nb = (int)(KIND == kGemmNvfp4Fwd ? A.N : A.K);
-    T.b_row = e * nb + nt * kPairN + 128 * cta;
-    T.b_tile0 = ((int64_t)e * nb + (int64_t)nt * kPairN) / 128;
+    T.b_row = e * nb + nt * BN + (BN / 2) * cta;
+    T.b_tile0 = ((int64_t)e * nb + (int64_t)nt * BN) / 128;
     T.nk = (int)(KIND == kGemmNvfp4Fwd ? A.K / 256 : A.N / 128);
     T.k_off = 0;
     T.k_atom0 = 0;
     T.out_row0 = T.a_row;
-    T.out_col0 = (int64_t)nt * kPairN;
+    T.out_col0 = (int64_t)nt * BN;
   } else {
     const int per_e = A.ntm * A.ntn;
     const int d = dw_sorted_index(t, pair, npairs, num_tiles);
@@ -601,15 +607,15 @@ __device__ __forceinline__ PairTile decode_pair(int t, const GemmArgs &A, const 
     const int r = d - k * per_e, mt = r / A.ntn, nt = r - (r / A.ntn) * A.ntn;
     T.e = e;
     T.a_row = mt * 256 + 128 * cta;
-    T.b_row = nt * kPairN + 128 * cta;
+    T.b_row = nt * BN + (BN / 2) * cta;
     T.mrows = 128;
     T.nk = (s_pad[e + 1] - s_pad[e]) / 128;
     T.k_off = s_pad[e];
     T.a_tile = T.a_row / 128;
-    T.b_tile0 = (int64_t)nt * 2;
+    T.b_tile0 = (int64_t)nt * (BN / 128);
     T.k_atom0 = s_pad[e] / 128;
     T.out_row0 = (int64_t)e * A.N + T.a_row;
-    T.out_col0 = (int64_t)nt * kPairN;
+    T.out_col0 = (int64_t)nt * BN;
   }
   return T;
 }
@@ -649,12 +655,12 @@ __device__ __forceinline__ bool wait_pair(uint32_t bar, uint32_t parity, uint64_
   return false;
 }
 
-template <int KIND, int STAGES>
-__global__ void __launch_bounds__(CfgPair<KIND, STAGES>::kThreads, 1)
+template <int KIND, int STAGES, int BN>
+__global__ void __launch_bounds__(CfgPair<KIND, STAGES, BN>::kThreads, CfgPair<KIND, STAGES, BN>::kCtasPerSm)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                              const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                              GemmArgs A) {
-  using C = CfgPair<KIND, STAGES>;
+  using C = CfgPair<KIND, STAGES, BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint8_t *sA = smem;
@@ -708,7 +714,7 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES>::kThreads, 1)
     uint32_t it = 0;
     bool ok = true;
     for (int t = pair; ok && t < num_tiles; t += npairs) {
-      const PairTile T = decode_pair<KIND>(t, A, s_off, s_pad, s_pb, s_ord, pair, npairs, num_tiles, cta);
+      const PairTile T = decode_pair<KIND, BN>(t, A, s_off, s_pad, s_pb, s_ord, pair, npairs, num_tiles, cta);
       for (int ks = 0; ks < T.nk; ++ks, ++it) {
         const uint32_t s = it % STAGES;
         if (it >= STAGES &&
@@ -724,7 +730,7 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES>::kThreads, 1)
         const int64_t katom = T.k_atom0 + (int64_t)ks * C::kAtomsPerStage;
         tma_load_2d_pair(smem_u32(sSFA + s * C::SFA_BYTES), &tmSA, 0, (int)((T.a_tile * A.ka + katom) * 4), fb);
 #pragma unroll
-        for (int j = 0; j < 2; ++j)
+        for (int j = 0; j < C::kSfbTiles; ++j)
           tma_load_2d_pair(smem_u32(sSFB + s * C::SFB_BYTES + j * C::SFA_BYTES), &tmSB, 0,
                            (int)(((T.b_tile0 + j) * A.ka + katom) * 4), fb);
       }
@@ -742,7 +748,7 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES>::kThreads, 1)
     uint32_t it = 0, tc = 0;
     bool ok = true;
     for (int t = pair; ok && t < num_tiles; t += npairs, ++tc) {
-      const PairTile T = decode_pair<KIND>(t, A, s_off, s_pad, s_pb, s_ord, pair, npairs, num_tiles, 0);
+      const PairTile T = decode_pair<KIND, BN>(t, A, s_off, s_pad, s_pb, s_ord, pair, npairs, num_tiles, 0);
       if (tc >= 1 && !wait_pair(smem_u32(acc_empty), (tc - 1) & 1, A.wait_limit, s_abort, peer_abort, A.status))
         break;
       tc_fence_after();
@@ -761,8 +767,8 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES>::kThreads, 1)
         for (int j = 0; j < C::kAtomsPerStage; ++j) {
           tc_cp_sf_pair(sfa + 4 * j, desc_sf(a_sf_smem + j * 512));
 #pragma unroll
-          for (int r = 0; r < 2; ++r)
-            tc_cp_sf_pair(sfb + j * 8 + 4 * r, desc_sf(b_sf_smem + r * C::SFA_BYTES + j * 512));
+          for (int r = 0; r < C::kSfbTiles; ++r)
+            tc_cp_sf_pair(sfb + j * (BN / 32) + 4 * r, desc_sf(b_sf_smem + r * C::SFA_BYTES + j * 512));
         }
         const uint64_t da = desc_sw128(smem_u32(sA + s * C::A_BYTES));
         const uint64_t db = desc_sw128(smem_u32(sB + s * C::B_BYTES));
@@ -770,7 +776,7 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES>::kThreads, 1)
         for (int j = 0; j < 4; ++j) {
           const uint32_t accum = (ks | j) != 0;
           if (C::kFp4) {
-            mma_nvf4_pair(tmem, da + 2 * j, db + 2 * j, C::IDESC, sfa + 4 * j, sfb + j * 8, accum);
+            mma_nvf4_pair(tmem, da + 2 * j, db + 2 * j, C::IDESC, sfa + 4 * j, sfb + j * (BN / 32), accum);
           } else {
             const uint32_t idesc = C::IDESC | ((uint32_t)j << 4) | ((uint32_t)j << 29);
             mma_mxf8_pair(tmem, da + 2 * j, db + 2 * j, idesc, sfa, sfb, accum);
@@ -781,14 +787,14 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES>::kThreads, 1)
       tc_commit_pair(smem_u32(acc_full));  // both CTAs: this tile's accumulator is complete
     }
   } else if (warp >= 2) {
-    // ---- epilogue (both CTAs): 8 warps, 128 columns each ----------------------------
+    // ---- epilogue (both CTAs): BN / 32 warps, 128 columns each ------------------------
     const int q = warp & 3;
     const int half = (warp - 2) >> 2;
     const int row = q * 32 + lane;
     const uint32_t acc_empty_addr = cta == 0 ? smem_u32(acc_empty) : mapa_shared(smem_u32(acc_empty), 0);
     uint32_t tc = 0;
     for (int t = pair; t < num_tiles; t += npairs, ++tc) {
-      const PairTile T = decode_pair<KIND>(t, A, s_off, s_pad, s_pb, s_ord, pair, npairs, num_tiles, cta);
+      const PairTile T = decode_pair<KIND, BN>(t, A, s_off, s_pad, s_pb, s_ord, pair, npairs, num_tiles, cta);
       if (!wait_pair(smem_u32(acc_full), tc & 1, A.wait_limit, s_abort, peer_abort, A.status)) break;
       tc_fence_after();
       float alpha = 1.0f;
@@ -920,12 +926,12 @@ static int run(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &arg
   return cudaGetLastError() == cudaSuccess ? NV_OK : NV_ERR_CUDA;
 }
 
-template <int KIND, int STAGES>
+template <int KIND, int STAGES, int BN>
 static int run_pair(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tsa, const CUtensorMap &tsb,
                     const GemmArgs &args, int64_t max_tiles, cudaStream_t s) {
-  using C = CfgPair<KIND, STAGES>;
+  using C = CfgPair<KIND, STAGES, BN>;
   const size_t sm = C::smem_bytes(args.E);
-  auto k = grouped_gemm_pair_kernel<KIND, STAGES>;
+  auto k = grouped_gemm_pair_kernel<KIND, STAGES, BN>;
   static size_t attr_bytes = 0;
   static int max_pairs = 0;  // co-resident CTA pairs at the largest shared-memory size requested so far
   cudaLaunchConfig_t cfg = {};
@@ -944,10 +950,13 @@ static int run_pair(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensor
       return NV_ERR_CUDA;
     const int sms = num_sms();
     if (sms <= 0) return NV_ERR_CUDA;
-    cfg.gridDim = dim3((unsigned)(sms & ~1), 1, 1);
+    cfg.gridDim = dim3((unsigned)(4 * sms), 1, 1);  // large enough not to cap the answer
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess || n <= 0) return NV_ERR_CUDA;
-    max_pairs = n;
+    // measured: for two CTAs per SM the query reports one pair per SM pair
+    // while the GPU runs two at once (the 256 x 128 variant then takes half
+    // the time); a persistent grid larger than what fits only queues pairs
+    max_pairs = n > (sms / 2) * C::kCtasPerSm ? n : (sms / 2) * C::kCtasPerSm;
     attr_bytes = sm;
   }
   const int64_t pairs = max_tiles < max_pairs ? max_tiles : max_pairs;
@@ -966,13 +975,13 @@ static int gemm_variant() {
   if (g_variant < 0) {
     const char *e = getenv("NVFP4MOE_GEMM_VARIANT");
     const int v = e ? atoi(e) : 0;
-    g_variant = (v >= 0 && v <= 3) ? v : 0;
+    g_variant = (v >= 0 && v <= 4) ? v : 0;
   }
   return g_variant;
 }
 
 int set_gemm_variant(int v) {
-  if (v < 0 || v > 3) return NV_ERR_ARG;
+  if (v < 0 || v > 4) return NV_ERR_ARG;
   g_variant = v;
   return NV_OK;
 }
@@ -1014,17 +1023,25 @@ int launch_grouped_gemm(const GemmProblem &p, int *status, cudaStream_t s) {
   } else {
     max_tiles = (P / 128) * a.ntn;
   }
-  // variant 3: CTA pairs with 256 x 256 tiles; variant 2: two CTAs per SM
-  // with one accumulator each (3 stages); variant 1: one CTA per SM with two
-  // accumulators (6 stages).  Default: 3 where it applies (see below), else 2.
+  // variants: 1 one CTA per SM with two accumulators (6 stages); 2 two CTAs
+  // per SM with one accumulator each (3 stages); 3 CTA pairs with 256 x 256
+  // tiles; 4 CTA pairs with 256 x 128 tiles, two pairs per SM pair.  A pair
+  // variant applies where the shape allows it (else 2).  Automatic, from
+  // measurements at the MoE shapes (16384 tokens, PFLOP/s, variants 2 / 3 / 4):
+  // NVFP4 forward 4.13 / 3.31 / 3.96 -> 2; MXFP8 dgrad 2.54 / 2.72 / 2.71 and
+  // wgrad 1.90 / 2.24 / 2.14 -> 3 when the experts hold several 128-row blocks
+  // (a half-empty pair block wastes half of its MMAs), else 2.
   const int forced = gemm_variant();
-  const int64_t out_rows_per_expert = p.kind == kGemmMxfp8Dw ? p.N : 0;
-  const bool pair_shape = (out_cols % kPairN == 0) && (p.kind != kGemmMxfp8Dw || out_rows_per_expert % 256 == 0);
-  // measured: the pair kernel is faster for the MXFP8 GEMMs; for NVFP4 its
-  // three tensor-memory scale copies per MMA cost more than the tile saves
-  const bool pair_pays = p.kind == kGemmMxfp8Dw || (p.kind == kGemmMxfp8Dx && p.M_total >= (int64_t)512 * p.E);
-  const bool use_pair = pair_shape && (forced == 3 || (forced == 0 && pair_pays));
-  if (use_pair) {
+  const bool rows_ok = p.kind != kGemmMxfp8Dw || p.N % 256 == 0;  // wgrad: pair tiles of 256 rows
+  const bool big_groups = p.kind == kGemmMxfp8Dw || p.M_total >= (int64_t)512 * p.E;
+  int pair_bn = 0;
+  if (forced == 3 || forced == 4) {
+    pair_bn = forced == 3 ? 256 : 128;
+  } else if (forced == 0 && big_groups && p.kind != kGemmNvfp4Fwd) {
+    pair_bn = 256;
+  }
+  if (pair_bn && (!rows_ok || out_cols % pair_bn)) pair_bn = 0;
+  if (pair_bn) {
     const int atoms = p.kind == kGemmNvfp4Fwd ? 4 : 1;
     uint64_t a_sf_bytes, b_sf_bytes;
     switch (p.kind) {
@@ -1041,11 +1058,21 @@ int launch_grouped_gemm(const GemmProblem &p, int *status, cudaStream_t s) {
         b_sf_bytes = (uint64_t)(p.K / 128) * a.ka * 512;
         break;
     }
-    CUtensorMap tsa, tsb;
+    CUtensorMap tsa, tsb, tbh;
     if (!make_sf_map(&tsa, p.a_scales, a_sf_bytes, 4 * atoms) || !make_sf_map(&tsb, p.b_scales, b_sf_bytes, 4 * atoms))
       return NV_ERR_CUDA;
+    const CUtensorMap *tbp = &tb;  // B box of BN / 2 rows
+    if (pair_bn == 128) {
+      switch (p.kind) {
+        case kGemmNvfp4Fwd: ok = make_map(&tbh, p.b_codes, p.K / 2, (uint64_t)p.E * p.N, p.K / 2, 64); break;
+        case kGemmMxfp8Dx: ok = make_map(&tbh, p.b_codes, p.N, (uint64_t)p.E * p.K, p.N, 64); break;
+        default: ok = make_map(&tbh, p.b_codes, P, p.K, P, 64); break;
+      }
+      if (!ok) return NV_ERR_CUDA;
+      tbp = &tbh;
+    }
     GemmArgs b = a;
-    b.ntn = (int)(out_cols / kPairN);
+    b.ntn = (int)(out_cols / pair_bn);
     int64_t pair_tiles;
     if (p.kind == kGemmMxfp8Dw) {
       b.ntm = (int)(p.N / 256);
@@ -1053,10 +1080,17 @@ int launch_grouped_gemm(const GemmProblem &p, int *status, cudaStream_t s) {
     } else {
       pair_tiles = ((P / 128 + p.E) / 2) * b.ntn;  // upper bound of sum_e ceil(P_e / 256) tiles
     }
+    if (pair_bn == 256) {
+      switch (p.kind) {
+        case kGemmNvfp4Fwd: return run_pair<kGemmNvfp4Fwd, 5, 256>(ta, *tbp, tsa, tsb, b, pair_tiles, s);
+        case kGemmMxfp8Dx: return run_pair<kGemmMxfp8Dx, 6, 256>(ta, *tbp, tsa, tsb, b, pair_tiles, s);
+        default: return run_pair<kGemmMxfp8Dw, 6, 256>(ta, *tbp, tsa, tsb, b, pair_tiles, s);
+      }
+    }
     switch (p.kind) {
-      case kGemmNvfp4Fwd: return run_pair<kGemmNvfp4Fwd, 5>(ta, tb, tsa, tsb, b, pair_tiles, s);
-      case kGemmMxfp8Dx: return run_pair<kGemmMxfp8Dx, 6>(ta, tb, tsa, tsb, b, pair_tiles, s);
-      default: return run_pair<kGemmMxfp8Dw, 6>(ta, tb, tsa, tsb, b, pair_tiles, s);
+      case kGemmNvfp4Fwd: return run_pair<kGemmNvfp4Fwd, 3, 128>(ta, *tbp, tsa, tsb, b, pair_tiles, s);
+      case kGemmMxfp8Dx: return run_pair<kGemmMxfp8Dx, 4, 128>(ta, *tbp, tsa, tsb, b, pair_tiles, s);
+      default: return run_pair<kGemmMxfp8Dw, 4, 128>(ta, *tbp, tsa, tsb, b, pair_tiles, s);
     }
   }
   const bool two_per_sm = forced != 1;

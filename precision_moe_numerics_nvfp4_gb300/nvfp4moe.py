@@ -144,12 +144,14 @@ def nvfp4moe_version() -> str:
     return lib().nvfp4moe_version().decode()
 
 
-GEMM_AUTO, GEMM_ONE_PER_SM, GEMM_TWO_PER_SM, GEMM_CTA_PAIR = 0, 1, 2, 3
+GEMM_AUTO, GEMM_ONE_PER_SM, GEMM_TWO_PER_SM, GEMM_CTA_PAIR, GEMM_CTA_PAIR_N128 = 0, 1, 2, 3, 4
 
 
 def nvfp4moe_set_gemm_kernel(variant: int) -> None:
     """Kernel choice of the grouped GEMMs: GEMM_AUTO, GEMM_ONE_PER_SM,
-    GEMM_TWO_PER_SM or GEMM_CTA_PAIR (the pair kernel where the shape allows)."""
+    GEMM_TWO_PER_SM, GEMM_CTA_PAIR (256 x 256 pair tiles) or
+    GEMM_CTA_PAIR_N128 (256 x 128 pair tiles, two pairs per SM pair); a pair
+    choice applies where the shape allows it."""
     _check("nvfp4moe_set_gemm_kernel", lib().nvfp4moe_set_gemm_kernel(int(variant)))
 
 

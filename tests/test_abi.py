@@ -48,8 +48,8 @@ def test_status_strings(lib):
 
 
 def test_gemm_kernel_choice_is_validated(lib):
-    for v in (N.GEMM_ONE_PER_SM, N.GEMM_TWO_PER_SM, N.GEMM_CTA_PAIR, N.GEMM_AUTO):
+    for v in (N.GEMM_ONE_PER_SM, N.GEMM_TWO_PER_SM, N.GEMM_CTA_PAIR, N.GEMM_CTA_PAIR_N128, N.GEMM_AUTO):
         N.nvfp4moe_set_gemm_kernel(v)
-    for bad in (-1, 4, 99):
+    for bad in (-1, 5, 99):
         with pytest.raises(N.NvError):
             N.nvfp4moe_set_gemm_kernel(bad)

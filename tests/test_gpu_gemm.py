@@ -54,8 +54,8 @@ def _fwd(sizes, N_, K, out_fp32=True, seed=0):
     return y, xq, wq, o
 
 
-@pytest.fixture(params=[N.GEMM_TWO_PER_SM, N.GEMM_CTA_PAIR, N.GEMM_ONE_PER_SM],
-                ids=["two_per_sm", "cta_pair", "one_per_sm"])
+@pytest.fixture(params=[N.GEMM_TWO_PER_SM, N.GEMM_CTA_PAIR, N.GEMM_ONE_PER_SM, N.GEMM_CTA_PAIR_N128],
+                ids=["two_per_sm", "cta_pair", "one_per_sm", "cta_pair_n128"])
 def gemm_kernel(request):
     """Each kernel choice must meet the same bound; shapes whose output width
     is not a multiple of 256 run the 128 x 128 kernel under every choice."""
