@@ -426,6 +426,29 @@ __device__ __forceinline__ void store_f16_products(uint8_t *s_in, int i, int kb,
       make_uint4(hmul2_u32(h1[0], s2), hmul2_u32(h1[1], s2), hmul2_u32(h1[2], s2), hmul2_u32(h1[3], s2));
 }
 
+// 16-byte asynchronous global -> shared copy (L2 only); `bytes` (0 or 16) are
+// read and the rest is zero-filled
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(bytes)
+               : "memory");
+}
+
+// The window's bf16 tile [128 rows][128 columns] straight into the swizzled
+// 16-bit layout with cp.async: 128 bytes per thread in flight without
+// registers; rows past the window's data are zero-filled.  Waits for the
+// thread's own copies; the caller's barrier makes the tile visible.
+__device__ __forceinline__ void stage_bf16_tile(const MxTArgs &A, const Window &w, int64_t col0, uint8_t *s_in) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int q = k * 256 + (int)threadIdx.x;
+    const int i = q >> 4, c16 = q & 15;
+    const bool ok = i < w.nvalid;
+    const uint16_t *src = ok ? A.x + (w.src_row0 + i) * A.cols + col0 + c16 * 8 : A.x;
+    cp_async16(s_in + i * 256 + chunk_of(i, c16) * 16, src, ok ? 16u : 0u);
+  }
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
+}
+
 template <int kMode>
 __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant__ MxTArgs A) {
   constexpr bool kNvfp4 = kMode != kSrcBf16;  // phase 2 on exact f16 products of NVFP4 values
@@ -452,114 +475,101 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant
 
   // ---- phase 1 --------------------------------------------------------------
   if (!kNvfp4) {
-    // items of 16 columns (32 bytes) of one row; a row-wise MXFP8 block of 32
-    // is two neighbouring lanes, and one Philox call covers an item's 8 pairs
-    const bool do_row = A.row_codes != nullptr;
+    stage_bf16_tile(A, w, col0, s_in);
+    __syncthreads();
+    // row-wise output: items of 16 columns (32 bytes) of one row; a row-wise
+    // MXFP8 block of 32 is two neighbouring lanes, and one Philox call covers
+    // an item's 8 pairs
+    if (A.row_codes != nullptr) {
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      uint4 raw[2][2];
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {  // all loads of this half in flight together
-        const int q = (half * 2 + u) * 256 + tid;
+      for (int u = 0; u < 4; ++u) {
+        const int q = u * 256 + tid;
         const int i = q >> 3, c16 = q & 7;
-        raw[u][0] = raw[u][1] = make_uint4(0, 0, 0, 0);
-        if (i < w.nvalid) {
-          const uint16_t *src = A.x + (w.src_row0 + i) * A.cols + col0 + c16 * 16;
-          raw[u][0] = ld_stream_v4(src);
-          raw[u][1] = ld_stream_v4(src + 8);
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int q = (half * 2 + u) * 256 + tid;
-        const int i = q >> 3, c16 = q & 7;
-        uint4 *row = reinterpret_cast<uint4 *>(s_in + i * 256);
-        row[chunk_of(i, 2 * c16)] = raw[u][0];
-        row[chunk_of(i, 2 * c16 + 1)] = raw[u][1];
-        if (do_row) {
-          const bool valid = i < w.nvalid;
-          const int64_t e0 = (w.src_row0 + i) * A.cols + col0 + c16 * 16;
-          uint32_t m = bf16x2_absmax(bf16x2_absmax(raw[u][0].x, raw[u][0].y), bf16x2_absmax(raw[u][0].z, raw[u][0].w));
-          m = bf16x2_absmax(m, bf16x2_absmax(bf16x2_absmax(raw[u][1].x, raw[u][1].y),
-                                             bf16x2_absmax(raw[u][1].z, raw[u][1].w)));
-          m = bf16x2_absmax(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-          if (valid) {
-            float mult;
-            const uint32_t sc = e8m0_scale(bf16x2_max_to_f32(m), &mult);
-            uint2 o0, o1;
-            if (A.sr) {
-              const uint4 b = philox_bits8_rk((uint64_t)(e0 >> 4), A.off_row, A.rk);  // pair keys e0/2 .. e0/2+7
-              const uint16_t mb = pow2_bf16_bits(mult);
-              o0 = mx_sr8(raw[u][0], mb, b.x, b.y);
-              o1 = mx_sr8(raw[u][1], mb, b.z, b.w);
-            } else {
-              float v0[8], v1[8];
-              unpack8(raw[u][0], v0);
-              unpack8(raw[u][1], v1);
-              o0 = mx_rn8(v0, mult);
-              o1 = mx_rn8(v1, mult);
-            }
-            *reinterpret_cast<uint4 *>(A.row_codes + e0) = make_uint4(o0.x, o0.y, o1.x, o1.y);
-            if ((c16 & 1) == 0) s_rsc[atom_pos(i, c16 >> 1)] = (uint8_t)sc;
+        const uint4 *row = reinterpret_cast<const uint4 *>(s_in + i * 256);
+        const uint4 r0 = row[chunk_of(i, 2 * c16)], r1 = row[chunk_of(i, 2 * c16 + 1)];
+        const bool valid = i < w.nvalid;
+        const int64_t e0 = (w.src_row0 + i) * A.cols + col0 + c16 * 16;
+        uint32_t m = bf16x2_absmax(bf16x2_absmax(r0.x, r0.y), bf16x2_absmax(r0.z, r0.w));
+        m = bf16x2_absmax(m, bf16x2_absmax(bf16x2_absmax(r1.x, r1.y), bf16x2_absmax(r1.z, r1.w)));
+        m = bf16x2_absmax(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+        if (valid) {
+          float mult;
+          const uint32_t sc = e8m0_scale(bf16x2_max_to_f32(m), &mult);
+          uint2 o0, o1;
+          if (A.sr) {
+            const uint4 b = philox_bits8_rk((uint64_t)(e0 >> 4), A.off_row, A.rk);  // pair keys e0/2 .. e0/2+7
+            const uint16_t mb = pow2_bf16_bits(mult);
+            o0 = mx_sr8(r0, mb, b.x, b.y);
+            o1 = mx_sr8(r1, mb, b.z, b.w);
+          } else {
+            float v0[8], v1[8];
+            unpack8(r0, v0);
+            unpack8(r1, v1);
+            o0 = mx_rn8(v0, mult);
+            o1 = mx_rn8(v1, mult);
           }
+          *reinterpret_cast<uint4 *>(A.row_codes + e0) = make_uint4(o0.x, o0.y, o1.x, o1.y);
+          if ((c16 & 1) == 0) s_rsc[atom_pos(i, c16 >> 1)] = (uint8_t)sc;
         }
       }
     }
   } else if (kMode == kSrcNvfp4) {
-    // NVFP4: (row, 16-column block) pairs; 8 code bytes + 1 scale byte each
-    const int64_t half_cols = A.cols >> 1;
-    const int64_t ka_src = (A.cols + 63) >> 6;
-    const int64_t tile0 = (w.rp0 >> 7) * ka_src + (col0 >> 6);
-    uint2 raw[4];
-    uint32_t sc[4];
+    // NVFP4: the window's codes [128 rows][64 bytes] and its two 512-byte
+    // scale tiles go through cp.async into the output tile (unused until
+    // phase 2), then each (row, 16-column block) unit is decoded to exact f16
+    // products e2m1 * e4m3
+    uint8_t *st_codes = s_out, *st_sc = s_out + 128 * 64;
+    {
+      const int64_t half_cols = A.cols >> 1;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int q = u * 256 + tid;
-      const int i = q >> 3, kb = q & 7;
-      raw[u] = make_uint2(0, 0);
-      sc[u] = 0;
-      if (i < w.nvalid) {
-        raw[u] = ld_stream_v2(A.nv_codes + (w.src_row0 + i) * half_cols + (col0 >> 1) + kb * 8);
-        sc[u] = A.nv_scales[(tile0 + (kb >> 2)) * 512 + atom_pos(i, kb)];
+      for (int k = 0; k < 2; ++k) {
+        const int q = k * 256 + tid;
+        const int i = q >> 2, part = q & 3;
+        const bool ok = i < w.nvalid;
+        const uint8_t *src = ok ? A.nv_codes + (w.src_row0 + i) * half_cols + (col0 >> 1) + part * 16 : A.nv_codes;
+        cp_async16(st_codes + i * 64 + part * 16, src, ok ? 16u : 0u);
       }
+      if (tid < 64) {
+        const int64_t ka_src = (A.cols + 63) >> 6;
+        const int64_t tile0 = (w.rp0 >> 7) * ka_src + (col0 >> 6);
+        const bool ok = w.nvalid > 0;
+        cp_async16(st_sc + tid * 16, ok ? A.nv_scales + tile0 * 512 + tid * 16 : A.nv_scales, ok ? 16u : 0u);
+      }
+      asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
     }
+    __syncthreads();
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int q = u * 256 + tid;
       const int i = q >> 3, kb = q & 7;
-      store_f16_products(s_in, i, kb, raw[u], sc[u]);
+      uint2 raw = make_uint2(0, 0);
+      uint32_t sc = 0;
+      if (i < w.nvalid) {
+        raw = *reinterpret_cast<const uint2 *>(st_codes + i * 64 + kb * 8);
+        sc = st_sc[(kb >> 2) * 512 + atom_pos(i, kb)];
+      }
+      store_f16_products(s_in, i, kb, raw, sc);
     }
   } else {
     // bf16 -> NVFP4 with the quantizer's block rule (nvfp4_block), codes to
-    // global memory, scales to the shared tile; then the exact f16 products
-    // of the new codes for phase 2
+    // global memory, scales to the shared tile; the exact f16 products of the
+    // new codes replace the unit's bf16 values in place for phase 2
+    stage_bf16_tile(A, w, col0, s_in);
+    __syncthreads();
     const float den6 = __fmul_rn(6.0f, sg);
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      uint4 va[2], vb[2];
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {  // the half's loads in flight together
-        const int q = (half * 2 + u) * 256 + tid;
-        const int i = q >> 3, kb = q & 7;
-        va[u] = vb[u] = make_uint4(0, 0, 0, 0);
-        if (i < w.nvalid) {
-          const uint16_t *src = A.x + (w.src_row0 + i) * A.cols + col0 + kb * 16;
-          va[u] = ld_stream_v4(src);
-          vb[u] = ld_stream_v4(src + 8);
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int q = (half * 2 + u) * 256 + tid;
-        const int i = q >> 3, kb = q & 7;
-        uint2 c;
-        uint32_t sc;
-        nvfp4_block(va[u], vb[u], sg, den6, c, sc);  // an all-zero (padding) block gives scale 0 and zero codes
-        if (i < w.nvalid)
-          *reinterpret_cast<uint2 *>(A.nv_codes_out + ((w.src_row0 + i) * A.cols + col0 + kb * 16) / 2) = c;
-        s_nvsc[(kb >> 2) * 512 + atom_pos(i, kb)] = (uint8_t)sc;
-        store_f16_products(s_in, i, kb, c, sc);
-      }
+    for (int u = 0; u < 4; ++u) {
+      const int q = u * 256 + tid;
+      const int i = q >> 3, kb = q & 7;
+      const uint4 *row = reinterpret_cast<const uint4 *>(s_in + i * 256);
+      const uint4 va = row[chunk_of(i, 2 * kb)], vb = row[chunk_of(i, 2 * kb + 1)];
+      uint2 c;
+      uint32_t sc;
+      nvfp4_block(va, vb, sg, den6, c, sc);  // an all-zero (padding) block gives scale 0 and zero codes
+      if (i < w.nvalid)
+        *reinterpret_cast<uint2 *>(A.nv_codes_out + ((w.src_row0 + i) * A.cols + col0 + kb * 16) / 2) = c;
+      s_nvsc[(kb >> 2) * 512 + atom_pos(i, kb)] = (uint8_t)sc;
+      store_f16_products(s_in, i, kb, c, sc);
     }
   }
   __syncthreads();
