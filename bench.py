@@ -257,13 +257,16 @@ def kernel_units(layer, m):
     M, d, I, E = layer.M, layer.d, layer.I, layer.E
     fl13 = 2.0 * M * 2 * I * d
     fl2 = 2.0 * M * d * I
+    # quantize (+ requant) of h: no amax pass when the w13 epilogue produced its outer scale
+    h_amax = 0.0 if layer.fuse_swiglu else 2.0
     return {
         # a call = the amax pass (2 B/elem) + the quantize pass (2 + 0.5 + 1/16 B/elem)
-        "nvfp4_quantize": [(E * 2 * I * d, 4.5625), (E * d * I, 4.5625), (M * d, 4.5625), (M * I, 4.5625)],
+        "nvfp4_quantize": [(E * 2 * I * d, 4.5625), (E * d * I, 4.5625), (M * d, 4.5625), (M * I, 2.5625 + h_amax)],
         # amax pass (2) + one pass reading bf16 (2) and writing NVFP4 (0.5 + 1/16) and MXFP8 (1 + 1/32)
         "nvfp4_quantize_requant": [(E * 2 * I * d, 5.59375), (E * d * I, 5.59375), (M * d, 5.59375),
-                                   (M * I, 5.59375)],
-        "grouped_gemm_nvfp4_fwd": [fl13, fl2],
+                                   (M * I, 3.59375 + h_amax)],
+        "grouped_gemm_nvfp4_fwd": [fl2] if layer.fuse_swiglu else [fl13, fl2],
+        "grouped_gemm_nvfp4_fwd_swiglu": [fl13],
         "dequant_transpose_requant_sr": [(E * 2 * I * d, 1.59375), (E * d * I, 1.59375), (M * d, 1.59375),
                                          (M * I, 1.59375)],
         "mxfp8_quantize": [(M * d, 4.0625), (M * 2 * I, 4.0625)],

@@ -249,8 +249,9 @@ int nvfp4_quantize_requant(const void *x, int64_t batch, int64_t rows, int64_t c
  * x_codes [M_total][K/2], x_scales grouped layout (K/16 block columns),
  * x_outer_scale fp32 [1]; w_codes [E][N][K/2], w_scales batched layout,
  * w_outer_scale fp32 [E]; y [M_total][N] bf16 or fp32.
- * N % 128 == 0, K % 256 == 0.  x_bf16 must be NULL (reserved for a fused
- * producer-side activation quantization; non-NULL returns NV_ERR_UNSUPPORTED).
+ * N % 128 == 0, K % 256 == 0; y 32-byte aligned (the kernels store 32 bytes
+ * at a time).  x_bf16 must be NULL (reserved for a fused producer-side
+ * activation quantization; non-NULL returns NV_ERR_UNSUPPORTED).
  * workspace: may be NULL (no scratch needed).
  */
 int grouped_gemm_nvfp4_fwd(const void *x_bf16, const float *x_outer_scale,
@@ -262,12 +263,36 @@ int grouped_gemm_nvfp4_fwd(const void *x_bf16, const float *x_outer_scale,
                            void *y, int y_dtype,
                            void *workspace, size_t workspace_bytes, nv_stream_t stream);
 
+/* ---- a3 + a4 fused: the w13 forward GEMM with SwiGLU in its epilogue ----------
+ * Chinese translation, Figure 5 (w13 GEMM -> Q -> w2 GEMM): the gate/up GEMM
+ * of grouped_gemm_nvfp4_fwd (bf16 output) on w13 = [E][2I][K] (gate rows
+ * 0..I-1 over up rows I..2I-1), and in the same kernel
+ *   y13 [M_total][2I] bf16  (bit-identical to grouped_gemm_nvfp4_fwd with
+ *                            NV_OUT_BF16),
+ *   h   [M_total][I]   bf16  (bit-identical to nvfp4moe_swiglu_fwd of y13),
+ *   h_outer_scale [1] fp32   (max |h| / 2688, or 1 when h is all zero:
+ *                            bit-identical to the outer scale nvfp4_quantize
+ *                            computes for h, so the quantization of h can take
+ *                            it as outer_scale_in and skip its amax pass).
+ * Each output tile holds 64 hidden features' gate and up columns; max |h| is
+ * reduced with atomic max (order-free, deterministic).
+ * I % 128 == 0, K % 256 == 0; y13 and h 32-byte aligned.  Other arguments as
+ * grouped_gemm_nvfp4_fwd.  No counterpart on the pages as one kernel.
+ */
+int grouped_gemm_nvfp4_fwd_swiglu(const float *x_outer_scale,
+                                  const uint8_t *x_codes, const uint8_t *x_scales,
+                                  const uint8_t *w13_codes, const uint8_t *w13_scales,
+                                  const float *w13_outer_scale,
+                                  const int32_t *group_offsets, int32_t E,
+                                  int64_t M_total, int64_t I, int64_t K,
+                                  void *y13, void *h, float *h_outer_scale, nv_stream_t stream);
+
 /* ---- a7: grouped MXFP8 dgrad  dx_e = g_e w_e -----------------------------------
  * "Block-scaled backward passes": dx = g w_q, here with both operands MXFP8.
  * g_codes [M_total][N] + g_scales (mxfp8_quantize row-wise output, grouped
  * layout); wt_codes [E][K][N] + wt_scales (dequant_transpose_requant_sr of the
- * weights [E][N][K]); dx [M_total][K] bf16 or fp32.  N % 128 == 0,
- * K % 128 == 0.
+ * weights [E][N][K]); dx [M_total][K] bf16 or fp32, 32-byte aligned.
+ * N % 128 == 0, K % 128 == 0.
  */
 int grouped_gemm_mxfp8_dx(const uint8_t *g_codes, const uint8_t *g_scales,
                           const uint8_t *wt_codes, const uint8_t *wt_scales,
@@ -283,8 +308,8 @@ int grouped_gemm_mxfp8_dx(const uint8_t *g_codes, const uint8_t *g_scales,
  * the tokens of expert e, zero-padded to a multiple of 128.
  * gt_codes [N][P_cap] + gt_scales (mxfp8_quantize transposed output of g),
  * xt_codes [K][P_cap] + xt_scales (dequant_transpose_requant_sr of x_q);
- * dw [E][N][K] fp32 (experts without tokens get zeros).  N % 128 == 0,
- * K % 128 == 0.
+ * dw [E][N][K] fp32 (experts without tokens get zeros), 32-byte aligned.
+ * N % 128 == 0, K % 128 == 0.
  */
 int grouped_gemm_mxfp8_dw(const uint8_t *gt_codes, const uint8_t *gt_scales,
                           const uint8_t *xt_codes, const uint8_t *xt_scales,

@@ -24,6 +24,7 @@ int *status_ptr() {
 }
 
 static bool al16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+static bool al32(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }  // GEMM outputs: 32-byte stores
 static int64_t rup(int64_t a, int64_t b) { return (a + b - 1) / b * b; }
 
 static int amax_blocks(int64_t per_batch) {
@@ -224,12 +225,39 @@ int grouped_gemm_nvfp4_fwd(const void *x_bf16, const float *x_outer_scale, const
   if (!x_outer_scale || !x_codes || !x_scales || !w_codes || !w_scales || !w_outer_scale || !y) return NV_ERR_ARG;
   if (y_dtype != NV_OUT_BF16 && y_dtype != NV_OUT_FP32) return NV_ERR_ARG;
   if (N % 128 || K % 256) return NV_ERR_SHAPE;
-  if (!al16(x_codes) || !al16(x_scales) || !al16(w_codes) || !al16(w_scales) || !al16(y)) return NV_ERR_ALIGN;
+  if (!al16(x_codes) || !al16(x_scales) || !al16(w_codes) || !al16(w_scales) || !al32(y)) return NV_ERR_ALIGN;
   int *st = status_ptr();
   if (!st) return NV_ERR_CUDA;
   GemmProblem p = {kGemmNvfp4Fwd, x_codes, x_scales, w_codes, w_scales, x_outer_scale, w_outer_scale,
                    group_offsets, E, M_total, N, K, y, y_dtype == NV_OUT_FP32};
   return launch_grouped_gemm(p, st, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int grouped_gemm_nvfp4_fwd_swiglu(const float *x_outer_scale, const uint8_t *x_codes, const uint8_t *x_scales,
+                                  const uint8_t *w_codes, const uint8_t *w_scales, const float *w_outer_scale,
+                                  const int32_t *group_offsets, int32_t E, int64_t M_total, int64_t I, int64_t K,
+                                  void *y13, void *h, float *h_outer_scale, nv_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (I <= 0) return NV_ERR_ARG;
+  int r = gemm_common_checks(group_offsets, E, M_total, 2 * I, K);
+  if (r != NV_OK) return r;
+  if (!x_outer_scale || !x_codes || !x_scales || !w_codes || !w_scales || !w_outer_scale || !y13 || !h ||
+      !h_outer_scale)
+    return NV_ERR_ARG;
+  if (I % 128 || K % 256) return NV_ERR_SHAPE;
+  if (!al16(x_codes) || !al16(x_scales) || !al16(w_codes) || !al16(w_scales) || !al32(y13) || !al32(h) ||
+      !al16(h_outer_scale))
+    return NV_ERR_ALIGN;
+  int *st = status_ptr();
+  if (!st) return NV_ERR_CUDA;
+  if (cudaMemsetAsync(h_outer_scale, 0, sizeof(float), s) != cudaSuccess) return NV_ERR_CUDA;
+  if (M_total > 0) {
+    GemmProblem p = {kGemmNvfp4FwdSwiglu, x_codes, x_scales, w_codes, w_scales, x_outer_scale, w_outer_scale,
+                     group_offsets, E, M_total, 2 * I, K, y13, 0, h, h_outer_scale};
+    r = launch_grouped_gemm(p, st, s);
+    if (r != NV_OK) return r;
+  }
+  return launch_outer_scale_from_amax(h_outer_scale, s);
 }
 
 int grouped_gemm_mxfp8_dx(const uint8_t *g_codes, const uint8_t *g_scales, const uint8_t *wt_codes,
@@ -242,7 +270,7 @@ int grouped_gemm_mxfp8_dx(const uint8_t *g_codes, const uint8_t *g_scales, const
   if (!g_codes || !g_scales || !wt_codes || !wt_scales || !dx) return NV_ERR_ARG;
   if (dx_dtype != NV_OUT_BF16 && dx_dtype != NV_OUT_FP32) return NV_ERR_ARG;
   if (N % 128 || K % 128) return NV_ERR_SHAPE;
-  if (!al16(g_codes) || !al16(g_scales) || !al16(wt_codes) || !al16(wt_scales) || !al16(dx)) return NV_ERR_ALIGN;
+  if (!al16(g_codes) || !al16(g_scales) || !al16(wt_codes) || !al16(wt_scales) || !al32(dx)) return NV_ERR_ALIGN;
   int *st = status_ptr();
   if (!st) return NV_ERR_CUDA;
   GemmProblem p = {kGemmMxfp8Dx, g_codes, g_scales, wt_codes, wt_scales, nullptr, nullptr,
@@ -259,7 +287,7 @@ int grouped_gemm_mxfp8_dw(const uint8_t *gt_codes, const uint8_t *gt_scales, con
   if (r != NV_OK) return r;
   if (!gt_codes || !gt_scales || !xt_codes || !xt_scales || !dw) return NV_ERR_ARG;
   if (N % 128 || K % 128) return NV_ERR_SHAPE;
-  if (!al16(gt_codes) || !al16(gt_scales) || !al16(xt_codes) || !al16(xt_scales) || !al16(dw)) return NV_ERR_ALIGN;
+  if (!al16(gt_codes) || !al16(gt_scales) || !al16(xt_codes) || !al16(xt_scales) || !al32(dw)) return NV_ERR_ALIGN;
   int *st = status_ptr();
   if (!st) return NV_ERR_CUDA;
   GemmProblem p = {kGemmMxfp8Dw, gt_codes, gt_scales, xt_codes, xt_scales, nullptr, nullptr,

@@ -79,6 +79,14 @@ __device__ __forceinline__ float bf16_hi_times(uint32_t w, uint16_t m) {
       : "=f"(d) : "r"(w), "h"(m), "f"(-0.0f));
   return d;
 }
+// SwiGLU in fp32 as every kernel of the library computes it (the elementwise
+// kernels and the fused GEMM epilogue must agree bit for bit):
+// h = (g * sigmoid(g)) * u with sigmoid(x) = 1 / (1 + e^-x), the exponential
+// from the hardware approximation (relative error ~1e-6 at these magnitudes,
+// far below the bf16 rounding that follows) and a correctly rounded
+// reciprocal (1 / inf = 0 for very negative x)
+__device__ __forceinline__ float sigmoidf_fast(float x) { return __frcp_rn(1.0f + __expf(-x)); }
+__device__ __forceinline__ float swiglu_h(float g, float u) { return g * sigmoidf_fast(g) * u; }
 // bf16 bits of a power of two held as fp32 (exact)
 __device__ __forceinline__ uint16_t pow2_bf16_bits(float p) { return (uint16_t)(__float_as_uint(p) >> 16); }
 

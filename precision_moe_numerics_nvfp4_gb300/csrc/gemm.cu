@@ -54,6 +54,16 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
                "l"(src), "r"(bytes), "r"(bar)
                : "memory");
 }
+// 8-byte asynchronous global -> shared copies in commit groups
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_prev_group() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all_groups() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
@@ -133,7 +143,7 @@ constexpr int kBN = 128;  // output tile columns (and rows: 128)
 
 template <int KIND, int STAGES, int NACC>
 struct Cfg {
-  static constexpr bool kFp4 = KIND == kGemmNvfp4Fwd;
+  static constexpr bool kFp4 = KIND == kGemmNvfp4Fwd || KIND == kGemmNvfp4FwdSwiglu;
   static constexpr int kAtomsPerStage = kFp4 ? 4 : 1;  // 128x4 scale tiles per 128 rows per stage
   static constexpr int A_BYTES = 128 * 128;
   static constexpr int B_BYTES = kBN * 128;
@@ -170,6 +180,10 @@ struct GemmArgs {
   int64_t out_ld;
   int *status;
   uint64_t wait_limit;
+  // kGemmNvfp4FwdSwiglu
+  void *h;
+  unsigned *h_amax;
+  int64_t I;
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -196,12 +210,35 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uin
 struct Tile {
   int e, nk, a_row, b_row, mrows, k_off;
   int64_t a_tile, b_tile, k_atom0, out_row0, out_col0;
+  int64_t sfb_g, sfb_u;  // SwiGLU kind: scale tiles of the gate and up rows
+  int bh;                // SwiGLU kind: which 64-row half of those tiles
 };
 
 template <int KIND>
 __device__ __forceinline__ Tile decode_tile(int t, const GemmArgs &A, const int *s_off, const int *s_pad) {
   Tile T;
-  if (KIND != kGemmMxfp8Dw) {
+  if (KIND == kGemmNvfp4FwdSwiglu) {
+    // 128 rows x 64 hidden features: B = gate rows [64 nt, 64 nt + 64) over the
+    // matching up rows (I further down the expert's w13)
+    const int pm = t / A.ntn, nt = t - (t / A.ntn) * A.ntn;
+    const int p0 = pm * 128;
+    const int e = find_group(s_pad, A.E, p0);
+    T.e = e;
+    T.a_row = s_off[e] + (p0 - s_pad[e]);
+    T.mrows = min(128, s_off[e + 1] - T.a_row);
+    const int64_t g_row = (int64_t)e * 2 * A.I + (int64_t)nt * 64;
+    T.b_row = (int)g_row;
+    T.sfb_g = g_row / 128;
+    T.sfb_u = (g_row + A.I) / 128;
+    T.bh = nt & 1;  // I % 128 == 0: gate and up rows sit in the same half of their tiles
+    T.a_tile = pm;
+    T.b_tile = 0;
+    T.nk = (int)(A.K / 256);
+    T.k_off = 0;
+    T.k_atom0 = 0;
+    T.out_row0 = T.a_row;
+    T.out_col0 = (int64_t)nt * 64;
+  } else if (KIND != kGemmMxfp8Dw) {
     const int pm = t / A.ntn, nt = t - (t / A.ntn) * A.ntn;
     const int p0 = pm * 128;
     const int e = find_group(s_pad, A.E, p0);
@@ -264,7 +301,10 @@ __global__ void __launch_bounds__(192, 2)
   uint64_t *full = bars, *empty = bars + STAGES, *acc_full = bars + 2 * STAGES, *acc_empty = acc_full + NACC;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(smem_u32(&full[s]), 1);
+      // SwiGLU kind: the 32 producer lanes' arrivals (their scale copies
+      // landed and made visible to the tensor core) come on top of the TMA
+      // transaction arrival
+      mbar_init(smem_u32(&full[s]), KIND == kGemmNvfp4FwdSwiglu ? 33 : 1);
       mbar_init(smem_u32(&empty[s]), 1);
     }
     for (int b = 0; b < NACC; ++b) {
@@ -280,10 +320,12 @@ __global__ void __launch_bounds__(192, 2)
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
 
-  if (warp == 0 && lane == 0) {
-    // ---- producer -----------------------------------------------------------
-    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmA) : "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmB) : "memory");
+  if (warp == 0 && (lane == 0 || KIND == kGemmNvfp4FwdSwiglu)) {
+    // ---- producer (lane 0; the whole warp for the SwiGLU kind) ------------------
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(&tmA) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(&tmB) : "memory");
+    }
     uint32_t it = 0;  // global stage counter of this CTA
     bool ok = true;
     for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
@@ -296,17 +338,52 @@ __global__ void __launch_bounds__(192, 2)
           break;
         }
         const uint32_t fb = smem_u32(&full[s]);
-        mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
-        tma_load_2d(smem_u32(sA + s * C::A_BYTES), &tmA, T.k_off + ks * 128, T.a_row, fb);
-        tma_load_2d(smem_u32(sB + s * C::B_BYTES), &tmB, T.k_off + ks * 128, T.b_row, fb);
         const int64_t katom = T.k_atom0 + (int64_t)ks * C::kAtomsPerStage;
-        bulk_load(smem_u32(sSFA + s * C::SFA_BYTES), A.a_scales + (T.a_tile * A.ka + katom) * 512, C::SFA_BYTES,
-                  fb);
+        if (KIND == kGemmNvfp4FwdSwiglu) {
+          if (lane == 0) {
+            mbar_arrive_expect_tx(fb, C::STAGE_BYTES - C::SFB_BYTES);
+            tma_load_2d(smem_u32(sA + s * C::A_BYTES), &tmA, T.k_off + ks * 128, T.a_row, fb);
+            tma_load_2d(smem_u32(sB + s * C::B_BYTES), &tmB, T.k_off + ks * 128, T.b_row, fb);
+            tma_load_2d(smem_u32(sB + s * C::B_BYTES + 64 * 128), &tmB, T.k_off + ks * 128, T.b_row + (int)A.I,
+                        fb);
+            bulk_load(smem_u32(sSFA + s * C::SFA_BYTES), A.a_scales + (T.a_tile * A.ka + katom) * 512,
+                      C::SFA_BYTES, fb);
+          }
+          // the B scale tiles of the 64 gate + 64 up rows: row `lane` of each
+          // 128x4 tile holds B rows lane, lane+32 (gate: 8 bytes of the gate
+          // rows' tile) and lane+64, lane+96 (up: 8 bytes of the up rows' tile)
 #pragma unroll
-        for (int j = 0; j < kBN / 128; ++j)
-          bulk_load(smem_u32(sSFB + s * C::SFB_BYTES + j * C::SFA_BYTES),
-                    A.b_scales + ((T.b_tile + j) * A.ka + katom) * 512, C::SFA_BYTES, fb);
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t dst = smem_u32(sSFB + s * C::SFB_BYTES + j * 512 + lane * 16);
+            cp_async8(dst, A.b_scales + (T.sfb_g * A.ka + katom + j) * 512 + lane * 16 + 8 * T.bh);
+            cp_async8(dst + 8, A.b_scales + (T.sfb_u * A.ka + katom + j) * 512 + lane * 16 + 8 * T.bh);
+          }
+          cp_async_commit();
+          // one stage behind: the previous stage's copies have landed; the
+          // proxy fence makes them visible to tcgen05.cp, then this lane
+          // arrives on that stage's barrier (off the MMA thread's path)
+          if (it >= 1) {
+            cp_async_wait_prev_group();
+            fence_proxy_async_smem();
+            mbar_arrive(smem_u32(&full[(it - 1) % STAGES]));
+          }
+        } else {
+          mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+          tma_load_2d(smem_u32(sA + s * C::A_BYTES), &tmA, T.k_off + ks * 128, T.a_row, fb);
+          tma_load_2d(smem_u32(sB + s * C::B_BYTES), &tmB, T.k_off + ks * 128, T.b_row, fb);
+          bulk_load(smem_u32(sSFA + s * C::SFA_BYTES), A.a_scales + (T.a_tile * A.ka + katom) * 512, C::SFA_BYTES,
+                    fb);
+#pragma unroll
+          for (int j = 0; j < kBN / 128; ++j)
+            bulk_load(smem_u32(sSFB + s * C::SFB_BYTES + j * C::SFA_BYTES),
+                      A.b_scales + ((T.b_tile + j) * A.ka + katom) * 512, C::SFA_BYTES, fb);
+        }
       }
+    }
+    if (KIND == kGemmNvfp4FwdSwiglu && it >= 1) {  // the last stage's scale copies
+      cp_async_wait_all_groups();
+      fence_proxy_async_smem();
+      mbar_arrive(smem_u32(&full[(it - 1) % STAGES]));
     }
     // drain: every copy this thread issued has landed before the CTA leaves
     const uint32_t first = it > STAGES ? it - STAGES : 0;
@@ -373,7 +450,7 @@ __global__ void __launch_bounds__(192, 2)
       if (!wait_or_abort(smem_u32(&acc_full[acc]), (tc / NACC) & 1, A.wait_limit, s_abort, A.status)) break;
       tc_fence_after();
       float alpha = 1.0f;
-      if (KIND == kGemmNvfp4Fwd) alpha = __fmul_rn(A.a_sg[0], A.b_sg[T.e]);
+      if (KIND == kGemmNvfp4Fwd || KIND == kGemmNvfp4FwdSwiglu) alpha = __fmul_rn(A.a_sg[0], A.b_sg[T.e]);
       const bool store = row < T.mrows;
       const int64_t orow = T.out_row0 + row;
       // read the whole accumulator row into registers, release the
@@ -391,7 +468,39 @@ __global__ void __launch_bounds__(192, 2)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&acc_empty[acc]));
-      if (store) {
+      if (KIND == kGemmNvfp4FwdSwiglu) {
+        // columns 0-63: gate, 64-127: up of hidden features out_col0 .. +63.
+        // y13 = bf16(acc * alpha) exactly as the plain bf16 output; h from the
+        // rounded gate and up with the SwiGLU kernel's arithmetic; max |h| of
+        // the rows that exist, one atomic per warp (max is order-free)
+        float hmax = 0.0f;
+        if (store) {
+          uint16_t *yg = static_cast<uint16_t *>(A.out) + orow * (2 * A.I) + T.out_col0;
+          uint16_t *yu = yg + A.I;
+          uint16_t *hp = static_cast<uint16_t *>(A.h) + orow * A.I + T.out_col0;
+#pragma unroll
+          for (int i = 0; i < 64; i += 16) {
+            uint32_t wg[8], wu[8], wh[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              wg[k] = pack_bf16x2(__fmul_rn(__uint_as_float(r[i + 2 * k]), alpha),
+                                  __fmul_rn(__uint_as_float(r[i + 2 * k + 1]), alpha));
+              wu[k] = pack_bf16x2(__fmul_rn(__uint_as_float(r[64 + i + 2 * k]), alpha),
+                                  __fmul_rn(__uint_as_float(r[64 + i + 2 * k + 1]), alpha));
+              const float h0 = swiglu_h(bf16_lo(wg[k]), bf16_lo(wu[k]));
+              const float h1 = swiglu_h(bf16_hi(wg[k]), bf16_hi(wu[k]));
+              wh[k] = f32_to_bf16_bits(h0) | (f32_to_bf16_bits(h1) << 16);
+              hmax = fmaxf(hmax, fmaxf(fabsf(bf16_lo(wh[k])), fabsf(bf16_hi(wh[k]))));
+            }
+            st_cs_v8(yg + i, wg[0], wg[1], wg[2], wg[3], wg[4], wg[5], wg[6], wg[7]);
+            st_cs_v8(yu + i, wu[0], wu[1], wu[2], wu[3], wu[4], wu[5], wu[6], wu[7]);
+            st_cs_v8(hp + i, wh[0], wh[1], wh[2], wh[3], wh[4], wh[5], wh[6], wh[7]);
+          }
+        }
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) hmax = fmaxf(hmax, __shfl_xor_sync(0xFFFFFFFFu, hmax, d));
+        if (lane == 0 && hmax > 0.0f) atomicMax(A.h_amax, __float_as_uint(hmax));
+      } else if (store) {
         if (A.out_fp32) {
           float *dst = static_cast<float *>(A.out) + orow * A.out_ld + T.out_col0;
 #pragma unroll
@@ -994,13 +1103,19 @@ int launch_grouped_gemm(const GemmProblem &p, int *status, cudaStream_t s) {
   a.groups = p.groups; a.E = p.E; a.M_total = p.M_total; a.N = p.N; a.K = p.K;
   a.out = p.out; a.out_fp32 = p.out_fp32; a.status = status;
   a.wait_limit = (uint64_t)1 << 26;
-  const int64_t out_cols = p.kind == kGemmNvfp4Fwd ? p.N : p.K;
+  a.h = p.h; a.h_amax = reinterpret_cast<unsigned *>(p.h_amax); a.I = p.N / 2;
+  const int64_t out_cols = (p.kind == kGemmNvfp4Fwd || p.kind == kGemmNvfp4FwdSwiglu) ? p.N : p.K;
   CUtensorMap ta, tb;
   bool ok;
   switch (p.kind) {
     case kGemmNvfp4Fwd:
       ok = make_map(&ta, p.a_codes, p.K / 2, p.M_total, p.K / 2, 128) &&
            make_map(&tb, p.b_codes, p.K / 2, (uint64_t)p.E * p.N, p.K / 2, kBN);
+      a.ka = p.K / 64;
+      break;
+    case kGemmNvfp4FwdSwiglu:  // B in boxes of 64 rows: gate rows, then the matching up rows
+      ok = make_map(&ta, p.a_codes, p.K / 2, p.M_total, p.K / 2, 128) &&
+           make_map(&tb, p.b_codes, p.K / 2, (uint64_t)p.E * p.N, p.K / 2, 64);
       a.ka = p.K / 64;
       break;
     case kGemmMxfp8Dx:
@@ -1031,6 +1146,8 @@ int launch_grouped_gemm(const GemmProblem &p, int *status, cudaStream_t s) {
   // NVFP4 forward 4.13 / 3.31 / 3.96 -> 2; MXFP8 dgrad 2.54 / 2.72 / 2.71 and
   // wgrad 1.90 / 2.24 / 2.14 -> 3 when the experts hold several 128-row blocks
   // (a half-empty pair block wastes half of its MMAs), else 2.
+  if (p.kind == kGemmNvfp4FwdSwiglu)  // one kernel: 128 x (64 gate + 64 up), two CTAs per SM
+    return run<kGemmNvfp4FwdSwiglu, 3, 1>(ta, tb, a, max_tiles, s);
   const int forced = gemm_variant();
   const bool rows_ok = p.kind != kGemmMxfp8Dw || p.N % 256 == 0;  // wgrad: pair tiles of 256 rows
   const bool big_groups = p.kind == kGemmMxfp8Dw || p.M_total >= (int64_t)512 * p.E;

@@ -24,12 +24,15 @@ int launch_requant(const uint8_t *codes, const uint8_t *scales, const float *sg,
 int launch_nvfp4_requant(const uint16_t *x, const float *sg, int64_t batch, int64_t rows, int64_t cols,
                          const int32_t *groups, int E, uint8_t *codes, uint8_t *scales, uint64_t seed, uint64_t off,
                          uint8_t *out_codes, uint8_t *out_scales, int *status, cudaStream_t s);
+int launch_outer_scale_from_amax(float *amax_in_sg_out, cudaStream_t s);
 int launch_swiglu_fwd(const uint16_t *y13, int64_t M, int64_t I, uint16_t *h, cudaStream_t s);
 int launch_swiglu_bwd(const uint16_t *dh, const uint16_t *y13, int64_t M, int64_t I, uint16_t *dy13, cudaStream_t s);
 int launch_wait_selftest(int64_t spins, int *status, cudaStream_t s);
 
 // grouped GEMMs (gemm.cu)
-enum GemmKind { kGemmNvfp4Fwd = 0, kGemmMxfp8Dx = 1, kGemmMxfp8Dw = 2 };
+// kGemmNvfp4FwdSwiglu: the w13 forward GEMM (N = 2I rows of gate over up per
+// expert) with SwiGLU in the epilogue: y13 bf16, h bf16 and max |h|
+enum GemmKind { kGemmNvfp4Fwd = 0, kGemmMxfp8Dx = 1, kGemmMxfp8Dw = 2, kGemmNvfp4FwdSwiglu = 3 };
 struct GemmProblem {
   int kind;
   const uint8_t *a_codes, *a_scales, *b_codes, *b_scales;
@@ -39,6 +42,8 @@ struct GemmProblem {
   int64_t M_total, N, K;
   void *out;
   int out_fp32;
+  void *h;                   // kGemmNvfp4FwdSwiglu: h [M_total][N / 2] bf16
+  float *h_amax;             // kGemmNvfp4FwdSwiglu: max |h| accumulated (bits of a non-negative float)
 };
 int launch_grouped_gemm(const GemmProblem &p, int *status, cudaStream_t s);
 int set_gemm_variant(int v);  // 0 automatic, 1-3 forced (see nvfp4moe_set_gemm_kernel)

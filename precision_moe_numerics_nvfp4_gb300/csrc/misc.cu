@@ -6,7 +6,6 @@
 
 namespace nvm {
 
-__device__ __forceinline__ float sigmoidf_acc(float x) { return 1.0f / (1.0f + expf(-x)); }
 
 // h[m][j] = bf16(silu(gate) * up), gate = y13[m][j], up = y13[m][I + j]
 __global__ void __launch_bounds__(256) swiglu_fwd_kernel(const uint16_t *__restrict__ y13, int64_t M, int64_t I,
@@ -21,8 +20,8 @@ __global__ void __launch_bounds__(256) swiglu_fwd_kernel(const uint16_t *__restr
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const float g0 = bf16_lo(gw[k]), g1 = bf16_hi(gw[k]);
-      const float h0 = g0 * sigmoidf_acc(g0) * bf16_lo(uw[k]);
-      const float h1 = g1 * sigmoidf_acc(g1) * bf16_hi(uw[k]);
+      const float h0 = swiglu_h(g0, bf16_lo(uw[k]));
+      const float h1 = swiglu_h(g1, bf16_hi(uw[k]));
       o[k] = f32_to_bf16_bits(h0) | (f32_to_bf16_bits(h1) << 16);
     }
     *reinterpret_cast<uint4 *>(h + m * I + j) = make_uint4(o[0], o[1], o[2], o[3]);
@@ -49,7 +48,7 @@ __global__ void __launch_bounds__(256) swiglu_bwd_kernel(const uint16_t *__restr
       uint32_t a[2], b[2];
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
-        const float s = sigmoidf_acc(gg[q]);
+        const float s = sigmoidf_fast(gg[q]);
         a[q] = f32_to_bf16_bits(dd[q] * uu[q] * s * (1.0f + gg[q] * (1.0f - s)));
         b[q] = f32_to_bf16_bits(dd[q] * gg[q] * s);
       }

@@ -706,6 +706,13 @@ int launch_amax(const uint16_t *x, int64_t batch, int64_t per_batch, float *part
   return launch_status(cudaGetLastError());
 }
 
+// sg = amax / 2688 (1 for a zero amax) in place, exactly as the amax pass
+// finishes (one partial maximum)
+int launch_outer_scale_from_amax(float *amax_in_sg_out, cudaStream_t s) {
+  outer_scale_finalize_kernel<<<1, 32, 0, s>>>(amax_in_sg_out, 1, amax_in_sg_out);
+  return launch_status(cudaGetLastError());
+}
+
 int launch_nvfp4_quant(const uint16_t *x, int64_t batch, int64_t rows, int64_t cols, const int32_t *groups, int E,
                        const float *sg, uint8_t *codes, uint8_t *scales, int *status, cudaStream_t s) {
   NvQuantArgs A;

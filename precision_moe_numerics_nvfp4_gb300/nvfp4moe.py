@@ -46,6 +46,8 @@ _SIGS = {
                                                     _P, _P, _P]),
     "grouped_gemm_nvfp4_fwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _I32, _I64, _I64, _I64,
                                               _P, ctypes.c_int, _P, _SZ, _P]),
+    "grouped_gemm_nvfp4_fwd_swiglu": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I32, _I64, _I64, _I64, _P, _P,
+                                                     _P, _P]),
     "grouped_gemm_mxfp8_dx": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I64, _I64, _I64, _P, ctypes.c_int,
                                              _P, _SZ, _P]),
     "grouped_gemm_mxfp8_dw": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I64, _I64, _I64, _P, _P, _SZ, _P]),
@@ -202,6 +204,14 @@ def grouped_gemm_nvfp4_fwd(x_bf16, x_outer_scale, x_codes, x_scales, w_codes, w_
     return _check("grouped_gemm_nvfp4_fwd", lib().grouped_gemm_nvfp4_fwd(
         _ptr(x_bf16), _ptr(x_outer_scale), _ptr(x_codes), _ptr(x_scales), _ptr(w_codes), _ptr(w_scales),
         _ptr(w_outer_scale), _ptr(group_offsets), E, M_total, N, K, _ptr(y), y_dtype, _ptr(workspace), ws_bytes,
+        _stream(stream)))
+
+
+def grouped_gemm_nvfp4_fwd_swiglu(x_outer_scale, x_codes, x_scales, w13_codes, w13_scales, w13_outer_scale,
+                                  group_offsets, E, M_total, I, K, y13, h, h_outer_scale, stream=None):
+    return _check("grouped_gemm_nvfp4_fwd_swiglu", lib().grouped_gemm_nvfp4_fwd_swiglu(
+        _ptr(x_outer_scale), _ptr(x_codes), _ptr(x_scales), _ptr(w13_codes), _ptr(w13_scales),
+        _ptr(w13_outer_scale), _ptr(group_offsets), E, M_total, I, K, _ptr(y13), _ptr(h), _ptr(h_outer_scale),
         _stream(stream)))
 
 

@@ -45,14 +45,15 @@ class NvTensor:
         self.sg = torch.empty(batch, dtype=F32, device=dev)
         self.ws = _u8(N.nvfp4moe_quantize_workspace_bytes(batch, rows, cols), dev)
 
-    def quantize(self, x, groups=None, stream=None):
-        N.nvfp4_quantize(x, self.batch, self.rows, self.cols, groups, None, self.sg, self.codes, self.scales,
+    def quantize(self, x, groups=None, stream=None, sg_in=None):
+        """`sg_in`: a given outer scale (skips the amax pass)."""
+        N.nvfp4_quantize(x, self.batch, self.rows, self.cols, groups, sg_in, self.sg, self.codes, self.scales,
                          self.ws, stream)
 
-    def quantize_requant(self, x, mx, seed, offset, groups=None, stream=None):
+    def quantize_requant(self, x, mx, seed, offset, groups=None, stream=None, sg_in=None):
         """quantize() plus the SR re-quantization of the result into `mx`
         (an MxTransposed), in one pass over x."""
-        N.nvfp4_quantize_requant(x, self.batch, self.rows, self.cols, groups, None, self.sg, self.codes,
+        N.nvfp4_quantize_requant(x, self.batch, self.rows, self.cols, groups, sg_in, self.sg, self.codes,
                                  self.scales, self.ws, seed, offset, mx.codes, mx.scales, stream)
 
 
@@ -139,10 +140,13 @@ class MoELayer:
     nvfp4_quantize_requant, so the MXFP8 re-quantized operands of the
     backward come out of the forward's quantization pass; `fuse_requant=False`
     runs nvfp4_quantize in the forward and the four
-    dequant_transpose_requant_sr calls in the backward instead (same results,
-    bit for bit)."""
+    dequant_transpose_requant_sr calls in the backward instead.  The w13 GEMM
+    computes SwiGLU and the outer scale of h in its epilogue
+    (grouped_gemm_nvfp4_fwd_swiglu) when d_ff % 128 == 0; `fuse_swiglu=False`
+    runs the GEMM, nvfp4moe_swiglu_fwd and the amax pass of h instead.  Every
+    choice gives the same results, bit for bit."""
 
-    def __init__(self, M, d_model, d_ff, E, device="cuda", backward=True, fuse_requant=True):
+    def __init__(self, M, d_model, d_ff, E, device="cuda", backward=True, fuse_requant=True, fuse_swiglu=True):
         dev = torch.device(device)
         self.M, self.d, self.I, self.E = M, d_model, d_ff, E
         I2 = 2 * d_ff
@@ -154,6 +158,8 @@ class MoELayer:
         self.h = torch.empty((M, d_ff), dtype=BF16, device=dev)
         self.hq = NvTensor(1, M, d_ff, dev, E=E)
         self.y2 = torch.empty((M, d_model), dtype=BF16, device=dev)
+        self.fuse_swiglu = fuse_swiglu and d_ff % 128 == 0
+        self.h_sg = torch.empty(1, dtype=F32, device=dev)  # outer scale of h from the fused epilogue
         self.fuse_requant = fuse_requant and backward
         self._requant_seed = None  # seed of the operands the last forward re-quantized
         if not backward:  # forward-only use (sampling): no backward buffers
@@ -203,14 +209,21 @@ class MoELayer:
             self.xq.quantize(x, groups, stream)
         else:
             self.xq.quantize_requant(x, self.xt, seed, OFF_XQ, groups, stream)
-        N.grouped_gemm_nvfp4_fwd(None, self.xq.sg, self.xq.codes, self.xq.scales, self.w13q.codes,
-                                 self.w13q.scales, self.w13q.sg, groups, E, M, 2 * I, d, self.y13, N.NV_OUT_BF16,
-                                 None, stream)
-        N.nvfp4moe_swiglu_fwd(self.y13, M, I, self.h, stream)
-        if seed is None:
-            self.hq.quantize(self.h, groups, stream)
+        sg_h = None
+        if self.fuse_swiglu:
+            N.grouped_gemm_nvfp4_fwd_swiglu(self.xq.sg, self.xq.codes, self.xq.scales, self.w13q.codes,
+                                            self.w13q.scales, self.w13q.sg, groups, E, M, I, d, self.y13, self.h,
+                                            self.h_sg, stream)
+            sg_h = self.h_sg
         else:
-            self.hq.quantize_requant(self.h, self.ht, seed, OFF_HQ, groups, stream)
+            N.grouped_gemm_nvfp4_fwd(None, self.xq.sg, self.xq.codes, self.xq.scales, self.w13q.codes,
+                                     self.w13q.scales, self.w13q.sg, groups, E, M, 2 * I, d, self.y13, N.NV_OUT_BF16,
+                                     None, stream)
+            N.nvfp4moe_swiglu_fwd(self.y13, M, I, self.h, stream)
+        if seed is None:
+            self.hq.quantize(self.h, groups, stream, sg_in=sg_h)
+        else:
+            self.hq.quantize_requant(self.h, self.ht, seed, OFF_HQ, groups, stream, sg_in=sg_h)
         N.grouped_gemm_nvfp4_fwd(None, self.hq.sg, self.hq.codes, self.hq.scales, self.w2q.codes, self.w2q.scales,
                                  self.w2q.sg, groups, E, M, d, I, self.y2, N.NV_OUT_BF16, None, stream)
 
@@ -262,9 +275,12 @@ class MoELayer:
     def launches_per_step(self):
         """Kernels one step launches: forward = 4 NVFP4 quantizations x 3
         kernels (amax, finalize, quantize or quantize + requant) + 2 GEMMs +
-        SwiGLU; backward = (4 requants unless fused) + 2 MXFP8 quantizations +
-        4 GEMMs + SwiGLU backward."""
-        return (4 * 3 + 2 + 1) + (0 if self.fuse_requant else 4) + (2 + 4 + 1)
+        SwiGLU, or with the SwiGLU epilogue: 3 x 3 + the fused GEMM, the
+        outer-scale kernel and one kernel for h + the w2 GEMM; backward = (4
+        requants unless fused) + 2 MXFP8 quantizations + 4 GEMMs + SwiGLU
+        backward."""
+        fwd = (3 * 3 + 2 + 1 + 1) if self.fuse_swiglu else (4 * 3 + 2 + 1)
+        return fwd + (0 if self.fuse_requant else 4) + (2 + 4 + 1)
 
 
 class HostStaged:
