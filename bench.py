@@ -614,6 +614,47 @@ def run_gemm(args):
                       "TFLOP_s": flops / (ms / 1e3) / 1e12}))
 
 
+def run_rht_s2f6(args):
+    """RHT-32 + block-scaled S2F6 of the MoE layer's output (the combine
+    direction): 131072 routed rows x d_model 4096, bf16, values Student-t(3)
+    x 0.05 with 0.01% outliers x1000 (the quantization sweep's recipe at this
+    shape), a fixed random sign mask.  Quantize reads 2 and writes 1 + 1/32
+    bytes per value; the inverse reads 1 + 1/32 and writes 2 (bf16)."""
+    import torch
+    from precision_moe_numerics_nvfp4_gb300 import nvfp4moe as N
+    from precision_moe_numerics_nvfp4_gb300 import workloads as W
+
+    N.lib()
+    peaks = load_peaks()
+    rows, cols, mask = 131072, SHAPE["d_model"], 0x9E3779B9
+    x = W.quant_sweep((rows, cols), "cuda", seed=6)
+    codes = torch.empty((rows, cols), dtype=torch.int8, device="cuda")
+    scales = torch.empty((rows, cols // 32), dtype=torch.uint8, device="cuda")
+    y = torch.empty((rows, cols), dtype=torch.bfloat16, device="cuda")
+    ops = {
+        "rht32_s2f6_quantize": lambda: N.rht32_s2f6_quantize(x, rows, cols, mask, codes, scales),
+        "s2f6_dequantize_rht32_inverse": lambda: N.s2f6_dequantize_rht32_inverse(codes, scales, rows, cols, mask, y,
+                                                                                 N.NV_OUT_BF16),
+    }
+    for name, fn in ops.items():
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        s = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(args.steps):
+            fn()
+        e1.record(s)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        gbs = rows * cols * 3.03125 / (ms / 1e3) / 1e9
+        print(json.dumps({"workload": "rht_s2f6", "op": name, "shape": [rows, cols], "ms": ms, "GB_s": gbs,
+                          "frac_hbm": gbs / peaks["hbm_gbs"], "bytes_per_value": 3.03125,
+                          "peak_source": peaks["source"]}))
+    assert N.nvfp4moe_get_device_status() == 0
+
+
 def run_decode(args):
     """Sampler-style decode forward: 128 experts, SwiGLU gate/up [7168 -> 2048
     x2] and down [2048 -> 7168] quantized to NVFP4 beforehand (untimed), 256
@@ -662,7 +703,7 @@ def main(argv=None):
     ap.add_argument("--ref-tokens", type=int, default=64)
     ap.add_argument("--ref-dff", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["moe", "quant_sweep", "gemm", "decode"], default="moe")
+    ap.add_argument("--workload", choices=["moe", "quant_sweep", "gemm", "decode", "rht_s2f6"], default="moe")
     ap.add_argument("--gemm-kind", choices=["fwd", "dx", "dw"], default="fwd")
     ap.add_argument("--gemm-tokens", type=int, default=16384)
     ap.add_argument("--sweep-op", default=None)
@@ -676,6 +717,8 @@ def main(argv=None):
         run_quant_sweep(args)
     elif args.workload == "gemm":
         run_gemm(args)
+    elif args.workload == "rht_s2f6":
+        run_rht_s2f6(args)
     elif args.workload == "decode":
         run_decode(args)
     else:

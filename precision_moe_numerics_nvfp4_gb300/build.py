@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "lib")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(OUT_DIR, "libnvfp4moe.so")
-SOURCES = ["api.cu", "quant.cu", "misc.cu", "gemm.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "quant.cu", "misc.cu", "gemm.cu", "noalloc.cu", "s2f6.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

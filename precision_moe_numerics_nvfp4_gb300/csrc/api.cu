@@ -159,6 +159,27 @@ int nvfp4_quantize_requant(const void *x, int64_t batch, int64_t rows, int64_t c
                               out_scales, st, s);
 }
 
+int rht32_s2f6_quantize(const void *x, int64_t rows, int64_t cols, uint32_t signs, int8_t *codes, uint8_t *scales,
+                        nv_stream_t stream) {
+  if (!x || !codes || !scales || rows < 0 || cols < 0) return NV_ERR_ARG;
+  if (cols % 32) return NV_ERR_SHAPE;
+  if (!al16(x) || (reinterpret_cast<uintptr_t>(codes) & 7u)) return NV_ERR_ALIGN;
+  if (rows == 0 || cols == 0) return NV_OK;
+  return launch_rht32_s2f6_quantize(static_cast<const uint16_t *>(x), rows * cols, signs, codes, scales,
+                                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+int s2f6_dequantize_rht32_inverse(const int8_t *codes, const uint8_t *scales, int64_t rows, int64_t cols,
+                                  uint32_t signs, void *y, int y_dtype, nv_stream_t stream) {
+  if (!codes || !scales || !y || rows < 0 || cols < 0) return NV_ERR_ARG;
+  if (y_dtype != NV_OUT_BF16 && y_dtype != NV_OUT_FP32) return NV_ERR_ARG;
+  if (cols % 32) return NV_ERR_SHAPE;
+  if ((reinterpret_cast<uintptr_t>(codes) & 7u) || !al16(y)) return NV_ERR_ALIGN;
+  if (rows == 0 || cols == 0) return NV_OK;
+  return launch_s2f6_dequant_irht32(codes, scales, rows * cols, signs, y, y_dtype == NV_OUT_FP32,
+                                    reinterpret_cast<cudaStream_t>(stream));
+}
+
 int mxfp8_quantize(const void *x, int64_t rows, int64_t cols, const int32_t *group_offsets, int32_t num_groups,
                    int mode, uint64_t seed, uint64_t counter_offset_row, uint64_t counter_offset_t,
                    uint8_t *codes_row, uint8_t *scales_row, uint8_t *codes_t, uint8_t *scales_t,

@@ -25,6 +25,11 @@ int launch_nvfp4_requant(const uint16_t *x, const float *sg, int64_t batch, int6
                          const int32_t *groups, int E, uint8_t *codes, uint8_t *scales, uint64_t seed, uint64_t off,
                          uint8_t *out_codes, uint8_t *out_scales, int *status, cudaStream_t s);
 int launch_outer_scale_from_amax(float *amax_in_sg_out, cudaStream_t s);
+// RHT-32 + block-scaled S2F6 (s2f6.cu); n values, n % 32 == 0
+int launch_rht32_s2f6_quantize(const uint16_t *x, int64_t n, uint32_t signs, int8_t *codes, uint8_t *scales,
+                               cudaStream_t s);
+int launch_s2f6_dequant_irht32(const int8_t *codes, const uint8_t *scales, int64_t n, uint32_t signs, void *y,
+                               int y_fp32, cudaStream_t s);
 int launch_swiglu_fwd(const uint16_t *y13, int64_t M, int64_t I, uint16_t *h, cudaStream_t s);
 int launch_swiglu_bwd(const uint16_t *dh, const uint16_t *y13, int64_t M, int64_t I, uint16_t *dy13, cudaStream_t s);
 int launch_wait_selftest(int64_t spins, int *status, cudaStream_t s);

@@ -51,6 +51,8 @@ _SIGS = {
     "grouped_gemm_mxfp8_dx": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I64, _I64, _I64, _P, ctypes.c_int,
                                              _P, _SZ, _P]),
     "grouped_gemm_mxfp8_dw": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I64, _I64, _I64, _P, _P, _SZ, _P]),
+    "rht32_s2f6_quantize": (ctypes.c_int, [_P, _I64, _I64, ctypes.c_uint32, _P, _P, _P]),
+    "s2f6_dequantize_rht32_inverse": (ctypes.c_int, [_P, _P, _I64, _I64, ctypes.c_uint32, _P, ctypes.c_int, _P]),
     "nvfp4moe_swiglu_fwd": (ctypes.c_int, [_P, _I64, _I64, _P, _P]),
     "nvfp4moe_swiglu_bwd": (ctypes.c_int, [_P, _P, _I64, _I64, _P, _P]),
     "nvfp4moe_get_device_status": (ctypes.c_int, [_P]),
@@ -205,6 +207,16 @@ def grouped_gemm_nvfp4_fwd(x_bf16, x_outer_scale, x_codes, x_scales, w_codes, w_
         _ptr(x_bf16), _ptr(x_outer_scale), _ptr(x_codes), _ptr(x_scales), _ptr(w_codes), _ptr(w_scales),
         _ptr(w_outer_scale), _ptr(group_offsets), E, M_total, N, K, _ptr(y), y_dtype, _ptr(workspace), ws_bytes,
         _stream(stream)))
+
+
+def rht32_s2f6_quantize(x, rows, cols, signs, codes, scales, stream=None):
+    return _check("rht32_s2f6_quantize", lib().rht32_s2f6_quantize(
+        _ptr(x), rows, cols, int(signs) & 0xFFFFFFFF, _ptr(codes), _ptr(scales), _stream(stream)))
+
+
+def s2f6_dequantize_rht32_inverse(codes, scales, rows, cols, signs, y, y_dtype, stream=None):
+    return _check("s2f6_dequantize_rht32_inverse", lib().s2f6_dequantize_rht32_inverse(
+        _ptr(codes), _ptr(scales), rows, cols, int(signs) & 0xFFFFFFFF, _ptr(y), y_dtype, _stream(stream)))
 
 
 def grouped_gemm_nvfp4_fwd_swiglu(x_outer_scale, x_codes, x_scales, w13_codes, w13_scales, w13_outer_scale,

@@ -1,0 +1,65 @@
+"""RHT-32 + block-scaled S2F6 on the GPU against the oracle: codes and scales
+bit-exact (the oracle takes the transform in the kernel's fp32 order), the
+inverse bit-exact in fp32 and bf16, ragged row counts, zero blocks, outlier
+blocks and several sign masks; the round trip stays within the quantization
+step plus the transform's rounding."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import rht as R
+from precision_moe_numerics_nvfp4_gb300 import nvfp4moe as N
+from tests.gpu_helpers import bf16_f32, check_status, dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _x(rows, cols, seed):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    x = torch.randn((rows, cols), generator=g, device="cuda") * 3.0
+    if rows > 2:
+        x[1, :32] = 0.0                      # a zero block
+        x[2, 5] = 4000.0                     # an outlier block
+        x[0, 32:64] = 1e-30                  # a tiny block (subnormal range after scaling)
+    return x.to(torch.bfloat16).contiguous()
+
+
+@pytest.mark.parametrize("rows,cols,mask", [(1, 32, 0), (3, 64, 0xFFFFFFFF), (37, 256, 0x9E3779B9),
+                                            (129, 4096, 0x12345678), (5, 96, 0x80000001)])
+def test_quantize_and_inverse_match_oracle(rows, cols, mask):
+    x = _x(rows, cols, seed=rows + cols)
+    codes = torch.full((rows, cols), 0x55, dtype=torch.int8, device=dev())
+    scales = torch.full((rows, cols // 32), 0xAA, dtype=torch.uint8, device=dev())
+    N.rht32_s2f6_quantize(x, rows, cols, mask, codes, scales)
+    y32 = torch.empty((rows, cols), dtype=torch.float32, device=dev())
+    y16 = torch.empty((rows, cols), dtype=torch.bfloat16, device=dev())
+    N.s2f6_dequantize_rht32_inverse(codes, scales, rows, cols, mask, y32, N.NV_OUT_FP32)
+    N.s2f6_dequantize_rht32_inverse(codes, scales, rows, cols, mask, y16, N.NV_OUT_BF16)
+    check_status()
+    xf = bf16_f32(x)
+    want_c, want_s = R.rht_s2f6_quantize(xf, mask)
+    assert np.array_equal(codes.cpu().numpy(), want_c)
+    assert np.array_equal(scales.cpu().numpy(), want_s)
+    back = R.s2f6_dequantize_irht(want_c, want_s, mask)
+    assert np.array_equal(y32.cpu().numpy().view(np.uint32), back.view(np.uint32))
+    want16 = torch.from_numpy(back).to(torch.bfloat16)
+    assert torch.equal(y16.cpu().view(torch.int16), want16.view(torch.int16))
+    # round trip: within half a quantization step (in the rotated basis; the
+    # orthonormal inverse keeps the Euclidean error) plus transform rounding
+    err = np.abs(back.astype(np.float64) - xf).reshape(rows, -1, 32)
+    step = np.ldexp(1.0, want_s.astype(np.int64) - 127 - 6)[..., None]
+    yq = R.rht_f32(xf, mask).reshape(rows, -1, 32).astype(np.float64)
+    unsat = np.all(np.abs(yq) / (step * 64) <= 127.5 / 64, axis=-1)
+    e2 = np.sqrt((err ** 2).sum(-1))
+    bound = np.sqrt(32) * step[..., 0] / 2 + 1e-5 * np.sqrt((xf.reshape(rows, -1, 32) ** 2).sum(-1)) + 1e-30
+    assert np.all(e2[unsat] <= bound[unsat])
+
+
+def test_rejects_bad_arguments():
+    x = torch.zeros((2, 48), dtype=torch.bfloat16, device=dev())
+    c = torch.zeros((2, 48), dtype=torch.int8, device=dev())
+    s = torch.zeros((2, 2), dtype=torch.uint8, device=dev())
+    with pytest.raises(N.NvError):
+        N.rht32_s2f6_quantize(x, 2, 48, 0, c, s)          # cols % 32
+    with pytest.raises(N.NvError):
+        N.s2f6_dequantize_rht32_inverse(c, s, 2, 32, 0, x, 7)  # bad dtype
