@@ -114,7 +114,7 @@ int64_t nvfp4moe_scale_offset(int64_t rp, int64_t c, int64_t kblocks);
 /* Workspace bytes nvfp4_quantize needs when it computes the outer scales. */
 size_t nvfp4moe_quantize_workspace_bytes(int64_t batch, int64_t rows, int64_t cols);
 
-/* ---- a1 + a2: NVFP4 quantization ----------------------------------------------
+/* ---- NVFP4 quantization (amax -> outer scale, 1x16 RN) ----------------------------------------------
  * "Low-precision formats on Blackwell": block scaling by the largest value of
  * each 16 consecutive values, E4M3 block scale, FP32 outer scale per tensor;
  * "Recipe details": one outer scale per expert for weights.
@@ -124,7 +124,7 @@ size_t nvfp4moe_quantize_workspace_bytes(int64_t batch, int64_t rows, int64_t co
  *           (batch == 1 only) the expert groups of the rows, which selects the
  *           grouped scale layout.
  * outer_scale_in: NULL -> compute sg = amax / 2688 of every batch entry
- *           (step a1, one extra read of x) and write it to outer_scale_out
+ *           (the amax pass, one extra read of x) and write it to outer_scale_out
  *           [batch]; non-NULL -> fp32 [batch] scales to use (copied to
  *           outer_scale_out when that is non-NULL).
  * codes:    u8 [batch][rows][cols / 2].
@@ -166,7 +166,7 @@ int nvfp4_quantize_noalloc(const void *x, int64_t batch, int64_t rows, int64_t c
                            const float *outer_scale_in, float *outer_scale_out,
                            uint8_t *codes, uint8_t *scales, nv_stream_t stream);
 
-/* ---- a6 (and the MXFP8 RN sweep): MXFP8 quantization of a bf16 matrix --------
+/* ---- MXFP8 quantization of a bf16 matrix (the gradient, SR or RN) --------
  * Chinese translation of the pages, Figure 4: the BF16 gradient is quantized
  * to MXFP8 with SR once row-wise (DGRAD operand) and once after a transpose
  * (WGRAD operand).
@@ -194,7 +194,7 @@ int mxfp8_quantize(const void *x, int64_t rows, int64_t cols,
                    uint8_t *codes_row, uint8_t *scales_row,
                    uint8_t *codes_t, uint8_t *scales_t, nv_stream_t stream);
 
-/* ---- a5: dequantize -> transpose -> SR re-quantize NVFP4 -> MXFP8 -------------
+/* ---- dequantize -> transpose -> SR re-quantize NVFP4 -> MXFP8 -------------
  * "Re-quantization with stochastic rounding": the forward NVFP4 tensor is
  * dequantized (fp32: fp32(e2m1 * e4m3) * sg), transposed at that precision,
  * and re-quantized to MXFP8 with stochastic rounding, so that the backward
@@ -218,7 +218,7 @@ int dequant_transpose_requant_sr(const uint8_t *codes, const uint8_t *scales,
                                  uint8_t *out_codes, uint8_t *out_scales,
                                  nv_stream_t stream);
 
-/* ---- a2 + a5 in one pass: NVFP4 quantize and the SR re-quantization ----------
+/* ---- NVFP4 quantize and the SR re-quantization in one pass ----------
  * Both outputs of nvfp4_quantize (codes, scales, outer scale) and of
  * dequant_transpose_requant_sr applied to them (same seed and counter
  * offset), bit-identical to the two calls in sequence, from one read of the
@@ -241,7 +241,7 @@ int nvfp4_quantize_requant(const void *x, int64_t batch, int64_t rows, int64_t c
                            uint64_t seed, uint64_t counter_offset,
                            uint8_t *out_codes, uint8_t *out_scales, nv_stream_t stream);
 
-/* ---- a3: grouped NVFP4 forward GEMM  y_e = x_q,e w_q,e^T ----------------------
+/* ---- grouped NVFP4 forward GEMM  y_e = x_q,e w_q,e^T ----------------------
  * "Block-scaled backward passes": y = x_q w_q^T, 16-value blocks of a row of
  * x_q and of w_q multiplied pairwise and scaled by both block scales; the
  * outer scales multiply the result (y = acc * sg_x * sg_w[e]).
@@ -263,7 +263,7 @@ int grouped_gemm_nvfp4_fwd(const void *x_bf16, const float *x_outer_scale,
                            void *y, int y_dtype,
                            void *workspace, size_t workspace_bytes, nv_stream_t stream);
 
-/* ---- a3 + a4 fused: the w13 forward GEMM with SwiGLU in its epilogue ----------
+/* ---- fused: the w13 forward GEMM with SwiGLU in its epilogue ----------
  * Chinese translation, Figure 5 (w13 GEMM -> Q -> w2 GEMM): the gate/up GEMM
  * of grouped_gemm_nvfp4_fwd (bf16 output) on w13 = [E][2I][K] (gate rows
  * 0..I-1 over up rows I..2I-1), and in the same kernel
@@ -287,7 +287,7 @@ int grouped_gemm_nvfp4_fwd_swiglu(const float *x_outer_scale,
                                   int64_t M_total, int64_t I, int64_t K,
                                   void *y13, void *h, float *h_outer_scale, nv_stream_t stream);
 
-/* ---- a7: grouped MXFP8 dgrad  dx_e = g_e w_e -----------------------------------
+/* ---- grouped MXFP8 dgrad  dx_e = g_e w_e -----------------------------------
  * "Block-scaled backward passes": dx = g w_q, here with both operands MXFP8.
  * g_codes [M_total][N] + g_scales (mxfp8_quantize row-wise output, grouped
  * layout); wt_codes [E][K][N] + wt_scales (dequant_transpose_requant_sr of the
@@ -301,7 +301,7 @@ int grouped_gemm_mxfp8_dx(const uint8_t *g_codes, const uint8_t *g_scales,
                           void *dx, int dx_dtype,
                           void *workspace, size_t workspace_bytes, nv_stream_t stream);
 
-/* ---- a8: grouped MXFP8 wgrad  dw_e = g_e^T x_q,e ---------------------------------
+/* ---- grouped MXFP8 wgrad  dw_e = g_e^T x_q,e ---------------------------------
  * "Block-scaled backward passes": dw = g^T x_q, computed from the quantized
  * forward activations ("Quantized communications": the WGRAD input is the
  * quantized, not the high-precision, activation).  The contraction runs over
@@ -336,7 +336,7 @@ int grouped_gemm_mxfp8_dw(const uint8_t *gt_codes, const uint8_t *gt_scales,
  * the same contraction with fp32 accumulation; summation order differs. */
 int nvfp4moe_set_gemm_kernel(int variant);
 
-/* ---- NEXT-4: 32-point random Hadamard transform + block-scaled S2F6 -------------
+/* ---- 32-point random Hadamard transform + block-scaled S2F6 -------------
  * "Quantized communications": the data of the combine direction is rotated by
  * a 32-dimensional random Hadamard transform and quantized to S2F6 (two signed
  * integer bits, six fractional bits: value k/64, k in [-128, 127]) with one
@@ -351,11 +351,17 @@ int nvfp4moe_set_gemm_kernel(int variant);
  *       an all-zero block gets code 0), k = RN(y * 2^-e * 64) ties to even,
  *       saturating to [-128, 127];
  *   inverse x = d * (H (k / 64 * 2^e)) / sqrt(32) in the same fp32 order.
- * x bf16 [rows][cols], codes int8 [rows][cols] (8-byte aligned), scales uint8
- * [rows][cols / 32] (row-major, no swizzle: not an MMA operand), y bf16 or
- * fp32 [rows][cols] (16-byte aligned).  cols % 32 == 0.  No counterpart of
- * the kernels themselves on the pages (their conversions are PTX
- * instructions this toolkit does not accept; the rounding is written out).
+ * x bf16 [rows][cols], codes int8 [rows][cols], scales uint8 [rows][cols / 32]
+ * (row-major, no swizzle: not an MMA operand), y bf16 or fp32 [rows][cols]
+ * (y_dtype NV_OUT_BF16 or NV_OUT_FP32); x, codes and y 32-byte aligned (the
+ * kernels move 32 bytes per access); cols % 32 == 0.  All buffers are device
+ * memory owned by the caller; the call only enqueues work on `stream` (no
+ * allocation, no synchronization).  Returns NV_OK (also for rows or cols 0),
+ * NV_ERR_ARG (null pointer, negative size, unknown y_dtype), NV_ERR_SHAPE
+ * (cols % 32 != 0), NV_ERR_ALIGN, or NV_ERR_CUDA (launch failure); nothing is
+ * written on error.  No counterpart of the kernels themselves on the pages
+ * (their conversions are PTX instructions this toolkit does not accept; the
+ * rounding is written out).
  */
 int rht32_s2f6_quantize(const void *x, int64_t rows, int64_t cols, uint32_t signs,
                         int8_t *codes, uint8_t *scales, nv_stream_t stream);
@@ -363,7 +369,7 @@ int s2f6_dequantize_rht32_inverse(const int8_t *codes, const uint8_t *scales,
                                   int64_t rows, int64_t cols, uint32_t signs,
                                   void *y, int y_dtype, nv_stream_t stream);
 
-/* ---- a4: SwiGLU between the expert GEMMs (Figure 5: w13 GEMM, Q, w2 GEMM) -----
+/* ---- SwiGLU between the expert GEMMs (Figure 5: w13 GEMM, Q, w2 GEMM) -----
  * y13 bf16 [M][2I] (gate columns 0..I-1, up columns I..2I-1);
  * h = bf16(silu(gate) * up) computed in fp32, silu(x) = x / (1 + exp(-x)).
  * Backward: dy13 = [dh * up * silu'(gate), dh * silu(gate)] as bf16.

@@ -163,7 +163,7 @@ int rht32_s2f6_quantize(const void *x, int64_t rows, int64_t cols, uint32_t sign
                         nv_stream_t stream) {
   if (!x || !codes || !scales || rows < 0 || cols < 0) return NV_ERR_ARG;
   if (cols % 32) return NV_ERR_SHAPE;
-  if (!al16(x) || (reinterpret_cast<uintptr_t>(codes) & 7u)) return NV_ERR_ALIGN;
+  if (!al32(x) || !al32(codes)) return NV_ERR_ALIGN;
   if (rows == 0 || cols == 0) return NV_OK;
   return launch_rht32_s2f6_quantize(static_cast<const uint16_t *>(x), rows * cols, signs, codes, scales,
                                     reinterpret_cast<cudaStream_t>(stream));
@@ -174,7 +174,7 @@ int s2f6_dequantize_rht32_inverse(const int8_t *codes, const uint8_t *scales, in
   if (!codes || !scales || !y || rows < 0 || cols < 0) return NV_ERR_ARG;
   if (y_dtype != NV_OUT_BF16 && y_dtype != NV_OUT_FP32) return NV_ERR_ARG;
   if (cols % 32) return NV_ERR_SHAPE;
-  if ((reinterpret_cast<uintptr_t>(codes) & 7u) || !al16(y)) return NV_ERR_ALIGN;
+  if (!al32(codes) || !al32(y)) return NV_ERR_ALIGN;
   if (rows == 0 || cols == 0) return NV_OK;
   return launch_s2f6_dequant_irht32(codes, scales, rows * cols, signs, y, y_dtype == NV_OUT_FP32,
                                     reinterpret_cast<cudaStream_t>(stream));

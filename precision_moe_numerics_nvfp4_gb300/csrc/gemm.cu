@@ -1,5 +1,5 @@
 // Grouped block-scaled expert GEMMs on the 5th-generation tensor cores
-// (tcgen05), steps a3, a7 and a8 of the hot path:
+// (tcgen05), the three expert GEMMs of the layer's training step:
 //   NVFP4 forward   y_e  = x_q,e w_q,e^T      kind::mxf4nvf4, E4M3 scales / 16
 //   MXFP8 dgrad     dx_e = g_e w_e            kind::mxf8f6f4, E8M0 scales / 32
 //   MXFP8 wgrad     dw_e = g_e^T x_q,e        kind::mxf8f6f4, contraction over
@@ -110,14 +110,6 @@ __device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t *v) {
       : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-// 32-byte streaming store (evict-first): the GEMM outputs are written once
-__device__ __forceinline__ void st_cs_v8(void *p, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t a4,
-                                         uint32_t a5, uint32_t a6, uint32_t a7) {
-  asm volatile("st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a0), "r"(a1), "r"(a2),
-               "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
-               : "memory");
-}
 
 // Shared-memory matrix descriptor, K-major operand tile with rows of 128 bytes
 // in the 128-byte swizzle (8-row groups 1024 bytes apart).

@@ -1,8 +1,8 @@
 // Quantization kernels of libnvfp4moe.so (HBM-bound):
-//   amax_partial / outer_scale_finalize   step a1: per-tensor amax -> sg
-//   nvfp4_quant                           step a2: bf16 -> NVFP4 1x16 (RN)
+//   amax_partial / outer_scale_finalize   per-tensor amax -> FP32 outer scale sg
+//   nvfp4_quant                           bf16 -> NVFP4 1x16 (RN)
 //   mxfp8_rowwise                         MXFP8 1x32 along rows (RN or SR)
-//   mx_transpose<...>                     steps a5 / a6: transpose through
+//   mx_transpose<...>                     transpose through
 //                                         shared memory + MXFP8 (SR or RN)
 //                                         of bf16 or dequantized NVFP4 input
 //
@@ -22,7 +22,7 @@
 namespace nvm {
 
 // ---------------------------------------------------------------------------
-// a1: amax
+// per-tensor amax
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) amax_partial_kernel(const uint16_t *__restrict__ x,
                                                            int64_t per_batch, float *__restrict__ partial,
@@ -129,7 +129,7 @@ __device__ __forceinline__ bool setup_groups(GroupSmem &g, const int32_t *go, in
 }
 
 // ---------------------------------------------------------------------------
-// a2: NVFP4 quantization, one CTA = 128 padded rows x 256 columns
+// NVFP4 quantization, one CTA = 128 padded rows x 256 columns
 // ---------------------------------------------------------------------------
 struct NvQuantArgs {
   const uint16_t *x;
@@ -317,7 +317,8 @@ __global__ void __launch_bounds__(256) mxfp8_rowwise_kernel(const __grid_constan
 }
 
 // ---------------------------------------------------------------------------
-// Transposed MXFP8 (a5 and the WGRAD operand of a6): one CTA = 128 padded
+// Transposed MXFP8 (the SR re-quantization of saved NVFP4 operands, and the
+// WGRAD operand of the gradient quantizer): one CTA = 128 padded
 // source rows (one window) x 128 source columns.  Three sources (kMode):
 //   kSrcBf16        bf16 -> MXFP8 SR/RN, transposed (+ optional row-wise)
 //   kSrcNvfp4       NVFP4 codes + scales + outer scale -> dequantize ->

@@ -49,27 +49,28 @@ __device__ __forceinline__ float pow2f_exact(int e) {
   return e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(0x00400000u);
 }
 
-// One block of 32 values per lane: a warp covers 32 consecutive blocks (2 KB
-// of bf16); the next warp-item's 64 bytes per lane are loaded before the
-// current block is converted.
+// One block of 32 values per thread, moved with 32-byte loads and stores; the
+// thread's next block is loaded before the current one is converted.
 __global__ void __launch_bounds__(256) rht32_s2f6_quantize_kernel(const uint16_t *__restrict__ x, int64_t nblk,
                                                                   uint32_t signs, int8_t *__restrict__ codes,
                                                                   uint8_t *__restrict__ scales) {
   const int64_t threads = (int64_t)gridDim.x * blockDim.x;
   const float c = __uint_as_float(kInvSqrt32Bits);
   int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  uint4 next[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) next[i] = b < nblk ? ld_stream_v4(x + b * 32 + 8 * i) : make_uint4(0, 0, 0, 0);
+  uint32_t next[16] = {};
+  if (b < nblk) {
+    ld_stream_v8(x + b * 32, reinterpret_cast<uint32_t(&)[8]>(next[0]));
+    ld_stream_v8(x + b * 32 + 16, reinterpret_cast<uint32_t(&)[8]>(next[8]));
+  }
   for (; b < nblk; b += threads) {
     uint32_t rw[16];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      rw[4 * i] = next[i].x; rw[4 * i + 1] = next[i].y; rw[4 * i + 2] = next[i].z; rw[4 * i + 3] = next[i].w;
-    }
+    for (int i = 0; i < 16; ++i) rw[i] = next[i];
     const int64_t b1 = b + threads;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) next[i] = b1 < nblk ? ld_stream_v4(x + b1 * 32 + 8 * i) : make_uint4(0, 0, 0, 0);
+    if (b1 < nblk) {
+      ld_stream_v8(x + b1 * 32, reinterpret_cast<uint32_t(&)[8]>(next[0]));
+      ld_stream_v8(x + b1 * 32 + 16, reinterpret_cast<uint32_t(&)[8]>(next[8]));
+    }
     float v[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j)  // bf16 -> fp32 with the random sign, one bit operation each
@@ -99,9 +100,7 @@ __global__ void __launch_bounds__(256) rht32_s2f6_quantize_kernel(const uint16_t
       k = k < -128 ? -128 : (k > 127 ? 127 : k);
       packed[j >> 2] |= ((uint32_t)k & 0xFFu) << (8 * (j & 3));
     }
-    uint4 *dst = reinterpret_cast<uint4 *>(codes + b * 32);
-    dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-    dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+    st_cs_v8(codes + b * 32, packed[0], packed[1], packed[2], packed[3], packed[4], packed[5], packed[6], packed[7]);
     scales[b] = (uint8_t)(e + 127);
   }
 }
@@ -113,23 +112,20 @@ __global__ void __launch_bounds__(256) s2f6_dequant_irht32_kernel(const int8_t *
   const int64_t threads = (int64_t)gridDim.x * blockDim.x;
   const float c = __uint_as_float(kInvSqrt32Bits);
   int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  uint4 next[2];
+  uint32_t next[8] = {};
   uint32_t next_sc = 0;
-  next[0] = next[1] = make_uint4(0, 0, 0, 0);
   if (b < nblk) {
-    next[0] = ld_stream_v4(codes + b * 32);
-    next[1] = ld_stream_v4(codes + b * 32 + 16);
+    ld_stream_v8(codes + b * 32, next);
     next_sc = scales[b];
   }
   for (; b < nblk; b += threads) {
-    const uint32_t cw[8] = {next[0].x, next[0].y, next[0].z, next[0].w, next[1].x, next[1].y, next[1].z, next[1].w};
+    uint32_t cw[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) cw[i] = next[i];
     const float s = pow2f_exact((int)next_sc - 127);
     const int64_t b1 = b + threads;
-    next[0] = next[1] = make_uint4(0, 0, 0, 0);
-    next_sc = 0;
     if (b1 < nblk) {
-      next[0] = ld_stream_v4(codes + b1 * 32);
-      next[1] = ld_stream_v4(codes + b1 * 32 + 16);
+      ld_stream_v8(codes + b1 * 32, next);
       next_sc = scales[b1];
     }
     float v[32];
@@ -142,20 +138,19 @@ __global__ void __launch_bounds__(256) s2f6_dequant_irht32_kernel(const int8_t *
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(__float_as_uint(__fmul_rn(v[j], c)) ^ (((signs >> j) & 1u) << 31));
     if (y_fp32) {
-      float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(y) + b * 32);
+      float *dst = static_cast<float *>(y) + b * 32;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+      for (int i = 0; i < 4; ++i)
+        st_cs_v8(dst + 8 * i, __float_as_uint(v[8 * i]), __float_as_uint(v[8 * i + 1]), __float_as_uint(v[8 * i + 2]),
+                 __float_as_uint(v[8 * i + 3]), __float_as_uint(v[8 * i + 4]), __float_as_uint(v[8 * i + 5]),
+                 __float_as_uint(v[8 * i + 6]), __float_as_uint(v[8 * i + 7]));
     } else {
-      uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(y) + b * 32);
+      uint32_t o[16];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint4 o;
-        o.x = f32_to_bf16_bits(v[8 * i]) | (f32_to_bf16_bits(v[8 * i + 1]) << 16);
-        o.y = f32_to_bf16_bits(v[8 * i + 2]) | (f32_to_bf16_bits(v[8 * i + 3]) << 16);
-        o.z = f32_to_bf16_bits(v[8 * i + 4]) | (f32_to_bf16_bits(v[8 * i + 5]) << 16);
-        o.w = f32_to_bf16_bits(v[8 * i + 6]) | (f32_to_bf16_bits(v[8 * i + 7]) << 16);
-        dst[i] = o;
-      }
+      for (int i = 0; i < 16; ++i) o[i] = f32_to_bf16_bits(v[2 * i]) | (f32_to_bf16_bits(v[2 * i + 1]) << 16);
+      uint16_t *dst = static_cast<uint16_t *>(y) + b * 32;
+      st_cs_v8(dst, o[0], o[1], o[2], o[3], o[4], o[5], o[6], o[7]);
+      st_cs_v8(dst + 16, o[8], o[9], o[10], o[11], o[12], o[13], o[14], o[15]);
     }
   }
 }

@@ -1,4 +1,5 @@
-"""GPU parity of the grouped GEMMs (a3, a7, a8) against the FP64 oracle:
+"""GPU parity of the grouped GEMMs (NVFP4 forward, MXFP8 dgrad and wgrad)
+against the FP64 oracle:
 every output element within 1e-4 * (|A||B|)_ij of the exact product of the
 dequantized operands (plus half a bf16 ulp for bf16 outputs).  The operands
 are the GPU's own quantized tensors, whose bit-exactness the quantizer tests

@@ -1,4 +1,6 @@
-"""GPU parity of the quantization steps (a1, a2, a5, a6) against the oracle:
+"""GPU parity of the quantization steps (amax -> outer scale, NVFP4 quantize,
+the SR re-quantization to transposed MXFP8, the gradient MXFP8 quantizer)
+against the oracle:
 codes, scales (every byte of the scale buffer, padding included) and outer
 scales must be bit-exact, stochastic rounding included for a given seed."""
 import numpy as np
@@ -34,7 +36,7 @@ def _groups(sizes):
     return torch.from_numpy(o).to(dev()), o
 
 
-# ---- a1 + a2: NVFP4 --------------------------------------------------------------
+# ---- amax + NVFP4 quantize --------------------------------------------------------------
 @pytest.mark.parametrize("batch,rows,cols", [(1, 256, 512), (1, 1024, 512), (1, 300, 272), (3, 200, 160),
                                              (1, 1, 16), (2, 129, 64)])
 def test_nvfp4_quantize_matches_oracle(batch, rows, cols):
@@ -219,7 +221,7 @@ def test_mxfp8_single_linear_gradient():
     assert np.array_equal(r["ct"].reshape(cols, r["P"]), tc)
 
 
-# ---- a5: dequant -> transpose -> SR requant ------------------------------------------
+# ---- dequant -> transpose -> SR requant ------------------------------------------
 def _gpu_requant(codes, scales, sg, batch, rows, cols, groups, seed, off):
     if groups is None:
         nb, sbts = N.requant_weight_sizes(batch, rows, cols)

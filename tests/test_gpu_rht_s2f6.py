@@ -63,3 +63,54 @@ def test_rejects_bad_arguments():
         N.rht32_s2f6_quantize(x, 2, 48, 0, c, s)          # cols % 32
     with pytest.raises(N.NvError):
         N.s2f6_dequantize_rht32_inverse(c, s, 2, 32, 0, x, 7)  # bad dtype
+
+
+def test_misaligned_pointers_are_rejected_and_nothing_is_written():
+    rows, cols = 4, 64
+    xb = torch.zeros(rows * cols + 16, dtype=torch.bfloat16, device=dev())
+    cb = torch.full((rows * cols + 32,), 0x55, dtype=torch.int8, device=dev())
+    s = torch.full((rows, cols // 32), 0xAA, dtype=torch.uint8, device=dev())
+    yb = torch.full((rows * cols + 16,), 7.0, dtype=torch.float32, device=dev())
+    with pytest.raises(N.NvError):
+        N.rht32_s2f6_quantize(xb[8:8 + rows * cols], rows, cols, 0, cb[:rows * cols], s)   # x 16-byte aligned
+    with pytest.raises(N.NvError):
+        N.rht32_s2f6_quantize(xb[:rows * cols], rows, cols, 0, cb[16:16 + rows * cols], s)  # codes 16-byte aligned
+    with pytest.raises(N.NvError):
+        N.s2f6_dequantize_rht32_inverse(cb[:rows * cols], s, rows, cols, 0, yb[4:4 + rows * cols], N.NV_OUT_FP32)
+    torch.cuda.synchronize()
+    assert torch.all(cb == 0x55) and torch.all(s == 0xAA) and torch.all(yb == 7.0)
+    check_status()
+
+
+def test_empty_inputs_are_no_ops():
+    c = torch.full((64,), 0x55, dtype=torch.int8, device=dev())
+    s = torch.full((2,), 0xAA, dtype=torch.uint8, device=dev())
+    x = torch.zeros((64,), dtype=torch.bfloat16, device=dev())
+    N.rht32_s2f6_quantize(x, 0, 64, 1, c, s)
+    N.s2f6_dequantize_rht32_inverse(c, s, 2, 0, 1, x, N.NV_OUT_BF16)
+    torch.cuda.synchronize()
+    assert torch.all(c == 0x55) and torch.all(s == 0xAA) and torch.all(x == 0)
+    check_status()
+
+
+def test_full_size_sampled_rows_match_oracle():
+    """The combine activations at full size ([131072 x 4096] bf16, the launch
+    the benchmark times): every code and scale of 48 sampled rows, and their
+    inverse, bit-exact against the oracle."""
+    rows, cols, mask = 131072, 4096, 0x6A09E667
+    g = torch.Generator(device="cuda").manual_seed(11)
+    x = (torch.randn((rows, cols), generator=g, device="cuda") * 2.0).to(torch.bfloat16)
+    codes = torch.empty((rows, cols), dtype=torch.int8, device=dev())
+    scales = torch.empty((rows, cols // 32), dtype=torch.uint8, device=dev())
+    N.rht32_s2f6_quantize(x, rows, cols, mask, codes, scales)
+    y = torch.empty((rows, cols), dtype=torch.bfloat16, device=dev())
+    N.s2f6_dequantize_rht32_inverse(codes, scales, rows, cols, mask, y, N.NV_OUT_BF16)
+    check_status()
+    pick = torch.cat([torch.tensor([0, rows - 1]), torch.randint(1, rows - 1, (46,), generator=torch.Generator().manual_seed(5))])
+    pick_d = pick.to(dev())
+    xs = bf16_f32(x[pick_d])
+    want_c, want_s = R.rht_s2f6_quantize(xs, mask)
+    assert np.array_equal(codes[pick_d].cpu().numpy(), want_c)
+    assert np.array_equal(scales[pick_d].cpu().numpy(), want_s)
+    back = torch.from_numpy(R.s2f6_dequantize_irht(want_c, want_s, mask)).to(torch.bfloat16)
+    assert torch.equal(y[pick_d].cpu().view(torch.int16), back.view(torch.int16))
