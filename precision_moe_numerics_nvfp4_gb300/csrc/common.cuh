@@ -110,6 +110,13 @@ __device__ __forceinline__ uint32_t f32_to_bf16_bits(float x) {
   return r;
 }
 
+// two fp32 -> bf16 (nearest even) packed: lo in bits 0..15, hi in 16..31
+__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 // ---------------------------------------------------------------------------
 // E2M1 / E4M3 conversions (hardware cvt: round to nearest even, saturating)
 // ---------------------------------------------------------------------------

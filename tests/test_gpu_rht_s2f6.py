@@ -21,6 +21,15 @@ def _x(rows, cols, seed):
         x[1, :32] = 0.0                      # a zero block
         x[2, 5] = 4000.0                     # an outlier block
         x[0, 32:64] = 1e-30                  # a tiny block (subnormal range after scaling)
+    if rows > 5 and cols >= 160:
+        # the far ends of the scale range: a huge block (scale near 127, the
+        # inverse's large-exponent path), a block of fp32 subnormals (scale
+        # clamped at -127), and a block whose small values turn subnormal
+        # after the 1/sqrt(32) multiply while the block max stays normal
+        x[3, 64:96] = torch.randn(32, generator=g, device="cuda") * 1e36
+        x[4, 96:128] = torch.randn(32, generator=g, device="cuda") * 1e-39
+        x[5, 128:160] = torch.randn(32, generator=g, device="cuda") * 1e-40
+        x[5, 128:132] = 3e-34
     return x.to(torch.bfloat16).contiguous()
 
 
@@ -51,7 +60,7 @@ def test_quantize_and_inverse_match_oracle(rows, cols, mask):
     yq = R.rht_f32(xf, mask).reshape(rows, -1, 32).astype(np.float64)
     unsat = np.all(np.abs(yq) / (step * 64) <= 127.5 / 64, axis=-1)
     e2 = np.sqrt((err ** 2).sum(-1))
-    bound = np.sqrt(32) * step[..., 0] / 2 + 1e-5 * np.sqrt((xf.reshape(rows, -1, 32) ** 2).sum(-1)) + 1e-30
+    bound = np.sqrt(32) * step[..., 0] / 2 + 1e-5 * np.sqrt((xf.astype(np.float64).reshape(rows, -1, 32) ** 2).sum(-1)) + 1e-30
     assert np.all(e2[unsat] <= bound[unsat])
 
 
