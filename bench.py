@@ -560,7 +560,8 @@ def run_quant_sweep(args):
 
 
 def run_gemm(args):
-    """One grouped GEMM of the MoE layer at a reduced token count (for
+    """One grouped GEMM of the MoE layer at a reduced token count, optionally
+    over fewer experts (same depth per expert, smaller footprint; for
     profiling): fwd = x_q w13^T (N 3072, K 4096), dx = dy13 w13 (N 3072,
     K 4096), dw = dy13^T x_q.  Prints achieved TFLOP/s."""
     import torch
@@ -570,8 +571,8 @@ def run_gemm(args):
 
     N.lib()
     dev = torch.device("cuda")
-    m = W.moe("cuda", seed=2, tokens=args.gemm_tokens)
-    M, d, I2, E = m.x_perm.shape[0], SHAPE["d_model"], 2 * SHAPE["d_ff"], SHAPE["experts"]
+    m = W.moe("cuda", seed=2, tokens=args.gemm_tokens, experts=args.gemm_experts, bias_std=args.gemm_bias_std)
+    M, d, I2, E = m.x_perm.shape[0], SHAPE["d_model"], 2 * SHAPE["d_ff"], args.gemm_experts
     go = m.group_offsets
     sizes = torch.diff(go.to(torch.int64))
     flops = float(2 * M * I2 * d)
@@ -706,6 +707,8 @@ def main(argv=None):
     ap.add_argument("--workload", choices=["moe", "quant_sweep", "gemm", "decode", "rht_s2f6"], default="moe")
     ap.add_argument("--gemm-kind", choices=["fwd", "dx", "dw"], default="fwd")
     ap.add_argument("--gemm-tokens", type=int, default=16384)
+    ap.add_argument("--gemm-experts", type=int, default=SHAPE["experts"])
+    ap.add_argument("--gemm-bias-std", type=float, default=1.0)
     ap.add_argument("--sweep-op", default=None)
     ap.add_argument("--sweep-shape", default=None, help="RxC, e.g. 8192x8192")
     args = ap.parse_args(argv)

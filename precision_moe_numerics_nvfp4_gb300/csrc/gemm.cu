@@ -607,21 +607,34 @@ __device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v
 // 256-column accumulator fills half of each SM's tensor memory); BN = 128: two
 // pairs per SM pair, so one pair's epilogue runs under the other's MMAs, with
 // half the scale copies per FLOP of the 128 x 128 kernel.
-template <int KIND, int STAGES, int BN>
+//
+// A ring stage holds CHUNKS k-chunks of 128 bytes per operand row.  Every
+// barrier wait of the MMA issuer leaves the tensor pipe idle for about 200
+// cycles (measured: the pipe queues almost nothing ahead of the issuing
+// thread), so the MXFP8 kernels take two chunks (8 MMAs) per wait in three
+// stages rather than one chunk per wait in six: the same shared memory and
+// bytes in flight, half the waits.  A tile's last stage may hold one chunk.
+template <int KIND, int STAGES, int BN, int CHUNKS = 1>
 struct CfgPair {
   static_assert(BN == 128 || BN == 256, "pair tile width");
   static constexpr bool kFp4 = KIND == kGemmNvfp4Fwd;
-  static constexpr int kAtomsPerStage = kFp4 ? 4 : 1;
+  static constexpr int kAtomsPerStage = kFp4 ? 4 : 1;   // 128x4 scale tiles per 128 rows per chunk
   static constexpr int kBHalf = BN / 2;                 // B rows staged by each CTA
   static constexpr int kSfbTiles = BN / 128;            // 128-row scale tiles of B per k-atom
-  static constexpr int A_BYTES = 128 * 128;
-  static constexpr int B_BYTES = kBHalf * 128;          // this CTA's half of B
-  static constexpr int SFA_BYTES = kAtomsPerStage * 512;
-  static constexpr int SFB_BYTES = kSfbTiles * SFA_BYTES;  // scales of all BN rows of B
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
-  static constexpr int SFA_COLS = kAtomsPerStage * 4;
+  static constexpr int A_CHUNK = 128 * 128;
+  static constexpr int B_CHUNK = kBHalf * 128;          // this CTA's half of B
+  static constexpr int SFA_CHUNK = kAtomsPerStage * 512;
+  static constexpr int SFB_CHUNK = kSfbTiles * SFA_CHUNK;  // scales of all BN rows of B
+  static constexpr int CHUNK_BYTES = A_CHUNK + B_CHUNK + SFA_CHUNK + SFB_CHUNK;
+  static constexpr int A_BYTES = CHUNKS * A_CHUNK;
+  static constexpr int B_BYTES = CHUNKS * B_CHUNK;
+  static constexpr int SFA_BYTES = CHUNKS * SFA_CHUNK;
+  static constexpr int SFB_BYTES = CHUNKS * SFB_CHUNK;
+  static constexpr int STAGE_BYTES = CHUNKS * CHUNK_BYTES;
+  static constexpr int SFA_COLS = kAtomsPerStage * 4;   // per chunk
   static constexpr int SFB_COLS = kAtomsPerStage * (BN / 32);
-  static constexpr int SF_COLS = SFA_COLS + SFB_COLS;
+  static constexpr int SF_CHUNK_COLS = SFA_COLS + SFB_COLS;
+  static constexpr int SF_COLS = CHUNKS * SF_CHUNK_COLS;  // per stage
   static constexpr int ACC_COLS = BN;
   static constexpr int TMEM_COLS = cpow2(ACC_COLS + STAGES * SF_COLS);
   static constexpr int NBARS = 2 * STAGES + 2;          // full, empty, acc_full, acc_empty
@@ -756,12 +769,13 @@ __device__ __forceinline__ bool wait_pair(uint32_t bar, uint32_t parity, uint64_
   return false;
 }
 
-template <int KIND, int STAGES, int BN>
-__global__ void __launch_bounds__(CfgPair<KIND, STAGES, BN>::kThreads, CfgPair<KIND, STAGES, BN>::kCtasPerSm)
+template <int KIND, int STAGES, int BN, int CHUNKS>
+__global__ void __launch_bounds__(CfgPair<KIND, STAGES, BN, CHUNKS>::kThreads,
+                                  CfgPair<KIND, STAGES, BN, CHUNKS>::kCtasPerSm)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                              const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                              GemmArgs A) {
-  using C = CfgPair<KIND, STAGES, BN>;
+  using C = CfgPair<KIND, STAGES, BN, CHUNKS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint8_t *sA = smem;
@@ -816,8 +830,9 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BN>::kThreads, CfgPair<K
     bool ok = true;
     for (int t = pair; ok && t < num_tiles; t += npairs) {
       const PairTile T = decode_pair<KIND, BN>(t, A, s_off, s_pad, s_pb, s_ord, pair, npairs, num_tiles, cta);
-      for (int ks = 0; ks < T.nk; ++ks, ++it) {
+      for (int ks = 0; ks < T.nk; ks += CHUNKS, ++it) {
         const uint32_t s = it % STAGES;
+        const int nc = T.nk - ks < CHUNKS ? T.nk - ks : CHUNKS;
         if (it >= STAGES &&
             !wait_pair(smem_u32(&empty[s]), ((it / STAGES) - 1) & 1, A.wait_limit, s_abort, peer_abort, A.status)) {
           ok = false;
@@ -825,15 +840,19 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BN>::kThreads, CfgPair<K
         }
         const uint32_t fb_local = smem_u32(&full[s]);
         const uint32_t fb = cta == 0 ? fb_local : mapa_shared(fb_local, 0);
-        if (cta == 0) mbar_arrive_expect_tx(fb_local, 2 * C::STAGE_BYTES);
-        tma_load_2d_pair(smem_u32(sA + s * C::A_BYTES), &tmA, T.k_off + ks * 128, T.a_row, fb);
-        tma_load_2d_pair(smem_u32(sB + s * C::B_BYTES), &tmB, T.k_off + ks * 128, T.b_row, fb);
-        const int64_t katom = T.k_atom0 + (int64_t)ks * C::kAtomsPerStage;
-        tma_load_2d_pair(smem_u32(sSFA + s * C::SFA_BYTES), &tmSA, 0, (int)((T.a_tile * A.ka + katom) * 4), fb);
+        if (cta == 0) mbar_arrive_expect_tx(fb_local, 2 * nc * C::CHUNK_BYTES);
+        for (int c = 0; c < nc; ++c) {
+          const int k = ks + c;
+          tma_load_2d_pair(smem_u32(sA + s * C::A_BYTES + c * C::A_CHUNK), &tmA, T.k_off + k * 128, T.a_row, fb);
+          tma_load_2d_pair(smem_u32(sB + s * C::B_BYTES + c * C::B_CHUNK), &tmB, T.k_off + k * 128, T.b_row, fb);
+          const int64_t katom = T.k_atom0 + (int64_t)k * C::kAtomsPerStage;
+          tma_load_2d_pair(smem_u32(sSFA + s * C::SFA_BYTES + c * C::SFA_CHUNK), &tmSA, 0,
+                           (int)((T.a_tile * A.ka + katom) * 4), fb);
 #pragma unroll
-        for (int j = 0; j < C::kSfbTiles; ++j)
-          tma_load_2d_pair(smem_u32(sSFB + s * C::SFB_BYTES + j * C::SFA_BYTES), &tmSB, 0,
-                           (int)(((T.b_tile0 + j) * A.ka + katom) * 4), fb);
+          for (int j = 0; j < C::kSfbTiles; ++j)
+            tma_load_2d_pair(smem_u32(sSFB + s * C::SFB_BYTES + c * C::SFB_CHUNK + j * C::SFA_CHUNK), &tmSB, 0,
+                             (int)(((T.b_tile0 + j) * A.ka + katom) * 4), fb);
+        }
       }
     }
     if (cta == 0) {  // the even CTA's barriers count both CTAs' bytes: wait for the last copies
@@ -853,34 +872,39 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BN>::kThreads, CfgPair<K
       if (tc >= 1 && !wait_pair(smem_u32(acc_empty), (tc - 1) & 1, A.wait_limit, s_abort, peer_abort, A.status))
         break;
       tc_fence_after();
-      for (int ks = 0; ks < T.nk; ++ks, ++it) {
+      for (int ks = 0; ks < T.nk; ks += CHUNKS, ++it) {
         const uint32_t s = it % STAGES;
+        const int nc = T.nk - ks < CHUNKS ? T.nk - ks : CHUNKS;
         if (!wait_pair(smem_u32(&full[s]), (it / STAGES) & 1, A.wait_limit, s_abort, peer_abort, A.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t sfa = tmem + C::ACC_COLS + s * C::SF_COLS;
-        const uint32_t sfb = sfa + C::SFA_COLS;
-        const uint32_t a_sf_smem = smem_u32(sSFA + s * C::SFA_BYTES);
-        const uint32_t b_sf_smem = smem_u32(sSFB + s * C::SFB_BYTES);
 #pragma unroll
-        for (int j = 0; j < C::kAtomsPerStage; ++j) {
-          tc_cp_sf_pair(sfa + 4 * j, desc_sf(a_sf_smem + j * 512));
+        for (int c = 0; c < CHUNKS; ++c) {
+          if (c >= nc) break;
+          const uint32_t sfa = tmem + C::ACC_COLS + s * C::SF_COLS + c * C::SF_CHUNK_COLS;
+          const uint32_t sfb = sfa + C::SFA_COLS;
+          const uint32_t a_sf_smem = smem_u32(sSFA + s * C::SFA_BYTES + c * C::SFA_CHUNK);
+          const uint32_t b_sf_smem = smem_u32(sSFB + s * C::SFB_BYTES + c * C::SFB_CHUNK);
 #pragma unroll
-          for (int r = 0; r < C::kSfbTiles; ++r)
-            tc_cp_sf_pair(sfb + j * (BN / 32) + 4 * r, desc_sf(b_sf_smem + r * C::SFA_BYTES + j * 512));
-        }
-        const uint64_t da = desc_sw128(smem_u32(sA + s * C::A_BYTES));
-        const uint64_t db = desc_sw128(smem_u32(sB + s * C::B_BYTES));
+          for (int j = 0; j < C::kAtomsPerStage; ++j) {
+            tc_cp_sf_pair(sfa + 4 * j, desc_sf(a_sf_smem + j * 512));
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t accum = (ks | j) != 0;
-          if (C::kFp4) {
-            mma_nvf4_pair(tmem, da + 2 * j, db + 2 * j, C::IDESC, sfa + 4 * j, sfb + j * (BN / 32), accum);
-          } else {
-            const uint32_t idesc = C::IDESC | ((uint32_t)j << 4) | ((uint32_t)j << 29);
-            mma_mxf8_pair(tmem, da + 2 * j, db + 2 * j, idesc, sfa, sfb, accum);
+            for (int r = 0; r < C::kSfbTiles; ++r)
+              tc_cp_sf_pair(sfb + j * (BN / 32) + 4 * r, desc_sf(b_sf_smem + r * C::SFA_CHUNK + j * 512));
+          }
+          const uint64_t da = desc_sw128(smem_u32(sA + s * C::A_BYTES + c * C::A_CHUNK));
+          const uint64_t db = desc_sw128(smem_u32(sB + s * C::B_BYTES + c * C::B_CHUNK));
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t accum = ((ks + c) | j) != 0;
+            if (C::kFp4) {
+              mma_nvf4_pair(tmem, da + 2 * j, db + 2 * j, C::IDESC, sfa + 4 * j, sfb + j * (BN / 32), accum);
+            } else {
+              const uint32_t idesc = C::IDESC | ((uint32_t)j << 4) | ((uint32_t)j << 29);
+              mma_mxf8_pair(tmem, da + 2 * j, db + 2 * j, idesc, sfa, sfb, accum);
+            }
           }
         }
         tc_commit_pair(smem_u32(&empty[s]));
@@ -1027,12 +1051,12 @@ static int run(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &arg
   return cudaGetLastError() == cudaSuccess ? NV_OK : NV_ERR_CUDA;
 }
 
-template <int KIND, int STAGES, int BN>
+template <int KIND, int STAGES, int BN, int CHUNKS = 1>
 static int run_pair(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tsa, const CUtensorMap &tsb,
                     const GemmArgs &args, int64_t max_tiles, cudaStream_t s) {
-  using C = CfgPair<KIND, STAGES, BN>;
+  using C = CfgPair<KIND, STAGES, BN, CHUNKS>;
   const size_t sm = C::smem_bytes(args.E);
-  auto k = grouped_gemm_pair_kernel<KIND, STAGES, BN>;
+  auto k = grouped_gemm_pair_kernel<KIND, STAGES, BN, CHUNKS>;
   static size_t attr_bytes = 0;
   static int max_pairs = 0;  // co-resident CTA pairs at the largest shared-memory size requested so far
   cudaLaunchConfig_t cfg = {};
@@ -1192,8 +1216,8 @@ int launch_grouped_gemm(const GemmProblem &p, int *status, cudaStream_t s) {
     if (pair_bn == 256) {
       switch (p.kind) {
         case kGemmNvfp4Fwd: return run_pair<kGemmNvfp4Fwd, 5, 256>(ta, *tbp, tsa, tsb, b, pair_tiles, s);
-        case kGemmMxfp8Dx: return run_pair<kGemmMxfp8Dx, 6, 256>(ta, *tbp, tsa, tsb, b, pair_tiles, s);
-        default: return run_pair<kGemmMxfp8Dw, 6, 256>(ta, *tbp, tsa, tsb, b, pair_tiles, s);
+        case kGemmMxfp8Dx: return run_pair<kGemmMxfp8Dx, 3, 256, 2>(ta, *tbp, tsa, tsb, b, pair_tiles, s);
+        default: return run_pair<kGemmMxfp8Dw, 3, 256, 2>(ta, *tbp, tsa, tsb, b, pair_tiles, s);
       }
     }
     switch (p.kind) {
