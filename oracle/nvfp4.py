@@ -19,6 +19,12 @@ Conventions (the pages do not state them):
 The element step multiplies by a per-block reciprocal rather than dividing.
 Results are defined while s * sg is a normal fp32 number (any tensor whose
 largest magnitude is at least 2^-100).
+
+Per-token outer scales ("Recipe details": activations get one FP32 scale per
+token, weights one per expert, for batch invariance): row r of an activation
+matrix takes sg_r = fp32(amax_r / 2688) (1 for an all-zero row) and is
+quantized exactly as a one-row tensor would be; dequantization multiplies by
+its own sg_r.
 """
 from __future__ import annotations
 
@@ -41,11 +47,12 @@ def outer_scale(x) -> np.float32:
     return F32(amax / OUTER_DEN)
 
 
-def _quantize_blocks(xb: np.ndarray, sg: np.float32):
-    """Quantize rows of a [nblocks, blocksize] float32 array, one scale each.
+def _quantize_blocks(xb: np.ndarray, sg):
+    """Quantize rows of a [nblocks, blocksize] float32 array, one scale each;
+    ``sg`` is the outer scale, a scalar or one value per block.
     Returns (nibble codes [nblocks, blocksize], E4M3 scale codes [nblocks])."""
-    sg = F32(sg)
-    den6 = F32(F32(6.0) * sg)
+    sg = np.asarray(sg, dtype=F32)
+    den6 = (F32(6.0) * sg).astype(F32)
     bamax = np.max(np.abs(xb), axis=1).astype(F32)
     s_code = F.rn_code((bamax / den6).astype(F32), F.E4M3_TABLE)
     s = F.decode_e4m3_array(s_code).astype(F32)
@@ -74,6 +81,28 @@ def quantize(x, sg=None):
     sg = outer_scale(x) if sg is None else F32(sg)
     codes, scales = _quantize_blocks(x.reshape(R * C // 16, 16), sg)
     return codes.reshape(R, C), scales.reshape(R, C // 16), sg
+
+
+def outer_scale_rows(x) -> np.ndarray:
+    """Per-token outer scales: sg_r = amax_r / 2688 of each row, 1 for an
+    all-zero row (float32 [R])."""
+    x = np.asarray(x, dtype=F32)
+    amax = np.max(np.abs(x), axis=1).astype(F32) if x.shape[1] else np.zeros(x.shape[0], F32)
+    return np.where(amax == 0, F32(1.0), (amax / OUTER_DEN).astype(F32)).astype(F32)
+
+
+def quantize_rows(x, sg_rows=None):
+    """NVFP4 1x16 RN quantization with one outer scale per row (per token).
+    Returns (codes [R, C], scales [R, C/16], sg_rows float32 [R]);
+    ``sg_rows`` defaults to ``outer_scale_rows(x)``."""
+    x = np.asarray(x, dtype=F32)
+    R, C = x.shape
+    if C % NVFP4_BLOCK:
+        raise ValueError("C must be a multiple of 16")
+    sg_rows = outer_scale_rows(x) if sg_rows is None else np.asarray(sg_rows, dtype=F32).reshape(R)
+    per_block = np.repeat(sg_rows, C // NVFP4_BLOCK)
+    codes, scales = _quantize_blocks(x.reshape(R * C // 16, 16), per_block)
+    return codes.reshape(R, C), scales.reshape(R, C // 16), sg_rows
 
 
 def quantize_col16(x, sg=None):
@@ -124,6 +153,20 @@ def dequantize_f64(codes, scales, sg) -> np.ndarray:
     v = F.decode_e2m1_array(codes)
     s = F.decode_e4m3_array(np.repeat(np.asarray(scales, dtype=np.uint8), NVFP4_BLOCK, axis=-1))
     return v * s * np.float64(F32(sg))
+
+
+def dequantize_rows_f32(codes, scales, sg_rows) -> np.ndarray:
+    """Per-token dequantization in fp32: fp32(fp32(e2m1 * e4m3) * sg_r)."""
+    v = F.decode_e2m1_array(codes)
+    s = F.decode_e4m3_array(np.repeat(np.asarray(scales, dtype=np.uint8), NVFP4_BLOCK, axis=-1))
+    return ((v * s).astype(F32) * np.asarray(sg_rows, dtype=F32).reshape(-1, 1)).astype(F32)
+
+
+def dequantize_rows_f64(codes, scales, sg_rows) -> np.ndarray:
+    """Exact per-token dequantized values e2m1 * e4m3 * sg_r in float64."""
+    v = F.decode_e2m1_array(codes)
+    s = F.decode_e4m3_array(np.repeat(np.asarray(scales, dtype=np.uint8), NVFP4_BLOCK, axis=-1))
+    return v * s * np.asarray(sg_rows, dtype=F32).astype(np.float64).reshape(-1, 1)
 
 
 def dequantize_tile16x16_f64(codes, tile_scales, sg) -> np.ndarray:

@@ -105,6 +105,13 @@ def requant_grouped(codes, scales, sg, group_offsets, seed: int, offset: int, P_
     return transposed_grouped_sr(deq, group_offsets, seed, offset, P_cols)
 
 
+def requant_grouped_rows(codes, scales, sg_rows, group_offsets, seed: int, offset: int, P_cols: int):
+    """Grouped activations with per-token outer scales: the dequantized value
+    of row r is fp32(fp32(e2m1 * e4m3) * sg_r); the rest as requant_grouped."""
+    deq = NV.dequantize_rows_f32(codes, scales, sg_rows)
+    return transposed_grouped_sr(deq, group_offsets, seed, offset, P_cols)
+
+
 def quantize_grad_rowwise(g, seed: int, offset: int):
     """BF16 gradient [M, N] (as float32) -> MXFP8 with SR along rows.
     Element (m, n) belongs to the pair of columns (n0, n0+1), n0 = n - n % 2,
