@@ -336,6 +336,58 @@ int grouped_gemm_mxfp8_dw(const uint8_t *gt_codes, const uint8_t *gt_scales,
  * the same contraction with fp32 accumulation; summation order differs. */
 int nvfp4moe_set_gemm_kernel(int variant);
 
+/* ---- per-token activation outer scales ----------------------------------------------
+ * "Recipe details": activations get one FP32 outer scale per token (weights
+ * one per expert), which keeps a token's quantization independent of the rest
+ * of the batch.  Row r of an activation matrix takes
+ *   sg_r = amax_r / 2688   (1 for an all-zero row)
+ * and is quantized exactly as nvfp4_quantize quantizes a one-row tensor; the
+ * dequantized value is fp32(fp32(e2m1 * e4m3) * sg_r).  These calls are the
+ * per-token forms of nvfp4_quantize, nvfp4_quantize_requant,
+ * dequant_transpose_requant_sr, grouped_gemm_nvfp4_fwd and
+ * grouped_gemm_nvfp4_fwd_swiglu (single matrix, no batch), with the same
+ * layouts, shape rules and errors as those, except:
+ *   sg_rows_in / sg_rows_out: fp32 [rows] device arrays (4-byte aligned).
+ *     sg_rows_in NULL -> the per-row amax pass (one extra read of x) writes
+ *     sg_rows_out, which must then be non-NULL (else NV_ERR_ARG); sg_rows_in
+ *     set -> those scales are used (and copied to sg_rows_out when that is a
+ *     different non-NULL array).
+ *   The transposed re-quantization forms the per-token dequantized values
+ *   first and takes each 32-token block's E8M0 scale from their maximum.
+ *   grouped_gemm_nvfp4_fwd_rows: y = acc * fp32(sg_r * sg_w[e]) per row.
+ *   grouped_gemm_nvfp4_fwd_swiglu_rows: h_sg_rows fp32 [M_total] receives the
+ *     per-token outer scales of h (max |h| of each row, then the rule above;
+ *     the array is cleared by the call).
+ * Nothing is allocated; every call only enqueues work on `stream`.
+ */
+int nvfp4_quantize_rows(const void *x, int64_t rows, int64_t cols,
+                        const int32_t *group_offsets, int32_t num_groups,
+                        const float *sg_rows_in, float *sg_rows_out,
+                        uint8_t *codes, uint8_t *scales, nv_stream_t stream);
+int nvfp4_quantize_requant_rows(const void *x, int64_t rows, int64_t cols,
+                                const int32_t *group_offsets, int32_t num_groups,
+                                const float *sg_rows_in, float *sg_rows_out,
+                                uint8_t *codes, uint8_t *scales,
+                                uint64_t seed, uint64_t counter_offset,
+                                uint8_t *out_codes, uint8_t *out_scales, nv_stream_t stream);
+int dequant_transpose_requant_sr_rows(const uint8_t *codes, const uint8_t *scales,
+                                      const float *sg_rows, int64_t rows, int64_t cols,
+                                      const int32_t *group_offsets, int32_t num_groups,
+                                      uint64_t seed, uint64_t counter_offset,
+                                      uint8_t *out_codes, uint8_t *out_scales, nv_stream_t stream);
+int grouped_gemm_nvfp4_fwd_rows(const float *x_sg_rows, const uint8_t *x_codes, const uint8_t *x_scales,
+                                const uint8_t *w_codes, const uint8_t *w_scales,
+                                const float *w_outer_scale,
+                                const int32_t *group_offsets, int32_t E,
+                                int64_t M_total, int64_t N, int64_t K,
+                                void *y, int y_dtype, nv_stream_t stream);
+int grouped_gemm_nvfp4_fwd_swiglu_rows(const float *x_sg_rows, const uint8_t *x_codes,
+                                       const uint8_t *x_scales, const uint8_t *w_codes,
+                                       const uint8_t *w_scales, const float *w_outer_scale,
+                                       const int32_t *group_offsets, int32_t E,
+                                       int64_t M_total, int64_t I, int64_t K,
+                                       void *y13, void *h, float *h_sg_rows, nv_stream_t stream);
+
 /* ---- 32-point random Hadamard transform + block-scaled S2F6 -------------
  * "Quantized communications": the data of the combine direction is rotated by
  * a 32-dimensional random Hadamard transform and quantized to S2F6 (two signed

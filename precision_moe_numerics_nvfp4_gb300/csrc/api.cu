@@ -24,6 +24,7 @@ int *status_ptr() {
 }
 
 static bool al16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+static bool al4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 static bool al32(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }  // GEMM outputs: 32-byte stores
 static int64_t rup(int64_t a, int64_t b) { return (a + b - 1) / b * b; }
 
@@ -227,6 +228,91 @@ int dequant_transpose_requant_sr(const uint8_t *codes, const uint8_t *scales, co
                         seed, counter_offset, out_codes, out_scales, st, s);
 }
 
+// ---- per-token outer scales ------------------------------------------------------
+// sg_rows_in NULL: the per-row amax pass writes sg_rows_out (required); else
+// the given scales are used (and copied to sg_rows_out when that differs).
+static int rows_scales(const void *x, int64_t rows, int64_t cols, const float *sg_rows_in, float *sg_rows_out,
+                       const float **sg, cudaStream_t s) {
+  if (!sg_rows_in) {
+    if (!sg_rows_out) return NV_ERR_ARG;
+    const int r = launch_row_outer_scale(static_cast<const uint16_t *>(x), rows, cols, sg_rows_out, s);
+    if (r != NV_OK) return r;
+    *sg = sg_rows_out;
+    return NV_OK;
+  }
+  if (sg_rows_out && sg_rows_out != sg_rows_in &&
+      cudaMemcpyAsync(sg_rows_out, sg_rows_in, rows * sizeof(float), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+    return NV_ERR_CUDA;
+  *sg = sg_rows_in;
+  return NV_OK;
+}
+
+int nvfp4_quantize_rows(const void *x, int64_t rows, int64_t cols, const int32_t *group_offsets, int32_t num_groups,
+                        const float *sg_rows_in, float *sg_rows_out, uint8_t *codes, uint8_t *scales,
+                        nv_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!x || !codes || !scales || rows < 0 || cols < 0) return NV_ERR_ARG;
+  if (!sg_rows_in && !sg_rows_out) return NV_ERR_ARG;
+  if (group_offsets && (num_groups < 1 || num_groups > kMaxGroups)) return NV_ERR_ARG;
+  if (cols % 16) return NV_ERR_SHAPE;
+  if (!al16(x) || !al16(codes) || !al16(scales) || !al16(group_offsets) || !al4(sg_rows_in) || !al4(sg_rows_out))
+    return NV_ERR_ALIGN;
+  if (rows == 0 || cols == 0) return NV_OK;
+  if (rows * cols / 16 >= (int64_t)1 << 31 || rows >= (int64_t)1 << 30) return NV_ERR_SHAPE;
+  int *st = status_ptr();
+  if (!st) return NV_ERR_CUDA;
+  const float *sg = nullptr;
+  int r = rows_scales(x, rows, cols, sg_rows_in, sg_rows_out, &sg, s);
+  if (r != NV_OK) return r;
+  return launch_nvfp4_quant(static_cast<const uint16_t *>(x), 1, rows, cols, group_offsets,
+                            group_offsets ? num_groups : 0, sg, codes, scales, st, s, sg);
+}
+
+int nvfp4_quantize_requant_rows(const void *x, int64_t rows, int64_t cols, const int32_t *group_offsets,
+                                int32_t num_groups, const float *sg_rows_in, float *sg_rows_out, uint8_t *codes,
+                                uint8_t *scales, uint64_t seed, uint64_t counter_offset, uint8_t *out_codes,
+                                uint8_t *out_scales, nv_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!x || !codes || !scales || !out_codes || !out_scales || rows < 0 || cols < 0) return NV_ERR_ARG;
+  if (!sg_rows_in && !sg_rows_out) return NV_ERR_ARG;
+  if (group_offsets && (num_groups < 1 || num_groups > kMaxGroups)) return NV_ERR_ARG;
+  if (cols % 128) return NV_ERR_SHAPE;
+  if (!group_offsets && rows % 128) return NV_ERR_SHAPE;
+  if (!al16(x) || !al16(codes) || !al16(scales) || !al16(out_codes) || !al16(out_scales) || !al16(group_offsets) ||
+      !al4(sg_rows_in) || !al4(sg_rows_out))
+    return NV_ERR_ALIGN;
+  if (rows == 0 || cols == 0) return NV_OK;
+  if (rows >= (int64_t)1 << 30 || rows * cols / 16 >= (int64_t)1 << 31) return NV_ERR_SHAPE;
+  int *st = status_ptr();
+  if (!st) return NV_ERR_CUDA;
+  const float *sg = nullptr;
+  int r = rows_scales(x, rows, cols, sg_rows_in, sg_rows_out, &sg, s);
+  if (r != NV_OK) return r;
+  return launch_nvfp4_requant(static_cast<const uint16_t *>(x), sg, 1, rows, cols, group_offsets,
+                              group_offsets ? num_groups : 0, codes, scales, seed, counter_offset, out_codes,
+                              out_scales, st, s, sg);
+}
+
+int dequant_transpose_requant_sr_rows(const uint8_t *codes, const uint8_t *scales, const float *sg_rows, int64_t rows,
+                                      int64_t cols, const int32_t *group_offsets, int32_t num_groups, uint64_t seed,
+                                      uint64_t counter_offset, uint8_t *out_codes, uint8_t *out_scales,
+                                      nv_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!codes || !scales || !sg_rows || !out_codes || !out_scales || rows < 0 || cols < 0) return NV_ERR_ARG;
+  if (group_offsets && (num_groups < 1 || num_groups > kMaxGroups)) return NV_ERR_ARG;
+  if (cols % 128) return NV_ERR_SHAPE;
+  if (!group_offsets && rows % 128) return NV_ERR_SHAPE;
+  if (!al16(codes) || !al16(scales) || !al16(out_codes) || !al16(out_scales) || !al16(group_offsets) ||
+      !al4(sg_rows))
+    return NV_ERR_ALIGN;
+  if (rows == 0 || cols == 0) return NV_OK;
+  if (rows >= (int64_t)1 << 30) return NV_ERR_SHAPE;
+  int *st = status_ptr();
+  if (!st) return NV_ERR_CUDA;
+  return launch_requant(codes, scales, sg_rows, 1, rows, cols, group_offsets, group_offsets ? num_groups : 0, seed,
+                        counter_offset, out_codes, out_scales, st, s, sg_rows);
+}
+
 static int gemm_common_checks(const int32_t *go, int32_t E, int64_t M_total, int64_t N, int64_t K) {
   if (!go || E < 1 || E > kMaxGroups || M_total < 0 || N <= 0 || K <= 0) return NV_ERR_ARG;
   if (!al16(go)) return NV_ERR_ALIGN;
@@ -279,6 +365,49 @@ int grouped_gemm_nvfp4_fwd_swiglu(const float *x_outer_scale, const uint8_t *x_c
     if (r != NV_OK) return r;
   }
   return launch_outer_scale_from_amax(h_outer_scale, s);
+}
+
+int grouped_gemm_nvfp4_fwd_rows(const float *x_sg_rows, const uint8_t *x_codes, const uint8_t *x_scales,
+                                const uint8_t *w_codes, const uint8_t *w_scales, const float *w_outer_scale,
+                                const int32_t *group_offsets, int32_t E, int64_t M_total, int64_t N, int64_t K,
+                                void *y, int y_dtype, nv_stream_t stream) {
+  int r = gemm_common_checks(group_offsets, E, M_total, N, K);
+  if (r != NV_OK) return r;
+  if (!x_sg_rows || !x_codes || !x_scales || !w_codes || !w_scales || !w_outer_scale || !y) return NV_ERR_ARG;
+  if (y_dtype != NV_OUT_BF16 && y_dtype != NV_OUT_FP32) return NV_ERR_ARG;
+  if (N % 128 || K % 256) return NV_ERR_SHAPE;
+  if (!al16(x_codes) || !al16(x_scales) || !al16(w_codes) || !al16(w_scales) || !al32(y) || !al4(x_sg_rows))
+    return NV_ERR_ALIGN;
+  int *st = status_ptr();
+  if (!st) return NV_ERR_CUDA;
+  GemmProblem p = {kGemmNvfp4Fwd, x_codes, x_scales, w_codes, w_scales, x_sg_rows, w_outer_scale,
+                   group_offsets, E, M_total, N, K, y, y_dtype == NV_OUT_FP32, nullptr, nullptr, 1, 0};
+  return launch_grouped_gemm(p, st, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int grouped_gemm_nvfp4_fwd_swiglu_rows(const float *x_sg_rows, const uint8_t *x_codes, const uint8_t *x_scales,
+                                       const uint8_t *w_codes, const uint8_t *w_scales, const float *w_outer_scale,
+                                       const int32_t *group_offsets, int32_t E, int64_t M_total, int64_t I, int64_t K,
+                                       void *y13, void *h, float *h_sg_rows, nv_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (I <= 0) return NV_ERR_ARG;
+  int r = gemm_common_checks(group_offsets, E, M_total, 2 * I, K);
+  if (r != NV_OK) return r;
+  if (!x_sg_rows || !x_codes || !x_scales || !w_codes || !w_scales || !w_outer_scale || !y13 || !h || !h_sg_rows)
+    return NV_ERR_ARG;
+  if (I % 128 || K % 256) return NV_ERR_SHAPE;
+  if (!al16(x_codes) || !al16(x_scales) || !al16(w_codes) || !al16(w_scales) || !al32(y13) || !al32(h) ||
+      !al4(x_sg_rows) || !al4(h_sg_rows))
+    return NV_ERR_ALIGN;
+  int *st = status_ptr();
+  if (!st) return NV_ERR_CUDA;
+  if (M_total == 0) return NV_OK;
+  if (cudaMemsetAsync(h_sg_rows, 0, M_total * sizeof(float), s) != cudaSuccess) return NV_ERR_CUDA;
+  GemmProblem p = {kGemmNvfp4FwdSwiglu, x_codes, x_scales, w_codes, w_scales, x_sg_rows, w_outer_scale,
+                   group_offsets, E, M_total, 2 * I, K, y13, 0, h, h_sg_rows, 1, 1};
+  r = launch_grouped_gemm(p, st, s);
+  if (r != NV_OK) return r;
+  return launch_row_outer_scale_from_amax(h_sg_rows, M_total, s);
 }
 
 int grouped_gemm_mxfp8_dx(const uint8_t *g_codes, const uint8_t *g_scales, const uint8_t *wt_codes,

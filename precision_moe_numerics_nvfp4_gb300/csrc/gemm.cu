@@ -176,6 +176,8 @@ struct GemmArgs {
   void *h;
   unsigned *h_amax;
   int64_t I;
+  int a_sg_rows;   // a_sg is per row of A (per token)
+  int h_amax_rows;  // h_amax is per row of h
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -441,10 +443,11 @@ __global__ void __launch_bounds__(192, 2)
       const uint32_t acc = tc % NACC;
       if (!wait_or_abort(smem_u32(&acc_full[acc]), (tc / NACC) & 1, A.wait_limit, s_abort, A.status)) break;
       tc_fence_after();
-      float alpha = 1.0f;
-      if (KIND == kGemmNvfp4Fwd || KIND == kGemmNvfp4FwdSwiglu) alpha = __fmul_rn(A.a_sg[0], A.b_sg[T.e]);
       const bool store = row < T.mrows;
       const int64_t orow = T.out_row0 + row;
+      float alpha = 1.0f;
+      if (KIND == kGemmNvfp4Fwd || KIND == kGemmNvfp4FwdSwiglu)  // the row's own outer scale when per token
+        alpha = __fmul_rn(A.a_sg_rows ? (store ? A.a_sg[orow] : 0.0f) : A.a_sg[0], A.b_sg[T.e]);
       // read the whole accumulator row into registers, release the
       // accumulator to the MMA thread, then convert and store
       uint32_t r[kBN];
@@ -489,9 +492,13 @@ __global__ void __launch_bounds__(192, 2)
             st_cs_v8(hp + i, wh[0], wh[1], wh[2], wh[3], wh[4], wh[5], wh[6], wh[7]);
           }
         }
+        if (A.h_amax_rows) {  // per token: this thread's row
+          if (store && hmax > 0.0f) atomicMax(A.h_amax + orow, __float_as_uint(hmax));
+        } else {
 #pragma unroll
-        for (int d = 16; d > 0; d >>= 1) hmax = fmaxf(hmax, __shfl_xor_sync(0xFFFFFFFFu, hmax, d));
-        if (lane == 0 && hmax > 0.0f) atomicMax(A.h_amax, __float_as_uint(hmax));
+          for (int d = 16; d > 0; d >>= 1) hmax = fmaxf(hmax, __shfl_xor_sync(0xFFFFFFFFu, hmax, d));
+          if (lane == 0 && hmax > 0.0f) atomicMax(A.h_amax, __float_as_uint(hmax));
+        }
       } else if (store) {
         if (A.out_fp32) {
           float *dst = static_cast<float *>(A.out) + orow * A.out_ld + T.out_col0;
@@ -922,10 +929,10 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BN, CHUNKS>::kThreads,
       const PairTile T = decode_pair<KIND, BN>(t, A, s_off, s_pad, s_pb, s_ord, pair, npairs, num_tiles, cta);
       if (!wait_pair(smem_u32(acc_full), tc & 1, A.wait_limit, s_abort, peer_abort, A.status)) break;
       tc_fence_after();
-      float alpha = 1.0f;
-      if (KIND == kGemmNvfp4Fwd) alpha = __fmul_rn(A.a_sg[0], A.b_sg[T.e]);
       const bool store = row < T.mrows;
       const int64_t orow = T.out_row0 + row;
+      float alpha = 1.0f;
+      if (KIND == kGemmNvfp4Fwd) alpha = __fmul_rn(A.a_sg_rows ? (store ? A.a_sg[orow] : 0.0f) : A.a_sg[0], A.b_sg[T.e]);
       const int64_t ocol = T.out_col0 + half * 128;
       uint32_t r[128];
       if (T.nk > 0) {
@@ -1120,6 +1127,7 @@ int launch_grouped_gemm(const GemmProblem &p, int *status, cudaStream_t s) {
   a.out = p.out; a.out_fp32 = p.out_fp32; a.status = status;
   a.wait_limit = (uint64_t)1 << 26;
   a.h = p.h; a.h_amax = reinterpret_cast<unsigned *>(p.h_amax); a.I = p.N / 2;
+  a.a_sg_rows = p.a_sg_rows; a.h_amax_rows = p.h_amax_rows;
   const int64_t out_cols = (p.kind == kGemmNvfp4Fwd || p.kind == kGemmNvfp4FwdSwiglu) ? p.N : p.K;
   CUtensorMap ta, tb;
   bool ok;

@@ -12,7 +12,10 @@ int *status_ptr();  // device address of this device's status word (api.cu)
 int launch_amax(const uint16_t *x, int64_t batch, int64_t per_batch, float *partial, int nblk, float *sg_out,
                 cudaStream_t s);
 int launch_nvfp4_quant(const uint16_t *x, int64_t batch, int64_t rows, int64_t cols, const int32_t *groups, int E,
-                       const float *sg, uint8_t *codes, uint8_t *scales, int *status, cudaStream_t s);
+                       const float *sg, uint8_t *codes, uint8_t *scales, int *status, cudaStream_t s,
+                       const float *sg_rows = nullptr);
+// per-token outer scales sg_rows[r] = amax_r / 2688 (1 for a zero row); cols % 8 == 0
+int launch_row_outer_scale(const uint16_t *x, int64_t rows, int64_t cols, float *sg_rows, cudaStream_t s);
 int launch_mxfp8_rowwise(const uint16_t *x, int64_t rows, int64_t cols, const int32_t *groups, int E, int sr,
                          uint64_t seed, uint64_t off, uint8_t *codes, uint8_t *scales, int *status, cudaStream_t s);
 int launch_mx_transpose_bf16(const uint16_t *x, int64_t rows, int64_t cols, const int32_t *groups, int E, int sr,
@@ -20,11 +23,14 @@ int launch_mx_transpose_bf16(const uint16_t *x, int64_t rows, int64_t cols, cons
                              uint8_t *codes_row, uint8_t *scales_row, int *status, cudaStream_t s);
 int launch_requant(const uint8_t *codes, const uint8_t *scales, const float *sg, int64_t batch, int64_t rows,
                    int64_t cols, const int32_t *groups, int E, uint64_t seed, uint64_t off, uint8_t *out_codes,
-                   uint8_t *out_scales, int *status, cudaStream_t s);
+                   uint8_t *out_scales, int *status, cudaStream_t s, const float *sg_rows = nullptr);
 int launch_nvfp4_requant(const uint16_t *x, const float *sg, int64_t batch, int64_t rows, int64_t cols,
                          const int32_t *groups, int E, uint8_t *codes, uint8_t *scales, uint64_t seed, uint64_t off,
-                         uint8_t *out_codes, uint8_t *out_scales, int *status, cudaStream_t s);
+                         uint8_t *out_codes, uint8_t *out_scales, int *status, cudaStream_t s,
+                         const float *sg_rows = nullptr);
 int launch_outer_scale_from_amax(float *amax_in_sg_out, cudaStream_t s);
+// per-row form: buf[r] = amax_r / 2688 (1 for zero) in place, r < n
+int launch_row_outer_scale_from_amax(float *amax_in_sg_out, int64_t n, cudaStream_t s);
 // RHT-32 + block-scaled S2F6 (s2f6.cu); n values, n % 32 == 0
 int launch_rht32_s2f6_quantize(const uint16_t *x, int64_t n, uint32_t signs, int8_t *codes, uint8_t *scales,
                                cudaStream_t s);
@@ -49,6 +55,8 @@ struct GemmProblem {
   int out_fp32;
   void *h;                   // kGemmNvfp4FwdSwiglu: h [M_total][N / 2] bf16
   float *h_amax;             // kGemmNvfp4FwdSwiglu: max |h| accumulated (bits of a non-negative float)
+  int a_sg_rows;             // 1: a_sg holds one outer scale per row of A (per token)
+  int h_amax_rows;           // 1: h_amax holds one maximum per row of h
 };
 int launch_grouped_gemm(const GemmProblem &p, int *status, cudaStream_t s);
 int set_gemm_variant(int v);  // 0 automatic, 1-3 forced (see nvfp4moe_set_gemm_kernel)

@@ -69,6 +69,28 @@ __global__ void __launch_bounds__(32) outer_scale_finalize_kernel(const float *_
   if (threadIdx.x == 0) sg_out[b] = (m == 0.0f) ? 1.0f : __fdiv_rn(m, 2688.0f);
 }
 
+// Per-token outer scales ("Recipe details": one FP32 scale per token for
+// activations): one warp per row, sg_r = amax_r / 2688, or 1 for an all-zero
+// row.  cols % 8 == 0 (16-byte rows).
+__global__ void __launch_bounds__(256) row_outer_scale_kernel(const uint16_t *__restrict__ x, int64_t rows,
+                                                              int64_t cols, float *__restrict__ sg) {
+  const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  const uint16_t *p = x + r * cols;
+  uint32_t m = 0u;
+  for (int64_t c = (int64_t)lane * 8; c < cols; c += 256) {
+    const uint4 v = ld_stream_v4(p + c);
+    m = bf16x2_absmax(m, bf16x2_absmax(bf16x2_absmax(v.x, v.y), bf16x2_absmax(v.z, v.w)));
+  }
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) m = bf16x2_absmax(m, __shfl_xor_sync(0xFFFFFFFFu, m, d));
+  if (lane == 0) {
+    const float a = bf16x2_max_to_f32(m);
+    sg[r] = (a == 0.0f) ? 1.0f : __fdiv_rn(a, 2688.0f);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // window -> rows mapping shared by the quantizers
 // ---------------------------------------------------------------------------
@@ -138,6 +160,7 @@ struct NvQuantArgs {
   int E;
   int wpb;                // windows per matrix (batched)
   const float *sg;        // [batch]
+  const float *sg_rows;   // non-null: one outer scale per row (per token) instead
   uint8_t *codes, *scales;
   int64_t ka;             // scale tiles per padded row tile = ceil(cols / 64)
   int *status;
@@ -166,7 +189,7 @@ __global__ void __launch_bounds__(256) nvfp4_quant_kernel(NvQuantArgs A) {
   int E = A.E;
   if (grouped && !load_groups(A.groups, E, A.rows, s_g.off, s_g.pad, &s_g.flag, A.status)) return;
   const Window w = map_window(grouped, blockIdx.y, E, s_g.off, s_g.pad, A.rows, A.wpb);
-  const float sg = A.sg[grouped ? 0 : w.seg];
+  const float sg = A.sg_rows ? 1.0f : A.sg[grouped ? 0 : w.seg];
   const float den6 = __fmul_rn(6.0f, sg);
 
   reinterpret_cast<uint2 *>(s_sc)[threadIdx.x] = make_uint2(0u, 0u);
@@ -199,7 +222,12 @@ __global__ void __launch_bounds__(256) nvfp4_quant_kernel(NvQuantArgs A) {
       const int i = q >> 4, kbl = q & 15;
       uint2 c;
       uint32_t sc;
-      nvfp4_block(va[u], vb[u], sg, den6, c, sc);
+      if (A.sg_rows) {
+        const float sgi = A.sg_rows[w.src_row0 + i];
+        nvfp4_block(va[u], vb[u], sgi, __fmul_rn(6.0f, sgi), c, sc);
+      } else {
+        nvfp4_block(va[u], vb[u], sg, den6, c, sc);
+      }
       *reinterpret_cast<uint2 *>(A.codes + (off[u] >> 1)) = c;
       s_sc[(kbl >> 2) * 512 + atom_pos(i, kbl)] = (uint8_t)sc;
     }
@@ -347,6 +375,7 @@ struct MxTArgs {
   const uint8_t *nv_codes;           // NVFP4 source (kSrcNvfp4)
   const uint8_t *nv_scales;
   const float *nv_sg;                // outer scale: [batch] (batched) or [1]
+  const float *nv_sg_rows;           // per-token outer scales [rows] (kRows kernels)
   // NVFP4 output (kSrcBf16ToNvfp4)
   uint8_t *nv_codes_out, *nv_scales_out;
   int64_t nv_ka;                     // NVFP4 scale tiles per 128 rows = cols / 64
@@ -450,9 +479,10 @@ __device__ __forceinline__ void stage_bf16_tile(const MxTArgs &A, const Window &
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
 }
 
-template <int kMode>
+template <int kMode, bool kRows = false>
 __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant__ MxTArgs A) {
   constexpr bool kNvfp4 = kMode != kSrcBf16;  // phase 2 on exact f16 products of NVFP4 values
+  static_assert(!kRows || kNvfp4, "per-token outer scales apply to NVFP4 sources");
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ GroupSmem s_g;
   __shared__ __align__(16) uint8_t s_tsc[512];   // transposed scale tile
@@ -472,7 +502,7 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant
   }
   const Window w = map_window(A.grouped != 0, blockIdx.y, E, s_g.off, s_g.pad, A.rows, A.wpb);
   const int64_t col0 = (int64_t)blockIdx.x * 128;
-  const float sg = kNvfp4 ? A.nv_sg[A.grouped ? 0 : w.seg] : 1.0f;
+  const float sg = kNvfp4 && !kRows ? A.nv_sg[A.grouped ? 0 : w.seg] : 1.0f;
 
   // ---- phase 1 --------------------------------------------------------------
   if (!kNvfp4) {
@@ -566,7 +596,12 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant
       const uint4 va = row[chunk_of(i, 2 * kb)], vb = row[chunk_of(i, 2 * kb + 1)];
       uint2 c;
       uint32_t sc;
-      nvfp4_block(va, vb, sg, den6, c, sc);  // an all-zero (padding) block gives scale 0 and zero codes
+      if (kRows) {
+        const float sgi = i < w.nvalid ? A.nv_sg_rows[w.src_row0 + i] : 1.0f;
+        nvfp4_block(va, vb, sgi, __fmul_rn(6.0f, sgi), c, sc);
+      } else {
+        nvfp4_block(va, vb, sg, den6, c, sc);  // an all-zero (padding) block gives scale 0 and zero codes
+      }
       if (i < w.nvalid)
         *reinterpret_cast<uint2 *>(A.nv_codes_out + ((w.src_row0 + i) * A.cols + col0 + kb * 16) / 2) = c;
       s_nvsc[(kb >> 2) * 512 + atom_pos(i, kb)] = (uint8_t)sc;
@@ -582,6 +617,12 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant
   // draw from one Philox call each: pair keys (row * cols + column) for the
   // 8 consecutive columns.  Each lane computes the E8M0 scale of one column
   // (lane & 7) of its block and broadcasts its multiplier.
+  float sg_tok[4];  // per-token outer scales of this lane's tokens (kRows)
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int i = 4 * lane + j;
+    sg_tok[j] = (kRows && i < w.nvalid) ? A.nv_sg_rows[w.src_row0 + i] : 0.0f;
+  }
 #pragma unroll 1
   for (int c8 = warp; c8 < 16; c8 += 8) {
     uint32_t v[4][4];  // [token j][column pair] packed 16-bit values
@@ -596,6 +637,59 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant
       const int64_t ka = (w.src_row0 + 4 * lane) * A.cols + col0 + c8 * 8;
       ba = philox_bits8_rk((uint64_t)(ka >> 3), A.off_t, A.rk);
       bb = philox_bits8_rk((uint64_t)((ka + 2 * A.cols) >> 3), A.off_t, A.rk);
+    }
+    if constexpr (kRows) {
+      // per-token outer scales: the dequantized values fp32(p * sg_token)
+      // first, their block maximum by a reduce-scatter over the 8 lanes of a
+      // block (lane & 7 ends with its own column), then SR of fp32(x * 2^-s)
+      float xv[4][8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          xv[j][2 * q] = __fmul_rn(f16_lo(v[j][q]), sg_tok[j]);
+          xv[j][2 * q + 1] = __fmul_rn(f16_hi(v[j][q]), sg_tok[j]);
+        }
+      float mk[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        mk[k] = fmaxf(fmaxf(fabsf(xv[0][k]), fabsf(xv[1][k])), fmaxf(fabsf(xv[2][k]), fabsf(xv[3][k])));
+      const bool b2 = lane & 4, b1 = lane & 2, b0 = lane & 1;
+      float k4[4], k2[2];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float send = b2 ? mk[k] : mk[k + 4];
+        k4[k] = fmaxf(b2 ? mk[k + 4] : mk[k], __shfl_xor_sync(0xFFFFFFFFu, send, 4));
+      }
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const float send = b1 ? k4[k] : k4[k + 2];
+        k2[k] = fmaxf(b1 ? k4[k + 2] : k4[k], __shfl_xor_sync(0xFFFFFFFFu, send, 2));
+      }
+      const float amax_own = fmaxf(b0 ? k2[1] : k2[0], __shfl_xor_sync(0xFFFFFFFFu, b0 ? k2[0] : k2[1], 1));
+      float mult_own;
+      const uint32_t sc = e8m0_scale(amax_own, &mult_own);
+      s_tsc[atom_pos(c8 * 8 + (lane & 7), lane >> 3)] = (uint8_t)sc;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int c = c8 * 8 + k;
+        const float m2 = __shfl_sync(0xFFFFFFFFu, mult_own, (lane & ~7) | k);
+        const int p = k >> 1, h = k & 1;
+        float x[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) x[j] = __fmul_rn(xv[j][k], m2);
+        uint32_t packed;
+        if (A.sr) {
+          const uint32_t wa = p == 0 ? ba.x : p == 1 ? ba.y : p == 2 ? ba.z : ba.w;
+          const uint32_t wb = p == 0 ? bb.x : p == 1 ? bb.y : p == 2 ? bb.z : bb.w;
+          const uint32_t u = __byte_perm(wa, wb, h ? 0x7632 : 0x5410);
+          packed = cvt_e4m3x4_sr(x[0], x[1], x[2], x[3], ~u);
+        } else {
+          packed = cvt_e4m3x2_rn(x[0], x[1]) | (cvt_e4m3x2_rn(x[2], x[3]) << 16);
+        }
+        reinterpret_cast<uint32_t *>(s_out + c * kTileOutStride)[lane] = packed;
+      }
+      continue;
     }
     uint32_t m[4];
 #pragma unroll
@@ -714,12 +808,33 @@ int launch_outer_scale_from_amax(float *amax_in_sg_out, cudaStream_t s) {
   return launch_status(cudaGetLastError());
 }
 
+__global__ void __launch_bounds__(256) row_outer_scale_from_amax_kernel(float *__restrict__ buf, int64_t n) {
+  const int64_t r = (int64_t)blockIdx.x * 256 + threadIdx.x;
+  if (r >= n) return;
+  const float a = buf[r];
+  buf[r] = (a == 0.0f) ? 1.0f : __fdiv_rn(a, 2688.0f);
+}
+
+int launch_row_outer_scale_from_amax(float *amax_in_sg_out, int64_t n, cudaStream_t s) {
+  if (n == 0) return NV_OK;
+  row_outer_scale_from_amax_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(amax_in_sg_out, n);
+  return launch_status(cudaGetLastError());
+}
+
+int launch_row_outer_scale(const uint16_t *x, int64_t rows, int64_t cols, float *sg_rows, cudaStream_t s) {
+  if (rows == 0) return NV_OK;
+  row_outer_scale_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(x, rows, cols, sg_rows);
+  return launch_status(cudaGetLastError());
+}
+
 int launch_nvfp4_quant(const uint16_t *x, int64_t batch, int64_t rows, int64_t cols, const int32_t *groups, int E,
-                       const float *sg, uint8_t *codes, uint8_t *scales, int *status, cudaStream_t s) {
+                       const float *sg, uint8_t *codes, uint8_t *scales, int *status, cudaStream_t s,
+                       const float *sg_rows) {
   NvQuantArgs A;
   A.x = x; A.rows = rows; A.cols = cols; A.groups = groups; A.E = E;
   A.wpb = (int)((rows + 127) / 128);
-  A.sg = sg; A.codes = codes; A.scales = scales; A.ka = (cols / 16 + 3) / 4; A.status = status;
+  A.sg = sg; A.sg_rows = sg_rows;
+  A.codes = codes; A.scales = scales; A.ka = (cols / 16 + 3) / 4; A.status = status;
   const int64_t nwin = groups ? nvfp4moe_padded_cap(rows, E) / 128 : batch * A.wpb;
   const int64_t nchunk = (cols / 16 + 15) / 16;
   if (nwin == 0) return NV_OK;
@@ -766,9 +881,9 @@ int launch_mx_transpose_bf16(const uint16_t *x, int64_t rows, int64_t cols, cons
 
 int launch_requant(const uint8_t *codes, const uint8_t *scales, const float *sg, int64_t batch, int64_t rows,
                    int64_t cols, const int32_t *groups, int E, uint64_t seed, uint64_t off, uint8_t *out_codes,
-                   uint8_t *out_scales, int *status, cudaStream_t s) {
+                   uint8_t *out_scales, int *status, cudaStream_t s, const float *sg_rows) {
   MxTArgs A = {};
-  A.nv_codes = codes; A.nv_scales = scales; A.nv_sg = sg; A.rows = rows; A.cols = cols; A.groups = groups; A.E = E;
+  A.nv_codes = codes; A.nv_scales = scales; A.nv_sg = sg; A.nv_sg_rows = sg_rows; A.rows = rows; A.cols = cols; A.groups = groups; A.E = E;
   A.sr = 1; A.seed = seed; A.off_t = off; A.status = status;
   A.rk = philox_round_keys(seed);
   A.out_codes = out_codes; A.out_scales = out_scales;
@@ -780,22 +895,22 @@ int launch_requant(const uint8_t *codes, const uint8_t *scales, const float *sg,
     A.grouped = 0; A.wpb = (int)(rows / 128); A.out_ka = rows / 128; nwin = batch * A.wpb;
   }
   const size_t sm = mx_t_smem(true);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaFuncSetAttribute(mx_transpose_kernel<kSrcNvfp4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    attr_set = true;
+  auto k = sg_rows ? mx_transpose_kernel<kSrcNvfp4, true> : mx_transpose_kernel<kSrcNvfp4, false>;
+  static bool attr_set[2] = {false, false};
+  if (!attr_set[sg_rows ? 1 : 0]) {
+    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    attr_set[sg_rows ? 1 : 0] = true;
   }
   if (nwin == 0) return NV_OK;
-  mx_transpose_kernel<kSrcNvfp4><<<dim3((unsigned)(cols / 128), (unsigned)nwin), 256, sm, s>>>(A);
+  k<<<dim3((unsigned)(cols / 128), (unsigned)nwin), 256, sm, s>>>(A);
   return launch_status(cudaGetLastError());
 }
 
-
 int launch_nvfp4_requant(const uint16_t *x, const float *sg, int64_t batch, int64_t rows, int64_t cols,
                          const int32_t *groups, int E, uint8_t *codes, uint8_t *scales, uint64_t seed, uint64_t off,
-                         uint8_t *out_codes, uint8_t *out_scales, int *status, cudaStream_t s) {
+                         uint8_t *out_codes, uint8_t *out_scales, int *status, cudaStream_t s, const float *sg_rows) {
   MxTArgs A = {};
-  A.x = x; A.nv_sg = sg; A.rows = rows; A.cols = cols; A.groups = groups; A.E = E;
+  A.x = x; A.nv_sg = sg; A.nv_sg_rows = sg_rows; A.rows = rows; A.cols = cols; A.groups = groups; A.E = E;
   A.nv_codes_out = codes; A.nv_scales_out = scales; A.nv_ka = cols / 64;
   A.sr = 1; A.seed = seed; A.off_t = off; A.status = status;
   A.rk = philox_round_keys(seed);
@@ -808,13 +923,14 @@ int launch_nvfp4_requant(const uint16_t *x, const float *sg, int64_t batch, int6
     A.grouped = 0; A.wpb = (int)(rows / 128); A.out_ka = rows / 128; nwin = batch * A.wpb;
   }
   const size_t sm = mx_t_smem(true);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaFuncSetAttribute(mx_transpose_kernel<kSrcBf16ToNvfp4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    attr_set = true;
+  auto k = sg_rows ? mx_transpose_kernel<kSrcBf16ToNvfp4, true> : mx_transpose_kernel<kSrcBf16ToNvfp4, false>;
+  static bool attr_set[2] = {false, false};
+  if (!attr_set[sg_rows ? 1 : 0]) {
+    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    attr_set[sg_rows ? 1 : 0] = true;
   }
   if (nwin == 0) return NV_OK;
-  mx_transpose_kernel<kSrcBf16ToNvfp4><<<dim3((unsigned)(cols / 128), (unsigned)nwin), 256, sm, s>>>(A);
+  k<<<dim3((unsigned)(cols / 128), (unsigned)nwin), 256, sm, s>>>(A);
   return launch_status(cudaGetLastError());
 }
 

@@ -60,6 +60,15 @@ _SIGS = {
     "nvfp4moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "nvfp4moe_version": (ctypes.c_char_p, []),
     "nvfp4moe_set_gemm_kernel": (ctypes.c_int, [ctypes.c_int]),
+    "nvfp4_quantize_rows": (ctypes.c_int, [_P, _I64, _I64, _P, _I32, _P, _P, _P, _P, _P]),
+    "nvfp4_quantize_requant_rows": (ctypes.c_int, [_P, _I64, _I64, _P, _I32, _P, _P, _P, _P, _U64, _U64, _P, _P,
+                                                   _P]),
+    "dequant_transpose_requant_sr_rows": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _P, _I32, _U64, _U64, _P, _P,
+                                                         _P]),
+    "grouped_gemm_nvfp4_fwd_rows": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I32, _I64, _I64, _I64, _P,
+                                                   ctypes.c_int, _P]),
+    "grouped_gemm_nvfp4_fwd_swiglu_rows": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I32, _I64, _I64, _I64, _P,
+                                                          _P, _P, _P]),
 }
 
 
@@ -225,6 +234,41 @@ def grouped_gemm_nvfp4_fwd_swiglu(x_outer_scale, x_codes, x_scales, w13_codes, w
         _ptr(x_outer_scale), _ptr(x_codes), _ptr(x_scales), _ptr(w13_codes), _ptr(w13_scales),
         _ptr(w13_outer_scale), _ptr(group_offsets), E, M_total, I, K, _ptr(y13), _ptr(h), _ptr(h_outer_scale),
         _stream(stream)))
+
+
+# ---- per-token activation outer scales ------------------------------------------------
+def nvfp4_quantize_rows(x, rows, cols, group_offsets, sg_rows_in, sg_rows_out, codes, scales, stream=None):
+    return _check("nvfp4_quantize_rows", lib().nvfp4_quantize_rows(
+        _ptr(x), rows, cols, _ptr(group_offsets), _ng(group_offsets), _ptr(sg_rows_in), _ptr(sg_rows_out),
+        _ptr(codes), _ptr(scales), _stream(stream)))
+
+
+def nvfp4_quantize_requant_rows(x, rows, cols, group_offsets, sg_rows_in, sg_rows_out, codes, scales, seed,
+                                counter_offset, out_codes, out_scales, stream=None):
+    return _check("nvfp4_quantize_requant_rows", lib().nvfp4_quantize_requant_rows(
+        _ptr(x), rows, cols, _ptr(group_offsets), _ng(group_offsets), _ptr(sg_rows_in), _ptr(sg_rows_out),
+        _ptr(codes), _ptr(scales), seed, counter_offset, _ptr(out_codes), _ptr(out_scales), _stream(stream)))
+
+
+def dequant_transpose_requant_sr_rows(codes, scales, sg_rows, rows, cols, group_offsets, seed, counter_offset,
+                                      out_codes, out_scales, stream=None):
+    return _check("dequant_transpose_requant_sr_rows", lib().dequant_transpose_requant_sr_rows(
+        _ptr(codes), _ptr(scales), _ptr(sg_rows), rows, cols, _ptr(group_offsets), _ng(group_offsets), seed,
+        counter_offset, _ptr(out_codes), _ptr(out_scales), _stream(stream)))
+
+
+def grouped_gemm_nvfp4_fwd_rows(x_sg_rows, x_codes, x_scales, w_codes, w_scales, w_outer_scale, group_offsets, E,
+                                M_total, N, K, y, y_dtype, stream=None):
+    return _check("grouped_gemm_nvfp4_fwd_rows", lib().grouped_gemm_nvfp4_fwd_rows(
+        _ptr(x_sg_rows), _ptr(x_codes), _ptr(x_scales), _ptr(w_codes), _ptr(w_scales), _ptr(w_outer_scale),
+        _ptr(group_offsets), E, M_total, N, K, _ptr(y), y_dtype, _stream(stream)))
+
+
+def grouped_gemm_nvfp4_fwd_swiglu_rows(x_sg_rows, x_codes, x_scales, w13_codes, w13_scales, w13_outer_scale,
+                                       group_offsets, E, M_total, I, K, y13, h, h_sg_rows, stream=None):
+    return _check("grouped_gemm_nvfp4_fwd_swiglu_rows", lib().grouped_gemm_nvfp4_fwd_swiglu_rows(
+        _ptr(x_sg_rows), _ptr(x_codes), _ptr(x_scales), _ptr(w13_codes), _ptr(w13_scales), _ptr(w13_outer_scale),
+        _ptr(group_offsets), E, M_total, I, K, _ptr(y13), _ptr(h), _ptr(h_sg_rows), _stream(stream)))
 
 
 def grouped_gemm_mxfp8_dx(g_codes, g_scales, wt_codes, wt_scales, group_offsets, E, M_total, N, K, dx, dx_dtype,

@@ -144,9 +144,14 @@ class MoELayer:
     computes SwiGLU and the outer scale of h in its epilogue
     (grouped_gemm_nvfp4_fwd_swiglu) when d_ff % 128 == 0; `fuse_swiglu=False`
     runs the GEMM, nvfp4moe_swiglu_fwd and the amax pass of h instead.  Every
-    choice gives the same results, bit for bit."""
+    choice gives the same results, bit for bit.
 
-    def __init__(self, M, d_model, d_ff, E, device="cuda", backward=True, fuse_requant=True, fuse_swiglu=True):
+    `per_token=True` quantizes the activations x and h with one outer scale
+    per token (the *_rows calls; weights keep one per expert), the recipe's
+    batch-invariant form; its results differ from the per-tensor layer's."""
+
+    def __init__(self, M, d_model, d_ff, E, device="cuda", backward=True, fuse_requant=True, fuse_swiglu=True,
+                 per_token=False):
         dev = torch.device(device)
         self.M, self.d, self.I, self.E = M, d_model, d_ff, E
         I2 = 2 * d_ff
@@ -160,6 +165,10 @@ class MoELayer:
         self.y2 = torch.empty((M, d_model), dtype=BF16, device=dev)
         self.fuse_swiglu = fuse_swiglu and d_ff % 128 == 0
         self.h_sg = torch.empty(1, dtype=F32, device=dev)  # outer scale of h from the fused epilogue
+        self.per_token = per_token
+        if per_token:
+            self.x_sg_rows = torch.empty(M, dtype=F32, device=dev)
+            self.h_sg_rows = torch.empty(M, dtype=F32, device=dev)
         self.fuse_requant = fuse_requant and backward
         self._requant_seed = None  # seed of the operands the last forward re-quantized
         if not backward:  # forward-only use (sampling): no backward buffers
@@ -204,6 +213,8 @@ class MoELayer:
 
     def forward_activations(self, x, groups, stream=None, seed=None):
         """The forward with the weights already quantized (e.g. sampling)."""
+        if self.per_token:
+            return self._forward_activations_rows(x, groups, stream, seed)
         M, d, I, E = self.M, self.d, self.I, self.E
         if seed is None:
             self.xq.quantize(x, groups, stream)
@@ -227,6 +238,31 @@ class MoELayer:
         N.grouped_gemm_nvfp4_fwd(None, self.hq.sg, self.hq.codes, self.hq.scales, self.w2q.codes, self.w2q.scales,
                                  self.w2q.sg, groups, E, M, d, I, self.y2, N.NV_OUT_BF16, None, stream)
 
+    def _forward_activations_rows(self, x, groups, stream, seed):
+        M, d, I, E = self.M, self.d, self.I, self.E
+        xq, hq, xs, hs = self.xq, self.hq, self.x_sg_rows, self.h_sg_rows
+        if seed is None:
+            N.nvfp4_quantize_rows(x, M, d, groups, None, xs, xq.codes, xq.scales, stream)
+        else:
+            N.nvfp4_quantize_requant_rows(x, M, d, groups, None, xs, xq.codes, xq.scales, seed, OFF_XQ,
+                                          self.xt.codes, self.xt.scales, stream)
+        h_in = None
+        if self.fuse_swiglu:
+            N.grouped_gemm_nvfp4_fwd_swiglu_rows(xs, xq.codes, xq.scales, self.w13q.codes, self.w13q.scales,
+                                                 self.w13q.sg, groups, E, M, I, d, self.y13, self.h, hs, stream)
+            h_in = hs
+        else:
+            N.grouped_gemm_nvfp4_fwd_rows(xs, xq.codes, xq.scales, self.w13q.codes, self.w13q.scales, self.w13q.sg,
+                                          groups, E, M, 2 * I, d, self.y13, N.NV_OUT_BF16, stream)
+            N.nvfp4moe_swiglu_fwd(self.y13, M, I, self.h, stream)
+        if seed is None:
+            N.nvfp4_quantize_rows(self.h, M, I, groups, h_in, hs, hq.codes, hq.scales, stream)
+        else:
+            N.nvfp4_quantize_requant_rows(self.h, M, I, groups, h_in, hs, hq.codes, hq.scales, seed, OFF_HQ,
+                                          self.ht.codes, self.ht.scales, stream)
+        N.grouped_gemm_nvfp4_fwd_rows(hs, hq.codes, hq.scales, self.w2q.codes, self.w2q.scales, self.w2q.sg, groups,
+                                      E, M, d, I, self.y2, N.NV_OUT_BF16, stream)
+
     def backward(self, g2, groups, seed=3, stream=None, dx_out=None):
         """dx goes to `dx_out` when given (bf16 [M][d_model]), else self.dx."""
         M, d, I, E = self.M, self.d, self.I, self.E
@@ -244,6 +280,12 @@ class MoELayer:
                                        OFF_W13, self.w13t.codes, self.w13t.scales, stream)
         N.dequant_transpose_requant_sr(self.w2q.codes, self.w2q.scales, self.w2q.sg, E, d, I, None, seed, OFF_W2,
                                        self.w2t.codes, self.w2t.scales, stream)
+        if self.per_token:
+            N.dequant_transpose_requant_sr_rows(self.xq.codes, self.xq.scales, self.x_sg_rows, M, d, groups, seed,
+                                                OFF_XQ, self.xt.codes, self.xt.scales, stream)
+            N.dequant_transpose_requant_sr_rows(self.hq.codes, self.hq.scales, self.h_sg_rows, M, I, groups, seed,
+                                                OFF_HQ, self.ht.codes, self.ht.scales, stream)
+            return
         N.dequant_transpose_requant_sr(self.xq.codes, self.xq.scales, self.xq.sg, 1, M, d, groups, seed, OFF_XQ,
                                        self.xt.codes, self.xt.scales, stream)
         N.dequant_transpose_requant_sr(self.hq.codes, self.hq.scales, self.hq.sg, 1, M, I, groups, seed, OFF_HQ,
@@ -280,6 +322,8 @@ class MoELayer:
         requants unless fused) + 2 MXFP8 quantizations + 4 GEMMs + SwiGLU
         backward."""
         fwd = (3 * 3 + 2 + 1 + 1) if self.fuse_swiglu else (4 * 3 + 2 + 1)
+        if self.per_token:  # x: row amax + quantize; h: from the epilogue's row scales (1) or row amax + quantize
+            fwd = (2 + 2 * 3 + 2 + 1 + 1) if self.fuse_swiglu else (2 + 2 * 3 + 2 + 2 + 1)
         return fwd + (0 if self.fuse_requant else 4) + (2 + 4 + 1)
 
 
