@@ -672,6 +672,48 @@ def run_rht_s2f6(args):
                           "peak_source": peaks["source"]}))
     assert N.nvfp4moe_get_device_status() == 0
 
+    # the w2 (down-projection) GEMM with the quantizer in its epilogue, against
+    # the GEMM followed by the standalone quantizer: h [131072 x 1536] NVFP4,
+    # w2 [64 x 4096 x 1536] NVFP4, the benchmark's routing
+    from precision_moe_numerics_nvfp4_gb300.pipeline import NvTensor
+    m = W.moe("cuda", seed=2, tokens=SHAPE["tokens"], weights=False)
+    go = m.group_offsets
+    E, Kh = go.numel() - 1, SHAPE["d_ff"]
+    del m
+    g = torch.Generator(device="cuda").manual_seed(7)
+    h = torch.randn((rows, Kh), generator=g, device="cuda").to(torch.bfloat16)
+    w2 = (torch.randn((E, cols, Kh), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    hq, wq = NvTensor(1, rows, Kh, torch.device("cuda"), E=E), NvTensor(E, cols, Kh, torch.device("cuda"))
+    hq.quantize(h, go)
+    wq.quantize(w2)
+    del h, w2
+    gemm = lambda: N.grouped_gemm_nvfp4_fwd(None, hq.sg, hq.codes, hq.scales, wq.codes, wq.scales, wq.sg, go, E, rows,
+                                            cols, Kh, y, N.NV_OUT_BF16)
+    fused = lambda yy: N.grouped_gemm_nvfp4_fwd_rht_s2f6(hq.sg, hq.codes, hq.scales, wq.codes, wq.scales, wq.sg, go,
+                                                         E, rows, cols, Kh, mask, yy, codes, scales)
+    ops2 = {
+        "w2_gemm_bf16": gemm,
+        "w2_gemm_bf16_then_rht32_s2f6_quantize": lambda: (gemm(), ops["rht32_s2f6_quantize"]()),
+        "w2_gemm_rht_s2f6_epilogue": lambda: fused(None),
+        "w2_gemm_rht_s2f6_epilogue_and_bf16": lambda: fused(y),
+    }
+    fl = 2.0 * rows * cols * Kh
+    for name, fn in ops2.items():
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        s = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(args.steps):
+            fn()
+        e1.record(s)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        print(json.dumps({"workload": "rht_s2f6", "op": name, "shape": [rows, cols, Kh], "experts": E, "ms": ms,
+                          "gemm_TFLOP_s": fl / (ms / 1e3) / 1e12}))
+    assert N.nvfp4moe_get_device_status() == 0
+
 
 def run_decode(args):
     """Sampler-style decode forward: 128 experts, SwiGLU gate/up [7168 -> 2048

@@ -421,6 +421,26 @@ int s2f6_dequantize_rht32_inverse(const int8_t *codes, const uint8_t *scales,
                                   int64_t rows, int64_t cols, uint32_t signs,
                                   void *y, int y_dtype, nv_stream_t stream);
 
+/* ---- the w2 forward GEMM with RHT-32 + S2F6 in its epilogue ----------------------------
+ * "Quantized communications": the combine direction quantizes the experts'
+ * output with the 32-point random Hadamard transform and block-scaled S2F6
+ * in the down-projection (w2) GEMM's epilogue.  The GEMM of
+ * grouped_gemm_nvfp4_fwd with bf16 output (same arguments, layouts and shape
+ * rules), and in the same kernel the rht32_s2f6_quantize of every output row
+ * (same `signs`): codes and scales bit-identical to the two calls in
+ * sequence.
+ *   y:      bf16 [M_total][N] (32-byte aligned), or NULL: no bf16 output.
+ *   codes:  int8 [M_total][N] (32-byte aligned); scales: u8 [M_total][N / 32].
+ * Always runs the 128 x 128 one-SM kernel (whatever nvfp4moe_set_gemm_kernel
+ * chose).  Returns as grouped_gemm_nvfp4_fwd; only enqueues work on `stream`.
+ */
+int grouped_gemm_nvfp4_fwd_rht_s2f6(const float *x_outer_scale, const uint8_t *x_codes,
+                                    const uint8_t *x_scales, const uint8_t *w_codes,
+                                    const uint8_t *w_scales, const float *w_outer_scale,
+                                    const int32_t *group_offsets, int32_t E,
+                                    int64_t M_total, int64_t N, int64_t K, uint32_t signs,
+                                    void *y, int8_t *codes, uint8_t *scales, nv_stream_t stream);
+
 /* ---- SwiGLU between the expert GEMMs (Figure 5: w13 GEMM, Q, w2 GEMM) -----
  * y13 bf16 [M][2I] (gate columns 0..I-1, up columns I..2I-1);
  * h = bf16(silu(gate) * up) computed in fp32, silu(x) = x / (1 + exp(-x)).

@@ -367,6 +367,24 @@ int grouped_gemm_nvfp4_fwd_swiglu(const float *x_outer_scale, const uint8_t *x_c
   return launch_outer_scale_from_amax(h_outer_scale, s);
 }
 
+int grouped_gemm_nvfp4_fwd_rht_s2f6(const float *x_outer_scale, const uint8_t *x_codes, const uint8_t *x_scales,
+                                    const uint8_t *w_codes, const uint8_t *w_scales, const float *w_outer_scale,
+                                    const int32_t *group_offsets, int32_t E, int64_t M_total, int64_t N, int64_t K,
+                                    uint32_t signs, void *y, int8_t *codes, uint8_t *scales, nv_stream_t stream) {
+  int r = gemm_common_checks(group_offsets, E, M_total, N, K);
+  if (r != NV_OK) return r;
+  if (!x_outer_scale || !x_codes || !x_scales || !w_codes || !w_scales || !w_outer_scale || !codes || !scales)
+    return NV_ERR_ARG;
+  if (N % 128 || K % 256) return NV_ERR_SHAPE;
+  if (!al16(x_codes) || !al16(x_scales) || !al16(w_codes) || !al16(w_scales) || !al32(y) || !al32(codes))
+    return NV_ERR_ALIGN;
+  int *st = status_ptr();
+  if (!st) return NV_ERR_CUDA;
+  GemmProblem p = {kGemmNvfp4Fwd, x_codes, x_scales, w_codes, w_scales, x_outer_scale, w_outer_scale,
+                   group_offsets, E, M_total, N, K, y, 0, nullptr, nullptr, 0, 0, codes, scales, signs};
+  return launch_grouped_gemm(p, st, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int grouped_gemm_nvfp4_fwd_rows(const float *x_sg_rows, const uint8_t *x_codes, const uint8_t *x_scales,
                                 const uint8_t *w_codes, const uint8_t *w_scales, const float *w_outer_scale,
                                 const int32_t *group_offsets, int32_t E, int64_t M_total, int64_t N, int64_t K,

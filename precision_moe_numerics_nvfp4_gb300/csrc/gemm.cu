@@ -36,6 +36,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "rht_s2f6_block.cuh"
 
 namespace nvm {
 
@@ -178,6 +179,10 @@ struct GemmArgs {
   int64_t I;
   int a_sg_rows;   // a_sg is per row of A (per token)
   int h_amax_rows;  // h_amax is per row of h
+  // NVFP4 forward: RHT-32 + S2F6 of the bf16 output rows (null: none)
+  int8_t *s2f6_codes;
+  uint8_t *s2f6_scales;
+  RhtSigns rht;
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -269,7 +274,7 @@ __device__ __forceinline__ Tile decode_tile(int t, const GemmArgs &A, const int 
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <int KIND, int STAGES, int NACC>
+template <int KIND, int STAGES, int NACC, bool kS2f6 = false>
 __global__ void __launch_bounds__(192, 2)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmArgs A) {
   using C = Cfg<KIND, STAGES, NACC>;
@@ -500,7 +505,29 @@ __global__ void __launch_bounds__(192, 2)
           if (lane == 0 && hmax > 0.0f) atomicMax(A.h_amax, __float_as_uint(hmax));
         }
       } else if (store) {
-        if (A.out_fp32) {
+        if constexpr (KIND == kGemmNvfp4Fwd && kS2f6) {
+          // the combine direction's quantizer on the bf16 output rows: each
+          // 32-column block of the row is rounded to bf16 exactly as the plain
+          // output, then rotated and quantized as rht32_s2f6_quantize would
+          uint16_t *dst = A.out ? static_cast<uint16_t *>(A.out) + orow * A.out_ld + T.out_col0 : nullptr;
+#pragma unroll
+          for (int blk = 0; blk < kBN / 32; ++blk) {
+            uint32_t w[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+              w[k] = pack_bf16x2(__fmul_rn(__uint_as_float(r[32 * blk + 2 * k]), alpha),
+                                 __fmul_rn(__uint_as_float(r[32 * blk + 2 * k + 1]), alpha));
+            if (dst) {
+              st_cs_v8(dst + 32 * blk, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+              st_cs_v8(dst + 32 * blk + 16, w[8], w[9], w[10], w[11], w[12], w[13], w[14], w[15]);
+            }
+            uint32_t pk[8];
+            const uint32_t sc = rht32_s2f6_block(w, A.rht, pk);
+            st_cs_v8(A.s2f6_codes + orow * A.out_ld + T.out_col0 + 32 * blk, pk[0], pk[1], pk[2], pk[3], pk[4], pk[5],
+                     pk[6], pk[7]);
+            A.s2f6_scales[orow * (A.out_ld / 32) + T.out_col0 / 32 + blk] = (uint8_t)sc;
+          }
+        } else if (A.out_fp32) {
           float *dst = static_cast<float *>(A.out) + orow * A.out_ld + T.out_col0;
 #pragma unroll
           for (int i = 0; i < kBN; i += 8) {
@@ -1037,12 +1064,12 @@ static int num_sms() {
   return n[dev];
 }
 
-template <int KIND, int STAGES, int NACC>
+template <int KIND, int STAGES, int NACC, bool kS2f6 = false>
 static int run(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &args, int64_t max_tiles,
                cudaStream_t s) {
   using C = Cfg<KIND, STAGES, NACC>;
   const size_t sm = C::smem_bytes(args.E);
-  auto k = grouped_gemm_kernel<KIND, STAGES, NACC>;
+  auto k = grouped_gemm_kernel<KIND, STAGES, NACC, kS2f6>;
   static size_t attr_bytes = 0;  // largest dynamic shared memory requested so far
   if (sm > attr_bytes) {
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) != cudaSuccess)
@@ -1128,6 +1155,8 @@ int launch_grouped_gemm(const GemmProblem &p, int *status, cudaStream_t s) {
   a.wait_limit = (uint64_t)1 << 26;
   a.h = p.h; a.h_amax = reinterpret_cast<unsigned *>(p.h_amax); a.I = p.N / 2;
   a.a_sg_rows = p.a_sg_rows; a.h_amax_rows = p.h_amax_rows;
+  a.s2f6_codes = p.s2f6_codes; a.s2f6_scales = p.s2f6_scales;
+  if (p.s2f6_codes) a.rht = make_signs(p.rht_signs);
   const int64_t out_cols = (p.kind == kGemmNvfp4Fwd || p.kind == kGemmNvfp4FwdSwiglu) ? p.N : p.K;
   CUtensorMap ta, tb;
   bool ok;
@@ -1172,6 +1201,8 @@ int launch_grouped_gemm(const GemmProblem &p, int *status, cudaStream_t s) {
   // (a half-empty pair block wastes half of its MMAs), else 2.
   if (p.kind == kGemmNvfp4FwdSwiglu)  // one kernel: 128 x (64 gate + 64 up), two CTAs per SM
     return run<kGemmNvfp4FwdSwiglu, 3, 1>(ta, tb, a, max_tiles, s);
+  if (p.s2f6_codes)  // the RHT + S2F6 epilogue exists in the 128 x 128 kernel only
+    return run<kGemmNvfp4Fwd, 3, 1, true>(ta, tb, a, max_tiles, s);
   const int forced = gemm_variant();
   const bool rows_ok = p.kind != kGemmMxfp8Dw || p.N % 256 == 0;  // wgrad: pair tiles of 256 rows
   const bool big_groups = p.kind == kGemmMxfp8Dw || p.M_total >= (int64_t)512 * p.E;

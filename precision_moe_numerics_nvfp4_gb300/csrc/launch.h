@@ -57,6 +57,12 @@ struct GemmProblem {
   float *h_amax;             // kGemmNvfp4FwdSwiglu: max |h| accumulated (bits of a non-negative float)
   int a_sg_rows;             // 1: a_sg holds one outer scale per row of A (per token)
   int h_amax_rows;           // 1: h_amax holds one maximum per row of h
+  // kGemmNvfp4Fwd with bf16 output: also RHT-32 + S2F6 of each row's bf16
+  // values (codes int8 [M_total][N], scales u8 [M_total][N / 32]); out may
+  // then be null (no bf16 output)
+  int8_t *s2f6_codes;
+  uint8_t *s2f6_scales;
+  uint32_t rht_signs;
 };
 int launch_grouped_gemm(const GemmProblem &p, int *status, cudaStream_t s);
 int set_gemm_variant(int v);  // 0 automatic, 1-3 forced (see nvfp4moe_set_gemm_kernel)

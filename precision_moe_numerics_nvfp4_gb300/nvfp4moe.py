@@ -60,6 +60,8 @@ _SIGS = {
     "nvfp4moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "nvfp4moe_version": (ctypes.c_char_p, []),
     "nvfp4moe_set_gemm_kernel": (ctypes.c_int, [ctypes.c_int]),
+    "grouped_gemm_nvfp4_fwd_rht_s2f6": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I32, _I64, _I64, _I64,
+                                                       ctypes.c_uint32, _P, _P, _P, _P]),
     "nvfp4_quantize_rows": (ctypes.c_int, [_P, _I64, _I64, _P, _I32, _P, _P, _P, _P, _P]),
     "nvfp4_quantize_requant_rows": (ctypes.c_int, [_P, _I64, _I64, _P, _I32, _P, _P, _P, _P, _U64, _U64, _P, _P,
                                                    _P]),
@@ -233,6 +235,14 @@ def grouped_gemm_nvfp4_fwd_swiglu(x_outer_scale, x_codes, x_scales, w13_codes, w
     return _check("grouped_gemm_nvfp4_fwd_swiglu", lib().grouped_gemm_nvfp4_fwd_swiglu(
         _ptr(x_outer_scale), _ptr(x_codes), _ptr(x_scales), _ptr(w13_codes), _ptr(w13_scales),
         _ptr(w13_outer_scale), _ptr(group_offsets), E, M_total, I, K, _ptr(y13), _ptr(h), _ptr(h_outer_scale),
+        _stream(stream)))
+
+
+def grouped_gemm_nvfp4_fwd_rht_s2f6(x_outer_scale, x_codes, x_scales, w_codes, w_scales, w_outer_scale,
+                                    group_offsets, E, M_total, N, K, signs, y, codes, scales, stream=None):
+    return _check("grouped_gemm_nvfp4_fwd_rht_s2f6", lib().grouped_gemm_nvfp4_fwd_rht_s2f6(
+        _ptr(x_outer_scale), _ptr(x_codes), _ptr(x_scales), _ptr(w_codes), _ptr(w_scales), _ptr(w_outer_scale),
+        _ptr(group_offsets), E, M_total, N, K, int(signs) & 0xFFFFFFFF, _ptr(y), _ptr(codes), _ptr(scales),
         _stream(stream)))
 
 

@@ -123,3 +123,58 @@ def test_full_size_sampled_rows_match_oracle():
     assert np.array_equal(scales[pick_d].cpu().numpy(), want_s)
     back = torch.from_numpy(R.s2f6_dequantize_irht(want_c, want_s, mask)).to(torch.bfloat16)
     assert torch.equal(y[pick_d].cpu().view(torch.int16), back.view(torch.int16))
+
+
+def _w2_operands(sizes, N_, K, seed):
+    from precision_moe_numerics_nvfp4_gb300.pipeline import NvTensor
+    o = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    go = torch.from_numpy(o).to(dev())
+    M, E = int(o[-1]), len(sizes)
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    h = torch.randn((M, K), generator=g, device="cuda").to(torch.bfloat16)
+    w = (torch.randn((E, N_, K), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    hq, wq = NvTensor(1, M, K, dev(), E=E), NvTensor(E, N_, K, dev())
+    hq.quantize(h, go)
+    wq.quantize(w)
+    return go, M, E, hq, wq
+
+
+def _fused_vs_separate(sizes, N_, K, mask, with_y):
+    go, M, E, hq, wq = _w2_operands(sizes, N_, K, seed=M_seed(sizes))
+    y_ref = torch.empty((M, N_), dtype=torch.bfloat16, device=dev())
+    N.grouped_gemm_nvfp4_fwd(None, hq.sg, hq.codes, hq.scales, wq.codes, wq.scales, wq.sg, go, E, M, N_, K, y_ref,
+                             N.NV_OUT_BF16)
+    c_ref = torch.empty((M, N_), dtype=torch.int8, device=dev())
+    s_ref = torch.empty((M, N_ // 32), dtype=torch.uint8, device=dev())
+    N.rht32_s2f6_quantize(y_ref, M, N_, mask, c_ref, s_ref)
+    y = torch.full((M, N_), 7.0, dtype=torch.bfloat16, device=dev()) if with_y else None
+    c = torch.full((M, N_), 0x55, dtype=torch.int8, device=dev())
+    s = torch.full((M, N_ // 32), 0xAA, dtype=torch.uint8, device=dev())
+    N.grouped_gemm_nvfp4_fwd_rht_s2f6(hq.sg, hq.codes, hq.scales, wq.codes, wq.scales, wq.sg, go, E, M, N_, K, mask,
+                                      y, c, s)
+    check_status()
+    assert torch.equal(c, c_ref) and torch.equal(s, s_ref)
+    if with_y:
+        assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16))
+
+
+def M_seed(sizes):
+    return int(sum(sizes)) + len(sizes)
+
+
+@pytest.mark.parametrize("with_y", [True, False])
+@pytest.mark.parametrize("sizes,N_,K,mask", [([37, 0, 200, 128], 256, 512, 0x9E3779B9), ([300, 1], 128, 256, 0)])
+def test_w2_epilogue_rht_s2f6_equals_gemm_then_quantize(sizes, N_, K, mask, with_y):
+    """The w2 GEMM's RHT + S2F6 epilogue: codes and scales identical to the
+    plain bf16 GEMM followed by rht32_s2f6_quantize (and the bf16 output, when
+    requested, identical to the plain GEMM's)."""
+    _fused_vs_separate(sizes, N_, K, mask, with_y)
+
+
+def test_w2_epilogue_rht_s2f6_full_size():
+    """The MoE layer's w2 GEMM at full size (131072 routed rows, d_ff 1536 ->
+    d_model 4096, 64 uneven experts): fused == separate over every element."""
+    from precision_moe_numerics_nvfp4_gb300 import workloads as W
+    m = W.moe("cpu", seed=2, tokens=16384, weights=False)
+    sizes = np.diff(m.group_offsets.numpy()).tolist()
+    _fused_vs_separate(sizes, 4096, 1536, 0x6A09E667, with_y=False)
