@@ -47,12 +47,14 @@ def outer_scale(x) -> np.float32:
     return F32(amax / OUTER_DEN)
 
 
-def _quantize_blocks(xb: np.ndarray, sg):
+def _quantize_blocks(xb: np.ndarray, sg, top: float = 6.0):
     """Quantize rows of a [nblocks, blocksize] float32 array, one scale each;
-    ``sg`` is the outer scale, a scalar or one value per block.
-    Returns (nibble codes [nblocks, blocksize], E4M3 scale codes [nblocks])."""
+    ``sg`` is the outer scale, a scalar or one value per block; ``top`` is the
+    E2M1 value the block maximum maps to (6; 4 for the Four Over Six
+    candidate).  Returns (nibble codes [nblocks, blocksize], E4M3 scale codes
+    [nblocks])."""
     sg = np.asarray(sg, dtype=F32)
-    den6 = (F32(6.0) * sg).astype(F32)
+    den6 = (F32(top) * sg).astype(F32)
     bamax = np.max(np.abs(xb), axis=1).astype(F32)
     s_code = F.rn_code((bamax / den6).astype(F32), F.E4M3_TABLE)
     s = F.decode_e4m3_array(s_code).astype(F32)
@@ -103,6 +105,47 @@ def quantize_rows(x, sg_rows=None):
     per_block = np.repeat(sg_rows, C // NVFP4_BLOCK)
     codes, scales = _quantize_blocks(x.reshape(R * C // 16, 16), per_block)
     return codes.reshape(R, C), scales.reshape(R, C // 16), sg_rows
+
+
+def block_sq_error_f32(xb, codes, s_code, sg) -> np.ndarray:
+    """Squared error of quantized blocks in fp32, in a fixed order: with the
+    dequantized d_i = fp32(fp32(e2m1_i * s) * sg), e_i = fp32(x_i - d_i), the
+    sum ((e_0^2 + e_1^2) + e_2^2) + ... over the block, each square and sum
+    rounded to fp32.  [nblocks, 16] -> [nblocks]."""
+    xb = np.asarray(xb, dtype=F32)
+    q = F.decode_e2m1_array(codes)
+    s = F.decode_e4m3_array(s_code)[:, None]
+    d = ((q * s).astype(F32) * np.asarray(sg, dtype=F32).reshape(-1, 1)).astype(F32)
+    e = (xb - d).astype(F32)
+    sq = (e * e).astype(F32)
+    acc = np.zeros(xb.shape[0], dtype=F32)
+    for i in range(xb.shape[1]):
+        acc = (acc + sq[:, i]).astype(F32)
+    return acc
+
+
+def quantize_four_over_six(x, sg=None, return_choice=False):
+    """Four Over Six ("Recipe details": the activation quantizer selects
+    between two scale factors per block).  Reading (the rule is not on the
+    pages): each 16-value block is quantized twice with the same outer scale
+    -- block maximum mapped to 6 (the plain rule) and to 4 -- and keeps the
+    candidate with the smaller squared error (``block_sq_error_f32``); ties
+    keep 6.  Returns (codes [R, C], scales [R, C/16], sg) and, when asked, the
+    boolean [R, C/16] of blocks that took 4."""
+    x = np.asarray(x, dtype=F32)
+    R, C = x.shape
+    if C % NVFP4_BLOCK:
+        raise ValueError("C must be a multiple of 16")
+    sg = outer_scale(x) if sg is None else F32(sg)
+    xb = x.reshape(R * C // 16, 16)
+    c6, s6 = _quantize_blocks(xb, sg, 6.0)
+    c4, s4 = _quantize_blocks(xb, sg, 4.0)
+    take4 = block_sq_error_f32(xb, c4, s4, sg) < block_sq_error_f32(xb, c6, s6, sg)
+    codes = np.where(take4[:, None], c4, c6).reshape(R, C)
+    scales = np.where(take4, s4, s6).reshape(R, C // 16)
+    if return_choice:
+        return codes, scales, sg, take4.reshape(R, C // 16)
+    return codes, scales, sg
 
 
 def quantize_col16(x, sg=None):
