@@ -259,6 +259,22 @@ def kernel_units(layer, m):
     fl2 = 2.0 * M * d * I
     # quantize (+ requant) of h: no amax pass when the w13 epilogue produced its outer scale
     h_amax = 0.0 if layer.fuse_swiglu else 2.0
+    if getattr(layer, "four_six", False):  # activations x and h through the Four Over Six calls
+        return {
+            "nvfp4_quantize": [(E * 2 * I * d, 4.5625), (E * d * I, 4.5625)],
+            "nvfp4_quantize_four_over_six": [(M * d, 4.5625), (M * I, 2.5625 + h_amax)],
+            "nvfp4_quantize_requant": [(E * 2 * I * d, 5.59375), (E * d * I, 5.59375)],
+            "nvfp4_quantize_requant_four_over_six": [(M * d, 5.59375), (M * I, 3.59375 + h_amax)],
+            "grouped_gemm_nvfp4_fwd": [fl2] if layer.fuse_swiglu else [fl13, fl2],
+            "grouped_gemm_nvfp4_fwd_swiglu": [fl13],
+            "dequant_transpose_requant_sr": [(E * 2 * I * d, 1.59375), (E * d * I, 1.59375), (M * d, 1.59375),
+                                             (M * I, 1.59375)],
+            "mxfp8_quantize": [(M * d, 4.0625), (M * 2 * I, 4.0625)],
+            "grouped_gemm_mxfp8_dx": [fl2, fl13],
+            "grouped_gemm_mxfp8_dw": [fl2, fl13],
+            "nvfp4moe_swiglu_fwd": [(M * I, 3 * 2.0)],
+            "nvfp4moe_swiglu_bwd": [(M * I, 5 * 2.0)],
+        }
     if getattr(layer, "per_token", False):  # activations: the row amax pass (2 B/elem) runs inside the call
         return {
             "nvfp4_quantize_rows": [(M * d, 4.5625), (M * I, 2.5625 + h_amax)],
@@ -306,8 +322,10 @@ def run_ours(args):
     peaks = load_peaks()
     m = W.moe("cuda", seed=2, with_grad=True, grad_seed=3)
     M = m.x_perm.shape[0]
-    layer = MoELayer(M, SHAPE["d_model"], SHAPE["d_ff"], SHAPE["experts"], per_token=args.per_token)
-    workload = WORKLOAD + (", per-token activation outer scales" if args.per_token else "")
+    layer = MoELayer(M, SHAPE["d_model"], SHAPE["d_ff"], SHAPE["experts"], per_token=args.per_token,
+                     four_over_six=args.four_over_six)
+    workload = WORKLOAD + (", per-token activation outer scales" if args.per_token else "") + (
+        ", Four Over Six activation blocks" if args.four_over_six else "")
     fwd_fl, bwd_fl = layer.flops()
     step_flops = fwd_fl + bwd_fl
 
@@ -393,7 +411,8 @@ def run_ours(args):
         raise RuntimeError(f"device status {st} after the end-to-end steps")
 
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline and not args.per_token:  # the oracle step is the per-tensor one
+    if rank == 0 and not args.no_cpu_baseline and not args.per_token and not args.four_over_six:
+        # the oracle step is the per-tensor, plain-rule one
         cpu = cpu_baseline(args.cpu_tokens)
 
     line = {
@@ -765,6 +784,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=["moe", "quant_sweep", "gemm", "decode", "rht_s2f6"], default="moe")
     ap.add_argument("--gemm-kind", choices=["fwd", "dx", "dw"], default="fwd")
+    ap.add_argument("--four-over-six", action="store_true",
+                    help="moe workload: the Four Over Six block rule for the activations x and h")
     ap.add_argument("--per-token", action="store_true",
                     help="moe workload: one outer scale per token for the activations x and h")
     ap.add_argument("--gemm-tokens", type=int, default=16384)

@@ -336,6 +336,32 @@ int grouped_gemm_mxfp8_dw(const uint8_t *gt_codes, const uint8_t *gt_scales,
  * the same contraction with fp32 accumulation; summation order differs. */
 int nvfp4moe_set_gemm_kernel(int variant);
 
+/* ---- Four Over Six: two candidate block scales for activations ------------------------
+ * "Recipe details": the activation quantizer selects between two scale
+ * factors per block (Four Over Six).  The pages do not state the selection
+ * rule; this library takes: each 16-value block is quantized twice under the
+ * same outer scale -- block maximum mapped to 6 (nvfp4_quantize's rule,
+ * s = RN_E4M3(bamax / fp32(6 sg))) and to 4 (s = RN_E4M3(bamax / fp32(4 sg)),
+ * saturating at 448) -- and keeps the candidate with the smaller squared
+ * error err = sum_i fp32(x_i - d_i)^2, d_i = fp32(fp32(e2m1_i * s) * sg),
+ * summed in fp32 in element order with every operation rounded on its own;
+ * ties keep 6.  Same arguments, layouts, outputs and errors as
+ * nvfp4_quantize and nvfp4_quantize_requant (the re-quantization reads the
+ * codes and scales this rule chose).
+ */
+int nvfp4_quantize_four_over_six(const void *x, int64_t batch, int64_t rows, int64_t cols,
+                                 const int32_t *group_offsets, int32_t num_groups,
+                                 const float *outer_scale_in, float *outer_scale_out,
+                                 uint8_t *codes, uint8_t *scales,
+                                 void *workspace, size_t workspace_bytes, nv_stream_t stream);
+int nvfp4_quantize_requant_four_over_six(const void *x, int64_t batch, int64_t rows, int64_t cols,
+                                         const int32_t *group_offsets, int32_t num_groups,
+                                         const float *outer_scale_in, float *outer_scale_out,
+                                         uint8_t *codes, uint8_t *scales,
+                                         void *workspace, size_t workspace_bytes,
+                                         uint64_t seed, uint64_t counter_offset,
+                                         uint8_t *out_codes, uint8_t *out_scales, nv_stream_t stream);
+
 /* ---- per-token activation outer scales ----------------------------------------------
  * "Recipe details": activations get one FP32 outer scale per token (weights
  * one per expert), which keeps a token's quantization independent of the rest

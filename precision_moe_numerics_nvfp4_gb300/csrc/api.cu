@@ -94,9 +94,10 @@ int nvfp4moe_selftest_wait_timeout(int64_t spins, nv_stream_t stream) {
   return launch_wait_selftest(spins, st, reinterpret_cast<cudaStream_t>(stream));
 }
 
-int nvfp4_quantize(const void *x, int64_t batch, int64_t rows, int64_t cols, const int32_t *group_offsets,
-                   int32_t num_groups, const float *outer_scale_in, float *outer_scale_out, uint8_t *codes,
-                   uint8_t *scales, void *workspace, size_t workspace_bytes, nv_stream_t stream) {
+static int quantize_impl(const void *x, int64_t batch, int64_t rows, int64_t cols, const int32_t *group_offsets,
+                         int32_t num_groups, const float *outer_scale_in, float *outer_scale_out, uint8_t *codes,
+                         uint8_t *scales, void *workspace, size_t workspace_bytes, nv_stream_t stream,
+                         int four_six) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (!x || !codes || !scales || batch < 1 || rows < 0 || cols < 0) return NV_ERR_ARG;
   if (cols % 16) return NV_ERR_SHAPE;
@@ -122,13 +123,29 @@ int nvfp4_quantize(const void *x, int64_t batch, int64_t rows, int64_t cols, con
       return NV_ERR_CUDA;
   }
   return launch_nvfp4_quant(static_cast<const uint16_t *>(x), batch, rows, cols, group_offsets, num_groups, sg, codes,
-                            scales, st, s);
+                            scales, st, s, nullptr, four_six);
 }
 
-int nvfp4_quantize_requant(const void *x, int64_t batch, int64_t rows, int64_t cols, const int32_t *group_offsets,
-                           int32_t num_groups, const float *outer_scale_in, float *outer_scale_out, uint8_t *codes,
-                           uint8_t *scales, void *workspace, size_t workspace_bytes, uint64_t seed,
-                           uint64_t counter_offset, uint8_t *out_codes, uint8_t *out_scales, nv_stream_t stream) {
+int nvfp4_quantize(const void *x, int64_t batch, int64_t rows, int64_t cols, const int32_t *group_offsets,
+                   int32_t num_groups, const float *outer_scale_in, float *outer_scale_out, uint8_t *codes,
+                   uint8_t *scales, void *workspace, size_t workspace_bytes, nv_stream_t stream) {
+  return quantize_impl(x, batch, rows, cols, group_offsets, num_groups, outer_scale_in, outer_scale_out, codes, scales,
+                       workspace, workspace_bytes, stream, 0);
+}
+
+int nvfp4_quantize_four_over_six(const void *x, int64_t batch, int64_t rows, int64_t cols,
+                                 const int32_t *group_offsets, int32_t num_groups, const float *outer_scale_in,
+                                 float *outer_scale_out, uint8_t *codes, uint8_t *scales, void *workspace,
+                                 size_t workspace_bytes, nv_stream_t stream) {
+  return quantize_impl(x, batch, rows, cols, group_offsets, num_groups, outer_scale_in, outer_scale_out, codes, scales,
+                       workspace, workspace_bytes, stream, 1);
+}
+
+static int quantize_requant_impl(const void *x, int64_t batch, int64_t rows, int64_t cols,
+                                 const int32_t *group_offsets, int32_t num_groups, const float *outer_scale_in,
+                                 float *outer_scale_out, uint8_t *codes, uint8_t *scales, void *workspace,
+                                 size_t workspace_bytes, uint64_t seed, uint64_t counter_offset, uint8_t *out_codes,
+                                 uint8_t *out_scales, nv_stream_t stream, int four_six) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (!x || !codes || !scales || !out_codes || !out_scales || batch < 1 || rows < 0 || cols < 0) return NV_ERR_ARG;
   if (group_offsets && (batch != 1 || num_groups < 1 || num_groups > kMaxGroups)) return NV_ERR_ARG;
@@ -157,7 +174,27 @@ int nvfp4_quantize_requant(const void *x, int64_t batch, int64_t rows, int64_t c
   }
   return launch_nvfp4_requant(static_cast<const uint16_t *>(x), sg, batch, rows, cols, group_offsets,
                               group_offsets ? num_groups : 0, codes, scales, seed, counter_offset, out_codes,
-                              out_scales, st, s);
+                              out_scales, st, s, nullptr, four_six);
+}
+
+int nvfp4_quantize_requant(const void *x, int64_t batch, int64_t rows, int64_t cols, const int32_t *group_offsets,
+                           int32_t num_groups, const float *outer_scale_in, float *outer_scale_out, uint8_t *codes,
+                           uint8_t *scales, void *workspace, size_t workspace_bytes, uint64_t seed,
+                           uint64_t counter_offset, uint8_t *out_codes, uint8_t *out_scales, nv_stream_t stream) {
+  return quantize_requant_impl(x, batch, rows, cols, group_offsets, num_groups, outer_scale_in, outer_scale_out, codes,
+                               scales, workspace, workspace_bytes, seed, counter_offset, out_codes, out_scales, stream,
+                               0);
+}
+
+int nvfp4_quantize_requant_four_over_six(const void *x, int64_t batch, int64_t rows, int64_t cols,
+                                         const int32_t *group_offsets, int32_t num_groups,
+                                         const float *outer_scale_in, float *outer_scale_out, uint8_t *codes,
+                                         uint8_t *scales, void *workspace, size_t workspace_bytes, uint64_t seed,
+                                         uint64_t counter_offset, uint8_t *out_codes, uint8_t *out_scales,
+                                         nv_stream_t stream) {
+  return quantize_requant_impl(x, batch, rows, cols, group_offsets, num_groups, outer_scale_in, outer_scale_out, codes,
+                               scales, workspace, workspace_bytes, seed, counter_offset, out_codes, out_scales, stream,
+                               1);
 }
 
 int rht32_s2f6_quantize(const void *x, int64_t rows, int64_t cols, uint32_t signs, int8_t *codes, uint8_t *scales,

@@ -13,7 +13,7 @@ int launch_amax(const uint16_t *x, int64_t batch, int64_t per_batch, float *part
                 cudaStream_t s);
 int launch_nvfp4_quant(const uint16_t *x, int64_t batch, int64_t rows, int64_t cols, const int32_t *groups, int E,
                        const float *sg, uint8_t *codes, uint8_t *scales, int *status, cudaStream_t s,
-                       const float *sg_rows = nullptr);
+                       const float *sg_rows = nullptr, int four_six = 0);
 // per-token outer scales sg_rows[r] = amax_r / 2688 (1 for a zero row); cols % 8 == 0
 int launch_row_outer_scale(const uint16_t *x, int64_t rows, int64_t cols, float *sg_rows, cudaStream_t s);
 int launch_mxfp8_rowwise(const uint16_t *x, int64_t rows, int64_t cols, const int32_t *groups, int E, int sr,
@@ -27,7 +27,7 @@ int launch_requant(const uint8_t *codes, const uint8_t *scales, const float *sg,
 int launch_nvfp4_requant(const uint16_t *x, const float *sg, int64_t batch, int64_t rows, int64_t cols,
                          const int32_t *groups, int E, uint8_t *codes, uint8_t *scales, uint64_t seed, uint64_t off,
                          uint8_t *out_codes, uint8_t *out_scales, int *status, cudaStream_t s,
-                         const float *sg_rows = nullptr);
+                         const float *sg_rows = nullptr, int four_six = 0);
 int launch_outer_scale_from_amax(float *amax_in_sg_out, cudaStream_t s);
 // per-row form: buf[r] = amax_r / 2688 (1 for zero) in place, r < n
 int launch_row_outer_scale_from_amax(float *amax_in_sg_out, int64_t n, cudaStream_t s);

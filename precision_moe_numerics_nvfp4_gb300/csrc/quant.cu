@@ -161,6 +161,7 @@ struct NvQuantArgs {
   int wpb;                // windows per matrix (batched)
   const float *sg;        // [batch]
   const float *sg_rows;   // non-null: one outer scale per row (per token) instead
+  int four_six;           // Four Over Six block rule (nvfp4_block46)
   uint8_t *codes, *scales;
   int64_t ka;             // scale tiles per padded row tile = ceil(cols / 64)
   int *status;
@@ -181,6 +182,9 @@ __device__ __forceinline__ void nvfp4_block(const uint4 &a, const uint4 &b, floa
                        __fmul_rn(bf16_hi(b.y), inv), __fmul_rn(bf16_lo(b.z), inv), __fmul_rn(bf16_hi(b.z), inv),
                        __fmul_rn(bf16_lo(b.w), inv), __fmul_rn(bf16_hi(b.w), inv));
 }
+
+__device__ __forceinline__ void nvfp4_block46(const uint4 &a, const uint4 &b, float sg, uint2 &codes,
+                                              uint32_t &scode);
 
 __global__ void __launch_bounds__(256) nvfp4_quant_kernel(NvQuantArgs A) {
   __shared__ __align__(16) uint8_t s_sc[4 * 512];
@@ -225,6 +229,8 @@ __global__ void __launch_bounds__(256) nvfp4_quant_kernel(NvQuantArgs A) {
       if (A.sg_rows) {
         const float sgi = A.sg_rows[w.src_row0 + i];
         nvfp4_block(va[u], vb[u], sgi, __fmul_rn(6.0f, sgi), c, sc);
+      } else if (A.four_six) {
+        nvfp4_block46(va[u], vb[u], sg, c, sc);
       } else {
         nvfp4_block(va[u], vb[u], sg, den6, c, sc);
       }
@@ -442,6 +448,43 @@ __device__ __forceinline__ uint32_t e4m3_to_f16x2_dup(uint32_t code) {
   return h2;
 }
 
+// Squared quantization error of one block in fp32, in element order:
+// d_i = fp32(fp32(e2m1_i * s) * sg), e_i = fp32(x_i - d_i), acc = fp32(acc + fp32(e_i^2))
+// (every operation rounded on its own: no fused multiply-add).
+__device__ __forceinline__ float nvfp4_block_sq_err(const uint4 &a, const uint4 &b, uint2 codes, float s, float sg) {
+  uint32_t h[8];
+  e2m1x8_to_f16x2(codes.x, reinterpret_cast<uint32_t(&)[4]>(h[0]));
+  e2m1x8_to_f16x2(codes.y, reinterpret_cast<uint32_t(&)[4]>(h[4]));
+  const uint32_t xw[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  float acc = 0.0f;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const float d0 = __fmul_rn(__fmul_rn(f16_lo(h[k]), s), sg);
+    const float d1 = __fmul_rn(__fmul_rn(f16_hi(h[k]), s), sg);
+    const float e0 = __fsub_rn(bf16_lo(xw[k]), d0);
+    const float e1 = __fsub_rn(bf16_hi(xw[k]), d1);
+    acc = __fadd_rn(acc, __fmul_rn(e0, e0));
+    acc = __fadd_rn(acc, __fmul_rn(e1, e1));
+  }
+  return acc;
+}
+
+// Four Over Six: the block quantized with its maximum mapped to 6 (the plain
+// rule) and to 4, under the same outer scale; the smaller squared error wins,
+// ties keep 6
+__device__ __forceinline__ void nvfp4_block46(const uint4 &a, const uint4 &b, float sg, uint2 &codes,
+                                              uint32_t &scode) {
+  uint2 c6, c4;
+  uint32_t s6, s4;
+  nvfp4_block(a, b, sg, __fmul_rn(6.0f, sg), c6, s6);
+  nvfp4_block(a, b, sg, __fmul_rn(4.0f, sg), c4, s4);
+  const float e6 = nvfp4_block_sq_err(a, b, c6, e4m3_to_f32(s6), sg);
+  const float e4 = nvfp4_block_sq_err(a, b, c4, e4m3_to_f32(s4), sg);
+  const bool take4 = e4 < e6;
+  codes = take4 ? c4 : c6;
+  scode = take4 ? s4 : s6;
+}
+
 // the 16 exact f16 products e2m1 * e4m3 of one (row i, 16-column block kb)
 // unit into the swizzled 16-bit tile
 __device__ __forceinline__ void store_f16_products(uint8_t *s_in, int i, int kb, uint2 codes, uint32_t scale) {
@@ -479,7 +522,7 @@ __device__ __forceinline__ void stage_bf16_tile(const MxTArgs &A, const Window &
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
 }
 
-template <int kMode, bool kRows = false>
+template <int kMode, bool kRows = false, bool k46 = false>
 __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant__ MxTArgs A) {
   constexpr bool kNvfp4 = kMode != kSrcBf16;  // phase 2 on exact f16 products of NVFP4 values
   static_assert(!kRows || kNvfp4, "per-token outer scales apply to NVFP4 sources");
@@ -599,6 +642,8 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant
       if (kRows) {
         const float sgi = i < w.nvalid ? A.nv_sg_rows[w.src_row0 + i] : 1.0f;
         nvfp4_block(va, vb, sgi, __fmul_rn(6.0f, sgi), c, sc);
+      } else if (k46) {
+        nvfp4_block46(va, vb, sg, c, sc);
       } else {
         nvfp4_block(va, vb, sg, den6, c, sc);  // an all-zero (padding) block gives scale 0 and zero codes
       }
@@ -829,11 +874,11 @@ int launch_row_outer_scale(const uint16_t *x, int64_t rows, int64_t cols, float 
 
 int launch_nvfp4_quant(const uint16_t *x, int64_t batch, int64_t rows, int64_t cols, const int32_t *groups, int E,
                        const float *sg, uint8_t *codes, uint8_t *scales, int *status, cudaStream_t s,
-                       const float *sg_rows) {
+                       const float *sg_rows, int four_six) {
   NvQuantArgs A;
   A.x = x; A.rows = rows; A.cols = cols; A.groups = groups; A.E = E;
   A.wpb = (int)((rows + 127) / 128);
-  A.sg = sg; A.sg_rows = sg_rows;
+  A.sg = sg; A.sg_rows = sg_rows; A.four_six = four_six;
   A.codes = codes; A.scales = scales; A.ka = (cols / 16 + 3) / 4; A.status = status;
   const int64_t nwin = groups ? nvfp4moe_padded_cap(rows, E) / 128 : batch * A.wpb;
   const int64_t nchunk = (cols / 16 + 15) / 16;
@@ -908,7 +953,8 @@ int launch_requant(const uint8_t *codes, const uint8_t *scales, const float *sg,
 
 int launch_nvfp4_requant(const uint16_t *x, const float *sg, int64_t batch, int64_t rows, int64_t cols,
                          const int32_t *groups, int E, uint8_t *codes, uint8_t *scales, uint64_t seed, uint64_t off,
-                         uint8_t *out_codes, uint8_t *out_scales, int *status, cudaStream_t s, const float *sg_rows) {
+                         uint8_t *out_codes, uint8_t *out_scales, int *status, cudaStream_t s, const float *sg_rows,
+                         int four_six) {
   MxTArgs A = {};
   A.x = x; A.nv_sg = sg; A.nv_sg_rows = sg_rows; A.rows = rows; A.cols = cols; A.groups = groups; A.E = E;
   A.nv_codes_out = codes; A.nv_scales_out = scales; A.nv_ka = cols / 64;
@@ -923,11 +969,14 @@ int launch_nvfp4_requant(const uint16_t *x, const float *sg, int64_t batch, int6
     A.grouped = 0; A.wpb = (int)(rows / 128); A.out_ka = rows / 128; nwin = batch * A.wpb;
   }
   const size_t sm = mx_t_smem(true);
-  auto k = sg_rows ? mx_transpose_kernel<kSrcBf16ToNvfp4, true> : mx_transpose_kernel<kSrcBf16ToNvfp4, false>;
-  static bool attr_set[2] = {false, false};
-  if (!attr_set[sg_rows ? 1 : 0]) {
+  const int which = sg_rows ? 1 : (four_six ? 2 : 0);
+  auto k = which == 1   ? mx_transpose_kernel<kSrcBf16ToNvfp4, true>
+           : which == 2 ? mx_transpose_kernel<kSrcBf16ToNvfp4, false, true>
+                        : mx_transpose_kernel<kSrcBf16ToNvfp4, false>;
+  static bool attr_set[3] = {false, false, false};
+  if (!attr_set[which]) {
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    attr_set[sg_rows ? 1 : 0] = true;
+    attr_set[which] = true;
   }
   if (nwin == 0) return NV_OK;
   k<<<dim3((unsigned)(cols / 128), (unsigned)nwin), 256, sm, s>>>(A);

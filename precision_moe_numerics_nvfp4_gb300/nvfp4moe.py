@@ -62,6 +62,9 @@ _SIGS = {
     "nvfp4moe_set_gemm_kernel": (ctypes.c_int, [ctypes.c_int]),
     "grouped_gemm_nvfp4_fwd_rht_s2f6": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I32, _I64, _I64, _I64,
                                                        ctypes.c_uint32, _P, _P, _P, _P]),
+    "nvfp4_quantize_four_over_six": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _I32, _P, _P, _P, _P, _P, _SZ, _P]),
+    "nvfp4_quantize_requant_four_over_six": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _I32, _P, _P, _P, _P, _P, _SZ,
+                                                            _U64, _U64, _P, _P, _P]),
     "nvfp4_quantize_rows": (ctypes.c_int, [_P, _I64, _I64, _P, _I32, _P, _P, _P, _P, _P]),
     "nvfp4_quantize_requant_rows": (ctypes.c_int, [_P, _I64, _I64, _P, _I32, _P, _P, _P, _P, _U64, _U64, _P, _P,
                                                    _P]),
@@ -236,6 +239,23 @@ def grouped_gemm_nvfp4_fwd_swiglu(x_outer_scale, x_codes, x_scales, w13_codes, w
         _ptr(x_outer_scale), _ptr(x_codes), _ptr(x_scales), _ptr(w13_codes), _ptr(w13_scales),
         _ptr(w13_outer_scale), _ptr(group_offsets), E, M_total, I, K, _ptr(y13), _ptr(h), _ptr(h_outer_scale),
         _stream(stream)))
+
+
+def nvfp4_quantize_four_over_six(x, batch, rows, cols, group_offsets, outer_scale_in, outer_scale_out, codes, scales,
+                                 workspace, stream=None):
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return _check("nvfp4_quantize_four_over_six", lib().nvfp4_quantize_four_over_six(
+        _ptr(x), batch, rows, cols, _ptr(group_offsets), _ng(group_offsets), _ptr(outer_scale_in),
+        _ptr(outer_scale_out), _ptr(codes), _ptr(scales), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def nvfp4_quantize_requant_four_over_six(x, batch, rows, cols, group_offsets, outer_scale_in, outer_scale_out, codes,
+                                         scales, workspace, seed, counter_offset, out_codes, out_scales, stream=None):
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return _check("nvfp4_quantize_requant_four_over_six", lib().nvfp4_quantize_requant_four_over_six(
+        _ptr(x), batch, rows, cols, _ptr(group_offsets), _ng(group_offsets), _ptr(outer_scale_in),
+        _ptr(outer_scale_out), _ptr(codes), _ptr(scales), _ptr(workspace), ws_bytes, seed, counter_offset,
+        _ptr(out_codes), _ptr(out_scales), _stream(stream)))
 
 
 def grouped_gemm_nvfp4_fwd_rht_s2f6(x_outer_scale, x_codes, x_scales, w_codes, w_scales, w_outer_scale,

@@ -45,16 +45,18 @@ class NvTensor:
         self.sg = torch.empty(batch, dtype=F32, device=dev)
         self.ws = _u8(N.nvfp4moe_quantize_workspace_bytes(batch, rows, cols), dev)
 
-    def quantize(self, x, groups=None, stream=None, sg_in=None):
-        """`sg_in`: a given outer scale (skips the amax pass)."""
-        N.nvfp4_quantize(x, self.batch, self.rows, self.cols, groups, sg_in, self.sg, self.codes, self.scales,
-                         self.ws, stream)
+    def quantize(self, x, groups=None, stream=None, sg_in=None, four_six=False):
+        """`sg_in`: a given outer scale (skips the amax pass); `four_six`: the
+        Four Over Six block rule."""
+        f = N.nvfp4_quantize_four_over_six if four_six else N.nvfp4_quantize
+        f(x, self.batch, self.rows, self.cols, groups, sg_in, self.sg, self.codes, self.scales, self.ws, stream)
 
-    def quantize_requant(self, x, mx, seed, offset, groups=None, stream=None, sg_in=None):
+    def quantize_requant(self, x, mx, seed, offset, groups=None, stream=None, sg_in=None, four_six=False):
         """quantize() plus the SR re-quantization of the result into `mx`
         (an MxTransposed), in one pass over x."""
-        N.nvfp4_quantize_requant(x, self.batch, self.rows, self.cols, groups, sg_in, self.sg, self.codes,
-                                 self.scales, self.ws, seed, offset, mx.codes, mx.scales, stream)
+        f = N.nvfp4_quantize_requant_four_over_six if four_six else N.nvfp4_quantize_requant
+        f(x, self.batch, self.rows, self.cols, groups, sg_in, self.sg, self.codes, self.scales, self.ws, seed, offset,
+          mx.codes, mx.scales, stream)
 
 
 class MxTransposed:
@@ -148,10 +150,13 @@ class MoELayer:
 
     `per_token=True` quantizes the activations x and h with one outer scale
     per token (the *_rows calls; weights keep one per expert), the recipe's
-    batch-invariant form; its results differ from the per-tensor layer's."""
+    batch-invariant form; `four_over_six=True` quantizes them with the Four
+    Over Six block rule.  Both change the results."""
 
     def __init__(self, M, d_model, d_ff, E, device="cuda", backward=True, fuse_requant=True, fuse_swiglu=True,
-                 per_token=False):
+                 per_token=False, four_over_six=False):
+        if per_token and four_over_six:
+            raise ValueError("per-token scales and Four Over Six are separate options")
         dev = torch.device(device)
         self.M, self.d, self.I, self.E = M, d_model, d_ff, E
         I2 = 2 * d_ff
@@ -166,6 +171,7 @@ class MoELayer:
         self.fuse_swiglu = fuse_swiglu and d_ff % 128 == 0
         self.h_sg = torch.empty(1, dtype=F32, device=dev)  # outer scale of h from the fused epilogue
         self.per_token = per_token
+        self.four_six = four_over_six
         if per_token:
             self.x_sg_rows = torch.empty(M, dtype=F32, device=dev)
             self.h_sg_rows = torch.empty(M, dtype=F32, device=dev)
@@ -216,10 +222,11 @@ class MoELayer:
         if self.per_token:
             return self._forward_activations_rows(x, groups, stream, seed)
         M, d, I, E = self.M, self.d, self.I, self.E
+        f6 = self.four_six
         if seed is None:
-            self.xq.quantize(x, groups, stream)
+            self.xq.quantize(x, groups, stream, four_six=f6)
         else:
-            self.xq.quantize_requant(x, self.xt, seed, OFF_XQ, groups, stream)
+            self.xq.quantize_requant(x, self.xt, seed, OFF_XQ, groups, stream, four_six=f6)
         sg_h = None
         if self.fuse_swiglu:
             N.grouped_gemm_nvfp4_fwd_swiglu(self.xq.sg, self.xq.codes, self.xq.scales, self.w13q.codes,
@@ -232,9 +239,9 @@ class MoELayer:
                                      None, stream)
             N.nvfp4moe_swiglu_fwd(self.y13, M, I, self.h, stream)
         if seed is None:
-            self.hq.quantize(self.h, groups, stream, sg_in=sg_h)
+            self.hq.quantize(self.h, groups, stream, sg_in=sg_h, four_six=f6)
         else:
-            self.hq.quantize_requant(self.h, self.ht, seed, OFF_HQ, groups, stream, sg_in=sg_h)
+            self.hq.quantize_requant(self.h, self.ht, seed, OFF_HQ, groups, stream, sg_in=sg_h, four_six=f6)
         N.grouped_gemm_nvfp4_fwd(None, self.hq.sg, self.hq.codes, self.hq.scales, self.w2q.codes, self.w2q.scales,
                                  self.w2q.sg, groups, E, M, d, I, self.y2, N.NV_OUT_BF16, None, stream)
 
