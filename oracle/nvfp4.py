@@ -25,6 +25,10 @@ token, weights one per expert, for batch invariance): row r of an activation
 matrix takes sg_r = fp32(amax_r / 2688) (1 for an all-zero row) and is
 quantized exactly as a one-row tensor would be; dequantization multiplies by
 its own sg_r.
+
+Four Over Six (``quantize_four_over_six``): parity unpinned as to the
+selection rule, which the pages do not give ("selects between two scale
+factors"); the function states a reading and its pins check that reading.
 """
 from __future__ import annotations
 
