@@ -1,0 +1,74 @@
+"""Argument validation of the C-ABI entry points, on the host: every call
+checks its pointers, sizes, shape rules and alignment before touching the
+GPU, so these run without one.  The addresses are never dereferenced (each
+case fails validation, or is an empty problem that returns at once)."""
+import ctypes
+
+import pytest
+
+from precision_moe_numerics_nvfp4_gb300 import nvfp4moe as N
+
+A = ctypes.c_void_p(1 << 24)            # 32-byte aligned fake device address
+A16 = ctypes.c_void_p((1 << 24) + 16)   # 16- but not 32-byte aligned
+A4 = ctypes.c_void_p((1 << 24) + 4)     # 4- but not 16-byte aligned
+A1 = ctypes.c_void_p((1 << 24) + 1)     # byte aligned only
+NULL = None
+S = None                                # default stream
+
+
+@pytest.fixture(scope="module")
+def L():
+    from precision_moe_numerics_nvfp4_gb300 import build
+    build.build()
+    return N.lib()
+
+
+def test_quantize_rows_validation(L):
+    f = L.nvfp4_quantize_rows
+    assert f(NULL, 128, 128, NULL, 0, NULL, A, A, A, S) == N.NV_ERR_ARG           # no x
+    assert f(A, 128, 128, NULL, 0, NULL, NULL, A, A, S) == N.NV_ERR_ARG           # no scale in or out
+    assert f(A, 128, 120, NULL, 0, NULL, A, A, A, S) == N.NV_ERR_SHAPE            # cols % 16
+    assert f(A4, 128, 128, NULL, 0, NULL, A, A, A, S) == N.NV_ERR_ALIGN           # x not 16-byte aligned
+    assert f(A, 128, 128, NULL, 0, NULL, A1, A, A, S) == N.NV_ERR_ALIGN           # row scales not 4-byte aligned
+    assert f(A, 128, 128, A, 0, NULL, A, A, A, S) == N.NV_ERR_ARG                 # groups without a count
+    assert f(A, 0, 128, NULL, 0, NULL, A, A, A, S) == N.NV_OK                     # empty: nothing launched
+    g = L.nvfp4_quantize_requant_rows
+    assert g(A, 128, 192, NULL, 0, NULL, A, A, A, 1, 0, A, A, S) == N.NV_ERR_SHAPE   # cols % 128
+    assert g(A, 100, 128, NULL, 0, NULL, A, A, A, 1, 0, A, A, S) == N.NV_ERR_SHAPE   # plain rows % 128
+    assert g(A, 128, 128, NULL, 0, NULL, A, A, A, 1, 0, NULL, A, S) == N.NV_ERR_ARG
+    h = L.dequant_transpose_requant_sr_rows
+    assert h(A, A, NULL, 128, 128, NULL, 0, 1, 0, A, A, S) == N.NV_ERR_ARG         # no row scales
+    assert h(A, A, A1, 128, 128, NULL, 0, 1, 0, A, A, S) == N.NV_ERR_ALIGN
+
+
+def test_gemm_rows_and_s2f6_epilogue_validation(L):
+    f = L.grouped_gemm_nvfp4_fwd_rows
+    assert f(A, A, A, A, A, A, NULL, 4, 256, 256, 512, A, N.NV_OUT_BF16, S) == N.NV_ERR_ARG   # no groups
+    assert f(A, A, A, A, A, A, A, 4, 256, 200, 512, A, N.NV_OUT_BF16, S) == N.NV_ERR_SHAPE   # N % 128
+    assert f(A, A, A, A, A, A, A, 4, 256, 256, 384, A, N.NV_OUT_BF16, S) == N.NV_ERR_SHAPE   # K % 256
+    assert f(A, A, A, A, A, A, A, 4, 256, 256, 512, A16, N.NV_OUT_BF16, S) == N.NV_ERR_ALIGN  # y 32-byte
+    assert f(A, A, A, A, A, A, A, 4, 256, 256, 512, A, 9, S) == N.NV_ERR_ARG                 # output type
+    g = L.grouped_gemm_nvfp4_fwd_swiglu_rows
+    assert g(A, A, A, A, A, A, A, 4, 256, 192, 512, A, A, A, S) == N.NV_ERR_SHAPE              # I % 128
+    assert g(A, A, A, A, A, A, A, 4, 256, 128, 512, A, A, NULL, S) == N.NV_ERR_ARG             # no h scales
+    h = L.grouped_gemm_nvfp4_fwd_rht_s2f6
+    assert h(A, A, A, A, A, A, A, 4, 256, 256, 512, 7, NULL, A16, A, S) == N.NV_ERR_ALIGN      # codes 32-byte
+    assert h(A, A, A, A, A, A, A, 4, 256, 256, 512, 7, NULL, NULL, A, S) == N.NV_ERR_ARG       # no codes
+    assert h(A, A, A, A, A, A, A, 4, 256, 96, 512, 7, NULL, A, A, S) == N.NV_ERR_SHAPE         # N % 128
+
+
+def test_rht_s2f6_and_four_over_six_validation(L):
+    q = L.rht32_s2f6_quantize
+    assert q(A, 4, 48, 0, A, A, S) == N.NV_ERR_SHAPE           # cols % 32
+    assert q(A16, 4, 64, 0, A, A, S) == N.NV_ERR_ALIGN         # x 32-byte
+    assert q(A, 4, 64, 0, A16, A, S) == N.NV_ERR_ALIGN         # codes 32-byte
+    assert q(A, 0, 64, 0, A, A, S) == N.NV_OK                  # empty
+    d = L.s2f6_dequantize_rht32_inverse
+    assert d(A, A, 4, 64, 0, A, 3, S) == N.NV_ERR_ARG          # output type
+    assert d(A, A, 4, 64, 0, A16, N.NV_OUT_FP32, S) == N.NV_ERR_ALIGN
+    f = L.nvfp4_quantize_four_over_six
+    assert f(A, 1, 128, 120, NULL, 0, A, A, A, A, A, 1 << 20, S) == N.NV_ERR_SHAPE   # cols % 16
+    assert f(NULL, 1, 128, 128, NULL, 0, A, A, A, A, A, 1 << 20, S) == N.NV_ERR_ARG
+    assert f(A, 1, 0, 128, NULL, 0, A, A, A, A, A, 1 << 20, S) == N.NV_OK
+    g = L.nvfp4_quantize_requant_four_over_six
+    assert g(A, 1, 128, 192, NULL, 0, A, A, A, A, A, 1 << 20, 1, 0, A, A, S) == N.NV_ERR_SHAPE  # cols % 128
