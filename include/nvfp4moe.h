@@ -114,6 +114,11 @@ int64_t nvfp4moe_scale_offset(int64_t rp, int64_t c, int64_t kblocks);
 /* Workspace bytes nvfp4_quantize needs when it computes the outer scales. */
 size_t nvfp4moe_quantize_workspace_bytes(int64_t batch, int64_t rows, int64_t cols);
 
+/* Workspace bytes grouped_gemm_nvfp4_fwd needs when it is given bf16
+ * activations (x_bf16 non-NULL): their NVFP4 codes, grouped scales, outer
+ * scale and the amax pass's scratch.  0 for invalid sizes. */
+size_t nvfp4moe_fwd_workspace_bytes(int64_t M_total, int64_t K, int64_t E);
+
 /* ---- NVFP4 quantization (amax -> outer scale, 1x16 RN) ----------------------------------------------
  * "Low-precision formats on Blackwell": block scaling by the largest value of
  * each 16 consecutive values, E4M3 block scale, FP32 outer scale per tensor;
@@ -250,9 +255,16 @@ int nvfp4_quantize_requant(const void *x, int64_t batch, int64_t rows, int64_t c
  * x_outer_scale fp32 [1]; w_codes [E][N][K/2], w_scales batched layout,
  * w_outer_scale fp32 [E]; y [M_total][N] bf16 or fp32.
  * N % 128 == 0, K % 256 == 0; y 32-byte aligned (the kernels store 32 bytes
- * at a time).  x_bf16 must be NULL (reserved for a fused producer-side
- * activation quantization; non-NULL returns NV_ERR_UNSUPPORTED).
- * workspace: may be NULL (no scratch needed).
+ * at a time).
+ * x_bf16: NULL -> x_codes / x_scales / x_outer_scale are the quantized
+ *   activations and workspace may be NULL.  Non-NULL -> bf16 [M_total][K]
+ *   activations (16-byte aligned) that the call quantizes itself exactly as
+ *   nvfp4_quantize does (grouped layout; x_outer_scale given, or NULL to
+ *   compute it), into the workspace (nvfp4moe_fwd_workspace_bytes(M_total, K,
+ *   E) bytes, 16-byte aligned; too small -> NV_ERR_WORKSPACE), before the
+ *   GEMM; x_codes / x_scales are ignored.  Bit-identical to the two calls.
+ *   (Two passes, not a quantizer inside the GEMM's producer: re-quantizing
+ *   each A tile once per N tile costs more than the tile's MMAs here.)
  */
 int grouped_gemm_nvfp4_fwd(const void *x_bf16, const float *x_outer_scale,
                            const uint8_t *x_codes, const uint8_t *x_scales,

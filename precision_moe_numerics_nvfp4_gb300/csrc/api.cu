@@ -58,6 +58,15 @@ size_t nvfp4moe_quantize_workspace_bytes(int64_t batch, int64_t rows, int64_t co
   return (size_t)rup((batch * nb + batch) * 4, 256);
 }
 
+// codes, then the grouped scale buffer, then the outer scale, then the amax
+// pass's workspace, each starting on a 256-byte boundary
+size_t nvfp4moe_fwd_workspace_bytes(int64_t M_total, int64_t K, int64_t E) {
+  if (M_total < 0 || K < 0 || E < 1) return 0;
+  const size_t codes = (size_t)rup(M_total * K / 2, 256);
+  const size_t scales = (size_t)rup(nvfp4moe_scale_bytes(nvfp4moe_padded_cap(M_total, E), K / 16), 256);
+  return codes + scales + 256 + nvfp4moe_quantize_workspace_bytes(1, M_total, K);
+}
+
 const char *nvfp4moe_version(void) { return "nvfp4moe 0.1 (sm_103a)"; }
 
 int nvfp4moe_set_gemm_kernel(int variant) { return nvm::set_gemm_variant(variant); }
@@ -362,14 +371,33 @@ int grouped_gemm_nvfp4_fwd(const void *x_bf16, const float *x_outer_scale, const
                            const float *w_outer_scale, const int32_t *group_offsets, int32_t E, int64_t M_total,
                            int64_t N, int64_t K, void *y, int y_dtype, void *workspace, size_t workspace_bytes,
                            nv_stream_t stream) {
-  (void)workspace; (void)workspace_bytes;
-  if (x_bf16) return NV_ERR_UNSUPPORTED;
   int r = gemm_common_checks(group_offsets, E, M_total, N, K);
   if (r != NV_OK) return r;
-  if (!x_outer_scale || !x_codes || !x_scales || !w_codes || !w_scales || !w_outer_scale || !y) return NV_ERR_ARG;
+  if (!w_codes || !w_scales || !w_outer_scale || !y) return NV_ERR_ARG;
+  if (!x_bf16 && (!x_outer_scale || !x_codes || !x_scales)) return NV_ERR_ARG;
   if (y_dtype != NV_OUT_BF16 && y_dtype != NV_OUT_FP32) return NV_ERR_ARG;
   if (N % 128 || K % 256) return NV_ERR_SHAPE;
-  if (!al16(x_codes) || !al16(x_scales) || !al16(w_codes) || !al16(w_scales) || !al32(y)) return NV_ERR_ALIGN;
+  if (!al16(w_codes) || !al16(w_scales) || !al32(y)) return NV_ERR_ALIGN;
+  if (!x_bf16 && (!al16(x_codes) || !al16(x_scales))) return NV_ERR_ALIGN;
+  if (x_bf16) {
+    // the activations arrive in bf16: quantize them (nvfp4_quantize, grouped
+    // layout, outer scale given or computed) into the workspace, then the GEMM
+    if (!al16(x_bf16)) return NV_ERR_ALIGN;
+    const size_t need = nvfp4moe_fwd_workspace_bytes(M_total, K, E);
+    if (!workspace || workspace_bytes < need || !al16(workspace)) return NV_ERR_WORKSPACE;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const size_t cb = (size_t)rup(M_total * K / 2, 256);
+    const size_t sb = (size_t)rup(nvfp4moe_scale_bytes(nvfp4moe_padded_cap(M_total, E), K / 16), 256);
+    uint8_t *codes = ws, *scales = ws + cb;
+    float *sg = reinterpret_cast<float *>(ws + cb + sb);
+    void *qws = ws + cb + sb + 256;
+    r = quantize_impl(x_bf16, 1, M_total, K, group_offsets, E, x_outer_scale, sg, codes, scales, qws,
+                      workspace_bytes - (cb + sb + 256), stream, 0);
+    if (r != NV_OK) return r;
+    x_codes = codes;
+    x_scales = scales;
+    x_outer_scale = sg;
+  }
   int *st = status_ptr();
   if (!st) return NV_ERR_CUDA;
   GemmProblem p = {kGemmNvfp4Fwd, x_codes, x_scales, w_codes, w_scales, x_outer_scale, w_outer_scale,

@@ -36,6 +36,7 @@ _SIGS = {
     "nvfp4moe_scale_bytes": (_I64, [_I64, _I64]),
     "nvfp4moe_scale_offset": (_I64, [_I64, _I64, _I64]),
     "nvfp4moe_quantize_workspace_bytes": (_SZ, [_I64, _I64, _I64]),
+    "nvfp4moe_fwd_workspace_bytes": (_SZ, [_I64, _I64, _I64]),
     "nvfp4_quantize": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _I32, _P, _P, _P, _P, _P, _SZ, _P]),
     "nvfp4_quantize_noalloc": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _I32, _P, _P, _P, _P, _P]),
     "nvfp4_quantize_requant": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _I32, _P, _P, _P, _P, _P, _SZ, _U64, _U64,
@@ -152,6 +153,10 @@ def nvfp4moe_scale_offset(rp: int, c: int, kblocks: int) -> int:
 
 def nvfp4moe_quantize_workspace_bytes(batch: int, rows: int, cols: int) -> int:
     return int(lib().nvfp4moe_quantize_workspace_bytes(batch, rows, cols))
+
+
+def nvfp4moe_fwd_workspace_bytes(M_total: int, K: int, E: int) -> int:
+    return int(lib().nvfp4moe_fwd_workspace_bytes(M_total, K, E))
 
 
 def status_string(status: int) -> str:

@@ -72,3 +72,17 @@ def test_rht_s2f6_and_four_over_six_validation(L):
     assert f(A, 1, 0, 128, NULL, 0, A, A, A, A, A, 1 << 20, S) == N.NV_OK
     g = L.nvfp4_quantize_requant_four_over_six
     assert g(A, 1, 128, 192, NULL, 0, A, A, A, A, A, 1 << 20, 1, 0, A, A, S) == N.NV_ERR_SHAPE  # cols % 128
+
+
+def test_fwd_with_bf16_activations_validation(L):
+    f = L.grouped_gemm_nvfp4_fwd
+    M, N_, K, E = 256, 256, 512, 4
+    need = N.nvfp4moe_fwd_workspace_bytes(M, K, E)
+    assert need >= M * K // 2 + N.nvfp4moe_scale_bytes(N.nvfp4moe_padded_cap(M, E), K // 16)
+    assert N.nvfp4moe_fwd_workspace_bytes(-1, K, E) == 0
+    # quantized activations missing without bf16 ones
+    assert f(NULL, A, NULL, A, A, A, A, A, E, M, N_, K, A, N.NV_OUT_BF16, NULL, 0, S) == N.NV_ERR_ARG
+    # bf16 activations: the workspace must be large enough and aligned
+    assert f(A, NULL, NULL, NULL, A, A, A, A, E, M, N_, K, A, N.NV_OUT_BF16, A, need - 1, S) == N.NV_ERR_WORKSPACE
+    assert f(A, NULL, NULL, NULL, A, A, A, A, E, M, N_, K, A, N.NV_OUT_BF16, A4, need, S) == N.NV_ERR_WORKSPACE
+    assert f(A4, NULL, NULL, NULL, A, A, A, A, E, M, N_, K, A, N.NV_OUT_BF16, A, need, S) == N.NV_ERR_ALIGN

@@ -154,3 +154,32 @@ def test_single_linear_layer_end_to_end():
     A, B = _deq_nvfp4(xq, np.array([0, 256])), _deq_nvfp4(wq)
     y_ref, bound = G.grouped_rows(A, B[None] if B.ndim == 2 else B, np.array([0, 256]))
     assert G.within_bound(out["y"], y_ref, bound).all()
+
+
+@pytest.mark.parametrize("given_scale", [False, True])
+def test_fwd_from_bf16_activations_equals_quantize_then_gemm(given_scale):
+    """grouped_gemm_nvfp4_fwd given bf16 activations quantizes them itself
+    (into its workspace) with nvfp4_quantize's rule: the output equals the
+    two calls in sequence, bit for bit."""
+    from precision_moe_numerics_nvfp4_gb300.pipeline import NvTensor
+    sizes, N_, K = [37, 0, 200, 129], 256, 512
+    o = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    go = torch.from_numpy(o).cuda()
+    M, E = int(o[-1]), len(sizes)
+    g = torch.Generator(device="cuda").manual_seed(41)
+    x = torch.randn((M, K), generator=g, device="cuda").to(torch.bfloat16)
+    w = (torch.randn((E, N_, K), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    wq = NvTensor(E, N_, K, torch.device("cuda"))
+    wq.quantize(w)
+    sg_in = torch.tensor([0.75], dtype=torch.float32, device="cuda") if given_scale else None
+    xq = NvTensor(1, M, K, torch.device("cuda"), E=E)
+    xq.quantize(x, go, sg_in=sg_in)
+    y_ref = torch.empty((M, N_), dtype=torch.float32, device="cuda")
+    N.grouped_gemm_nvfp4_fwd(None, xq.sg, xq.codes, xq.scales, wq.codes, wq.scales, wq.sg, go, E, M, N_, K, y_ref,
+                             N.NV_OUT_FP32)
+    ws = torch.empty(N.nvfp4moe_fwd_workspace_bytes(M, K, E), dtype=torch.uint8, device="cuda")
+    y = torch.full((M, N_), 7.0, dtype=torch.float32, device="cuda")
+    N.grouped_gemm_nvfp4_fwd(x, sg_in, None, None, wq.codes, wq.scales, wq.sg, go, E, M, N_, K, y, N.NV_OUT_FP32,
+                             workspace=ws)
+    assert N.nvfp4moe_get_device_status() == 0
+    assert torch.equal(y, y_ref)
