@@ -338,12 +338,15 @@ class HostStaged:
     """MoELayer steps whose activations x and upstream gradient g2 come from
     pinned host memory and whose dx goes back to pinned host memory.
 
-    Step i copies its inputs into device slot i % 2 on the copy-in stream,
-    computes on the caller's current stream and copies dx out of slot i % 2 on
-    the copy-out stream, so the transfers of neighbouring steps overlap the
-    compute of step i.  Events order every reuse of a slot: the copy into a
-    slot waits until the step that last read it has finished, and a step waits
-    until the copy out of its dx slot (from two steps earlier) has finished.
+    Step i copies its inputs into device slot i % 2 on the copy-in stream (x,
+    then g2), computes on the caller's current stream and copies dx out of
+    slot i % 2 on the copy-out stream, so the transfers of neighbouring steps
+    overlap the compute of step i.  The forward waits only for x and the
+    backward for g2, so the g2 copy overlaps the step's own forward.  Events
+    order every reuse of a slot: a copy into a slot waits until the step that
+    last read that tensor has finished with it (x: its forward, g2: its
+    backward), and a backward waits until the copy out of its dx slot (from two
+    steps earlier) has finished.
     The host buffers must stay untouched until `synchronize()` (or until the
     copy-out of that step has completed)."""
 
@@ -356,7 +359,8 @@ class HostStaged:
         self.dx = [torch.empty((M, d), dtype=BF16, device=dev) for _ in range(2)]
         self.s_in = torch.cuda.Stream(dev)
         self.s_out = torch.cuda.Stream(dev)
-        self.read_done = [None, None]   # compute of the slot's last step finished
+        self.x_read = [None, None]      # forward of the slot's last step finished (x free)
+        self.g2_read = [None, None]     # backward of the slot's last step finished (g2 free)
         self.out_done = [None, None]    # copy-out of the slot's last dx finished
         self.n = 0
 
@@ -368,20 +372,28 @@ class HostStaged:
     def step(self, x_h, g2_h, dx_h, w13, w2, groups, seed=3):
         k = self.n % 2
         comp = torch.cuda.current_stream()
-        if self.read_done[k] is not None:
-            self.s_in.wait_event(self.read_done[k])
+        x_in, g2_in = torch.cuda.Event(), torch.cuda.Event()
         with torch.cuda.stream(self.s_in):
+            if self.x_read[k] is not None:
+                self.s_in.wait_event(self.x_read[k])
             self.x[k].copy_(x_h, non_blocking=True)
+            x_in.record(self.s_in)
+            if self.g2_read[k] is not None:
+                self.s_in.wait_event(self.g2_read[k])
             self.g2[k].copy_(g2_h, non_blocking=True)
-        landed = torch.cuda.Event()
-        landed.record(self.s_in)
-        comp.wait_event(landed)
+            g2_in.record(self.s_in)
+        comp.wait_event(x_in)
+        self.layer.forward(self.x[k], w13, w2, groups, comp, seed)
+        fwd_done = torch.cuda.Event()
+        fwd_done.record(comp)
+        self.x_read[k] = fwd_done
+        comp.wait_event(g2_in)
         if self.out_done[k] is not None:
             comp.wait_event(self.out_done[k])
-        self.layer.step(self.x[k], w13, w2, self.g2[k], groups, seed, stream=comp, dx_out=self.dx[k])
+        self.layer.backward(self.g2[k], groups, seed, comp, dx_out=self.dx[k])
         done = torch.cuda.Event()
         done.record(comp)
-        self.read_done[k] = done
+        self.g2_read[k] = done
         self.s_out.wait_event(done)
         with torch.cuda.stream(self.s_out):
             dx_h.copy_(self.dx[k], non_blocking=True)
