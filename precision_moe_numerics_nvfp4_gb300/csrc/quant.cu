@@ -167,14 +167,22 @@ struct NvQuantArgs {
   int *status;
 };
 
+// inv_tab: when the outer scale is the same for every block of the CTA, the
+// 127 values fp32(1 / fp32(s * sg)) of the E4M3 codes (0 for code 0), read
+// instead of computing the reciprocal per block (the same bits)
 __device__ __forceinline__ void nvfp4_block(const uint4 &a, const uint4 &b, float sg, float den6, uint2 &codes,
-                                            uint32_t &scode) {
+                                            uint32_t &scode, const float *inv_tab = nullptr) {
   uint32_t m = bf16x2_absmax(bf16x2_absmax(a.x, a.y), bf16x2_absmax(a.z, a.w));
   m = bf16x2_absmax(m, bf16x2_absmax(bf16x2_absmax(b.x, b.y), bf16x2_absmax(b.z, b.w)));
   const float bamax = bf16x2_max_to_f32(m);
   scode = cvt_e4m3_rn(__fdiv_rn(bamax, den6));
-  const float s = e4m3_to_f32(scode);
-  const float inv = (s == 0.0f) ? 0.0f : __frcp_rn(__fmul_rn(s, sg));
+  float inv;
+  if (inv_tab) {
+    inv = inv_tab[scode];
+  } else {
+    const float s = e4m3_to_f32(scode);
+    inv = (s == 0.0f) ? 0.0f : __frcp_rn(__fmul_rn(s, sg));
+  }
   codes.x = cvt_e2m1x8(__fmul_rn(bf16_lo(a.x), inv), __fmul_rn(bf16_hi(a.x), inv), __fmul_rn(bf16_lo(a.y), inv),
                        __fmul_rn(bf16_hi(a.y), inv), __fmul_rn(bf16_lo(a.z), inv), __fmul_rn(bf16_hi(a.z), inv),
                        __fmul_rn(bf16_lo(a.w), inv), __fmul_rn(bf16_hi(a.w), inv));
@@ -186,6 +194,14 @@ __device__ __forceinline__ void nvfp4_block(const uint4 &a, const uint4 &b, floa
 __device__ __forceinline__ void nvfp4_block46(const uint4 &a, const uint4 &b, float sg, uint2 &codes,
                                               uint32_t &scode);
 
+// the reciprocal table of nvfp4_block for one outer scale (threads 0..127)
+__device__ __forceinline__ void fill_inv_table(float *tab, float sg) {
+  if (threadIdx.x < 128) {
+    const float s = e4m3_to_f32(threadIdx.x);
+    tab[threadIdx.x] = (s == 0.0f) ? 0.0f : __frcp_rn(__fmul_rn(s, sg));  // the formula of nvfp4_block
+  }
+}
+
 __global__ void __launch_bounds__(256) nvfp4_quant_kernel(NvQuantArgs A) {
   __shared__ __align__(16) uint8_t s_sc[4 * 512];
   __shared__ GroupSmem s_g;
@@ -195,6 +211,8 @@ __global__ void __launch_bounds__(256) nvfp4_quant_kernel(NvQuantArgs A) {
   const Window w = map_window(grouped, blockIdx.y, E, s_g.off, s_g.pad, A.rows, A.wpb);
   const float sg = A.sg_rows ? 1.0f : A.sg[grouped ? 0 : w.seg];
   const float den6 = __fmul_rn(6.0f, sg);
+  __shared__ float s_inv[128];
+  fill_inv_table(s_inv, sg);
 
   reinterpret_cast<uint2 *>(s_sc)[threadIdx.x] = make_uint2(0u, 0u);
   __syncthreads();
@@ -232,7 +250,7 @@ __global__ void __launch_bounds__(256) nvfp4_quant_kernel(NvQuantArgs A) {
       } else if (A.four_six) {
         nvfp4_block46(va[u], vb[u], sg, c, sc);
       } else {
-        nvfp4_block(va[u], vb[u], sg, den6, c, sc);
+        nvfp4_block(va[u], vb[u], sg, den6, c, sc, s_inv);
       }
       *reinterpret_cast<uint2 *>(A.codes + (off[u] >> 1)) = c;
       s_sc[(kbl >> 2) * 512 + atom_pos(i, kbl)] = (uint8_t)sc;
@@ -628,6 +646,8 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant
     // bf16 -> NVFP4 with the quantizer's block rule (nvfp4_block), codes to
     // global memory, scales to the shared tile; the exact f16 products of the
     // new codes replace the unit's bf16 values in place for phase 2
+    __shared__ float s_inv[128];
+    if (!kRows) fill_inv_table(s_inv, sg);
     stage_bf16_tile(A, w, col0, s_in);
     __syncthreads();
     const float den6 = __fmul_rn(6.0f, sg);
@@ -645,7 +665,7 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant
       } else if (k46) {
         nvfp4_block46(va, vb, sg, c, sc);
       } else {
-        nvfp4_block(va, vb, sg, den6, c, sc);  // an all-zero (padding) block gives scale 0 and zero codes
+        nvfp4_block(va, vb, sg, den6, c, sc, s_inv);  // an all-zero (padding) block gives scale 0 and zero codes
       }
       if (i < w.nvalid)
         *reinterpret_cast<uint2 *>(A.nv_codes_out + ((w.src_row0 + i) * A.cols + col0 + kb * 16) / 2) = c;
