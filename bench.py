@@ -211,7 +211,11 @@ class EventLog:
 
     def call(self, name, fn, *a, **k):
         import torch
-        s = torch.cuda.current_stream()
+        s = k.get("stream")  # the call's own stream when it names one, else the current one
+        if s is None:
+            s = next((v for v in a if isinstance(v, torch.cuda.Stream)), None)
+        if s is None:
+            s = torch.cuda.current_stream()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(s)
         fn(*a, **k)
@@ -259,12 +263,19 @@ def kernel_units(layer, m):
     fl2 = 2.0 * M * d * I
     # quantize (+ requant) of h: no amax pass when the w13 epilogue produced its outer scale
     h_amax = 0.0 if layer.fuse_swiglu else 2.0
-    if getattr(layer, "four_six", False):  # activations x and h through the Four Over Six calls
-        return {
-            "nvfp4_quantize": [(E * 2 * I * d, 4.5625), (E * d * I, 4.5625)],
-            "nvfp4_quantize_four_over_six": [(M * d, 4.5625), (M * I, 2.5625 + h_amax)],
-            "nvfp4_quantize_requant": [(E * 2 * I * d, 5.59375), (E * d * I, 5.59375)],
-            "nvfp4_quantize_requant_four_over_six": [(M * d, 5.59375), (M * I, 3.59375 + h_amax)],
+    side = getattr(layer, "side", None) is not None
+    if side or getattr(layer, "four_six", False):
+        # side stream: the amax passes of w13, w2 and x are nvfp4_outer_scale
+        # calls and the quantize calls take the scales as given; Four Over Six:
+        # the activation calls have their own names
+        a = 0.0 if side else 2.0
+        act = "_four_over_six" if getattr(layer, "four_six", False) else ""
+        q, qr = (2.5625, 3.59375)
+        w_q = [(E * 2 * I * d, q + a), (E * d * I, q + a)]
+        w_qr = [(E * 2 * I * d, qr + a), (E * d * I, qr + a)]
+        x_q = [(M * d, q + a), (M * I, q + h_amax)]
+        x_qr = [(M * d, qr + a), (M * I, qr + h_amax)]
+        units = {
             "grouped_gemm_nvfp4_fwd": [fl2] if layer.fuse_swiglu else [fl13, fl2],
             "grouped_gemm_nvfp4_fwd_swiglu": [fl13],
             "dequant_transpose_requant_sr": [(E * 2 * I * d, 1.59375), (E * d * I, 1.59375), (M * d, 1.59375),
@@ -275,6 +286,14 @@ def kernel_units(layer, m):
             "nvfp4moe_swiglu_fwd": [(M * I, 3 * 2.0)],
             "nvfp4moe_swiglu_bwd": [(M * I, 5 * 2.0)],
         }
+        if side:
+            units["nvfp4_outer_scale"] = [(E * 2 * I * d, 2.0), (E * d * I, 2.0), (M * d, 2.0)]
+        if act:
+            units.update({"nvfp4_quantize": w_q, "nvfp4_quantize_requant": w_qr,
+                          "nvfp4_quantize" + act: x_q, "nvfp4_quantize_requant" + act: x_qr})
+        else:
+            units.update({"nvfp4_quantize": w_q + x_q, "nvfp4_quantize_requant": w_qr + x_qr})
+        return units
     if getattr(layer, "per_token", False):  # activations: the row amax pass (2 B/elem) runs inside the call
         return {
             "nvfp4_quantize_rows": [(M * d, 4.5625), (M * I, 2.5625 + h_amax)],

@@ -145,6 +145,18 @@ int nvfp4_quantize(const void *x, int64_t batch, int64_t rows, int64_t cols,
                    uint8_t *codes, uint8_t *scales,
                    void *workspace, size_t workspace_bytes, nv_stream_t stream);
 
+/* ---- the outer scales alone (the amax pass of nvfp4_quantize) ------------------------
+ * sg[b] = amax / 2688 of each of `batch` consecutive bf16 tensors of n values
+ * (1 for an all-zero or empty tensor), exactly as nvfp4_quantize computes
+ * them; feeding them back as outer_scale_in gives nvfp4_quantize's own
+ * result.  Lets the amax pass of one tensor run on another stream while an
+ * earlier tensor is being quantized.  n % 8 == 0; x 16-byte aligned;
+ * outer_scale_out fp32 [batch]; workspace nvfp4moe_quantize_workspace_bytes(
+ * batch, 1, n) bytes (16-byte aligned; else NV_ERR_WORKSPACE).
+ */
+int nvfp4_outer_scale(const void *x, int64_t batch, int64_t n, float *outer_scale_out,
+                      void *workspace, size_t workspace_bytes, nv_stream_t stream);
+
 /* ---- nvfp4_quantize for callers that cannot allocate device memory -------------
  * The pages have no counterpart to this entry point; it is a convenience of
  * this library.  nvfp4_quantize needs a caller-provided workspace when it

@@ -103,6 +103,26 @@ int nvfp4moe_selftest_wait_timeout(int64_t spins, nv_stream_t stream) {
   return launch_wait_selftest(spins, st, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int nvfp4_outer_scale(const void *x, int64_t batch, int64_t n, float *outer_scale_out, void *workspace,
+                      size_t workspace_bytes, nv_stream_t stream) {
+  if (!x || !outer_scale_out || batch < 1 || n < 0) return NV_ERR_ARG;
+  if (n % 8) return NV_ERR_SHAPE;
+  if (!al16(x) || !al4(outer_scale_out)) return NV_ERR_ALIGN;
+  const size_t need = nvfp4moe_quantize_workspace_bytes(batch, 1, n);
+  if (!workspace || workspace_bytes < need || !al16(workspace)) return NV_ERR_WORKSPACE;
+  if (n == 0) {  // an empty tensor: scale 1
+    const float one[1] = {1.0f};
+    for (int64_t b = 0; b < batch; ++b)
+      if (cudaMemcpyAsync(outer_scale_out + b, one, sizeof(float), cudaMemcpyHostToDevice,
+                          reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return NV_ERR_CUDA;
+    return NV_OK;
+  }
+  const int nb = amax_blocks(n);
+  return launch_amax(static_cast<const uint16_t *>(x), batch, n, static_cast<float *>(workspace), nb,
+                     outer_scale_out, reinterpret_cast<cudaStream_t>(stream));
+}
+
 static int quantize_impl(const void *x, int64_t batch, int64_t rows, int64_t cols, const int32_t *group_offsets,
                          int32_t num_groups, const float *outer_scale_in, float *outer_scale_out, uint8_t *codes,
                          uint8_t *scales, void *workspace, size_t workspace_bytes, nv_stream_t stream,

@@ -63,6 +63,7 @@ _SIGS = {
     "nvfp4moe_set_gemm_kernel": (ctypes.c_int, [ctypes.c_int]),
     "grouped_gemm_nvfp4_fwd_rht_s2f6": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I32, _I64, _I64, _I64,
                                                        ctypes.c_uint32, _P, _P, _P, _P]),
+    "nvfp4_outer_scale": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _SZ, _P]),
     "nvfp4_quantize_four_over_six": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _I32, _P, _P, _P, _P, _P, _SZ, _P]),
     "nvfp4_quantize_requant_four_over_six": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _I32, _P, _P, _P, _P, _P, _SZ,
                                                             _U64, _U64, _P, _P, _P]),
@@ -244,6 +245,12 @@ def grouped_gemm_nvfp4_fwd_swiglu(x_outer_scale, x_codes, x_scales, w13_codes, w
         _ptr(x_outer_scale), _ptr(x_codes), _ptr(x_scales), _ptr(w13_codes), _ptr(w13_scales),
         _ptr(w13_outer_scale), _ptr(group_offsets), E, M_total, I, K, _ptr(y13), _ptr(h), _ptr(h_outer_scale),
         _stream(stream)))
+
+
+def nvfp4_outer_scale(x, batch, n, outer_scale_out, workspace, stream=None):
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return _check("nvfp4_outer_scale", lib().nvfp4_outer_scale(
+        _ptr(x), batch, n, _ptr(outer_scale_out), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def nvfp4_quantize_four_over_six(x, batch, rows, cols, group_offsets, outer_scale_in, outer_scale_out, codes, scales,

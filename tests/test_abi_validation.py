@@ -86,3 +86,12 @@ def test_fwd_with_bf16_activations_validation(L):
     assert f(A, NULL, NULL, NULL, A, A, A, A, E, M, N_, K, A, N.NV_OUT_BF16, A, need - 1, S) == N.NV_ERR_WORKSPACE
     assert f(A, NULL, NULL, NULL, A, A, A, A, E, M, N_, K, A, N.NV_OUT_BF16, A4, need, S) == N.NV_ERR_WORKSPACE
     assert f(A4, NULL, NULL, NULL, A, A, A, A, E, M, N_, K, A, N.NV_OUT_BF16, A, need, S) == N.NV_ERR_ALIGN
+
+
+def test_outer_scale_validation(L):
+    f = L.nvfp4_outer_scale
+    ws = N.nvfp4moe_quantize_workspace_bytes(2, 1, 4096)
+    assert f(NULL, 2, 4096, A, A, ws, S) == N.NV_ERR_ARG
+    assert f(A, 2, 4100, A, A, ws, S) == N.NV_ERR_SHAPE        # n % 8
+    assert f(A4, 2, 4096, A, A, ws, S) == N.NV_ERR_ALIGN
+    assert f(A, 2, 4096, A, A, ws - 1, S) == N.NV_ERR_WORKSPACE

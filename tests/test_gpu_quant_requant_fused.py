@@ -89,3 +89,37 @@ def test_fused_against_oracle():
     assert np.array_equal(got_c, want_c)
     got_s = L.unswizzle(mb.scales.cpu().numpy(), L.batched_row_map(batch, cols), rows // 32)
     assert np.array_equal(got_s.reshape(want_s.shape), want_s)
+
+
+def test_outer_scale_alone_equals_quantize_and_feeds_back():
+    """nvfp4_outer_scale computes the outer scales nvfp4_quantize computes;
+    given back as outer_scale_in they reproduce its result bit for bit."""
+    batch, rows, cols = 3, 256, 384
+    x = _x((batch, rows, cols), seed=77, std=0.05)
+    a = NvTensor(batch, rows, cols, dev())
+    N.nvfp4_quantize(x, batch, rows, cols, None, None, a.sg, a.codes, a.scales, a.ws)
+    b = NvTensor(batch, rows, cols, dev())
+    N.nvfp4_outer_scale(x, batch, rows * cols, b.sg, b.ws)
+    N.nvfp4_quantize(x, batch, rows, cols, None, b.sg, b.sg, b.codes, b.scales, None)
+    check_status()
+    assert torch.equal(a.sg, b.sg) and torch.equal(a.codes, b.codes) and torch.equal(a.scales, b.scales)
+
+
+def test_moe_layer_side_stream_amax_equals_inline():
+    """The layer's side-stream amax passes change nothing: forward and
+    backward outputs equal the inline-amax layer's bit for bit."""
+    from precision_moe_numerics_nvfp4_gb300 import workloads as W
+    from precision_moe_numerics_nvfp4_gb300.pipeline import MoELayer
+    m = W.moe("cuda", seed=2, tokens=160, d_model=256, experts=8, topk=4, d_ff=256, with_grad=True)
+    M = m.x_perm.shape[0]
+    outs = []
+    for overlap in (True, False):
+        layer = MoELayer(M, 256, 256, 8, overlap_amax=overlap)
+        for _ in range(2):  # a second step reuses the scale buffers
+            layer.step(m.x_perm, m.w13, m.w2, m.g2, m.group_offsets, seed=3)
+        torch.cuda.synchronize()
+        check_status()
+        outs.append([t.clone() for t in (layer.xq.sg, layer.w13q.sg, layer.w2q.sg, layer.y2, layer.dx, layer.dw13,
+                                         layer.dw2)])
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
