@@ -772,21 +772,26 @@ def run_decode(args):
     layer.quantize_weights(m.w13, m.w2)
     params = E * (2 * I * D + D * I)
     wbytes = params * 0.5625
+    fwd = lambda: layer.forward_activations(m.x_perm, m.group_offsets)
+    if args.graph:  # the whole forward as one CUDA graph: no launch gaps between its kernels
+        graph = MoELayer.capture(fwd)
+        fwd = graph.replay
     for _ in range(args.warmup):
-        layer.forward_activations(m.x_perm, m.group_offsets)
+        fwd()
     torch.cuda.synchronize()
     s = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(s)
     for _ in range(args.steps):
-        layer.forward_activations(m.x_perm, m.group_offsets)
+        fwd()
     e1.record(s)
     torch.cuda.synchronize()
     assert N.nvfp4moe_get_device_status() == 0
     ms = e0.elapsed_time(e1) / args.steps
     gbs = wbytes / (ms / 1e3) / 1e9
     sizes = torch.diff(m.group_offsets.to(torch.int64))
-    print(json.dumps({"workload": "decode", "experts": E, "rows": M, "min_group": int(sizes.min()),
+    print(json.dumps({"workload": "decode", "graph": bool(args.graph), "experts": E, "rows": M,
+                      "min_group": int(sizes.min()),
                       "max_group": int(sizes.max()), "weight_bytes": wbytes, "ms": ms, "GB_s": gbs,
                       "frac_hbm": gbs / peaks["hbm_gbs"], "peak_source": peaks["source"]}))
 
@@ -803,6 +808,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=["moe", "quant_sweep", "gemm", "decode", "rht_s2f6"], default="moe")
     ap.add_argument("--gemm-kind", choices=["fwd", "dx", "dw"], default="fwd")
+    ap.add_argument("--graph", action="store_true", help="decode workload: replay the forward as a CUDA graph")
     ap.add_argument("--four-over-six", action="store_true",
                     help="moe workload: the Four Over Six block rule for the activations x and h")
     ap.add_argument("--per-token", action="store_true",

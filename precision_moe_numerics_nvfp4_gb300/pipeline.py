@@ -350,6 +350,22 @@ class MoELayer:
         self.forward(x, w13, w2, groups, stream, seed)
         self.backward(g2, groups, seed, stream, dx_out)
 
+    @staticmethod
+    def capture(fn):
+        """Capture `fn()` -- this layer's calls on the current stream, e.g.
+        `lambda: layer.forward_activations(x, groups)` -- into a CUDA graph
+        and return it; `graph.replay()` reruns the same launches on the same
+        buffers.  One eager call first sets up what the library does once
+        (kernel attributes, occupancy queries, the device status word), none
+        of which may run during a capture."""
+        fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        torch.cuda.synchronize()
+        return g
+
     def launches_per_step(self):
         """Kernels one step launches: forward = 4 NVFP4 quantizations x 3
         kernels (amax, finalize, quantize or quantize + requant) + 2 GEMMs +

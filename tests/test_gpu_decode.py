@@ -72,3 +72,30 @@ def test_decode_forward_full_size():
                                       np.array([0, len(rows)]))
         y2 = layer.y2[torch.as_tensor(rows, device="cuda")].float().cpu().numpy()
         assert G.within_bound(y2, y_ref, bound, bf16_out=True).all()
+
+
+def test_decode_forward_replays_as_a_cuda_graph():
+    """The decode forward captured into a CUDA graph and replayed gives the
+    eager forward's outputs bit for bit (every library call is capturable
+    once its one-time setup has run), also after new activations are copied
+    into the captured input buffer."""
+    import torch
+    from precision_moe_numerics_nvfp4_gb300 import workloads as W
+    from precision_moe_numerics_nvfp4_gb300.pipeline import MoELayer
+    m = W.decode("cuda")
+    M, D, I, E = m.x_perm.shape[0], 7168, 2048, 128
+    layer = MoELayer(M, D, I, E, backward=False)
+    layer.quantize_weights(m.w13, m.w2)
+    x = m.x_perm.clone()
+    graph = MoELayer.capture(lambda: layer.forward_activations(x, m.group_offsets))
+    x2 = (m.x_perm.float() * 0.5).to(x.dtype)
+    for src in (m.x_perm, x2):
+        layer.forward_activations(src, m.group_offsets)
+        torch.cuda.synchronize()
+        want = layer.y2.clone()
+        layer.y2.zero_()
+        x.copy_(src)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(layer.y2, want)
+    assert N.nvfp4moe_get_device_status() == 0
