@@ -191,6 +191,44 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return d;
 }
 
+// Stores 128 bytes of each of a warp's 32 output rows (lane = row; w[] =
+// the lane's 32 words, row rr at seg0 + rr * ld_bytes) as whole 128-byte
+// lines.  Each group of four lanes transposes its 4 x 4 block of 32-byte
+// chunks with two butterfly exchanges (over lane bits 1 and 0), after which
+// lane 4g + i holds chunk i of rows 4g .. 4g + 3; store k then writes row
+// 4g + k's 128 bytes with the group's four lanes: eight full lines per
+// instruction, where storing each lane's own row touches 32 lines.  Rows from
+// `nrows` on are not stored.  Every lane of the warp must call it.
+__device__ __forceinline__ void store_segment_coalesced(uint8_t *seg0, int64_t ld_bytes, uint32_t (&w)[32], int lane,
+                                                        int nrows) {
+  const int g = lane >> 2, i = lane & 3;
+#pragma unroll
+  for (int d = 2; d >= 1; d >>= 1) {
+    const bool b = (lane & d) != 0;
+#pragma unroll
+    for (int j0 = 0; j0 < 4; ++j0) {
+      if (j0 & d) continue;
+      const int j1 = j0 | d;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const uint32_t got = __shfl_xor_sync(0xFFFFFFFFu, b ? w[8 * j0 + e] : w[8 * j1 + e], d);
+        if (b)
+          w[8 * j0 + e] = got;
+        else
+          w[8 * j1 + e] = got;
+      }
+    }
+  }
+  uint8_t *p = seg0 + (int64_t)(4 * g) * ld_bytes + 32 * i;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    if (4 * g + k < nrows)
+      st_cs_v8(p, w[8 * k], w[8 * k + 1], w[8 * k + 2], w[8 * k + 3], w[8 * k + 4], w[8 * k + 5], w[8 * k + 6],
+               w[8 * k + 7]);
+    p += ld_bytes;
+  }
+}
+
 // A bounded mbarrier wait that also gives up when another role of the CTA
 // has raised the abort flag.  A wait that runs out raises the flag and records
 // NV_ERR_TIMEOUT.
@@ -979,7 +1017,19 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BN, CHUNKS>::kThreads,
         else
           mbar_arrive_cluster(acc_empty_addr);
       }
-      if (store) {
+      if (KIND == kGemmMxfp8Dw && A.out_fp32) {
+        // wgrad: fp32 dW rows are 512 bytes per lane and the stores are the
+        // epilogue's bottleneck, so the warp writes them as whole lines (the
+        // tile's 128 rows all exist; alpha is 1)
+        uint8_t *row0 = static_cast<uint8_t *>(A.out) + ((T.out_row0 + q * 32) * A.out_ld + ocol) * 4;
+#pragma unroll
+        for (int S = 0; S < 4; ++S) {
+          uint32_t w[32];
+#pragma unroll
+          for (int k = 0; k < 32; ++k) w[k] = r[32 * S + k];
+          store_segment_coalesced(row0 + 128 * S, A.out_ld * 4, w, lane, T.mrows - q * 32);
+        }
+      } else if (store) {
         if (A.out_fp32) {
           float *dst = static_cast<float *>(A.out) + orow * A.out_ld + ocol;
 #pragma unroll
