@@ -542,6 +542,16 @@ __global__ void __launch_bounds__(192, 2)
           for (int d = 16; d > 0; d >>= 1) hmax = fmaxf(hmax, __shfl_xor_sync(0xFFFFFFFFu, hmax, d));
           if (lane == 0 && hmax > 0.0f) atomicMax(A.h_amax, __float_as_uint(hmax));
         }
+      } else if (KIND == kGemmMxfp8Dw && A.out_fp32) {
+        // wgrad: the warp's 32 fp32 dW rows (all exist; alpha is 1) as whole lines
+        uint8_t *row0 = static_cast<uint8_t *>(A.out) + ((T.out_row0 + q * 32) * A.out_ld + T.out_col0) * 4;
+#pragma unroll
+        for (int S = 0; S < kBN / 32; ++S) {
+          uint32_t w[32];
+#pragma unroll
+          for (int k = 0; k < 32; ++k) w[k] = r[32 * S + k];
+          store_segment_coalesced(row0 + 128 * S, A.out_ld * 4, w, lane, T.mrows - q * 32);
+        }
       } else if (store) {
         if constexpr (KIND == kGemmNvfp4Fwd && kS2f6) {
           // the combine direction's quantizer on the bf16 output rows: each
