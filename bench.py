@@ -617,8 +617,9 @@ def run_quant_sweep(args):
 def run_gemm(args):
     """One grouped GEMM of the MoE layer at a reduced token count, optionally
     over fewer experts (same depth per expert, smaller footprint; for
-    profiling): fwd = x_q w13^T (N 3072, K 4096), dx = dy13 w13 (N 3072,
-    K 4096), dw = dy13^T x_q.  Prints achieved TFLOP/s."""
+    profiling): fwd = x_q w13^T (N 3072, K 4096), swiglu = the same GEMM with
+    SwiGLU and max |h| in its epilogue (y13 and h written), dx = dy13 w13
+    (N 3072, K 4096), dw = dy13^T x_q.  Prints achieved TFLOP/s."""
     import torch
     from precision_moe_numerics_nvfp4_gb300 import nvfp4moe as N
     from precision_moe_numerics_nvfp4_gb300 import workloads as W
@@ -638,6 +639,12 @@ def run_gemm(args):
         y = torch.empty((M, I2), dtype=torch.bfloat16, device=dev)
         fn = lambda: N.grouped_gemm_nvfp4_fwd(None, xq.sg, xq.codes, xq.scales, wq.codes, wq.scales, wq.sg, go, E, M,
                                               I2, d, y, N.NV_OUT_BF16)
+    elif args.gemm_kind == "swiglu":
+        y13 = torch.empty((M, I2), dtype=torch.bfloat16, device=dev)
+        h = torch.empty((M, I2 // 2), dtype=torch.bfloat16, device=dev)
+        h_sg = torch.empty(1, dtype=torch.float32, device=dev)
+        fn = lambda: N.grouped_gemm_nvfp4_fwd_swiglu(xq.sg, xq.codes, xq.scales, wq.codes, wq.scales, wq.sg, go, E, M,
+                                                     I2 // 2, d, y13, h, h_sg)
     else:
         g = (torch.randn((M, I2), device=dev) * 1e-3).to(torch.bfloat16)
         gr, gt = MxRows(M, I2, dev, E=E), MxTransposed(M, I2, dev, E=E)
@@ -807,7 +814,7 @@ def main(argv=None):
     ap.add_argument("--ref-dff", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=["moe", "quant_sweep", "gemm", "decode", "rht_s2f6"], default="moe")
-    ap.add_argument("--gemm-kind", choices=["fwd", "dx", "dw"], default="fwd")
+    ap.add_argument("--gemm-kind", choices=["fwd", "swiglu", "dx", "dw"], default="fwd")
     ap.add_argument("--graph", action="store_true", help="decode workload: replay the forward as a CUDA graph")
     ap.add_argument("--four-over-six", action="store_true",
                     help="moe workload: the Four Over Six block rule for the activations x and h")
