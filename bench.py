@@ -360,8 +360,7 @@ def run_ours(args):
     # timed region: device-resident inputs
     log = EventLog()
     step = build_step(layer, m, log)
-    sampler = ClockSampler(local, os.path.join(ROOT, "gpurun_out", "clocks.csv") if os.path.isdir(
-        os.path.join(ROOT, "gpurun_out")) else None)
+    sampler = ClockSampler(local, args.clocks_csv)
     sampler.start()
     barrier()
     torch.cuda.synchronize()
@@ -813,6 +812,7 @@ def main(argv=None):
     ap.add_argument("--ref-tokens", type=int, default=64)
     ap.add_argument("--ref-dff", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clocks-csv", default=None, help="also write the nvidia-smi clock samples of the timed region here")
     ap.add_argument("--workload", choices=["moe", "quant_sweep", "gemm", "decode", "rht_s2f6"], default="moe")
     ap.add_argument("--gemm-kind", choices=["fwd", "swiglu", "dx", "dw"], default="fwd")
     ap.add_argument("--graph", action="store_true", help="decode workload: replay the forward as a CUDA graph")
