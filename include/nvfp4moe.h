@@ -93,7 +93,7 @@ enum nv_status {
   NV_ERR_OFFSETS = -4,      /* (device) group offsets inconsistent */
   NV_ERR_TIMEOUT = -5,      /* (device) a bounded wait ran out */
   NV_ERR_CUDA = -6,         /* a CUDA runtime call failed */
-  NV_ERR_UNSUPPORTED = -7,  /* a feature or GPU this build does not support */
+  NV_ERR_UNSUPPORTED = -7,  /* a feature or GPU the compiled library does not support */
   NV_ERR_WORKSPACE = -8     /* workspace missing or too small */
 };
 enum nv_round { NV_RN = 0, NV_SR = 1 };
