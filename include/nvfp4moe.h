@@ -170,8 +170,13 @@ int nvfp4_outer_scale(const void *x, int64_t batch, int64_t n, float *outer_scal
  *    nvfp4moe_quantize_workspace_bytes(batch, rows, cols) <= 524288, else it
  *    returns NV_ERR_WORKSPACE and enqueues nothing.  With outer_scale_in set
  *    no scratch is used and there is no limit.
+ *  - Arguments are checked exactly as nvfp4_quantize checks them, before the
+ *    limit, so a bad call returns the same error through both entry points.
  *  - The first call on a device looks up the scratch's device address (with
- *    that device current); make that first call before any stream capture.
+ *    that device current) and caches it; make that first call before any
+ *    stream capture.  cudaDeviceReset invalidates the cached addresses (of
+ *    this scratch and of the status word): do not call the library again in a
+ *    process after resetting a device it has used.
  *  - Every call shares the one array and it keeps the last call's contents;
  *    nothing in it needs clearing (each call writes every slot it reads), but
  *    calls that overlap on the GPU (different streams, or another thread)
@@ -509,7 +514,9 @@ int nvfp4moe_get_device_status(nv_stream_t stream);
 /* Self-test of the bounded-wait path: launches one CTA that waits on an
  * mbarrier nothing arrives at, with an iteration limit of `spins`; the wait
  * runs out, the kernel records NV_ERR_TIMEOUT and returns.  No fault, no
- * hang.  Returns the launch status. */
+ * hang.  1 <= spins <= 2^20 (about a millisecond of polling), else NV_ERR_ARG
+ * and nothing is launched, so no caller can keep a CTA spinning for long.
+ * Returns the launch status. */
 int nvfp4moe_selftest_wait_timeout(int64_t spins, nv_stream_t stream);
 
 /* Static description of a status code (never NULL). */

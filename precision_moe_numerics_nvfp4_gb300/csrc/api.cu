@@ -1,6 +1,7 @@
 // The C ABI of libnvfp4moe.so: argument checks, the per-device status word,
 // and the launches of every step of the hot path.  See include/nvfp4moe.h for
 // the contract of each entry point.
+#include <atomic>
 #include <cstdio>
 
 #include "common.cuh"
@@ -11,16 +12,21 @@ namespace nvm {
 // First error any kernel recorded on this device (0 = none).
 static __device__ int g_status;
 
+// Looked up once per device (with that device current) and cached; host
+// threads that race on the first lookup store the same address, and the
+// atomic makes that race well-defined.
 int *status_ptr() {
-  static int *cache[64] = {};
+  static std::atomic<int *> cache[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (!cache[dev]) {
-    void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
-    cache[dev] = static_cast<int *>(p);
+  int *p = cache[dev].load(std::memory_order_acquire);
+  if (!p) {
+    void *a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_status) != cudaSuccess) return nullptr;
+    p = static_cast<int *>(a);
+    cache[dev].store(p, std::memory_order_release);
   }
-  return cache[dev];
+  return p;
 }
 
 static bool al16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -34,6 +40,20 @@ static int amax_blocks(int64_t per_batch) {
   if (nb < 1) nb = 1;
   if (nb > 1216) nb = 1216;
   return (int)nb;
+}
+
+// The argument and shape checks of nvfp4_quantize (also run first by
+// nvfp4_quantize_noalloc, so that both report the same error for the same
+// bad call).  Empty shapes pass.
+int quantize_check_args(const void *x, int64_t batch, int64_t rows, int64_t cols, const int32_t *group_offsets,
+                        int32_t num_groups, const uint8_t *codes, const uint8_t *scales) {
+  if (!x || !codes || !scales || batch < 1 || rows < 0 || cols < 0) return NV_ERR_ARG;
+  if (cols % 16) return NV_ERR_SHAPE;
+  if (group_offsets && (batch != 1 || num_groups < 1 || num_groups > kMaxGroups)) return NV_ERR_ARG;
+  if (!al16(x) || !al16(codes) || !al16(scales) || !al16(group_offsets)) return NV_ERR_ALIGN;
+  if (rows == 0 || cols == 0) return NV_OK;
+  if (rows * cols / 16 >= (int64_t)1 << 31 || (group_offsets && rows >= (int64_t)1 << 30)) return NV_ERR_SHAPE;
+  return NV_OK;
 }
 
 }  // namespace nvm
@@ -97,7 +117,7 @@ int nvfp4moe_get_device_status(nv_stream_t stream) {
 }
 
 int nvfp4moe_selftest_wait_timeout(int64_t spins, nv_stream_t stream) {
-  if (spins < 1) return NV_ERR_ARG;
+  if (spins < 1 || spins > kMaxSelftestSpins) return NV_ERR_ARG;
   int *st = status_ptr();
   if (!st) return NV_ERR_CUDA;
   return launch_wait_selftest(spins, st, reinterpret_cast<cudaStream_t>(stream));
@@ -110,14 +130,8 @@ int nvfp4_outer_scale(const void *x, int64_t batch, int64_t n, float *outer_scal
   if (!al16(x) || !al4(outer_scale_out)) return NV_ERR_ALIGN;
   const size_t need = nvfp4moe_quantize_workspace_bytes(batch, 1, n);
   if (!workspace || workspace_bytes < need || !al16(workspace)) return NV_ERR_WORKSPACE;
-  if (n == 0) {  // an empty tensor: scale 1
-    const float one[1] = {1.0f};
-    for (int64_t b = 0; b < batch; ++b)
-      if (cudaMemcpyAsync(outer_scale_out + b, one, sizeof(float), cudaMemcpyHostToDevice,
-                          reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
-        return NV_ERR_CUDA;
-    return NV_OK;
-  }
+  if (n == 0)  // an empty tensor: scale 1, written by a kernel (no host copy, so the call stays capturable)
+    return launch_fill_f32(outer_scale_out, batch, 1.0f, reinterpret_cast<cudaStream_t>(stream));
   const int nb = amax_blocks(n);
   return launch_amax(static_cast<const uint16_t *>(x), batch, n, static_cast<float *>(workspace), nb,
                      outer_scale_out, reinterpret_cast<cudaStream_t>(stream));
@@ -128,12 +142,9 @@ static int quantize_impl(const void *x, int64_t batch, int64_t rows, int64_t col
                          uint8_t *scales, void *workspace, size_t workspace_bytes, nv_stream_t stream,
                          int four_six) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (!x || !codes || !scales || batch < 1 || rows < 0 || cols < 0) return NV_ERR_ARG;
-  if (cols % 16) return NV_ERR_SHAPE;
-  if (group_offsets && (batch != 1 || num_groups < 1 || num_groups > kMaxGroups)) return NV_ERR_ARG;
-  if (!al16(x) || !al16(codes) || !al16(scales) || !al16(group_offsets)) return NV_ERR_ALIGN;
+  const int chk = quantize_check_args(x, batch, rows, cols, group_offsets, num_groups, codes, scales);
+  if (chk != NV_OK) return chk;
   if (rows == 0 || cols == 0) return NV_OK;
-  if (rows * cols / 16 >= (int64_t)1 << 31 || (group_offsets && rows >= (int64_t)1 << 30)) return NV_ERR_SHAPE;
   int *st = status_ptr();
   if (!st) return NV_ERR_CUDA;
   const float *sg = outer_scale_in;

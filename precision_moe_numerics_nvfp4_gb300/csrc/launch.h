@@ -9,6 +9,15 @@ namespace nvm {
 
 int *status_ptr();  // device address of this device's status word (api.cu)
 
+// largest iteration limit nvfp4moe_selftest_wait_timeout accepts
+constexpr int64_t kMaxSelftestSpins = (int64_t)1 << 20;
+
+// argument and shape checks of nvfp4_quantize (api.cu); NV_OK or NV_ERR_*
+int quantize_check_args(const void *x, int64_t batch, int64_t rows, int64_t cols, const int32_t *group_offsets,
+                        int32_t num_groups, const uint8_t *codes, const uint8_t *scales);
+// p[0 .. n) = v (one small kernel)
+int launch_fill_f32(float *p, int64_t n, float v, cudaStream_t s);
+
 int launch_amax(const uint16_t *x, int64_t batch, int64_t per_batch, float *partial, int nblk, float *sg_out,
                 cudaStream_t s);
 int launch_nvfp4_quant(const uint16_t *x, int64_t batch, int64_t rows, int64_t cols, const int32_t *groups, int E,

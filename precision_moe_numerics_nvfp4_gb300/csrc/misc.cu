@@ -73,6 +73,11 @@ __global__ void wait_selftest_kernel(int64_t spins, int *status) {
   if (threadIdx.x == 0 && !mbar_wait(a, 0, (uint64_t)spins)) record_error(status, NV_ERR_TIMEOUT);
 }
 
+__global__ void __launch_bounds__(256) fill_f32_kernel(float *__restrict__ p, int64_t n, float v) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    p[i] = v;
+}
+
 static int grid_for(int64_t n) {
   int64_t g = (n + 255) / 256;
   if (g > 152 * 16) g = 152 * 16;
@@ -86,6 +91,12 @@ int launch_swiglu_fwd(const uint16_t *y13, int64_t M, int64_t I, uint16_t *h, cu
 
 int launch_swiglu_bwd(const uint16_t *dh, const uint16_t *y13, int64_t M, int64_t I, uint16_t *dy13, cudaStream_t s) {
   swiglu_bwd_kernel<<<grid_for(M * I / 8), 256, 0, s>>>(dh, y13, M, I, dy13);
+  return cudaGetLastError() == cudaSuccess ? NV_OK : NV_ERR_CUDA;
+}
+
+int launch_fill_f32(float *p, int64_t n, float v, cudaStream_t s) {
+  if (n <= 0) return NV_OK;
+  fill_f32_kernel<<<grid_for(n), 256, 0, s>>>(p, n, v);
   return cudaGetLastError() == cudaSuccess ? NV_OK : NV_ERR_CUDA;
 }
 

@@ -95,3 +95,26 @@ def test_outer_scale_validation(L):
     assert f(A, 2, 4100, A, A, ws, S) == N.NV_ERR_SHAPE        # n % 8
     assert f(A4, 2, 4096, A, A, ws, S) == N.NV_ERR_ALIGN
     assert f(A, 2, 4096, A, A, ws - 1, S) == N.NV_ERR_WORKSPACE
+
+
+def test_selftest_spins_are_bounded(L):
+    f = L.nvfp4moe_selftest_wait_timeout
+    assert f(0, S) == N.NV_ERR_ARG                  # no iterations
+    assert f((1 << 20) + 1, S) == N.NV_ERR_ARG      # above the limit: refused before any launch
+    assert f(1 << 40, S) == N.NV_ERR_ARG
+
+
+def test_noalloc_reports_argument_errors_like_the_workspace_entry_point(L):
+    # a shape too large for the fixed scratch AND a bad argument: the argument
+    # error wins, exactly as nvfp4_quantize reports it
+    big = (1024, 16384, 256)
+    assert N.nvfp4moe_quantize_workspace_bytes(*big) > 524288
+    q, qn = L.nvfp4_quantize, L.nvfp4_quantize_noalloc
+    for args, want in [((NULL,) + big, N.NV_ERR_ARG),                    # no x
+                       ((A, 1024, 16384, 248), N.NV_ERR_SHAPE),           # cols % 16
+                       ((A4,) + big, N.NV_ERR_ALIGN)]:                    # x not 16-byte aligned
+        assert qn(*args, NULL, 0, NULL, A, A, A, S) == want
+        assert q(*args, NULL, 0, NULL, A, A, A, A, 1 << 30, S) == want
+    assert qn(A, *big, NULL, 0, NULL, A, NULL, A, S) == N.NV_ERR_ARG      # no codes
+    assert qn(A, *big, NULL, 0, NULL, A, A, A, S) == N.NV_ERR_WORKSPACE   # valid, too large
+    assert qn(A, 1, 0, 256, NULL, 0, NULL, A, A, A, S) == N.NV_OK         # empty: nothing launched

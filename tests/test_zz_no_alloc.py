@@ -18,19 +18,23 @@ def _input(shape, seed):
     return (torch.randn(shape, generator=g, device="cuda") * 0.05).to(torch.bfloat16).contiguous()
 
 
-def _run(fn_name, x, batch, rows, cols, groups=None):
+def _run(fn_name, x, batch, rows, cols, groups=None, sg_in=None, want_sg=True):
+    """Codes, scales and (when want_sg) the outer scales the call wrote."""
     E = None if groups is None else groups.numel() - 1
     cb, sb = N.nvfp4_sizes(batch, rows, cols, E)
     codes = torch.full((cb,), 0xA5, dtype=torch.uint8, device="cuda")
     scales = torch.full((sb,), 0xA5, dtype=torch.uint8, device="cuda")
-    sg = torch.full((batch,), -1.0, dtype=torch.float32, device="cuda")
+    sg = torch.full((batch,), -1.0, dtype=torch.float32, device="cuda") if want_sg else None
     if fn_name == "nvfp4_quantize":
         ws = torch.zeros(N.nvfp4moe_quantize_workspace_bytes(batch, rows, cols), dtype=torch.uint8, device="cuda")
-        N.nvfp4_quantize(x, batch, rows, cols, groups, None, sg, codes, scales, ws)
+        N.nvfp4_quantize(x, batch, rows, cols, groups, sg_in, sg, codes, scales, None if sg_in is not None else ws)
     else:
-        N.nvfp4_quantize_noalloc(x, batch, rows, cols, groups, None, sg, codes, scales)
+        N.nvfp4_quantize_noalloc(x, batch, rows, cols, groups, sg_in, sg, codes, scales)
     assert N.nvfp4moe_get_device_status() == 0
-    return codes.cpu().numpy(), scales.cpu().numpy(), sg.cpu().numpy()
+    out = [codes.cpu().numpy(), scales.cpu().numpy()]
+    if want_sg:
+        out.append(sg.cpu().numpy())
+    return out
 
 
 def test_noalloc_matches_workspace_entry_point_on_two_calls():
@@ -42,6 +46,43 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
         got = _run("nvfp4_quantize_noalloc", x, batch, rows, cols, go)
         for a, b in zip(ref, got):
             assert np.array_equal(a, b)
+
+
+def test_noalloc_without_outer_scale_output():
+    # outer_scale_out NULL: the outer scales then live in the shared scratch
+    # itself, between the amax pass and the quantizer that reads them
+    x = _input((2, 256, 192), 3)
+    for _ in range(2):
+        ref = _run("nvfp4_quantize", x, 2, 256, 192, want_sg=False)
+        got = _run("nvfp4_quantize_noalloc", x, 2, 256, 192, want_sg=False)
+        for a, b in zip(ref, got):
+            assert np.array_equal(a, b)
+
+
+def test_noalloc_with_given_outer_scale_has_no_size_limit():
+    # outer_scale_in set: no amax pass, no scratch, so a shape whose workspace
+    # would exceed the scratch (26216 matrices of 128 x 512, 3.4 GB of bf16)
+    # is accepted and matches the workspace entry point; compared on the device
+    batch, rows, cols = 26216, 128, 512
+    assert N.nvfp4moe_quantize_workspace_bytes(batch, rows, cols) > 524288
+    x = _input((batch, rows, cols), 4)
+    sg_in = torch.linspace(0.5, 2.0, batch, device="cuda", dtype=torch.float32)
+    cb, sb = N.nvfp4_sizes(batch, rows, cols, None)
+    outs = []
+    for fn in ("nvfp4_quantize", "nvfp4_quantize_noalloc"):
+        codes = torch.full((cb,), 0xA5, dtype=torch.uint8, device="cuda")
+        scales = torch.full((sb,), 0xA5, dtype=torch.uint8, device="cuda")
+        sg = torch.full((batch,), -1.0, dtype=torch.float32, device="cuda")
+        if fn == "nvfp4_quantize":
+            N.nvfp4_quantize(x, batch, rows, cols, None, sg_in, sg, codes, scales, None)
+        else:
+            N.nvfp4_quantize_noalloc(x, batch, rows, cols, None, sg_in, sg, codes, scales)
+        assert N.nvfp4moe_get_device_status() == 0
+        outs.append((codes, scales, sg))
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
+    assert torch.equal(outs[1][2], sg_in)
+    assert not torch.all(outs[1][0] == 0xA5)   # the codes were written
 
 
 def test_noalloc_refuses_requests_beyond_its_scratch():
