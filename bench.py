@@ -432,6 +432,10 @@ def run_ours(args):
     if rank == 0 and not args.no_cpu_baseline and not args.per_token and not args.four_over_six:
         # the oracle step is the per-tensor, plain-rule one
         cpu = cpu_baseline(args.cpu_tokens)
+    configs = None
+    if not args.no_configs and not args.per_token and not args.four_over_six:
+        del staged, x_h, g_h, dx_h
+        configs = other_configs(peaks, rank == 0 and not args.no_cpu_baseline)
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -448,6 +452,7 @@ def run_ours(args):
         "gpu_launches": layer.launches_per_step() * args.steps,
         "peaks": peaks,
         "cpu_baseline": cpu,
+        "configs": configs,
     }
     if rank == 0:
         print(json.dumps(line))
@@ -527,6 +532,351 @@ def cpu_baseline(tokens: int):
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"one expert of the workload with {tokens} routed rows, full d_model/d_ff, every step "
                       f"(quantize, GEMM references in float64, requant, SR) in numpy; {dt:.1f} s"}
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the other workloads: bounded samples, timed on one host core
+# and on all of them (spawned worker processes, one BLAS thread each)
+# ---------------------------------------------------------------------------
+def _oracle_single_linear(payload):
+    """The single linear layer, forward and backward, through the oracle: NVFP4
+    x and w, the FP64 forward GEMM, the SR re-quantization of both, the SR
+    MXFP8 quantization of g (row-wise and transposed) and the two backward
+    GEMMs.  Returns the GEMM FLOPs."""
+    from oracle import gemm as G
+    from oracle import layout as L
+    from oracle import mxfp8 as MX
+    from oracle import nvfp4 as NV
+    from oracle import requant as RQ
+    x, w, g = payload
+    T, din = x.shape
+    dout = w.shape[0]
+    o = np.array([0, T])
+    P = L.padded_cap(T, 1)
+    xc, xs, xsg = NV.quantize(x)
+    wc, ws, wsg = NV.quantize(w)
+    G.grouped_rows(NV.dequantize_f64(xc, xs, xsg), NV.dequantize_f64(wc, ws, wsg)[None], o)
+    wt = RQ.requant_weights(wc[None], ws[None], np.array([wsg]), 0, 0)
+    xt = RQ.requant_grouped(xc, xs, xsg, o, 0, 1, P)
+    gr = RQ.quantize_grad_rowwise(g, 0, 2)
+    gt = RQ.transposed_grouped_sr(g, o, 0, 3, P)
+    G.grouped_rows(MX.dequantize_f64(*gr), MX.dequantize_f64(wt[0][0], wt[1][0])[None], o)
+    G.grouped_contraction(MX.dequantize_f64(*gt), MX.dequantize_f64(*xt), np.array([0, P]))
+    return 3 * 2.0 * T * din * dout
+
+
+def _oracle_quant_op(payload):
+    """One op of the quantization sweep on a slice of rows; returns its
+    algorithmic bytes (the GPU kernel's per-element figure x elements)."""
+    from oracle import nvfp4 as NV
+    from oracle import requant as RQ
+    op, x, extra = payload
+    n = x.size
+    if op == "nvfp4_amax":  # far faster than the others: repeated so that the task outlasts its dispatch
+        for _ in range(100):
+            NV.outer_scale(x)
+        return 100 * 2.0 * n
+    if op == "nvfp4_quantize":
+        NV.quantize(x, extra)
+        return 2.5625 * n
+    if op == "mxfp8_quantize_rn":
+        RQ.quantize_rowwise_rn(x)
+        return 3.03125 * n
+    codes, scales, sg = extra  # dequant_transpose_requant_sr of the slice's NVFP4 form
+    RQ.requant_weights(codes[None], scales[None], np.array([sg]), 1, 0)
+    return 1.59375 * n
+
+
+def _oracle_decode_expert(payload):
+    """One expert of the decode forward through the oracle: its rows
+    quantized to NVFP4, the FP64 w13 GEMM over the dequantized (pre-quantized)
+    weights, SwiGLU, NVFP4 of h, the w2 GEMM.  Returns the NVFP4 weight +
+    scale bytes it consumed (0.5625 per parameter; the weight matrices here
+    are [2 I' x d] and [d x I'] for a slice of I' hidden features)."""
+    from oracle import gemm as G
+    from oracle import nvfp4 as NV
+    from oracle import swiglu as SW
+    x, w13q, w2q = payload
+    o = np.array([0, x.shape[0]])
+    xc, xs, xsg = NV.quantize(x)
+    y13, _ = G.grouped_rows(NV.dequantize_f64(xc, xs, xsg), NV.dequantize_f64(*w13q)[None], o)
+    h = SW.forward(y13.astype(np.float32))
+    hc, hs, hsg = NV.quantize(h.astype(np.float32))
+    G.grouped_rows(NV.dequantize_f64(hc, hs, hsg), NV.dequantize_f64(*w2q)[None], o)
+    return 0.5625 * (w13q[0].size + w2q[0].size)
+
+
+_ORACLE_TASKS = {"single_linear": _oracle_single_linear, "quant_op": _oracle_quant_op,
+                 "decode_expert": _oracle_decode_expert}
+
+
+def _oracle_worker(task):
+    """Runs one oracle task in a worker process and times it there."""
+    kind, payload = task
+    t0 = time.perf_counter()
+    units = _ORACLE_TASKS[kind](payload)
+    return units, time.perf_counter() - t0
+
+
+class OraclePools:
+    """Two pools of spawned worker processes (never forked from a process
+    that has used the GPU), one BLAS thread each: one worker for the
+    single-thread timings and one per host core for the all-core ones."""
+
+    KEYS = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS")
+
+    def __init__(self, cores):
+        import multiprocessing as mp
+        self.cores = cores
+        saved = {k: os.environ.get(k) for k in self.KEYS}
+        for k in self.KEYS:
+            os.environ[k] = "1"
+        try:
+            ctx = mp.get_context("spawn")
+            self.one = ctx.Pool(1)
+            self.all = ctx.Pool(cores)
+        finally:
+            for k, v in saved.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+        warm = [("quant_op", ("nvfp4_amax", np.zeros((1, 16), np.float32), None))]
+        self.one.map(_oracle_worker, warm)
+        self.all.map(_oracle_worker, warm * cores, chunksize=1)
+
+    def time(self, tasks_single, tasks_all):
+        """Units per second: the single-thread tasks one after another in one
+        worker (their own run time), and the all-core tasks at once (wall)."""
+        res = self.one.map(_oracle_worker, tasks_single, chunksize=1)
+        single = sum(u for u, _ in res) / sum(t for _, t in res)
+        t0 = time.perf_counter()
+        res = self.all.map(_oracle_worker, tasks_all, chunksize=1)
+        allc = sum(u for u, _ in res) / (time.perf_counter() - t0)
+        return single, allc
+
+    def close(self):
+        for p in (self.one, self.all):
+            p.close()
+            p.join()
+
+
+def _bf16_numpy(t):
+    import torch
+    return t.detach().to("cpu", torch.float32).numpy()
+
+
+def oracle_single_linear(pools):
+    from precision_moe_numerics_nvfp4_gb300 import workloads as W
+    s = W.single_linear("cpu")
+    payload = (_bf16_numpy(s.x), _bf16_numpy(s.w), _bf16_numpy(s.g))
+    single, allc = pools.time([("single_linear", payload)] * 2, [("single_linear", payload)] * pools.cores)
+    fl = 3 * 2.0 * 256 * 512 * 1024
+    return {"kind": "oracle", "cores": pools.cores, "unit": "us per fwd+bwd",
+            "sample": "the whole layer (seed 0), every step; all cores: one layer per core at once",
+            "single_thread": {"value": fl / single * 1e6, "threads": 1},
+            "all_cores": {"value": fl / allc * 1e6, "threads": pools.cores}}
+
+
+def oracle_quant_sweep(shapes, pools, rows_per_task=32):
+    """Per (shape, op): GB/s of algorithmic bytes on `rows_per_task` rows per
+    task (one task single-threaded, one per core at once)."""
+    from oracle import nvfp4 as NV
+    from precision_moe_numerics_nvfp4_gb300 import workloads as W
+    cores = pools.cores
+    out = []
+    for shape in shapes:
+        x = W.quant_sweep(shape, "cpu")
+        R, C = shape
+        slices = [_bf16_numpy(x[(i * rows_per_task) % R:(i * rows_per_task) % R + rows_per_task])
+                  for i in range(cores)]
+        del x
+        sg = [NV.outer_scale(v) for v in slices]
+        nvf = []
+        for v, g in zip(slices, sg):
+            c, sc, _ = NV.quantize(v, g)
+            nvf.append((c, sc, g))
+        for op in ("nvfp4_amax", "nvfp4_quantize", "mxfp8_quantize_rn", "dequant_transpose_requant_sr"):
+            extra = {"nvfp4_amax": [None] * cores, "nvfp4_quantize": sg,
+                     "mxfp8_quantize_rn": [None] * cores, "dequant_transpose_requant_sr": nvf}[op]
+            tasks = [("quant_op", (op, v, e)) for v, e in zip(slices, extra)]
+            single, allc = pools.time(tasks[:1], tasks)
+            out.append({"shape": [R, C], "op": op, "single_thread_GB_s": single / 1e9,
+                        "all_cores_GB_s": allc / 1e9})
+    return {"kind": "oracle", "cores": cores, "unit": "GB/s (algorithmic bytes)",
+            "sample": f"{rows_per_task} rows of each tensor per task (full width); all cores: one task per core, "
+                      f"different rows", "ops": out}
+
+
+def oracle_decode(sample, pools):
+    """`sample`: expert 0's weights restricted to the first 256 hidden
+    features (bf16, from the GPU run) and the routed rows of the first
+    experts; the weights are quantized once here (untimed, as on the GPU)."""
+    from oracle import nvfp4 as NV
+    w13, w2, rows = sample
+    w13q, w2q = NV.quantize(w13), NV.quantize(w2)
+    tasks = [("decode_expert", (r, w13q, w2q)) for r in rows[:pools.cores]]
+    single, allc = pools.time(tasks[:1], tasks)
+    return {"kind": "oracle", "cores": pools.cores, "unit": "GB/s of NVFP4 weight + scale bytes",
+            "sample": "expert 0's gate/up/down restricted to 256 of the 2048 hidden features, pre-quantized; one "
+                      "task per expert's routed rows; all cores: one task per core at once",
+            "single_thread": {"value": single / 1e9, "threads": 1},
+            "all_cores": {"value": allc / 1e9, "threads": pools.cores}}
+
+
+# ---------------------------------------------------------------------------
+# the other workloads on the GPU, measured in the default run beside the
+# MoE step: the single linear layer, the quantization sweep, the decode
+# ---------------------------------------------------------------------------
+class L2Flush:
+    """Writes a buffer larger than the L2 cache (512 MiB) so that the next
+    call reads its inputs from HBM."""
+
+    def __init__(self):
+        import torch
+        self.buf = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+
+    def __call__(self):
+        self.buf.zero_()
+
+
+def time_calls(fn, iters, flush=None):
+    """Mean device ms of fn() over `iters` calls, CUDA events on the current
+    stream around each call (the flush, when given, runs between calls,
+    outside the events)."""
+    import torch
+    s = torch.cuda.current_stream()
+    evs = []
+    for _ in range(iters):
+        if flush is not None:
+            flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        fn()
+        e1.record(s)
+        evs.append((e0, e1))
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in evs) / iters
+
+
+def gpu_single_linear(iters=50):
+    """Config: one expert linear layer x [256 x 512], w [1024 x 512], g [256 x
+    1024] (seed 0), forward and backward through the library; microseconds
+    per fwd+bwd, eager and replayed as one CUDA graph."""
+    import torch
+    from precision_moe_numerics_nvfp4_gb300 import workloads as W
+    from precision_moe_numerics_nvfp4_gb300.pipeline import MoELayer, SingleLinear
+    s = W.single_linear("cuda")
+    layer = SingleLinear(256, 512, 1024)
+    fn = lambda: layer.enqueue(s.x, s.w, s.g, seed=0)
+    for _ in range(3):
+        fn()
+    eager = time_calls(fn, iters)
+    graph = MoELayer.capture(fn)
+    for _ in range(3):
+        graph.replay()
+    replay = time_calls(graph.replay, iters)
+    return {"workload": "single expert linear, x [256 x 512] (4 rows x64), w [1024 x 512] (8 elements x100), "
+                        "g [256 x 1024], seed 0: NVFP4 fwd GEMM, SR requant of x and w, SR MXFP8 of g (row-wise + "
+                        "transposed), dgrad + wgrad",
+            "us_per_fwd_bwd": eager * 1e3, "us_per_fwd_bwd_graph": replay * 1e3, "calls": 10,
+            "gemm_flops": 3 * 2.0 * 256 * 512 * 1024, "roofline": "latency-bound (no roofline bar)"}
+
+
+def gpu_quant_sweep(peaks, iters=20):
+    """Config: the quantization-only sweep, bf16 [8192 x 8192] and [16384 x
+    7168], Student-t(3) x 0.05 with 0.01% x1000 (seed 1).  Per op: the amax
+    pass alone (nvfp4_outer_scale, 2 B/elem), the NVFP4 quantization with the
+    outer scale given (2.5625 B/elem), both in one call (4.5625), MXFP8 RN
+    row-wise (3.03125) and dequant -> transpose -> SR requant of the NVFP4
+    result (1.59375).  L2 is flushed before every timed call."""
+    import torch
+    from precision_moe_numerics_nvfp4_gb300 import nvfp4moe as N
+    from precision_moe_numerics_nvfp4_gb300 import workloads as W
+    from precision_moe_numerics_nvfp4_gb300.pipeline import MxRows, MxTransposed, NvTensor
+    flush = L2Flush()
+    out = []
+    for R, C in W.QUANT_SWEEP_SHAPES:
+        x = W.quant_sweep((R, C), "cuda")
+        nv = NvTensor(1, R, C, torch.device("cuda"))
+        mr = MxRows(R, C, torch.device("cuda"))
+        mt = MxTransposed(R, C, torch.device("cuda"), batch=1)
+        sg = torch.empty(1, dtype=torch.float32, device="cuda")
+        nv.quantize(x)
+        torch.cuda.synchronize()
+        ops = {
+            "nvfp4_amax": (lambda: N.nvfp4_outer_scale(x, 1, R * C, sg, nv.ws), 2.0),
+            "nvfp4_quantize_given_scale": (lambda: nv.quantize(x, sg_in=nv.sg), 2.5625),
+            "nvfp4_quantize": (lambda: nv.quantize(x), 4.5625),
+            "mxfp8_quantize_rn": (lambda: N.mxfp8_quantize(x, R, C, None, N.NV_RN, 0, 0, 0, mr.codes, mr.scales,
+                                                           None, None), 3.03125),
+            "dequant_transpose_requant_sr": (lambda: N.dequant_transpose_requant_sr(
+                nv.codes, nv.scales, nv.sg, 1, R, C, None, 1, 0, mt.codes, mt.scales), 1.59375),
+        }
+        for name, (fn, bpe) in ops.items():
+            for _ in range(3):
+                fn()
+            ms = time_calls(fn, iters, flush)
+            gbs = R * C * bpe / (ms / 1e3) / 1e9
+            out.append({"shape": [R, C], "op": name, "ms": ms, "GB_s": gbs, "frac_hbm": gbs / peaks["hbm_gbs"],
+                        "bytes_per_elem": bpe})
+        assert N.nvfp4moe_get_device_status() == 0
+        del x, nv, mr, mt
+    del flush
+    torch.cuda.empty_cache()
+    return {"workload": "quantization sweep: bf16 [8192 x 8192] and [16384 x 7168], Student-t(3) x 0.05 with 0.01% "
+                        "of elements x1000, seed 1", "l2": "flushed (512 MiB write) before every timed call",
+            "peak": peaks["hbm_gbs"], "ops": out}
+
+
+def gpu_decode(peaks, iters=50):
+    """Config: the sampler-style decode forward (128 experts [7168 x 2048]
+    gate/up/down pre-quantized, 256 tokens top-8), replayed as one CUDA
+    graph; GB/s of the NVFP4 weight + scale bytes (0.5625 B per parameter)."""
+    import torch
+    from precision_moe_numerics_nvfp4_gb300 import nvfp4moe as N
+    from precision_moe_numerics_nvfp4_gb300 import workloads as W
+    from precision_moe_numerics_nvfp4_gb300.pipeline import MoELayer
+    m = W.decode("cuda")
+    M, D, I, E = m.x_perm.shape[0], 7168, 2048, 128
+    layer = MoELayer(M, D, I, E, backward=False)
+    layer.quantize_weights(m.w13, m.w2)
+    wbytes = E * (2 * I * D + D * I) * 0.5625
+    graph = MoELayer.capture(lambda: layer.forward_activations(m.x_perm, m.group_offsets))
+    for _ in range(3):
+        graph.replay()
+    ms = time_calls(graph.replay, iters)
+    assert N.nvfp4moe_get_device_status() == 0
+    sizes = torch.diff(m.group_offsets.to(torch.int64))
+    gbs = wbytes / (ms / 1e3) / 1e9
+    go = m.group_offsets.to("cpu", torch.int64)
+    # the oracle's sample: expert 0 restricted to 256 hidden features, and
+    # the routed rows of the first experts
+    sample = (_bf16_numpy(torch.cat([m.w13[0, :256], m.w13[0, I:I + 256]])), _bf16_numpy(m.w2[0][:, :256]),
+              [_bf16_numpy(m.x_perm[int(go[e]):int(go[e + 1])]) for e in range(min(E, 64))])
+    del layer, m, graph
+    torch.cuda.empty_cache()
+    return sample, {"workload": "decode: 128 experts, gate/up/down [7168 x 2048] NVFP4 (pre-quantized), 256 tokens top-8, "
+                        f"{int(sizes.min())}..{int(sizes.max())} rows per expert, seed 4",
+            "ms": ms, "GB_s": gbs, "frac_hbm": gbs / peaks["hbm_gbs"], "weight_bytes": wbytes, "graph": True,
+            "l2": "weights (3.2 GB) exceed L2"}
+
+
+def other_configs(peaks, with_oracle):
+    """The single linear layer, the quantization sweep and the decode, each
+    with the oracle beside it (rank 0 only)."""
+    sample, dec = gpu_decode(peaks)
+    cfg = {"single_linear": gpu_single_linear(), "quant_sweep": gpu_quant_sweep(peaks), "decode": dec}
+    if with_oracle:
+        from precision_moe_numerics_nvfp4_gb300 import workloads as W
+        pools = OraclePools(os.cpu_count() or 1)
+        try:
+            cfg["single_linear"]["oracle"] = oracle_single_linear(pools)
+            cfg["quant_sweep"]["oracle"] = oracle_quant_sweep(W.QUANT_SWEEP_SHAPES, pools)
+            cfg["decode"]["oracle"] = oracle_decode(sample, pools)
+        finally:
+            pools.close()
+    return cfg
 
 
 def run_reference(args):
@@ -812,6 +1162,8 @@ def main(argv=None):
     ap.add_argument("--ref-tokens", type=int, default=64)
     ap.add_argument("--ref-dff", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="moe workload: skip the single-layer, quantization-sweep and decode records")
     ap.add_argument("--clocks-csv", default=None, help="also write the nvidia-smi clock samples of the timed region here")
     ap.add_argument("--workload", choices=["moe", "quant_sweep", "gemm", "decode", "rht_s2f6"], default="moe")
     ap.add_argument("--gemm-kind", choices=["fwd", "swiglu", "dx", "dw"], default="fwd")
