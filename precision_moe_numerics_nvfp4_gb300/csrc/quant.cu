@@ -194,6 +194,33 @@ __device__ __forceinline__ void nvfp4_block(const uint4 &a, const uint4 &b, floa
 __device__ __forceinline__ void nvfp4_block46(const uint4 &a, const uint4 &b, float sg, uint2 &codes,
                                               uint32_t &scode);
 
+// nvfp4_block with the division bamax / den6 read from a table and the
+// element multiplies packed two at a time; the same bits.  qtab[m] holds
+// fp32((1 + m / 128) / den6): for a normal bf16 block maximum
+// (1 + m / 128) 2^e, fp32(bamax / den6) = qtab[m] 2^e exactly while the
+// quotient is a normal fp32 number (scaling by a power of two commutes with
+// rounding there), and below that range or at overflow both forms give the
+// same E4M3 code (0, or the 448 saturation).  A subnormal bf16 maximum takes
+// the division.  inv_tab as in nvfp4_block.
+__device__ __forceinline__ void mul2_rn(float a, float b, float m, float &ra, float &rb);
+__device__ __forceinline__ void nvfp4_block_tab(const uint4 &a, const uint4 &b, const float *qtab,
+                                                const float *inv_tab, float den6, uint2 &codes, uint32_t &scode) {
+  uint32_t m = bf16x2_absmax(bf16x2_absmax(a.x, a.y), bf16x2_absmax(a.z, a.w));
+  m = bf16x2_absmax(m, bf16x2_absmax(bf16x2_absmax(b.x, b.y), bf16x2_absmax(b.z, b.w)));
+  const uint32_t u = max(m & 0x7FFFu, (m >> 16) & 0x7FFFu);  // |block max| as bf16 bits (signs meaningless)
+  const uint32_t e = u & 0x7F80u;
+  const float q = (e == 0u && u != 0u) ? __fdiv_rn(__uint_as_float(u << 16), den6)
+                                       : __fmul_rn(qtab[u & 0x7Fu], __uint_as_float(e << 16));
+  scode = cvt_e4m3_rn(q);
+  const float inv = inv_tab[scode];
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  float f[16];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) mul2_rn(bf16_lo(w[k]), bf16_hi(w[k]), inv, f[2 * k], f[2 * k + 1]);
+  codes.x = cvt_e2m1x8(f[0], f[1], f[2], f[3], f[4], f[5], f[6], f[7]);
+  codes.y = cvt_e2m1x8(f[8], f[9], f[10], f[11], f[12], f[13], f[14], f[15]);
+}
+
 // the reciprocal table of nvfp4_block for one outer scale (threads 0..127)
 __device__ __forceinline__ void fill_inv_table(float *tab, float sg) {
   if (threadIdx.x < 128) {
@@ -386,7 +413,9 @@ __global__ void __launch_bounds__(256) mxfp8_rowwise_kernel(const __grid_constan
 //   phase 2  per output row (= source column) and 32-token block: amax on
 //            packed halves, E8M0 scale, SR (bits drawn at the source index) or
 //            RN -> bytes
-//   phase 3  write 128-byte output rows and one 512-byte scale tile
+//            -> 128-byte output rows, stored from registers (a warp writes
+//            one whole row per store instruction)
+//   phase 3  write the 512-byte scale tiles
 // The value tile keeps 16-byte chunk c8 of row i at chunk c8 ^ ((i >> 2) & 7),
 // which makes both the row-wise fill and the 4-tokens-per-lane column reads
 // bank-conflict free.
@@ -422,7 +451,7 @@ struct MxTArgs {
 };
 
 constexpr int kTileSmem = 128 * 256;                 // 128 rows x 128 16-bit values, swizzled
-constexpr int kTileOutStride = 128;                  // output tile row stride (bytes)
+constexpr int kNvStage = 128 * 64 + 1024;            // NVFP4 source: staged codes and two scale tiles
 
 __device__ __forceinline__ int chunk_of(int i, int c8) { return c8 ^ ((i >> 2) & 7); }
 
@@ -447,6 +476,15 @@ __device__ __forceinline__ uint32_t habsmax2(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("max.xorsign.abs.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
+}
+// (fp32(a * m), fp32(b * m)) with one packed fp32x2 multiply (each lane
+// rounded to nearest even, exactly as two separate multiplies)
+__device__ __forceinline__ void mul2_rn(float a, float b, float m, float &ra, float &rb) {
+  uint64_t x, mm, d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a), "f"(b));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(mm) : "f"(m));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(x), "l"(mm));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(ra), "=f"(rb) : "l"(d));
 }
 __device__ __forceinline__ float f16_lo(uint32_t w) {
   float f;
@@ -549,8 +587,8 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant
   __shared__ __align__(16) uint8_t s_tsc[512];   // transposed scale tile
   __shared__ __align__(16) uint8_t s_rsc[512];   // row-wise scale tile
   __shared__ __align__(16) uint8_t s_nvsc[kMode == kSrcBf16ToNvfp4 ? 1024 : 16];  // NVFP4 scale tiles
-  uint8_t *s_out = smem;                                  // [128][128] output bytes
-  uint8_t *s_in = smem + 128 * kTileOutStride;            // [128][256 B] 16-bit values
+  uint8_t *s_stage = smem;                                           // NVFP4 source staging (kSrcNvfp4)
+  uint8_t *s_in = smem + (kMode == kSrcNvfp4 ? kNvStage : 0);         // [128][256 B] 16-bit values
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // the row-wise scale tile (bf16 source, always grouped) keeps zeros for rows
@@ -607,10 +645,9 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant
     }
   } else if (kMode == kSrcNvfp4) {
     // NVFP4: the window's codes [128 rows][64 bytes] and its two 512-byte
-    // scale tiles go through cp.async into the output tile (unused until
-    // phase 2), then each (row, 16-column block) unit is decoded to exact f16
-    // products e2m1 * e4m3
-    uint8_t *st_codes = s_out, *st_sc = s_out + 128 * 64;
+    // scale tiles go through cp.async into the staging area, then each (row,
+    // 16-column block) unit is decoded to exact f16 products e2m1 * e4m3
+    uint8_t *st_codes = s_stage, *st_sc = s_stage + 128 * 64;
     {
       const int64_t half_cols = A.cols >> 1;
 #pragma unroll
@@ -647,10 +684,15 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant
     // global memory, scales to the shared tile; the exact f16 products of the
     // new codes replace the unit's bf16 values in place for phase 2
     __shared__ float s_inv[128];
+    __shared__ float s_qt[128];
+    const float den6 = __fmul_rn(6.0f, sg);
+    // the block-scale table of nvfp4_block_tab applies while every quotient
+    // (1 + m / 128) / den6 is a normal fp32 number
+    const bool tab = !kRows && !k46 && den6 >= 0x1p-100f && den6 <= 0x1p100f;
     if (!kRows) fill_inv_table(s_inv, sg);
+    if (tab && tid >= 128) s_qt[tid - 128] = __fdiv_rn(__uint_as_float(0x3F800000u | ((uint32_t)(tid - 128) << 16)), den6);
     stage_bf16_tile(A, w, col0, s_in);
     __syncthreads();
-    const float den6 = __fmul_rn(6.0f, sg);
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int q = u * 256 + tid;
@@ -664,8 +706,10 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant
         nvfp4_block(va, vb, sgi, __fmul_rn(6.0f, sgi), c, sc);
       } else if (k46) {
         nvfp4_block46(va, vb, sg, c, sc);
+      } else if (tab) {
+        nvfp4_block_tab(va, vb, s_qt, s_inv, den6, c, sc);  // an all-zero (padding) block gives scale 0 and zero codes
       } else {
-        nvfp4_block(va, vb, sg, den6, c, sc, s_inv);  // an all-zero (padding) block gives scale 0 and zero codes
+        nvfp4_block(va, vb, sg, den6, c, sc, s_inv);
       }
       if (i < w.nvalid)
         *reinterpret_cast<uint2 *>(A.nv_codes_out + ((w.src_row0 + i) * A.cols + col0 + kb * 16) / 2) = c;
@@ -674,6 +718,23 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant
     }
   }
   __syncthreads();
+
+  // output addressing: transposed codes [source column][token], scale tile
+  int64_t out_base, out_stride, tile_idx;
+  if (A.grouped) {
+    out_base = col0 * A.out_stride + w.rp0;
+    out_stride = A.out_stride;
+    tile_idx = (col0 >> 7) * A.out_ka + (w.rp0 >> 7);
+  } else {
+    const int b = w.seg;
+    const int64_t wb = w.rp0 / 128 - (int64_t)b * A.wpb;
+    out_base = ((int64_t)b * A.cols + col0) * A.rows + wb * 128;
+    out_stride = A.rows;
+    const int64_t cpad = (A.cols + 127) & ~127LL;
+    tile_idx = (((int64_t)b * cpad + col0) >> 7) * A.out_ka + wb;
+  }
+  // a window without data (grouped padding past the last expert) stores no codes
+  uint8_t *const out_lane = w.nvalid > 0 ? A.out_codes + out_base + 4 * lane : nullptr;
 
   // ---- phase 2 --------------------------------------------------------------
   // warp handles groups of 8 output rows (source columns c8*8 .. c8*8+7);
@@ -752,7 +813,7 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant
         } else {
           packed = cvt_e4m3x2_rn(x[0], x[1]) | (cvt_e4m3x2_rn(x[2], x[3]) << 16);
         }
-        reinterpret_cast<uint32_t *>(s_out + c * kTileOutStride)[lane] = packed;
+        if (out_lane) *reinterpret_cast<uint32_t *>(out_lane + (int64_t)c * out_stride) = packed;
       }
       continue;
     }
@@ -814,34 +875,12 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant
       } else {
         packed = cvt_e4m3x2_rn(x[0], x[1]) | (cvt_e4m3x2_rn(x[2], x[3]) << 16);
       }
-      reinterpret_cast<uint32_t *>(s_out + c * kTileOutStride)[lane] = packed;
+      if (out_lane) *reinterpret_cast<uint32_t *>(out_lane + (int64_t)c * out_stride) = packed;
     }
   }
   __syncthreads();
 
   // ---- phase 3 --------------------------------------------------------------
-  int64_t out_base, out_stride, tile_idx;
-  if (A.grouped) {
-    out_base = col0 * A.out_stride + w.rp0;
-    out_stride = A.out_stride;
-    tile_idx = (col0 >> 7) * A.out_ka + (w.rp0 >> 7);
-  } else {
-    const int b = w.seg;
-    const int64_t wb = w.rp0 / 128 - (int64_t)b * A.wpb;
-    out_base = ((int64_t)b * A.cols + col0) * A.rows + wb * 128;
-    out_stride = A.rows;
-    const int64_t cpad = (A.cols + 127) & ~127LL;
-    tile_idx = (((int64_t)b * cpad + col0) >> 7) * A.out_ka + wb;
-  }
-  if (w.nvalid > 0) {
-#pragma unroll
-    for (int it = 0; it < 4; ++it) {
-      const int t = it * 256 + tid;
-      const int c = t >> 3, part = t & 7;
-      *reinterpret_cast<uint4 *>(A.out_codes + out_base + (int64_t)c * out_stride + part * 16) =
-          *reinterpret_cast<const uint4 *>(s_out + c * kTileOutStride + part * 16);
-    }
-  }
   if (tid < 32) {
     if (w.nvalid > 0 || A.grouped)
       reinterpret_cast<uint4 *>(A.out_scales + tile_idx * 512)[tid] = reinterpret_cast<const uint4 *>(s_tsc)[tid];
@@ -920,7 +959,7 @@ int launch_mxfp8_rowwise(const uint16_t *x, int64_t rows, int64_t cols, const in
   return launch_status(cudaGetLastError());
 }
 
-static size_t mx_t_smem(bool) { return 128 * kTileOutStride + (size_t)kTileSmem; }
+static size_t mx_t_smem(bool nvfp4_source) { return (nvfp4_source ? kNvStage : 0) + (size_t)kTileSmem; }
 
 int launch_mx_transpose_bf16(const uint16_t *x, int64_t rows, int64_t cols, const int32_t *groups, int E, int sr,
                              uint64_t seed, uint64_t off_t, uint64_t off_row, uint8_t *codes_t, uint8_t *scales_t,
@@ -988,7 +1027,7 @@ int launch_nvfp4_requant(const uint16_t *x, const float *sg, int64_t batch, int6
   } else {
     A.grouped = 0; A.wpb = (int)(rows / 128); A.out_ka = rows / 128; nwin = batch * A.wpb;
   }
-  const size_t sm = mx_t_smem(true);
+  const size_t sm = mx_t_smem(false);
   const int which = sg_rows ? 1 : (four_six ? 2 : 0);
   auto k = which == 1   ? mx_transpose_kernel<kSrcBf16ToNvfp4, true>
            : which == 2 ? mx_transpose_kernel<kSrcBf16ToNvfp4, false, true>
