@@ -365,6 +365,18 @@ int grouped_gemm_mxfp8_dw(const uint8_t *gt_codes, const uint8_t *gt_scales,
  * the same contraction with fp32 accumulation; summation order differs. */
 int nvfp4moe_set_gemm_kernel(int variant);
 
+/* Iteration limit of the grouped GEMMs' pipeline waits (the producer, MMA and
+ * epilogue roles waiting on one another's mbarriers), for testing the
+ * bounded-wait path: with a limit far below a healthy wait's length the
+ * waits run out, the kernel records NV_ERR_TIMEOUT in the status word, every
+ * role leaves its loop, and the CTA still waits (with a separate, fixed
+ * bound) for the copies and MMAs it has in flight before it frees its tensor
+ * memory and exits; the outputs are then incomplete.  spins: 1 .. 2^26, or 0
+ * for the default (2^26 polls, far longer than any healthy wait).  Applies to
+ * later GEMM launches from every host thread.  Returns NV_OK, or NV_ERR_ARG
+ * (setting unchanged) outside that range. */
+int nvfp4moe_set_gemm_wait_limit(int64_t spins);
+
 /* ---- Four Over Six: two candidate block scales for activations ------------------------
  * "Recipe details": the activation quantizer selects between two scale
  * factors per block (Four Over Six).  The pages do not state the selection
@@ -518,6 +530,18 @@ int nvfp4moe_get_device_status(nv_stream_t stream);
  * and nothing is launched, so no caller can keep a CTA spinning for long.
  * Returns the launch status. */
 int nvfp4moe_selftest_wait_timeout(int64_t spins, nv_stream_t stream);
+
+/* Diagnostic: the library's stochastic rounding to E4M3 on caller-given
+ * values and draws, exactly as the SR kernels apply it ("Re-quantization with
+ * stochastic rounding"; the rule and draw convention at the top of this
+ * header).  x: fp32 [4 n4] (16-byte aligned); draws: [n4], word i =
+ * U_a | U_b << 16, the 16-bit draws of the two pairs (4i, 4i+1) and
+ * (4i+2, 4i+3): values 4i and 4i+2 round with U_a and U_b, values 4i+1 and
+ * 4i+3 with bitrev16(U_a) and bitrev16(U_b); codes: u8 [4 n4] E4M3
+ * (saturating at 448).  Lets a test hold Blackwell's SR conversion to the
+ * rule draw by draw. */
+int nvfp4moe_sr_e4m3x4(const float *x, const uint32_t *draws, int64_t n4, uint8_t *codes,
+                       nv_stream_t stream);
 
 /* Static description of a status code (never NULL). */
 const char *nvfp4moe_status_string(int status);

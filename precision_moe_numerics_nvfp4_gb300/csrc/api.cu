@@ -91,6 +91,8 @@ const char *nvfp4moe_version(void) { return "nvfp4moe 0.1 (sm_103a)"; }
 
 int nvfp4moe_set_gemm_kernel(int variant) { return nvm::set_gemm_variant(variant); }
 
+int nvfp4moe_set_gemm_wait_limit(int64_t spins) { return nvm::set_gemm_wait_limit(spins); }
+
 const char *nvfp4moe_status_string(int s) {
   switch (s) {
     case NV_OK: return "ok";
@@ -121,6 +123,13 @@ int nvfp4moe_selftest_wait_timeout(int64_t spins, nv_stream_t stream) {
   int *st = status_ptr();
   if (!st) return NV_ERR_CUDA;
   return launch_wait_selftest(spins, st, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int nvfp4moe_sr_e4m3x4(const float *x, const uint32_t *draws, int64_t n4, uint8_t *codes, nv_stream_t stream) {
+  if (!x || !draws || !codes || n4 < 0) return NV_ERR_ARG;
+  if (!al16(x) || !al4(draws) || !al4(codes)) return NV_ERR_ALIGN;
+  if (n4 == 0) return NV_OK;
+  return launch_sr_e4m3x4(x, draws, n4, codes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int nvfp4_outer_scale(const void *x, int64_t batch, int64_t n, float *outer_scale_out, void *workspace,

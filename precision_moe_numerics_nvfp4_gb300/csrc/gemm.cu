@@ -168,7 +168,7 @@ struct Cfg {
   // one scale buffer per ring stage: a stage's buffer is rewritten only after
   // the producer has refilled that stage, i.e. after its previous MMAs retired
   static constexpr int TMEM_COLS = cpow2(ACC_COLS + STAGES * SF_COLS);
-  static constexpr int NBARS = 2 * STAGES + 2 * NACC;   // full, empty, acc_full[], acc_empty[]
+  static constexpr int NBARS = 2 * STAGES + 2 * NACC + 1;  // full, empty, acc_full[], acc_empty[], mma_done
   static constexpr uint32_t IDESC =
       (kFp4 ? ((1u << 7) | (1u << 10)) : (1u << 23)) | ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
   static size_t smem_bytes(int E) {
@@ -246,6 +246,14 @@ __device__ __forceinline__ void store_segment_coalesced(uint8_t *seg0, int64_t l
     p += ld_bytes;
   }
 }
+
+// Bound of the waits that let a CTA leave cleanly: the producer's wait for its
+// own copies to land and the MMA thread's wait for its own MMAs to finish.
+// They are separate from the pipeline waits' limit (GemmArgs::wait_limit,
+// which a test may shrink so that pipeline waits run out): the copies and
+// MMAs in flight complete by themselves, and no CTA may leave (or free its
+// tensor memory) before they have.
+constexpr uint64_t kDrainLimit = (uint64_t)1 << 26;
 
 // A bounded mbarrier wait that also gives up when another role of the CTA
 // has raised the abort flag.  A wait that runs out raises the flag and records
@@ -354,7 +362,9 @@ __global__ void __launch_bounds__(192, 2)
   if ((int)blockIdx.x >= num_tiles) return;  // uniform over the CTA
 
   uint64_t *full = bars, *empty = bars + STAGES, *acc_full = bars + 2 * STAGES, *acc_empty = acc_full + NACC;
+  uint64_t *mma_done = acc_empty + NACC;
   if (threadIdx.x == 0) {
+    mbar_init(smem_u32(mma_done), 1);
     for (int s = 0; s < STAGES; ++s) {
       // SwiGLU kind: the 32 producer lanes' arrivals (their scale copies
       // landed and made visible to the tensor core) come on top of the TMA
@@ -443,7 +453,7 @@ __global__ void __launch_bounds__(192, 2)
     // drain: every copy this thread issued has landed before the CTA leaves
     const uint32_t first = it > STAGES ? it - STAGES : 0;
     for (uint32_t k = first; k < it; ++k)
-      if (!mbar_wait(smem_u32(&full[k % STAGES]), (k / STAGES) & 1, A.wait_limit)) {
+      if (!mbar_wait(smem_u32(&full[k % STAGES]), (k / STAGES) & 1, kDrainLimit)) {
         record_error(A.status, NV_ERR_TIMEOUT);
         break;
       }
@@ -500,6 +510,10 @@ __global__ void __launch_bounds__(192, 2)
       }
       tc_commit(smem_u32(&acc_full[acc]));  // arrives once this tile's MMAs are done (at once if none)
     }
+    // every MMA and scale copy this thread issued has finished (also after an
+    // abort) before tensor memory can be freed
+    tc_commit(smem_u32(mma_done));
+    if (!mbar_wait(smem_u32(mma_done), 0, kDrainLimit)) record_error(A.status, NV_ERR_TIMEOUT);
   } else if (warp >= 2) {
     // ---- epilogue ----------------------------------------------------------------
     const int q = warp & 3;
@@ -678,6 +692,10 @@ __device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
       "h"((uint16_t)3)
       : "memory");
 }
+// completion of this thread's earlier pair MMAs, signalled on this CTA's barrier only
+__device__ __forceinline__ void tc_commit_pair_local(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
 __device__ __forceinline__ void tc_cp_sf_pair(uint32_t taddr, uint64_t sdesc) {
   asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
@@ -752,7 +770,7 @@ struct CfgPair {
   static constexpr int SF_COLS = CHUNKS * SF_CHUNK_COLS;  // per stage
   static constexpr int ACC_COLS = BN;
   static constexpr int TMEM_COLS = cpow2(ACC_COLS + STAGES * SF_COLS);
-  static constexpr int NBARS = 2 * STAGES + 2;          // full, empty, acc_full, acc_empty
+  static constexpr int NBARS = 2 * STAGES + 3;          // full, empty, acc_full, acc_empty, mma_done
   static constexpr int kEpiWarps = BN / 32;             // per lane quadrant: BN / 128 warps of 128 columns
   static constexpr int kThreads = 32 * (2 + kEpiWarps);
   static constexpr int kCtasPerSm = BN == 128 ? 2 : 1;
@@ -917,7 +935,9 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BN, CHUNKS>::kThreads,
   if (pair >= num_tiles) return;
 
   uint64_t *full = bars, *empty = bars + STAGES, *acc_full = bars + 2 * STAGES, *acc_empty = acc_full + 1;
+  uint64_t *mma_done = acc_empty + 1;
   if (threadIdx.x == 0) {
+    mbar_init(smem_u32(mma_done), 1);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
       mbar_init(smem_u32(&empty[s]), 1);
@@ -973,7 +993,7 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BN, CHUNKS>::kThreads,
     if (cta == 0) {  // the even CTA's barriers count both CTAs' bytes: wait for the last copies
       const uint32_t first = it > STAGES ? it - STAGES : 0;
       for (uint32_t k = first; k < it; ++k)
-        if (!mbar_wait(smem_u32(&full[k % STAGES]), (k / STAGES) & 1, A.wait_limit)) {
+        if (!mbar_wait(smem_u32(&full[k % STAGES]), (k / STAGES) & 1, kDrainLimit)) {
           record_error(A.status, NV_ERR_TIMEOUT);
           break;
         }
@@ -1029,6 +1049,11 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BN, CHUNKS>::kThreads,
       }
       tc_commit_pair(smem_u32(acc_full));  // both CTAs: this tile's accumulator is complete
     }
+    // every MMA and scale copy this thread issued (for both CTAs) has finished,
+    // also after an abort, before either CTA frees its tensor memory (both
+    // pass the cluster barrier below first)
+    tc_commit_pair_local(smem_u32(mma_done));
+    if (!mbar_wait(smem_u32(mma_done), 0, kDrainLimit)) record_error(A.status, NV_ERR_TIMEOUT);
   } else if (warp >= 2) {
     // ---- epilogue (both CTAs): BN / 32 warps, 128 columns each ------------------------
     const int q = warp & 3;
@@ -1235,6 +1260,16 @@ static int gemm_variant() {
   return g_variant;
 }
 
+// Limit of the GEMMs' pipeline waits (polls); the default lets a wait last
+// far longer than any healthy step takes.
+static volatile uint64_t g_wait_limit = (uint64_t)1 << 26;
+
+int set_gemm_wait_limit(int64_t spins) {
+  if (spins < 0 || spins > ((int64_t)1 << 26)) return NV_ERR_ARG;
+  g_wait_limit = spins == 0 ? ((uint64_t)1 << 26) : (uint64_t)spins;
+  return NV_OK;
+}
+
 int set_gemm_variant(int v) {
   if (v < 0 || v > 4) return NV_ERR_ARG;
   g_variant = v;
@@ -1248,7 +1283,7 @@ int launch_grouped_gemm(const GemmProblem &p, int *status, cudaStream_t s) {
   a.a_scales = p.a_scales; a.b_scales = p.b_scales; a.a_sg = p.a_sg; a.b_sg = p.b_sg;
   a.groups = p.groups; a.E = p.E; a.M_total = p.M_total; a.N = p.N; a.K = p.K;
   a.out = p.out; a.out_fp32 = p.out_fp32; a.status = status;
-  a.wait_limit = (uint64_t)1 << 26;
+  a.wait_limit = g_wait_limit;
   a.h = p.h; a.h_amax = reinterpret_cast<unsigned *>(p.h_amax); a.I = p.N / 2;
   a.a_sg_rows = p.a_sg_rows; a.h_amax_rows = p.h_amax_rows;
   a.s2f6_codes = p.s2f6_codes; a.s2f6_scales = p.s2f6_scales;

@@ -15,6 +15,8 @@ constexpr int64_t kMaxSelftestSpins = (int64_t)1 << 20;
 // argument and shape checks of nvfp4_quantize (api.cu); NV_OK or NV_ERR_*
 int quantize_check_args(const void *x, int64_t batch, int64_t rows, int64_t cols, const int32_t *group_offsets,
                         int32_t num_groups, const uint8_t *codes, const uint8_t *scales);
+// the library's SR conversion on caller-given values and draws (misc.cu)
+int launch_sr_e4m3x4(const float *x, const uint32_t *draws, int64_t n4, uint8_t *codes, cudaStream_t s);
 // p[0 .. n) = v (one small kernel)
 int launch_fill_f32(float *p, int64_t n, float v, cudaStream_t s);
 
@@ -75,5 +77,6 @@ struct GemmProblem {
 };
 int launch_grouped_gemm(const GemmProblem &p, int *status, cudaStream_t s);
 int set_gemm_variant(int v);  // 0 automatic, 1-3 forced (see nvfp4moe_set_gemm_kernel)
+int set_gemm_wait_limit(int64_t spins);  // 0: default (see nvfp4moe_set_gemm_wait_limit)
 
 }  // namespace nvm

@@ -78,6 +78,18 @@ __global__ void __launch_bounds__(256) fill_f32_kernel(float *__restrict__ p, in
     p[i] = v;
 }
 
+// Four fp32 values per thread through the library's stochastic rounding to
+// E4M3 (cvt_e4m3x4_sr with the draw convention of the SR kernels: word i holds
+// the draws U_a | U_b << 16 of values 4i .. 4i + 3)
+__global__ void __launch_bounds__(256) sr_e4m3x4_kernel(const float4 *__restrict__ x,
+                                                        const uint32_t *__restrict__ draws, int64_t n4,
+                                                        uint32_t *__restrict__ out) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
+    const float4 v = x[i];
+    out[i] = cvt_e4m3x4_sr(v.x, v.y, v.z, v.w, ~draws[i]);
+  }
+}
+
 static int grid_for(int64_t n) {
   int64_t g = (n + 255) / 256;
   if (g > 152 * 16) g = 152 * 16;
@@ -91,6 +103,12 @@ int launch_swiglu_fwd(const uint16_t *y13, int64_t M, int64_t I, uint16_t *h, cu
 
 int launch_swiglu_bwd(const uint16_t *dh, const uint16_t *y13, int64_t M, int64_t I, uint16_t *dy13, cudaStream_t s) {
   swiglu_bwd_kernel<<<grid_for(M * I / 8), 256, 0, s>>>(dh, y13, M, I, dy13);
+  return cudaGetLastError() == cudaSuccess ? NV_OK : NV_ERR_CUDA;
+}
+
+int launch_sr_e4m3x4(const float *x, const uint32_t *draws, int64_t n4, uint8_t *codes, cudaStream_t s) {
+  sr_e4m3x4_kernel<<<grid_for(n4), 256, 0, s>>>(reinterpret_cast<const float4 *>(x), draws, n4,
+                                               reinterpret_cast<uint32_t *>(codes));
   return cudaGetLastError() == cudaSuccess ? NV_OK : NV_ERR_CUDA;
 }
 

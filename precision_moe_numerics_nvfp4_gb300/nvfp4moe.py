@@ -61,6 +61,8 @@ _SIGS = {
     "nvfp4moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "nvfp4moe_version": (ctypes.c_char_p, []),
     "nvfp4moe_set_gemm_kernel": (ctypes.c_int, [ctypes.c_int]),
+    "nvfp4moe_set_gemm_wait_limit": (ctypes.c_int, [_I64]),
+    "nvfp4moe_sr_e4m3x4": (ctypes.c_int, [_P, _P, _I64, _P, _P]),
     "grouped_gemm_nvfp4_fwd_rht_s2f6": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I32, _I64, _I64, _I64,
                                                        ctypes.c_uint32, _P, _P, _P, _P]),
     "nvfp4_outer_scale": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _SZ, _P]),
@@ -177,6 +179,19 @@ def nvfp4moe_set_gemm_kernel(variant: int) -> None:
     GEMM_CTA_PAIR_N128 (256 x 128 pair tiles, two pairs per SM pair); a pair
     choice applies where the shape allows it."""
     _check("nvfp4moe_set_gemm_kernel", lib().nvfp4moe_set_gemm_kernel(int(variant)))
+
+
+def nvfp4moe_sr_e4m3x4(x, draws, n4, codes, stream=None):
+    """codes[4i + k] = the library's SR of x[4i + k] to E4M3 with the draws
+    draws[i] = U_a | U_b << 16 (see the header)."""
+    return _check("nvfp4moe_sr_e4m3x4", lib().nvfp4moe_sr_e4m3x4(_ptr(x), _ptr(draws), int(n4), _ptr(codes),
+                                                                  _stream(stream)))
+
+
+def nvfp4moe_set_gemm_wait_limit(spins: int) -> None:
+    """Iteration limit of the grouped GEMMs' pipeline waits (0: the default);
+    a tiny limit makes them run out (a test of the bounded-wait path)."""
+    _check("nvfp4moe_set_gemm_wait_limit", lib().nvfp4moe_set_gemm_wait_limit(int(spins)))
 
 
 # ---- the hot path -------------------------------------------------------------

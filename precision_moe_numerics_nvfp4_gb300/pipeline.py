@@ -34,6 +34,11 @@ def _u8(n, dev):
     return torch.empty(max(int(n), 16), dtype=U8, device=dev)
 
 
+def _empty(shape, dtype, dev):
+    """Every output buffer of the layers comes from here (and _u8)."""
+    return torch.empty(shape, dtype=dtype, device=dev)
+
+
 class NvTensor:
     """NVFP4 codes + block scales + outer scale(s) of a [batch][rows][cols]
     matrix (grouped layout when E is given)."""
@@ -42,7 +47,7 @@ class NvTensor:
         cb, sb = N.nvfp4_sizes(batch, rows, cols, E)
         self.batch, self.rows, self.cols, self.E = batch, rows, cols, E
         self.codes, self.scales = _u8(cb, dev), _u8(sb, dev)
-        self.sg = torch.empty(batch, dtype=F32, device=dev)
+        self.sg = _empty(batch, F32, dev)
         self.ws = _u8(N.nvfp4moe_quantize_workspace_bytes(batch, rows, cols), dev)
 
     def quantize(self, x, groups=None, stream=None, sg_in=None, four_six=False):
@@ -89,13 +94,13 @@ class SingleLinear:
         self.groups = torch.tensor([0, tokens], dtype=torch.int32, device=dev)
         self.xq = NvTensor(1, tokens, d_in, dev, E=1)
         self.wq = NvTensor(1, d_out, d_in, dev)
-        self.y = torch.empty((tokens, d_out), dtype=F32, device=dev)
+        self.y = _empty((tokens, d_out), F32, dev)
         self.xt = MxTransposed(tokens, d_in, dev, E=1)
         self.wt = MxTransposed(d_out, d_in, dev)
         self.g_row = MxRows(tokens, d_out, dev, E=1)
         self.gt = MxTransposed(tokens, d_out, dev, E=1)
-        self.dx = torch.empty((tokens, d_in), dtype=F32, device=dev)
-        self.dw = torch.empty((d_out, d_in), dtype=F32, device=dev)
+        self.dx = _empty((tokens, d_in), F32, dev)
+        self.dw = _empty((d_out, d_in), F32, dev)
 
     def enqueue(self, x, w, g, seed=0, stream=None):
         T, din, dout, go = self.T, self.din, self.dout, self.groups
@@ -164,12 +169,12 @@ class MoELayer:
         self.xq = NvTensor(1, M, d_model, dev, E=E)
         self.w13q = NvTensor(E, I2, d_model, dev)
         self.w2q = NvTensor(E, d_model, d_ff, dev)
-        self.y13 = torch.empty((M, I2), dtype=BF16, device=dev)
-        self.h = torch.empty((M, d_ff), dtype=BF16, device=dev)
+        self.y13 = _empty((M, I2), BF16, dev)
+        self.h = _empty((M, d_ff), BF16, dev)
         self.hq = NvTensor(1, M, d_ff, dev, E=E)
-        self.y2 = torch.empty((M, d_model), dtype=BF16, device=dev)
+        self.y2 = _empty((M, d_model), BF16, dev)
         self.fuse_swiglu = fuse_swiglu and d_ff % 128 == 0
-        self.h_sg = torch.empty(1, dtype=F32, device=dev)  # outer scale of h from the fused epilogue
+        self.h_sg = _empty(1, F32, dev)  # outer scale of h from the fused epilogue
         self.per_token = per_token
         self.four_six = four_over_six
         # overlap_amax: the per-tensor amax passes of w13, w2 and x (HBM-bound)
@@ -179,8 +184,8 @@ class MoELayer:
         # 9.05 ms per step, so off by default)
         self.side = torch.cuda.Stream(dev) if overlap_amax and not per_token else None
         if per_token:
-            self.x_sg_rows = torch.empty(M, dtype=F32, device=dev)
-            self.h_sg_rows = torch.empty(M, dtype=F32, device=dev)
+            self.x_sg_rows = _empty(M, F32, dev)
+            self.h_sg_rows = _empty(M, F32, dev)
         self.fuse_requant = fuse_requant and backward
         self._requant_seed = None  # seed of the operands the last forward re-quantized
         if not backward:  # forward-only use (sampling): no backward buffers
@@ -192,13 +197,13 @@ class MoELayer:
         self.w2t = MxTransposed(d_model, d_ff, dev, batch=E)
         self.g2_row = MxRows(M, d_model, dev, E=E)
         self.g2t = MxTransposed(M, d_model, dev, E=E)
-        self.dh = torch.empty((M, d_ff), dtype=BF16, device=dev)
-        self.dy13 = torch.empty((M, I2), dtype=BF16, device=dev)
+        self.dh = _empty((M, d_ff), BF16, dev)
+        self.dy13 = _empty((M, I2), BF16, dev)
         self.dy13_row = MxRows(M, I2, dev, E=E)
         self.dy13t = MxTransposed(M, I2, dev, E=E)
-        self.dx = torch.empty((M, d_model), dtype=BF16, device=dev)
-        self.dw2 = torch.empty((E, d_model, d_ff), dtype=F32, device=dev)
-        self.dw13 = torch.empty((E, I2, d_model), dtype=F32, device=dev)
+        self.dx = _empty((M, d_model), BF16, dev)
+        self.dw2 = _empty((E, d_model, d_ff), F32, dev)
+        self.dw13 = _empty((E, I2, d_model), F32, dev)
 
     # GEMM FLOPs of one forward (2 GEMMs) and one backward (4 GEMMs)
     def flops(self):
@@ -402,7 +407,7 @@ class HostStaged:
         self.layer = layer
         self.x = [torch.empty((M, d), dtype=BF16, device=dev) for _ in range(2)]
         self.g2 = [torch.empty((M, d), dtype=BF16, device=dev) for _ in range(2)]
-        self.dx = [torch.empty((M, d), dtype=BF16, device=dev) for _ in range(2)]
+        self.dx = [_empty((M, d), BF16, dev) for _ in range(2)]
         self.s_in = torch.cuda.Stream(dev)
         self.s_out = torch.cuda.Stream(dev)
         self.x_read = [None, None]      # forward of the slot's last step finished (x free)

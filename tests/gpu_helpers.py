@@ -12,18 +12,74 @@ from precision_moe_numerics_nvfp4_gb300 import nvfp4moe as N
 
 CANARY = 0xA5
 
+# Guard regions: every device buffer a GPU test hands to the library as an
+# output (and the layers' own buffers, see conftest) is the front of a larger
+# allocation whose last GUARD bytes hold GUARD_BYTE.  A write past the end of
+# the buffer changes them; check_guards() (run by check_status() after every
+# call and at the end of every GPU test) finds it.  This stands in for a
+# memory checker, which is not available here.
+GUARD = 4096
+GUARD_BYTE = 0xA5
+_GUARDED: list = []  # (allocation, bytes in front of the guard)
+
 
 def dev():
     return torch.device("cuda")
 
 
+def guarded_bytes(nbytes: int, value=None) -> torch.Tensor:
+    """uint8 device buffer of `nbytes` (filled with `value` when given)
+    followed by the guard region."""
+    n = max(int(nbytes), 1)
+    base = torch.empty(n + GUARD, dtype=torch.uint8, device=dev())
+    base[n:] = GUARD_BYTE
+    if value is not None:
+        base[:n] = value
+    _GUARDED.append((base, n))
+    return base[:n]
+
+
+def _shape(size):
+    return tuple(size) if isinstance(size, (tuple, list, torch.Size)) else (int(size),)
+
+
+def gempty(size, dtype=torch.float32, device=None):
+    """torch.empty with a guard region after the tensor (CUDA only)."""
+    if device is not None and torch.device(device).type != "cuda":
+        return torch.empty(size, dtype=dtype, device=device)
+    shape = _shape(size)
+    numel = 1
+    for d in shape:
+        numel *= int(d)
+    nbytes = numel * torch.empty((), dtype=dtype).element_size()
+    return guarded_bytes(max(nbytes, 1))[:nbytes].view(dtype).view(shape)
+
+
+def gfull(size, fill_value, dtype=torch.float32, device=None):
+    """torch.full with a guard region after the tensor (CUDA only)."""
+    t = gempty(size, dtype=dtype, device=device)
+    t.fill_(fill_value)
+    return t
+
+
+def check_guards():
+    for base, n in _GUARDED:
+        bad = int((base[n:] != GUARD_BYTE).sum())
+        assert bad == 0, f"{bad} guard bytes past the end of a {n}-byte output buffer were overwritten"
+
+
+def clear_guards():
+    _GUARDED.clear()
+
+
 def filled(nbytes: int, value: int = CANARY):
-    return torch.full((max(int(nbytes), 1),), value, dtype=torch.uint8, device=dev())
+    return guarded_bytes(nbytes, value)
 
 
 def check_status():
     s = N.nvfp4moe_get_device_status()
     assert s == 0, f"device status {s} ({N.status_string(s)})"
+    check_guards()
 
 
 def bf16_f32(t: torch.Tensor) -> np.ndarray:

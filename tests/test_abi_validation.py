@@ -118,3 +118,10 @@ def test_noalloc_reports_argument_errors_like_the_workspace_entry_point(L):
     assert qn(A, *big, NULL, 0, NULL, A, NULL, A, S) == N.NV_ERR_ARG      # no codes
     assert qn(A, *big, NULL, 0, NULL, A, A, A, S) == N.NV_ERR_WORKSPACE   # valid, too large
     assert qn(A, 1, 0, 256, NULL, 0, NULL, A, A, A, S) == N.NV_OK         # empty: nothing launched
+
+
+def test_gemm_wait_limit_range(L):
+    f = L.nvfp4moe_set_gemm_wait_limit
+    assert f(-1) == N.NV_ERR_ARG
+    assert f((1 << 26) + 1) == N.NV_ERR_ARG
+    assert f(0) == N.NV_OK          # the default

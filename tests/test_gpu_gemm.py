@@ -15,7 +15,7 @@ from oracle import nvfp4 as NV
 from precision_moe_numerics_nvfp4_gb300 import nvfp4moe as N
 from precision_moe_numerics_nvfp4_gb300 import workloads as W
 from precision_moe_numerics_nvfp4_gb300.pipeline import MxRows, MxTransposed, NvTensor, SingleLinear
-from tests.gpu_helpers import bf16_f32, check_status, dev, unpack_gpu_nvfp4
+from tests.gpu_helpers import bf16_f32, check_status, dev, gempty, gfull, unpack_gpu_nvfp4
 
 pytestmark = pytest.mark.gpu
 
@@ -48,7 +48,7 @@ def _fwd(sizes, N_, K, out_fp32=True, seed=0):
     xq, wq = NvTensor(1, M, K, dev(), E=E), NvTensor(E, N_, K, dev())
     xq.quantize(x, go)
     wq.quantize(w)
-    y = torch.full((M, N_), float("nan"), dtype=torch.float32 if out_fp32 else torch.bfloat16, device=dev())
+    y = gfull((M, N_), float("nan"), dtype=torch.float32 if out_fp32 else torch.bfloat16, device=dev())
     N.grouped_gemm_nvfp4_fwd(None, xq.sg, xq.codes, xq.scales, wq.codes, wq.scales, wq.sg, go, E, M, N_, K, y,
                              N.NV_OUT_FP32 if out_fp32 else N.NV_OUT_BF16)
     check_status()
@@ -114,8 +114,8 @@ def _mx_operands(sizes, Nd, K, seed):
                                        ([5, 0, 295, 130], 256, 512), ([0, 700, 1, 0, 129], 512, 768)])
 def test_mxfp8_dgrad_and_wgrad_within_bound(sizes, Nd, K, gemm_kernel):
     go, o, M, E, gr, gt, wt, xt = _mx_operands(sizes, Nd, K, seed=len(sizes) + Nd)
-    dx = torch.full((M, K), float("nan"), dtype=torch.float32, device=dev())
-    dw = torch.full((E, Nd, K), float("nan"), dtype=torch.float32, device=dev())
+    dx = gfull((M, K), float("nan"), dtype=torch.float32, device=dev())
+    dw = gfull((E, Nd, K), float("nan"), dtype=torch.float32, device=dev())
     N.grouped_gemm_mxfp8_dx(gr.codes, gr.scales, wt.codes, wt.scales, go, E, M, Nd, K, dx, N.NV_OUT_FP32)
     N.grouped_gemm_mxfp8_dw(gt.codes, gt.scales, xt.codes, xt.scales, go, E, M, Nd, K, dw)
     check_status()
@@ -174,11 +174,11 @@ def test_fwd_from_bf16_activations_equals_quantize_then_gemm(given_scale):
     sg_in = torch.tensor([0.75], dtype=torch.float32, device="cuda") if given_scale else None
     xq = NvTensor(1, M, K, torch.device("cuda"), E=E)
     xq.quantize(x, go, sg_in=sg_in)
-    y_ref = torch.empty((M, N_), dtype=torch.float32, device="cuda")
+    y_ref = gempty((M, N_), dtype=torch.float32, device="cuda")
     N.grouped_gemm_nvfp4_fwd(None, xq.sg, xq.codes, xq.scales, wq.codes, wq.scales, wq.sg, go, E, M, N_, K, y_ref,
                              N.NV_OUT_FP32)
-    ws = torch.empty(N.nvfp4moe_fwd_workspace_bytes(M, K, E), dtype=torch.uint8, device="cuda")
-    y = torch.full((M, N_), 7.0, dtype=torch.float32, device="cuda")
+    ws = gempty(N.nvfp4moe_fwd_workspace_bytes(M, K, E), dtype=torch.uint8, device="cuda")
+    y = gfull((M, N_), 7.0, dtype=torch.float32, device="cuda")
     N.grouped_gemm_nvfp4_fwd(x, sg_in, None, None, wq.codes, wq.scales, wq.sg, go, E, M, N_, K, y, N.NV_OUT_FP32,
                              workspace=ws)
     assert N.nvfp4moe_get_device_status() == 0

@@ -17,7 +17,7 @@ from oracle import nvfp4 as NV
 from oracle import requant as RQ
 from precision_moe_numerics_nvfp4_gb300 import nvfp4moe as N
 from precision_moe_numerics_nvfp4_gb300.pipeline import MxTransposed, NvTensor
-from tests.gpu_helpers import bf16_f32, check_status, dev, filled, unpack_gpu_nvfp4
+from tests.gpu_helpers import bf16_f32, check_status, dev, filled, gempty, gfull, unpack_gpu_nvfp4
 
 pytestmark = pytest.mark.gpu
 
@@ -25,7 +25,7 @@ pytestmark = pytest.mark.gpu
 def _x(rows, cols, seed):
     g = torch.Generator(device="cuda").manual_seed(seed)
     # tokens of very different magnitudes: what per-token scales are for
-    mag = torch.exp(torch.empty((rows, 1), device="cuda").uniform_(-8, 8, generator=g))
+    mag = torch.exp(gempty((rows, 1), device="cuda").uniform_(-8, 8, generator=g))
     x = torch.randn((rows, cols), generator=g, device="cuda") * mag
     if rows > 4:
         x[2] = 0.0                      # an all-zero token
@@ -49,7 +49,7 @@ def _gpu_rows(x, rows, cols, go, E):
     t = NvTensor(1, rows, cols, dev(), E=E)
     t.codes.fill_(0xA5)
     t.scales.fill_(0xA5)
-    sg = torch.full((rows,), -1.0, dtype=torch.float32, device=dev())
+    sg = gfull((rows,), -1.0, dtype=torch.float32, device=dev())
     N.nvfp4_quantize_rows(x, rows, cols, go, None, sg, t.codes, t.scales)
     check_status()
     return t, sg
@@ -113,7 +113,7 @@ def test_quantize_requant_rows_fused_separate_and_oracle(sizes, cols):
     mb = MxTransposed(rows, cols, dev(), E=E)
     for t in (b.codes, b.scales, mb.codes, mb.scales):
         t.fill_(0x5A)
-    sgb = torch.empty(rows, dtype=torch.float32, device=dev())
+    sgb = gempty(rows, dtype=torch.float32, device=dev())
     N.nvfp4_quantize_requant_rows(x, rows, cols, go, None, sgb, b.codes, b.scales, 7, 2, mb.codes, mb.scales)
     check_status()
     assert torch.equal(sga, sgb) and torch.equal(a.codes, b.codes) and torch.equal(a.scales, b.scales)
@@ -141,7 +141,7 @@ def test_fwd_gemm_rows_within_bound(sizes, N_, K):
     x = _x(M, K, seed=M + K)
     xq, sgx = _gpu_rows(x, M, K, go, E)
     wq = _weights(E, N_, K, seed=E)
-    y = torch.empty((M, N_), dtype=torch.float32, device=dev())
+    y = gempty((M, N_), dtype=torch.float32, device=dev())
     N.grouped_gemm_nvfp4_fwd_rows(sgx, xq.codes, xq.scales, wq.codes, wq.scales, wq.sg, go, E, M, N_, K, y,
                                   N.NV_OUT_FP32)
     check_status()
@@ -161,9 +161,9 @@ def test_swiglu_rows_epilogue():
     x = _x(M, K, seed=77)
     xq, sgx = _gpu_rows(x, M, K, go, E)
     wq = _weights(E, 2 * I, K, seed=8)
-    y13 = torch.empty((M, 2 * I), dtype=torch.bfloat16, device=dev())
-    h = torch.empty((M, I), dtype=torch.bfloat16, device=dev())
-    hsg = torch.full((M,), -1.0, dtype=torch.float32, device=dev())
+    y13 = gempty((M, 2 * I), dtype=torch.bfloat16, device=dev())
+    h = gempty((M, I), dtype=torch.bfloat16, device=dev())
+    hsg = gfull((M,), -1.0, dtype=torch.float32, device=dev())
     N.grouped_gemm_nvfp4_fwd_swiglu_rows(sgx, xq.codes, xq.scales, wq.codes, wq.scales, wq.sg, go, E, M, I, K,
                                          y13, h, hsg)
     y_ref = torch.empty_like(y13)
@@ -201,7 +201,7 @@ def test_full_size_sampled_rows():
     rows, cols, E = x.shape[0], x.shape[1], go.numel() - 1
     t = NvTensor(1, rows, cols, dev(), E=E)
     mx = MxTransposed(rows, cols, dev(), E=E)
-    sg = torch.empty(rows, dtype=torch.float32, device=dev())
+    sg = gempty(rows, dtype=torch.float32, device=dev())
     N.nvfp4_quantize_requant_rows(x, rows, cols, go, None, sg, t.codes, t.scales, 3, 2, mx.codes, mx.scales)
     check_status()
     pick = torch.randint(0, rows, (64,), generator=torch.Generator().manual_seed(1))

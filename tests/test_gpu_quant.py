@@ -15,7 +15,7 @@ from oracle import requant as RQ
 from oracle import swiglu as SW
 from precision_moe_numerics_nvfp4_gb300 import nvfp4moe as N
 from precision_moe_numerics_nvfp4_gb300 import workloads as W
-from tests.gpu_helpers import (bf16_f32, check_status, dev, filled, gpu_nvfp4, oracle_nvfp4,
+from tests.gpu_helpers import (bf16_f32, check_status, dev, filled, gempty, gfull, gpu_nvfp4, oracle_nvfp4,
                                unpack_gpu_nvfp4)
 
 pytestmark = pytest.mark.gpu
@@ -97,7 +97,7 @@ def test_nvfp4_cvt_rounding_sweep():
     ok = torch.isfinite(vals) & (vals.abs() <= 2688.0)
     vals = vals[ok]
     vals = vals[: (vals.numel() // 16) * 16].reshape(-1, 16).to(torch.bfloat16).to(dev())
-    sg = torch.full((1,), 1.0, dtype=torch.float32, device=dev())
+    sg = gfull((1,), 1.0, dtype=torch.float32, device=dev())
     r, c = vals.shape
     codes, scales, _ = gpu_nvfp4(vals.contiguous(), 1, r, c, sg_in=sg)
     ec, es, _ = oracle_nvfp4(bf16_f32(vals), 1, r, c, sg_in=[1.0])
@@ -237,7 +237,7 @@ def _nvfp4_on_gpu(x, batch, rows, cols, groups=None):
     E = None if groups is None else groups.numel() - 1
     cb, sb = N.nvfp4_sizes(batch, rows, cols, E)
     codes, scales = filled(cb), filled(sb)
-    sg = torch.empty(batch, dtype=torch.float32, device=dev())
+    sg = gempty(batch, dtype=torch.float32, device=dev())
     ws = filled(N.nvfp4moe_quantize_workspace_bytes(batch, rows, cols), 0)
     N.nvfp4_quantize(x, batch, rows, cols, groups, None, sg, codes, scales, ws)
     check_status()
@@ -292,8 +292,8 @@ def test_swiglu_forward_backward():
     M, I = 300, 1536
     y13 = _tensor((M, 2 * I), seed=5, kind="n", scale=1.0)
     dh = _tensor((M, I), seed=6, kind="n", scale=1e-3)
-    h = torch.empty((M, I), dtype=torch.bfloat16, device=dev())
-    d = torch.empty((M, 2 * I), dtype=torch.bfloat16, device=dev())
+    h = gempty((M, I), dtype=torch.bfloat16, device=dev())
+    d = gempty((M, 2 * I), dtype=torch.bfloat16, device=dev())
     N.nvfp4moe_swiglu_fwd(y13, M, I, h)
     N.nvfp4moe_swiglu_bwd(dh, y13, M, I, d)
     check_status()

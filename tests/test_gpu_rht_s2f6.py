@@ -9,7 +9,7 @@ import torch
 
 from oracle import rht as R
 from precision_moe_numerics_nvfp4_gb300 import nvfp4moe as N
-from tests.gpu_helpers import bf16_f32, check_status, dev
+from tests.gpu_helpers import bf16_f32, check_status, dev, gempty, gfull
 
 pytestmark = pytest.mark.gpu
 
@@ -37,11 +37,11 @@ def _x(rows, cols, seed):
                                             (129, 4096, 0x12345678), (5, 96, 0x80000001)])
 def test_quantize_and_inverse_match_oracle(rows, cols, mask):
     x = _x(rows, cols, seed=rows + cols)
-    codes = torch.full((rows, cols), 0x55, dtype=torch.int8, device=dev())
-    scales = torch.full((rows, cols // 32), 0xAA, dtype=torch.uint8, device=dev())
+    codes = gfull((rows, cols), 0x55, dtype=torch.int8, device=dev())
+    scales = gfull((rows, cols // 32), 0xAA, dtype=torch.uint8, device=dev())
     N.rht32_s2f6_quantize(x, rows, cols, mask, codes, scales)
-    y32 = torch.empty((rows, cols), dtype=torch.float32, device=dev())
-    y16 = torch.empty((rows, cols), dtype=torch.bfloat16, device=dev())
+    y32 = gempty((rows, cols), dtype=torch.float32, device=dev())
+    y16 = gempty((rows, cols), dtype=torch.bfloat16, device=dev())
     N.s2f6_dequantize_rht32_inverse(codes, scales, rows, cols, mask, y32, N.NV_OUT_FP32)
     N.s2f6_dequantize_rht32_inverse(codes, scales, rows, cols, mask, y16, N.NV_OUT_BF16)
     check_status()
@@ -77,9 +77,9 @@ def test_rejects_bad_arguments():
 def test_misaligned_pointers_are_rejected_and_nothing_is_written():
     rows, cols = 4, 64
     xb = torch.zeros(rows * cols + 16, dtype=torch.bfloat16, device=dev())
-    cb = torch.full((rows * cols + 32,), 0x55, dtype=torch.int8, device=dev())
-    s = torch.full((rows, cols // 32), 0xAA, dtype=torch.uint8, device=dev())
-    yb = torch.full((rows * cols + 16,), 7.0, dtype=torch.float32, device=dev())
+    cb = gfull((rows * cols + 32,), 0x55, dtype=torch.int8, device=dev())
+    s = gfull((rows, cols // 32), 0xAA, dtype=torch.uint8, device=dev())
+    yb = gfull((rows * cols + 16,), 7.0, dtype=torch.float32, device=dev())
     with pytest.raises(N.NvError):
         N.rht32_s2f6_quantize(xb[8:8 + rows * cols], rows, cols, 0, cb[:rows * cols], s)   # x 16-byte aligned
     with pytest.raises(N.NvError):
@@ -92,8 +92,8 @@ def test_misaligned_pointers_are_rejected_and_nothing_is_written():
 
 
 def test_empty_inputs_are_no_ops():
-    c = torch.full((64,), 0x55, dtype=torch.int8, device=dev())
-    s = torch.full((2,), 0xAA, dtype=torch.uint8, device=dev())
+    c = gfull((64,), 0x55, dtype=torch.int8, device=dev())
+    s = gfull((2,), 0xAA, dtype=torch.uint8, device=dev())
     x = torch.zeros((64,), dtype=torch.bfloat16, device=dev())
     N.rht32_s2f6_quantize(x, 0, 64, 1, c, s)
     N.s2f6_dequantize_rht32_inverse(c, s, 2, 0, 1, x, N.NV_OUT_BF16)
@@ -109,10 +109,10 @@ def test_full_size_sampled_rows_match_oracle():
     rows, cols, mask = 131072, 4096, 0x6A09E667
     g = torch.Generator(device="cuda").manual_seed(11)
     x = (torch.randn((rows, cols), generator=g, device="cuda") * 2.0).to(torch.bfloat16)
-    codes = torch.empty((rows, cols), dtype=torch.int8, device=dev())
-    scales = torch.empty((rows, cols // 32), dtype=torch.uint8, device=dev())
+    codes = gempty((rows, cols), dtype=torch.int8, device=dev())
+    scales = gempty((rows, cols // 32), dtype=torch.uint8, device=dev())
     N.rht32_s2f6_quantize(x, rows, cols, mask, codes, scales)
-    y = torch.empty((rows, cols), dtype=torch.bfloat16, device=dev())
+    y = gempty((rows, cols), dtype=torch.bfloat16, device=dev())
     N.s2f6_dequantize_rht32_inverse(codes, scales, rows, cols, mask, y, N.NV_OUT_BF16)
     check_status()
     pick = torch.cat([torch.tensor([0, rows - 1]), torch.randint(1, rows - 1, (46,), generator=torch.Generator().manual_seed(5))])
@@ -141,15 +141,15 @@ def _w2_operands(sizes, N_, K, seed):
 
 def _fused_vs_separate(sizes, N_, K, mask, with_y):
     go, M, E, hq, wq = _w2_operands(sizes, N_, K, seed=M_seed(sizes))
-    y_ref = torch.empty((M, N_), dtype=torch.bfloat16, device=dev())
+    y_ref = gempty((M, N_), dtype=torch.bfloat16, device=dev())
     N.grouped_gemm_nvfp4_fwd(None, hq.sg, hq.codes, hq.scales, wq.codes, wq.scales, wq.sg, go, E, M, N_, K, y_ref,
                              N.NV_OUT_BF16)
-    c_ref = torch.empty((M, N_), dtype=torch.int8, device=dev())
-    s_ref = torch.empty((M, N_ // 32), dtype=torch.uint8, device=dev())
+    c_ref = gempty((M, N_), dtype=torch.int8, device=dev())
+    s_ref = gempty((M, N_ // 32), dtype=torch.uint8, device=dev())
     N.rht32_s2f6_quantize(y_ref, M, N_, mask, c_ref, s_ref)
-    y = torch.full((M, N_), 7.0, dtype=torch.bfloat16, device=dev()) if with_y else None
-    c = torch.full((M, N_), 0x55, dtype=torch.int8, device=dev())
-    s = torch.full((M, N_ // 32), 0xAA, dtype=torch.uint8, device=dev())
+    y = gfull((M, N_), 7.0, dtype=torch.bfloat16, device=dev()) if with_y else None
+    c = gfull((M, N_), 0x55, dtype=torch.int8, device=dev())
+    s = gfull((M, N_ // 32), 0xAA, dtype=torch.uint8, device=dev())
     N.grouped_gemm_nvfp4_fwd_rht_s2f6(hq.sg, hq.codes, hq.scales, wq.codes, wq.scales, wq.sg, go, E, M, N_, K, mask,
                                       y, c, s)
     check_status()
