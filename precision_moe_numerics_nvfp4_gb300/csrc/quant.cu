@@ -799,7 +799,7 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const int c = c8 * 8 + k;
-        const float m2 = __shfl_sync(0xFFFFFFFFu, mult_own, (lane & ~7) | k);
+        const float m2 = __shfl_sync(0xFFFFFFFFu, mult_own, k, 8);  // from lane 8 * (lane / 8) + k
         const int p = k >> 1, h = k & 1;
         float x[4];
 #pragma unroll
@@ -854,12 +854,14 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const int c = c8 * 8 + k;
-      const float m2 = __shfl_sync(0xFFFFFFFFu, m2_own, (lane & ~7) | k);
+      const float m2 = __shfl_sync(0xFFFFFFFFu, m2_own, k, 8);  // from lane 8 * (lane / 8) + k
       const int p = k >> 1, h = k & 1;
       float x[4];
       if (kNvfp4) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) x[j] = __fmul_rn(h ? f16_hi(v[j][p]) : f16_lo(v[j][p]), m2);
+        for (int j = 0; j < 4; j += 2)
+          mul2_rn(h ? f16_hi(v[j][p]) : f16_lo(v[j][p]), h ? f16_hi(v[j + 1][p]) : f16_lo(v[j + 1][p]), m2, x[j],
+                  x[j + 1]);
       } else {  // m2 is a power of two: one mixed-precision FMA per value
         const uint16_t mb = pow2_bf16_bits(m2);
 #pragma unroll
