@@ -1122,8 +1122,9 @@ def run_decode(args):
 
     N.lib()
     peaks = load_peaks()
-    m = W.decode("cuda")
-    M, D, I, E = m.x_perm.shape[0], 7168, 2048, 128
+    E = args.decode_experts  # fewer experts (same per-expert shapes, ~16 rows each) for profiling
+    m = W.decode("cuda", tokens=256 * E // 128, experts=E)
+    M, D, I = m.x_perm.shape[0], 7168, 2048
     layer = MoELayer(M, D, I, E, backward=False)
     layer.quantize_weights(m.w13, m.w2)
     params = E * (2 * I * D + D * I)
@@ -1168,6 +1169,8 @@ def main(argv=None):
     ap.add_argument("--workload", choices=["moe", "quant_sweep", "gemm", "decode", "rht_s2f6"], default="moe")
     ap.add_argument("--gemm-kind", choices=["fwd", "swiglu", "dx", "dw"], default="fwd")
     ap.add_argument("--graph", action="store_true", help="decode workload: replay the forward as a CUDA graph")
+    ap.add_argument("--decode-experts", type=int, default=128,
+                    help="decode workload: experts (tokens scale with them, ~16 rows per expert); for profiling")
     ap.add_argument("--four-over-six", action="store_true",
                     help="moe workload: the Four Over Six block rule for the activations x and h")
     ap.add_argument("--per-token", action="store_true",
