@@ -218,9 +218,10 @@ class EventLog:
             s = torch.cuda.current_stream()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(s)
-        fn(*a, **k)
+        r = fn(*a, **k)
         e1.record(s)
         self.rec.append((name, e0, e1))
+        return r
 
     def per_name_ms(self):
         out = {}
@@ -239,16 +240,18 @@ def build_step(layer, m, log: EventLog | None):
             return fn
         return lambda *a, **k: log.call(name, fn, *a, **k)
 
-    class Proxy:  # the layer's calls go through the event log
+    class Proxy:  # the layer's launching calls go through the event log (size queries do not)
         def __getattr__(self, n):
             f = getattr(N, n)
-            return wrap(n, f) if callable(f) and not n.startswith("_") else f
+            return wrap(n, f) if callable(f) and not n.startswith("_") and not n.endswith("_bytes") else f
 
-    def step(x, g2):
+    rows = m.rows if layer.gathers_rows else None
+
+    def step(x, g2):  # x: the tokens (the x quantization gathers the routed rows), else the routed rows
         saved = PL.N
         PL.N = Proxy()
         try:
-            layer.step(x, m.w13, m.w2, g2, m.group_offsets, seed=3)
+            layer.step(x, m.w13, m.w2, g2, m.group_offsets, seed=3, x_rows=rows)
         finally:
             PL.N = saved
 
@@ -259,6 +262,7 @@ def kernel_units(layer, m):
     """Algorithmic bytes (quantizers) and FLOPs (GEMMs) per call, by call name
     and argument pattern, in the order MoELayer.step issues them."""
     M, d, I, E = layer.M, layer.d, layer.I, layer.E
+    T = m.x.shape[0]  # tokens
     fl13 = 2.0 * M * 2 * I * d
     fl2 = 2.0 * M * d * I
     # quantize (+ requant) of h: no amax pass when the w13 epilogue produced its outer scale
@@ -313,9 +317,11 @@ def kernel_units(layer, m):
     return {
         # a call = the amax pass (2 B/elem) + the quantize pass (2 + 0.5 + 1/16 B/elem)
         "nvfp4_quantize": [(E * 2 * I * d, 4.5625), (E * d * I, 4.5625), (M * d, 4.5625), (M * I, 2.5625 + h_amax)],
-        # amax pass (2) + one pass reading bf16 (2) and writing NVFP4 (0.5 + 1/16) and MXFP8 (1 + 1/32)
-        "nvfp4_quantize_requant": [(E * 2 * I * d, 5.59375), (E * d * I, 5.59375), (M * d, 5.59375),
-                                   (M * I, 3.59375 + h_amax)],
+        # amax pass (2) + one pass reading bf16 (2) and writing NVFP4 (0.5 + 1/16) and MXFP8 (1 + 1/32);
+        # x: the routed rows gathered from the tokens (the quantize pass, 3.59375 B per routed-row
+        # element) after an amax pass reading each token once (2 B per token element)
+        "nvfp4_quantize_requant": [(E * 2 * I * d, 5.59375), (E * d * I, 5.59375), (M * I, 3.59375 + h_amax)],
+        "nvfp4_quantize_requant_gather": [(M * d, 3.59375 + 2.0 * T / M)],
         "grouped_gemm_nvfp4_fwd": [fl2] if layer.fuse_swiglu else [fl13, fl2],
         "grouped_gemm_nvfp4_fwd_swiglu": [fl13],
         "dequant_transpose_requant_sr": [(E * 2 * I * d, 1.59375), (E * d * I, 1.59375), (M * d, 1.59375),
@@ -347,11 +353,12 @@ def run_ours(args):
         ", Four Over Six activation blocks" if args.four_over_six else "")
     fwd_fl, bwd_fl = layer.flops()
     step_flops = fwd_fl + bwd_fl
+    x_in = m.x if layer.gathers_rows else m.x_perm  # the step's activation input
 
     # warm-up
     plain = build_step(layer, m, None)
     for _ in range(args.warmup):
-        plain(m.x_perm, m.g2)
+        plain(x_in, m.g2)
     torch.cuda.synchronize()
     st = N.nvfp4moe_get_device_status()
     if st != 0:
@@ -368,7 +375,7 @@ def run_ours(args):
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record(s)
     for _ in range(args.steps):
-        step(m.x_perm, m.g2)
+        step(x_in, m.g2)
     t1.record(s)
     torch.cuda.synchronize()
     barrier()
@@ -402,14 +409,16 @@ def run_ours(args):
     roof["traffic"] = measured_traffic(dom)
     roof["traffic_unit"] = "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum), null if stale"
 
-    # e2e through host buffers: x and g2 in, dx out, every step; the copies of
-    # neighbouring steps overlap the compute (pipeline.HostStaged)
+    # e2e through host buffers: the tokens, their routed rows' source map and
+    # g2 in, dx out, every step; the copies of neighbouring steps overlap the
+    # compute (pipeline.HostStaged)
     from precision_moe_numerics_nvfp4_gb300.pipeline import HostStaged
-    x_h = m.x_perm.cpu().pin_memory()
+    x_h = x_in.cpu().pin_memory()
+    rows_h = m.rows.cpu().pin_memory() if layer.gathers_rows else None
     g_h = m.g2.cpu().pin_memory()
     dx_h = torch.empty(layer.dx.shape, dtype=layer.dx.dtype).pin_memory()
-    staged = HostStaged(layer)
-    staged.step(x_h, g_h, dx_h, m.w13, m.w2, m.group_offsets, seed=3)  # untimed: first use of the slots
+    staged = HostStaged(layer, tokens=m.x.shape[0] if layer.gathers_rows else None)
+    staged.step(x_h, g_h, dx_h, m.w13, m.w2, m.group_offsets, seed=3, rows_h=rows_h)  # untimed: first use
     staged.synchronize()
     e2e_steps = max(2, min(args.steps, 10))
     torch.cuda.synchronize()
@@ -418,7 +427,7 @@ def run_ours(args):
     e0.record(s)
     staged.s_in.wait_event(e0)
     for _ in range(e2e_steps):
-        last = staged.step(x_h, g_h, dx_h, m.w13, m.w2, m.group_offsets, seed=3)
+        last = staged.step(x_h, g_h, dx_h, m.w13, m.w2, m.group_offsets, seed=3, rows_h=rows_h)
     s.wait_event(last)
     e1.record(s)
     torch.cuda.synchronize()
@@ -434,7 +443,7 @@ def run_ours(args):
         cpu = cpu_baseline(args.cpu_tokens)
     configs = None
     if not args.no_configs and not args.per_token and not args.four_over_six:
-        del staged, x_h, g_h, dx_h
+        del staged, x_h, rows_h, g_h, dx_h
         configs = other_configs(peaks, rank == 0 and not args.no_cpu_baseline)
 
     line = {
@@ -443,12 +452,16 @@ def run_ours(args):
         "vs_baseline": None, "dtype": "nvfp4 fwd / mxfp8 bwd (fp32 accumulate)", "data": "synthetic",
         "config": {"workload": workload, "global_batch": SHAPE["tokens"] * world, "rows": M,
                    "group_sizes": "top-8 of logits~N(0,1)+bias~N(0,1), uneven", "seed": 2,
-                   "parallelism": f"replicas x{world}", "l2": "inputs > L2 (GB-sized tensors), no flush"},
+                   "parallelism": f"replicas x{world}", "l2": "inputs > L2 (GB-sized tensors), no flush",
+                   "activations": ("per token [16384 x 4096]; the quantization of x gathers the routed rows"
+                                   if layer.gathers_rows else "routed rows [T*k x 4096], already dispatched")},
         "gemm_flops_per_step": step_flops,
         "roofline": roof, "kernels": kernels, "clocks": clocks,
         "e2e": {"value": aggregate(step_flops / 1e12, e2e_ms / 1e3, world), "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                "overlap": "copies in (step i+1) and out (step i-1) on their own streams during step i"},
+                "overlap": "copies in (step i+1) and out (step i-1) on their own streams during step i",
+                "inputs": ("tokens x [16384 x 4096] bf16, the routed rows' source tokens (int32), g2 per routed row"
+                           if layer.gathers_rows else "routed rows x [T*k x 4096] bf16, g2 per routed row")},
         "gpu_launches": layer.launches_per_step() * args.steps,
         "peaks": peaks,
         "cpu_baseline": cpu,

@@ -114,6 +114,11 @@ int64_t nvfp4moe_scale_offset(int64_t rp, int64_t c, int64_t kblocks);
 /* Workspace bytes nvfp4_quantize needs when it computes the outer scales. */
 size_t nvfp4moe_quantize_workspace_bytes(int64_t batch, int64_t rows, int64_t cols);
 
+/* Workspace bytes nvfp4_quantize_requant_gather needs when it computes the
+ * outer scale: src_rows token rows gathered into rows x cols.  0 for
+ * negative sizes. */
+size_t nvfp4moe_quantize_gather_workspace_bytes(int64_t src_rows, int64_t rows, int64_t cols);
+
 /* Workspace bytes grouped_gemm_nvfp4_fwd needs when it is given bf16
  * activations (x_bf16 non-NULL): their NVFP4 codes, grouped scales, outer
  * scale and the amax pass's scratch.  0 for invalid sizes. */
@@ -156,6 +161,32 @@ int nvfp4_quantize(const void *x, int64_t batch, int64_t rows, int64_t cols,
  */
 int nvfp4_outer_scale(const void *x, int64_t batch, int64_t n, float *outer_scale_out,
                       void *workspace, size_t workspace_bytes, nv_stream_t stream);
+
+/* ---- nvfp4_quantize_requant of gathered rows (the expert dispatch) ------------
+ * The MoE layer's activations arrive per token; the experts see them per
+ * routed row, each token repeated once per expert it is routed to.  This
+ * call quantizes the routed-row matrix X without materializing it: row r of
+ * X is row row_src[r] of x.  Its outputs are exactly those of
+ * nvfp4_quantize_requant on X (the same codes, scales, outer scale and SR
+ * draws: draws are keyed by the row of X), for the grouped (expert) layout
+ * and the per-tensor outer scale.
+ * x:        bf16 [src_rows][cols] (the tokens), cols % 128 == 0.
+ * row_src:  int32 [rows] (4-byte aligned), each in [0, src_rows); an index
+ *           outside that range makes its row read as zeros and records
+ *           NV_ERR_ARG in the device status word.
+ * The other arguments as for nvfp4_quantize_requant with batch = 1 and
+ * group_offsets required (num_groups >= 1).  The amax pass (outer_scale_in ==
+ * NULL) takes the maximum over the rows of X; when src_rows <= rows it reads
+ * each token row once (its row maximum) and takes the maximum of those over
+ * row_src, the same value.  Its workspace:
+ * nvfp4moe_quantize_gather_workspace_bytes(src_rows, rows, cols) bytes,
+ * 16-byte aligned. */
+int nvfp4_quantize_requant_gather(const void *x, const int32_t *row_src, int64_t src_rows, int64_t rows,
+                                  int64_t cols, const int32_t *group_offsets, int32_t num_groups,
+                                  const float *outer_scale_in, float *outer_scale_out, uint8_t *codes,
+                                  uint8_t *scales, void *workspace, size_t workspace_bytes, uint64_t seed,
+                                  uint64_t counter_offset, uint8_t *out_codes, uint8_t *out_scales,
+                                  nv_stream_t stream);
 
 /* ---- nvfp4_quantize for callers that cannot allocate device memory -------------
  * The pages have no counterpart to this entry point; it is a convenience of

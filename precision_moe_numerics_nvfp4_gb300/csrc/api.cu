@@ -78,6 +78,12 @@ size_t nvfp4moe_quantize_workspace_bytes(int64_t batch, int64_t rows, int64_t co
   return (size_t)rup((batch * nb + batch) * 4, 256);
 }
 
+// the amax pass's partial maxima, then one float per token
+size_t nvfp4moe_quantize_gather_workspace_bytes(int64_t src_rows, int64_t rows, int64_t cols) {
+  if (src_rows < 0 || rows < 0 || cols < 0) return 0;
+  return nvfp4moe_quantize_workspace_bytes(1, rows, cols) + (size_t)rup(src_rows * 4, 256);
+}
+
 // codes, then the grouped scale buffer, then the outer scale, then the amax
 // pass's workspace, each starting on a 256-byte boundary
 size_t nvfp4moe_fwd_workspace_bytes(int64_t M_total, int64_t K, int64_t E) {
@@ -244,6 +250,49 @@ int nvfp4_quantize_requant_four_over_six(const void *x, int64_t batch, int64_t r
   return quantize_requant_impl(x, batch, rows, cols, group_offsets, num_groups, outer_scale_in, outer_scale_out, codes,
                                scales, workspace, workspace_bytes, seed, counter_offset, out_codes, out_scales, stream,
                                1);
+}
+
+int nvfp4_quantize_requant_gather(const void *x, const int32_t *row_src, int64_t src_rows, int64_t rows,
+                                  int64_t cols, const int32_t *group_offsets, int32_t num_groups,
+                                  const float *outer_scale_in, float *outer_scale_out, uint8_t *codes,
+                                  uint8_t *scales, void *workspace, size_t workspace_bytes, uint64_t seed,
+                                  uint64_t counter_offset, uint8_t *out_codes, uint8_t *out_scales,
+                                  nv_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!x || !row_src || !codes || !scales || !out_codes || !out_scales || !group_offsets || src_rows < 0 ||
+      rows < 0 || cols < 0)
+    return NV_ERR_ARG;
+  if (num_groups < 1 || num_groups > kMaxGroups) return NV_ERR_ARG;
+  if (cols % 128) return NV_ERR_SHAPE;
+  if (!al16(x) || !al4(row_src) || !al16(codes) || !al16(scales) || !al16(out_codes) || !al16(out_scales) ||
+      !al16(group_offsets))
+    return NV_ERR_ALIGN;
+  if (rows == 0 || cols == 0) return NV_OK;
+  if (rows >= (int64_t)1 << 30 || src_rows >= (int64_t)1 << 31 || rows * cols / 16 >= (int64_t)1 << 31)
+    return NV_ERR_SHAPE;
+  if (!outer_scale_in &&
+      (!workspace || workspace_bytes < nvfp4moe_quantize_gather_workspace_bytes(src_rows, rows, cols) ||
+       !al16(workspace)))
+    return NV_ERR_WORKSPACE;
+  int *st = status_ptr();
+  if (!st) return NV_ERR_CUDA;
+  const float *sg = outer_scale_in;
+  if (!outer_scale_in) {
+    const int nb = amax_blocks(rows * cols);
+    float *partial = static_cast<float *>(workspace);
+    float *dst = outer_scale_out ? outer_scale_out : partial + nb;
+    float *row_amax = partial + nvfp4moe_quantize_workspace_bytes(1, rows, cols) / 4;
+    int r = launch_amax_gather(static_cast<const uint16_t *>(x), row_src, src_rows, rows, cols, partial, nb, row_amax,
+                               dst, st, s);
+    if (r != NV_OK) return r;
+    sg = dst;
+  } else if (outer_scale_out && outer_scale_out != outer_scale_in) {
+    if (cudaMemcpyAsync(outer_scale_out, outer_scale_in, sizeof(float), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+      return NV_ERR_CUDA;
+  }
+  return launch_nvfp4_requant(static_cast<const uint16_t *>(x), sg, 1, rows, cols, group_offsets, num_groups, codes,
+                              scales, seed, counter_offset, out_codes, out_scales, st, s, nullptr, 0, row_src,
+                              src_rows);
 }
 
 int rht32_s2f6_quantize(const void *x, int64_t rows, int64_t cols, uint32_t signs, int8_t *codes, uint8_t *scales,

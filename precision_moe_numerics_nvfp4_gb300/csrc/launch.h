@@ -38,7 +38,12 @@ int launch_requant(const uint8_t *codes, const uint8_t *scales, const float *sg,
 int launch_nvfp4_requant(const uint16_t *x, const float *sg, int64_t batch, int64_t rows, int64_t cols,
                          const int32_t *groups, int E, uint8_t *codes, uint8_t *scales, uint64_t seed, uint64_t off,
                          uint8_t *out_codes, uint8_t *out_scales, int *status, cudaStream_t s,
-                         const float *sg_rows = nullptr, int four_six = 0);
+                         const float *sg_rows = nullptr, int four_six = 0, const int32_t *row_src = nullptr,
+                         int64_t src_rows = 0);
+// amax pass over the gathered rows x[row_src[r]] (r < rows) -> sg_out[0];
+// row_amax: src_rows floats of scratch, used when src_rows <= rows
+int launch_amax_gather(const uint16_t *x, const int32_t *row_src, int64_t src_rows, int64_t rows, int64_t cols,
+                       float *partial, int nblk, float *row_amax, float *sg_out, int *status, cudaStream_t s);
 int launch_outer_scale_from_amax(float *amax_in_sg_out, cudaStream_t s);
 // per-row form: buf[r] = amax_r / 2688 (1 for zero) in place, r < n
 int launch_row_outer_scale_from_amax(float *amax_in_sg_out, int64_t n, cudaStream_t s);

@@ -58,6 +58,100 @@ __global__ void __launch_bounds__(256) amax_partial_kernel(const uint16_t *__res
   }
 }
 
+// The amax pass over the rows x[row_src[r]], r < rows (a gathered matrix):
+// one warp per row at a time, one partial maximum per block.  An index out
+// of range counts as a zero row and is recorded.  cols % 8 == 0.
+__global__ void __launch_bounds__(256) amax_gather_partial_kernel(const uint16_t *__restrict__ x,
+                                                                  const int32_t *__restrict__ row_src,
+                                                                  int64_t src_rows, int64_t rows, int64_t cols,
+                                                                  float *__restrict__ partial, int nblk, int *status) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint32_t acc0 = 0, acc1 = 0;
+  for (int64_t r = (int64_t)blockIdx.x * 8 + warp; r < rows; r += (int64_t)nblk * 8) {
+    const int64_t sr = row_src[r];
+    if (sr < 0 || sr >= src_rows) {
+      if (lane == 0) record_error(status, NV_ERR_ARG);
+      continue;
+    }
+    const uint16_t *p = x + sr * cols;
+    int64_t c = (int64_t)lane * 8;
+    for (; c + 256 < cols; c += 512) {
+      const uint4 v0 = ld_stream_v4(p + c), v1 = ld_stream_v4(p + c + 256);
+      acc0 = bf16x2_absmax(acc0, bf16x2_absmax(bf16x2_absmax(v0.x, v0.y), bf16x2_absmax(v0.z, v0.w)));
+      acc1 = bf16x2_absmax(acc1, bf16x2_absmax(bf16x2_absmax(v1.x, v1.y), bf16x2_absmax(v1.z, v1.w)));
+    }
+    for (; c < cols; c += 256) {
+      const uint4 v = ld_stream_v4(p + c);
+      acc0 = bf16x2_absmax(acc0, bf16x2_absmax(bf16x2_absmax(v.x, v.y), bf16x2_absmax(v.z, v.w)));
+    }
+  }
+  float m = bf16x2_max_to_f32(bf16x2_absmax(acc0, acc1));
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, d));
+  __shared__ float s_m[8];
+  if (lane == 0) s_m[warp] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float q = s_m[0];
+    for (int w = 1; w < 8; ++w) q = fmaxf(q, s_m[w]);
+    partial[blockIdx.x] = q;
+  }
+}
+
+// The same maximum from the tokens' own row maxima, for a token matrix no
+// larger than X: a row of X is a token row, so max|X| = max over r of
+// amax(x[row_src[r]]), and each token row is read once however many rows of
+// X repeat it.  Stage 1: one warp per token row -> row_amax[token].
+__global__ void __launch_bounds__(256) token_amax_kernel(const uint16_t *__restrict__ x, int64_t src_rows,
+                                                         int64_t cols, float *__restrict__ row_amax) {
+  const int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= src_rows) return;
+  const uint16_t *p = x + t * cols;
+  uint32_t acc0 = 0u, acc1 = 0u;
+  int64_t c = (int64_t)lane * 8;
+  for (; c + 256 < cols; c += 512) {
+    const uint4 v0 = ld_stream_v4(p + c), v1 = ld_stream_v4(p + c + 256);
+    acc0 = bf16x2_absmax(acc0, bf16x2_absmax(bf16x2_absmax(v0.x, v0.y), bf16x2_absmax(v0.z, v0.w)));
+    acc1 = bf16x2_absmax(acc1, bf16x2_absmax(bf16x2_absmax(v1.x, v1.y), bf16x2_absmax(v1.z, v1.w)));
+  }
+  for (; c < cols; c += 256) {
+    const uint4 v = ld_stream_v4(p + c);
+    acc0 = bf16x2_absmax(acc0, bf16x2_absmax(bf16x2_absmax(v.x, v.y), bf16x2_absmax(v.z, v.w)));
+  }
+  uint32_t m = bf16x2_absmax(acc0, acc1);
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) m = bf16x2_absmax(m, __shfl_xor_sync(0xFFFFFFFFu, m, d));
+  if (lane == 0) row_amax[t] = bf16x2_max_to_f32(m);
+}
+
+// Stage 2: one partial maximum per block of row_amax[row_src[r]]; an index
+// out of range counts as a zero row and is recorded.
+__global__ void __launch_bounds__(256) gather_amax_partial_kernel(const float *__restrict__ row_amax,
+                                                                  const int32_t *__restrict__ row_src,
+                                                                  int64_t src_rows, int64_t rows,
+                                                                  float *__restrict__ partial, int nblk, int *status) {
+  float m = 0.0f;
+  for (int64_t r = (int64_t)blockIdx.x * 256 + threadIdx.x; r < rows; r += (int64_t)nblk * 256) {
+    const int64_t sr = row_src[r];
+    if (sr < 0 || sr >= src_rows) {
+      record_error(status, NV_ERR_ARG);
+      continue;
+    }
+    m = fmaxf(m, row_amax[sr]);
+  }
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, d));
+  __shared__ float s_m[8];
+  if ((threadIdx.x & 31) == 0) s_m[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float q = s_m[0];
+    for (int w = 1; w < 8; ++w) q = fmaxf(q, s_m[w]);
+    partial[blockIdx.x] = q;
+  }
+}
+
 // sg = amax / (6 * 448), or 1 for an all-zero tensor
 __global__ void __launch_bounds__(32) outer_scale_finalize_kernel(const float *__restrict__ partial, int nblk,
                                                                   float *__restrict__ sg_out) {
@@ -425,6 +519,8 @@ enum { kSrcBf16 = 0, kSrcNvfp4 = 1, kSrcBf16ToNvfp4 = 2 };
 struct MxTArgs {
   // input
   const uint16_t *x;                 // bf16 source (kSrcBf16, kSrcBf16ToNvfp4)
+  const int32_t *row_src;            // kSrcBf16ToNvfp4: row r of the source is x row row_src[r] (null: r)
+  int64_t src_rows;                  // rows of x when row_src is given
   const uint8_t *nv_codes;           // NVFP4 source (kSrcNvfp4)
   const uint8_t *nv_scales;
   const float *nv_sg;                // outer scale: [batch] (batched) or [1]
@@ -571,8 +667,16 @@ __device__ __forceinline__ void stage_bf16_tile(const MxTArgs &A, const Window &
   for (int k = 0; k < 8; ++k) {
     const int q = k * 256 + (int)threadIdx.x;
     const int i = q >> 4, c16 = q & 15;
-    const bool ok = i < w.nvalid;
-    const uint16_t *src = ok ? A.x + (w.src_row0 + i) * A.cols + col0 + c16 * 8 : A.x;
+    bool ok = i < w.nvalid;
+    int64_t row = w.src_row0 + i;
+    if (A.row_src && ok) {  // gathered source: a row index out of range reads as zeros and is recorded
+      row = A.row_src[row];
+      if (row < 0 || row >= A.src_rows) {
+        record_error(A.status, NV_ERR_ARG);
+        ok = false;
+      }
+    }
+    const uint16_t *src = ok ? A.x + row * A.cols + col0 + c16 * 8 : A.x;
     cp_async16(s_in + i * 256 + chunk_of(i, c16) * 16, src, ok ? 16u : 0u);
   }
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
@@ -907,6 +1011,20 @@ int launch_amax(const uint16_t *x, int64_t batch, int64_t per_batch, float *part
   return launch_status(cudaGetLastError());
 }
 
+// the amax pass of the gathered rows x[row_src[r]]: row_amax holds src_rows
+// floats when src_rows <= rows
+int launch_amax_gather(const uint16_t *x, const int32_t *row_src, int64_t src_rows, int64_t rows, int64_t cols,
+                       float *partial, int nblk, float *row_amax, float *sg_out, int *status, cudaStream_t s) {
+  if (src_rows <= rows) {  // the tokens once each, then the maximum over the row map
+    if (src_rows > 0) token_amax_kernel<<<(unsigned)((src_rows + 7) / 8), 256, 0, s>>>(x, src_rows, cols, row_amax);
+    gather_amax_partial_kernel<<<nblk, 256, 0, s>>>(row_amax, row_src, src_rows, rows, partial, nblk, status);
+  } else {  // more tokens than rows: read the routed rows themselves
+    amax_gather_partial_kernel<<<nblk, 256, 0, s>>>(x, row_src, src_rows, rows, cols, partial, nblk, status);
+  }
+  outer_scale_finalize_kernel<<<1, 32, 0, s>>>(partial, nblk, sg_out);
+  return launch_status(cudaGetLastError());
+}
+
 // sg = amax / 2688 (1 for a zero amax) in place, exactly as the amax pass
 // finishes (one partial maximum)
 int launch_outer_scale_from_amax(float *amax_in_sg_out, cudaStream_t s) {
@@ -1015,9 +1133,9 @@ int launch_requant(const uint8_t *codes, const uint8_t *scales, const float *sg,
 int launch_nvfp4_requant(const uint16_t *x, const float *sg, int64_t batch, int64_t rows, int64_t cols,
                          const int32_t *groups, int E, uint8_t *codes, uint8_t *scales, uint64_t seed, uint64_t off,
                          uint8_t *out_codes, uint8_t *out_scales, int *status, cudaStream_t s, const float *sg_rows,
-                         int four_six) {
+                         int four_six, const int32_t *row_src, int64_t src_rows) {
   MxTArgs A = {};
-  A.x = x; A.nv_sg = sg; A.nv_sg_rows = sg_rows; A.rows = rows; A.cols = cols; A.groups = groups; A.E = E;
+  A.x = x; A.row_src = row_src; A.src_rows = src_rows; A.nv_sg = sg; A.nv_sg_rows = sg_rows; A.rows = rows; A.cols = cols; A.groups = groups; A.E = E;
   A.nv_codes_out = codes; A.nv_scales_out = scales; A.nv_ka = cols / 64;
   A.sr = 1; A.seed = seed; A.off_t = off; A.status = status;
   A.rk = philox_round_keys(seed);

@@ -36,6 +36,7 @@ _SIGS = {
     "nvfp4moe_scale_bytes": (_I64, [_I64, _I64]),
     "nvfp4moe_scale_offset": (_I64, [_I64, _I64, _I64]),
     "nvfp4moe_quantize_workspace_bytes": (_SZ, [_I64, _I64, _I64]),
+    "nvfp4moe_quantize_gather_workspace_bytes": (_SZ, [_I64, _I64, _I64]),
     "nvfp4moe_fwd_workspace_bytes": (_SZ, [_I64, _I64, _I64]),
     "nvfp4_quantize": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _I32, _P, _P, _P, _P, _P, _SZ, _P]),
     "nvfp4_quantize_noalloc": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _I32, _P, _P, _P, _P, _P]),
@@ -63,6 +64,8 @@ _SIGS = {
     "nvfp4moe_set_gemm_kernel": (ctypes.c_int, [ctypes.c_int]),
     "nvfp4moe_set_gemm_wait_limit": (ctypes.c_int, [_I64]),
     "nvfp4moe_sr_e4m3x4": (ctypes.c_int, [_P, _P, _I64, _P, _P]),
+    "nvfp4_quantize_requant_gather": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _P, _I32, _P, _P, _P, _P, _P, _SZ,
+                                                     _U64, _U64, _P, _P, _P]),
     "grouped_gemm_nvfp4_fwd_rht_s2f6": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I32, _I64, _I64, _I64,
                                                        ctypes.c_uint32, _P, _P, _P, _P]),
     "nvfp4_outer_scale": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _SZ, _P]),
@@ -158,6 +161,10 @@ def nvfp4moe_quantize_workspace_bytes(batch: int, rows: int, cols: int) -> int:
     return int(lib().nvfp4moe_quantize_workspace_bytes(batch, rows, cols))
 
 
+def nvfp4moe_quantize_gather_workspace_bytes(src_rows: int, rows: int, cols: int) -> int:
+    return int(lib().nvfp4moe_quantize_gather_workspace_bytes(src_rows, rows, cols))
+
+
 def nvfp4moe_fwd_workspace_bytes(M_total: int, K: int, E: int) -> int:
     return int(lib().nvfp4moe_fwd_workspace_bytes(M_total, K, E))
 
@@ -179,6 +186,15 @@ def nvfp4moe_set_gemm_kernel(variant: int) -> None:
     GEMM_CTA_PAIR_N128 (256 x 128 pair tiles, two pairs per SM pair); a pair
     choice applies where the shape allows it."""
     _check("nvfp4moe_set_gemm_kernel", lib().nvfp4moe_set_gemm_kernel(int(variant)))
+
+
+def nvfp4_quantize_requant_gather(x, row_src, src_rows, rows, cols, group_offsets, outer_scale_in, outer_scale_out,
+                                  codes, scales, workspace, seed, counter_offset, out_codes, out_scales, stream=None):
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return _check("nvfp4_quantize_requant_gather", lib().nvfp4_quantize_requant_gather(
+        _ptr(x), _ptr(row_src), int(src_rows), int(rows), int(cols), _ptr(group_offsets), _ng(group_offsets),
+        _ptr(outer_scale_in), _ptr(outer_scale_out), _ptr(codes), _ptr(scales), _ptr(workspace), ws_bytes, seed,
+        counter_offset, _ptr(out_codes), _ptr(out_scales), _stream(stream)))
 
 
 def nvfp4moe_sr_e4m3x4(x, draws, n4, codes, stream=None):

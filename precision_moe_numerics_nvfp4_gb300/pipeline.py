@@ -49,6 +49,13 @@ class NvTensor:
         self.codes, self.scales = _u8(cb, dev), _u8(sb, dev)
         self.sg = _empty(batch, F32, dev)
         self.ws = _u8(N.nvfp4moe_quantize_workspace_bytes(batch, rows, cols), dev)
+        self.gws = None  # the gathered quantization's workspace, sized on first use
+
+    def gather_workspace(self, src_rows):
+        n = N.nvfp4moe_quantize_gather_workspace_bytes(src_rows, self.rows, self.cols)
+        if self.gws is None or self.gws.numel() < n:
+            self.gws = _u8(n, self.codes.device)
+        return self.gws
 
     def quantize(self, x, groups=None, stream=None, sg_in=None, four_six=False):
         """`sg_in`: a given outer scale (skips the amax pass); `four_six`: the
@@ -56,9 +63,18 @@ class NvTensor:
         f = N.nvfp4_quantize_four_over_six if four_six else N.nvfp4_quantize
         f(x, self.batch, self.rows, self.cols, groups, sg_in, self.sg, self.codes, self.scales, self.ws, stream)
 
-    def quantize_requant(self, x, mx, seed, offset, groups=None, stream=None, sg_in=None, four_six=False):
+    def quantize_requant(self, x, mx, seed, offset, groups=None, stream=None, sg_in=None, four_six=False,
+                         x_rows=None):
         """quantize() plus the SR re-quantization of the result into `mx`
-        (an MxTransposed), in one pass over x."""
+        (an MxTransposed), in one pass over x.  `x_rows` (int32 [rows]): row
+        r of the matrix is x[x_rows[r]] (grouped, per-tensor scale only)."""
+        if x_rows is not None:
+            if four_six or groups is None:
+                raise ValueError("gathered rows: grouped layout and the plain block rule only")
+            ws = None if sg_in is not None else self.gather_workspace(x.shape[0])
+            N.nvfp4_quantize_requant_gather(x, x_rows, x.shape[0], self.rows, self.cols, groups, sg_in, self.sg,
+                                            self.codes, self.scales, ws, seed, offset, mx.codes, mx.scales, stream)
+            return
         f = N.nvfp4_quantize_requant_four_over_six if four_six else N.nvfp4_quantize_requant
         f(x, self.batch, self.rows, self.cols, groups, sg_in, self.sg, self.codes, self.scales, self.ws, seed, offset,
           mx.codes, mx.scales, stream)
@@ -205,6 +221,13 @@ class MoELayer:
         self.dw2 = _empty((E, d_model, d_ff), F32, dev)
         self.dw13 = _empty((E, I2, d_model), F32, dev)
 
+    @property
+    def gathers_rows(self):
+        """Whether step() can take the tokens and the routed rows' source map
+        (the quantization of x gathering the rows): the fused training step
+        with per-tensor scales, the plain block rule and no side stream."""
+        return self.fuse_requant and not self.per_token and not self.four_six and self.side is None
+
     # GEMM FLOPs of one forward (2 GEMMs) and one backward (4 GEMMs)
     def flops(self):
         fwd = 2 * self.M * (2 * self.I) * self.d + 2 * self.M * self.d * self.I
@@ -220,10 +243,14 @@ class MoELayer:
             self.w13q.quantize_requant(w13, self.w13t, seed, OFF_W13, None, stream)
             self.w2q.quantize_requant(w2, self.w2t, seed, OFF_W2, None, stream)
 
-    def forward(self, x, w13, w2, groups, stream=None, seed=None):
+    def forward(self, x, w13, w2, groups, stream=None, seed=None, x_rows=None):
         """`seed` (training): also re-quantize the forward tensors for the
-        backward in the same passes."""
+        backward in the same passes.  `x_rows` (int32 [M]): x holds the
+        tokens and routed row r is token x_rows[r] (the dispatch), gathered
+        by the quantization of x itself (training step, per-tensor scales)."""
         seed = seed if self.fuse_requant else None
+        if x_rows is not None and (seed is None or not self.gathers_rows):
+            raise ValueError("gathered activations need the fused training step with per-tensor scales")
         x_sg = None
         if self.side is not None:
             main = stream if stream is not None else torch.cuda.current_stream()
@@ -247,12 +274,12 @@ class MoELayer:
             x_sg = self.xq.sg
         else:
             self.quantize_weights(w13, w2, stream, seed)
-        self.forward_activations(x, groups, stream, seed, x_sg=x_sg)
+        self.forward_activations(x, groups, stream, seed, x_sg=x_sg, x_rows=x_rows)
         self._requant_seed = seed
 
-    def forward_activations(self, x, groups, stream=None, seed=None, x_sg=None):
+    def forward_activations(self, x, groups, stream=None, seed=None, x_sg=None, x_rows=None):
         """The forward with the weights already quantized (e.g. sampling);
-        `x_sg`: x's outer scale, already computed."""
+        `x_sg`: x's outer scale, already computed; `x_rows`: see forward."""
         if self.per_token:
             return self._forward_activations_rows(x, groups, stream, seed)
         M, d, I, E = self.M, self.d, self.I, self.E
@@ -260,7 +287,8 @@ class MoELayer:
         if seed is None:
             self.xq.quantize(x, groups, stream, sg_in=x_sg, four_six=f6)
         else:
-            self.xq.quantize_requant(x, self.xt, seed, OFF_XQ, groups, stream, sg_in=x_sg, four_six=f6)
+            self.xq.quantize_requant(x, self.xt, seed, OFF_XQ, groups, stream, sg_in=x_sg, four_six=f6,
+                                     x_rows=x_rows)
         sg_h = None
         if self.fuse_swiglu:
             N.grouped_gemm_nvfp4_fwd_swiglu(self.xq.sg, self.xq.codes, self.xq.scales, self.w13q.codes,
@@ -351,8 +379,8 @@ class MoELayer:
         N.grouped_gemm_mxfp8_dw(self.dy13t.codes, self.dy13t.scales, self.xt.codes, self.xt.scales, groups, E, M,
                                 I2, d, self.dw13, None, stream)
 
-    def step(self, x, w13, w2, g2, groups, seed=3, stream=None, dx_out=None):
-        self.forward(x, w13, w2, groups, stream, seed)
+    def step(self, x, w13, w2, g2, groups, seed=3, stream=None, dx_out=None, x_rows=None):
+        self.forward(x, w13, w2, groups, stream, seed, x_rows=x_rows)
         self.backward(g2, groups, seed, stream, dx_out)
 
     @staticmethod
@@ -401,11 +429,15 @@ class HostStaged:
     The host buffers must stay untouched until `synchronize()` (or until the
     copy-out of that step has completed)."""
 
-    def __init__(self, layer: MoELayer, device="cuda"):
+    def __init__(self, layer: MoELayer, device="cuda", tokens=None):
+        """`tokens`: the steps take the token matrix [tokens, d] and the routed
+        rows' source tokens (int32 [M]) instead of the routed rows themselves."""
         dev = torch.device(device)
         M, d = layer.M, layer.d
         self.layer = layer
-        self.x = [torch.empty((M, d), dtype=BF16, device=dev) for _ in range(2)]
+        self.tokens = tokens
+        self.x = [torch.empty((tokens if tokens is not None else M, d), dtype=BF16, device=dev) for _ in range(2)]
+        self.rows = [torch.empty(M, dtype=torch.int32, device=dev) for _ in range(2)] if tokens is not None else None
         self.g2 = [torch.empty((M, d), dtype=BF16, device=dev) for _ in range(2)]
         self.dx = [_empty((M, d), BF16, dev) for _ in range(2)]
         self.s_in = torch.cuda.Stream(dev)
@@ -418,9 +450,10 @@ class HostStaged:
     def bytes_per_step(self):
         """(host -> device, device -> host) bytes of one step."""
         b = lambda t: t.numel() * t.element_size()
-        return b(self.x[0]) + b(self.g2[0]), b(self.dx[0])
+        rows = b(self.rows[0]) if self.rows is not None else 0
+        return b(self.x[0]) + rows + b(self.g2[0]), b(self.dx[0])
 
-    def step(self, x_h, g2_h, dx_h, w13, w2, groups, seed=3):
+    def step(self, x_h, g2_h, dx_h, w13, w2, groups, seed=3, rows_h=None):
         k = self.n % 2
         comp = torch.cuda.current_stream()
         x_in, g2_in = torch.cuda.Event(), torch.cuda.Event()
@@ -428,13 +461,16 @@ class HostStaged:
             if self.x_read[k] is not None:
                 self.s_in.wait_event(self.x_read[k])
             self.x[k].copy_(x_h, non_blocking=True)
+            if self.rows is not None:
+                self.rows[k].copy_(rows_h, non_blocking=True)
             x_in.record(self.s_in)
             if self.g2_read[k] is not None:
                 self.s_in.wait_event(self.g2_read[k])
             self.g2[k].copy_(g2_h, non_blocking=True)
             g2_in.record(self.s_in)
         comp.wait_event(x_in)
-        self.layer.forward(self.x[k], w13, w2, groups, comp, seed)
+        self.layer.forward(self.x[k], w13, w2, groups, comp, seed,
+                           x_rows=self.rows[k] if self.rows is not None else None)
         fwd_done = torch.cuda.Event()
         fwd_done.record(comp)
         self.x_read[k] = fwd_done

@@ -117,6 +117,8 @@ class MoE:
     w13: torch.Tensor             # bf16 [E, 2I, d_model] (gate rows then up rows)
     w2: torch.Tensor              # bf16 [E, d_model, I]
     g2: torch.Tensor | None       # bf16 [T*k, d_model] gradient of the down output
+    x: torch.Tensor | None = None     # bf16 [T, d_model] the tokens (x_perm = x[token])
+    rows: torch.Tensor | None = None  # int32 [T*k] source token of each row
 
 
 def moe(device="cpu", seed: int = 2, tokens: int = 16384, d_model: int = 4096, experts: int = 64,
@@ -141,7 +143,7 @@ def moe(device="cpu", seed: int = 2, tokens: int = 16384, d_model: int = 4096, e
     if with_grad:
         gg = _gen(grad_seed, device)
         g2 = normal((tokens * topk, d_model), 1e-3, gg, device)
-    return MoE(x_perm, offsets, token, w13, w2, g2)
+    return MoE(x_perm, offsets, token, w13, w2, g2, x, token.to(torch.int32))
 
 
 def decode(device="cpu", seed: int = 4, tokens: int = 256, d_model: int = 7168, d_ff: int = 2048,

@@ -125,3 +125,22 @@ def test_gemm_wait_limit_range(L):
     assert f(-1) == N.NV_ERR_ARG
     assert f((1 << 26) + 1) == N.NV_ERR_ARG
     assert f(0) == N.NV_OK          # the default
+
+
+def test_quantize_requant_gather_validation(L):
+    f = L.nvfp4_quantize_requant_gather
+    ws = 1 << 20
+    # x, row_src, src_rows, rows, cols, groups, ngroups, sg_in, sg_out, codes, scales, ws, ws_bytes, seed, off, oc, os
+    assert f(A, NULL, 64, 128, 128, A, 2, NULL, A, A, A, A, ws, 1, 0, A, A, S) == N.NV_ERR_ARG      # no row map
+    assert f(A, A, 64, 128, 128, NULL, 0, NULL, A, A, A, A, ws, 1, 0, A, A, S) == N.NV_ERR_ARG      # groups required
+    assert f(A, A, 64, 128, 192, A, 2, NULL, A, A, A, A, ws, 1, 0, A, A, S) == N.NV_ERR_SHAPE       # cols % 128
+    assert f(A, A1, 64, 128, 128, A, 2, NULL, A, A, A, A, ws, 1, 0, A, A, S) == N.NV_ERR_ALIGN      # row map 4-byte
+    assert f(A, A, 64, 128, 128, A, 2, NULL, A, A, A, A, 16, 1, 0, A, A, S) == N.NV_ERR_WORKSPACE   # no room
+    assert f(A, A, 64, 0, 128, A, 2, NULL, A, A, A, A, ws, 1, 0, A, A, S) == N.NV_OK                # empty
+
+
+def test_quantize_gather_workspace_bytes():
+    for src, rows, cols in ((16384, 131072, 4096), (1000, 64, 256), (0, 128, 128)):
+        want = N.nvfp4moe_quantize_workspace_bytes(1, rows, cols) + (src * 4 + 255) // 256 * 256
+        assert N.nvfp4moe_quantize_gather_workspace_bytes(src, rows, cols) == want
+    assert N.nvfp4moe_quantize_gather_workspace_bytes(-1, 128, 128) == 0
