@@ -247,6 +247,47 @@ __device__ __forceinline__ void store_segment_coalesced(uint8_t *seg0, int64_t l
   }
 }
 
+// SwiGLU epilogue of one accumulator row segment: r[0..63] the gate and
+// r[64..127] the up columns of hidden features col0 .. col0 + 63 of output row
+// `orow`.  y13 = bf16(acc * alpha) exactly as the plain bf16 output; h from
+// the rounded gate and up with the SwiGLU kernel's arithmetic; max |h| of the
+// rows that exist, one atomic per warp, or per row with per-token scales (max
+// is order-free).  Every lane of the warp must call it.
+__device__ __forceinline__ void swiglu_epilogue(const GemmArgs &A, const uint32_t *r, float alpha, bool store,
+                                                int64_t orow, int64_t col0, int lane) {
+  float hmax = 0.0f;
+  if (store) {
+    uint16_t *yg = static_cast<uint16_t *>(A.out) + orow * (2 * A.I) + col0;
+    uint16_t *yu = yg + A.I;
+    uint16_t *hp = static_cast<uint16_t *>(A.h) + orow * A.I + col0;
+#pragma unroll
+    for (int i = 0; i < 64; i += 16) {
+      uint32_t wg[8], wu[8], wh[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        wg[k] = pack_bf16x2(__fmul_rn(__uint_as_float(r[i + 2 * k]), alpha),
+                            __fmul_rn(__uint_as_float(r[i + 2 * k + 1]), alpha));
+        wu[k] = pack_bf16x2(__fmul_rn(__uint_as_float(r[64 + i + 2 * k]), alpha),
+                            __fmul_rn(__uint_as_float(r[64 + i + 2 * k + 1]), alpha));
+        const float h0 = swiglu_h(bf16_lo(wg[k]), bf16_lo(wu[k]));
+        const float h1 = swiglu_h(bf16_hi(wg[k]), bf16_hi(wu[k]));
+        wh[k] = f32_to_bf16_bits(h0) | (f32_to_bf16_bits(h1) << 16);
+        hmax = fmaxf(hmax, fmaxf(fabsf(bf16_lo(wh[k])), fabsf(bf16_hi(wh[k]))));
+      }
+      st_cs_v8(yg + i, wg[0], wg[1], wg[2], wg[3], wg[4], wg[5], wg[6], wg[7]);
+      st_cs_v8(yu + i, wu[0], wu[1], wu[2], wu[3], wu[4], wu[5], wu[6], wu[7]);
+      st_cs_v8(hp + i, wh[0], wh[1], wh[2], wh[3], wh[4], wh[5], wh[6], wh[7]);
+    }
+  }
+  if (A.h_amax_rows) {  // per token: this thread's row
+    if (store && hmax > 0.0f) atomicMax(A.h_amax + orow, __float_as_uint(hmax));
+  } else {
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) hmax = fmaxf(hmax, __shfl_xor_sync(0xFFFFFFFFu, hmax, d));
+    if (lane == 0 && hmax > 0.0f) atomicMax(A.h_amax, __float_as_uint(hmax));
+  }
+}
+
 // Bound of the waits that let a CTA leave cleanly: the producer's wait for its
 // own copies to land and the MMA thread's wait for its own MMAs to finish.
 // They are separate from the pipeline waits' limit (GemmArgs::wait_limit,
@@ -545,41 +586,8 @@ __global__ void __launch_bounds__(192, 2)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&acc_empty[acc]));
       if (KIND == kGemmNvfp4FwdSwiglu) {
-        // columns 0-63: gate, 64-127: up of hidden features out_col0 .. +63.
-        // y13 = bf16(acc * alpha) exactly as the plain bf16 output; h from the
-        // rounded gate and up with the SwiGLU kernel's arithmetic; max |h| of
-        // the rows that exist, one atomic per warp (max is order-free)
-        float hmax = 0.0f;
-        if (store) {
-          uint16_t *yg = static_cast<uint16_t *>(A.out) + orow * (2 * A.I) + T.out_col0;
-          uint16_t *yu = yg + A.I;
-          uint16_t *hp = static_cast<uint16_t *>(A.h) + orow * A.I + T.out_col0;
-#pragma unroll
-          for (int i = 0; i < 64; i += 16) {
-            uint32_t wg[8], wu[8], wh[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              wg[k] = pack_bf16x2(__fmul_rn(__uint_as_float(r[i + 2 * k]), alpha),
-                                  __fmul_rn(__uint_as_float(r[i + 2 * k + 1]), alpha));
-              wu[k] = pack_bf16x2(__fmul_rn(__uint_as_float(r[64 + i + 2 * k]), alpha),
-                                  __fmul_rn(__uint_as_float(r[64 + i + 2 * k + 1]), alpha));
-              const float h0 = swiglu_h(bf16_lo(wg[k]), bf16_lo(wu[k]));
-              const float h1 = swiglu_h(bf16_hi(wg[k]), bf16_hi(wu[k]));
-              wh[k] = f32_to_bf16_bits(h0) | (f32_to_bf16_bits(h1) << 16);
-              hmax = fmaxf(hmax, fmaxf(fabsf(bf16_lo(wh[k])), fabsf(bf16_hi(wh[k]))));
-            }
-            st_cs_v8(yg + i, wg[0], wg[1], wg[2], wg[3], wg[4], wg[5], wg[6], wg[7]);
-            st_cs_v8(yu + i, wu[0], wu[1], wu[2], wu[3], wu[4], wu[5], wu[6], wu[7]);
-            st_cs_v8(hp + i, wh[0], wh[1], wh[2], wh[3], wh[4], wh[5], wh[6], wh[7]);
-          }
-        }
-        if (A.h_amax_rows) {  // per token: this thread's row
-          if (store && hmax > 0.0f) atomicMax(A.h_amax + orow, __float_as_uint(hmax));
-        } else {
-#pragma unroll
-          for (int d = 16; d > 0; d >>= 1) hmax = fmaxf(hmax, __shfl_xor_sync(0xFFFFFFFFu, hmax, d));
-          if (lane == 0 && hmax > 0.0f) atomicMax(A.h_amax, __float_as_uint(hmax));
-        }
+        // columns 0-63: gate, 64-127: up of hidden features out_col0 .. +63
+        swiglu_epilogue(A, r, alpha, store, orow, T.out_col0, lane);
       } else if (KIND == kGemmMxfp8Dw && A.out_fp32) {
         // wgrad: the warp's 32 fp32 dW rows (all exist; alpha is 1) as whole lines
         uint8_t *row0 = static_cast<uint8_t *>(A.out) + ((T.out_row0 + q * 32) * A.out_ld + T.out_col0) * 4;
@@ -637,6 +645,7 @@ __global__ void __launch_bounds__(192, 2)
       }
     }
   }
+  __syncwarp();  // single-lane roles rejoin their warps before the CTA barrier
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -750,7 +759,8 @@ __device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v
 template <int KIND, int STAGES, int BN, int CHUNKS = 1>
 struct CfgPair {
   static_assert(BN == 128 || BN == 256, "pair tile width");
-  static constexpr bool kFp4 = KIND == kGemmNvfp4Fwd;
+  static_assert(KIND != kGemmNvfp4FwdSwiglu || BN == 256, "SwiGLU pair tiles: 128 gate + 128 up rows");
+  static constexpr bool kFp4 = KIND == kGemmNvfp4Fwd || KIND == kGemmNvfp4FwdSwiglu;
   static constexpr int kAtomsPerStage = kFp4 ? 4 : 1;   // 128x4 scale tiles per 128 rows per chunk
   static constexpr int kBHalf = BN / 2;                 // B rows staged by each CTA
   static constexpr int kSfbTiles = BN / 128;            // 128-row scale tiles of B per k-atom
@@ -770,10 +780,20 @@ struct CfgPair {
   static constexpr int SF_COLS = CHUNKS * SF_CHUNK_COLS;  // per stage
   static constexpr int ACC_COLS = BN;
   static constexpr int TMEM_COLS = cpow2(ACC_COLS + STAGES * SF_COLS);
-  static constexpr int NBARS = 2 * STAGES + 3;          // full, empty, acc_full, acc_empty, mma_done
-  static constexpr int kEpiWarps = BN / 32;             // per lane quadrant: BN / 128 warps of 128 columns
-  static constexpr int kThreads = 32 * (2 + kEpiWarps);
+  // full, empty, acc_full, acc_empty, mma_done, then (with copy issuers)
+  // sf_full and sf_land per stage and one drain barrier per issuer
   static constexpr int kCtasPerSm = BN == 128 ? 2 : 1;
+  // A tcgen05.cp holds its issuing thread for about 64 cycles and runs
+  // alongside the MMAs only when another thread issues it, so with one pair
+  // per SM pair (room for two more warps) two warps of the even CTA issue a
+  // stage's scale copies, half each, while the MMA thread issues its MMAs.
+  // The 256 x 128 variant (two pairs per SM pair) keeps the copies on the MMA
+  // thread: its registers leave no room for more warps.
+  static constexpr int kSfWarps = kCtasPerSm == 1 ? 2 : 0;
+  static constexpr int NBARS = 2 * STAGES + 3 + (kSfWarps ? 2 * STAGES + kSfWarps : 0);
+  static constexpr int kEpi0 = 2 + kSfWarps;            // first epilogue warp
+  static constexpr int kEpiWarps = BN / 32;             // per lane quadrant: BN / 128 warps of 128 columns
+  static constexpr int kThreads = 32 * (kEpi0 + kEpiWarps);
   static constexpr uint32_t IDESC = (kFp4 ? ((1u << 7) | (1u << 10)) : (1u << 23)) |
                                     ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
   static size_t smem_bytes(int E) {
@@ -817,7 +837,8 @@ __device__ inline void sort_experts_by_size(const int *s_pad, int E, int *s_ord)
 struct PairTile {
   int e, nk, k_off, mrows;
   int a_row, b_row;
-  int64_t a_tile, b_tile0, k_atom0, out_row0, out_col0;
+  int64_t a_tile, k_atom0, out_row0, out_col0;
+  int64_t b_sft[2];  // 128-row scale tiles of the tile's B rows
 };
 
 // s_pb[e]: number of 256-row pair blocks before expert e (fwd, dgrad);
@@ -838,14 +859,27 @@ __device__ __forceinline__ PairTile decode_pair(int t, const GemmArgs &A, const 
     T.a_row = s_off[e] + (ph - s_pad[e]);
     T.mrows = live ? min(128, s_off[e + 1] - T.a_row) : 0;
     T.a_tile = ph / 128;
-    const int nb = (int)(KIND == kGemmNvfp4Fwd ? A.N : A.K);
-    T.b_row = e * nb + nt * BN + (BN / 2) * cta;
-    T.b_tile0 = ((int64_t)e * nb + (int64_t)nt * BN) / 128;
-    T.nk = (int)(KIND == kGemmNvfp4Fwd ? A.K / 256 : A.N / 128);
+    constexpr bool kFwd = KIND == kGemmNvfp4Fwd || KIND == kGemmNvfp4FwdSwiglu;
+    const int nb = (int)(kFwd ? A.N : A.K);
+    if (KIND == kGemmNvfp4FwdSwiglu) {
+      // 128 hidden features: the even CTA stages their 128 gate rows, the odd
+      // CTA the matching up rows (I further down the expert's w13), so that
+      // accumulator columns 0-127 are the gate and 128-255 the up
+      const int64_t g_row = (int64_t)e * nb + (int64_t)nt * 128;
+      T.b_row = (int)(g_row + (int64_t)cta * A.I);
+      T.b_sft[0] = g_row / 128;
+      T.b_sft[1] = (g_row + A.I) / 128;
+      T.out_col0 = (int64_t)nt * 128;
+    } else {
+      T.b_row = e * nb + nt * BN + (BN / 2) * cta;
+      T.b_sft[0] = ((int64_t)e * nb + (int64_t)nt * BN) / 128;
+      T.b_sft[1] = T.b_sft[0] + 1;
+      T.out_col0 = (int64_t)nt * BN;
+    }
+    T.nk = (int)(kFwd ? A.K / 256 : A.N / 128);
     T.k_off = 0;
     T.k_atom0 = 0;
     T.out_row0 = T.a_row;
-    T.out_col0 = (int64_t)nt * BN;
   } else {
     const int per_e = A.ntm * A.ntn;
     const int d = dw_sorted_index(t, pair, npairs, num_tiles);
@@ -859,7 +893,8 @@ __device__ __forceinline__ PairTile decode_pair(int t, const GemmArgs &A, const 
     T.nk = (s_pad[e + 1] - s_pad[e]) / 128;
     T.k_off = s_pad[e];
     T.a_tile = T.a_row / 128;
-    T.b_tile0 = (int64_t)nt * (BN / 128);
+    T.b_sft[0] = (int64_t)nt * (BN / 128);
+    T.b_sft[1] = T.b_sft[0] + 1;
     T.k_atom0 = s_pad[e] / 128;
     T.out_row0 = (int64_t)e * A.N + T.a_row;
     T.out_col0 = (int64_t)nt * BN;
@@ -902,6 +937,36 @@ __device__ __forceinline__ bool wait_pair(uint32_t bar, uint32_t parity, uint64_
   return false;
 }
 
+// The scale copies of one ring stage into its tensor-memory buffer: the A
+// tiles (4 columns each) then the B tiles of each k-atom, numbered in that
+// order over the stage's chunks; `part` < 0 issues all of them, else issuer
+// `part` issues those with (number % kSfWarps) == part.
+template <class C, int BN, int CHUNKS>
+__device__ __forceinline__ void issue_stage_sf_copies(uint32_t tmem, uint32_t s, int nc, uint32_t a_sf_stage,
+                                                      uint32_t b_sf_stage, int part) {
+  constexpr int kParts = C::kSfWarps > 0 ? C::kSfWarps : 1;
+  int k = 0;
+#pragma unroll
+  for (int c = 0; c < CHUNKS; ++c) {
+    if (c >= nc) break;
+    const uint32_t sfa = tmem + C::ACC_COLS + s * C::SF_COLS + c * C::SF_CHUNK_COLS;
+    const uint32_t sfb = sfa + C::SFA_COLS;
+    const uint32_t a_sf_smem = a_sf_stage + c * C::SFA_CHUNK;
+    const uint32_t b_sf_smem = b_sf_stage + c * C::SFB_CHUNK;
+#pragma unroll
+    for (int j = 0; j < C::kAtomsPerStage; ++j) {
+      if (part < 0 || k % kParts == part) tc_cp_sf_pair(sfa + 4 * j, desc_sf(a_sf_smem + j * 512));
+      ++k;
+#pragma unroll
+      for (int r = 0; r < C::kSfbTiles; ++r) {
+        if (part < 0 || k % kParts == part)
+          tc_cp_sf_pair(sfb + j * (BN / 32) + 4 * r, desc_sf(b_sf_smem + r * C::SFA_CHUNK + j * 512));
+        ++k;
+      }
+    }
+  }
+}
+
 template <int KIND, int STAGES, int BN, int CHUNKS>
 __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BN, CHUNKS>::kThreads,
                                   CfgPair<KIND, STAGES, BN, CHUNKS>::kCtasPerSm)
@@ -936,12 +1001,20 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BN, CHUNKS>::kThreads,
 
   uint64_t *full = bars, *empty = bars + STAGES, *acc_full = bars + 2 * STAGES, *acc_empty = acc_full + 1;
   uint64_t *mma_done = acc_empty + 1;
+  // with copy issuers: sf_land (a stage's scale tiles have landed, loaded
+  // ahead of its operand tiles), sf_full (they are in tensor memory), sf_done
+  uint64_t *sf_full = mma_done + 1, *sf_land = sf_full + STAGES, *sf_done = sf_land + STAGES;
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(mma_done), 1);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
       mbar_init(smem_u32(&empty[s]), 1);
+      if (C::kSfWarps) {
+        mbar_init(smem_u32(&sf_full[s]), C::kSfWarps);  // one commit per issuer
+        mbar_init(smem_u32(&sf_land[s]), 1);
+      }
     }
+    for (int w = 0; w < C::kSfWarps; ++w) mbar_init(smem_u32(&sf_done[w]), 1);
     mbar_init(smem_u32(acc_full), 1);
     mbar_init(smem_u32(acc_empty), 2 * C::kEpiWarps);  // every epilogue warp of both CTAs
     *s_abort = 0;
@@ -975,25 +1048,40 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BN, CHUNKS>::kThreads,
         }
         const uint32_t fb_local = smem_u32(&full[s]);
         const uint32_t fb = cta == 0 ? fb_local : mapa_shared(fb_local, 0);
-        if (cta == 0) mbar_arrive_expect_tx(fb_local, 2 * nc * C::CHUNK_BYTES);
+        // with copy issuers the scale tiles go first, on their own barrier,
+        // so that their copies to tensor memory overlap the operand loads
+        const uint32_t sb_local = C::kSfWarps ? smem_u32(&sf_land[s]) : fb_local;
+        const uint32_t sb = cta == 0 ? sb_local : mapa_shared(sb_local, 0);
+        constexpr int kSfBytes = C::SFA_CHUNK + C::SFB_CHUNK;
+        if (cta == 0) {
+          if (C::kSfWarps) {
+            mbar_arrive_expect_tx(sb_local, 2 * nc * kSfBytes);
+            mbar_arrive_expect_tx(fb_local, 2 * nc * (C::CHUNK_BYTES - kSfBytes));
+          } else {
+            mbar_arrive_expect_tx(fb_local, 2 * nc * C::CHUNK_BYTES);
+          }
+        }
+        for (int c = 0; c < nc; ++c) {
+          const int64_t katom = T.k_atom0 + (int64_t)(ks + c) * C::kAtomsPerStage;
+          tma_load_2d_pair(smem_u32(sSFA + s * C::SFA_BYTES + c * C::SFA_CHUNK), &tmSA, 0,
+                           (int)((T.a_tile * A.ka + katom) * 4), sb);
+#pragma unroll
+          for (int j = 0; j < C::kSfbTiles; ++j)
+            tma_load_2d_pair(smem_u32(sSFB + s * C::SFB_BYTES + c * C::SFB_CHUNK + j * C::SFA_CHUNK), &tmSB, 0,
+                             (int)((T.b_sft[j] * A.ka + katom) * 4), sb);
+        }
         for (int c = 0; c < nc; ++c) {
           const int k = ks + c;
           tma_load_2d_pair(smem_u32(sA + s * C::A_BYTES + c * C::A_CHUNK), &tmA, T.k_off + k * 128, T.a_row, fb);
           tma_load_2d_pair(smem_u32(sB + s * C::B_BYTES + c * C::B_CHUNK), &tmB, T.k_off + k * 128, T.b_row, fb);
-          const int64_t katom = T.k_atom0 + (int64_t)k * C::kAtomsPerStage;
-          tma_load_2d_pair(smem_u32(sSFA + s * C::SFA_BYTES + c * C::SFA_CHUNK), &tmSA, 0,
-                           (int)((T.a_tile * A.ka + katom) * 4), fb);
-#pragma unroll
-          for (int j = 0; j < C::kSfbTiles; ++j)
-            tma_load_2d_pair(smem_u32(sSFB + s * C::SFB_BYTES + c * C::SFB_CHUNK + j * C::SFA_CHUNK), &tmSB, 0,
-                             (int)(((T.b_tile0 + j) * A.ka + katom) * 4), fb);
         }
       }
     }
     if (cta == 0) {  // the even CTA's barriers count both CTAs' bytes: wait for the last copies
       const uint32_t first = it > STAGES ? it - STAGES : 0;
       for (uint32_t k = first; k < it; ++k)
-        if (!mbar_wait(smem_u32(&full[k % STAGES]), (k / STAGES) & 1, kDrainLimit)) {
+        if (!mbar_wait(smem_u32(&full[k % STAGES]), (k / STAGES) & 1, kDrainLimit) ||
+            (C::kSfWarps && !mbar_wait(smem_u32(&sf_land[k % STAGES]), (k / STAGES) & 1, kDrainLimit))) {
           record_error(A.status, NV_ERR_TIMEOUT);
           break;
         }
@@ -1010,25 +1098,21 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BN, CHUNKS>::kThreads,
       for (int ks = 0; ks < T.nk; ks += CHUNKS, ++it) {
         const uint32_t s = it % STAGES;
         const int nc = T.nk - ks < CHUNKS ? T.nk - ks : CHUNKS;
-        if (!wait_pair(smem_u32(&full[s]), (it / STAGES) & 1, A.wait_limit, s_abort, peer_abort, A.status)) {
+        if (!wait_pair(smem_u32(&full[s]), (it / STAGES) & 1, A.wait_limit, s_abort, peer_abort, A.status) ||
+            (C::kSfWarps &&
+             !wait_pair(smem_u32(&sf_full[s]), (it / STAGES) & 1, A.wait_limit, s_abort, peer_abort, A.status))) {
           ok = false;
           break;
         }
         tc_fence_after();
+        if (!C::kSfWarps)
+          issue_stage_sf_copies<C, BN, CHUNKS>(tmem, s, nc, smem_u32(sSFA + s * C::SFA_BYTES),
+                                               smem_u32(sSFB + s * C::SFB_BYTES), -1);
 #pragma unroll
         for (int c = 0; c < CHUNKS; ++c) {
           if (c >= nc) break;
           const uint32_t sfa = tmem + C::ACC_COLS + s * C::SF_COLS + c * C::SF_CHUNK_COLS;
           const uint32_t sfb = sfa + C::SFA_COLS;
-          const uint32_t a_sf_smem = smem_u32(sSFA + s * C::SFA_BYTES + c * C::SFA_CHUNK);
-          const uint32_t b_sf_smem = smem_u32(sSFB + s * C::SFB_BYTES + c * C::SFB_CHUNK);
-#pragma unroll
-          for (int j = 0; j < C::kAtomsPerStage; ++j) {
-            tc_cp_sf_pair(sfa + 4 * j, desc_sf(a_sf_smem + j * 512));
-#pragma unroll
-            for (int r = 0; r < C::kSfbTiles; ++r)
-              tc_cp_sf_pair(sfb + j * (BN / 32) + 4 * r, desc_sf(b_sf_smem + r * C::SFA_CHUNK + j * 512));
-          }
           const uint64_t da = desc_sw128(smem_u32(sA + s * C::A_BYTES + c * C::A_CHUNK));
           const uint64_t db = desc_sw128(smem_u32(sB + s * C::B_BYTES + c * C::B_CHUNK));
           if (C::kFp4) {  // K = 96, 96, 64 per 128-byte row, as in the one-CTA kernel
@@ -1054,10 +1138,41 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BN, CHUNKS>::kThreads,
     // pass the cluster barrier below first)
     tc_commit_pair_local(smem_u32(mma_done));
     if (!mbar_wait(smem_u32(mma_done), 0, kDrainLimit)) record_error(A.status, NV_ERR_TIMEOUT);
-  } else if (warp >= 2) {
+  } else if (warp >= 2 && warp < C::kEpi0) {
+    // ---- scale-copy issuers (even CTA only) ------------------------------------------
+    // each stage, once its scale tiles have landed: this issuer's half of
+    // the stage's copies, then a commit on the stage's sf_full barrier, which
+    // completes when both halves have been written to tensor memory.  A
+    // stage's buffer is rewritten only after its refill has landed, i.e.
+    // after the MMAs that read it have completed (the producer refills a
+    // stage after its MMAs' commit).
+    if (lane == 0 && cta == 0) {
+      const int part = warp - 2;
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = pair; ok && t < num_tiles; t += npairs) {
+        const PairTile T = decode_pair<KIND, BN>(t, A, s_off, s_pad, s_pb, s_ord, pair, npairs, num_tiles, 0);
+        for (int ks = 0; ks < T.nk; ks += CHUNKS, ++it) {
+          const uint32_t s = it % STAGES;
+          const int nc = T.nk - ks < CHUNKS ? T.nk - ks : CHUNKS;
+          if (!wait_pair(smem_u32(&sf_land[s]), (it / STAGES) & 1, A.wait_limit, s_abort, peer_abort, A.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_stage_sf_copies<C, BN, CHUNKS>(tmem, s, nc, smem_u32(sSFA + s * C::SFA_BYTES),
+                                               smem_u32(sSFB + s * C::SFB_BYTES), part);
+          tc_commit_pair_local(smem_u32(&sf_full[s]));
+        }
+      }
+      // every copy this thread issued has landed before tensor memory is freed
+      tc_commit_pair_local(smem_u32(&sf_done[part]));
+      if (!mbar_wait(smem_u32(&sf_done[part]), 0, kDrainLimit)) record_error(A.status, NV_ERR_TIMEOUT);
+    }
+  } else if (warp >= C::kEpi0) {
     // ---- epilogue (both CTAs): BN / 32 warps, 128 columns each ------------------------
     const int q = warp & 3;
-    const int half = (warp - 2) >> 2;
+    const int half = (warp - C::kEpi0) >> 2;
     const int row = q * 32 + lane;
     const uint32_t acc_empty_addr = cta == 0 ? smem_u32(acc_empty) : mapa_shared(smem_u32(acc_empty), 0);
     uint32_t tc = 0;
@@ -1068,13 +1183,21 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BN, CHUNKS>::kThreads,
       const bool store = row < T.mrows;
       const int64_t orow = T.out_row0 + row;
       float alpha = 1.0f;
-      if (KIND == kGemmNvfp4Fwd) alpha = __fmul_rn(A.a_sg_rows ? (store ? A.a_sg[orow] : 0.0f) : A.a_sg[0], A.b_sg[T.e]);
+      if (C::kFp4) alpha = __fmul_rn(A.a_sg_rows ? (store ? A.a_sg[orow] : 0.0f) : A.a_sg[0], A.b_sg[T.e]);
       const int64_t ocol = T.out_col0 + half * 128;
       uint32_t r[128];
       if (T.nk > 0) {
-        const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(half * 128);
+        const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16);
+        if (KIND == kGemmNvfp4FwdSwiglu) {  // gate columns half*64 .. +63, then the matching up columns
 #pragma unroll
-        for (int c0 = 0; c0 < 128; c0 += 32) tmem_ld32_nowait(tb + (uint32_t)c0, &r[c0]);
+          for (int c0 = 0; c0 < 64; c0 += 32) {
+            tmem_ld32_nowait(tb + (uint32_t)(half * 64 + c0), &r[c0]);
+            tmem_ld32_nowait(tb + (uint32_t)(128 + half * 64 + c0), &r[64 + c0]);
+          }
+        } else {
+#pragma unroll
+          for (int c0 = 0; c0 < 128; c0 += 32) tmem_ld32_nowait(tb + (uint32_t)(half * 128 + c0), &r[c0]);
+        }
         tmem_wait_ld();
       } else {
 #pragma unroll
@@ -1088,7 +1211,9 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BN, CHUNKS>::kThreads,
         else
           mbar_arrive_cluster(acc_empty_addr);
       }
-      if (KIND == kGemmMxfp8Dw && A.out_fp32) {
+      if (KIND == kGemmNvfp4FwdSwiglu) {
+        swiglu_epilogue(A, r, alpha, store, orow, T.out_col0 + half * 64, lane);
+      } else if (KIND == kGemmMxfp8Dw && A.out_fp32) {
         // wgrad: fp32 dW rows are 512 bytes per lane and the stores are the
         // epilogue's bottleneck, so the warp writes them as whole lines (the
         // tile's 128 rows all exist; alpha is 1)
@@ -1125,6 +1250,9 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BN, CHUNKS>::kThreads,
       }
     }
   }
+  // single-lane roles rejoin their warps first: an aligned barrier reached
+  // by part of a warp must not let the CTA (or its peer) move on
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   cluster_sync_all();  // no CTA leaves while its peer may still signal it or read its shared memory
@@ -1325,13 +1453,12 @@ int launch_grouped_gemm(const GemmProblem &p, int *status, cudaStream_t s) {
   // variants: 1 one CTA per SM with two accumulators (6 stages); 2 two CTAs
   // per SM with one accumulator each (3 stages); 3 CTA pairs with 256 x 256
   // tiles; 4 CTA pairs with 256 x 128 tiles, two pairs per SM pair.  A pair
-  // variant applies where the shape allows it (else 2).  Automatic, from
-  // measurements at the MoE shapes (16384 tokens, PFLOP/s, variants 2 / 3 / 4):
-  // NVFP4 forward 4.13 / 3.31 / 3.96 -> 2; MXFP8 dgrad 2.54 / 2.72 / 2.71 and
-  // wgrad 1.90 / 2.24 / 2.14 -> 3 when the experts hold several 128-row blocks
-  // (a half-empty pair block wastes half of its MMAs), else 2.
-  if (p.kind == kGemmNvfp4FwdSwiglu)  // one kernel: 128 x (64 gate + 64 up), two CTAs per SM
-    return run<kGemmNvfp4FwdSwiglu, 3, 1>(ta, tb, a, max_tiles, s);
+  // variant applies where the shape allows it (else 2).  Automatic: 3 when the
+  // experts hold several 128-row blocks (a half-empty pair block wastes half
+  // of its MMAs), else 2.  Measured at the MoE shapes (16384 tokens, 64
+  // experts, ms, variants 2 / 3): NVFP4 forward w13 0.78 / 0.68, w2 0.48 /
+  // 0.42; MXFP8 dgrad and wgrad faster with 3 as well.  The SwiGLU kind has
+  // no 256 x 128 pair form (its 64 gate + 64 up rows would split scale tiles).
   if (p.s2f6_codes)  // the RHT + S2F6 epilogue exists in the 128 x 128 kernel only
     return run<kGemmNvfp4Fwd, 3, 1, true>(ta, tb, a, max_tiles, s);
   const int forced = gemm_variant();
@@ -1340,15 +1467,18 @@ int launch_grouped_gemm(const GemmProblem &p, int *status, cudaStream_t s) {
   int pair_bn = 0;
   if (forced == 3 || forced == 4) {
     pair_bn = forced == 3 ? 256 : 128;
-  } else if (forced == 0 && big_groups && p.kind != kGemmNvfp4Fwd) {
+  } else if (forced == 0 && big_groups) {
     pair_bn = 256;
   }
   if (pair_bn && (!rows_ok || out_cols % pair_bn)) pair_bn = 0;
+  if (p.kind == kGemmNvfp4FwdSwiglu && pair_bn != 256)  // 128 x (64 gate + 64 up), two CTAs per SM
+    return run<kGemmNvfp4FwdSwiglu, 3, 1>(ta, tb, a, max_tiles, s);
   if (pair_bn) {
-    const int atoms = p.kind == kGemmNvfp4Fwd ? 4 : 1;
+    const int atoms = (p.kind == kGemmNvfp4Fwd || p.kind == kGemmNvfp4FwdSwiglu) ? 4 : 1;
     uint64_t a_sf_bytes, b_sf_bytes;
     switch (p.kind) {
       case kGemmNvfp4Fwd:
+      case kGemmNvfp4FwdSwiglu:
         a_sf_bytes = (uint64_t)(P / 128) * a.ka * 512;
         b_sf_bytes = (uint64_t)(p.E * p.N / 128) * a.ka * 512;
         break;
@@ -1365,7 +1495,10 @@ int launch_grouped_gemm(const GemmProblem &p, int *status, cudaStream_t s) {
     if (!make_sf_map(&tsa, p.a_scales, a_sf_bytes, 4 * atoms) || !make_sf_map(&tsb, p.b_scales, b_sf_bytes, 4 * atoms))
       return NV_ERR_CUDA;
     const CUtensorMap *tbp = &tb;  // B box of BN / 2 rows
-    if (pair_bn == 128) {
+    if (p.kind == kGemmNvfp4FwdSwiglu) {  // 128 gate or up rows per CTA
+      if (!make_map(&tbh, p.b_codes, p.K / 2, (uint64_t)p.E * p.N, p.K / 2, 128)) return NV_ERR_CUDA;
+      tbp = &tbh;
+    } else if (pair_bn == 128) {
       switch (p.kind) {
         case kGemmNvfp4Fwd: ok = make_map(&tbh, p.b_codes, p.K / 2, (uint64_t)p.E * p.N, p.K / 2, 64); break;
         case kGemmMxfp8Dx: ok = make_map(&tbh, p.b_codes, p.N, (uint64_t)p.E * p.K, p.N, 64); break;
@@ -1386,6 +1519,8 @@ int launch_grouped_gemm(const GemmProblem &p, int *status, cudaStream_t s) {
     if (pair_bn == 256) {
       switch (p.kind) {
         case kGemmNvfp4Fwd: return run_pair<kGemmNvfp4Fwd, 5, 256>(ta, *tbp, tsa, tsb, b, pair_tiles, s);
+        case kGemmNvfp4FwdSwiglu:
+          return run_pair<kGemmNvfp4FwdSwiglu, 5, 256>(ta, *tbp, tsa, tsb, b, pair_tiles, s);
         case kGemmMxfp8Dx: return run_pair<kGemmMxfp8Dx, 3, 256, 2>(ta, *tbp, tsa, tsb, b, pair_tiles, s);
         default: return run_pair<kGemmMxfp8Dw, 3, 256, 2>(ta, *tbp, tsa, tsb, b, pair_tiles, s);
       }

@@ -21,9 +21,19 @@ def _rand(shape, seed, std):
     return (torch.randn(shape, generator=g, device="cuda") * std).to(torch.bfloat16).contiguous()
 
 
+@pytest.fixture(params=[N.GEMM_AUTO, N.GEMM_TWO_PER_SM, N.GEMM_CTA_PAIR], ids=["auto", "two_per_sm", "cta_pair"])
+def gemm_kernel(request):
+    """The fused epilogue exists in the 128 x 128 kernel and in the CTA-pair
+    kernel (128 gate + 128 up rows per pair tile); both must match the
+    unfused sequence run with the same kernel choice."""
+    N.nvfp4moe_set_gemm_kernel(request.param)
+    yield request.param
+    N.nvfp4moe_set_gemm_kernel(N.GEMM_AUTO)
+
+
 @pytest.mark.parametrize("sizes,I,K", [([300], 128, 256), ([5, 0, 295, 130, 1], 256, 512), ([0, 700, 0], 384, 256),
-                                       ([128, 128], 1536, 1024)])
-def test_fused_swiglu_equals_unfused(sizes, I, K):
+                                       ([128, 128], 1536, 1024), ([600, 1, 0, 257, 513], 256, 512)])
+def test_fused_swiglu_equals_unfused(sizes, I, K, gemm_kernel):
     o = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
     go = torch.from_numpy(o).to(dev())
     M, E = int(o[-1]), len(sizes)

@@ -134,8 +134,18 @@ def _weights(E, n, k, seed):
     return wq
 
 
+@pytest.fixture(params=[N.GEMM_AUTO, N.GEMM_CTA_PAIR], ids=["auto", "cta_pair"])
+def gemm_kernel(request):
+    """Per-token outer scales in the 128 x 128 kernel's epilogue and in the
+    CTA-pair kernel's (shapes whose width is not a multiple of 256 fall back
+    to the former)."""
+    N.nvfp4moe_set_gemm_kernel(request.param)
+    yield request.param
+    N.nvfp4moe_set_gemm_kernel(N.GEMM_AUTO)
+
+
 @pytest.mark.parametrize("sizes,N_,K", [([37, 0, 200, 128], 256, 512), ([300, 1], 128, 256)])
-def test_fwd_gemm_rows_within_bound(sizes, N_, K):
+def test_fwd_gemm_rows_within_bound(sizes, N_, K, gemm_kernel):
     go, o = _groups(sizes)
     M, E = int(o[-1]), len(sizes)
     x = _x(M, K, seed=M + K)
@@ -154,7 +164,7 @@ def test_fwd_gemm_rows_within_bound(sizes, N_, K):
     assert G.within_bound(y.cpu().numpy(), ref, bound).all()
 
 
-def test_swiglu_rows_epilogue():
+def test_swiglu_rows_epilogue(gemm_kernel):
     sizes, I, K = [40, 0, 300, 129], 128, 512
     go, o = _groups(sizes)
     M, E = int(o[-1]), len(sizes)
