@@ -687,6 +687,14 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       "l"(map), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
+__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap *map, int x, int y, int z, int w,
+                                                 uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+      "%4, %5}], [%6];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+      : "memory");
+}
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t slot, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(ncols)
                : "memory");
@@ -1065,10 +1073,13 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BN, CHUNKS>::kThreads,
           const int64_t katom = T.k_atom0 + (int64_t)(ks + c) * C::kAtomsPerStage;
           tma_load_2d_pair(smem_u32(sSFA + s * C::SFA_BYTES + c * C::SFA_CHUNK), &tmSA, 0,
                            (int)((T.a_tile * A.ka + katom) * 4), sb);
-#pragma unroll
-          for (int j = 0; j < C::kSfbTiles; ++j)
-            tma_load_2d_pair(smem_u32(sSFB + s * C::SFB_BYTES + c * C::SFB_CHUNK + j * C::SFA_CHUNK), &tmSB, 0,
-                             (int)((T.b_sft[j] * A.ka + katom) * 4), sb);
+          if (C::kSfbTiles == 2) {  // both scale tiles of the B rows in one load (tmSB: 4-D view)
+            tma_load_4d_pair(smem_u32(sSFB + s * C::SFB_BYTES + c * C::SFB_CHUNK), &tmSB, 0, (int)(katom * 4), 0,
+                             (int)T.b_sft[0], sb);
+          } else {
+            tma_load_2d_pair(smem_u32(sSFB + s * C::SFB_BYTES + c * C::SFB_CHUNK), &tmSB, 0,
+                             (int)((T.b_sft[0] * A.ka + katom) * 4), sb);
+          }
         }
         for (int c = 0; c < nc; ++c) {
           const int k = ks + c;
@@ -1305,6 +1316,24 @@ static bool make_sf_map(CUtensorMap *m, const void *base, uint64_t bytes, uint32
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The B scale buffer as [tile][pair member z][ka * 4 rows of 128 bytes]:
+// element (x, y, z, w) is byte x of row y of scale tile w + z * gap, so one
+// box {128, rows, 2, 1} loads the same rows of two tiles `gap` tiles apart
+// (consecutive tiles, or the gate and up tiles of the SwiGLU kind).
+static bool make_sf_map_pair(CUtensorMap *m, const void *base, uint64_t n_tiles, uint64_t ka, uint64_t gap,
+                             uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn || n_tiles <= gap) return false;
+  const uint64_t tile_bytes = ka * 512;
+  cuuint64_t dims[4] = {128, ka * 4, 2, n_tiles - gap};
+  cuuint64_t strides[3] = {128, gap * tile_bytes, tile_bytes};
+  cuuint32_t box[4] = {128, box_rows, 2, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 static int num_sms() {
   static int n[64] = {};
   int dev = 0;
@@ -1492,7 +1521,11 @@ int launch_grouped_gemm(const GemmProblem &p, int *status, cudaStream_t s) {
         break;
     }
     CUtensorMap tsa, tsb, tbh;
-    if (!make_sf_map(&tsa, p.a_scales, a_sf_bytes, 4 * atoms) || !make_sf_map(&tsb, p.b_scales, b_sf_bytes, 4 * atoms))
+    // 256-wide tiles take two B scale tiles per k-atom, one 4-D load
+    const uint64_t sf_gap = p.kind == kGemmNvfp4FwdSwiglu ? (uint64_t)(p.N / 2) / 128 : 1;
+    if (!make_sf_map(&tsa, p.a_scales, a_sf_bytes, 4 * atoms) ||
+        !(pair_bn == 256 ? make_sf_map_pair(&tsb, p.b_scales, b_sf_bytes / (a.ka * 512), a.ka, sf_gap, 4 * atoms)
+                         : make_sf_map(&tsb, p.b_scales, b_sf_bytes, 4 * atoms)))
       return NV_ERR_CUDA;
     const CUtensorMap *tbp = &tb;  // B box of BN / 2 rows
     if (p.kind == kGemmNvfp4FwdSwiglu) {  // 128 gate or up rows per CTA
