@@ -462,7 +462,7 @@ def run_ours(args):
                 "overlap": "copies in (step i+1) and out (step i-1) on their own streams during step i",
                 "inputs": ("tokens x [16384 x 4096] bf16, the routed rows' source tokens (int32), g2 per routed row"
                            if layer.gathers_rows else "routed rows x [T*k x 4096] bf16, g2 per routed row")},
-        "gpu_launches": layer.launches_per_step() * args.steps,
+        "gpu_launches": layer.launches_per_step(gathered=layer.gathers_rows, tokens=m.x.shape[0]) * args.steps,
         "peaks": peaks,
         "cpu_baseline": cpu,
         "configs": configs,

@@ -399,14 +399,18 @@ class MoELayer:
         torch.cuda.synchronize()
         return g
 
-    def launches_per_step(self):
+    def launches_per_step(self, gathered=False, tokens=None):
         """Kernels one step launches: forward = 4 NVFP4 quantizations x 3
         kernels (amax, finalize, quantize or quantize + requant) + 2 GEMMs +
         SwiGLU, or with the SwiGLU epilogue: 3 x 3 + the fused GEMM, the
         outer-scale kernel and one kernel for h + the w2 GEMM; backward = (4
         requants unless fused) + 2 MXFP8 quantizations + 4 GEMMs + SwiGLU
-        backward."""
+        backward.  `gathered`: x given as tokens + row map; its amax pass adds
+        the tokens' row-maximum kernel when there are no more tokens than
+        routed rows."""
         fwd = (3 * 3 + 2 + 1 + 1) if self.fuse_swiglu else (4 * 3 + 2 + 1)
+        if gathered and (tokens is None or tokens <= self.M):
+            fwd += 1
         # (with the side-stream amax passes the same kernels run, the amax ones on the side stream)
         if self.per_token:  # x: row amax + quantize; h: from the epilogue's row scales (1) or row amax + quantize
             fwd = (2 + 2 * 3 + 2 + 1 + 1) if self.fuse_swiglu else (2 + 2 * 3 + 2 + 2 + 1)
