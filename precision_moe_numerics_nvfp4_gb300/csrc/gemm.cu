@@ -687,6 +687,22 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       "l"(map), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap *map, int x, int y, int z,
+                                                 uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+      "%4}], [%5];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_5d_pair(uint32_t dst, const CUtensorMap *map, int x, int y, int z, int w,
+                                                 int v, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+      "%4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(w), "r"(v), "r"(bar)
+      : "memory");
+}
 __device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap *map, int x, int y, int z, int w,
                                                  uint32_t bar) {
   asm volatile(
@@ -800,6 +816,13 @@ struct CfgPair {
   static constexpr int kSfWarps = kCtasPerSm == 1 ? 2 : 0;
   static constexpr int NBARS = 2 * STAGES + 3 + (kSfWarps ? 2 * STAGES + kSfWarps : 0);
   static constexpr int kEpi0 = 2 + kSfWarps;            // first epilogue warp
+  // Wide loads (two-chunk stages with copy issuers): a stage's two k-chunks
+  // come in one load per tensor (A, B: 3-D boxes of two 128-byte k-chunks;
+  // A scales: the two chunks' rows; B scales: a 5-D box [chunk][tile][rows]),
+  // four loads a stage instead of eight -- a thread issuing TMA loads gets
+  // about 46 B/clk whatever the box size.  A stage holding one chunk (the
+  // last of an odd count) still loads two; the second is not used.
+  static constexpr bool kWideLoads = CHUNKS == 2 && kSfWarps > 0;
   static constexpr int kEpiWarps = BN / 32;             // per lane quadrant: BN / 128 warps of 128 columns
   static constexpr int kThreads = 32 * (kEpi0 + kEpiWarps);
   static constexpr uint32_t IDESC = (kFp4 ? ((1u << 7) | (1u << 10)) : (1u << 23)) |
@@ -1053,6 +1076,20 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BN, CHUNKS>::kThreads,
             !wait_pair(smem_u32(&empty[s]), ((it / STAGES) - 1) & 1, A.wait_limit, s_abort, peer_abort, A.status)) {
           ok = false;
           break;
+        }
+        if constexpr (C::kWideLoads) {
+          const uint32_t f0 = smem_u32(&full[s]), l0 = smem_u32(&sf_land[s]);
+          if (cta == 0) {
+            mbar_arrive_expect_tx(l0, 2 * 2 * (C::SFA_CHUNK + C::SFB_CHUNK));
+            mbar_arrive_expect_tx(f0, 2 * 2 * (C::A_CHUNK + C::B_CHUNK));
+          }
+          const uint32_t lb = cta == 0 ? l0 : mapa_shared(l0, 0), fb = cta == 0 ? f0 : mapa_shared(f0, 0);
+          const int64_t katom = T.k_atom0 + (int64_t)ks * C::kAtomsPerStage;
+          tma_load_2d_pair(smem_u32(sSFA + s * C::SFA_BYTES), &tmSA, 0, (int)((T.a_tile * A.ka + katom) * 4), lb);
+          tma_load_5d_pair(smem_u32(sSFB + s * C::SFB_BYTES), &tmSB, 0, 0, 0, (int)katom, (int)T.b_sft[0], lb);
+          tma_load_3d_pair(smem_u32(sA + s * C::A_BYTES), &tmA, 0, T.a_row, T.k_off / 128 + ks, fb);
+          tma_load_3d_pair(smem_u32(sB + s * C::B_BYTES), &tmB, 0, T.b_row, T.k_off / 128 + ks, fb);
+          continue;
         }
         const uint32_t fb_local = smem_u32(&full[s]);
         const uint32_t fb = cta == 0 ? fb_local : mapa_shared(fb_local, 0);
@@ -1334,6 +1371,35 @@ static bool make_sf_map_pair(CUtensorMap *m, const void *base, uint64_t n_tiles,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Wide-load views: codes as [k-chunk][row][128 bytes] (box of two k-chunks,
+// 128-byte swizzle), and B scales as [tile][k-chunk][pair member][rows of
+// one chunk][128 bytes] (box: both members' rows of two k-chunks).
+static bool make_map_chunks(CUtensorMap *m, const void *base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {128, rows, row_bytes / 128};
+  cuuint64_t strides[2] = {row_bytes, 128};
+  cuuint32_t box[3] = {128, box_rows, 2};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+static bool make_sf_map_pair_chunks(CUtensorMap *m, const void *base, uint64_t n_tiles, uint64_t ka, uint64_t gap,
+                                    uint32_t chunk_rows) {
+  auto fn = encode_fn();
+  const uint64_t rows = ka * 4;  // 128-byte rows of one tile's scale block
+  if (!fn || n_tiles <= gap || rows % chunk_rows) return false;
+  const uint64_t tile_bytes = ka * 512;
+  cuuint64_t dims[5] = {128, chunk_rows, 2, rows / chunk_rows, n_tiles - gap};
+  cuuint64_t strides[4] = {128, gap * tile_bytes, (uint64_t)chunk_rows * 128, tile_bytes};
+  cuuint32_t box[5] = {128, chunk_rows, 2, 2, 1};
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void *>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 static int num_sms() {
   static int n[64] = {};
   int dev = 0;
@@ -1548,6 +1614,20 @@ int launch_grouped_gemm(const GemmProblem &p, int *status, cudaStream_t s) {
       pair_tiles = (int64_t)p.E * b.ntm * b.ntn;
     } else {
       pair_tiles = ((P / 128 + p.E) / 2) * b.ntn;  // upper bound of sum_e ceil(P_e / 256) tiles
+    }
+    if (pair_bn == 256 && (p.kind == kGemmMxfp8Dx || p.kind == kGemmMxfp8Dw)) {
+      // two-chunk stages with wide loads (see CfgPair::kWideLoads)
+      const bool dx = p.kind == kGemmMxfp8Dx;
+      const uint64_t row_bytes = dx ? (uint64_t)p.N : (uint64_t)P;
+      const uint64_t a_rows = dx ? (uint64_t)p.M_total : (uint64_t)p.N;
+      const uint64_t b_rows = dx ? (uint64_t)p.E * p.K : (uint64_t)p.K;
+      CUtensorMap wa, wb, wsa, wsb;
+      if (!make_map_chunks(&wa, p.a_codes, row_bytes, a_rows, 128) ||
+          !make_map_chunks(&wb, p.b_codes, row_bytes, b_rows, 128) || !make_sf_map(&wsa, p.a_scales, a_sf_bytes, 8) ||
+          !make_sf_map_pair_chunks(&wsb, p.b_scales, b_sf_bytes / (a.ka * 512), a.ka, 1, 4))
+        return NV_ERR_CUDA;
+      return dx ? run_pair<kGemmMxfp8Dx, 3, 256, 2>(wa, wb, wsa, wsb, b, pair_tiles, s)
+                : run_pair<kGemmMxfp8Dw, 3, 256, 2>(wa, wb, wsa, wsb, b, pair_tiles, s);
     }
     if (pair_bn == 256) {
       switch (p.kind) {
