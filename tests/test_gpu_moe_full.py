@@ -1,7 +1,8 @@
 """Full-size, stage-wise parity of one MoE expert layer step (forward and
 backward) at the benchmark workload: 16384 tokens x top-8 = 131072 rows,
 d_model 4096, d_ff 1536, 64 experts with uneven groups.  The step runs exactly
-as bench.py times it; afterwards sampled outputs of every stage are compared
+as bench.py times it (the tokens and the routing map in, the routed rows
+gathered by the quantization of x); afterwards sampled outputs of every stage are compared
 with the oracle fed the GPU's own input to that stage:
 codes / scales / outer scales bit-exact (stochastic rounding included), GEMM
 outputs within 1e-4 (|A||B|) (+ half a bf16 ulp), SwiGLU within a bf16 ulp.
@@ -58,7 +59,10 @@ def run():
         mp.setattr(PL, "_u8", lambda n, dev: gh.guarded_bytes(max(int(n), 16)))
         mp.setattr(PL, "_empty", lambda shape, dtype, dev: gh.gempty(shape, dtype=dtype, device=dev))
         layer = PL.MoELayer(M, D, I, E)
-    layer.step(m.x_perm, m.w13, m.w2, m.g2, m.group_offsets, seed=SEED)
+    # the tokens and the routing map, as bench.py runs it: the quantization of
+    # x gathers the routed rows (m.x_perm, which the oracle side reads)
+    assert layer.gathers_rows
+    layer.step(m.x, m.w13, m.w2, m.g2, m.group_offsets, seed=SEED, x_rows=m.rows)
     torch.cuda.synchronize()
     assert N.nvfp4moe_get_device_status() == 0
     gh.check_guards()
