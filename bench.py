@@ -230,13 +230,14 @@ class EventLog:
         return out
 
 
-def build_step(layer, m, log: EventLog | None):
-    """Returns step() running the whole path; with `log`, each call is bracketed by events."""
+def build_step(layer, m, log: EventLog | None, only: str | None = None):
+    """Returns step() running the whole path; with `log`, each call (or each
+    call of the entry point `only`) is bracketed by events."""
     from precision_moe_numerics_nvfp4_gb300 import nvfp4moe as N
     from precision_moe_numerics_nvfp4_gb300 import pipeline as PL
 
     def wrap(name, fn):
-        if log is None:
+        if log is None or (only is not None and name != only):
             return fn
         return lambda *a, **k: log.call(name, fn, *a, **k)
 
@@ -364,9 +365,21 @@ def run_ours(args):
     if st != 0:
         raise RuntimeError(f"device status {st} after warm-up")
 
-    # timed region: device-resident inputs
+    # per-entry-point breakdown: untimed steps with an event pair around
+    # every call (those events would add about 1% to a timed step)
+    blog = EventLog()
+    logged = build_step(layer, m, blog)
+    n_logged = max(1, min(args.steps, 5))
+    for _ in range(n_logged):
+        logged(x_in, m.g2)
+    torch.cuda.synchronize()
+    per_all = blog.per_name_ms()
+    dom = max(per_all, key=lambda k: sum(per_all[k]))
+
+    # timed region: device-resident inputs; events only around the dominant
+    # entry point's calls, for its roofline
     log = EventLog()
-    step = build_step(layer, m, log)
+    step = build_step(layer, m, log, only=dom)
     sampler = ClockSampler(local, args.clocks_csv)
     sampler.start()
     barrier()
@@ -387,24 +400,23 @@ def run_ours(args):
     if st != 0:
         raise RuntimeError(f"device status {st} after the timed region")
 
-    # per-kernel breakdown (same timed region)
+    # per-kernel breakdown (the logged steps; shares of the timed step)
     per = log.per_name_ms()
     units = kernel_units(layer, m)
     kernels = {}
-    for name, times in per.items():
+    for name, times in per_all.items():
         n_per_step = len(units.get(name, [])) or 1
-        tot = sum(times) / args.steps
+        tot = sum(times) / n_logged
         u = units.get(name, [])
         entry = {"ms_per_step": tot, "share": tot / ms, "calls_per_step": n_per_step}
         if u and isinstance(u[0], tuple):
-            by = [sum(times[i::n_per_step]) / args.steps for i in range(n_per_step)]
+            by = [sum(times[i::n_per_step]) / n_logged for i in range(n_per_step)]
             gbs = [uu[0] * uu[1] / (b / 1e3) / 1e9 for uu, b in zip(u, by)]
             entry.update({"GB_s": gbs, "frac_hbm": [g / peaks["hbm_gbs"] for g in gbs]})
         elif u:
-            by = [sum(times[i::n_per_step]) / args.steps for i in range(n_per_step)]
+            by = [sum(times[i::n_per_step]) / n_logged for i in range(n_per_step)]
             entry.update({"TFLOP_s": [f / (b / 1e3) / 1e12 for f, b in zip(u, by)]})
         kernels[name] = entry
-    dom = max(kernels, key=lambda k: kernels[k]["ms_per_step"])
     roof = roofline_of(dom, per[dom], units[dom], args.steps, peaks)
     roof["traffic"] = measured_traffic(dom)
     roof["traffic_unit"] = "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum), null if stale"
@@ -420,7 +432,7 @@ def run_ours(args):
     staged = HostStaged(layer, tokens=m.x.shape[0] if layer.gathers_rows else None)
     staged.step(x_h, g_h, dx_h, m.w13, m.w2, m.group_offsets, seed=3, rows_h=rows_h)  # untimed: first use
     staged.synchronize()
-    e2e_steps = max(2, min(args.steps, 10))
+    e2e_steps = max(2, min(args.steps, 20))  # the copy pipeline's fill and drain amortized as over the timed steps
     torch.cuda.synchronize()
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -457,6 +469,8 @@ def run_ours(args):
                                    if layer.gathers_rows else "routed rows [T*k x 4096], already dispatched")},
         "gemm_flops_per_step": step_flops,
         "roofline": roof, "kernels": kernels, "clocks": clocks,
+        "kernels_note": (f"per entry point: {n_logged} untimed steps with an event pair around every call; "
+                         "shares of the timed step; the roofline's kernel timed live in the timed region"),
         "e2e": {"value": aggregate(step_flops / 1e12, e2e_ms / 1e3, world), "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "overlap": "copies in (step i+1) and out (step i-1) on their own streams during step i",
