@@ -91,3 +91,38 @@ def test_layer_step_from_tokens_equals_step_from_routed_rows():
     check_status()
     for u, v in zip(*outs):
         assert torch.equal(u.view(torch.uint8), v.view(torch.uint8))
+
+
+@pytest.mark.parametrize("sizes,T,K", [([5, 0, 295, 130], 300, 256), ([40, 0, 24], 1000, 128)])
+def test_gather_against_the_oracle(sizes, T, K):
+    """The gathered call held directly to the oracle quantizing X = x[row_src]:
+    NVFP4 codes, block scales and outer scale exact, and the transposed SR
+    re-quantization exact (draws keyed by the routed row), for both amax
+    paths (T <= M reads each token once, T > M the routed rows)."""
+    from oracle import layout as L
+    from oracle import nvfp4 as NV
+    from oracle import requant as RQ
+    from tests.gpu_helpers import oracle_nvfp4, unpack_gpu_nvfp4
+    g = torch.Generator(device="cuda").manual_seed(T + K)
+    x = (torch.randn((T, K), generator=g, device="cuda") * 2).to(torch.bfloat16)
+    M = int(sum(sizes))
+    rows = torch.randint(0, T, (M,), generator=g, device="cuda", dtype=torch.int32)
+    o = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    groups = torch.tensor(o, device=dev())
+    E = len(sizes)
+    q, mt = NvTensor(1, M, K, dev(), E=E), MxTransposed(M, K, dev(), E=E)
+    N.nvfp4_quantize_requant_gather(x, rows, T, M, K, groups, None, q.sg, q.codes, q.scales,
+                                    q.gather_workspace(T), 7, 2, mt.codes, mt.scales)
+    check_status()
+    X = x.float().cpu().numpy()[rows.long().cpu().numpy()]  # the routed rows, gathered on the host
+    codes, scales, sg = oracle_nvfp4(X, 1, M, K, groups=o)
+    assert np.array_equal(q.sg.cpu().numpy(), sg)
+    assert np.array_equal(q.codes.cpu().numpy()[: codes.size], codes)
+    got_c, got_s = unpack_gpu_nvfp4(q.codes.cpu().numpy(), q.scales.cpu().numpy(), 1, M, K, o)
+    want_c, want_s, _ = NV.quantize(X, sg[0])
+    assert np.array_equal(got_c, want_c) and np.array_equal(got_s, want_s)
+    P = N.nvfp4moe_padded_cap(M, E)
+    ec, es = RQ.requant_grouped(want_c, want_s, sg[0], o, 7, 2, P)
+    Ptot = int(L.group_padded_starts(o)[-1])
+    assert np.array_equal(mt.codes.cpu().numpy()[: K * P].reshape(K, P)[:, :Ptot], ec[:, :Ptot])
+    assert np.array_equal(L.unswizzle(mt.scales.cpu().numpy(), np.arange(K), P // 32), es)
