@@ -804,9 +804,9 @@ def gpu_single_linear(iters=50):
         graph.replay()
     replay = time_calls(graph.replay, iters)
     return {"workload": "single expert linear, x [256 x 512] (4 rows x64), w [1024 x 512] (8 elements x100), "
-                        "g [256 x 1024], seed 0: NVFP4 fwd GEMM, SR requant of x and w, SR MXFP8 of g (row-wise + "
-                        "transposed), dgrad + wgrad",
-            "us_per_fwd_bwd": eager * 1e3, "us_per_fwd_bwd_graph": replay * 1e3, "calls": 10,
+                        "g [256 x 1024], seed 0: NVFP4 quantization of x and w with their SR requant in the same "
+                        "pass, NVFP4 fwd GEMM, SR MXFP8 of g (row-wise + transposed), dgrad + wgrad",
+            "us_per_fwd_bwd": eager * 1e3, "us_per_fwd_bwd_graph": replay * 1e3, "calls": 6, "launches": 10,
             "gemm_flops": 3 * 2.0 * 256 * 512 * 1024, "roofline": "latency-bound (no roofline bar)"}
 
 

@@ -119,15 +119,15 @@ class SingleLinear:
         self.dw = _empty((d_out, d_in), F32, dev)
 
     def enqueue(self, x, w, g, seed=0, stream=None):
+        """x and w are quantized with their SR re-quantizations for the
+        backward in the same passes (bit-identical to nvfp4_quantize followed
+        by dequant_transpose_requant_sr; two launches fewer for a layer this
+        small, whose time is mostly launches)."""
         T, din, dout, go = self.T, self.din, self.dout, self.groups
-        self.xq.quantize(x, go, stream)
-        self.wq.quantize(w, None, stream)
+        self.xq.quantize_requant(x, self.xt, seed, 1, go, stream)
+        self.wq.quantize_requant(w, self.wt, seed, 0, None, stream)
         N.grouped_gemm_nvfp4_fwd(None, self.xq.sg, self.xq.codes, self.xq.scales, self.wq.codes, self.wq.scales,
                                  self.wq.sg, go, 1, T, dout, din, self.y, N.NV_OUT_FP32, None, stream)
-        N.dequant_transpose_requant_sr(self.wq.codes, self.wq.scales, self.wq.sg, 1, dout, din, None, seed, 0,
-                                       self.wt.codes, self.wt.scales, stream)
-        N.dequant_transpose_requant_sr(self.xq.codes, self.xq.scales, self.xq.sg, 1, T, din, go, seed, 1,
-                                       self.xt.codes, self.xt.scales, stream)
         N.mxfp8_quantize(g, T, dout, go, N.NV_SR, seed, 2, 3, self.g_row.codes, self.g_row.scales,
                          self.gt.codes, self.gt.scales, stream)
         N.grouped_gemm_mxfp8_dx(self.g_row.codes, self.g_row.scales, self.wt.codes, self.wt.scales, go, 1, T, dout,
