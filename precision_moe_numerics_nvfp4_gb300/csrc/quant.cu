@@ -244,6 +244,73 @@ __device__ __forceinline__ bool setup_groups(GroupSmem &g, const int32_t *go, in
   return load_groups(go, E, rows, g.off, g.pad, &g.flag, status);
 }
 
+// The CTA's window in the grouped layout, worked out by warp 0 alone: it
+// reads the group offsets, checks them as load_groups does (offsets[0] == 0,
+// offsets[E] == rows, non-decreasing, within [0, rows]; otherwise
+// NV_ERR_OFFSETS is recorded and every thread gets false), scans the
+// 128-padded group sizes and finds the group holding padded row 128 * win
+// (the result of map_window); the other warps read it after one barrier
+// instead of repeating the setup and a binary search each.  go == nullptr:
+// one group of all rows.  Every thread of the CTA must call it.
+__device__ __forceinline__ bool grouped_window(const int32_t *__restrict__ go, int E, int64_t rows, int win,
+                                               int *status, Window &w) {
+  __shared__ Window s_win;
+  __shared__ int s_bad;
+  if (threadIdx.x < 32) {
+    const int lane = (int)threadIdx.x;
+    const int p0 = win * 128;
+    if (go == nullptr) E = 1;
+    bool bad = false, found = false;
+    int carry = 0;
+    for (int base = 0; base < E; base += 32) {
+      const int e = base + lane;
+      int lo = 0, hi = 0;
+      if (e < E) {
+        lo = go ? go[e] : 0;
+        hi = go ? go[e + 1] : (int)rows;
+        bad |= lo < 0 || hi < lo || (int64_t)hi > rows || (e == 0 && lo != 0) || (e == E - 1 && (int64_t)hi != rows);
+      }
+      const int sz = (hi - lo + 127) & ~127;  // 0 past the last group
+      int incl = sz;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int n = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+        if (lane >= d) incl += n;
+      }
+      const int start = carry + incl - sz;
+      const bool hit = sz > 0 && p0 >= start && p0 < start + sz;
+      if (hit) {
+        Window t;
+        t.rp0 = p0;
+        t.seg = e;
+        t.src_row0 = (int64_t)lo + (p0 - start);
+        const int64_t left = (int64_t)hi - t.src_row0;
+        t.nvalid = left < 128 ? (int)left : 128;
+        s_win = t;
+      }
+      found |= __any_sync(0xFFFFFFFFu, hit);
+      carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    }
+    bad = __any_sync(0xFFFFFFFFu, bad);
+    if (lane == 0) {
+      s_bad = bad ? 1 : 0;
+      if (bad) record_error(status, NV_ERR_OFFSETS);
+      if (!found) {  // a window past the last group's padded rows
+        Window t;
+        t.rp0 = p0;
+        t.seg = E;
+        t.src_row0 = 0;
+        t.nvalid = 0;
+        s_win = t;
+      }
+    }
+  }
+  __syncthreads();
+  if (s_bad) return false;
+  w = s_win;
+  return true;
+}
+
 // ---------------------------------------------------------------------------
 // NVFP4 quantization, one CTA = 128 padded rows x 256 columns
 // ---------------------------------------------------------------------------
@@ -325,11 +392,13 @@ __device__ __forceinline__ void fill_inv_table(float *tab, float sg) {
 
 __global__ void __launch_bounds__(256) nvfp4_quant_kernel(NvQuantArgs A) {
   __shared__ __align__(16) uint8_t s_sc[4 * 512];
-  __shared__ GroupSmem s_g;
   const bool grouped = A.groups != nullptr;
-  int E = A.E;
-  if (grouped && !load_groups(A.groups, E, A.rows, s_g.off, s_g.pad, &s_g.flag, A.status)) return;
-  const Window w = map_window(grouped, blockIdx.y, E, s_g.off, s_g.pad, A.rows, A.wpb);
+  Window w;
+  if (grouped) {
+    if (!grouped_window(A.groups, A.E, A.rows, blockIdx.y, A.status, w)) return;
+  } else {
+    w = map_window(false, blockIdx.y, 0, nullptr, nullptr, A.rows, A.wpb);
+  }
   const float sg = A.sg_rows ? 1.0f : A.sg[grouped ? 0 : w.seg];
   const float den6 = __fmul_rn(6.0f, sg);
   __shared__ float s_inv[128];
@@ -431,10 +500,8 @@ __device__ __forceinline__ void unpack8(const uint4 &q, float (&v)[8]) {
 
 __global__ void __launch_bounds__(256) mxfp8_rowwise_kernel(const __grid_constant__ MxRowArgs A) {
   __shared__ __align__(16) uint8_t s_sc[2 * 512];
-  __shared__ GroupSmem s_g;
-  int E = A.E;
-  if (!setup_groups(s_g, A.groups, E, A.rows, A.status)) return;
-  const Window w = map_window(true, blockIdx.y, E, s_g.off, s_g.pad, A.rows, 0);
+  Window w;
+  if (!grouped_window(A.groups, A.E, A.rows, blockIdx.y, A.status, w)) return;
   reinterpret_cast<uint32_t *>(s_sc)[threadIdx.x] = 0u;
   __syncthreads();
   const int KB = (int)(A.cols >> 5);
@@ -687,7 +754,6 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant
   constexpr bool kNvfp4 = kMode != kSrcBf16;  // phase 2 on exact f16 products of NVFP4 values
   static_assert(!kRows || kNvfp4, "per-token outer scales apply to NVFP4 sources");
   extern __shared__ __align__(16) uint8_t smem[];
-  __shared__ GroupSmem s_g;
   __shared__ __align__(16) uint8_t s_tsc[512];   // transposed scale tile
   __shared__ __align__(16) uint8_t s_rsc[512];   // row-wise scale tile
   __shared__ __align__(16) uint8_t s_nvsc[kMode == kSrcBf16ToNvfp4 ? 1024 : 16];  // NVFP4 scale tiles
@@ -696,14 +762,15 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // the row-wise scale tile (bf16 source, always grouped) keeps zeros for rows
-  // without data; the barriers of the group setup order this clearing before
+  // without data; the barrier of the group lookup orders this clearing before
   // any phase-1 write
   if (kMode == kSrcBf16 && tid < 128) reinterpret_cast<uint32_t *>(s_rsc)[tid] = 0u;
-  int E = A.E;
+  Window w;
   if (A.grouped) {
-    if (!setup_groups(s_g, A.groups, E, A.rows, A.status)) return;
+    if (!grouped_window(A.groups, A.E, A.rows, blockIdx.y, A.status, w)) return;
+  } else {
+    w = map_window(false, blockIdx.y, 0, nullptr, nullptr, A.rows, A.wpb);
   }
-  const Window w = map_window(A.grouped != 0, blockIdx.y, E, s_g.off, s_g.pad, A.rows, A.wpb);
   const int64_t col0 = (int64_t)blockIdx.x * 128;
   const float sg = kNvfp4 && !kRows ? A.nv_sg[A.grouped ? 0 : w.seg] : 1.0f;
 

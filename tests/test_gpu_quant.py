@@ -116,6 +116,33 @@ def test_nvfp4_bad_offsets_recorded_and_nothing_written():
     assert N.nvfp4moe_get_device_status() == 0
 
 
+@pytest.mark.parametrize("offsets", [[0, 10, 5, 40], [0, 10, 20, 39], [3, 10, 20, 40], [0, -1, 20, 40]],
+                         ids=["decreasing", "last_not_rows", "first_not_zero", "negative"])
+def test_bad_offsets_recorded_and_nothing_written_every_grouped_quantizer(offsets):
+    """The group lookup of every grouped quantizer (NVFP4 quantize, the MXFP8
+    gradient quantizer row-wise + transposed, the fused quantize + SR
+    requant) rejects offsets that are not a partition of the rows: the status
+    word says NV_ERR_OFFSETS and no output byte changes."""
+    from precision_moe_numerics_nvfp4_gb300.pipeline import MxRows, MxTransposed, NvTensor
+    go = torch.tensor(offsets, dtype=torch.int32, device=dev())
+    R, C, E = 40, 128, 3
+    x = _tensor((R, C), seed=5)
+    one = torch.ones(1, dtype=torch.float32, device=dev())
+    nv, mr, mt = NvTensor(1, R, C, dev(), E=E), MxRows(R, C, dev(), E=E), MxTransposed(R, C, dev(), E=E)
+    outs = (nv.codes, nv.scales, mr.codes, mr.scales, mt.codes, mt.scales)
+    for t in outs:
+        t.fill_(0xA5)
+    N.nvfp4_quantize(x, 1, R, C, go, one, None, nv.codes, nv.scales, None)
+    assert N.nvfp4moe_get_device_status() == N.NV_ERR_OFFSETS
+    N.mxfp8_quantize(x, R, C, go, N.NV_SR, 1, 2, 3, mr.codes, mr.scales, mt.codes, mt.scales)
+    assert N.nvfp4moe_get_device_status() == N.NV_ERR_OFFSETS
+    N.nvfp4_quantize_requant(x, 1, R, C, go, one, None, nv.codes, nv.scales, None, 1, 2, mt.codes, mt.scales)
+    assert N.nvfp4moe_get_device_status() == N.NV_ERR_OFFSETS
+    for t in outs:
+        assert torch.all(t == 0xA5)
+    assert N.nvfp4moe_get_device_status() == 0
+
+
 def test_host_argument_errors():
     x = torch.zeros((4, 24), dtype=torch.bfloat16, device=dev())
     c = filled(64)
