@@ -57,8 +57,15 @@ def test_nvfp4_quantize_single_linear_workload():
         assert sg[0] == esg[0] and np.array_equal(codes, ec) and np.array_equal(scales, es)
 
 
-def test_nvfp4_quantize_grouped_layout():
-    sizes = [5, 0, 295, 128, 272, 0]
+def _many_groups(n, seed):
+    """n groups of 0..9 rows (many empty): more groups than the window
+    lookup's first four chunks of 32."""
+    return [int(v) for v in np.random.default_rng(seed).integers(0, 10, size=n)]
+
+
+@pytest.mark.parametrize("sizes", [[5, 0, 295, 128, 272, 0], _many_groups(200, 1), _many_groups(300, 2)],
+                         ids=["six", "200_groups", "300_groups"])
+def test_nvfp4_quantize_grouped_layout(sizes):
     go, o = _groups(sizes)
     rows, cols = int(o[-1]), 256
     x = _tensor((rows, cols), seed=11)
@@ -217,8 +224,10 @@ def test_mxfp8_rowwise_only(mode, rows, cols, sizes):
 
 @pytest.mark.parametrize("want_row", [False, True])
 @pytest.mark.parametrize("rows,cols,sizes", [(700, 128, [5, 0, 295, 128, 272]), (256, 1024, None),
-                                             (513, 256, [1, 512])])
+                                             (513, 256, [1, 512]), (None, 128, _many_groups(260, 3))])
 def test_mxfp8_transposed_grouped_sr(want_row, rows, cols, sizes):
+    if rows is None:
+        rows = sum(sizes)
     x = _tensor((rows, cols), seed=rows * 3 + cols, kind="n", scale=1e-3)
     go, o = (None, None) if sizes is None else _groups(sizes)
     r = _gpu_mx(x, rows, cols, go, N.NV_SR, 9, 4, 5, want_row=want_row, want_t=True)
