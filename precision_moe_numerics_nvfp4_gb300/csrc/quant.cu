@@ -361,17 +361,18 @@ __device__ __forceinline__ void nvfp4_block46(const uint4 &a, const uint4 &b, fl
 // (1 + m / 128) 2^e, fp32(bamax / den6) = qtab[m] 2^e exactly while the
 // quotient is a normal fp32 number (scaling by a power of two commutes with
 // rounding there), and below that range or at overflow both forms give the
-// same E4M3 code (0, or the 448 saturation).  A subnormal bf16 maximum takes
-// the division.  inv_tab as in nvfp4_block.
+// same E4M3 code (0, or the 448 saturation).  qtab[128 + m] holds the
+// quotient itself for the subnormal (and zero) bf16 maximum m 2^-133, read
+// with multiplier 1.  inv_tab as in nvfp4_block.
 __device__ __forceinline__ void mul2_rn(float a, float b, float m, float &ra, float &rb);
 __device__ __forceinline__ void nvfp4_block_tab(const uint4 &a, const uint4 &b, const float *qtab,
-                                                const float *inv_tab, float den6, uint2 &codes, uint32_t &scode) {
+                                                const float *inv_tab, uint2 &codes, uint32_t &scode) {
   uint32_t m = bf16x2_absmax(bf16x2_absmax(a.x, a.y), bf16x2_absmax(a.z, a.w));
   m = bf16x2_absmax(m, bf16x2_absmax(bf16x2_absmax(b.x, b.y), bf16x2_absmax(b.z, b.w)));
   const uint32_t u = max(m & 0x7FFFu, (m >> 16) & 0x7FFFu);  // |block max| as bf16 bits (signs meaningless)
   const uint32_t e = u & 0x7F80u;
-  const float q = (e == 0u && u != 0u) ? __fdiv_rn(__uint_as_float(u << 16), den6)
-                                       : __fmul_rn(qtab[u & 0x7Fu], __uint_as_float(e << 16));
+  const bool sub = e == 0u;
+  const float q = __fmul_rn(qtab[(u & 0x7Fu) | (sub ? 128u : 0u)], __uint_as_float(sub ? 0x3F800000u : e << 16));
   scode = cvt_e4m3_rn(q);
   const float inv = inv_tab[scode];
   const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
@@ -729,6 +730,8 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t 
 // 16-bit layout with cp.async: 128 bytes per thread in flight without
 // registers; rows past the window's data are zero-filled.  Waits for the
 // thread's own copies; the caller's barrier makes the tile visible.
+// kGather: row r of the window is source row row_src[r].
+template <bool kGather>
 __device__ __forceinline__ void stage_bf16_tile(const MxTArgs &A, const Window &w, int64_t col0, uint8_t *s_in) {
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
@@ -736,7 +739,7 @@ __device__ __forceinline__ void stage_bf16_tile(const MxTArgs &A, const Window &
     const int i = q >> 4, c16 = q & 15;
     bool ok = i < w.nvalid;
     int64_t row = w.src_row0 + i;
-    if (A.row_src && ok) {  // gathered source: a row index out of range reads as zeros and is recorded
+    if (kGather && ok) {  // a row index out of range reads as zeros and is recorded
       row = A.row_src[row];
       if (row < 0 || row >= A.src_rows) {
         record_error(A.status, NV_ERR_ARG);
@@ -749,10 +752,11 @@ __device__ __forceinline__ void stage_bf16_tile(const MxTArgs &A, const Window &
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
 }
 
-template <int kMode, bool kRows = false, bool k46 = false>
+template <int kMode, bool kRows = false, bool k46 = false, bool kGather = false>
 __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant__ MxTArgs A) {
   constexpr bool kNvfp4 = kMode != kSrcBf16;  // phase 2 on exact f16 products of NVFP4 values
   static_assert(!kRows || kNvfp4, "per-token outer scales apply to NVFP4 sources");
+  static_assert(!kGather || (kMode == kSrcBf16ToNvfp4 && !kRows && !k46), "gathered rows: bf16 -> NVFP4 only");
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ __align__(16) uint8_t s_tsc[512];   // transposed scale tile
   __shared__ __align__(16) uint8_t s_rsc[512];   // row-wise scale tile
@@ -772,11 +776,40 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant
     w = map_window(false, blockIdx.y, 0, nullptr, nullptr, A.rows, A.wpb);
   }
   const int64_t col0 = (int64_t)blockIdx.x * 128;
+
+  // output addressing: transposed codes [source column][token], scale tile
+  int64_t out_base, out_stride, tile_idx;
+  if (A.grouped) {
+    out_base = col0 * A.out_stride + w.rp0;
+    out_stride = A.out_stride;
+    tile_idx = (col0 >> 7) * A.out_ka + (w.rp0 >> 7);
+  } else {
+    const int b = w.seg;
+    const int64_t wb = w.rp0 / 128 - (int64_t)b * A.wpb;
+    out_base = ((int64_t)b * A.cols + col0) * A.rows + wb * 128;
+    out_stride = A.rows;
+    const int64_t cpad = (A.cols + 127) & ~127LL;
+    tile_idx = (((int64_t)b * cpad + col0) >> 7) * A.out_ka + wb;
+  }
+  if (w.nvalid == 0) {
+    // a window without data (grouped padding past the last group): zero
+    // scale tiles, no codes (w is the same for every thread: no barrier is
+    // left unmatched)
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    if (tid < 32) {
+      reinterpret_cast<uint4 *>(A.out_scales + tile_idx * 512)[tid] = z;
+    } else if (tid < 64 && A.row_codes != nullptr) {
+      reinterpret_cast<uint4 *>(A.row_scales + ((w.rp0 >> 7) * A.row_ka + (col0 >> 7)) * 512)[tid - 32] = z;
+    } else if (kMode == kSrcBf16ToNvfp4 && tid >= 64 && tid < 128) {
+      reinterpret_cast<uint4 *>(A.nv_scales_out + ((w.rp0 >> 7) * A.nv_ka + (col0 >> 6)) * 512)[tid - 64] = z;
+    }
+    return;
+  }
   const float sg = kNvfp4 && !kRows ? A.nv_sg[A.grouped ? 0 : w.seg] : 1.0f;
 
   // ---- phase 1 --------------------------------------------------------------
   if (!kNvfp4) {
-    stage_bf16_tile(A, w, col0, s_in);
+    stage_bf16_tile<false>(A, w, col0, s_in);
     __syncthreads();
     // row-wise output: items of 16 columns (32 bytes) of one row; a row-wise
     // MXFP8 block of 32 is two neighbouring lanes, and one Philox call covers
@@ -855,14 +888,17 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant
     // global memory, scales to the shared tile; the exact f16 products of the
     // new codes replace the unit's bf16 values in place for phase 2
     __shared__ float s_inv[128];
-    __shared__ float s_qt[128];
+    __shared__ float s_qt[256];
     const float den6 = __fmul_rn(6.0f, sg);
     // the block-scale table of nvfp4_block_tab applies while every quotient
     // (1 + m / 128) / den6 is a normal fp32 number
     const bool tab = !kRows && !k46 && den6 >= 0x1p-100f && den6 <= 0x1p100f;
     if (!kRows) fill_inv_table(s_inv, sg);
-    if (tab && tid >= 128) s_qt[tid - 128] = __fdiv_rn(__uint_as_float(0x3F800000u | ((uint32_t)(tid - 128) << 16)), den6);
-    stage_bf16_tile(A, w, col0, s_in);
+    if (tab) {  // normal mantissas (1 + m / 128), then the subnormal maxima m 2^-133
+      const uint32_t t = (uint32_t)tid;
+      s_qt[t] = __fdiv_rn(__uint_as_float(t < 128 ? 0x3F800000u | (t << 16) : (t - 128) << 16), den6);
+    }
+    stage_bf16_tile<kGather>(A, w, col0, s_in);
     __syncthreads();
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -878,7 +914,7 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant
       } else if (k46) {
         nvfp4_block46(va, vb, sg, c, sc);
       } else if (tab) {
-        nvfp4_block_tab(va, vb, s_qt, s_inv, den6, c, sc);  // an all-zero (padding) block gives scale 0 and zero codes
+        nvfp4_block_tab(va, vb, s_qt, s_inv, c, sc);  // an all-zero (padding) block gives scale 0 and zero codes
       } else {
         nvfp4_block(va, vb, sg, den6, c, sc, s_inv);
       }
@@ -890,22 +926,7 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant
   }
   __syncthreads();
 
-  // output addressing: transposed codes [source column][token], scale tile
-  int64_t out_base, out_stride, tile_idx;
-  if (A.grouped) {
-    out_base = col0 * A.out_stride + w.rp0;
-    out_stride = A.out_stride;
-    tile_idx = (col0 >> 7) * A.out_ka + (w.rp0 >> 7);
-  } else {
-    const int b = w.seg;
-    const int64_t wb = w.rp0 / 128 - (int64_t)b * A.wpb;
-    out_base = ((int64_t)b * A.cols + col0) * A.rows + wb * 128;
-    out_stride = A.rows;
-    const int64_t cpad = (A.cols + 127) & ~127LL;
-    tile_idx = (((int64_t)b * cpad + col0) >> 7) * A.out_ka + wb;
-  }
-  // a window without data (grouped padding past the last expert) stores no codes
-  uint8_t *const out_lane = w.nvalid > 0 ? A.out_codes + out_base + 4 * lane : nullptr;
+  uint8_t *const out_lane = A.out_codes + out_base + 4 * lane;
 
   // ---- phase 2 --------------------------------------------------------------
   // warp handles groups of 8 output rows (source columns c8*8 .. c8*8+7);
@@ -920,6 +941,11 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant
     const int i = 4 * lane + j;
     sg_tok[j] = (kRows && i < w.nvalid) ? A.nv_sg_rows[w.src_row0 + i] : 0.0f;
   }
+  // Philox counters: pair keys (row * cols + column) / 8 of token 4l's columns
+  // c8 * 8 .. c8 * 8 + 7 are q0 + c8, token 4l + 2's are q0 + c8 + cols / 4
+  // (cols and col0 are multiples of 128)
+  const uint64_t q0 = (uint64_t)(((w.src_row0 + 4 * lane) * A.cols + col0) >> 3);
+  const uint64_t q2 = (uint64_t)(A.cols >> 2);
 #pragma unroll 1
   for (int c8 = warp; c8 < 16; c8 += 8) {
     uint32_t v[4][4];  // [token j][column pair] packed 16-bit values
@@ -930,10 +956,9 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant
       v[j][0] = raw.x; v[j][1] = raw.y; v[j][2] = raw.z; v[j][3] = raw.w;
     }
     uint4 ba = make_uint4(0, 0, 0, 0), bb = make_uint4(0, 0, 0, 0);
-    if (A.sr && 4 * lane < w.nvalid) {
-      const int64_t ka = (w.src_row0 + 4 * lane) * A.cols + col0 + c8 * 8;
-      ba = philox_bits8_rk((uint64_t)(ka >> 3), A.off_t, A.rk);
-      bb = philox_bits8_rk((uint64_t)((ka + 2 * A.cols) >> 3), A.off_t, A.rk);
+    if (A.sr) {  // rows past the window's data draw too: their values are zeros, which SR keeps
+      ba = philox_bits8_rk(q0 + c8, A.off_t, A.rk);
+      bb = philox_bits8_rk(q0 + c8 + q2, A.off_t, A.rk);
     }
     if constexpr (kRows) {
       // per-token outer scales: the dequantized values fp32(p * sg_token)
@@ -984,30 +1009,39 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant
         } else {
           packed = cvt_e4m3x2_rn(x[0], x[1]) | (cvt_e4m3x2_rn(x[2], x[3]) << 16);
         }
-        if (out_lane) *reinterpret_cast<uint32_t *>(out_lane + (int64_t)c * out_stride) = packed;
+        *reinterpret_cast<uint32_t *>(out_lane + (int64_t)c * out_stride) = packed;
       }
       continue;
     }
+    // column pairs (2p, 2p+1): maxima over the lane's 4 tokens, then over the
+    // 8 lanes of the block by a reduce-scatter (keep half, send half), after
+    // which lanes 2q and 2q+1 of a block both hold pair q over all 32 tokens:
+    // the pair of the lane's own column k_own = lane & 7
     uint32_t m[4];
 #pragma unroll
-    for (int p = 0; p < 4; ++p) {  // column pair (2p, 2p+1): max over the 32 tokens of the block
-      if (kNvfp4) {
-        m[p] = habsmax2(habsmax2(v[0][p], v[1][p]), habsmax2(v[2][p], v[3][p]));
-        m[p] = habsmax2(m[p], __shfl_xor_sync(0xFFFFFFFFu, m[p], 1));
-        m[p] = habsmax2(m[p], __shfl_xor_sync(0xFFFFFFFFu, m[p], 2));
-        m[p] = habsmax2(m[p], __shfl_xor_sync(0xFFFFFFFFu, m[p], 4));
-      } else {
-        m[p] = bf16x2_absmax(bf16x2_absmax(v[0][p], v[1][p]), bf16x2_absmax(v[2][p], v[3][p]));
-        m[p] = bf16x2_absmax(m[p], __shfl_xor_sync(0xFFFFFFFFu, m[p], 1));
-        m[p] = bf16x2_absmax(m[p], __shfl_xor_sync(0xFFFFFFFFu, m[p], 2));
-        m[p] = bf16x2_absmax(m[p], __shfl_xor_sync(0xFFFFFFFFu, m[p], 4));
-      }
+    for (int p = 0; p < 4; ++p)
+      m[p] = kNvfp4 ? habsmax2(habsmax2(v[0][p], v[1][p]), habsmax2(v[2][p], v[3][p]))
+                    : bf16x2_absmax(bf16x2_absmax(v[0][p], v[1][p]), bf16x2_absmax(v[2][p], v[3][p]));
+    const bool b2 = lane & 4, b1 = lane & 2;
+    uint32_t m4[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const uint32_t keep = b2 ? m[q + 2] : m[q], send = b2 ? m[q] : m[q + 2];
+      const uint32_t got = __shfl_xor_sync(0xFFFFFFFFu, send, 4);
+      m4[q] = kNvfp4 ? habsmax2(keep, got) : bf16x2_absmax(keep, got);
+    }
+    uint32_t mp;
+    {
+      const uint32_t keep = b1 ? m4[1] : m4[0], send = b1 ? m4[0] : m4[1];
+      const uint32_t got = __shfl_xor_sync(0xFFFFFFFFu, send, 2);
+      mp = kNvfp4 ? habsmax2(keep, got) : bf16x2_absmax(keep, got);
+      const uint32_t got1 = __shfl_xor_sync(0xFFFFFFFFu, mp, 1);
+      mp = kNvfp4 ? habsmax2(mp, got1) : bf16x2_absmax(mp, got1);
     }
     // this lane's column: k_own = lane & 7
     float m2_own;
     {
       const int k_own = lane & 7;
-      const uint32_t mp = k_own < 2 ? m[0] : k_own < 4 ? m[1] : k_own < 6 ? m[2] : m[3];
       float amax, mult;
       if (kNvfp4) {
         // max_i fp32(p_i * sg) = fp32(max_i p_i * sg): rounding is monotonic
@@ -1022,9 +1056,10 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant
       m2_own = kNvfp4 ? (amax == 0.0f ? 0.0f : __fmul_rn(sg, mult)) : mult;
       s_tsc[atom_pos(c8 * 8 + k_own, lane >> 3)] = (uint8_t)sc;
     }
+    // output rows c8 * 8 .. c8 * 8 + 7, one stepped pointer
+    uint8_t *out_row = out_lane + (int64_t)(c8 * 8) * out_stride;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      const int c = c8 * 8 + k;
       const float m2 = __shfl_sync(0xFFFFFFFFu, m2_own, k, 8);  // from lane 8 * (lane / 8) + k
       const int p = k >> 1, h = k & 1;
       float x[4];
@@ -1048,15 +1083,15 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant
       } else {
         packed = cvt_e4m3x2_rn(x[0], x[1]) | (cvt_e4m3x2_rn(x[2], x[3]) << 16);
       }
-      if (out_lane) *reinterpret_cast<uint32_t *>(out_lane + (int64_t)c * out_stride) = packed;
+      *reinterpret_cast<uint32_t *>(out_row) = packed;
+      out_row += out_stride;
     }
   }
   __syncthreads();
 
   // ---- phase 3 --------------------------------------------------------------
   if (tid < 32) {
-    if (w.nvalid > 0 || A.grouped)
-      reinterpret_cast<uint4 *>(A.out_scales + tile_idx * 512)[tid] = reinterpret_cast<const uint4 *>(s_tsc)[tid];
+    reinterpret_cast<uint4 *>(A.out_scales + tile_idx * 512)[tid] = reinterpret_cast<const uint4 *>(s_tsc)[tid];
   } else if (tid < 64 && A.row_codes != nullptr) {  // zero tiles for padding windows too
     reinterpret_cast<uint4 *>(A.row_scales + ((w.rp0 >> 7) * A.row_ka + (col0 >> 7)) * 512)[tid - 32] =
         reinterpret_cast<const uint4 *>(s_rsc)[tid - 32];
@@ -1215,11 +1250,13 @@ int launch_nvfp4_requant(const uint16_t *x, const float *sg, int64_t batch, int6
     A.grouped = 0; A.wpb = (int)(rows / 128); A.out_ka = rows / 128; nwin = batch * A.wpb;
   }
   const size_t sm = mx_t_smem(false);
-  const int which = sg_rows ? 1 : (four_six ? 2 : 0);
+  if (row_src && (sg_rows || four_six)) return NV_ERR_ARG;  // gathered rows: per-tensor scale, plain rule
+  const int which = sg_rows ? 1 : four_six ? 2 : row_src ? 3 : 0;
   auto k = which == 1   ? mx_transpose_kernel<kSrcBf16ToNvfp4, true>
            : which == 2 ? mx_transpose_kernel<kSrcBf16ToNvfp4, false, true>
+           : which == 3 ? mx_transpose_kernel<kSrcBf16ToNvfp4, false, false, true>
                         : mx_transpose_kernel<kSrcBf16ToNvfp4, false>;
-  static bool attr_set[3] = {false, false, false};
+  static bool attr_set[4] = {false, false, false, false};
   if (!attr_set[which]) {
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     attr_set[which] = true;

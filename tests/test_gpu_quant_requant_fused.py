@@ -73,6 +73,23 @@ def test_fused_with_given_outer_scale():
     _assert_same(*_both(x, 2, 128, 256, None, sg, seed=1, off=0))
 
 
+@pytest.mark.parametrize("sg", [1.0, 1e-39], ids=["table_range", "below_table_range"])
+def test_fused_subnormal_block_maxima(sg):
+    """Blocks of bf16 subnormals (|x| < 2^-126, some zero) beside normal
+    blocks: under an outer scale whose 6 sg lies in the block-scale table's
+    range the fused kernel reads the subnormal quotients from the table, under
+    a tiny one it divides; both must match the separate quantizer."""
+    rows, cols = 128, 256
+    g = torch.Generator(device="cuda").manual_seed(31)
+    x = torch.randn((1, rows, cols), generator=g, device="cuda") * 0.5
+    x[:, :, :64] *= 2.0 ** -130
+    x[:, ::3, 64:96] *= 2.0 ** -136
+    x = x.to(torch.bfloat16).contiguous()
+    assert (x[:, :, :64].float().abs().max() < 2.0 ** -126).item()
+    sg_in = torch.tensor([sg], dtype=torch.float32, device=dev())
+    _assert_same(*_both(x, 1, rows, cols, None, sg_in, seed=4, off=3))
+
+
 def test_fused_against_oracle():
     batch, rows, cols, seed, off = 2, 128, 256, 11, 5
     x = _x((batch, rows, cols), seed=21, std=0.02)
