@@ -259,6 +259,14 @@ def build_step(layer, m, log: EventLog | None, only: str | None = None):
     return step
 
 
+def gather_bytes_per_routed_elem(T, M):
+    """Algorithmic bytes per routed-row element of nvfp4_quantize_requant_gather
+    with T tokens and M routed rows."""
+    if T <= M:  # tokens quantized once, routed rows copied + re-quantized from their codes
+        return 0.5625 + 0.5625 + 1.03125 + (2.0 + 2.5625) * T / M
+    return 3.59375 + 2.0  # routed rows read by the amax pass and by the quantize pass
+
+
 def kernel_units(layer, m):
     """Algorithmic bytes (quantizers) and FLOPs (GEMMs) per call, by call name
     and argument pattern, in the order MoELayer.step issues them."""
@@ -319,10 +327,11 @@ def kernel_units(layer, m):
         # a call = the amax pass (2 B/elem) + the quantize pass (2 + 0.5 + 1/16 B/elem)
         "nvfp4_quantize": [(E * 2 * I * d, 4.5625), (E * d * I, 4.5625), (M * d, 4.5625), (M * I, 2.5625 + h_amax)],
         # amax pass (2) + one pass reading bf16 (2) and writing NVFP4 (0.5 + 1/16) and MXFP8 (1 + 1/32);
-        # x: the routed rows gathered from the tokens (the quantize pass, 3.59375 B per routed-row
-        # element) after an amax pass reading each token once (2 B per token element)
+        # x: the tokens read by the amax pass (2 B per token element) and quantized once (2 + 0.5625),
+        # then per routed-row element the token's NVFP4 codes and scales read (0.5625), copied to the
+        # routed layout (0.5625) and re-quantized to MXFP8 (1 + 1/32)
         "nvfp4_quantize_requant": [(E * 2 * I * d, 5.59375), (E * d * I, 5.59375), (M * I, 3.59375 + h_amax)],
-        "nvfp4_quantize_requant_gather": [(M * d, 3.59375 + 2.0 * T / M)],
+        "nvfp4_quantize_requant_gather": [(M * d, gather_bytes_per_routed_elem(T, M))],
         "grouped_gemm_nvfp4_fwd": [fl2] if layer.fuse_swiglu else [fl13, fl2],
         "grouped_gemm_nvfp4_fwd_swiglu": [fl13],
         "dequant_transpose_requant_sr": [(E * 2 * I * d, 1.59375), (E * d * I, 1.59375), (M * d, 1.59375),

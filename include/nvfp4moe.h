@@ -114,9 +114,9 @@ int64_t nvfp4moe_scale_offset(int64_t rp, int64_t c, int64_t kblocks);
 /* Workspace bytes nvfp4_quantize needs when it computes the outer scales. */
 size_t nvfp4moe_quantize_workspace_bytes(int64_t batch, int64_t rows, int64_t cols);
 
-/* Workspace bytes nvfp4_quantize_requant_gather needs when it computes the
- * outer scale: src_rows token rows gathered into rows x cols.  0 for
- * negative sizes. */
+/* Workspace bytes nvfp4_quantize_requant_gather needs: src_rows token rows
+ * gathered into rows x cols (the amax pass's scratch and, when src_rows <=
+ * rows, the tokens' NVFP4 codes and scales).  0 for negative sizes. */
 size_t nvfp4moe_quantize_gather_workspace_bytes(int64_t src_rows, int64_t rows, int64_t cols);
 
 /* Workspace bytes grouped_gemm_nvfp4_fwd needs when it is given bf16
@@ -178,9 +178,14 @@ int nvfp4_outer_scale(const void *x, int64_t batch, int64_t n, float *outer_scal
  * group_offsets required (num_groups >= 1).  The amax pass (outer_scale_in ==
  * NULL) takes the maximum over the rows of X; when src_rows <= rows it reads
  * each token row once (its row maximum) and takes the maximum of those over
- * row_src, the same value.  Its workspace:
+ * row_src, the same value.  When src_rows <= rows the tokens are also
+ * NVFP4-quantized once, into the workspace, and each routed row's codes and
+ * scales are copied from its token's and re-quantized from them (the block
+ * rule reads one row at a time, so these are the codes of X's row; a token no
+ * row routes may saturate, and is never read).  Workspace:
  * nvfp4moe_quantize_gather_workspace_bytes(src_rows, rows, cols) bytes,
- * 16-byte aligned. */
+ * 16-byte aligned, required when outer_scale_in is NULL or src_rows <= rows
+ * (else NV_ERR_WORKSPACE); otherwise it may be NULL. */
 int nvfp4_quantize_requant_gather(const void *x, const int32_t *row_src, int64_t src_rows, int64_t rows,
                                   int64_t cols, const int32_t *group_offsets, int32_t num_groups,
                                   const float *outer_scale_in, float *outer_scale_out, uint8_t *codes,

@@ -1,6 +1,7 @@
 // The C ABI of libnvfp4moe.so: argument checks, the per-device status word,
 // and the launches of every step of the hot path.  See include/nvfp4moe.h for
 // the contract of each entry point.
+#include <algorithm>
 #include <atomic>
 #include <cstdio>
 
@@ -79,9 +80,19 @@ size_t nvfp4moe_quantize_workspace_bytes(int64_t batch, int64_t rows, int64_t co
 }
 
 // the amax pass's partial maxima, then one float per token
+// the amax pass's scratch, the token row maxima, then (src_rows <= rows) the
+// tokens' NVFP4 codes and batched scales, each on a 256-byte boundary
+static size_t gather_tok_codes_at(int64_t src_rows, int64_t rows, int64_t cols) {
+  return nvfp4moe_quantize_workspace_bytes(1, rows, cols) + (size_t)rup(src_rows * 4, 256);
+}
+static size_t gather_tok_scales_at(int64_t src_rows, int64_t rows, int64_t cols) {
+  return gather_tok_codes_at(src_rows, rows, cols) + (size_t)rup(std::max<int64_t>(src_rows * cols / 2, 1), 256);
+}
 size_t nvfp4moe_quantize_gather_workspace_bytes(int64_t src_rows, int64_t rows, int64_t cols) {
   if (src_rows < 0 || rows < 0 || cols < 0) return 0;
-  return nvfp4moe_quantize_workspace_bytes(1, rows, cols) + (size_t)rup(src_rows * 4, 256);
+  if (src_rows > rows) return gather_tok_codes_at(src_rows, rows, cols);
+  const int64_t tok_scales = nvfp4moe_scale_bytes(((src_rows + 127) / 128) * 128, cols / 16);
+  return gather_tok_scales_at(src_rows, rows, cols) + (size_t)rup(std::max<int64_t>(tok_scales, 1), 256);
 }
 
 // codes, then the grouped scale buffer, then the outer scale, then the amax
@@ -270,7 +281,10 @@ int nvfp4_quantize_requant_gather(const void *x, const int32_t *row_src, int64_t
   if (rows == 0 || cols == 0) return NV_OK;
   if (rows >= (int64_t)1 << 30 || src_rows >= (int64_t)1 << 31 || rows * cols / 16 >= (int64_t)1 << 31)
     return NV_ERR_SHAPE;
-  if (!outer_scale_in &&
+  // no more tokens than routed rows: the tokens are quantized once into the
+  // workspace and the routed rows copied and re-quantized from their codes
+  const bool tokens_once = src_rows <= rows;
+  if ((!outer_scale_in || tokens_once) &&
       (!workspace || workspace_bytes < nvfp4moe_quantize_gather_workspace_bytes(src_rows, rows, cols) ||
        !al16(workspace)))
     return NV_ERR_WORKSPACE;
@@ -289,6 +303,17 @@ int nvfp4_quantize_requant_gather(const void *x, const int32_t *row_src, int64_t
   } else if (outer_scale_out && outer_scale_out != outer_scale_in) {
     if (cudaMemcpyAsync(outer_scale_out, outer_scale_in, sizeof(float), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
       return NV_ERR_CUDA;
+  }
+  if (tokens_once) {
+    // a routed row's NVFP4 codes and scales are its token's under the same
+    // outer scale (the block rule sees one row at a time)
+    uint8_t *tok_codes = static_cast<uint8_t *>(workspace) + gather_tok_codes_at(src_rows, rows, cols);
+    uint8_t *tok_scales = static_cast<uint8_t *>(workspace) + gather_tok_scales_at(src_rows, rows, cols);
+    int r = launch_nvfp4_quant(static_cast<const uint16_t *>(x), 1, src_rows, cols, nullptr, 0, sg, tok_codes,
+                               tok_scales, st, s);
+    if (r != NV_OK) return r;
+    return launch_requant_gather(tok_codes, tok_scales, sg, row_src, src_rows, rows, cols, group_offsets, num_groups,
+                                 codes, scales, seed, counter_offset, out_codes, out_scales, st, s);
   }
   return launch_nvfp4_requant(static_cast<const uint16_t *>(x), sg, 1, rows, cols, group_offsets, num_groups, codes,
                               scales, seed, counter_offset, out_codes, out_scales, st, s, nullptr, 0, row_src,

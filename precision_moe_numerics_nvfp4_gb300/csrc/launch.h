@@ -40,6 +40,14 @@ int launch_nvfp4_requant(const uint16_t *x, const float *sg, int64_t batch, int6
                          uint8_t *out_codes, uint8_t *out_scales, int *status, cudaStream_t s,
                          const float *sg_rows = nullptr, int four_six = 0, const int32_t *row_src = nullptr,
                          int64_t src_rows = 0);
+// the re-quantization of gathered rows: routed row r is token row_src[r] of
+// the NVFP4 token matrix (codes [src_rows][cols / 2], batched scale layout);
+// writes the routed rows' NVFP4 codes and grouped scales and their
+// transposed MXFP8 SR re-quantization
+int launch_requant_gather(const uint8_t *tok_codes, const uint8_t *tok_scales, const float *sg,
+                          const int32_t *row_src, int64_t src_rows, int64_t rows, int64_t cols,
+                          const int32_t *groups, int E, uint8_t *codes, uint8_t *scales, uint64_t seed, uint64_t off,
+                          uint8_t *out_codes, uint8_t *out_scales, int *status, cudaStream_t s);
 // amax pass over the gathered rows x[row_src[r]] (r < rows) -> sg_out[0];
 // row_amax: src_rows floats of scratch, used when src_rows <= rows
 int launch_amax_gather(const uint16_t *x, const int32_t *row_src, int64_t src_rows, int64_t rows, int64_t cols,

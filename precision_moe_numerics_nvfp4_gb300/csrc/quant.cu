@@ -725,6 +725,11 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t 
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(bytes)
                : "memory");
 }
+// the same for 4 bytes (`bytes` 0 or 4)
+__device__ __forceinline__ void cp_async4(void *dst, const void *src, uint32_t bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(bytes)
+               : "memory");
+}
 
 // The window's bf16 tile [128 rows][128 columns] straight into the swizzled
 // 16-bit layout with cp.async: 128 bytes per thread in flight without
@@ -756,11 +761,14 @@ template <int kMode, bool kRows = false, bool k46 = false, bool kGather = false>
 __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant__ MxTArgs A) {
   constexpr bool kNvfp4 = kMode != kSrcBf16;  // phase 2 on exact f16 products of NVFP4 values
   static_assert(!kRows || kNvfp4, "per-token outer scales apply to NVFP4 sources");
-  static_assert(!kGather || (kMode == kSrcBf16ToNvfp4 && !kRows && !k46), "gathered rows: bf16 -> NVFP4 only");
+  static_assert(!kGather || (kMode != kSrcBf16 && !kRows && !k46), "gathered rows: NVFP4 output, per-tensor scale");
+  // the routed rows' NVFP4 codes and scales are written too (from the bf16
+  // source, or copied from the gathered token codes)
+  constexpr bool kNvOut = kMode == kSrcBf16ToNvfp4 || kGather;
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ __align__(16) uint8_t s_tsc[512];   // transposed scale tile
   __shared__ __align__(16) uint8_t s_rsc[512];   // row-wise scale tile
-  __shared__ __align__(16) uint8_t s_nvsc[kMode == kSrcBf16ToNvfp4 ? 1024 : 16];  // NVFP4 scale tiles
+  __shared__ __align__(16) uint8_t s_nvsc[kNvOut ? 1024 : 16];  // NVFP4 scale tiles
   uint8_t *s_stage = smem;                                           // NVFP4 source staging (kSrcNvfp4)
   uint8_t *s_in = smem + (kMode == kSrcNvfp4 ? kNvStage : 0);         // [128][256 B] 16-bit values
 
@@ -800,7 +808,7 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant
       reinterpret_cast<uint4 *>(A.out_scales + tile_idx * 512)[tid] = z;
     } else if (tid < 64 && A.row_codes != nullptr) {
       reinterpret_cast<uint4 *>(A.row_scales + ((w.rp0 >> 7) * A.row_ka + (col0 >> 7)) * 512)[tid - 32] = z;
-    } else if (kMode == kSrcBf16ToNvfp4 && tid >= 64 && tid < 128) {
+    } else if (kNvOut && tid >= 64 && tid < 128) {
       reinterpret_cast<uint4 *>(A.nv_scales_out + ((w.rp0 >> 7) * A.nv_ka + (col0 >> 6)) * 512)[tid - 64] = z;
     }
     return;
@@ -850,10 +858,33 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant
   } else if (kMode == kSrcNvfp4) {
     // NVFP4: the window's codes [128 rows][64 bytes] and its two 512-byte
     // scale tiles go through cp.async into the staging area, then each (row,
-    // 16-column block) unit is decoded to exact f16 products e2m1 * e4m3
+    // 16-column block) unit is decoded to exact f16 products e2m1 * e4m3.
+    // kGather: row i is token row_src[src_row0 + i] of a token matrix in the
+    // batched layout; thread (i = tid / 2, half h = tid % 2) stages that
+    // row's 32 code bytes of half h and its four block scales of half h (one
+    // 4-byte word of the token's scale tile h), rows per unit instead of the
+    // two tiles
     uint8_t *st_codes = s_stage, *st_sc = s_stage + 128 * 64;
-    {
-      const int64_t half_cols = A.cols >> 1;
+    const int64_t half_cols = A.cols >> 1;
+    if (kGather) {
+      const int i = tid >> 1, h = tid & 1;
+      bool ok = i < w.nvalid;
+      int64_t t = 0;
+      if (ok) {  // a row index out of range reads as zeros and is recorded
+        t = A.row_src[w.src_row0 + i];
+        if (t < 0 || t >= A.src_rows) {
+          record_error(A.status, NV_ERR_ARG);
+          ok = false;
+        }
+      }
+      const uint8_t *src = ok ? A.nv_codes + t * half_cols + (col0 >> 1) + h * 32 : A.nv_codes;
+      cp_async16(st_codes + i * 64 + h * 32, src, ok ? 16u : 0u);
+      cp_async16(st_codes + i * 64 + h * 32 + 16, ok ? src + 16 : A.nv_codes, ok ? 16u : 0u);
+      const int64_t ka_src = A.cols >> 6;
+      const uint8_t *ssrc =
+          ok ? A.nv_scales + ((t >> 7) * ka_src + (col0 >> 6) + h) * 512 + atom_pos((int)(t & 127), 0) : A.nv_scales;
+      cp_async4(st_sc + i * 8 + h * 4, ssrc, ok ? 4u : 0u);
+    } else {
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
         const int q = k * 256 + tid;
@@ -868,9 +899,19 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant
         const bool ok = w.nvalid > 0;
         cp_async16(st_sc + tid * 16, ok ? A.nv_scales + tile0 * 512 + tid * 16 : A.nv_scales, ok ? 16u : 0u);
       }
-      asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
     }
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
     __syncthreads();
+    if (kGather) {  // the routed rows' codes: a copy of the staged token codes
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int q = k * 256 + tid;
+        const int i = q >> 2, part = q & 3;
+        if (i < w.nvalid)
+          *reinterpret_cast<uint4 *>(A.nv_codes_out + (w.src_row0 + i) * half_cols + (col0 >> 1) + part * 16) =
+              *reinterpret_cast<const uint4 *>(st_codes + i * 64 + part * 16);
+      }
+    }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int q = u * 256 + tid;
@@ -879,8 +920,9 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant
       uint32_t sc = 0;
       if (i < w.nvalid) {
         raw = *reinterpret_cast<const uint2 *>(st_codes + i * 64 + kb * 8);
-        sc = st_sc[(kb >> 2) * 512 + atom_pos(i, kb)];
+        sc = kGather ? st_sc[i * 8 + kb] : st_sc[(kb >> 2) * 512 + atom_pos(i, kb)];
       }
+      if (kGather) s_nvsc[(kb >> 2) * 512 + atom_pos(i, kb)] = (uint8_t)sc;
       store_f16_products(s_in, i, kb, raw, sc);
     }
   } else {
@@ -1095,7 +1137,7 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(const __grid_constant
   } else if (tid < 64 && A.row_codes != nullptr) {  // zero tiles for padding windows too
     reinterpret_cast<uint4 *>(A.row_scales + ((w.rp0 >> 7) * A.row_ka + (col0 >> 7)) * 512)[tid - 32] =
         reinterpret_cast<const uint4 *>(s_rsc)[tid - 32];
-  } else if (kMode == kSrcBf16ToNvfp4 && tid >= 64 && tid < 128) {  // the two NVFP4 tiles (zeros for padding)
+  } else if (kNvOut && tid >= 64 && tid < 128) {  // the two NVFP4 tiles (zeros for padding)
     reinterpret_cast<uint4 *>(A.nv_scales_out + ((w.rp0 >> 7) * A.nv_ka + (col0 >> 6)) * 512)[tid - 64] =
         reinterpret_cast<const uint4 *>(s_nvsc)[tid - 64];
   }
@@ -1229,6 +1271,35 @@ int launch_requant(const uint8_t *codes, const uint8_t *scales, const float *sg,
   }
   if (nwin == 0) return NV_OK;
   k<<<dim3((unsigned)(cols / 128), (unsigned)nwin), 256, sm, s>>>(A);
+  return launch_status(cudaGetLastError());
+}
+
+// the gathered re-quantization: routed row r of the grouped output is token
+// row row_src[r] of the NVFP4 token matrix (codes [src_rows][cols / 2],
+// batched scale layout); its codes and scales are copied to the routed
+// layout and its values re-quantized (transposed MXFP8 SR)
+int launch_requant_gather(const uint8_t *tok_codes, const uint8_t *tok_scales, const float *sg,
+                          const int32_t *row_src, int64_t src_rows, int64_t rows, int64_t cols,
+                          const int32_t *groups, int E, uint8_t *codes, uint8_t *scales, uint64_t seed, uint64_t off,
+                          uint8_t *out_codes, uint8_t *out_scales, int *status, cudaStream_t s) {
+  MxTArgs A = {};
+  A.nv_codes = tok_codes; A.nv_scales = tok_scales; A.nv_sg = sg; A.row_src = row_src; A.src_rows = src_rows;
+  A.rows = rows; A.cols = cols; A.groups = groups; A.E = E;
+  A.nv_codes_out = codes; A.nv_scales_out = scales; A.nv_ka = cols / 64;
+  A.sr = 1; A.seed = seed; A.off_t = off; A.status = status;
+  A.rk = philox_round_keys(seed);
+  A.out_codes = out_codes; A.out_scales = out_scales;
+  const int64_t P = nvfp4moe_padded_cap(rows, E);
+  A.grouped = 1; A.out_stride = P; A.out_ka = P / 128;
+  const size_t sm = mx_t_smem(true);
+  auto k = mx_transpose_kernel<kSrcNvfp4, false, false, true>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    attr_set = true;
+  }
+  if (P == 0) return NV_OK;
+  k<<<dim3((unsigned)(cols / 128), (unsigned)(P / 128)), 256, sm, s>>>(A);
   return launch_status(cudaGetLastError());
 }
 

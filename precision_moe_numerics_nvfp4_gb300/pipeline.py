@@ -71,7 +71,7 @@ class NvTensor:
         if x_rows is not None:
             if four_six or groups is None:
                 raise ValueError("gathered rows: grouped layout and the plain block rule only")
-            ws = None if sg_in is not None else self.gather_workspace(x.shape[0])
+            ws = self.gather_workspace(x.shape[0])
             N.nvfp4_quantize_requant_gather(x, x_rows, x.shape[0], self.rows, self.cols, groups, sg_in, self.sg,
                                             self.codes, self.scales, ws, seed, offset, mx.codes, mx.scales, stream)
             return
@@ -405,12 +405,13 @@ class MoELayer:
         SwiGLU, or with the SwiGLU epilogue: 3 x 3 + the fused GEMM, the
         outer-scale kernel and one kernel for h + the w2 GEMM; backward = (4
         requants unless fused) + 2 MXFP8 quantizations + 4 GEMMs + SwiGLU
-        backward.  `gathered`: x given as tokens + row map; its amax pass adds
-        the tokens' row-maximum kernel when there are no more tokens than
-        routed rows."""
+        backward.  `gathered`: x given as tokens + row map; with no more tokens
+        than routed rows its amax pass adds the tokens' row-maximum kernel and
+        its quantization the tokens' NVFP4 pass (then the routed rows'
+        copy + re-quantization)."""
         fwd = (3 * 3 + 2 + 1 + 1) if self.fuse_swiglu else (4 * 3 + 2 + 1)
         if gathered and (tokens is None or tokens <= self.M):
-            fwd += 1
+            fwd += 2
         # (with the side-stream amax passes the same kernels run, the amax ones on the side stream)
         if self.per_token:  # x: row amax + quantize; h: from the epilogue's row scales (1) or row amax + quantize
             fwd = (2 + 2 * 3 + 2 + 1 + 1) if self.fuse_swiglu else (2 + 2 * 3 + 2 + 2 + 1)

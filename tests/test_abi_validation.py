@@ -136,11 +136,17 @@ def test_quantize_requant_gather_validation(L):
     assert f(A, A, 64, 128, 192, A, 2, NULL, A, A, A, A, ws, 1, 0, A, A, S) == N.NV_ERR_SHAPE       # cols % 128
     assert f(A, A1, 64, 128, 128, A, 2, NULL, A, A, A, A, ws, 1, 0, A, A, S) == N.NV_ERR_ALIGN      # row map 4-byte
     assert f(A, A, 64, 128, 128, A, 2, NULL, A, A, A, A, 16, 1, 0, A, A, S) == N.NV_ERR_WORKSPACE   # no room
+    # a given outer scale still needs room for the tokens' codes (src_rows <= rows)
+    assert f(A, A, 64, 128, 128, A, 2, A, A, A, A, NULL, 0, 1, 0, A, A, S) == N.NV_ERR_WORKSPACE
     assert f(A, A, 64, 0, 128, A, 2, NULL, A, A, A, A, ws, 1, 0, A, A, S) == N.NV_OK                # empty
 
 
 def test_quantize_gather_workspace_bytes():
-    for src, rows, cols in ((16384, 131072, 4096), (1000, 64, 256), (0, 128, 128)):
+    def r256(n):
+        return (max(n, 1) + 255) // 256 * 256
+    for src, rows, cols in ((16384, 131072, 4096), (1000, 64, 256), (0, 128, 128), (300, 300, 128)):
         want = N.nvfp4moe_quantize_workspace_bytes(1, rows, cols) + (src * 4 + 255) // 256 * 256
+        if src <= rows:  # the tokens' NVFP4 codes and batched scales
+            want += r256(src * cols // 2) + r256(N.nvfp4moe_scale_bytes((src + 127) // 128 * 128, cols // 16))
         assert N.nvfp4moe_quantize_gather_workspace_bytes(src, rows, cols) == want
     assert N.nvfp4moe_quantize_gather_workspace_bytes(-1, 128, 128) == 0
