@@ -270,6 +270,18 @@ def gather_bytes_per_routed_elem(T, M):
 def kernel_units(layer, m):
     """Algorithmic bytes (quantizers) and FLOPs (GEMMs) per call, by call name
     and argument pattern, in the order MoELayer.step issues them."""
+    units = _kernel_units(layer, m)
+    if getattr(layer, "fuse_swiglu_bwd", False):
+        # the w2 dgrad carries the SwiGLU backward in its epilogue: its own
+        # entry point (counted by its FLOPs), no separate SwiGLU backward call
+        fl2, fl13 = units["grouped_gemm_mxfp8_dx"]
+        units["grouped_gemm_mxfp8_dx_swiglu_bwd"] = [fl2]
+        units["grouped_gemm_mxfp8_dx"] = [fl13]
+        del units["nvfp4moe_swiglu_bwd"]
+    return units
+
+
+def _kernel_units(layer, m):
     M, d, I, E = layer.M, layer.d, layer.I, layer.E
     T = m.x.shape[0]  # tokens
     fl13 = 2.0 * M * 2 * I * d

@@ -366,6 +366,27 @@ int grouped_gemm_mxfp8_dx(const uint8_t *g_codes, const uint8_t *g_scales,
                           void *dx, int dx_dtype,
                           void *workspace, size_t workspace_bytes, nv_stream_t stream);
 
+/* ---- grouped MXFP8 dgrad of the down projection with the SwiGLU backward ------
+ * "Block-scaled backward passes" (dh = g2 w2, the dgrad of the down
+ * projection) followed by the SwiGLU backward ("MoE expert layer": h =
+ * silu(gate) * up), in the GEMM's epilogue: each output dh is rounded to bf16
+ * exactly as grouped_gemm_mxfp8_dx writes it, and with the row's gate g and up
+ * u of y13, s = sigmoid(g), dgate = dh u s (1 + g (1 - s)) and dup = dh g s
+ * are computed in fp32 as nvfp4moe_swiglu_bwd computes them.  The output is
+ * exactly grouped_gemm_mxfp8_dx (bf16) followed by nvfp4moe_swiglu_bwd,
+ * without dh in memory.  No counterpart on the pages as one kernel.
+ * g_codes, g_scales, wt_codes, wt_scales, group_offsets, E, M_total, N as
+ * grouped_gemm_mxfp8_dx, with I (its K) the hidden width; y13 [M_total][2I]
+ * bf16 (gate columns, then up), read; dy13 [M_total][2I] bf16 (dgate, then
+ * dup), written; both 32-byte aligned, not overlapping (else NV_ERR_ARG).
+ * N % 128 == 0, I % 128 == 0.
+ */
+int grouped_gemm_mxfp8_dx_swiglu_bwd(const uint8_t *g_codes, const uint8_t *g_scales,
+                                     const uint8_t *wt_codes, const uint8_t *wt_scales,
+                                     const int32_t *group_offsets, int32_t E,
+                                     int64_t M_total, int64_t N, int64_t I,
+                                     const void *y13, void *dy13, nv_stream_t stream);
+
 /* ---- grouped MXFP8 wgrad  dw_e = g_e^T x_q,e ---------------------------------
  * "Block-scaled backward passes": dw = g^T x_q, computed from the quantized
  * forward activations ("Quantized communications": the WGRAD input is the

@@ -625,6 +625,27 @@ int grouped_gemm_mxfp8_dx(const uint8_t *g_codes, const uint8_t *g_scales, const
   return launch_grouped_gemm(p, st, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int grouped_gemm_mxfp8_dx_swiglu_bwd(const uint8_t *g_codes, const uint8_t *g_scales, const uint8_t *wt_codes,
+                                     const uint8_t *wt_scales, const int32_t *group_offsets, int32_t E,
+                                     int64_t M_total, int64_t N, int64_t I, const void *y13, void *dy13,
+                                     nv_stream_t stream) {
+  int r = gemm_common_checks(group_offsets, E, M_total, N, I);
+  if (r != NV_OK) return r;
+  if (!g_codes || !g_scales || !wt_codes || !wt_scales || !y13 || !dy13) return NV_ERR_ARG;
+  if (N % 128 || I % 128) return NV_ERR_SHAPE;
+  if (!al16(g_codes) || !al16(g_scales) || !al16(wt_codes) || !al16(wt_scales) || !al32(y13) || !al32(dy13))
+    return NV_ERR_ALIGN;
+  const uintptr_t yb = reinterpret_cast<uintptr_t>(y13), db = reinterpret_cast<uintptr_t>(dy13);
+  const uintptr_t bytes = (uintptr_t)(M_total * 2 * I * 2);
+  if (yb < db + bytes && db < yb + bytes) return NV_ERR_ARG;  // y13 and dy13 overlap
+  int *st = status_ptr();
+  if (!st) return NV_ERR_CUDA;
+  GemmProblem p = {kGemmMxfp8Dx, g_codes, g_scales, wt_codes, wt_scales, nullptr, nullptr,
+                   group_offsets, E, M_total, N, I, dy13, 0};
+  p.swb_y13 = static_cast<const uint16_t *>(y13);
+  return launch_grouped_gemm(p, st, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int grouped_gemm_mxfp8_dw(const uint8_t *gt_codes, const uint8_t *gt_scales, const uint8_t *xt_codes,
                           const uint8_t *xt_scales, const int32_t *group_offsets, int32_t E, int64_t M_total,
                           int64_t N, int64_t K, float *dw, void *workspace, size_t workspace_bytes,

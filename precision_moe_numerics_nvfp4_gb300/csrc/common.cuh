@@ -100,6 +100,16 @@ __device__ __forceinline__ float bf16_hi_times(uint32_t w, uint16_t m) {
 // reciprocal (1 / inf = 0 for very negative x)
 __device__ __forceinline__ float sigmoidf_fast(float x) { return __frcp_rn(1.0f + __expf(-x)); }
 __device__ __forceinline__ float swiglu_h(float g, float u) { return g * sigmoidf_fast(g) * u; }
+// SwiGLU backward of one element in fp32, as every kernel of the library
+// computes it (the standalone kernel and the fused dgrad epilogue must agree
+// bit for bit): with s = sigmoid(g), dg = ((d u) s) (1 + g (1 - s)) and
+// du = (d g) s, each operation rounded on its own (no fused multiply-add)
+__device__ __forceinline__ void swiglu_bwd_f32(float d, float g, float u, float &dg, float &du) {
+  const float s = sigmoidf_fast(g);
+  const float t = __fadd_rn(1.0f, __fmul_rn(g, __fsub_rn(1.0f, s)));
+  dg = __fmul_rn(__fmul_rn(__fmul_rn(d, u), s), t);
+  du = __fmul_rn(__fmul_rn(d, g), s);
+}
 // bf16 bits of a power of two held as fp32 (exact)
 __device__ __forceinline__ uint16_t pow2_bf16_bits(float p) { return (uint16_t)(__float_as_uint(p) >> 16); }
 

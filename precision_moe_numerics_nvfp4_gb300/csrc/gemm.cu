@@ -201,6 +201,9 @@ struct GemmArgs {
   int8_t *s2f6_codes;
   uint8_t *s2f6_scales;
   RhtSigns rht;
+  // kGemmMxfp8Dx: the SwiGLU backward of the bf16 output dh (the K output
+  // columns) with y13 [M_total][2K] bf16; `out` is then dy13 [M_total][2K]
+  const uint16_t *swb_y13;
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -285,6 +288,85 @@ __device__ __forceinline__ void swiglu_epilogue(const GemmArgs &A, const uint32_
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) hmax = fmaxf(hmax, __shfl_xor_sync(0xFFFFFFFFu, hmax, d));
     if (lane == 0 && hmax > 0.0f) atomicMax(A.h_amax, __float_as_uint(hmax));
+  }
+}
+
+// The y13 lines (gate and up, NC columns from col0) that swiglu_bwd_epilogue
+// will read for row orow, fetched into L2 while the tile's MMAs run (the
+// epilogue warps are idle until its accumulator is complete).
+template <int NC>
+__device__ __forceinline__ void prefetch_swiglu_rows(const GemmArgs &A, int64_t orow, int64_t col0) {
+  const uint16_t *yg = A.swb_y13 + orow * (2 * A.K) + col0;
+#pragma unroll
+  for (int i = 0; i < NC; i += 64) {  // 128-byte lines
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(yg + i));
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(yg + A.K + i));
+  }
+}
+
+// SwiGLU backward epilogue of a warp's 32 output rows of the dgrad GEMM dh =
+// g2 w2 (lane = row; r[0..NC) the lane's fp32 dh of columns col0 .. col0 +
+// NC; rows from `nrows` on do not exist).  Each dh is rounded to bf16 exactly
+// as the plain bf16 output (alpha is 1) and combined with the row's gate and
+// up values of y13 by the SwiGLU backward kernel's arithmetic: dgate to
+// dy13 columns col0 .., dup to I + col0 .. (I = K).  Per 64 columns, the
+// packed dh rows go through the 4 x 4 chunk transpose of
+// store_segment_coalesced, after which lane 4g + i holds 16 columns (chunk i)
+// of rows 4g .. 4g + 3: the y13 loads and dy13 stores then cover whole
+// 128-byte lines (eight per warp instruction) instead of 32 lines of 16 or 32
+// bytes.  Every lane of the warp must call it.
+template <int NC>
+__device__ __forceinline__ void swiglu_bwd_epilogue(const GemmArgs &A, const uint32_t *r, int64_t row0,
+                                                    int64_t col0, int lane, int nrows) {
+  const int64_t I = A.K, ld = 2 * I;
+  const int g = lane >> 2, ci = lane & 3;
+#pragma unroll
+  for (int S = 0; S < NC / 64; ++S) {
+    uint32_t w[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) w[k] = pack_bf16x2(__uint_as_float(r[64 * S + 2 * k]), __uint_as_float(r[64 * S + 2 * k + 1]));
+#pragma unroll
+    for (int d = 2; d >= 1; d >>= 1) {
+      const bool b = (lane & d) != 0;
+#pragma unroll
+      for (int j0 = 0; j0 < 4; ++j0) {
+        if (j0 & d) continue;
+        const int j1 = j0 | d;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const uint32_t got = __shfl_xor_sync(0xFFFFFFFFu, b ? w[8 * j0 + e] : w[8 * j1 + e], d);
+          if (b)
+            w[8 * j0 + e] = got;
+          else
+            w[8 * j1 + e] = got;
+        }
+      }
+    }
+    // w[8k .. 8k + 7]: columns col0 + 64 S + 16 ci .. + 15 of row 4g + k
+    const int64_t c = col0 + 64 * S + 16 * ci;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (4 * g + k >= nrows) continue;
+      const int64_t rr = row0 + 4 * g + k;
+      const uint16_t *yg = A.swb_y13 + rr * ld + c;
+      const uint4 g0 = ld_stream_v4(yg), g1 = ld_stream_v4(yg + 8);
+      const uint4 u0 = ld_stream_v4(yg + I), u1 = ld_stream_v4(yg + I + 8);
+      const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+      const uint32_t uw[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+      uint32_t wg[8], wu[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const uint32_t dw = w[8 * k + e];
+        float a0, b0, a1, b1;
+        swiglu_bwd_f32(bf16_lo(dw), bf16_lo(gw[e]), bf16_lo(uw[e]), a0, b0);
+        swiglu_bwd_f32(bf16_hi(dw), bf16_hi(gw[e]), bf16_hi(uw[e]), a1, b1);
+        wg[e] = f32_to_bf16_bits(a0) | (f32_to_bf16_bits(a1) << 16);
+        wu[e] = f32_to_bf16_bits(b0) | (f32_to_bf16_bits(b1) << 16);
+      }
+      uint16_t *pg = static_cast<uint16_t *>(A.out) + rr * ld + c;
+      st_cs_v8(pg, wg[0], wg[1], wg[2], wg[3], wg[4], wg[5], wg[6], wg[7]);
+      st_cs_v8(pg + I, wu[0], wu[1], wu[2], wu[3], wu[4], wu[5], wu[6], wu[7]);
+    }
   }
 }
 
@@ -379,9 +461,10 @@ __device__ __forceinline__ Tile decode_tile(int t, const GemmArgs &A, const int 
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <int KIND, int STAGES, int NACC, bool kS2f6 = false>
+template <int KIND, int STAGES, int NACC, bool kS2f6 = false, bool kSwb = false>
 __global__ void __launch_bounds__(192, 2)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmArgs A) {
+  static_assert(!kSwb || KIND == kGemmMxfp8Dx, "the SwiGLU backward epilogue is the dgrad's");
   using C = Cfg<KIND, STAGES, NACC>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -563,6 +646,7 @@ __global__ void __launch_bounds__(192, 2)
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++tc) {
       const Tile T = decode_tile<KIND>(t, A, s_off, s_pad);
       const uint32_t acc = tc % NACC;
+      if (kSwb && row < T.mrows) prefetch_swiglu_rows<kBN>(A, T.out_row0 + row, T.out_col0);
       if (!wait_or_abort(smem_u32(&acc_full[acc]), (tc / NACC) & 1, A.wait_limit, s_abort, A.status)) break;
       tc_fence_after();
       const bool store = row < T.mrows;
@@ -588,6 +672,8 @@ __global__ void __launch_bounds__(192, 2)
       if (KIND == kGemmNvfp4FwdSwiglu) {
         // columns 0-63: gate, 64-127: up of hidden features out_col0 .. +63
         swiglu_epilogue(A, r, alpha, store, orow, T.out_col0, lane);
+      } else if (kSwb) {  // dgrad with the SwiGLU backward: the warp's 32 rows together
+        swiglu_bwd_epilogue<kBN>(A, r, T.out_row0 + q * 32, T.out_col0, lane, T.mrows - q * 32);
       } else if (KIND == kGemmMxfp8Dw && A.out_fp32) {
         // wgrad: the warp's 32 fp32 dW rows (all exist; alpha is 1) as whole lines
         uint8_t *row0 = static_cast<uint8_t *>(A.out) + ((T.out_row0 + q * 32) * A.out_ld + T.out_col0) * 4;
@@ -998,12 +1084,13 @@ __device__ __forceinline__ void issue_stage_sf_copies(uint32_t tmem, uint32_t s,
   }
 }
 
-template <int KIND, int STAGES, int BN, int CHUNKS>
+template <int KIND, int STAGES, int BN, int CHUNKS, bool kSwb = false>
 __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BN, CHUNKS>::kThreads,
                                   CfgPair<KIND, STAGES, BN, CHUNKS>::kCtasPerSm)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                              const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                              GemmArgs A) {
+  static_assert(!kSwb || KIND == kGemmMxfp8Dx, "the SwiGLU backward epilogue is the dgrad's");
   using C = CfgPair<KIND, STAGES, BN, CHUNKS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -1226,6 +1313,7 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BN, CHUNKS>::kThreads,
     uint32_t tc = 0;
     for (int t = pair; t < num_tiles; t += npairs, ++tc) {
       const PairTile T = decode_pair<KIND, BN>(t, A, s_off, s_pad, s_pb, s_ord, pair, npairs, num_tiles, cta);
+      if (kSwb && row < T.mrows) prefetch_swiglu_rows<128>(A, T.out_row0 + row, T.out_col0 + half * 128);
       if (!wait_pair(smem_u32(acc_full), tc & 1, A.wait_limit, s_abort, peer_abort, A.status)) break;
       tc_fence_after();
       const bool store = row < T.mrows;
@@ -1261,6 +1349,8 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BN, CHUNKS>::kThreads,
       }
       if (KIND == kGemmNvfp4FwdSwiglu) {
         swiglu_epilogue(A, r, alpha, store, orow, T.out_col0 + half * 64, lane);
+      } else if (kSwb) {  // dgrad with the SwiGLU backward: the warp's 32 rows together
+        swiglu_bwd_epilogue<128>(A, r, T.out_row0 + q * 32, ocol, lane, T.mrows - q * 32);
       } else if (KIND == kGemmMxfp8Dw && A.out_fp32) {
         // wgrad: fp32 dW rows are 512 bytes per lane and the stores are the
         // epilogue's bottleneck, so the warp writes them as whole lines (the
@@ -1408,12 +1498,12 @@ static int num_sms() {
   return n[dev];
 }
 
-template <int KIND, int STAGES, int NACC, bool kS2f6 = false>
+template <int KIND, int STAGES, int NACC, bool kS2f6 = false, bool kSwb = false>
 static int run(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &args, int64_t max_tiles,
                cudaStream_t s) {
   using C = Cfg<KIND, STAGES, NACC>;
   const size_t sm = C::smem_bytes(args.E);
-  auto k = grouped_gemm_kernel<KIND, STAGES, NACC, kS2f6>;
+  auto k = grouped_gemm_kernel<KIND, STAGES, NACC, kS2f6, kSwb>;
   static size_t attr_bytes = 0;  // largest dynamic shared memory requested so far
   if (sm > attr_bytes) {
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) != cudaSuccess)
@@ -1429,12 +1519,12 @@ static int run(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &arg
   return cudaGetLastError() == cudaSuccess ? NV_OK : NV_ERR_CUDA;
 }
 
-template <int KIND, int STAGES, int BN, int CHUNKS = 1>
+template <int KIND, int STAGES, int BN, int CHUNKS = 1, bool kSwb = false>
 static int run_pair(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tsa, const CUtensorMap &tsb,
                     const GemmArgs &args, int64_t max_tiles, cudaStream_t s) {
   using C = CfgPair<KIND, STAGES, BN, CHUNKS>;
   const size_t sm = C::smem_bytes(args.E);
-  auto k = grouped_gemm_pair_kernel<KIND, STAGES, BN, CHUNKS>;
+  auto k = grouped_gemm_pair_kernel<KIND, STAGES, BN, CHUNKS, kSwb>;
   static size_t attr_bytes = 0;
   static int max_pairs = 0;  // co-resident CTA pairs at the largest shared-memory size requested so far
   cudaLaunchConfig_t cfg = {};
@@ -1511,6 +1601,7 @@ int launch_grouped_gemm(const GemmProblem &p, int *status, cudaStream_t s) {
   a.a_sg_rows = p.a_sg_rows; a.h_amax_rows = p.h_amax_rows;
   a.s2f6_codes = p.s2f6_codes; a.s2f6_scales = p.s2f6_scales;
   if (p.s2f6_codes) a.rht = make_signs(p.rht_signs);
+  a.swb_y13 = p.swb_y13;
   const int64_t out_cols = (p.kind == kGemmNvfp4Fwd || p.kind == kGemmNvfp4FwdSwiglu) ? p.N : p.K;
   CUtensorMap ta, tb;
   bool ok;
@@ -1626,6 +1717,7 @@ int launch_grouped_gemm(const GemmProblem &p, int *status, cudaStream_t s) {
           !make_map_chunks(&wb, p.b_codes, row_bytes, b_rows, 128) || !make_sf_map(&wsa, p.a_scales, a_sf_bytes, 8) ||
           !make_sf_map_pair_chunks(&wsb, p.b_scales, b_sf_bytes / (a.ka * 512), a.ka, 1, 4))
         return NV_ERR_CUDA;
+      if (dx && p.swb_y13) return run_pair<kGemmMxfp8Dx, 3, 256, 2, true>(wa, wb, wsa, wsb, b, pair_tiles, s);
       return dx ? run_pair<kGemmMxfp8Dx, 3, 256, 2>(wa, wb, wsa, wsb, b, pair_tiles, s)
                 : run_pair<kGemmMxfp8Dw, 3, 256, 2>(wa, wb, wsa, wsb, b, pair_tiles, s);
     }
@@ -1634,13 +1726,17 @@ int launch_grouped_gemm(const GemmProblem &p, int *status, cudaStream_t s) {
         case kGemmNvfp4Fwd: return run_pair<kGemmNvfp4Fwd, 5, 256>(ta, *tbp, tsa, tsb, b, pair_tiles, s);
         case kGemmNvfp4FwdSwiglu:
           return run_pair<kGemmNvfp4FwdSwiglu, 5, 256>(ta, *tbp, tsa, tsb, b, pair_tiles, s);
-        case kGemmMxfp8Dx: return run_pair<kGemmMxfp8Dx, 3, 256, 2>(ta, *tbp, tsa, tsb, b, pair_tiles, s);
+        case kGemmMxfp8Dx:
+          return p.swb_y13 ? run_pair<kGemmMxfp8Dx, 3, 256, 2, true>(ta, *tbp, tsa, tsb, b, pair_tiles, s)
+                           : run_pair<kGemmMxfp8Dx, 3, 256, 2>(ta, *tbp, tsa, tsb, b, pair_tiles, s);
         default: return run_pair<kGemmMxfp8Dw, 3, 256, 2>(ta, *tbp, tsa, tsb, b, pair_tiles, s);
       }
     }
     switch (p.kind) {
       case kGemmNvfp4Fwd: return run_pair<kGemmNvfp4Fwd, 3, 128>(ta, *tbp, tsa, tsb, b, pair_tiles, s);
-      case kGemmMxfp8Dx: return run_pair<kGemmMxfp8Dx, 4, 128>(ta, *tbp, tsa, tsb, b, pair_tiles, s);
+      case kGemmMxfp8Dx:
+        return p.swb_y13 ? run_pair<kGemmMxfp8Dx, 4, 128, 1, true>(ta, *tbp, tsa, tsb, b, pair_tiles, s)
+                         : run_pair<kGemmMxfp8Dx, 4, 128>(ta, *tbp, tsa, tsb, b, pair_tiles, s);
       default: return run_pair<kGemmMxfp8Dw, 4, 128>(ta, *tbp, tsa, tsb, b, pair_tiles, s);
     }
   }
@@ -1650,6 +1746,9 @@ int launch_grouped_gemm(const GemmProblem &p, int *status, cudaStream_t s) {
       return two_per_sm ? run<kGemmNvfp4Fwd, 3, 1>(ta, tb, a, max_tiles, s)
                         : run<kGemmNvfp4Fwd, 6, 2>(ta, tb, a, max_tiles, s);
     case kGemmMxfp8Dx:
+      if (p.swb_y13)
+        return two_per_sm ? run<kGemmMxfp8Dx, 3, 1, false, true>(ta, tb, a, max_tiles, s)
+                          : run<kGemmMxfp8Dx, 6, 2, false, true>(ta, tb, a, max_tiles, s);
       return two_per_sm ? run<kGemmMxfp8Dx, 3, 1>(ta, tb, a, max_tiles, s)
                         : run<kGemmMxfp8Dx, 6, 2>(ta, tb, a, max_tiles, s);
     default:

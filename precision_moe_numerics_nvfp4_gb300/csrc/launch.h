@@ -87,6 +87,9 @@ struct GemmProblem {
   int8_t *s2f6_codes;
   uint8_t *s2f6_scales;
   uint32_t rht_signs;
+  // kGemmMxfp8Dx with bf16 output: the SwiGLU backward of the output dh with
+  // y13 [M_total][2K] bf16; out is then dy13 [M_total][2K] bf16
+  const uint16_t *swb_y13;
 };
 int launch_grouped_gemm(const GemmProblem &p, int *status, cudaStream_t s);
 int set_gemm_variant(int v);  // 0 automatic, 1-3 forced (see nvfp4moe_set_gemm_kernel)

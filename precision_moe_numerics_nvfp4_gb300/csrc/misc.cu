@@ -48,9 +48,10 @@ __global__ void __launch_bounds__(256) swiglu_bwd_kernel(const uint16_t *__restr
       uint32_t a[2], b[2];
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
-        const float s = sigmoidf_fast(gg[q]);
-        a[q] = f32_to_bf16_bits(dd[q] * uu[q] * s * (1.0f + gg[q] * (1.0f - s)));
-        b[q] = f32_to_bf16_bits(dd[q] * gg[q] * s);
+        float dg, du;
+        swiglu_bwd_f32(dd[q], gg[q], uu[q], dg, du);
+        a[q] = f32_to_bf16_bits(dg);
+        b[q] = f32_to_bf16_bits(du);
       }
       og[k] = a[0] | (a[1] << 16);
       ou[k] = b[0] | (b[1] << 16);

@@ -52,6 +52,7 @@ _SIGS = {
                                                      _P, _P]),
     "grouped_gemm_mxfp8_dx": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I64, _I64, _I64, _P, ctypes.c_int,
                                              _P, _SZ, _P]),
+    "grouped_gemm_mxfp8_dx_swiglu_bwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I64, _I64, _I64, _P, _P, _P]),
     "grouped_gemm_mxfp8_dw": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I64, _I64, _I64, _P, _P, _SZ, _P]),
     "rht32_s2f6_quantize": (ctypes.c_int, [_P, _I64, _I64, ctypes.c_uint32, _P, _P, _P]),
     "s2f6_dequantize_rht32_inverse": (ctypes.c_int, [_P, _P, _I64, _I64, ctypes.c_uint32, _P, ctypes.c_int, _P]),
@@ -350,6 +351,13 @@ def grouped_gemm_mxfp8_dx(g_codes, g_scales, wt_codes, wt_scales, group_offsets,
     return _check("grouped_gemm_mxfp8_dx", lib().grouped_gemm_mxfp8_dx(
         _ptr(g_codes), _ptr(g_scales), _ptr(wt_codes), _ptr(wt_scales), _ptr(group_offsets), E, M_total, N, K,
         _ptr(dx), dx_dtype, _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def grouped_gemm_mxfp8_dx_swiglu_bwd(g_codes, g_scales, wt_codes, wt_scales, group_offsets, E, M_total, N, I, y13,
+                                     dy13, stream=None):
+    return _check("grouped_gemm_mxfp8_dx_swiglu_bwd", lib().grouped_gemm_mxfp8_dx_swiglu_bwd(
+        _ptr(g_codes), _ptr(g_scales), _ptr(wt_codes), _ptr(wt_scales), _ptr(group_offsets), E, M_total, N, I,
+        _ptr(y13), _ptr(dy13), _stream(stream)))
 
 
 def grouped_gemm_mxfp8_dw(gt_codes, gt_scales, xt_codes, xt_scales, group_offsets, E, M_total, N, K, dw,

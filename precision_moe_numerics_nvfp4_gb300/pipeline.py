@@ -166,7 +166,10 @@ class MoELayer:
     dequant_transpose_requant_sr calls in the backward instead.  The w13 GEMM
     computes SwiGLU and the outer scale of h in its epilogue
     (grouped_gemm_nvfp4_fwd_swiglu) when d_ff % 128 == 0; `fuse_swiglu=False`
-    runs the GEMM, nvfp4moe_swiglu_fwd and the amax pass of h instead.  Every
+    runs the GEMM, nvfp4moe_swiglu_fwd and the amax pass of h instead.  The
+    dgrad of w2 applies the SwiGLU backward in its epilogue
+    (grouped_gemm_mxfp8_dx_swiglu_bwd, dh never stored) when d_ff % 128 == 0;
+    `fuse_swiglu_bwd=False` stores dh and runs nvfp4moe_swiglu_bwd.  Every
     choice gives the same results, bit for bit.
 
     `per_token=True` quantizes the activations x and h with one outer scale
@@ -175,7 +178,7 @@ class MoELayer:
     Over Six block rule.  Both change the results."""
 
     def __init__(self, M, d_model, d_ff, E, device="cuda", backward=True, fuse_requant=True, fuse_swiglu=True,
-                 per_token=False, four_over_six=False, overlap_amax=False):
+                 per_token=False, four_over_six=False, overlap_amax=False, fuse_swiglu_bwd=True):
         if per_token and four_over_six:
             raise ValueError("per-token scales and Four Over Six are separate options")
         dev = torch.device(device)
@@ -203,6 +206,7 @@ class MoELayer:
             self.x_sg_rows = _empty(M, F32, dev)
             self.h_sg_rows = _empty(M, F32, dev)
         self.fuse_requant = fuse_requant and backward
+        self.fuse_swiglu_bwd = fuse_swiglu_bwd and d_ff % 128 == 0
         self._requant_seed = None  # seed of the operands the last forward re-quantized
         if not backward:  # forward-only use (sampling): no backward buffers
             return
@@ -213,7 +217,7 @@ class MoELayer:
         self.w2t = MxTransposed(d_model, d_ff, dev, batch=E)
         self.g2_row = MxRows(M, d_model, dev, E=E)
         self.g2t = MxTransposed(M, d_model, dev, E=E)
-        self.dh = _empty((M, d_ff), BF16, dev)
+        self.dh = None if self.fuse_swiglu_bwd else _empty((M, d_ff), BF16, dev)
         self.dy13 = _empty((M, I2), BF16, dev)
         self.dy13_row = MxRows(M, I2, dev, E=E)
         self.dy13t = MxTransposed(M, I2, dev, E=E)
@@ -366,12 +370,18 @@ class MoELayer:
         # down projection: dh = g2 w2, dW2 = g2^T h_q
         N.mxfp8_quantize(g2, M, d, groups, N.NV_SR, seed, OFF_G2_ROW, OFF_G2_T, self.g2_row.codes,
                          self.g2_row.scales, self.g2t.codes, self.g2t.scales, stream)
-        N.grouped_gemm_mxfp8_dx(self.g2_row.codes, self.g2_row.scales, self.w2t.codes, self.w2t.scales, groups, E,
-                                M, d, I, self.dh, N.NV_OUT_BF16, None, stream)
+        # (fused: the SwiGLU backward in the dgrad's epilogue, dh never stored)
+        if self.fuse_swiglu_bwd:
+            N.grouped_gemm_mxfp8_dx_swiglu_bwd(self.g2_row.codes, self.g2_row.scales, self.w2t.codes,
+                                               self.w2t.scales, groups, E, M, d, I, self.y13, self.dy13, stream)
+        else:
+            N.grouped_gemm_mxfp8_dx(self.g2_row.codes, self.g2_row.scales, self.w2t.codes, self.w2t.scales, groups,
+                                    E, M, d, I, self.dh, N.NV_OUT_BF16, None, stream)
         N.grouped_gemm_mxfp8_dw(self.g2t.codes, self.g2t.scales, self.ht.codes, self.ht.scales, groups, E, M, d, I,
                                 self.dw2, None, stream)
-        # SwiGLU backward, then gate/up: dx = dy13 w13, dW13 = dy13^T x_q
-        N.nvfp4moe_swiglu_bwd(self.dh, self.y13, M, I, self.dy13, stream)
+        # SwiGLU backward (unless fused above), then gate/up: dx = dy13 w13, dW13 = dy13^T x_q
+        if not self.fuse_swiglu_bwd:
+            N.nvfp4moe_swiglu_bwd(self.dh, self.y13, M, I, self.dy13, stream)
         N.mxfp8_quantize(self.dy13, M, I2, groups, N.NV_SR, seed, OFF_DY13_ROW, OFF_DY13_T, self.dy13_row.codes,
                          self.dy13_row.scales, self.dy13t.codes, self.dy13t.scales, stream)
         N.grouped_gemm_mxfp8_dx(self.dy13_row.codes, self.dy13_row.scales, self.w13t.codes, self.w13t.scales,
@@ -415,7 +425,8 @@ class MoELayer:
         # (with the side-stream amax passes the same kernels run, the amax ones on the side stream)
         if self.per_token:  # x: row amax + quantize; h: from the epilogue's row scales (1) or row amax + quantize
             fwd = (2 + 2 * 3 + 2 + 1 + 1) if self.fuse_swiglu else (2 + 2 * 3 + 2 + 2 + 1)
-        return fwd + (0 if self.fuse_requant else 4) + (2 + 4 + 1)
+        # backward: 2 MXFP8 quantizations + 4 GEMMs (+ the SwiGLU backward unless in the dgrad epilogue)
+        return fwd + (0 if self.fuse_requant else 4) + (2 + 4 + (0 if self.fuse_swiglu_bwd else 1))
 
 
 class HostStaged:

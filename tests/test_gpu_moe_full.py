@@ -228,14 +228,27 @@ def test_gradient_quantization(run):
 
 # ---- backward GEMMs and SwiGLU backward --------------------------------------------
 def test_backward_gemms_and_swiglu(run):
-    layer, o, P = run["layer"], run["o"], run["P"]
+    layer, o, P, M = run["layer"], run["o"], run["P"], run["M"]
+    # the step applied the SwiGLU backward in the w2 dgrad's epilogue (dh never
+    # stored): it must equal the dgrad's bf16 dh followed by the SwiGLU
+    # backward kernel, over the whole tensor
+    assert layer.fuse_swiglu_bwd and layer.dh is None
+    dh_full = gh.gempty((M, I), dtype=torch.bfloat16, device=gh.dev())
+    dy13_ref = gh.gempty((M, 2 * I), dtype=torch.bfloat16, device=gh.dev())
+    go = run["m"].group_offsets
+    N.grouped_gemm_mxfp8_dx(layer.g2_row.codes, layer.g2_row.scales, layer.w2t.codes, layer.w2t.scales, go, E, M, D,
+                            I, dh_full, N.NV_OUT_BF16)
+    N.nvfp4moe_swiglu_bwd(dh_full, layer.y13, M, I, dy13_ref)
+    torch.cuda.synchronize()
+    assert N.nvfp4moe_get_device_status() == 0
+    assert torch.equal(dy13_ref.view(torch.int16), layer.dy13.view(torch.int16))
     for e, rows in run["rows"].items():
         # dh = g2 w2 (dgrad of the down projection)
         gc, gs = _mx_rows(layer.g2_row.codes, layer.g2_row.scales, rows, D, run["rmap"])
         wc, ws = _mx_w_expert(layer.w2t, e, I, D)
         ref, bound = G.grouped_rows(MX.dequantize_f64(gc, gs), MX.dequantize_f64(wc, ws)[None],
                                     np.array([0, len(rows)]))
-        dh = _bf16_rows(layer.dh, rows)
+        dh = _bf16_rows(dh_full, rows)
         assert G.within_bound(dh, ref, bound, bf16_out=True).all()
         # dy13 = SwiGLU backward
         y13 = _bf16_rows(layer.y13, rows).astype(np.float64)
