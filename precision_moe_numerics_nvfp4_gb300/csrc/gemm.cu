@@ -314,58 +314,75 @@ __device__ __forceinline__ void prefetch_swiglu_rows(const GemmArgs &A, int64_t 
 // store_segment_coalesced, after which lane 4g + i holds 16 columns (chunk i)
 // of rows 4g .. 4g + 3: the y13 loads and dy13 stores then cover whole
 // 128-byte lines (eight per warp instruction) instead of 32 lines of 16 or 32
-// bytes.  Every lane of the warp must call it.
+// bytes.  y13, dy13 and their row length 32-byte aligned.  Every lane of the
+// warp must call it.
 template <int NC>
 __device__ __forceinline__ void swiglu_bwd_epilogue(const GemmArgs &A, const uint32_t *r, int64_t row0,
                                                     int64_t col0, int lane, int nrows) {
+  static_assert(NC % 64 == 0, "64-column segments");
   const int64_t I = A.K, ld = 2 * I;
   const int g = lane >> 2, ci = lane & 3;
+  // every segment's dh packed first (the fp32 values are then dead), so that
+  // a segment's y13 loads can all be in flight while its dh is transposed
+  uint32_t w[NC / 64][32];
+#pragma unroll
+  for (int S = 0; S < NC / 64; ++S)
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+      w[S][k] = pack_bf16x2(__uint_as_float(r[64 * S + 2 * k]), __uint_as_float(r[64 * S + 2 * k + 1]));
 #pragma unroll
   for (int S = 0; S < NC / 64; ++S) {
-    uint32_t w[32];
-#pragma unroll
-    for (int k = 0; k < 32; ++k) w[k] = pack_bf16x2(__uint_as_float(r[64 * S + 2 * k]), __uint_as_float(r[64 * S + 2 * k + 1]));
-#pragma unroll
-    for (int d = 2; d >= 1; d >>= 1) {
-      const bool b = (lane & d) != 0;
-#pragma unroll
-      for (int j0 = 0; j0 < 4; ++j0) {
-        if (j0 & d) continue;
-        const int j1 = j0 | d;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const uint32_t got = __shfl_xor_sync(0xFFFFFFFFu, b ? w[8 * j0 + e] : w[8 * j1 + e], d);
-          if (b)
-            w[8 * j0 + e] = got;
-          else
-            w[8 * j1 + e] = got;
-        }
-      }
-    }
-    // w[8k .. 8k + 7]: columns col0 + 64 S + 16 ci .. + 15 of row 4g + k
+    // after the transpose lane 4g + ci holds columns col0 + 64 S + 16 ci ..
+    // + 15 of rows 4g .. 4g + 3: their gate and up, 32 bytes each, two rows'
+    // worth in flight at a time (the first pair's during the transpose)
     const int64_t c = col0 + 64 * S + 16 * ci;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      if (4 * g + k >= nrows) continue;
-      const int64_t rr = row0 + 4 * g + k;
-      const uint16_t *yg = A.swb_y13 + rr * ld + c;
-      const uint4 g0 = ld_stream_v4(yg), g1 = ld_stream_v4(yg + 8);
-      const uint4 u0 = ld_stream_v4(yg + I), u1 = ld_stream_v4(yg + I + 8);
-      const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-      const uint32_t uw[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-      uint32_t wg[8], wu[8];
+    for (int kb = 0; kb < 4; kb += 2) {
+      uint32_t gl[2][8], ul[2][8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const uint32_t dw = w[8 * k + e];
-        float a0, b0, a1, b1;
-        swiglu_bwd_f32(bf16_lo(dw), bf16_lo(gw[e]), bf16_lo(uw[e]), a0, b0);
-        swiglu_bwd_f32(bf16_hi(dw), bf16_hi(gw[e]), bf16_hi(uw[e]), a1, b1);
-        wg[e] = f32_to_bf16_bits(a0) | (f32_to_bf16_bits(a1) << 16);
-        wu[e] = f32_to_bf16_bits(b0) | (f32_to_bf16_bits(b1) << 16);
+      for (int k = 0; k < 2; ++k) {
+        if (4 * g + kb + k < nrows) {
+          const uint16_t *yg = A.swb_y13 + (row0 + 4 * g + kb + k) * ld + c;
+          ld_stream_v8(yg, gl[k]);
+          ld_stream_v8(yg + I, ul[k]);
+        }
       }
-      uint16_t *pg = static_cast<uint16_t *>(A.out) + rr * ld + c;
-      st_cs_v8(pg, wg[0], wg[1], wg[2], wg[3], wg[4], wg[5], wg[6], wg[7]);
-      st_cs_v8(pg + I, wu[0], wu[1], wu[2], wu[3], wu[4], wu[5], wu[6], wu[7]);
+      if (kb == 0) {
+#pragma unroll
+        for (int d = 2; d >= 1; d >>= 1) {
+          const bool b = (lane & d) != 0;
+#pragma unroll
+          for (int j0 = 0; j0 < 4; ++j0) {
+            if (j0 & d) continue;
+            const int j1 = j0 | d;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const uint32_t got = __shfl_xor_sync(0xFFFFFFFFu, b ? w[S][8 * j0 + e] : w[S][8 * j1 + e], d);
+              if (b)
+                w[S][8 * j0 + e] = got;
+              else
+                w[S][8 * j1 + e] = got;
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        if (4 * g + kb + k >= nrows) continue;
+        uint32_t wg[8], wu[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const uint32_t dw = w[S][8 * (kb + k) + e];
+          float a0, b0, a1, b1;
+          swiglu_bwd_f32(bf16_lo(dw), bf16_lo(gl[k][e]), bf16_lo(ul[k][e]), a0, b0);
+          swiglu_bwd_f32(bf16_hi(dw), bf16_hi(gl[k][e]), bf16_hi(ul[k][e]), a1, b1);
+          wg[e] = f32_to_bf16_bits(a0) | (f32_to_bf16_bits(a1) << 16);
+          wu[e] = f32_to_bf16_bits(b0) | (f32_to_bf16_bits(b1) << 16);
+        }
+        uint16_t *pg = static_cast<uint16_t *>(A.out) + (row0 + 4 * g + kb + k) * ld + c;
+        st_cs_v8(pg, wg[0], wg[1], wg[2], wg[3], wg[4], wg[5], wg[6], wg[7]);
+        st_cs_v8(pg + I, wu[0], wu[1], wu[2], wu[3], wu[4], wu[5], wu[6], wu[7]);
+      }
     }
   }
 }
