@@ -908,7 +908,7 @@ struct CfgPair {
   static constexpr int ACC_COLS = BN;
   static constexpr int TMEM_COLS = cpow2(ACC_COLS + STAGES * SF_COLS);
   // full, empty, acc_full, acc_empty, mma_done, then (with copy issuers)
-  // sf_full and sf_land per stage and one drain barrier per issuer
+  // sf_land per stage and one drain barrier per issuer
   static constexpr int kCtasPerSm = BN == 128 ? 2 : 1;
   // A tcgen05.cp holds its issuing thread for about 64 cycles and runs
   // alongside the MMAs only when another thread issues it, so with one pair
@@ -917,7 +917,7 @@ struct CfgPair {
   // The 256 x 128 variant (two pairs per SM pair) keeps the copies on the MMA
   // thread: its registers leave no room for more warps.
   static constexpr int kSfWarps = kCtasPerSm == 1 ? 2 : 0;
-  static constexpr int NBARS = 2 * STAGES + 3 + (kSfWarps ? 2 * STAGES + kSfWarps : 0);
+  static constexpr int NBARS = 2 * STAGES + 3 + (kSfWarps ? STAGES + kSfWarps : 0);
   static constexpr int kEpi0 = 2 + kSfWarps;            // first epilogue warp
   // Wide loads (two-chunk stages with copy issuers): a stage's two k-chunks
   // come in one load per tensor (A, B: 3-D boxes of two 128-byte k-chunks;
@@ -1137,17 +1137,17 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BN, CHUNKS>::kThreads,
   uint64_t *full = bars, *empty = bars + STAGES, *acc_full = bars + 2 * STAGES, *acc_empty = acc_full + 1;
   uint64_t *mma_done = acc_empty + 1;
   // with copy issuers: sf_land (a stage's scale tiles have landed, loaded
-  // ahead of its operand tiles), sf_full (they are in tensor memory), sf_done
-  uint64_t *sf_full = mma_done + 1, *sf_land = sf_full + STAGES, *sf_done = sf_land + STAGES;
+  // ahead of its operand tiles) and sf_done; a stage's "full" barrier then
+  // also takes one commit per issuer, completing once its operand tiles have
+  // landed and its scale tiles are in tensor memory, so that the MMA thread
+  // waits once per stage (each wait idles the tensor pipe ~200 cycles)
+  uint64_t *sf_land = mma_done + 1, *sf_done = sf_land + STAGES;
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(mma_done), 1);
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&full[s]), 1 + C::kSfWarps);  // the producer's arrival (+ one commit per issuer)
       mbar_init(smem_u32(&empty[s]), 1);
-      if (C::kSfWarps) {
-        mbar_init(smem_u32(&sf_full[s]), C::kSfWarps);  // one commit per issuer
-        mbar_init(smem_u32(&sf_land[s]), 1);
-      }
+      if (C::kSfWarps) mbar_init(smem_u32(&sf_land[s]), 1);
     }
     for (int w = 0; w < C::kSfWarps; ++w) mbar_init(smem_u32(&sf_done[w]), 1);
     mbar_init(smem_u32(acc_full), 1);
@@ -1250,9 +1250,7 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BN, CHUNKS>::kThreads,
       for (int ks = 0; ks < T.nk; ks += CHUNKS, ++it) {
         const uint32_t s = it % STAGES;
         const int nc = T.nk - ks < CHUNKS ? T.nk - ks : CHUNKS;
-        if (!wait_pair(smem_u32(&full[s]), (it / STAGES) & 1, A.wait_limit, s_abort, peer_abort, A.status) ||
-            (C::kSfWarps &&
-             !wait_pair(smem_u32(&sf_full[s]), (it / STAGES) & 1, A.wait_limit, s_abort, peer_abort, A.status))) {
+        if (!wait_pair(smem_u32(&full[s]), (it / STAGES) & 1, A.wait_limit, s_abort, peer_abort, A.status)) {
           ok = false;
           break;
         }
@@ -1293,8 +1291,9 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BN, CHUNKS>::kThreads,
   } else if (warp >= 2 && warp < C::kEpi0) {
     // ---- scale-copy issuers (even CTA only) ------------------------------------------
     // each stage, once its scale tiles have landed: this issuer's half of
-    // the stage's copies, then a commit on the stage's sf_full barrier, which
-    // completes when both halves have been written to tensor memory.  A
+    // the stage's copies, then a commit on the stage's full barrier, which
+    // completes when both halves have been written to tensor memory (and the
+    // stage's operand tiles have landed).  A
     // stage's buffer is rewritten only after its refill has landed, i.e.
     // after the MMAs that read it have completed (the producer refills a
     // stage after its MMAs' commit).
@@ -1314,7 +1313,7 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BN, CHUNKS>::kThreads,
           tc_fence_after();
           issue_stage_sf_copies<C, BN, CHUNKS>(tmem, s, nc, smem_u32(sSFA + s * C::SFA_BYTES),
                                                smem_u32(sSFB + s * C::SFB_BYTES), part);
-          tc_commit_pair_local(smem_u32(&sf_full[s]));
+          tc_commit_pair_local(smem_u32(&full[s]));
         }
       }
       // every copy this thread issued has landed before tensor memory is freed
