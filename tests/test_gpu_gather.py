@@ -30,7 +30,7 @@ def _pair(M, K, E):
 # the amax pass: tokens read once (T <= M) or the routed rows read (T > M)
 @pytest.mark.parametrize("sizes,T,K,given", [([5, 0, 295, 130], 300, 256, False), ([128, 1, 0, 257], 97, 512, True),
                                              ([0, 640], 640, 128, False), ([40, 0, 24], 1000, 256, False),
-                                             ([128, 1, 0, 257], 97, 512, False)])
+                                             ([128, 1, 0, 257], 97, 512, False), ([40, 0, 24], 1000, 256, True)])
 def test_gather_equals_materialized_rows(sizes, T, K, given):
     g = torch.Generator(device="cuda").manual_seed(sum(sizes) + K)
     x = (torch.randn((T, K), generator=g, device="cuda") * 3).to(torch.bfloat16)
