@@ -93,12 +93,18 @@ __device__ __forceinline__ float bf16_hi_times(uint32_t w, uint16_t m) {
   return d;
 }
 // SwiGLU in fp32 as every kernel of the library computes it (the elementwise
-// kernels and the fused GEMM epilogue must agree bit for bit):
+// kernels and the fused GEMM epilogues must agree bit for bit):
 // h = (g * sigmoid(g)) * u with sigmoid(x) = 1 / (1 + e^-x), the exponential
-// from the hardware approximation (relative error ~1e-6 at these magnitudes,
-// far below the bf16 rounding that follows) and a correctly rounded
-// reciprocal (1 / inf = 0 for very negative x)
-__device__ __forceinline__ float sigmoidf_fast(float x) { return __frcp_rn(1.0f + __expf(-x)); }
+// and the reciprocal both from the hardware approximations (relative error
+// ~1e-6 and ~1 ulp of fp32 at these magnitudes, far below the bf16 rounding
+// that follows; 1 / inf = 0 for very negative x).  The approximate
+// reciprocal is one instruction where the correctly rounded one is a short
+// sequence, which shows in the GEMM epilogues that evaluate it per element.
+__device__ __forceinline__ float sigmoidf_fast(float x) {
+  float r;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(1.0f + __expf(-x)));
+  return r;
+}
 __device__ __forceinline__ float swiglu_h(float g, float u) { return g * sigmoidf_fast(g) * u; }
 // SwiGLU backward of one element in fp32, as every kernel of the library
 // computes it (the standalone kernel and the fused dgrad epilogue must agree
