@@ -116,6 +116,41 @@ __device__ __forceinline__ void swiglu_bwd_f32(float d, float g, float u, float 
   dg = __fmul_rn(__fmul_rn(__fmul_rn(d, u), s), t);
   du = __fmul_rn(__fmul_rn(d, g), s);
 }
+// The same for two elements at once, with packed fp32x2 arithmetic (each lane
+// rounded exactly as the single operation): bit-identical to two calls of
+// swiglu_bwd_f32, in fewer instructions.
+__device__ __forceinline__ uint64_t f32x2_pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f32x2_unpack(uint64_t v, float &a, float &b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f32x2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f32x2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f32x2_sub(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ void swiglu_bwd_f32x2(float d0, float d1, float g0, float g1, float u0, float u1,
+                                                 float &dg0, float &dg1, float &du0, float &du1) {
+  const uint64_t one = f32x2_pack(1.0f, 1.0f);
+  const uint64_t d = f32x2_pack(d0, d1), g = f32x2_pack(g0, g1), u = f32x2_pack(u0, u1);
+  const uint64_t s = f32x2_pack(sigmoidf_fast(g0), sigmoidf_fast(g1));
+  const uint64_t t = f32x2_add(one, f32x2_mul(g, f32x2_sub(one, s)));
+  f32x2_unpack(f32x2_mul(f32x2_mul(f32x2_mul(d, u), s), t), dg0, dg1);
+  f32x2_unpack(f32x2_mul(f32x2_mul(d, g), s), du0, du1);
+}
 // bf16 bits of a power of two held as fp32 (exact)
 __device__ __forceinline__ uint16_t pow2_bf16_bits(float p) { return (uint16_t)(__float_as_uint(p) >> 16); }
 

@@ -374,8 +374,8 @@ __device__ __forceinline__ void swiglu_bwd_epilogue(const GemmArgs &A, const uin
         for (int e = 0; e < 8; ++e) {
           const uint32_t dw = w[S][8 * (kb + k) + e];
           float a0, b0, a1, b1;
-          swiglu_bwd_f32(bf16_lo(dw), bf16_lo(gl[k][e]), bf16_lo(ul[k][e]), a0, b0);
-          swiglu_bwd_f32(bf16_hi(dw), bf16_hi(gl[k][e]), bf16_hi(ul[k][e]), a1, b1);
+          swiglu_bwd_f32x2(bf16_lo(dw), bf16_hi(dw), bf16_lo(gl[k][e]), bf16_hi(gl[k][e]), bf16_lo(ul[k][e]),
+                           bf16_hi(ul[k][e]), a0, a1, b0, b1);
           wg[e] = f32_to_bf16_bits(a0) | (f32_to_bf16_bits(a1) << 16);
           wu[e] = f32_to_bf16_bits(b0) | (f32_to_bf16_bits(b1) << 16);
         }

@@ -45,16 +45,10 @@ __global__ void __launch_bounds__(256) swiglu_bwd_kernel(const uint16_t *__restr
       float gg[2] = {bf16_lo(gw[k]), bf16_hi(gw[k])};
       float uu[2] = {bf16_lo(uw[k]), bf16_hi(uw[k])};
       float dd[2] = {bf16_lo(dw[k]), bf16_hi(dw[k])};
-      uint32_t a[2], b[2];
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        float dg, du;
-        swiglu_bwd_f32(dd[q], gg[q], uu[q], dg, du);
-        a[q] = f32_to_bf16_bits(dg);
-        b[q] = f32_to_bf16_bits(du);
-      }
-      og[k] = a[0] | (a[1] << 16);
-      ou[k] = b[0] | (b[1] << 16);
+      float dg0, dg1, du0, du1;
+      swiglu_bwd_f32x2(dd[0], dd[1], gg[0], gg[1], uu[0], uu[1], dg0, dg1, du0, du1);
+      og[k] = f32_to_bf16_bits(dg0) | (f32_to_bf16_bits(dg1) << 16);
+      ou[k] = f32_to_bf16_bits(du0) | (f32_to_bf16_bits(du1) << 16);
     }
     *reinterpret_cast<uint4 *>(dy13 + m * 2 * I + j) = make_uint4(og[0], og[1], og[2], og[3]);
     *reinterpret_cast<uint4 *>(dy13 + m * 2 * I + I + j) = make_uint4(ou[0], ou[1], ou[2], ou[3]);
