@@ -568,6 +568,11 @@ __global__ void __launch_bounds__(256) mxfp8_rowwise_kernel(const __grid_constan
 //                   and, from the codes just made, the same re-quantization:
 //                   both outputs of nvfp4_quantize + dequant_transpose_
 //                   requant_sr in one pass over the source
+// kGather (NVFP4 output, per-tensor scale): row r of the window is source
+// row row_src[r] -- bf16 token rows (kSrcBf16ToNvfp4), or the NVFP4 codes
+// and per-row block scales of already quantized tokens (kSrcNvfp4, which
+// then also copies them to the routed rows' NVFP4 layout).  A window without
+// data (grouped padding past the last group) only writes zero scale tiles.
 //   phase 1  stream the tile into shared memory as 16-bit values: bf16 input
 //            as is, NVFP4 input as the exact f16 products e2m1 * e4m3 (at most
 //            6 significant bits, inside the f16 range); optionally emit the
