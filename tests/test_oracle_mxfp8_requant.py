@@ -175,6 +175,37 @@ def test_gradient_rowwise_pairs_share_a_draw():
 
 
 @pytest.mark.slow
+@pytest.mark.parametrize("f1,f2", [(0.5, 0.5), (0.75, 0.25), (0.625, 0.625), (1 / 3, 1 / 3)])
+def test_pair_decisions_over_every_draw(f1, f2):
+    """The pairing of the draw convention: the pair's first element rounds
+    with U, the second with bitrev16(U).  Over all 2^16 draws each element
+    alone rounds up exactly floor(f 2^16) times.  When both thresholds are
+    multiples of 2^-8, the first decision reads only U's top 8 bits and the
+    second only its bottom 8, so the joint count is exactly the product
+    t1 t2 / 2^16 (independent decisions).  For f = 1/3 (threshold 0x5555,
+    every bit) the two decisions share bits: the joint count is not the
+    product, though within 2^-13 of it."""
+    U = np.arange(1 << 16, dtype=np.int64)
+    U2 = bitrev16(U).astype(np.int64)
+    # values 1 + f/8 sit between the E4M3 neighbours 1 and 1.125 at fraction f
+    x1, x2 = np.float32(1 + f1 * 0.125), np.float32(1 + f2 * 0.125)
+    t1 = int(np.floor((float(x1) - 1.0) / 0.125 * 65536))
+    t2 = int(np.floor((float(x2) - 1.0) / 0.125 * 65536))
+
+    def ups(x, draws):
+        codes = F.sr_code(np.full(1 << 16, x, np.float32), F.E4M3_TABLE, draws)
+        return F.decode_e4m3_array(codes) > 1.0
+
+    a, b = ups(x1, U), ups(x2, U2)
+    assert a.sum() == t1 and b.sum() == t2
+    joint = int((a & b).sum())
+    if t1 % 256 == 0 and t2 % 256 == 0:
+        assert joint * 65536 == t1 * t2
+    else:
+        assert joint * 65536 != t1 * t2
+        assert abs(joint / 65536 - (t1 / 65536) * (t2 / 65536)) < 2.0 ** -13
+
+
 def test_requant_is_unbiased_over_seeds():
     # "Re-quantization with stochastic rounding": E[w_q] = E[(w_q^T)^T]
     rng = np.random.default_rng(4)
