@@ -623,6 +623,17 @@ constexpr int kTileSmem = 128 * 256;                 // 128 rows x 128 16-bit va
 constexpr int kNvStage = 128 * 64 + 1024;            // NVFP4 source: staged codes and two scale tiles
 
 __device__ __forceinline__ int chunk_of(int i, int c8) { return c8 ^ ((i >> 2) & 7); }
+// The swizzle of the NVFP4-source kernel's 8-tokens-per-lane column pass:
+// chunk c of row i at (c even: c / 2, odd: 8 + c / 2) XOR ((i >> 3) & 7).
+// The product fill (eight lanes, one row's even or odd chunks) and the
+// column reads (eight lanes, one chunk of rows 8 apart) both land on eight
+// distinct bank groups.
+__device__ __forceinline__ int chunk_of8(int i, int c) { return ((c & 1) << 3) | ((c >> 1) ^ ((i >> 3) & 7)); }
+template <bool kT8>
+__device__ __forceinline__ int tile_chunk(int i, int c) { return kT8 ? chunk_of8(i, c) : chunk_of(i, c); }
+__device__ __forceinline__ uint32_t word_of(const uint4 &v, int p) {
+  return p == 0 ? v.x : p == 1 ? v.y : p == 2 ? v.z : v.w;
+}
 
 // eight E2M1 codes (one 32-bit word, element k in nibble k) -> four f16x2
 __device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&h)[4]) {
@@ -712,15 +723,16 @@ __device__ __forceinline__ void nvfp4_block46(const uint4 &a, const uint4 &b, fl
 
 // the 16 exact f16 products e2m1 * e4m3 of one (row i, 16-column block kb)
 // unit into the swizzled 16-bit tile
+template <bool kT8 = false>
 __device__ __forceinline__ void store_f16_products(uint8_t *s_in, int i, int kb, uint2 codes, uint32_t scale) {
   const uint32_t s2 = e4m3_to_f16x2_dup(scale);
   uint32_t h0[4], h1[4];
   e2m1x8_to_f16x2(codes.x, h0);
   e2m1x8_to_f16x2(codes.y, h1);
   uint4 *row = reinterpret_cast<uint4 *>(s_in + i * 256);
-  row[chunk_of(i, 2 * kb)] =
+  row[tile_chunk<kT8>(i, 2 * kb)] =
       make_uint4(hmul2_u32(h0[0], s2), hmul2_u32(h0[1], s2), hmul2_u32(h0[2], s2), hmul2_u32(h0[3], s2));
-  row[chunk_of(i, 2 * kb + 1)] =
+  row[tile_chunk<kT8>(i, 2 * kb + 1)] =
       make_uint4(hmul2_u32(h1[0], s2), hmul2_u32(h1[1], s2), hmul2_u32(h1[2], s2), hmul2_u32(h1[3], s2));
 }
 
@@ -762,13 +774,13 @@ __device__ __forceinline__ void stage_bf16_tile(const MxTArgs &A, const Window &
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
 }
 
-// CTAs per SM: five (48 registers) for the NVFP4-source and bf16 -> NVFP4
-// kernels, where the extra warps hide more of the barrier and load waits
-// (about 3% faster than four); four (64 registers) for the bf16 gradient
-// kernel, for which five was slower; three for the per-token kernels, which
-// spill at more
+// CTAs per SM: five (48 registers) for the bf16 -> NVFP4 kernels, where the
+// extra warps hide more of the barrier and load waits (about 3% faster than
+// four); four (64 registers) for the bf16 gradient kernel, for which five was
+// slower, and for the NVFP4-source kernel, whose 8-tokens-per-lane column
+// pass needs them; three for the per-token kernels, which spill at more
 template <int kMode, bool kRows>
-constexpr int mx_t_min_blocks() { return kRows ? 3 : kMode == 0 ? 4 : 5; }
+constexpr int mx_t_min_blocks() { return kRows ? 3 : (kMode == 0 || kMode == 1) ? 4 : 5; }
 
 template <int kMode, bool kRows = false, bool k46 = false, bool kGather = false>
 __global__ void __launch_bounds__(256, mx_t_min_blocks<kMode, kRows>()) mx_transpose_kernel(
@@ -779,6 +791,9 @@ __global__ void __launch_bounds__(256, mx_t_min_blocks<kMode, kRows>()) mx_trans
   // the routed rows' NVFP4 codes and scales are written too (from the bf16
   // source, or copied from the gathered token codes)
   constexpr bool kNvOut = kMode == kSrcBf16ToNvfp4 || kGather;
+  // the NVFP4-source kernel (per-tensor scale) runs the column pass with 8
+  // tokens per lane, on its own tile swizzle (chunk_of8)
+  constexpr bool kT8 = kMode == kSrcNvfp4 && !kRows;
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ __align__(16) uint8_t s_tsc[512];   // transposed scale tile
   __shared__ __align__(16) uint8_t s_rsc[512];   // row-wise scale tile
@@ -937,7 +952,7 @@ __global__ void __launch_bounds__(256, mx_t_min_blocks<kMode, kRows>()) mx_trans
         sc = kGather ? st_sc[i * 8 + kb] : st_sc[(kb >> 2) * 512 + atom_pos(i, kb)];
       }
       if (kGather) s_nvsc[(kb >> 2) * 512 + atom_pos(i, kb)] = (uint8_t)sc;
-      store_f16_products(s_in, i, kb, raw, sc);
+      store_f16_products<kT8>(s_in, i, kb, raw, sc);
     }
   } else {
     // bf16 -> NVFP4 with the quantizer's block rule (nvfp4_block), codes to
@@ -991,6 +1006,94 @@ __global__ void __launch_bounds__(256, mx_t_min_blocks<kMode, kRows>()) mx_trans
   // draw from one Philox call each: pair keys (row * cols + column) for the
   // 8 consecutive columns.  Each lane computes the E8M0 scale of one column
   // (lane & 7) of its block and broadcasts its multiplier.
+  if constexpr (kT8) {
+    // Warp w covers source columns 16w .. 16w + 15: lane 16h + tg owns the
+    // column group cg = 2w + h (8 columns) and tokens 8tg .. 8tg + 7, so the
+    // 32 tokens of block b sit on lanes 4b .. 4b + 3 of each half-warp.  Each
+    // of the lane's token pairs (8tg + 2m, 8tg + 2m + 1) draws the keys of its
+    // 8 columns from one Philox call (pair key row * cols + column, as the
+    // 4-token pass).  Lane 4b + r ends the block-maximum reduce-scatter with
+    // column pair r, computes the E8M0 scales of columns 2r and 2r + 1, and
+    // hands their multipliers to the block's four lanes.
+    const int tg = lane & 15;
+    const int cg = 2 * warp + (lane >> 4);
+    const int r = lane & 3;
+    uint32_t v[8][4];  // [token j][column pair] exact f16 products
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = 8 * tg + j;
+      const uint4 raw = reinterpret_cast<const uint4 *>(s_in + i * 256)[chunk_of8(i, cg)];
+      v[j][0] = raw.x; v[j][1] = raw.y; v[j][2] = raw.z; v[j][3] = raw.w;
+    }
+    uint4 bits[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) bits[m] = make_uint4(0u, 0u, 0u, 0u);
+    if (A.sr) {  // rows past the window's data draw too: their values are zeros, which SR keeps
+      const uint64_t q = (uint64_t)(((w.src_row0 + 8 * tg) * A.cols + col0 + 8 * cg) >> 3);
+      const uint64_t qs = (uint64_t)(A.cols >> 2);  // two rows on (cols % 128 == 0)
+#pragma unroll
+      for (int m = 0; m < 4; ++m) bits[m] = philox_bits8_rk(q + m * qs, A.off_t, A.rk);
+    }
+    // column pairs: maxima over the lane's 8 tokens, then a reduce-scatter
+    // over the block's 4 lanes that leaves pair r on lane 4b + r
+    uint32_t mx[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      uint32_t x = habsmax2(v[0][p], v[1][p]);
+#pragma unroll
+      for (int j = 2; j < 8; ++j) x = habsmax2(x, v[j][p]);
+      mx[p] = x;
+    }
+    const bool b1 = lane & 2, b0 = lane & 1;
+    uint32_t m2p[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const uint32_t keep = b1 ? mx[q + 2] : mx[q], send = b1 ? mx[q] : mx[q + 2];
+      m2p[q] = habsmax2(keep, __shfl_xor_sync(0xFFFFFFFFu, send, 2));
+    }
+    const uint32_t keep1 = b0 ? m2p[1] : m2p[0], send1 = b0 ? m2p[0] : m2p[1];
+    const uint32_t mp = habsmax2(keep1, __shfl_xor_sync(0xFFFFFFFFu, send1, 1));
+    float m2a, m2b;  // multipliers of columns 2r and 2r + 1 of the group
+    {
+      // max_i fp32(p_i * sg) = fp32(max_i p_i * sg): rounding is monotonic
+      const float aa = __fmul_rn(fabsf(f16_lo(mp)), sg), ab = __fmul_rn(fabsf(f16_hi(mp)), sg);
+      float ma, mb;
+      const uint32_t sca = e8m0_scale(aa, &ma), scb = e8m0_scale(ab, &mb);
+      // an all-zero block keeps its signed zeros: multiplier 0, not sg * 2^127
+      m2a = aa == 0.0f ? 0.0f : __fmul_rn(sg, ma);
+      m2b = ab == 0.0f ? 0.0f : __fmul_rn(sg, mb);
+      const int c0 = 8 * cg + 2 * r, blk = tg >> 2;
+      s_tsc[atom_pos(c0, blk)] = (uint8_t)sca;
+      s_tsc[atom_pos(c0 + 1, blk)] = (uint8_t)scb;
+    }
+    // output rows 8cg .. 8cg + 7, the lane's 8 tokens each (a half-warp
+    // writes one whole 128-byte row per store)
+    uint8_t *out8 = A.out_codes + out_base + 8 * tg + (int64_t)(8 * cg) * out_stride;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int p = k >> 1, h = k & 1;
+      const float m2 = __shfl_sync(0xFFFFFFFFu, h ? m2b : m2a, p, 4);  // from lane 4 * (lane / 4) + p
+      float x[8];
+#pragma unroll
+      for (int j = 0; j < 8; j += 2)
+        mul2_rn(h ? f16_hi(v[j][p]) : f16_lo(v[j][p]), h ? f16_hi(v[j + 1][p]) : f16_lo(v[j + 1][p]), m2, x[j],
+                x[j + 1]);
+      uint32_t lo, hi;
+      if (A.sr) {
+        // tokens 2m, 2m + 1 take half h of word p of pair m's draws (U, then bitrev16(U))
+        const uint32_t sel = h ? 0x7632u : 0x5410u;
+        const uint32_t u0 = __byte_perm(word_of(bits[0], p), word_of(bits[1], p), sel);
+        const uint32_t u1 = __byte_perm(word_of(bits[2], p), word_of(bits[3], p), sel);
+        lo = cvt_e4m3x4_sr(x[0], x[1], x[2], x[3], ~u0);
+        hi = cvt_e4m3x4_sr(x[4], x[5], x[6], x[7], ~u1);
+      } else {
+        lo = cvt_e4m3x2_rn(x[0], x[1]) | (cvt_e4m3x2_rn(x[2], x[3]) << 16);
+        hi = cvt_e4m3x2_rn(x[4], x[5]) | (cvt_e4m3x2_rn(x[6], x[7]) << 16);
+      }
+      *reinterpret_cast<uint2 *>(out8) = make_uint2(lo, hi);
+      out8 += out_stride;
+    }
+  } else {
   float sg_tok[4];  // per-token outer scales of this lane's tokens (kRows)
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
@@ -1142,6 +1245,7 @@ __global__ void __launch_bounds__(256, mx_t_min_blocks<kMode, kRows>()) mx_trans
       *reinterpret_cast<uint32_t *>(out_row) = packed;
       out_row += out_stride;
     }
+  }
   }
   __syncthreads();
 
