@@ -1016,7 +1016,9 @@ def run_gemm(args):
     over fewer experts (same depth per expert, smaller footprint; for
     profiling): fwd = x_q w13^T (N 3072, K 4096), swiglu = the same GEMM with
     SwiGLU and max |h| in its epilogue (y13 and h written), dx = dy13 w13
-    (N 3072, K 4096), dw = dy13^T x_q.  Prints achieved TFLOP/s."""
+    (N 3072, K 4096), dx_swiglu = the w2 dgrad g2 w2 (N 4096, K 1536) with
+    the SwiGLU backward in its epilogue (y13 read, dy13 written), dw = dy13^T
+    x_q.  Prints achieved TFLOP/s (of the GEMM's FLOPs)."""
     import torch
     from precision_moe_numerics_nvfp4_gb300 import nvfp4moe as N
     from precision_moe_numerics_nvfp4_gb300 import workloads as W
@@ -1042,6 +1044,21 @@ def run_gemm(args):
         h_sg = torch.empty(1, dtype=torch.float32, device=dev)
         fn = lambda: N.grouped_gemm_nvfp4_fwd_swiglu(xq.sg, xq.codes, xq.scales, wq.codes, wq.scales, wq.sg, go, E, M,
                                                      I2 // 2, d, y13, h, h_sg)
+    elif args.gemm_kind == "dx_swiglu":
+        I = I2 // 2
+        flops = float(2 * M * d * I)
+        g2 = (torch.randn((M, d), device=dev) * 1e-3).to(torch.bfloat16)
+        gr2, gt2 = MxRows(M, d, dev, E=E), MxTransposed(M, d, dev, E=E)
+        N.mxfp8_quantize(g2, M, d, go, N.NV_SR, 3, 6, 7, gr2.codes, gr2.scales, gt2.codes, gt2.scales)
+        w2 = (torch.randn((E, d, I), device=dev) * 0.02).to(torch.bfloat16)
+        w2q = NvTensor(E, d, I, dev)
+        w2q.quantize(w2)
+        w2t = MxTransposed(d, I, dev, batch=E)
+        N.dequant_transpose_requant_sr(w2q.codes, w2q.scales, w2q.sg, E, d, I, None, 3, 1, w2t.codes, w2t.scales)
+        y13 = torch.randn((M, I2), device=dev).to(torch.bfloat16)
+        dy13 = torch.empty((M, I2), dtype=torch.bfloat16, device=dev)
+        fn = lambda: N.grouped_gemm_mxfp8_dx_swiglu_bwd(gr2.codes, gr2.scales, w2t.codes, w2t.scales, go, E, M, d, I,
+                                                        y13, dy13)
     else:
         g = (torch.randn((M, I2), device=dev) * 1e-3).to(torch.bfloat16)
         gr, gt = MxRows(M, I2, dev, E=E), MxTransposed(M, I2, dev, E=E)
@@ -1215,7 +1232,7 @@ def main(argv=None):
                     help="moe workload: skip the single-layer, quantization-sweep and decode records")
     ap.add_argument("--clocks-csv", default=None, help="also write the nvidia-smi clock samples of the timed region here")
     ap.add_argument("--workload", choices=["moe", "quant_sweep", "gemm", "decode", "rht_s2f6"], default="moe")
-    ap.add_argument("--gemm-kind", choices=["fwd", "swiglu", "dx", "dw"], default="fwd")
+    ap.add_argument("--gemm-kind", choices=["fwd", "swiglu", "dx", "dx_swiglu", "dw"], default="fwd")
     ap.add_argument("--graph", action="store_true", help="decode workload: replay the forward as a CUDA graph")
     ap.add_argument("--decode-experts", type=int, default=128,
                     help="decode workload: experts (tokens scale with them, ~16 rows per expert); for profiling")
