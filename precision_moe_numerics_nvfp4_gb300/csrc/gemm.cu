@@ -945,16 +945,14 @@ struct CfgPair {
 // experts alternate), and with an even number of pairs every other round is
 // walked in reverse so that each pair alternates between the two kinds.
 // Only two experts' operands are live at a time; within an expert the tiles
-// go in bands of kDwBand tile columns (decode_pair).
+// go column-major when A has fewer row blocks than B, else row-major
+// (decode_pair).
 __device__ __forceinline__ int dw_sorted_index(int t, int pair, int npairs, int T) {
   const int r = t / npairs;
   int x = t;
   if ((npairs & 1) == 0 && (r & 1) && (r + 1) * npairs <= T) x = r * npairs + (npairs - 1 - pair);
   return (x & 1) ? T - 1 - (x >> 1) : (x >> 1);
 }
-
-// Tile columns per band of the wgrad's order within an expert (decode_pair).
-constexpr int kDwBand = 8;
 
 // s_ord[k]: the expert with the k-th largest padded token count (ties: lower
 // index first).  Every thread of the CTA must call it.
@@ -1023,17 +1021,16 @@ __device__ __forceinline__ PairTile decode_pair(int t, const GemmArgs &A, const 
     const int d = dw_sorted_index(t, pair, npairs, num_tiles);
     const int k = d / per_e;
     const int e = s_ord[k];
-    // within the expert, bands of 8 tile columns, rows within a band: the
-    // ~38 tiles of an expert in flight at a time then need about 5 A and 8 B
-    // row blocks instead of 3 A and all B blocks, and a band's B blocks stay
-    // in the L2 from one round to the next
+    // within the expert, the operand with fewer 256-row blocks is swept in
+    // the inner loop: the ~38 tiles of an expert in flight at a time then
+    // read all of its blocks (which stay in the L2 from one round to the
+    // next) and only a few blocks of the other operand, each once
     const int r = d - k * per_e;
     int mt, nt;
-    if (A.ntn % kDwBand == 0 && A.ntn > kDwBand) {
-      const int b = r / (A.ntm * kDwBand), rb = r - b * (A.ntm * kDwBand);
-      mt = rb / kDwBand;
-      nt = b * kDwBand + (rb - mt * kDwBand);
-    } else {
+    if (A.ntm < A.ntn) {  // column-major
+      nt = r / A.ntm;
+      mt = r - nt * A.ntm;
+    } else {  // row-major
       mt = r / A.ntn;
       nt = r - mt * A.ntn;
     }
