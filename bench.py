@@ -1091,6 +1091,41 @@ def run_gemm(args):
                       "TFLOP_s": flops / (ms / 1e3) / 1e12}))
 
 
+def run_gather(args):
+    """The quantization of the MoE layer's activations from its tokens
+    (nvfp4_quantize_requant_gather) alone: the tokens [T x d_model] bf16 and
+    the routed rows' source tokens in; the routed rows' NVFP4 codes, scales and
+    outer scale and their transposed MXFP8 SR re-quantization out.  T =
+    --gemm-tokens, top-8 over --gemm-experts experts (the MoE step's routing
+    recipe; fewer experts give a smaller case for profiling).  Prints achieved
+    GB/s of algorithmic bytes (the amax pass included)."""
+    import torch
+    from precision_moe_numerics_nvfp4_gb300 import nvfp4moe as N
+    from precision_moe_numerics_nvfp4_gb300 import workloads as W
+    from precision_moe_numerics_nvfp4_gb300.pipeline import MxTransposed, NvTensor
+
+    N.lib()
+    peaks = load_peaks()
+    dev = torch.device("cuda")
+    E = args.gemm_experts
+    m = W.moe("cuda", seed=2, tokens=args.gemm_tokens, experts=E, bias_std=args.gemm_bias_std, weights=False)
+    T, d = m.x.shape
+    M = m.rows.shape[0]
+    q, mx = NvTensor(1, M, d, dev, E=E), MxTransposed(M, d, dev, E=E)
+    ws = q.gather_workspace(T)
+    fn = lambda: N.nvfp4_quantize_requant_gather(m.x, m.rows, T, M, d, m.group_offsets, None, q.sg, q.codes,
+                                                 q.scales, ws, 3, 1, mx.codes, mx.scales)
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    ms = time_calls(fn, args.steps)
+    assert N.nvfp4moe_get_device_status() == 0
+    bpe = gather_bytes_per_routed_elem(T, M)
+    gbs = M * d * bpe / (ms / 1e3) / 1e9
+    print(json.dumps({"workload": "gather", "tokens": T, "rows": M, "experts": E, "ms": ms, "GB_s": gbs,
+                      "frac_hbm": gbs / peaks["hbm_gbs"], "bytes_per_routed_elem": bpe}))
+
+
 def run_rht_s2f6(args):
     """RHT-32 + block-scaled S2F6 of the MoE layer's output (the combine
     direction): 131072 routed rows x d_model 4096, bf16, values Student-t(3)
@@ -1231,7 +1266,8 @@ def main(argv=None):
     ap.add_argument("--no-configs", action="store_true",
                     help="moe workload: skip the single-layer, quantization-sweep and decode records")
     ap.add_argument("--clocks-csv", default=None, help="also write the nvidia-smi clock samples of the timed region here")
-    ap.add_argument("--workload", choices=["moe", "quant_sweep", "gemm", "decode", "rht_s2f6"], default="moe")
+    ap.add_argument("--workload", choices=["moe", "quant_sweep", "gemm", "gather", "decode", "rht_s2f6"],
+                    default="moe")
     ap.add_argument("--gemm-kind", choices=["fwd", "swiglu", "dx", "dx_swiglu", "dw"], default="fwd")
     ap.add_argument("--graph", action="store_true", help="decode workload: replay the forward as a CUDA graph")
     ap.add_argument("--decode-experts", type=int, default=128,
@@ -1254,6 +1290,8 @@ def main(argv=None):
         run_quant_sweep(args)
     elif args.workload == "gemm":
         run_gemm(args)
+    elif args.workload == "gather":
+        run_gather(args)
     elif args.workload == "rht_s2f6":
         run_rht_s2f6(args)
     elif args.workload == "decode":
