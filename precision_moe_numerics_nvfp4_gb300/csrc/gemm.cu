@@ -936,22 +936,18 @@ struct CfgPair {
   static_assert(TMEM_COLS * kCtasPerSm <= 512, "tensor memory");
 };
 
-// Wgrad tile order.  Every expert writes its whole fp32 dW (the same bytes
-// whatever its token count) while its MMA time grows with its tokens, so a
-// small expert's tiles are store-bound and a large one's MMA-bound.  The
-// schedule interleaves the two: D lists the tiles expert by expert in
-// decreasing padded token count; position i of the processing order takes
-// D[i / 2] for even i and D[T - 1 - i / 2] for odd i (largest and smallest
-// experts alternate), and with an even number of pairs every other round is
-// walked in reverse so that each pair alternates between the two kinds.
-// Only two experts' operands are live at a time; within an expert the tiles
-// go column-major when A has fewer row blocks than B, else row-major
-// (decode_pair).
+// Wgrad tile order.  D lists the tiles expert by expert in decreasing padded
+// token count (a tile's MMA time grows with its expert's tokens; every tile
+// stores the same 256 x 256 fp32 block).  Pair p takes D[r * P + p] in round
+// r, with every odd round walked in reverse (position r * P + P - 1 - p), so
+// that the pairs' sums of tile times stay within about 1% of each other (the
+// last, partial round is not reversed).  At most two experts' operands are
+// live at a time; within an expert the tiles go column-major when A has fewer
+// row blocks than B, else row-major (decode_pair).
 __device__ __forceinline__ int dw_sorted_index(int t, int pair, int npairs, int T) {
   const int r = t / npairs;
-  int x = t;
-  if ((npairs & 1) == 0 && (r & 1) && (r + 1) * npairs <= T) x = r * npairs + (npairs - 1 - pair);
-  return (x & 1) ? T - 1 - (x >> 1) : (x >> 1);
+  if ((r & 1) && (r + 1) * npairs <= T) return r * npairs + (npairs - 1 - pair);
+  return t;
 }
 
 // s_ord[k]: the expert with the k-th largest padded token count (ties: lower
