@@ -995,7 +995,10 @@ __global__ void __launch_bounds__(256, mx_t_min_blocks<kMode, kRows>()) mx_trans
       store_f16_products(s_in, i, kb, c, sc);
     }
   }
-  __syncthreads();
+  // the NVFP4 sources' phase 1 wrote the tile that phase 2 reads; the bf16
+  // source's phase 1 only read it (and wrote the row-wise scale tile, which
+  // the barrier before phase 3 orders), so its warps go on without waiting
+  if (kNvfp4) __syncthreads();
 
   uint8_t *const out_lane = A.out_codes + out_base + 4 * lane;
 
