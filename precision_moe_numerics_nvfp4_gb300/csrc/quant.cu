@@ -752,13 +752,20 @@ __device__ __forceinline__ void cp_async4(void *dst, const void *src, uint32_t b
 // 16-bit layout with cp.async: 128 bytes per thread in flight without
 // registers; rows past the window's data are zero-filled.  Waits for the
 // thread's own copies; the caller's barrier makes the tile visible.
-// kGather: row r of the window is source row row_src[r].
-template <bool kGather>
+// kGather: row r of the window is source row row_src[r].  kWarpRows: warp w
+// stages rows 32 u + 4 w + j (u, j < 4), the rows of its units in the
+// row-wise NVFP4 pass, so that a __syncwarp makes them visible to it.
+template <bool kGather, bool kWarpRows = false>
 __device__ __forceinline__ void stage_bf16_tile(const MxTArgs &A, const Window &w, int64_t col0, uint8_t *s_in) {
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     const int q = k * 256 + (int)threadIdx.x;
-    const int i = q >> 4, c16 = q & 15;
+    int i = q >> 4, c16 = q & 15;
+    if (kWarpRows) {  // 16 rows x 16 chunks per warp, two whole rows per warp instruction
+      const int m = k * 32 + (int)(threadIdx.x & 31), rho = m >> 4;
+      i = 32 * (rho >> 2) + 4 * (int)(threadIdx.x >> 5) + (rho & 3);
+      c16 = m & 15;
+    }
     bool ok = i < w.nvalid;
     int64_t row = w.src_row0 + i;
     if (kGather && ok) {  // a row index out of range reads as zeros and is recorded
@@ -969,8 +976,12 @@ __global__ void __launch_bounds__(256, mx_t_min_blocks<kMode, kRows>()) mx_trans
       const uint32_t t = (uint32_t)tid;
       s_qt[t] = __fdiv_rn(__uint_as_float(t < 128 ? 0x3F800000u | (t << 16) : (t - 128) << 16), den6);
     }
-    stage_bf16_tile<kGather>(A, w, col0, s_in);
-    __syncthreads();
+    // every warp reads the tables: one barrier, before any warp has a copy
+    // in flight; the tile's rows are then each warp's own (no CTA barrier
+    // between a warp's copies landing and its row-wise pass)
+    if (!kRows) __syncthreads();
+    stage_bf16_tile<kGather, true>(A, w, col0, s_in);
+    __syncwarp();
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int q = u * 256 + tid;
