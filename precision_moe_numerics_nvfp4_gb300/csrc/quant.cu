@@ -853,8 +853,10 @@ __global__ void __launch_bounds__(256, mx_t_min_blocks<kMode, kRows>()) mx_trans
 
   // ---- phase 1 --------------------------------------------------------------
   if (!kNvfp4) {
-    stage_bf16_tile<false>(A, w, col0, s_in);
-    __syncthreads();
+    // the warp's own rows (a __syncwarp): the row-wise pass reads only them;
+    // the barrier after it makes the whole tile visible to the column pass
+    stage_bf16_tile<false, true>(A, w, col0, s_in);
+    __syncwarp();
     // row-wise output: items of 16 columns (32 bytes) of one row; a row-wise
     // MXFP8 block of 32 is two neighbouring lanes, and one Philox call covers
     // an item's 8 pairs
@@ -1006,10 +1008,9 @@ __global__ void __launch_bounds__(256, mx_t_min_blocks<kMode, kRows>()) mx_trans
       store_f16_products(s_in, i, kb, c, sc);
     }
   }
-  // the NVFP4 sources' phase 1 wrote the tile that phase 2 reads; the bf16
-  // source's phase 1 only read it (and wrote the row-wise scale tile, which
-  // the barrier before phase 3 orders), so its warps go on without waiting
-  if (kNvfp4) __syncthreads();
+  // phase 2 reads every row of the tile: the NVFP4 sources' products written
+  // in phase 1, the bf16 source's rows staged per warp
+  __syncthreads();
 
   uint8_t *const out_lane = A.out_codes + out_base + 4 * lane;
 
