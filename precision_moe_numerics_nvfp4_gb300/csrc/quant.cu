@@ -901,7 +901,8 @@ __global__ void __launch_bounds__(256, mx_t_min_blocks<kMode, kRows>()) mx_trans
     // batched layout; thread (i = tid / 2, half h = tid % 2) stages that
     // row's 32 code bytes of half h and its four block scales of half h (one
     // 4-byte word of the token's scale tile h), rows per unit instead of the
-    // two tiles
+    // two tiles, and a CTA barrier follows (the fill's rows are other warps');
+    // otherwise each warp stages exactly what its own fill reads
     uint8_t *st_codes = s_stage, *st_sc = s_stage + 128 * 64;
     const int64_t half_cols = A.cols >> 1;
     if (kGather) {
@@ -923,23 +924,31 @@ __global__ void __launch_bounds__(256, mx_t_min_blocks<kMode, kRows>()) mx_trans
           ok ? A.nv_scales + ((t >> 7) * ka_src + (col0 >> 6) + h) * 512 + atom_pos((int)(t & 127), 0) : A.nv_scales;
       cp_async4(st_sc + i * 8 + h * 4, ssrc, ok ? 4u : 0u);
     } else {
+      // warp w: the codes of rows 32 u + 4 w + j (u, j < 4), the rows of its
+      // units in the product fill below, and their scales: bytes 64 w ..
+      // 64 w + 63 of both scale tiles (row i's four scales sit at (i % 32) 16
+      // + (i / 32) 4), so that a __syncwarp makes them visible to it
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
-        const int q = k * 256 + tid;
-        const int i = q >> 2, part = q & 3;
+        const int unit = k * 32 + lane, rho = unit >> 2;
+        const int i = 32 * (rho >> 2) + 4 * warp + (rho & 3), part = unit & 3;
         const bool ok = i < w.nvalid;
         const uint8_t *src = ok ? A.nv_codes + (w.src_row0 + i) * half_cols + (col0 >> 1) + part * 16 : A.nv_codes;
         cp_async16(st_codes + i * 64 + part * 16, src, ok ? 16u : 0u);
       }
-      if (tid < 64) {
+      if (lane < 8) {
         const int64_t ka_src = (A.cols + 63) >> 6;
         const int64_t tile0 = (w.rp0 >> 7) * ka_src + (col0 >> 6);
+        const int off = (lane >> 2) * 512 + 64 * warp + (lane & 3) * 16;
         const bool ok = w.nvalid > 0;
-        cp_async16(st_sc + tid * 16, ok ? A.nv_scales + tile0 * 512 + tid * 16 : A.nv_scales, ok ? 16u : 0u);
+        cp_async16(st_sc + off, ok ? A.nv_scales + tile0 * 512 + off : A.nv_scales, ok ? 16u : 0u);
       }
     }
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
-    __syncthreads();
+    if (kGather)
+      __syncthreads();
+    else
+      __syncwarp();
     if (kGather) {  // the routed rows' codes: a copy of the staged token codes
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
