@@ -110,12 +110,14 @@ def _mx_operands(sizes, Nd, K, seed):
     return go, o, M, E, gr, gt, wt, xt
 
 
-# the last case has 200 wgrad pair tiles (10 experts x 4 x 5): more than two
-# rounds of the 76 CTA pairs, so the pair kernel's snake order walks a round
-# in reverse and ends on a partial one, over experts of very different sizes
+# the last two cases have 200 wgrad pair tiles (10 experts x 4 x 5) and 256
+# (one expert, 16 x 16): more than two rounds of the 76 CTA pairs, so the
+# pair kernel's snake order walks a round in reverse and ends on a partial
+# one, over experts of very different sizes and within a single expert
 @pytest.mark.parametrize("sizes,Nd,K", [([256], 1024, 512), ([5, 0, 295, 130], 256, 384), ([1, 300], 128, 256),
                                        ([5, 0, 295, 130], 256, 512), ([0, 700, 1, 0, 129], 512, 768),
-                                       ([300, 0, 5, 129, 700, 1, 256, 0, 33, 128], 1024, 1280)])
+                                       ([300, 0, 5, 129, 700, 1, 256, 0, 33, 128], 1024, 1280),
+                                       ([200], 4096, 4096)])
 def test_mxfp8_dgrad_and_wgrad_within_bound(sizes, Nd, K, gemm_kernel):
     go, o, M, E, gr, gt, wt, xt = _mx_operands(sizes, Nd, K, seed=len(sizes) + Nd)
     dx = gfull((M, K), float("nan"), dtype=torch.float32, device=dev())
