@@ -783,9 +783,10 @@ __device__ __forceinline__ void stage_bf16_tile(const MxTArgs &A, const Window &
 
 // CTAs per SM: five (48 registers) for the bf16 -> NVFP4 kernels, where the
 // extra warps hide more of the barrier and load waits (about 3% faster than
-// four); four (64 registers) for the bf16 gradient kernel, for which five was
-// slower, and for the NVFP4-source kernel, whose 8-tokens-per-lane column
-// pass needs them; three for the per-token kernels, which spill at more
+// four); four (64 registers) for the bf16 gradient kernel, for which five
+// measured no faster, and for the NVFP4-source kernel, whose
+// 8-tokens-per-lane column pass needs them; three for the per-token
+// kernels, which spill at more
 template <int kMode, bool kRows>
 constexpr int mx_t_min_blocks() { return kRows ? 3 : (kMode == 0 || kMode == 1) ? 4 : 5; }
 
